@@ -1,0 +1,275 @@
+"""fp64 CPU oracle of the batch-B INT4 GQA decode step -- TEST INFRASTRUCTURE.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the ``cpu_baseline`` /
+``--impl reference`` legs of ``bench.py`` may import this package.  It never
+imports the CUDA library package and shares no code with it; the only thing
+both sides share is the seeded input generator (``synth``), which holds none
+of the method's arithmetic.
+
+The arithmetic lives in ``ddl_oracle.c`` (plain C, fp64, OpenMP over
+independent outputs), compiled here with gcc at first use.  Each function
+states the passage it follows; see the C file's header for the readings of
+the pages taken where they are silent.
+
+Pinning: every function below is pinned by ``tests/test_oracle_pins.py``
+against closed forms, invariants, library routines and brute force; the
+composed layer is additionally pinned against a composition of PyTorch
+library routines (F.rms_norm, scaled_dot_product_attention, F.silu) and
+against residual-identity special cases.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+from dataclasses import dataclass
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "ddl_oracle.c")
+_BUILD = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile ddl_oracle.c to a shared library (gcc, -O2, no fast-math)."""
+    os.makedirs(_BUILD, exist_ok=True)
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-fopenmp", "-ffp-contract=off", "-fPIC", "-shared",
+           "-o", tmp, _SRC, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+class _Shape(ctypes.Structure):
+    _fields_ = [("D", ctypes.c_int64), ("H_q", ctypes.c_int64), ("H_kv", ctypes.c_int64),
+                ("head_dim", ctypes.c_int64), ("d_ff", ctypes.c_int64),
+                ("rope_base", ctypes.c_double), ("eps", ctypes.c_double)]
+
+
+class _Mat(ctypes.Structure):
+    _fields_ = [("q", ctypes.c_void_p), ("s", ctypes.c_void_p), ("w", ctypes.c_void_p)]
+
+
+class _Layer(ctypes.Structure):
+    _fields_ = [("norm1", ctypes.c_void_p), ("wq", _Mat), ("wk", _Mat), ("wv", _Mat),
+                ("wo", _Mat), ("norm2", ctypes.c_void_p), ("wg", _Mat), ("wu", _Mat),
+                ("wd", _Mat)]
+
+
+class _Stages(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in ("h", "q", "k", "v", "attn", "y", "a")]
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            i64, dbl, vp = ctypes.c_int64, ctypes.c_double, ctypes.c_void_p
+            lib.orc_bf16_to_f64.restype = dbl
+            lib.orc_bf16_to_f64.argtypes = [ctypes.c_uint16]
+            lib.orc_bf16_from_f64.restype = ctypes.c_uint16
+            lib.orc_bf16_from_f64.argtypes = [dbl]
+            lib.orc_bf16_from_f64_array.argtypes = [vp, i64, vp]
+            lib.orc_quantize_int4.argtypes = [vp, i64, i64, vp, vp]
+            lib.orc_unpack_int4.argtypes = [vp, i64, i64, vp]
+            lib.orc_gemv_int4.argtypes = [vp, vp, i64, i64, vp, vp]
+            lib.orc_gemv_bf16.argtypes = [vp, i64, i64, vp, vp]
+            lib.orc_rmsnorm.argtypes = [vp, vp, i64, dbl, vp]
+            lib.orc_rope.argtypes = [vp, i64, i64, dbl]
+            lib.orc_attention.argtypes = [vp, vp, vp, i64, i64, i64, i64, i64, vp, vp]
+            lib.orc_layer_decode.restype = ctypes.c_int
+            lib.orc_layer_decode.argtypes = [ctypes.POINTER(_Shape), ctypes.POINTER(_Layer),
+                                             vp, vp, i64, i64, i64, vp, vp,
+                                             ctypes.POINTER(_Stages)]
+            lib.orc_num_threads.restype = ctypes.c_int
+            _lib = lib
+    return _lib
+
+
+def _c(a: np.ndarray, dtype) -> np.ndarray:
+    return np.ascontiguousarray(a, dtype=dtype)
+
+
+def _p(a):
+    return None if a is None else a.ctypes.data
+
+
+def num_threads() -> int:
+    """OpenMP threads the oracle uses."""
+    return int(_load().orc_num_threads())
+
+
+# ---------------------------------------------------------------- bf16
+
+def bf16_to_f64(bits) -> np.ndarray:
+    """Exact widening of bf16 bit patterns (uint16) to fp64."""
+    b = _c(bits, np.uint16)
+    with np.errstate(invalid="ignore"):
+        return (b.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def bf16_from_f64(x) -> np.ndarray:
+    """Round fp64 values to bf16 bit patterns, nearest-even, one rounding."""
+    x = _c(x, np.float64)
+    out = np.empty(x.shape, np.uint16)
+    _load().orc_bf16_from_f64_array(_p(x), x.size, _p(out))
+    return out
+
+
+# ---------------------------------------------------------------- INT4
+
+def quantize_int4(w_bf16) -> tuple[np.ndarray, np.ndarray]:
+    """Symmetric INT4, group 64 along K (Unsloth article §二.3 4-bit weights).
+
+    w_bf16: uint16 [N, K] bf16 bits.  Returns (q uint8 [N, K/2] with even k in
+    the low nibble, s uint16 [N, K/64] bf16 scales)."""
+    w = _c(w_bf16, np.uint16)
+    N, K = w.shape
+    if K % 64:
+        raise ValueError("K must be a multiple of 64")
+    q = np.zeros((N, K // 2), np.uint8)
+    s = np.zeros((N, K // 64), np.uint16)
+    _load().orc_quantize_int4(_p(w), N, K, _p(q), _p(s))
+    return q, s
+
+
+def unpack_int4(q) -> np.ndarray:
+    """Codes int8 [N, K] of a packed [N, K/2] matrix."""
+    q = _c(q, np.uint8)
+    N, Kh = q.shape
+    out = np.empty((N, 2 * Kh), np.int8)
+    _load().orc_unpack_int4(_p(q), N, 2 * Kh, _p(out))
+    return out
+
+
+# ---------------------------------------------------------------- primitives
+
+def gemv_int4(q, s, x) -> np.ndarray:
+    """y = (q*s) x in fp64 (primer §1.1 projections with dequantized weights)."""
+    q = _c(q, np.uint8)
+    s = _c(s, np.uint16)
+    x = _c(x, np.float64)
+    N, Kh = q.shape
+    y = np.empty(N, np.float64)
+    _load().orc_gemv_int4(_p(q), _p(s), N, 2 * Kh, _p(x), _p(y))
+    return y
+
+
+def gemv_bf16(w, x) -> np.ndarray:
+    w = _c(w, np.uint16)
+    x = _c(x, np.float64)
+    N, K = w.shape
+    y = np.empty(N, np.float64)
+    _load().orc_gemv_bf16(_p(w), N, K, _p(x), _p(y))
+    return y
+
+
+def rmsnorm(x, w_bf16, eps: float) -> np.ndarray:
+    """x * w / sqrt(mean(x^2) + eps) (primer §1.1 rmsnorm)."""
+    x = _c(x, np.float64)
+    w = _c(w_bf16, np.uint16)
+    out = np.empty_like(x)
+    _load().orc_rmsnorm(_p(x), _p(w), x.size, float(eps), _p(out))
+    return out
+
+
+def rope(v, pos: int, base: float) -> np.ndarray:
+    """Half-split RoPE of one head vector (roofline reply §五)."""
+    v = np.array(v, np.float64, copy=True, order="C")
+    _load().orc_rope(_p(v), v.size, int(pos), float(base))
+    return v
+
+
+def attention(q, kc, vc, n_keys: int, return_probs: bool = False):
+    """Softmax attention of one query token per head over keys 0..n_keys-1.
+
+    q: [H_q, hd] fp64; kc, vc: [H_kv, s_max, hd] bf16 bits (one sequence).
+    Returns o [H_q, hd] (and the weights [H_q, n_keys] when asked)."""
+    q = _c(q, np.float64)
+    kc = _c(kc, np.uint16)
+    vc = _c(vc, np.uint16)
+    Hq, hd = q.shape
+    Hkv, s_max, _ = kc.shape
+    out = np.empty((Hq, hd), np.float64)
+    probs = np.empty((Hq, n_keys), np.float64) if return_probs else None
+    _load().orc_attention(_p(q), _p(kc), _p(vc), Hq, Hkv, hd, s_max, int(n_keys),
+                          _p(out), _p(probs))
+    return (out, probs) if return_probs else out
+
+
+# ---------------------------------------------------------------- layer
+
+@dataclass
+class OracleMat:
+    """A weight matrix [N, K]: INT4 (q, s) or bf16 (w)."""
+    q: np.ndarray | None = None
+    s: np.ndarray | None = None
+    w: np.ndarray | None = None
+
+
+def quantized_layer(weights: dict) -> dict:
+    """Quantize every matrix of a bf16 layer dict with the oracle's quantizer."""
+    out = {"norm1": weights["norm1"], "norm2": weights["norm2"]}
+    for name in ("wq", "wk", "wv", "wo", "wg", "wu", "wd"):
+        q, s = quantize_int4(weights[name])
+        out[name] = OracleMat(q=q, s=s)
+    return out
+
+
+def bf16_layer(weights: dict) -> dict:
+    out = {"norm1": weights["norm1"], "norm2": weights["norm2"]}
+    for name in ("wq", "wk", "wv", "wo", "wg", "wu", "wd"):
+        out[name] = OracleMat(w=_c(weights[name], np.uint16))
+    return out
+
+
+def layer_decode(shape, layer: dict, kc, vc, pos: int, x, stages: bool = False):
+    """One decode step of one layer for B sequences (primer §1.2 decode_step).
+
+    shape: object with D, H_q, H_kv, head_dim, d_ff, rope_base, eps.
+    layer: dict from quantized_layer() / bf16_layer().
+    kc, vc: uint16 [B, H_kv, s_max, hd], modified in place (slot pos written).
+    x: fp64 [B, D].  Returns z [B, D] (and a dict of stage outputs)."""
+    lib = _load()
+    x = _c(x, np.float64)
+    B, D = x.shape
+    assert kc.dtype == np.uint16 and kc.flags.c_contiguous
+    assert vc.dtype == np.uint16 and vc.flags.c_contiguous
+    s_max = kc.shape[2]
+    sh = _Shape(shape.D, shape.H_q, shape.H_kv, shape.head_dim, shape.d_ff,
+                float(shape.rope_base), float(shape.eps))
+    keep = []
+
+    def mat(m: OracleMat) -> _Mat:
+        arrs = [None if a is None else np.ascontiguousarray(a) for a in (m.q, m.s, m.w)]
+        keep.extend(a for a in arrs if a is not None)
+        return _Mat(*[_p(a) for a in arrs])
+
+    n1 = _c(layer["norm1"], np.uint16)
+    n2 = _c(layer["norm2"], np.uint16)
+    L = _Layer(_p(n1), mat(layer["wq"]), mat(layer["wk"]), mat(layer["wv"]), mat(layer["wo"]),
+               _p(n2), mat(layer["wg"]), mat(layer["wu"]), mat(layer["wd"]))
+    z = np.empty((B, D), np.float64)
+    st = None
+    st_arrays = {}
+    if stages:
+        Nq = shape.H_q * shape.head_dim
+        Nkv = shape.H_kv * shape.head_dim
+        sizes = {"h": D, "q": Nq, "k": Nkv, "v": Nkv, "attn": Nq, "y": D, "a": shape.d_ff}
+        st_arrays = {k: np.empty((B, n), np.float64) for k, n in sizes.items()}
+        st = _Stages(*[_p(st_arrays[k]) for k in ("h", "q", "k", "v", "attn", "y", "a")])
+    rc = lib.orc_layer_decode(ctypes.byref(sh), ctypes.byref(L), _p(kc), _p(vc), s_max, B,
+                              int(pos), _p(x), _p(z), ctypes.byref(st) if st else None)
+    if rc != 0:
+        raise ValueError(f"oracle rejected the shape/position (rc={rc})")
+    return (z, st_arrays) if stages else z
