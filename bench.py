@@ -1,0 +1,345 @@
+"""Decode-step benchmark: tokens/s of the 27B-class 64-layer INT4 stack at batch 1.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME] [--batch B] [--weights int4|bf16] [--mode 0|1]
+
+A step is one decode step of the whole stack (every layer's fused QKV+RoPE+
+append, GQA attention, Wo, gate/up+SwiGLU, down) for one batch of synthetic
+input, with weights and KV history resident in HBM.  The stack streams
+18.7 GB per step, far more than the 129 MB L2, so no flush is needed
+between steps.  Under torchrun (N > 1) every rank runs an independent
+replica of the step (the path has no exchange step); value = tokens of all
+ranks / the slowest rank's time.  Prints one JSON line on rank 0.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "batch-1 decode tokens/s (27B-shape INT4, 64 layers); achieved HBM GB/s vs 8 TB/s"
+
+
+def _args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--workload", default=None)
+    p.add_argument("--batch", type=int, default=None)
+    p.add_argument("--weights", default=None, choices=[None, "int4", "bf16"])
+    p.add_argument("--layers", type=int, default=None)
+    p.add_argument("--mode", type=int, default=0, help="0 persistent kernel, 1 launch per stage")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    return p.parse_args()
+
+
+def _dist():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        d = json.load(open(path))
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def _source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "memory_bound_transformer_decode_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        h.update(open(os.path.join(csrc, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def _traffic(workload: str):
+    """DRAM bytes per launch of the decode kernel from the committed ncu
+    summary, if it was taken on the current kernel sources."""
+    path = os.path.join(ROOT, "profiles", "decode_kernel_traffic.json")
+    try:
+        d = json.load(open(path))
+        e = d.get(workload)
+        if e and e.get("source_hash") == _source_hash():
+            return float(e["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+class Clocks:
+    """nvidia-smi samples during the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def _cpu_baseline(cfg, target_s: float = 12.0):
+    """The oracle as it stands, on the host cores, over whole layers of the
+    workload; tokens/s = 1 / (seconds per layer * layers)."""
+    import torch
+
+    import oracle
+    from memory_bound_transformer_decode_gb300 import synth
+
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    w = {k: synth.bits(v) for k, v in synth.layer_weights(cfg, 0, device=dev).items()}
+    lw = oracle.quantized_layer(w)
+    del w
+    kc, vc = synth.kv_cache(cfg, 0, cfg.kv_len + 1, device=dev, batch=cfg.batch)
+    kc, vc = synth.bits(kc).copy(), synth.bits(vc).copy()
+    x = oracle.bf16_to_f64(synth.bits(synth.input_x(cfg, device=dev, batch=cfg.batch)))
+    times = []
+    t_start = time.perf_counter()
+    while True:
+        t0 = time.perf_counter()
+        oracle.layer_decode(cfg, lw, kc, vc, cfg.pos, x)
+        times.append(time.perf_counter() - t0)
+        if time.perf_counter() - t_start > target_s or len(times) >= 50:
+            break
+    per_layer = statistics.median(times)
+    return {
+        "value": cfg.batch / (per_layer * cfg.layers),
+        "unit": "tokens/s",
+        "cores": oracle.num_threads(),
+        "kind": "oracle",
+        "sample": f"{len(times)} decode steps of one layer (layer 0) of the {cfg.layers}-layer "
+                  f"stack, fp64 C oracle, median {per_layer:.3f} s/layer, scaled x{cfg.layers} layers",
+    }, per_layer
+
+
+def _config_json(cfg, B, wname, L):
+    return {"workload": cfg.name, "layers": L, "batch": B, "kv_len": cfg.kv_len, "D": cfg.D,
+            "H_q": cfg.H_q, "H_kv": cfg.H_kv, "head_dim": cfg.head_dim, "d_ff": cfg.d_ff,
+            "weights": "int4-g64-bf16-scale" if wname == "int4" else "bf16",
+            "l2": "inputs larger than L2 (no flush needed)", "parallelism": "replicas"}
+
+
+def run_reference(args):
+    from memory_bound_transformer_decode_gb300 import configs
+
+    rank, world, _ = _dist()
+    if rank != 0:
+        return
+    cfg = configs.BY_NAME.get(args.workload) if args.workload else configs.STACK27B
+    B = args.batch or cfg.batch
+    cfg = cfg.with_(batch=B)
+    per = []
+    cores = None
+    for i in range(args.warmup + args.steps):
+        cb, pl = _cpu_baseline(cfg, target_s=0.0)
+        cores = cb["cores"]
+        if i >= args.warmup:
+            per.append(pl)
+    step_s = statistics.median(per) * cfg.layers
+    value = B / step_s
+    sample = (f"each step: one layer (layer 0) of the {cfg.layers}-layer stack through the fp64 C "
+              f"oracle, scaled x{cfg.layers}; {args.steps} timed steps")
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_s * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": _config_json(cfg, B, cfg.weights, cfg.layers),
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }))
+
+
+def run_ours(args):
+    import torch
+
+    from memory_bound_transformer_decode_gb300 import configs, ddl, roofline, workload
+
+    rank, world, local = _dist()
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    ddl.load(build_if_missing=True)
+    ddl.ddl_set_launch_mode(args.mode)
+    cfg = configs.BY_NAME.get(args.workload) if args.workload else configs.STACK27B
+    B = args.batch or cfg.batch
+    wname = args.weights or cfg.weights
+    L = args.layers or cfg.layers
+    cfg = cfg.with_(batch=B, weights=wname, layers=L)
+    st = workload.build_stack(cfg)
+    stream = torch.cuda.current_stream()
+    out = torch.empty((B, cfg.D), dtype=torch.bfloat16, device="cuda")
+
+    def barrier():
+        torch.cuda.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+
+    for _ in range(max(3, args.warmup)):
+        st.decode(out_bf16=out)
+    barrier()
+    status = ddl.ddl_read_device_status(st.workspace, st.shape, B, st.s_max)
+    if status != 0:
+        raise RuntimeError(f"device status {status} after warm-up")
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    with Clocks(local) as clk:
+        barrier()
+        t_all0 = torch.cuda.Event(enable_timing=True)
+        t_all1 = torch.cuda.Event(enable_timing=True)
+        t_all0.record(stream)
+        for i in range(args.steps):
+            ev[i][0].record(stream)
+            st.decode(out_bf16=out)
+            ev[i][1].record(stream)
+        t_all1.record(stream)
+        barrier()
+    total_ms = t_all0.elapsed_time(t_all1)
+    per_ms = [a.elapsed_time(b) for a, b in ev]
+    ms = total_ms / args.steps
+    if world > 1:
+        t = torch.tensor([ms], device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    status = ddl.ddl_read_device_status(st.workspace, st.shape, B, st.s_max)
+    if status != 0:
+        raise RuntimeError(f"device status {status} in the timed region")
+
+    # end to end through the public API: pinned host x in, bf16 out back, every step
+    x_host = st.x.cpu().pin_memory()
+    out_host = torch.empty((B, cfg.D), dtype=torch.bfloat16).pin_memory()
+    x_dev = torch.empty_like(st.x)
+    barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        x_dev.copy_(x_host, non_blocking=True)
+        st.decode(out_bf16=out, x=x_dev)
+        out_host.copy_(out, non_blocking=True)
+    e1.record(stream)
+    barrier()
+    e2e_ms = e0.elapsed_time(e1) / args.steps
+    if world > 1:
+        t = torch.tensor([e2e_ms], device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+
+    nbytes = roofline.step_bytes(cfg)
+    peak, peak_kind = _peaks()
+    kernel_ms = statistics.mean(per_ms)
+    achieved = nbytes / (kernel_ms * 1e-3) / 1e9
+    launches_per_step = (L + 95) // 96 if args.mode == 0 else L * 6
+    line = {
+        "metric": METRIC,
+        "value": world * B / (ms * 1e-3),
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": max(3, args.warmup),
+        "ms_per_step": ms,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic (seeded N(0,0.02) weights quantized to INT4, N(0,1) KV and x)",
+        "config": _config_json(cfg, B, wname, L),
+        "us_per_layer": ms * 1e3 / L,
+        "hbm_gbs": nbytes / (ms * 1e-3) / 1e9,
+        "bytes_per_step": nbytes,
+        "p10_p50_p90_ms": [float(np.percentile(per_ms, q)) for q in (10, 50, 90)],
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "peak_source": f"hbm_gbs of {peak_kind}",
+                     "traffic": _traffic(cfg.name),
+                     "kernel": "decode_kernel (one persistent launch per step)"},
+        "e2e": {"value": world * B / (e2e_ms * 1e-3), "unit": "tokens/s",
+                "h2d_bytes_per_step": B * cfg.D * 2, "d2h_bytes_per_step": B * cfg.D * 2},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk.summary(),
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        cb, _ = _cpu_baseline(cfg)
+        line["cpu_baseline"] = cb
+    if rank == 0:
+        print(json.dumps(line))
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def main():
+    args = _args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,192 @@
+/*
+ * ddl.h -- C ABI of the GB300 (sm_103a) batch-B INT4 GQA decode step.
+ *
+ * The library computes one autoregressive decode step of a stack of GQA
+ * transformer decoder layers ("把基础打牢" primer, §1.1 block and §1.2
+ * decode_step): per layer
+ *     h = rmsnorm(x, norm1);  q, k, v = h Wq, h Wk, h Wv;  RoPE on q and k;
+ *     append bf16(k), bf16(v) to the KV cache at slot pos;
+ *     attn = softmax(q K^T / sqrt(hd)) V over slots 0..pos, K/V head
+ *            floor(h / (H_q / H_kv)) shared by its query group;
+ *     y = x + attn Wo;  z = y + (silu(h2 Wg) * (h2 Wu)) Wd,  h2 = rmsnorm(y, norm2)
+ * with the 4-bit weights expanded to floating point only in registers
+ * (Unsloth/Qwen-27B article, §二.3) and RMSNorm, RoPE, the KV append,
+ * SwiGLU and the residual adds fused into the weight-streaming kernels
+ * (same article §二.1; roofline reply, §三 lever 1).
+ *
+ * Conventions (every entry point):
+ *  - Pointers marked "device" are CUDA device pointers owned by the caller;
+ *    the library never frees them and allocates no device memory on the
+ *    decode path.  Pointers marked "host" are ordinary host memory.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *    stream).  Calls are asynchronous on it unless stated otherwise.
+ *  - Return value: DDL_OK (0) or a ddl_status code; nothing throws, nothing
+ *    traps.  Argument errors are found on the host before any launch.  A
+ *    device-side wait that gives up (DDL_ERR_TIMEOUT) is recorded in the
+ *    workspace and read back with ddl_read_device_status().
+ *  - bf16 tensors are passed as uint16_t bit patterns.
+ *  - All device pointers must be 16-byte aligned (DDL_ERR_ALIGN otherwise).
+ */
+#ifndef DDL_H
+#define DDL_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define DDL_GROUP 64      /* INT4 scale group along the input dimension K */
+#define DDL_MAX_BATCH 4   /* sequences per step on the batch <= 4 path */
+#define DDL_MAX_GROUP_HEADS 8 /* H_q / H_kv */
+
+typedef enum {
+    DDL_OK = 0,
+    DDL_ERR_SHAPE = 1,       /* a dimension is not supported (see ddl_shape) */
+    DDL_ERR_POS = 2,         /* pos < 0 or pos >= s_max */
+    DDL_ERR_ALIGN = 3,       /* a device pointer is not 16-byte aligned */
+    DDL_ERR_WORKSPACE = 4,   /* workspace NULL or smaller than ddl_workspace_bytes() */
+    DDL_ERR_UNSUPPORTED = 5, /* weight type / batch / layer count not supported */
+    DDL_ERR_CUDA = 6,        /* a CUDA runtime call failed (see ddl_last_cuda_error) */
+    DDL_ERR_TIMEOUT = 7,     /* a bounded device wait gave up (device status word) */
+    DDL_ERR_ARG = 8          /* NULL pointer or negative size */
+} ddl_status;
+
+/* Layer shape.  Supported: D, d_ff, H_q*head_dim multiples of 64;
+ * head_dim in {64, 128}; H_q % H_kv == 0 with H_q/H_kv <= 8; eps >= 0. */
+typedef struct {
+    int32_t D;          /* model width */
+    int32_t H_q;        /* query heads */
+    int32_t H_kv;       /* key/value heads */
+    int32_t head_dim;   /* hd */
+    int32_t d_ff;       /* SwiGLU hidden width */
+    float eps;          /* RMSNorm epsilon, inside the square root */
+    double rope_base;   /* RoPE base: angle of pair i at position p is p * base^(-2i/hd) */
+} ddl_shape;
+
+typedef enum { DDL_W_INT4 = 0, DDL_W_BF16 = 1 } ddl_wtype;
+
+/* One weight matrix W [N][K] (y = W x) in the canonical formats:
+ *  INT4: q [N][K/2] uint8, two 4-bit two's-complement codes per byte, even k
+ *        in the low nibble; scale [N][K/64] bf16.  W[n][k] = code * scale.
+ *  BF16: w [N][K] bf16.
+ * All device pointers. */
+typedef struct {
+    const uint8_t* q;
+    const uint16_t* scale;
+    const uint16_t* w;
+} ddl_mat;
+
+/* One layer's matrices in canonical format (input of ddl_pack_layer).
+ * Shapes: wq [H_q*hd][D], wk/wv [H_kv*hd][D], wo [D][H_q*hd],
+ * wg/wu [d_ff][D], wd [D][d_ff]. */
+typedef struct {
+    ddl_mat wq, wk, wv, wo, wg, wu, wd;
+} ddl_layer_src;
+
+/* One layer as the decode kernels read it.
+ *  packed: device blob written by ddl_pack_layer (ddl_packed_layer_bytes).
+ *  norm1, norm2: device bf16 [D] RMSNorm weights. */
+typedef struct {
+    const void* packed;
+    const uint16_t* norm1;
+    const uint16_t* norm2;
+} ddl_layer_w;
+
+/* One layer's KV cache: k and v each [B][H_kv][s_max][head_dim] bf16, device.
+ * Slots 0..pos-1 hold the history; decode writes slot pos. */
+typedef struct {
+    uint16_t* k;
+    uint16_t* v;
+    int64_t s_max;
+} ddl_kv;
+
+/* ------------------------------------------------------------ weights */
+
+/* Symmetric INT4 quantization with group 64 along K and a bf16 scale per
+ * group (4-bit storage expanded with its scale on arrival, Unsloth/Qwen-27B
+ * article §二.3; format: symmetric, group 64, low nibble first):
+ *     s = bf16_rne(max|w_group| / 7),  code = clamp(rne(w / s), -7, 7),
+ *     all-zero group -> s = 0, codes 0.
+ * w_bf16: device [N][K] bf16.  q_out: device [N][K/2].  scale_out: device
+ * [N][K/64].  K must be a multiple of 64, N >= 1.  Bit-exact with the oracle. */
+int ddl_quantize_int4(const uint16_t* w_bf16, int64_t N, int64_t K, uint8_t* q_out,
+                      uint16_t* scale_out, void* stream);
+
+/* Bytes of one packed layer for `shape` and weight type. */
+size_t ddl_packed_layer_bytes(const ddl_shape* shape, ddl_wtype wtype);
+
+/* Rearrange one layer's canonical matrices into the kernel-native stream
+ * (a permutation of the same codes, scales or bf16 values: 16-row tiles in
+ * tensor-core fragment order, RoPE pair rows and gate/up rows side by side,
+ * the input dimension cut into chunks of 2048).  src: device canonical
+ * matrices of `wtype`; packed_out: device, ddl_packed_layer_bytes() bytes. */
+int ddl_pack_layer(const ddl_shape* shape, ddl_wtype wtype, const ddl_layer_src* src,
+                   void* packed_out, void* stream);
+
+/* ------------------------------------------------------------ KV cache */
+
+/* Append one token's k and v for B sequences at slot pos (primer §1.2
+ * append_to_kv_cache): K[b][g][pos][:] = k_new[b][g][:], same for V.
+ * k_new, v_new: device [B][H_kv][head_dim] bf16.  Pure copy, bit-exact. */
+int ddl_kv_append(const ddl_kv* kv, int32_t B, int32_t H_kv, int32_t head_dim, int64_t pos,
+                  const uint16_t* k_new, const uint16_t* v_new, void* stream);
+
+/* ------------------------------------------------------------ decode */
+
+/* Device workspace bytes for a decode call with this shape, batch and
+ * cache length (depends on the device's SM count; query on the device the
+ * call will run on). */
+size_t ddl_workspace_bytes(const ddl_shape* shape, int32_t B, int64_t s_max);
+
+/* Where the per-stage results of the last layer of a call live inside the
+ * workspace (byte offsets; fp32 arrays):
+ *   q [B][H_q*hd] after RoPE, attn [B][H_q*hd], y [B][D], a [B][d_ff],
+ *   and the device status word (int32). */
+typedef struct {
+    size_t q, attn, y, a, status;
+} ddl_ws_view;
+int ddl_workspace_view(const ddl_shape* shape, int32_t B, int64_t s_max, ddl_ws_view* out);
+
+/* One decode step of one layer for B <= 4 sequences, all at position pos:
+ * writes KV slot pos and attends over slots 0..pos (the caller keeps slots
+ * < pos filled).  Input: resid_in [B][D] fp32, or x_bf16 [B][D] bf16 when
+ * resid_in is NULL.  Output: resid_out [B][D] fp32 (may be NULL) and
+ * out_bf16 [B][D] (may be NULL).  Outputs must not alias inputs.
+ * workspace: device, >= ddl_workspace_bytes(shape, B, kv->s_max).
+ * Calls sharing a workspace must be ordered on one stream. */
+int ddl_layer_decode(const ddl_shape* shape, ddl_wtype wtype, const ddl_layer_w* layer,
+                     const ddl_kv* kv, int32_t B, int64_t pos, const float* resid_in,
+                     const uint16_t* x_bf16, float* resid_out, uint16_t* out_bf16,
+                     void* workspace, size_t ws_bytes, void* stream);
+
+/* One decode step of an L-layer stack (primer §1.2 decode_step without the
+ * embedding and sampling): layer l's output residual (fp32) is layer l+1's
+ * input.  layers, kv: host arrays of L entries (device pointers inside);
+ * every kv[l] has the same s_max.  Other arguments as ddl_layer_decode.
+ * The whole stack runs as one persistent cooperative kernel (one CTA per
+ * SM) when the device allows it, else one launch per fused stage. */
+int ddl_stack_decode(const ddl_shape* shape, ddl_wtype wtype, const ddl_layer_w* layers,
+                     const ddl_kv* kv, int32_t L, int32_t B, int64_t pos,
+                     const float* resid_in, const uint16_t* x_bf16, float* resid_out,
+                     uint16_t* out_bf16, void* workspace, size_t ws_bytes, void* stream);
+
+/* Launch mode of the decode calls: 0 = automatic (persistent cooperative
+ * kernel when possible), 1 = one launch per fused stage. */
+int ddl_set_launch_mode(int32_t mode);
+
+/* Synchronize `stream` and read the device status word of the last decode
+ * call that used `workspace` (DDL_OK or DDL_ERR_TIMEOUT); host-blocking. */
+int ddl_read_device_status(const void* workspace, const ddl_shape* shape, int32_t B,
+                           int64_t s_max, int32_t* status_out, void* stream);
+
+const char* ddl_status_string(int status);
+
+/* The last CUDA error string seen by the library in this process ("" if none). */
+const char* ddl_last_cuda_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* DDL_H */

@@ -1,0 +1,72 @@
+// ddl_internal.h -- host-side helpers shared by the library's translation units:
+// argument validation, CUDA error capture and the packed-layer geometry.
+#pragma once
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <string.h>
+
+#include "../../include/ddl.h"
+#include "ddl_plan.h"
+
+namespace ddl {
+
+void set_cuda_error(cudaError_t e);  // records cudaGetErrorString(e) for ddl_last_cuda_error
+
+inline int cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return DDL_OK;
+  set_cuda_error(e);
+  return DDL_ERR_CUDA;
+}
+
+inline bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+// Shape rules of ddl.h.
+inline int check_shape(const ddl_shape* s) {
+  if (!s) return DDL_ERR_ARG;
+  if (s->D <= 0 || s->H_q <= 0 || s->H_kv <= 0 || s->d_ff <= 0) return DDL_ERR_SHAPE;
+  if (s->head_dim != 64 && s->head_dim != 128) return DDL_ERR_SHAPE;
+  if (s->H_q % s->H_kv != 0 || s->H_q / s->H_kv > MAX_GH) return DDL_ERR_SHAPE;
+  if (s->D % 64 || s->d_ff % 64 || (s->H_q * s->head_dim) % 64) return DDL_ERR_SHAPE;
+  if (!(s->eps >= 0.f) || !(s->rope_base > 0.0)) return DDL_ERR_SHAPE;
+  return DDL_OK;
+}
+
+inline int64_t align256(int64_t x) { return (x + 255) & ~int64_t(255); }
+
+// Geometry of the four streamed matrices of one layer (independent of the
+// grid), and the byte size of a packed layer.
+inline int64_t make_geoms(const ddl_shape& s, int wtype, MatGeom mg[4]) {
+  const int32_t Nq = s.H_q * s.head_dim, Nkv = s.H_kv * s.head_dim;
+  const int32_t dims[4][2] = {{Nq + 2 * Nkv, s.D}, {s.D, Nq}, {2 * s.d_ff, s.D}, {s.D, s.d_ff}};
+  int64_t off = 0;
+  for (int k = 0; k < 4; ++k) {
+    MatGeom& m = mg[k];
+    memset(&m, 0, sizeof m);
+    m.N = dims[k][0];
+    m.K = dims[k][1];
+    m.NT = m.N / 16;
+    m.G = m.K / DDL_GROUP;
+    m.Gc = m.G < GC ? m.G : GC;
+    m.Sk = (m.G + m.Gc - 1) / m.Gc;
+    m.T = (int64_t)m.NT * m.G;
+    m.woff = off;
+    off = align256(off + m.T * (wtype == DDL_W_INT4 ? BLK_BYTES : BF16_BLK_BYTES));
+    m.soff = off;
+    if (wtype == DDL_W_INT4) off = align256(off + m.T * SCL_BYTES);
+  }
+  return off;
+}
+
+// Partial slots per (k-chunk, tile) unit when the blocks are split over W warps.
+inline int32_t max_warps_per_unit(const MatGeom& m, int64_t W) {
+  int32_t J = 1;
+  for (int kc = 0; kc < m.Sk; ++kc)
+    for (int T = 0; T < m.NT; ++T) {
+      int64_t s = unit_start(m, kc, T), e = s + chunk_groups(m, kc) - 1;
+      int64_t n = owner_of(m.T, W, e) - owner_of(m.T, W, s) + 1;
+      if (n > J) J = (int32_t)n;
+    }
+  return J;
+}
+
+}  // namespace ddl

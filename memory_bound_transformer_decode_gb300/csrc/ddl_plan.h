@@ -1,0 +1,145 @@
+// ddl_plan.h -- geometry of the packed weight streams and of the work split,
+// shared by the host runtime and the kernels.
+//
+// Weight stream.  Each matrix W [N][K] (y = W x) is cut into 16-row tiles and
+// 64-wide groups along K (the INT4 scale group).  One (tile, group) "block" is
+// 512 bytes of 4-bit codes laid out in the register order of one
+// m16n8k16 tensor-core A fragment per 16 columns: lane (g, t) = (lane/4,
+// lane%4) owns 16 bytes = four 32-bit words, word j covering columns
+// 16j..16j+15 of rows g and g+8.  Within a word the eight nibbles are
+//   bits  0- 3: row g,   k 2t      bits 16-19: row g,   k 2t+1
+//   bits  4- 7: row g+8, k 2t      bits 20-23: row g+8, k 2t+1
+//   bits  8-11: row g,   k 2t+8    bits 24-27: row g,   k 2t+9
+//   bits 12-15: row g+8, k 2t+8    bits 28-31: row g+8, k 2t+9
+// (codes stay 4-bit two's complement, as in the canonical format).  The 16
+// bf16 scales of a block follow in a separate stream, 8 words of
+// (scale of row g | scale of row g+8 << 16).
+// Blocks are ordered (k-chunk, tile, group-in-chunk) with k-chunks of GC=32
+// groups (2048 columns; the last chunk may be shorter), so that a CTA's
+// contiguous share of the stream touches at most two chunks of x.
+//
+// Row order inside tiles (the "row map"): QKV tiles pair row i of a head with
+// row i + hd/2 (the two halves RoPE rotates together); gate/up tiles pair gate
+// row j (rows 0-7) with up row j (rows 8-15); Wo and down tiles are 16
+// consecutive rows.
+//
+// Work split ("stream-K"): the blocks of a matrix are split into W contiguous
+// ranges, one per warp of the grid.  A (k-chunk, tile) unit covered by more
+// than one warp, or a tile with more than one k-chunk, is finished by the
+// last warp that contributes to it (an atomic counter per tile), which sums
+// the partial results in a fixed order: results do not depend on timing.
+#pragma once
+#include <stdint.h>
+
+#if defined(__CUDACC__)
+#define DDL_HD __host__ __device__ __forceinline__
+#else
+#define DDL_HD inline
+#endif
+
+namespace ddl {
+
+constexpr int NW = 8;                 // warps per CTA (each streams its own ring)
+constexpr int NTHREADS = NW * 32;
+constexpr int DEPTH = 4;              // ring slots per warp
+constexpr int SLOT_BYTES = 4352;      // 8 INT4 blocks + their scales, or 16 padded KV rows
+constexpr int BLK_BYTES = 512;        // one INT4 block: 16 rows x 64 columns
+constexpr int SCL_BYTES = 32;         // scales of one block
+constexpr int BLKS_PER_SLOT = 8;
+constexpr int BF16_BLK_BYTES = 2048;  // one bf16 block: 16 rows x 64 columns
+constexpr int BF16_BLKS_PER_SLOT = 2;
+constexpr int GC = 32;                // groups per k-chunk
+constexpr int MAX_LAYERS = 96;        // layers per launch (longer stacks use several launches)
+constexpr int MAX_B = 4;
+constexpr int MAX_GH = 8;             // query heads per KV head
+constexpr int NSTAGE = 6;
+
+enum Stage { ST_QKV = 0, ST_ATT = 1, ST_COMB = 2, ST_WO = 3, ST_GU = 4, ST_DOWN = 5 };
+enum MatKind { MK_QKV = 0, MK_WO = 1, MK_GU = 2, MK_DOWN = 3 };
+
+DDL_HD int stage_mat(int st) {
+  return st == ST_QKV ? MK_QKV : st == ST_WO ? MK_WO : st == ST_GU ? MK_GU : st == ST_DOWN ? MK_DOWN : -1;
+}
+
+struct MatGeom {
+  int32_t N, K;       // rows of the (combined) matrix, input dimension
+  int32_t NT, G;      // 16-row tiles, 64-column groups per row
+  int32_t Gc, Sk;     // groups per full k-chunk, number of k-chunks
+  int32_t J;          // partial slots per (k-chunk, tile) unit
+  int32_t pad;
+  int64_t T;          // blocks
+  int64_t woff, soff; // byte offsets of the code and scale streams in a packed layer
+};
+
+DDL_HD int32_t chunk_groups(const MatGeom& m, int kc) {
+  return kc == m.Sk - 1 ? m.G - (m.Sk - 1) * m.Gc : m.Gc;
+}
+DDL_HD int64_t chunk_start(const MatGeom& m, int kc) { return (int64_t)kc * m.NT * m.Gc; }
+DDL_HD void block_coord(const MatGeom& m, int64_t b, int& kc, int& T, int& gi) {
+  int64_t per = (int64_t)m.NT * m.Gc;
+  kc = (int)(b / per);
+  if (kc > m.Sk - 1) kc = m.Sk - 1;
+  int64_t rem = b - chunk_start(m, kc);
+  int gk = chunk_groups(m, kc);
+  T = (int)(rem / gk);
+  gi = (int)(rem % gk);
+}
+DDL_HD int64_t unit_start(const MatGeom& m, int kc, int T) {
+  return chunk_start(m, kc) + (int64_t)T * chunk_groups(m, kc);
+}
+// Contiguous split of [0, total) into `parts` ranges: range i = [lo(i), lo(i+1)).
+DDL_HD int64_t range_lo(int64_t total, int64_t parts, int64_t i) { return total * i / parts; }
+// The part owning item b (total > 0).
+DDL_HD int64_t owner_of(int64_t total, int64_t parts, int64_t b) {
+  return ((b + 1) * parts - 1) / total;
+}
+
+// Row of the combined matrix held by row r (0..15) of tile T.
+DDL_HD int32_t tile_row(int kind, int T, int r, int hd) {
+  if (kind == MK_QKV) {
+    int tph = hd / 16, head = T / tph, mm = T % tph;
+    return head * hd + (r < 8 ? 8 * mm + r : 8 * mm + (r - 8) + hd / 2);
+  }
+  if (kind == MK_GU) return r < 8 ? 8 * T + r : 8 * T + (r - 8);  // gate row / up row
+  return 16 * T + r;
+}
+
+struct LayerDev {
+  const uint8_t* packed;
+  const uint16_t* norm1;
+  const uint16_t* norm2;
+  uint16_t* kc;
+  uint16_t* vc;
+};
+
+struct Params {
+  int32_t D, Hq, Hkv, hd, dff, B, GH;  // GH = Hq / Hkv
+  float eps;
+  int32_t wtype;
+  double rope_base;
+  int64_t pos, s_max;
+  int32_t L;            // layers in this launch
+  int32_t l0;           // global index of this launch's first layer
+  int32_t final_last;   // this launch's last layer is the stack's last
+  int32_t stage_begin, stage_end;  // flattened (layer * NSTAGE + stage) range
+  int32_t cooperative;
+  int32_t nt_att;       // 16-key tiles per sequence
+  int32_t J_att;        // attention partial slots per sequence
+  MatGeom mg[4];
+  const float* resid_in;
+  const uint16_t* x_bf16;
+  float* resid_out;
+  uint16_t* out_bf16;
+  uint32_t* ctrl;       // [0] grid barrier counter, [1] status word
+  uint32_t* cnt;        // per-tile arrival counters
+  float* gpart;         // GEMV partials: [unit][J][32 lanes][2]
+  float* apart;         // attention partials: [seq][J_att][GH*(hd+2)]
+  float* Z;             // [2][B][D] residual ping-pong between layers
+  float* q;             // [B][Hq*hd]
+  float* attn;          // [B][Hq*hd]
+  float* y;             // [B][D]
+  float* a;             // [B][dff]
+  LayerDev layers[MAX_LAYERS];
+};
+
+}  // namespace ddl

@@ -1,0 +1,83 @@
+"""Host-side checks of the C-ABI library that need no GPU: it builds for
+sm_103a, loads, exports every entry point include/ddl.h declares, and its
+host-only calls (status strings, packed-layer sizes, argument checks) behave.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+from memory_bound_transformer_decode_gb300 import build, configs, ddl
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    text = open(os.path.join(ROOT, "include", "ddl.h")).read()
+    return sorted(set(re.findall(r"^(?:int|size_t|const char\*)\s+(ddl_\w+)\(", text, re.M)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return ddl.load()
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = _declared()
+    assert len(names) >= 12
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(names) == set(ddl.EXPORTED)
+
+
+def test_status_strings(lib):
+    for code in range(9):
+        assert lib.ddl_status_string(code)
+    assert lib.ddl_status_string(99) == b"unknown status"
+
+
+def _geom_bytes(cfg, int4: bool) -> int:
+    al = lambda x: (x + 255) // 256 * 256  # noqa: E731
+    dims = [(cfg.Nq + 2 * cfg.Nkv, cfg.D), (cfg.D, cfg.Nq), (2 * cfg.d_ff, cfg.D), (cfg.D, cfg.d_ff)]
+    off = 0
+    for N, K in dims:
+        T = (N // 16) * (K // 64)
+        off = al(off + T * (512 if int4 else 2048))
+        if int4:
+            off = al(off + T * 32)
+    return off
+
+
+@pytest.mark.parametrize("cfg", configs.ALL)
+def test_packed_layer_bytes(lib, cfg):
+    shape = ddl.make_shape(cfg)
+    n4 = ddl.ddl_packed_layer_bytes(shape, ddl.INT4)
+    nb = ddl.ddl_packed_layer_bytes(shape, ddl.BF16)
+    assert n4 == _geom_bytes(cfg, True)
+    assert nb == _geom_bytes(cfg, False)
+    # exactly the codes and scales (or bf16 values), up to 256-byte alignment
+    mac = sum(n * k for n, k in [(cfg.Nq + 2 * cfg.Nkv, cfg.D), (cfg.D, cfg.Nq),
+                                 (2 * cfg.d_ff, cfg.D), (cfg.D, cfg.d_ff)])
+    assert 0 <= n4 - (mac // 2 + mac // 32) < 8 * 256
+    assert 0 <= nb - 2 * mac < 4 * 256
+
+
+def test_shape_rules(lib):
+    bad = [ddl.Shape(128, 4, 2, 96, 192, 1e-6, 1e4),   # head_dim
+           ddl.Shape(100, 4, 2, 64, 192, 1e-6, 1e4),   # D % 64
+           ddl.Shape(128, 4, 3, 64, 192, 1e-6, 1e4),   # H_q % H_kv
+           ddl.Shape(128, 16, 1, 64, 192, 1e-6, 1e4),  # group > 8
+           ddl.Shape(128, 4, 2, 64, 100, 1e-6, 1e4)]   # d_ff % 64
+    for s in bad:
+        assert ddl.ddl_packed_layer_bytes(s, ddl.INT4) == 0
+
+
+def test_host_argument_checks(lib):
+    assert lib.ddl_set_launch_mode(7) == 8
+    assert lib.ddl_set_launch_mode(0) == 0
+    assert lib.ddl_quantize_int4(None, 4, 64, None, None, None) == 8
+    kv = ddl.KV(16, 16, 10)
+    assert lib.ddl_kv_append(ctypes.byref(kv), 1, 1, 64, 10, ctypes.c_void_p(16),
+                             ctypes.c_void_p(16), None) == 2
