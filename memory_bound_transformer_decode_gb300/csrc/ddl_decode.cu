@@ -398,10 +398,12 @@ __device__ void gemv_finish(const Params& P, int layer, int st, const MatGeom& m
   const int64_t u = (int64_t)kc * m.NT + T;
   float2* part = reinterpret_cast<float2*>(P.gpart);
   part[(u * m.J + (wg - wf)) * 32 + lane] = make_float2(v0, v1);
+  // contributors = warps with a non-empty range that own blocks of the tile
+  // (with fewer blocks than warps, a warp owns at most one block)
   int ncontrib = 0;
   for (int k = 0; k < m.Sk; ++k) {
     const int64_t s0 = unit_start(m, k, T), e0 = s0 + chunk_groups(m, k) - 1;
-    ncontrib += (int)(owner_of(m.T, W, e0) - owner_of(m.T, W, s0) + 1);
+    ncontrib += (int)(m.T >= W ? owner_of(m.T, W, e0) - owner_of(m.T, W, s0) + 1 : e0 - s0 + 1);
   }
   __syncwarp();
   uint32_t old = 0;
@@ -418,6 +420,7 @@ __device__ void gemv_finish(const Params& P, int layer, int st, const MatGeom& m
     const int64_t a0 = unit_start(m, k, T), e0 = a0 + chunk_groups(m, k) - 1;
     const int64_t f0 = owner_of(m.T, W, a0), n0 = owner_of(m.T, W, e0) - f0 + 1;
     for (int64_t j = 0; j < n0; ++j) {
+      if (range_lo(m.T, W, f0 + j) == range_lo(m.T, W, f0 + j + 1)) continue;  // empty range
       const float2 v = __ldcg(part + (uk * m.J + j) * 32 + lane);
       s0 += v.x;
       s1 += v.y;
@@ -755,6 +758,7 @@ __device__ void stage_comb(const Params& P, int64_t wg, int64_t W) {
     const int64_t cf = owner_of(Ta, C, seq * nt), cl = owner_of(Ta, C, seq * nt + nt - 1);
     float mx = -INFINITY, l = 0.f, o = 0.f;
     for (int64_t jc = 0; jc <= cl - cf; ++jc) {
+      if (range_lo(Ta, C, cf + jc) == range_lo(Ta, C, cf + jc + 1)) continue;  // CTA with no tiles
       const float* rec = P.apart + (seq * P.J_att + jc) * REC;
       const float m = __ldcg(rec + GH * HD + hl), lj = __ldcg(rec + GH * HD + GH + hl);
       const float oj = __ldcg(rec + hl * HD + d);
@@ -901,8 +905,10 @@ static int64_t att_J(int64_t seqs, int64_t nt, int64_t C) {
 static void ws_layout(const ddl_shape& s, int B, int64_t s_max, int C, const MatGeom mg[4],
                       WsLayout& w) {
   const int64_t Nq = (int64_t)s.H_q * s.head_dim, GH = s.H_q / s.H_kv;
-  int64_t nt_max = (s_max + 15) / 16;
-  int64_t Jatt = nt_max < C ? nt_max : C;
+  // attention partial slot of a sequence = CTA index - the sequence's first CTA;
+  // with fewer tiles than CTAs that span includes CTAs without tiles, so it is
+  // bounded by the grid, not by the tile count
+  const int64_t Jatt = C;
   int64_t gpart = 0, ntmax = 0;
   for (int k = 0; k < 4; ++k) {
     const int64_t u = (int64_t)mg[k].Sk * mg[k].NT * mg[k].J * 32 * 2 * 4;
