@@ -172,6 +172,31 @@ int ddl_stack_decode(const ddl_shape* shape, ddl_wtype wtype, const ddl_layer_w*
                      const float* resid_in, const uint16_t* x_bf16, float* resid_out,
                      uint16_t* out_bf16, void* workspace, size_t ws_bytes, void* stream);
 
+/* Size of the library's own static scratch array (32 MiB), used only by
+ * ddl_stack_decode_noalloc. */
+#define DDL_NOALLOC_SCRATCH_BYTES (32u << 20)
+
+/* ddl_stack_decode without a workspace argument, for callers that cannot
+ * allocate device memory (a plugin whose host framework owns all device
+ * memory and passes only inputs and outputs, or a loop that must not take
+ * cudaMalloc's implicit device synchronization).  The pages have no
+ * counterpart: this is an interface convenience, not part of the method.
+ * Arguments and results are those of ddl_stack_decode.  The scratch is a
+ * file-scope device array of DDL_NOALLOC_SCRATCH_BYTES that every GPU loading
+ * the library keeps until process exit; the call allocates nothing.
+ *  - The first call on a device looks up the array's device address
+ *    (cudaGetSymbolAddress); make that first call before any stream capture.
+ *  - Returns DDL_ERR_WORKSPACE when the shape, batch and cache length need
+ *    more scratch than DDL_NOALLOC_SCRATCH_BYTES (ddl_workspace_bytes tells).
+ *  - All calls share the array and a call leaves its contents behind; calls
+ *    that overlap on the GPU (other streams, other threads) race on it, so
+ *    order them on one stream.  The device status word of these calls is
+ *    not readable through ddl_read_device_status. */
+int ddl_stack_decode_noalloc(const ddl_shape* shape, ddl_wtype wtype, const ddl_layer_w* layers,
+                             const ddl_kv* kv, int32_t L, int32_t B, int64_t pos,
+                             const float* resid_in, const uint16_t* x_bf16, float* resid_out,
+                             uint16_t* out_bf16, void* stream);
+
 /* Launch mode of the decode calls: 0 = automatic (persistent cooperative
  * kernel when possible), 1 = one launch per fused stage. */
 int ddl_set_launch_mode(int32_t mode);

@@ -22,7 +22,7 @@ STATUS = {0: "DDL_OK", 1: "DDL_ERR_SHAPE", 2: "DDL_ERR_POS", 3: "DDL_ERR_ALIGN",
           7: "DDL_ERR_TIMEOUT", 8: "DDL_ERR_ARG"}
 EXPORTED = ("ddl_quantize_int4", "ddl_packed_layer_bytes", "ddl_pack_layer", "ddl_kv_append",
             "ddl_workspace_bytes", "ddl_workspace_view", "ddl_layer_decode", "ddl_stack_decode",
-            "ddl_set_launch_mode", "ddl_read_device_status", "ddl_status_string",
+            "ddl_stack_decode_noalloc", "ddl_set_launch_mode", "ddl_read_device_status", "ddl_status_string",
             "ddl_last_cuda_error")
 
 
@@ -98,6 +98,8 @@ def load(build_if_missing: bool = False):
                                          vp, vp, vp, sz, vp]
         lib.ddl_stack_decode.argtypes = [P(Shape), ctypes.c_int, P(LayerW), P(KV), i32, i32, i64,
                                          vp, vp, vp, vp, vp, sz, vp]
+        lib.ddl_stack_decode_noalloc.argtypes = [P(Shape), ctypes.c_int, P(LayerW), P(KV), i32, i32,
+                                                 i64, vp, vp, vp, vp, vp]
         lib.ddl_set_launch_mode.argtypes = [i32]
         lib.ddl_read_device_status.argtypes = [vp, P(Shape), i32, i64, P(i32), vp]
         lib.ddl_status_string.argtypes = [ctypes.c_int]
@@ -233,6 +235,22 @@ def ddl_stack_decode(shape: Shape, wtype: int, layers: list, kvs: list, pos: int
                               _ptr(workspace), workspace.numel() * workspace.element_size(),
                               _stream(stream))
     _check("ddl_stack_decode", st)
+
+
+def ddl_stack_decode_noalloc(shape: Shape, wtype: int, layers: list, kvs: list, pos: int, *,
+                             x_bf16: torch.Tensor | None = None,
+                             resid_in: torch.Tensor | None = None,
+                             resid_out: torch.Tensor | None = None,
+                             out_bf16: torch.Tensor | None = None, stream=None):
+    """ddl_stack_decode with the library's static scratch instead of a
+    workspace, for callers that cannot allocate device memory."""
+    lib = load()
+    B = (x_bf16 if x_bf16 is not None else resid_in).shape[0]
+    lw, kv = _layers_and_kv(layers, kvs)
+    st = lib.ddl_stack_decode_noalloc(ctypes.byref(shape), wtype, lw, kv, len(layers), B, int(pos),
+                                      _ptr(resid_in), _ptr(x_bf16), _ptr(resid_out),
+                                      _ptr(out_bf16), _stream(stream))
+    _check("ddl_stack_decode_noalloc", st)
 
 
 def ddl_layer_decode(shape: Shape, wtype: int, layer: dict, kv: tuple, pos: int, *,

@@ -1,0 +1,58 @@
+"""ddl_stack_decode_noalloc against ddl_stack_decode.
+
+The allocation-free entry point serves callers that cannot allocate device
+memory (a plugin that is handed only its inputs and outputs, or a loop that
+must not pay cudaMalloc's implicit device synchronization); it takes its
+scratch from the library's static device array.  Two calls in a row must
+match the workspace entry point within the decode tolerance (the second call
+runs on whatever the first left in the shared array), and a problem larger
+than the array must be rejected.  This file is collected last.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from memory_bound_transformer_decode_gb300 import configs, ddl, synth, workload
+
+pytestmark = pytest.mark.gpu
+
+REL_L2, MAX_ABS = 2e-3, 2e-2
+
+
+def test_noalloc_matches_workspace_entry_point_twice():
+    ddl.load(build_if_missing=True)
+    cfg = configs.DecodeConfig("noalloc-3L", D=256, H_q=8, H_kv=2, head_dim=128, d_ff=320,
+                               rope_base=1e4, kv_len=37, layers=3, seed=21)
+    st = workload.build_stack(cfg, batch=2)
+    B, D = st.batch, cfg.D
+    out_ref = torch.empty((B, D), dtype=torch.bfloat16, device="cuda")
+    res_ref = torch.empty((B, D), dtype=torch.float32, device="cuda")
+    st.decode(out_bf16=out_ref, resid_out=res_ref)
+    torch.cuda.synchronize()
+    ref_o = oracle.bf16_to_f64(synth.bits(out_ref))
+    ref_r = res_ref.cpu().numpy().astype(np.float64)
+    for _ in range(2):
+        out = torch.full((B, D), float("nan"), dtype=torch.bfloat16, device="cuda")
+        res = torch.full((B, D), float("nan"), dtype=torch.float32, device="cuda")
+        ddl.ddl_stack_decode_noalloc(st.shape, st.wtype, st.layers, st.kvs, st.pos, x_bf16=st.x,
+                                     resid_out=res, out_bf16=out)
+        torch.cuda.synchronize()
+        got_o = oracle.bf16_to_f64(synth.bits(out))
+        got_r = res.cpu().numpy().astype(np.float64)
+        assert np.linalg.norm(got_o - ref_o) / np.linalg.norm(ref_o) <= REL_L2
+        assert np.max(np.abs(got_r - ref_r)) <= MAX_ABS
+
+
+def test_noalloc_rejects_problems_larger_than_its_scratch():
+    lib = ddl.load(build_if_missing=True)
+    big = ddl.Shape(8192, 64, 8, 128, 262144, 1e-6, 5e5)
+    need = ddl.ddl_workspace_bytes(big, 4, 1024)
+    assert need > (32 << 20)
+    lw = (ddl.LayerW * 1)(ddl.LayerW(256, 256, 256))
+    kv = (ddl.KV * 1)(ddl.KV(256, 256, 1024))
+    st = lib.ddl_stack_decode_noalloc(ctypes.byref(big), ddl.INT4, lw, kv, 1, 4, 0, None,
+                                      ctypes.c_void_p(256), None, ctypes.c_void_p(256), None)
+    assert st == 4  # DDL_ERR_WORKSPACE, before any launch
