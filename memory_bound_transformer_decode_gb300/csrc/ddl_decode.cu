@@ -1,7 +1,7 @@
 // ddl_decode.cu -- the decode step: one persistent kernel that streams every
 // weight and KV byte of an L-layer stack once, and its host runtime.
 //
-// Per layer the kernel runs six stages (primer "把基础打牢" §1.1 block, §1.2
+// Per layer the kernel runs five stages (primer "把基础打牢" §1.1 block, §1.2
 // decode_step):
 //   QKV  : rmsnorm(x) folded into the GEMV (W (x*w1)) * r, INT4 codes expanded
 //          in registers and multiplied on the tensor cores, RoPE on q and k,
@@ -10,8 +10,8 @@
 //   ATT  : split-KV GQA decode attention: each K/V head is read once, in
 //          place, for its whole query group (same article §二.2), with an
 //          online softmax per 16-key tile (FlashAttention-style tiling, roofline
-//          reply §四)
-//   COMB : merge of the split-KV partial softmax states
+//          reply §四); the last CTA to finish a sequence merges its
+//          split-KV partial softmax states
 //   WO   : y = x + attn Wo
 //   GU   : rmsnorm(y) folded into the gate/up GEMV, silu(g) * u in the epilogue
 //          (Unsloth/Qwen-27B article §二.1 fused SwiGLU)
@@ -37,39 +37,51 @@ namespace ddl {
 constexpr int SM_RING = 0;
 constexpr int SM_RING_BYTES = NW * DEPTH * SLOT_BYTES;
 constexpr int SM_BARS = SM_RING_BYTES;
-constexpr int SM_SCR = SM_BARS + 256;
-constexpr int XF_BYTES = 2 * GC * 4 * (2 * MAX_B) * 4 * 8;  // x fragments, 2 k-chunks
-constexpr int SX_BYTES = 2 * GC * MAX_B * 4;                // per-group sums of x
+constexpr int SM_PBAR = SM_BARS + NW * DEPTH * 8;  // the prologue's bulk-copy barrier
+constexpr int SM_SCR = SM_BARS + 512;
+constexpr int XF_BYTES = XF_CHUNKS * GC * 4 * 2 * 4 * 8;  // x fragments: chunks x batch <= 8
+constexpr int SX_BYTES = XF_CHUNKS * GC * MAX_B * 4;        // per-group sums of x
 constexpr int SM_SCR_BYTES = 70 * 1024;
 constexpr int SM_MISC = SM_SCR + SM_SCR_BYTES;
 constexpr int SM_MISC_BYTES = 2048;
 constexpr int SM_TOTAL = SM_MISC + SM_MISC_BYTES;
-static_assert(XF_BYTES + SX_BYTES <= SM_SCR_BYTES, "x fragments do not fit");
-static_assert(NW * 2 * MAX_GH * (128 + 2) * 4 <= SM_SCR_BYTES, "attention records do not fit");
+static_assert(XF_BYTES + SX_BYTES + NW * 32 * 4 <= SM_SCR_BYTES, "x fragments do not fit");
+static_assert(NW * 2 * (MAX_GH * (128 + 2) + 3) * 4 <= SM_SCR_BYTES, "attention records do not fit");
 static_assert(SM_TOTAL <= 227 * 1024, "shared memory budget");
 
 struct Misc {
   float rnorm[MAX_B];
-  float escale[2][MAX_B];  // 2^e of each staged k-chunk and sequence
-  float edown[2][MAX_B];   // 2^-e
-  float red[NW][3 * MAX_B];
-  float rope[64][2];       // cos, sin of pair i at position pos
+  float escale[MAX_B];     // 2^e of the staged x of each sequence
+  float edown[MAX_B];      // 2^-e
+  float red[NW][2 * MAX_B];
   int kc_lo, nkc;
   int abort;
   int seg_n[NW];
   long long seg_first[NW], seg_last[NW];
+  long long mseq[8];       // sequences this CTA merges last
+  uint32_t pphase;         // completed phases of the prologue barrier
 };
 static_assert(sizeof(Misc) <= SM_MISC_BYTES, "misc");
 
 enum SlotKind { SK_GEMV = 0, SK_K = 1, SK_V = 2 };
 
 struct SlotDesc {
-  int kind, layer, mk, cnt;
+  int kind, cnt;
   int64_t a;
 };
+// Producer cursor over this warp's slots of every stage of the launch; it
+// caches the current stage's stream bases so that issuing a slot reads no
+// per-layer parameter with a run-time index.
 struct Cursor {
   int s;
   int64_t pos, end;
+  const uint8_t* wbase;   // GEMV: code (or bf16) stream of the matrix
+  const uint8_t* sbase;   // GEMV: scale stream (INT4)
+  const uint16_t* kbase;  // ATT: K cache of the layer
+  const uint16_t* vbase;  // ATT: V cache of the layer
+  int kc, T, gi, gk;      // GEMV: (k-chunk, tile, group) of work index `pos`
+  int NT, Sk, Gc, G;      // GEMV: geometry of the matrix
+  int pk0, pk1;           // GEMV: k-chunks of this CTA's panel
 };
 struct Ring {
   uint32_t slot0, bar0, n_issued, n_done;
@@ -86,92 +98,109 @@ __device__ __forceinline__ void att_range(const Params& P, int64_t& lo, int64_t&
   lo = clo + range_lo(chi - clo, NW, w);
   hi = clo + range_lo(chi - clo, NW, w + 1);
 }
-__device__ __forceinline__ int slot_blocks(const Params& P) {
-  return P.wtype == DDL_W_INT4 ? BLKS_PER_SLOT : BF16_BLKS_PER_SLOT;
-}
-__device__ __forceinline__ void cursor_range(const Params& P, int s, int64_t wg, int64_t W,
-                                             int64_t& lo, int64_t& hi) {
-  const int st = s % NSTAGE;
+template <int WT>
+__device__ __forceinline__ void cursor_enter(const Params& P, Cursor& c, int64_t wg, int64_t W) {
+  const int st = c.s % NSTAGE;
+  const LayerDev& Ld = P.layers[c.s / NSTAGE];
   if (st == ST_ATT) {
-    att_range(P, lo, hi);
-    lo *= 2;
-    hi *= 2;
-  } else if (st == ST_COMB) {
-    lo = hi = 0;
+    att_range(P, c.pos, c.end);
+    c.pos *= 2;
+    c.end *= 2;
+    c.kbase = Ld.kc;
+    c.vbase = Ld.vc;
   } else {
-    const int64_t T = P.mg[stage_mat(st)].T;
-    lo = range_lo(T, W, wg);
-    hi = range_lo(T, W, wg + 1);
+    const MatGeom& m = P.mg[stage_mat(st)];
+    const int p = panel_of_cta(m, blockIdx.x);
+    uint32_t lo, hi;
+    warp_work(m, p, blockIdx.x - m.pc[p], threadIdx.x >> 5, NW, lo, hi);
+    c.pos = lo;
+    c.end = hi;
+    c.wbase = Ld.packed + m.woff;
+    c.sbase = Ld.packed + m.soff;
+    c.NT = m.NT;
+    c.Sk = m.Sk;
+    c.Gc = m.Gc;
+    c.G = m.G;
+    c.pk0 = m.pk[p];
+    c.pk1 = m.pk[p + 1];
+    if (lo < hi) {
+      work_coord(m, p, lo, c.T, c.kc, c.gi);
+      c.gk = chunk_groups(m, c.kc);
+    }
   }
 }
+template <int WT>
 __device__ __forceinline__ bool cursor_next(const Params& P, Cursor& c, int64_t wg, int64_t W,
                                             SlotDesc& d) {
   while (c.pos >= c.end) {
     if (++c.s >= P.stage_end) return false;
-    cursor_range(P, c.s, wg, W, c.pos, c.end);
+    cursor_enter<WT>(P, c, wg, W);
   }
-  const int st = c.s % NSTAGE;
-  d.layer = c.s / NSTAGE;
-  if (st == ST_ATT) {
+  if (c.s % NSTAGE == ST_ATT) {
     const int64_t tile = c.pos >> 1;
     d.kind = (c.pos & 1) ? SK_V : SK_K;
     d.a = tile;
-    const int64_t i = tile % P.nt_att;
-    const int64_t rows = P.pos - 16 * i;
+    const int64_t rows = P.pos - 16 * (int64_t)((uint32_t)tile % (uint32_t)P.nt_att);
     d.cnt = (int)(rows < 0 ? 0 : rows > 16 ? 16 : rows);
-    d.mk = -1;
     c.pos += 1;
-  } else {
+  } else {  // up to PER blocks of one (k-chunk, tile) unit, in panel work order
+    constexpr int PER = WT == DDL_W_INT4 ? BLKS_PER_SLOT : BF16_BLKS_PER_SLOT;
     d.kind = SK_GEMV;
-    d.mk = stage_mat(st);
-    d.a = c.pos;
     const int64_t left = c.end - c.pos;
-    d.cnt = (int)(left < slot_blocks(P) ? left : slot_blocks(P));
-    c.pos += d.cnt;
+    int n = (int)(left < PER ? left : PER);
+    if (n > c.gk - c.gi) n = c.gk - c.gi;
+    d.a = (int64_t)c.kc * c.NT * c.Gc + (int64_t)c.T * c.gk + c.gi;  // stream block index
+    d.cnt = n;
+    c.pos += n;
+    c.gi += n;
+    if (c.gi == c.gk) {
+      c.gi = 0;
+      if (++c.kc == c.pk1) {
+        c.kc = c.pk0;
+        ++c.T;
+      }
+      c.gk = c.kc == c.Sk - 1 ? c.G - (c.Sk - 1) * c.Gc : c.Gc;
+    }
   }
   return true;
 }
 
-template <int HD>
-__device__ __forceinline__ void issue_slot(const Params& P, const SlotDesc& d, uint32_t slot,
-                                           uint32_t bar, int lane, uint64_t policy) {
+template <int HD, int WT>
+__device__ __forceinline__ void issue_slot(const Params& P, const Cursor& c, const SlotDesc& d,
+                                           uint32_t slot, uint32_t bar, int lane, uint64_t policy) {
   constexpr int ROWB = HD * 2 + 16;
-  const LayerDev& Ld = P.layers[d.layer];
   if (d.kind == SK_GEMV) {
     if (lane == 0) {
-      const MatGeom& m = P.mg[d.mk];
-      const bool q4 = P.wtype == DDL_W_INT4;
-      const uint32_t wb = d.cnt * (q4 ? BLK_BYTES : BF16_BLK_BYTES);
-      const uint32_t sb = q4 ? d.cnt * SCL_BYTES : 0;
+      constexpr bool q4 = WT == DDL_W_INT4;
+      constexpr uint32_t BB = q4 ? BLK_BYTES : BF16_BLK_BYTES;
+      const uint32_t wb = d.cnt * BB, sb = q4 ? d.cnt * SCL_BYTES : 0;
       mbar_arrive_expect_tx(bar, wb + sb);
-      bulk_g2s_evict_first(slot, Ld.packed + m.woff + d.a * (q4 ? BLK_BYTES : BF16_BLK_BYTES), wb,
-                           bar, policy);
-      if (sb) bulk_g2s_evict_first(slot + BLKS_PER_SLOT * BLK_BYTES, Ld.packed + m.soff + d.a * SCL_BYTES,
-                                   sb, bar, policy);
+      bulk_g2s_evict_first(slot, c.wbase + d.a * BB, wb, bar, policy);
+      if (q4) bulk_g2s_evict_first(slot + BLKS_PER_SLOT * BLK_BYTES, c.sbase + d.a * SCL_BYTES, sb, bar, policy);
     }
   } else {
-    const int64_t seq = d.a / P.nt_att, i = d.a % P.nt_att;
-    const uint16_t* base = (d.kind == SK_K ? Ld.kc : Ld.vc) + (seq * P.s_max + 16 * i) * HD;
+    const uint32_t seq = (uint32_t)d.a / (uint32_t)P.nt_att, i = (uint32_t)d.a - seq * (uint32_t)P.nt_att;
+    const uint16_t* base = (d.kind == SK_K ? c.kbase : c.vbase) + ((int64_t)seq * P.s_max + 16 * i) * HD;
     if (lane == 0) mbar_arrive_expect_tx(bar, d.cnt * HD * 2);
     if (lane < d.cnt) bulk_g2s_evict_first(slot + lane * ROWB, base + lane * HD, HD * 2, bar, policy);
   }
 }
 
 // Release the slot just consumed and refill the ring from the cursor.
-template <int HD>
+template <int HD, int WT>
 __device__ __forceinline__ void ring_advance(const Params& P, Ring& R, Cursor& prod, int64_t wg,
                                              int64_t W, int lane, uint64_t policy) {
   __syncwarp();
   SlotDesc d;
-  if (cursor_next(P, prod, wg, W, d)) {
+  if (cursor_next<WT>(P, prod, wg, W, d)) {
     fence_proxy_async_smem();  // every issuing lane: earlier generic smem accesses first
-    issue_slot<HD>(P, d, R.slot(R.n_issued), R.bar(R.n_issued), lane, policy);
+    issue_slot<HD, WT>(P, prod, d, R.slot(R.n_issued), R.bar(R.n_issued), lane, policy);
     R.n_issued++;
   }
   R.n_done++;
 }
 
-// ------------------------------------------------------------------ block-wide reduce
+// ------------------------------------------------------------------ small helpers
 __device__ __forceinline__ float warp_sum(float v) {
   for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(FULL, v, o);
   return v;
@@ -180,144 +209,252 @@ __device__ __forceinline__ float warp_max(float v) {
   for (int o = 16; o; o >>= 1) v = fmaxf(v, __shfl_xor_sync(FULL, v, o));
   return v;
 }
-
-// Layer input x (fp32 residual) of global layer gl, element i of sequence b.
-__device__ __forceinline__ float layer_input(const Params& P, int gl, int b, int i) {
-  const int64_t o = (int64_t)b * P.D + i;
-  if (gl == 0) return P.resid_in ? __ldcg(P.resid_in + o) : bf16_bits_to_f32(P.x_bf16[o]);
-  return __ldcg(P.Z + (int64_t)((gl - 1) & 1) * P.B * P.D + o);
+__device__ __forceinline__ float lds_f32(uint32_t a) { return __uint_as_float(lds32(a)); }
+__device__ __forceinline__ uint32_t atom_add_acq_rel(uint32_t* p, uint32_t v) {
+  uint32_t old;
+  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+__device__ __forceinline__ float4 bf16x4_f32(uint2 u) {
+  return make_float4(bf16lo_f32(u.x), bf16hi_f32(u.x), bf16lo_f32(u.y), bf16hi_f32(u.y));
 }
 
+// Optional trace: %globaltimer stamps per (stage, CTA): start, end of the
+// prologue, end of each warp's stream, end of the stage.
+__device__ __forceinline__ void trace_stamp(const Params& P, int s, int slot) {
+  if (P.trace)
+    P.trace[((int64_t)(s - P.stage_begin) * gridDim.x + blockIdx.x) * TRACE_WORDS + slot] = globaltimer();
+}
+
+// Per-stage constants of a GEMV stage, read once from the parameters.
+struct GemvCtx {
+  MatGeom m;
+  int st, layer, gl;
+  const float* xin32;     // layer input (fp32) or NULL
+  const uint16_t* xin16;  // layer input (bf16) when xin32 is NULL (QKV / WO of layer 0)
+  uint16_t* kc;           // K, V caches (QKV epilogue)
+  uint16_t* vc;
+  float* zout;            // residual output of this layer (DOWN)
+  bool final_layer;
+  int p, cl;              // this CTA's panel and its index among the panel's CTAs
+};
+
 // ------------------------------------------------------------------ GEMV prologue
-// Stages this CTA's share of the activation as m16n8k16 B fragments: column
-// 2b is the fp16 "high" part of sequence b's x (times the norm weight and
-// 2^-e), column 2b+1 the fp16 remainder, so x is carried to ~22 bits.  Also
-// computes the RMSNorm factor r (QKV, GU), the per-k-chunk power-of-two scale
+// Stages this CTA's panel of the activation (k-chunks pk[p]..pk[p+1]-1) as
+// m16n8k16 B fragments: column 2b is the fp16 "high" part of sequence b's x
+// (times the norm weight and 2^-e), column 2b+1 the fp16 remainder, so x is
+// carried to ~22 bits.  Also computes the RMSNorm factor r (QKV, GU), the
+// power-of-two scale 2^e that brings the panel's largest |x| to [2^11, 2^12),
 // and, for INT4, the per-group sums of x used to remove the +8 code offset.
+// One round trip: every thread issues a 256-byte bulk copy of one (group,
+// sequence) of x into shared memory while the sum of squares is loaded; the
+// conversion then runs in place, group by group, from shared memory.
+// Shared layout of a group (B x 256 bytes): raw x[b][64] fp32, later the
+// fragments [j][column 2b+h][lane t][register half] of 2 x fp16.
 template <int HD, int WT>
-__device__ void gemv_prologue(const Params& P, int layer, int st, const MatGeom& m, int64_t W,
-                              uint8_t* smem, Misc& M) {
+__device__ void gemv_prologue(const Params& P, const GemvCtx& E, uint8_t* smem, Misc& M,
+                              uint32_t pbar) {
+  const MatGeom& m = E.m;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int B = P.B, B2 = 2 * B, gl = P.l0 + layer;
-  const LayerDev& Ld = P.layers[layer];
-  const int64_t clo = range_lo(m.T, W, (int64_t)blockIdx.x * NW);
-  const int64_t chi = range_lo(m.T, W, (int64_t)(blockIdx.x + 1) * NW);
-  int kc_lo = 0, nkc = 0;
-  if (clo < chi) {
-    int a, b_, kc_hi;
-    block_coord(m, clo, kc_lo, a, b_);
-    block_coord(m, chi - 1, kc_hi, a, b_);
-    nkc = kc_hi - kc_lo + 1;
-  }
-  const float* xf32 = nullptr;
+  const int B = P.B;
+  const int kc_lo = m.pk[E.p], nkc = m.pk[E.p + 1] - kc_lo;
+  const float* x32 = nullptr;
+  const uint16_t* x16 = nullptr;
   const uint16_t* nw = nullptr;
-  bool from_input = false;
-  switch (st) {
-    case ST_QKV: from_input = true; nw = Ld.norm1; break;
-    case ST_WO: xf32 = P.attn; break;
-    case ST_GU: xf32 = P.y; nw = Ld.norm2; break;
-    default: xf32 = P.a; break;
+  const LayerDev& Ld = P.layers[E.layer];
+  switch (E.st) {
+    case ST_QKV: nw = Ld.norm1; x32 = E.xin32; x16 = E.xin16; break;
+    case ST_WO: x32 = P.attn; break;
+    case ST_GU: x32 = P.y; nw = Ld.norm2; break;
+    default: x32 = P.a; break;
   }
   const int K = m.K;
-  const int k_lo = kc_lo * GC * DDL_GROUP;
-  const int k_hi = min(K, (kc_lo + nkc) * GC * DDL_GROUP);
-  auto load = [&](int b, int k) -> float {
-    return from_input ? layer_input(P, gl, b, k) : __ldcg(xf32 + (int64_t)b * K + k);
-  };
-  if (st == ST_QKV && tid < HD / 2) {
-    const double theta = pow(P.rope_base, -2.0 * (double)tid / (double)HD);
-    double sn, cs;
-    sincos((double)P.pos * theta, &sn, &cs);
-    M.rope[tid][0] = (float)cs;
-    M.rope[tid][1] = (float)sn;
+  const int ngr = nkc * GC;  // group slots of the panel (the last chunk may use fewer)
+  uint8_t* raw = smem + SM_SCR;
+  const uint32_t gbytes = x32 ? 256u : 128u;  // bytes of one (group, sequence) of x in memory
+  // 1. bulk copies: item = (group slot, sequence).  Earlier generic accesses
+  //    to the scratch area (any thread) come before the copies overwrite it.
+  fence_proxy_async_smem();
+  __syncthreads();
+  {
+    uint32_t nbytes = 0;
+    for (int kcl = 0; kcl < nkc; ++kcl) nbytes += (uint32_t)chunk_groups(m, kc_lo + kcl) * gbytes * B;
+    if (tid == 0) mbar_arrive_expect_tx(pbar, nbytes);
+    for (int it = tid; it < ngr * B; it += NTHREADS) {
+      const int gs = it / B, b = it - gs * B, kcl = gs / GC, gi = gs - kcl * GC;
+      if (gi < chunk_groups(m, kc_lo + kcl)) {
+        const int64_t k = (int64_t)(kc_lo + kcl) * GC * DDL_GROUP + (int64_t)gi * DDL_GROUP;
+        const void* src = x32 ? (const void*)(x32 + (int64_t)b * K + k) : (const void*)(x16 + (int64_t)b * K + k);
+        bulk_g2s(smem_addr(raw + (size_t)it * 256), src, gbytes, pbar);
+      }
+    }
   }
-  // pass 1: sum of squares (norm stages, whole vector) and max |x'| per staged chunk
+  if (tid == 0) trace_stamp(P, E.layer * NSTAGE + E.st, NW + 3);
+  // 2. meanwhile: sum of squares over the whole vector (norm stages) and the
+  //    panel's norm weights into L1
+  if (nw) {
+    const int k0 = kc_lo * GC * DDL_GROUP, k1 = min(K, (kc_lo + nkc) * GC * DDL_GROUP);
+    for (int k = k0 + tid * 64; k < k1; k += NTHREADS * 64)
+      asm volatile("prefetch.global.L1 [%0];" ::"l"(nw + k));
+  }
   for (int b = 0; b < B; ++b) {
-    float ss = 0.f, mx0 = 0.f, mx1 = 0.f;
-    const int a0 = nw ? 0 : k_lo, a1 = nw ? K : k_hi;
-    for (int k = a0 + tid; k < a1; k += NTHREADS) {
-      const float x = load(b, k);
-      ss = fmaf(x, x, ss);
-      if (k >= k_lo && k < k_hi) {
-        const float v = fabsf(nw ? x * bf16_bits_to_f32(nw[k]) : x);
-        if (k - k_lo < GC * DDL_GROUP) mx0 = fmaxf(mx0, v);
-        else mx1 = fmaxf(mx1, v);
+    float ss = 0.f;
+    if (nw) {
+      const int nq = K / 4;
+      for (int q0 = tid; q0 < nq; q0 += 8 * NTHREADS) {
+        float4 v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int q = q0 + u * NTHREADS;
+          if (q >= nq) v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+          else if (x32) v[u] = __ldcg(reinterpret_cast<const float4*>(x32 + (int64_t)b * K) + q);
+          else v[u] = bf16x4_f32(__ldcg(reinterpret_cast<const uint2*>(x16 + (int64_t)b * K) + q));
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          ss = fmaf(v[u].x, v[u].x, fmaf(v[u].y, v[u].y, fmaf(v[u].z, v[u].z, fmaf(v[u].w, v[u].w, ss))));
       }
     }
     ss = warp_sum(ss);
-    mx0 = warp_max(mx0);
-    mx1 = warp_max(mx1);
-    if (lane == 0) {
-      M.red[warp][3 * b + 0] = ss;
-      M.red[warp][3 * b + 1] = mx0;
-      M.red[warp][3 * b + 2] = mx1;
+    if (lane == 0) M.red[warp][2 * b] = ss;
+  }
+  if (tid == 0) trace_stamp(P, E.layer * NSTAGE + E.st, NW + 4);
+  const uint32_t parity = M.pphase & 1u;
+  if (!mbar_wait_warp(pbar, parity, P.ctrl + 1)) M.abort = 1;
+  if (tid == 0) trace_stamp(P, E.layer * NSTAGE + E.st, NW + 5);
+  // 3. pass A: x <- x * w in place (fp32), max |x| per sequence.  Lane l of
+  //    the warp owning a group handles columns 2l, 2l+1 of every sequence;
+  //    four groups per step keep their loads in flight together.
+  float mx[MAX_B] = {0.f, 0.f, 0.f, 0.f};
+  for (int gs0 = warp; gs0 < ngr; gs0 += 4 * NW) {
+    float2 w[4], v[4][MAX_B];
+    bool ok[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int gs = gs0 + u * NW, kcl = gs / GC, gi = gs - kcl * GC;
+      ok[u] = gs < ngr && gi < chunk_groups(m, kc_lo + kcl);
+      w[u] = make_float2(1.f, 1.f);
+      if (ok[u] && nw) {
+        const int k = (kc_lo + kcl) * GC * DDL_GROUP + gi * DDL_GROUP + 2 * lane;
+        const uint32_t wb = __ldg(reinterpret_cast<const uint32_t*>(nw + k));
+        w[u] = make_float2(bf16lo_f32(wb), bf16hi_f32(wb));
+      }
+#pragma unroll
+      for (int b = 0; b < MAX_B; ++b) {
+        v[u][b] = make_float2(0.f, 0.f);
+        if (ok[u] && b < B) {
+          const uint8_t* g = raw + ((size_t)gs * B + b) * 256;
+          if (x32) v[u][b] = *reinterpret_cast<const float2*>(g + lane * 8);
+          else {
+            const uint32_t q = *reinterpret_cast<const uint32_t*>(g + lane * 4);
+            v[u][b] = make_float2(bf16lo_f32(q), bf16hi_f32(q));
+          }
+        }
+      }
+    }
+    __syncwarp();
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int gs = gs0 + u * NW;
+#pragma unroll
+      for (int b = 0; b < MAX_B; ++b) {
+        if (ok[u] && b < B) {
+          const float2 x = make_float2(v[u][b].x * w[u].x, v[u][b].y * w[u].y);
+          mx[b] = fmaxf(mx[b], fmaxf(fabsf(x.x), fabsf(x.y)));
+          *reinterpret_cast<float2*>(raw + ((size_t)gs * B + b) * 256 + lane * 8) = x;
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int b = 0; b < MAX_B; ++b) {
+    if (b < B) {
+      const float v = warp_max(mx[b]);
+      if (lane == 0) M.red[warp][2 * b + 1] = v;
     }
   }
   __syncthreads();
   if (tid < B) {
-    float ss = 0.f, mx0 = 0.f, mx1 = 0.f;
+    float ss = 0.f, mxa = 0.f;
     for (int w = 0; w < NW; ++w) {
-      ss += M.red[w][3 * tid + 0];
-      mx0 = fmaxf(mx0, M.red[w][3 * tid + 1]);
-      mx1 = fmaxf(mx1, M.red[w][3 * tid + 2]);
+      ss += M.red[w][2 * tid];
+      mxa = fmaxf(mxa, M.red[w][2 * tid + 1]);
     }
     M.rnorm[tid] = nw ? 1.0f / sqrtf(ss / (float)K + P.eps) : 1.0f;
-    const float mxs[2] = {mx0, mx1};
-    for (int c = 0; c < 2; ++c) {
-      const int e = mxs[c] > 0.f ? ilogbf(mxs[c]) - 11 : 0;
-      M.escale[c][tid] = ldexpf(1.0f, e);
-      M.edown[c][tid] = ldexpf(1.0f, -e);
-    }
+    const int e = mxa > 0.f ? ilogbf(mxa) - 11 : 0;
+    M.escale[tid] = ldexpf(1.0f, e);
+    M.edown[tid] = ldexpf(1.0f, -e);
   }
-  if (tid == 0) {
-    M.kc_lo = kc_lo;
-    M.nkc = nkc;
-  }
+  if (tid == 0) M.pphase++;
   __syncthreads();
-  // pass 2: fragments.  Item = (chunk, group, sequence, j, t); 16 consecutive
-  // threads cover one (chunk, group, sequence).
-  uint2* xf = reinterpret_cast<uint2*>(smem + SM_SCR);
+  if (tid == 0) trace_stamp(P, E.layer * NSTAGE + E.st, NW + 6);
+  // 4. pass B: fragments in place.  Columns 2l, 2l+1 (MMA j = l/8) go to
+  //    lane t = l%4, register half (l%8)/4; Sx = sum of hi + lo per sequence.
+  //    Four groups per step.
   float* Sx = reinterpret_cast<float*>(smem + SM_SCR + XF_BYTES);
-  const int n_items = nkc * GC * B * 16;
-  for (int it0 = 0; it0 < n_items; it0 += NTHREADS) {
-    const int it = it0 + tid;
-    const int jt = it & 15, j = jt >> 2, t = jt & 3;
-    int rest = it >> 4;
-    const int b = rest % B;
-    rest /= B;
-    const int gi = rest % GC, kcl = rest / GC;
-    const bool valid = it < n_items && gi < chunk_groups(m, kc_lo + kcl);
-    double part = 0.0;
-    if (valid) {
-      const int k0 = (kc_lo + kcl) * GC * DDL_GROUP + gi * DDL_GROUP + 16 * j + 2 * t;
-      const int kk[4] = {k0, k0 + 1, k0 + 8, k0 + 9};
-      float hi[4], lo[4];
-      const float sc = M.edown[kcl][b];
-      for (int e = 0; e < 4; ++e) {
-        float x = load(b, kk[e]);
-        if (nw) x *= bf16_bits_to_f32(nw[kk[e]]);
-        x *= sc;
-        if (WT == DDL_W_INT4) {
-          hi[e] = __half2float(__float2half_rn(x));
-          lo[e] = __half2float(__float2half_rn(x - hi[e]));
-        } else {
-          hi[e] = __bfloat162float(__float2bfloat16_rn(x));
-          lo[e] = __bfloat162float(__float2bfloat16_rn(x - hi[e]));
+  const int j = lane >> 3, half = (lane >> 2) & 1, t = lane & 3;
+  for (int gs0 = warp; gs0 < ngr; gs0 += 4 * NW) {
+    float2 v[4][MAX_B];
+    bool ok[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int gs = gs0 + u * NW, kcl = gs / GC, gi = gs - kcl * GC;
+      ok[u] = gs < ngr && gi < chunk_groups(m, kc_lo + kcl);
+#pragma unroll
+      for (int b = 0; b < MAX_B; ++b)
+        v[u][b] = (ok[u] && b < B) ? *reinterpret_cast<const float2*>(raw + ((size_t)gs * B + b) * 256 + lane * 8)
+                                   : make_float2(0.f, 0.f);
+    }
+    __syncwarp();
+    float part[4][MAX_B];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int gs = gs0 + u * NW;
+      uint32_t* f = reinterpret_cast<uint32_t*>(raw + (size_t)gs * B * 256);
+#pragma unroll
+      for (int b = 0; b < MAX_B; ++b) {
+        part[u][b] = 0.f;
+        if (ok[u] && b < B) {
+          const float sc = M.edown[b];
+          const float x0 = v[u][b].x * sc, x1 = v[u][b].y * sc;
+          float h0, h1, l0, l1;
+          uint32_t hw, lw;
+          if (WT == DDL_W_INT4) {
+            h0 = __half2float(__float2half_rn(x0));
+            h1 = __half2float(__float2half_rn(x1));
+            l0 = __half2float(__float2half_rn(x0 - h0));
+            l1 = __half2float(__float2half_rn(x1 - h1));
+            hw = pack_f16x2(h0, h1);
+            lw = pack_f16x2(l0, l1);
+          } else {
+            h0 = __bfloat162float(__float2bfloat16_rn(x0));
+            h1 = __bfloat162float(__float2bfloat16_rn(x1));
+            l0 = __bfloat162float(__float2bfloat16_rn(x0 - h0));
+            l1 = __bfloat162float(__float2bfloat16_rn(x1 - h1));
+            hw = pack_bf16x2(h0, h1);
+            lw = pack_bf16x2(l0, l1);
+          }
+          f[((j * 2 * B + 2 * b) * 4 + t) * 2 + half] = hw;
+          f[((j * 2 * B + 2 * b + 1) * 4 + t) * 2 + half] = lw;
+          part[u][b] = (h0 + l0) + (h1 + l1);
         }
-        part += (double)hi[e] + (double)lo[e];
-      }
-      const int base = (((kcl * GC + gi) * 4 + j) * B2) * 4 + t;
-      if (WT == DDL_W_INT4) {
-        xf[base + (2 * b) * 4] = make_uint2(pack_f16x2(hi[0], hi[1]), pack_f16x2(hi[2], hi[3]));
-        xf[base + (2 * b + 1) * 4] = make_uint2(pack_f16x2(lo[0], lo[1]), pack_f16x2(lo[2], lo[3]));
-      } else {
-        xf[base + (2 * b) * 4] = make_uint2(pack_bf16x2(hi[0], hi[1]), pack_bf16x2(hi[2], hi[3]));
-        xf[base + (2 * b + 1) * 4] =
-            make_uint2(pack_bf16x2(lo[0], lo[1]), pack_bf16x2(lo[2], lo[3]));
       }
     }
-    for (int o = 8; o; o >>= 1) part += __shfl_xor_sync(FULL, part, o);
-    if (valid && jt == 0) Sx[(kcl * GC + gi) * MAX_B + b] = (float)part;
+#pragma unroll
+    for (int o = 16; o; o >>= 1)
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+#pragma unroll
+        for (int b = 0; b < MAX_B; ++b) part[u][b] += __shfl_xor_sync(FULL, part[u][b], o);
+    if (lane == 0) {
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int gs = gs0 + u * NW;
+#pragma unroll
+        for (int b = 0; b < MAX_B; ++b)
+          if (ok[u] && b < B) Sx[gs * MAX_B + b] = part[u][b];
+      }
+    }
   }
   __syncthreads();
 }
@@ -325,19 +462,17 @@ __device__ void gemv_prologue(const Params& P, int layer, int st, const MatGeom&
 // ------------------------------------------------------------------ GEMV epilogues
 // Lane (g, t) holds rows g and g+8 of tile T for sequence t.
 template <int HD>
-__device__ void gemv_epilogue(const Params& P, int layer, int st, int T, float v0, float v1,
+__device__ void gemv_epilogue(const Params& P, const GemvCtx& E, int T, float v0, float v1,
                               const Misc& M) {
   const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
   if (t >= P.B) return;
-  const int gl = P.l0 + layer;
-  const LayerDev& Ld = P.layers[layer];
-  if (st == ST_QKV) {
+  if (E.st == ST_QKV) {
     const float r = M.rnorm[t];
     v0 *= r;
     v1 *= r;
     const int tph = HD / 16, head = T / tph, i = 8 * (T % tph) + g;
     if (head < P.Hq + P.Hkv) {  // RoPE on q and k: pair (i, i + hd/2)
-      const float c = M.rope[i][0], s = M.rope[i][1], a = v0, b = v1;
+      const float c = P.rope[i][0], s = P.rope[i][1], a = v0, b = v1;
       v0 = a * c - b * s;
       v1 = a * s + b * c;
     }
@@ -348,204 +483,442 @@ __device__ void gemv_epilogue(const Params& P, int layer, int st, int T, float v
     } else {
       const bool is_k = head < P.Hq + P.Hkv;
       const int kvh = is_k ? head - P.Hq : head - P.Hq - P.Hkv;
-      uint16_t* row = (is_k ? Ld.kc : Ld.vc) + (((int64_t)t * P.Hkv + kvh) * P.s_max + P.pos) * HD;
+      uint16_t* row = (is_k ? E.kc : E.vc) + (((int64_t)t * P.Hkv + kvh) * P.s_max + P.pos) * HD;
       row[i] = f32_to_bf16_bits(v0);
       row[i + HD / 2] = f32_to_bf16_bits(v1);
     }
-  } else if (st == ST_WO) {
+  } else if (E.st == ST_WO) {
     const int r0 = 16 * T + g, r1 = r0 + 8;
-    float* y = P.y + (int64_t)t * P.D;
-    y[r0] = layer_input(P, gl, t, r0) + v0;
-    y[r1] = layer_input(P, gl, t, r1) + v1;
-  } else if (st == ST_GU) {
+    const int64_t o = (int64_t)t * P.D;
+    const float x0 = E.xin32 ? __ldcg(E.xin32 + o + r0) : bf16_bits_to_f32(E.xin16[o + r0]);
+    const float x1 = E.xin32 ? __ldcg(E.xin32 + o + r1) : bf16_bits_to_f32(E.xin16[o + r1]);
+    P.y[o + r0] = x0 + v0;
+    P.y[o + r1] = x1 + v1;
+  } else if (E.st == ST_GU) {
     const float r = M.rnorm[t], gt = v0 * r, up = v1 * r;
     P.a[(int64_t)t * P.dff + 8 * T + g] = gt / (1.0f + expf(-gt)) * up;
   } else {
     const int r0 = 16 * T + g, r1 = r0 + 8;
-    const float* y = P.y + (int64_t)t * P.D;
-    const float z0 = __ldcg(y + r0) + v0, z1 = __ldcg(y + r1) + v1;
-    float* Z = P.Z + (int64_t)(gl & 1) * P.B * P.D + (int64_t)t * P.D;
-    Z[r0] = z0;
-    Z[r1] = z1;
-    if (P.final_last && layer == P.L - 1) {
+    const int64_t o = (int64_t)t * P.D;
+    const float z0 = __ldcg(P.y + o + r0) + v0, z1 = __ldcg(P.y + o + r1) + v1;
+    E.zout[o + r0] = z0;
+    E.zout[o + r1] = z1;
+    if (E.final_layer) {
       if (P.resid_out) {
-        P.resid_out[(int64_t)t * P.D + r0] = z0;
-        P.resid_out[(int64_t)t * P.D + r1] = z1;
+        P.resid_out[o + r0] = z0;
+        P.resid_out[o + r1] = z1;
       }
       if (P.out_bf16) {
-        P.out_bf16[(int64_t)t * P.D + r0] = f32_to_bf16_bits(z0);
-        P.out_bf16[(int64_t)t * P.D + r1] = f32_to_bf16_bits(z1);
+        P.out_bf16[o + r0] = f32_to_bf16_bits(z0);
+        P.out_bf16[o + r1] = f32_to_bf16_bits(z1);
       }
     }
   }
 }
 
-// Finish this warp's share of unit (kc, T): epilogue directly when the warp
-// covered the whole tile, else publish the partial; the last contributor to
-// the tile sums all partials in (k-chunk, warp) order and runs the epilogue.
+// Sum the partials of tile T in slot order (panel, then warp; 8 loads in
+// flight) and run its epilogue.
 template <int HD>
-__device__ void gemv_finish(const Params& P, int layer, int st, const MatGeom& m, int kc, int T,
-                            float acc0, float acc1, int64_t wg, int64_t W, const Misc& M) {
-  const int lane = threadIdx.x & 31, t = lane & 3;
-  const float sc = t < P.B ? M.escale[kc - M.kc_lo][t] : 0.f;
-  const float v0 = acc0 * sc, v1 = acc1 * sc;
-  const int64_t us = unit_start(m, kc, T), ue = us + chunk_groups(m, kc) - 1;
-  const int64_t wf = owner_of(m.T, W, us), wl = owner_of(m.T, W, ue);
-  if (m.Sk == 1 && wf == wl) {
-    gemv_epilogue<HD>(P, layer, st, T, v0, v1, M);
-    return;
-  }
-  const int64_t u = (int64_t)kc * m.NT + T;
-  float2* part = reinterpret_cast<float2*>(P.gpart);
-  part[(u * m.J + (wg - wf)) * 32 + lane] = make_float2(v0, v1);
-  // contributors = warps with a non-empty range that own blocks of the tile
-  // (with fewer blocks than warps, a warp owns at most one block)
-  int ncontrib = 0;
-  for (int k = 0; k < m.Sk; ++k) {
-    const int64_t s0 = unit_start(m, k, T), e0 = s0 + chunk_groups(m, k) - 1;
-    ncontrib += (int)(m.T >= W ? owner_of(m.T, W, e0) - owner_of(m.T, W, s0) + 1 : e0 - s0 + 1);
-  }
-  __syncwarp();
-  uint32_t old = 0;
-  if (lane == 0) {
-    __threadfence();
-    old = atomicAdd(P.cnt + T, 1u);
-  }
-  old = __shfl_sync(FULL, old, 0);
-  if ((int)old != ncontrib - 1) return;
-  __threadfence();
+__device__ __noinline__ void gemv_fixup(const Params& P, const GemvCtx& E, int T, const Misc& M) {
+  const MatGeom& m = E.m;
+  const int lane = threadIdx.x & 31, nslot = m.NP * m.J;
+  const float2* part = reinterpret_cast<const float2*>(P.gpart) + (int64_t)T * nslot * 32 + lane;
   float s0 = 0.f, s1 = 0.f;
-  for (int k = 0; k < m.Sk; ++k) {
-    const int64_t uk = (int64_t)k * m.NT + T;
-    const int64_t a0 = unit_start(m, k, T), e0 = a0 + chunk_groups(m, k) - 1;
-    const int64_t f0 = owner_of(m.T, W, a0), n0 = owner_of(m.T, W, e0) - f0 + 1;
-    for (int64_t j = 0; j < n0; ++j) {
-      if (range_lo(m.T, W, f0 + j) == range_lo(m.T, W, f0 + j + 1)) continue;  // empty range
-      const float2 v = __ldcg(part + (uk * m.J + j) * 32 + lane);
-      s0 += v.x;
-      s1 += v.y;
+  for (int f0 = 0; f0 < nslot; f0 += 8) {
+    float2 v[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int f = f0 + u, p = f / m.J, j = f - p * m.J;
+      bool ok = f < nslot;
+      if (ok) {
+        const uint32_t Gp = panel_groups(m, p);
+        const uint32_t v0 = work_owner(m, p, (uint32_t)T * Gp, NW);
+        const uint32_t v1 = work_owner(m, p, (uint32_t)(T + 1) * Gp - 1, NW);
+        ok = v0 + j <= v1 && !warp_empty(m, p, v0 + j, NW);
+      }
+      v[u] = ok ? __ldcg(part + (int64_t)f * 32) : make_float2(0.f, 0.f);
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      s0 += v[u].x;
+      s1 += v[u].y;
     }
   }
-  gemv_epilogue<HD>(P, layer, st, T, s0, s1, M);
+  gemv_epilogue<HD>(P, E, T, s0, s1, M);
   if (lane == 0) P.cnt[T] = 0;
 }
 
+// Publish the partials this warp wrote: one fence, then per queued tile (on
+// its own lane) add the warp's block count to the tile's counter; the warp
+// that brings a counter to G finishes that tile.
+template <int HD>
+__device__ __noinline__ void gemv_publish(const Params& P, const GemvCtx& E, const uint32_t* pend,
+                                          int npend, const Misc& M) {
+  const int lane = threadIdx.x & 31;
+  __syncwarp();
+  __threadfence();
+  uint32_t last = 0;
+  if (lane < npend) {
+    const uint32_t T = pend[lane] & 0xFFFFFu, nblk = pend[lane] >> 20;
+    last = atomicAdd(P.cnt + T, nblk) + nblk == (uint32_t)E.m.G;
+  }
+  uint32_t mask = __ballot_sync(FULL, last);
+  if (mask) __threadfence();
+  while (mask) {
+    const int l = __ffs(mask) - 1;
+    mask &= mask - 1;
+    gemv_fixup<HD>(P, E, (int)(pend[l] & 0xFFFFFu), M);
+  }
+}
+
+// Finish this warp's share of tile T (nblk of its blocks, sums v0, v1 in true
+// scale): a warp that covered the whole tile runs the epilogue directly;
+// otherwise the partial goes to slot (T, panel, warp - first warp of the tile
+// in the panel) and the tile is queued for publication.
+template <int HD>
+__device__ __forceinline__ void tile_finish(const Params& P, const GemvCtx& E, const Misc& M, int T,
+                                            uint32_t nblk, float v0, float v1, uint32_t* pend,
+                                            int& npend) {
+  const MatGeom& m = E.m;
+  const int lane = threadIdx.x & 31;
+  if (nblk == (uint32_t)m.G) {
+    gemv_epilogue<HD>(P, E, T, v0, v1, M);
+    return;
+  }
+  const uint32_t me = (uint32_t)E.cl * NW + (threadIdx.x >> 5);
+  const uint32_t first = work_owner(m, E.p, (uint32_t)T * panel_groups(m, E.p), NW);
+  const int64_t slot = ((int64_t)T * m.NP + E.p) * m.J + (me - first);
+  reinterpret_cast<float2*>(P.gpart)[slot * 32 + lane] = make_float2(v0, v1);
+  if (lane == 0) pend[npend] = (uint32_t)T | (nblk << 20);
+  if (++npend == 32) {
+    gemv_publish<HD>(P, E, pend, npend, M);
+    npend = 0;
+  }
+}
+
 // ------------------------------------------------------------------ GEMV stage
+// The warp walks its range of the panel's work order (tile, k-chunk, group).
+// Per ring slot (up to 8 groups of one (k-chunk, tile) unit): the 8 blocks'
+// MMAs run as 8 independent chains, then fold into the unit sums; a unit's
+// sums join the tile sums in true scale, and a tile is finished when the
+// warp leaves it.
 template <int HD, int WT>
-__device__ bool stage_gemv(const Params& P, int layer, int st, Ring& R, Cursor& prod, int64_t wg,
-                           int64_t W, uint8_t* smem, Misc& M, uint64_t policy) {
-  const MatGeom& m = P.mg[stage_mat(st)];
-  gemv_prologue<HD, WT>(P, layer, st, m, W, smem, M);
-  const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
-  const int B = P.B, B2 = 2 * B;
-  const int64_t lo = range_lo(m.T, W, wg), hi = range_lo(m.T, W, wg + 1);
-  if (lo >= hi) return true;
-  const uint32_t xf_base = smem_addr(smem + SM_SCR);
-  const float* Sx = reinterpret_cast<const float*>(smem + SM_SCR + XF_BYTES);
-  const int kc_lo = M.kc_lo;
+__device__ __forceinline__ bool stage_gemv_body(const Params& P, int layer, int st, Ring& R,
+                                                Cursor& prod, int64_t wg, int64_t W, uint8_t* smem,
+                                                Misc& M, uint64_t policy);
+// The ring and the cursor live in registers while the stage runs.
+template <int HD, int WT>
+__device__ __noinline__ bool stage_gemv(const Params& P, int layer, int st, Ring& Rm, Cursor& prodm,
+                                        int64_t wg, int64_t W, uint8_t* smem, Misc& M,
+                                        uint64_t policy) {
+  Ring R = Rm;
+  Cursor prod = prodm;
+  const bool ok = stage_gemv_body<HD, WT>(P, layer, st, R, prod, wg, W, smem, M, policy);
+  Rm = R;
+  prodm = prod;
+  return ok;
+}
+template <int HD, int WT>
+__device__ __forceinline__ bool stage_gemv_body(const Params& P, int layer, int st, Ring& R,
+                                                Cursor& prod, int64_t wg, int64_t W, uint8_t* smem,
+                                                Misc& M, uint64_t policy) {
+  GemvCtx E;
+  E.m = P.mg[stage_mat(st)];
+  E.st = st;
+  E.layer = layer;
+  E.gl = P.l0 + layer;
+  E.p = panel_of_cta(E.m, blockIdx.x);
+  E.cl = blockIdx.x - E.m.pc[E.p];
+  {
+    const LayerDev& Ld = P.layers[layer];
+    E.kc = Ld.kc;
+    E.vc = Ld.vc;
+    E.xin32 = nullptr;
+    E.xin16 = nullptr;
+    if (E.gl == 0) {
+      if (P.resid_in) E.xin32 = P.resid_in;
+      else E.xin16 = P.x_bf16;
+    } else {
+      E.xin32 = P.Z + (int64_t)((E.gl - 1) & 1) * P.B * P.D;
+    }
+    E.zout = P.Z + (int64_t)(E.gl & 1) * P.B * P.D;
+    E.final_layer = P.final_last && layer == P.L - 1;
+  }
+  const MatGeom& m = E.m;
+  gemv_prologue<HD, WT>(P, E, smem, M, smem_addr(smem + SM_PBAR));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+  if (threadIdx.x == 0) trace_stamp(P, layer * NSTAGE + st, 1);
+  uint32_t lo, hi;
+  warp_work(m, E.p, E.cl, warp, NW, lo, hi);
+  if (lo >= hi) {
+    if (lane == 0) trace_stamp(P, layer * NSTAGE + st, 2 + warp);
+    return true;
+  }
+  uint32_t* pend = reinterpret_cast<uint32_t*>(smem + SM_SCR + XF_BYTES + SX_BYTES) + warp * 32;
+  int npend = 0;
+  const int B = P.B, B2 = 2 * B, Sk = m.Sk, pk0 = m.pk[E.p], pk1 = m.pk[E.p + 1];
+  const uint32_t jstride = B2 * 32, gstride = 4 * jstride, kstride = GC * gstride;
+  const uint32_t xf_lane = smem_addr(smem + SM_SCR) + (g * 4 + t) * 8;
+  const uint32_t sx_lane = smem_addr(smem + SM_SCR + XF_BYTES) + t * 4;
+  const float esc = M.escale[t < B ? t : 0];
   int kc, T, gi;
-  block_coord(m, lo, kc, T, gi);
+  work_coord(m, E.p, lo, T, kc, gi);
   int gk = chunk_groups(m, kc);
-  float acc0 = 0.f, acc1 = 0.f;
-  float cb[4] = {0.f, 0.f, 0.f, 0.f};  // bf16 path: fragment accumulators
-  const int per = WT == DDL_W_INT4 ? BLKS_PER_SLOT : BF16_BLKS_PER_SLOT;
-  for (int64_t b = lo; b < hi; b += per) {
-    const int nb = (int)(hi - b < per ? hi - b : per);
+  float acc0 = 0.f, acc1 = 0.f, tac0 = 0.f, tac1 = 0.f;
+  uint32_t nblk = 0;
+  constexpr int PER = WT == DDL_W_INT4 ? BLKS_PER_SLOT : BF16_BLKS_PER_SLOT;
+  const uint32_t jst1 = jstride, jst2 = 2 * jstride, jst3 = 3 * jstride;
+  for (uint32_t b = lo; b < hi;) {
+    // a slot holds nb consecutive groups gi.. of unit (kc, T) (see cursor_next)
+    int nb = (int)(hi - b < (uint32_t)PER ? hi - b : (uint32_t)PER);
+    if (nb > gk - gi) nb = gk - gi;
     const uint32_t slot = R.slot(R.n_done);
     if (!mbar_wait_warp(R.bar(R.n_done), R.parity(R.n_done), P.ctrl + 1)) {
       M.abort = 1;
       return false;
     }
-    for (int i = 0; i < nb; ++i) {
-      const int kcl = kc - kc_lo;
-      const uint32_t xfa = xf_base + (uint32_t)(((((kcl * GC + gi) * 4) * B2 + g) * 4 + t) * 8);
-      if (WT == DDL_W_INT4) {
-        const uint4 wv = lds128(slot + i * BLK_BYTES + lane * 16);
-        const uint32_t sc = lds32(slot + BLKS_PER_SLOT * BLK_BYTES + i * SCL_BYTES + g * 4);
-        float c[4] = {0.f, 0.f, 0.f, 0.f};
-        const uint32_t ws[4] = {wv.x, wv.y, wv.z, wv.w};
+    const int kcl = kc - pk0;
+    const uint32_t xb = xf_lane + kcl * kstride + gi * gstride;
+    const uint32_t sb = sx_lane + ((kcl * GC + gi) * MAX_B) * 4;
+    float c[PER][4];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const uint32_t w = ws[j], w8 = w >> 8;
-          const uint32_t a0 = lop3_merge(w, 0x000F000Fu, 0x64086408u);
-          const uint32_t a1 = lop3_merge(w, 0x00F000F0u, 0x64806480u);
-          const uint32_t a2 = lop3_merge(w8, 0x000F000Fu, 0x64086408u);
-          const uint32_t a3 = lop3_merge(w8, 0x00F000F0u, 0x64806480u);
-          uint2 bf = make_uint2(0u, 0u);
-          if (g < B2) bf = lds64(xfa + j * B2 * 32);
-          mma_f16(c, a0, a1, a2, a3, bf.x, bf.y);
-        }
-        // rows g hold 1024 + (q+8), rows g+8 hold 1024 + 16 (q+8):
-        // sum q x = v - 1032 Sx  and  (v - 1152 Sx) / 16
-        const float sx = t < B ? Sx[(kcl * GC + gi) * MAX_B + t] : 0.f;
-        acc0 = fmaf(bf16lo_f32(sc), (c[0] + c[1]) - 1032.f * sx, acc0);
-        acc1 = fmaf(bf16hi_f32(sc) * 0.0625f, (c[2] + c[3]) - 1152.f * sx, acc1);
-      } else {
+    for (int i = 0; i < PER; ++i) {
+      c[i][0] = c[i][1] = c[i][2] = c[i][3] = 0.f;
+      if (nb == PER || i < nb) {
+        const uint32_t xi = xb + i * gstride;
+        const uint32_t jo[4] = {0u, jst1, jst2, jst3};
+        if (WT == DDL_W_INT4) {
+          const uint4 wv = lds128(slot + i * BLK_BYTES + lane * 16);
+          const uint32_t ws[4] = {wv.x, wv.y, wv.z, wv.w};
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const uint4 av = lds128(slot + i * BF16_BLK_BYTES + j * 512 + lane * 16);
-          uint2 bf = make_uint2(0u, 0u);
-          if (g < B2) bf = lds64(xfa + j * B2 * 32);
-          mma_bf16(cb, av.x, av.y, av.z, av.w, bf.x, bf.y);
-        }
-      }
-      if (++gi == gk) {
-        if (WT != DDL_W_INT4) {
-          acc0 = cb[0] + cb[1];
-          acc1 = cb[2] + cb[3];
-          cb[0] = cb[1] = cb[2] = cb[3] = 0.f;
-        }
-        gemv_finish<HD>(P, layer, st, m, kc, T, acc0, acc1, wg, W, M);
-        acc0 = acc1 = 0.f;
-        gi = 0;
-        if (++T == m.NT) {
-          T = 0;
-          ++kc;
-          gk = kc < m.Sk ? chunk_groups(m, kc) : 0;
+          for (int j = 0; j < 4; ++j) {
+            const uint32_t w = ws[j], w8 = w >> 8;
+            const uint32_t a0 = lop3_merge(w, 0x000F000Fu, 0x64086408u);
+            const uint32_t a1 = lop3_merge(w, 0x00F000F0u, 0x64806480u);
+            const uint32_t a2 = lop3_merge(w8, 0x000F000Fu, 0x64086408u);
+            const uint32_t a3 = lop3_merge(w8, 0x00F000F0u, 0x64806480u);
+            // lanes g >= 2B read unrelated fragments: they only feed C columns >= 2B, never used
+            const uint2 bf = lds64(xi + jo[j]);
+            mma_f16(c[i], a0, a1, a2, a3, bf.x, bf.y);
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const uint4 av = lds128(slot + i * BF16_BLK_BYTES + j * 512 + lane * 16);
+            const uint2 bf = lds64(xi + jo[j]);
+            mma_bf16(c[i], av.x, av.y, av.z, av.w, bf.x, bf.y);
+          }
         }
       }
     }
-    ring_advance<HD>(P, R, prod, wg, W, lane, policy);
-  }
-  if (gi != 0) {
-    if (WT != DDL_W_INT4) {
-      acc0 = cb[0] + cb[1];
-      acc1 = cb[2] + cb[3];
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+      if (nb == PER || i < nb) {
+        if (WT == DDL_W_INT4) {
+          // rows g hold 1024 + (q+8), rows g+8 hold 1024 + 16 (q+8):
+          // sum q x = v - 1032 Sx  and  (v - 1152 Sx) / 16
+          const uint32_t sc = lds32(slot + BLKS_PER_SLOT * BLK_BYTES + i * SCL_BYTES + g * 4);
+          const float sx = lds_f32(sb + i * (MAX_B * 4));
+          acc0 = fmaf(bf16lo_f32(sc), (c[i][0] + c[i][1]) - 1032.f * sx, acc0);
+          acc1 = fmaf(bf16hi_f32(sc) * 0.0625f, (c[i][2] + c[i][3]) - 1152.f * sx, acc1);
+        } else {
+          acc0 += c[i][0] + c[i][1];
+          acc1 += c[i][2] + c[i][3];
+        }
+      }
     }
-    gemv_finish<HD>(P, layer, st, m, kc, T, acc0, acc1, wg, W, M);
+    b += nb;
+    gi += nb;
+    nblk += nb;
+    if (gi == gk) {  // end of the unit: its sums join the tile's
+      tac0 = fmaf(acc0, esc, tac0);
+      tac1 = fmaf(acc1, esc, tac1);
+      acc0 = acc1 = 0.f;
+      gi = 0;
+      if (++kc == pk1) {  // end of the tile in this panel
+        tile_finish<HD>(P, E, M, T, nblk, tac0, tac1, pend, npend);
+        tac0 = tac1 = 0.f;
+        nblk = 0;
+        kc = pk0;
+        ++T;
+      }
+      gk = kc < Sk ? chunk_groups(m, kc) : 1;
+    }
+    ring_advance<HD, WT>(P, R, prod, wg, W, lane, policy);
   }
+  if (nblk != 0)
+    tile_finish<HD>(P, E, M, T, nblk, fmaf(acc0, esc, tac0), fmaf(acc1, esc, tac1), pend, npend);
+  if (npend) gemv_publish<HD>(P, E, pend, npend, M);
+  if (lane == 0) trace_stamp(P, layer * NSTAGE + st, 2 + warp);
   return true;
 }
 
 // ------------------------------------------------------------------ attention
-// Merge n softmax states (m, l, o) into `out` (fp32 records of GH*(hd+2)).
+// Merge n <= NW+1 softmax states (m, l, o) into `out` (fp32 records of
+// GH*(hd+2)): per head the rescale factors exp2(m_k - max m) are computed once.
 template <int HD>
 __device__ void merge_records(const float* const* recs, int n, float* out, int GH) {
   const int lane = threadIdx.x & 31;
-  for (int h = lane; h < GH; h += 32) {
-    float mx = -INFINITY;
-    for (int k = 0; k < n; ++k) mx = fmaxf(mx, recs[k][GH * HD + h]);
-    float l = 0.f;
-    for (int k = 0; k < n; ++k) l += exp2f(recs[k][GH * HD + h] - mx) * recs[k][GH * HD + GH + h];
-    out[GH * HD + h] = mx;
-    out[GH * HD + GH + h] = l;
+  float f[NW + 1][MAX_GH];
+  float mxh[MAX_GH];
+#pragma unroll
+  for (int h = 0; h < MAX_GH; ++h) {
+    mxh[h] = -INFINITY;
+    if (h < GH)
+      for (int k = 0; k < n; ++k) mxh[h] = fmaxf(mxh[h], recs[k][GH * HD + h]);
   }
-  for (int e = lane; e < GH * HD; e += 32) {
-    const int h = e / HD;
-    float mx = -INFINITY;
-    for (int k = 0; k < n; ++k) mx = fmaxf(mx, recs[k][GH * HD + h]);
-    float o = 0.f;
-    for (int k = 0; k < n; ++k) o += exp2f(recs[k][GH * HD + h] - mx) * recs[k][e];
-    out[e] = o;
+#pragma unroll
+  for (int k = 0; k < NW + 1; ++k)
+#pragma unroll
+    for (int h = 0; h < MAX_GH; ++h)
+      f[k][h] = (k < n && h < GH) ? exp2f(recs[k][GH * HD + h] - mxh[h]) : 0.f;
+  if (lane < GH) {
+    float l = 0.f;
+#pragma unroll
+    for (int k = 0; k < NW + 1; ++k)
+      if (k < n) l += f[k][lane] * recs[k][GH * HD + GH + lane];
+    out[GH * HD + lane] = mxh[lane];
+    out[GH * HD + GH + lane] = l;
+  }
+#pragma unroll
+  for (int h = 0; h < MAX_GH; ++h) {
+    if (h >= GH) break;
+    for (int d = lane; d < HD; d += 32) {
+      float o = 0.f;
+#pragma unroll
+      for (int k = 0; k < NW + 1; ++k)
+        if (k < n) o += f[k][h] * recs[k][h * HD + d];
+      out[h * HD + d] = o;
+    }
   }
 }
 
+// Final merge of all CTA records of one sequence into attn, by the last CTA
+// to finish it.  Phase 1: warp h < GH folds every record's (m, l) of head h
+// into per-record factors exp2(m_j - M) / L (one record per lane per step).
+// Phase 2: thread (h, d-quad) sums factor * o over the records, 16 loads in
+// flight.
 template <int HD>
-__device__ bool stage_att(const Params& P, int layer, Ring& R, Cursor& prod, int64_t wg, int64_t W,
-                          uint8_t* smem, Misc& M, uint64_t policy) {
+__device__ void merge_sequence(const Params& P, int64_t seq, int64_t Ta, int64_t C, float* fac) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int GH = P.GH, REC = att_rec_floats(GH, HD), nt = P.nt_att;
+  const int64_t cf = owner_of(Ta, C, seq * nt), cl = owner_of(Ta, C, seq * nt + nt - 1);
+  const int n = (int)(cl - cf + 1);
+  const float* base = P.apart + seq * P.J_att * REC;
+  if (warp < GH) {
+    float mx = -INFINITY;
+    for (int j = lane; j < n; j += 32) {
+      const bool ok = range_lo(Ta, C, cf + j) != range_lo(Ta, C, cf + j + 1);
+      if (ok) mx = fmaxf(mx, __ldcg(base + (int64_t)j * REC + GH * HD + warp));
+    }
+    mx = warp_max(mx);
+    float l = 0.f;
+    for (int j = lane; j < n; j += 32) {
+      const bool ok = range_lo(Ta, C, cf + j) != range_lo(Ta, C, cf + j + 1);
+      float fj = 0.f;
+      if (ok) {
+        const float* rec = base + (int64_t)j * REC;
+        fj = exp2f(__ldcg(rec + GH * HD + warp) - mx);
+        l += fj * __ldcg(rec + GH * HD + GH + warp);
+      }
+      fac[warp * P.J_att + j] = fj;
+    }
+    l = warp_sum(l);
+    for (int j = lane; j < n; j += 32) fac[warp * P.J_att + j] /= l;
+  }
+  __syncthreads();
+  constexpr int DQ = HD / 4;  // float4 columns of a head
+  const int64_t b = seq / P.Hkv, kvh = seq % P.Hkv;
+  for (int e = threadIdx.x; e < GH * DQ; e += NTHREADS) {
+    const int h = e / DQ, dq = e - h * DQ;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int j0 = 0; j0 < n; j0 += 16) {
+      float4 v[16];
+#pragma unroll
+      for (int u = 0; u < 16; ++u)
+        v[u] = j0 + u < n ? __ldcg(reinterpret_cast<const float4*>(base + (int64_t)(j0 + u) * REC + h * HD) + dq)
+                          : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int u = 0; u < 16; ++u) {
+        const float fj = j0 + u < n ? fac[h * P.J_att + j0 + u] : 0.f;
+        acc.x = fmaf(fj, v[u].x, acc.x);
+        acc.y = fmaf(fj, v[u].y, acc.y);
+        acc.z = fmaf(fj, v[u].z, acc.z);
+        acc.w = fmaf(fj, v[u].w, acc.w);
+      }
+    }
+    float* dst = P.attn + b * P.Hq * HD + (kvh * GH + h) * HD;
+    reinterpret_cast<float4*>(dst)[dq] = acc;
+  }
+  __syncthreads();
+}
+
+// Write one warp's softmax state (m, l, o) for its current sequence segment:
+// to the CTA's record slot 0 (first segment) or 1 (last), or, for a segment
+// wholly inside the warp, straight to the sequence's partial of this CTA.
+template <int HD>
+__device__ __forceinline__ void att_flush(const Params& P, float* rec, const float (&o)[HD / 8][4],
+                                          float mrun, float lrun) {
+  const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3, GH = P.GH;
+  float ls = lrun + __shfl_xor_sync(FULL, lrun, 1);
+  ls += __shfl_xor_sync(FULL, ls, 2);
+  if (g < GH) {
+#pragma unroll
+    for (int nb = 0; nb < HD / 8; ++nb) {
+      rec[g * HD + 8 * nb + 2 * t] = o[nb][0] + o[nb][2];
+      rec[g * HD + 8 * nb + 2 * t + 1] = o[nb][1] + o[nb][3];
+    }
+    if (t == 0) {
+      rec[GH * HD + g] = mrun;
+      rec[GH * HD + GH + g] = ls;
+    }
+  }
+}
+
+// Merge the run of CTA records of sequence `seq` that starts at this warp's
+// record slot rec_idx (continuing into later warps when the run does) into
+// the sequence's partial of this CTA.
+template <int HD>
+__device__ void att_chain(const Params& P, const Misc& M, const float* recs, int64_t seq,
+                          int rec_idx, bool continues, int64_t Ta, int64_t C) {
+  const int warp = threadIdx.x >> 5, GH = P.GH, REC = att_rec_floats(GH, HD), nt = P.nt_att;
+  const float* list[NW + 1];
+  int n = 0;
+  list[n++] = recs + (warp * 2 + rec_idx) * REC;
+  if (continues) {
+    for (int v = warp + 1; v < NW; ++v) {
+      if (M.seg_n[v] == 0) continue;
+      if (M.seg_first[v] != seq) break;
+      list[n++] = recs + (v * 2 + 0) * REC;
+      if (M.seg_n[v] > 1) break;
+    }
+  }
+  float* out = P.apart + (seq * P.J_att + (blockIdx.x - owner_of(Ta, C, seq * nt))) * REC;
+  merge_records<HD>(list, n, out, GH);
+}
+
+template <int HD, int WT>
+__device__ __forceinline__ bool stage_att_body(const Params& P, int layer, Ring& R, Cursor& prod,
+                                               int64_t wg, int64_t W, uint8_t* smem, Misc& M,
+                                               uint64_t policy);
+template <int HD, int WT>
+__device__ __noinline__ bool stage_att(const Params& P, int layer, Ring& Rm, Cursor& prodm,
+                                       int64_t wg, int64_t W, uint8_t* smem, Misc& M,
+                                       uint64_t policy) {
+  Ring R = Rm;
+  Cursor prod = prodm;
+  const bool ok = stage_att_body<HD, WT>(P, layer, R, prod, wg, W, smem, M, policy);
+  Rm = R;
+  prodm = prod;
+  return ok;
+}
+template <int HD, int WT>
+__device__ __forceinline__ bool stage_att_body(const Params& P, int layer, Ring& R, Cursor& prod,
+                                               int64_t wg, int64_t W, uint8_t* smem, Misc& M,
+                                               uint64_t policy) {
   constexpr int ROWB = HD * 2 + 16, KS = HD / 16, NB = HD / 8;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
-  const int GH = P.GH, REC = GH * (HD + 2), nt = P.nt_att;
+  const int GH = P.GH, REC = att_rec_floats(GH, HD), nt = P.nt_att;
   const int64_t Ta = (int64_t)P.B * P.Hkv * nt, C = gridDim.x;
   const LayerDev& Ld = P.layers[layer];
   float* recs = reinterpret_cast<float*>(smem + SM_SCR);
@@ -554,36 +927,19 @@ __device__ bool stage_att(const Params& P, int layer, Ring& R, Cursor& prod, int
   const float qscale = 1.4426950408889634f / sqrtf((float)HD);  // log2(e) / sqrt(hd)
   int nseg = 0;
   int64_t first_seq = -1, cur = -1;
-  uint32_t qh[KS][2], ql[KS][2];
+  uint32_t qa[KS][4];
   float mrun = -INFINITY, lrun = 0.f;
   float o[NB][4];
   bool ok = true;
 
-  auto flush = [&](bool at_end) {
-    float ls = lrun + __shfl_xor_sync(FULL, lrun, 1);
-    ls += __shfl_xor_sync(FULL, ls, 2);
-    float* rec;
-    if (nseg == 1) rec = recs + (warp * 2 + 0) * REC;
-    else if (at_end) rec = recs + (warp * 2 + 1) * REC;
-    else rec = P.apart + (cur * P.J_att + (blockIdx.x - owner_of(Ta, C, cur * nt))) * REC;
-    if (g < GH) {
-#pragma unroll
-      for (int nb = 0; nb < NB; ++nb) {
-        rec[g * HD + 8 * nb + 2 * t] = o[nb][0];
-        rec[g * HD + 8 * nb + 2 * t + 1] = o[nb][1];
-      }
-      if (t == 0) {
-        rec[GH * HD + g] = mrun;
-        rec[GH * HD + GH + g] = ls;
-      }
-    }
-  };
-
   for (int64_t it = lo; it < hi && ok; ++it) {
-    const int64_t seq = it / nt;
-    const int i = (int)(it % nt);
+    const int64_t seq = (uint32_t)it / (uint32_t)nt;
+    const int i = (int)((uint32_t)it - (uint32_t)seq * (uint32_t)nt);
     if (seq != cur) {
-      if (cur >= 0) flush(false);
+      if (cur >= 0)  // a segment wholly inside this warp (or the warp's first)
+        att_flush<HD>(P, nseg == 1 ? recs + (warp * 2) * REC
+                                   : P.apart + (cur * P.J_att + (blockIdx.x - owner_of(Ta, C, cur * nt))) * REC,
+                      o, mrun, lrun);
       cur = seq;
       ++nseg;
       if (first_seq < 0) first_seq = seq;
@@ -591,22 +947,22 @@ __device__ bool stage_att(const Params& P, int layer, Ring& R, Cursor& prod, int
       const float* qp = P.q + (int64_t)b * P.Hq * HD + (int64_t)(kvh * GH + g) * HD;
 #pragma unroll
       for (int j = 0; j < KS; ++j) {
-        float v[4] = {0.f, 0.f, 0.f, 0.f};
+        float2 v0 = make_float2(0.f, 0.f), v1 = make_float2(0.f, 0.f);
         if (g < GH) {
-          v[0] = __ldcg(qp + 16 * j + 2 * t) * qscale;
-          v[1] = __ldcg(qp + 16 * j + 2 * t + 1) * qscale;
-          v[2] = __ldcg(qp + 16 * j + 2 * t + 8) * qscale;
-          v[3] = __ldcg(qp + 16 * j + 2 * t + 9) * qscale;
+          v0 = __ldcg(reinterpret_cast<const float2*>(qp + 16 * j + 2 * t));
+          v1 = __ldcg(reinterpret_cast<const float2*>(qp + 16 * j + 2 * t + 8));
         }
+        const float v[4] = {v0.x * qscale, v0.y * qscale, v1.x * qscale, v1.y * qscale};
         float h[4], l[4];
+#pragma unroll
         for (int e = 0; e < 4; ++e) {
           h[e] = __bfloat162float(__float2bfloat16_rn(v[e]));
           l[e] = v[e] - h[e];
         }
-        qh[j][0] = pack_bf16x2(h[0], h[1]);
-        qh[j][1] = pack_bf16x2(h[2], h[3]);
-        ql[j][0] = pack_bf16x2(l[0], l[1]);
-        ql[j][1] = pack_bf16x2(l[2], l[3]);
+        qa[j][0] = pack_bf16x2(h[0], h[1]);  // rows g: high part
+        qa[j][1] = pack_bf16x2(l[0], l[1]);  // rows g+8: low part
+        qa[j][2] = pack_bf16x2(h[2], h[3]);
+        qa[j][3] = pack_bf16x2(l[2], l[3]);
       }
       mrun = -INFINITY;
       lrun = 0.f;
@@ -634,7 +990,7 @@ __device__ bool stage_att(const Params& P, int layer, Ring& R, Cursor& prod, int
       }
       __syncwarp();
     }
-    // scores S[head g][keys 8n + 2t, +1] = (q * log2e / sqrt(hd)) . K
+    // scores: rows g = high-part dot products, rows g+8 = low-part ones
     float s[2][4];
 #pragma unroll
     for (int n = 0; n < 2; ++n) {
@@ -644,34 +1000,34 @@ __device__ bool stage_att(const Params& P, int layer, Ring& R, Cursor& prod, int
         const int mat = lane >> 3, r = lane & 7;
         uint32_t b0, b1, b2, b3;
         ldsm_x4(ks + (8 * n + r) * ROWB + (16 * (jj + (mat >> 1)) + 8 * (mat & 1)) * 2, b0, b1, b2, b3);
-        mma_bf16(s[n], qh[jj][0], 0u, qh[jj][1], 0u, b0, b1);
-        mma_bf16(s[n], ql[jj][0], 0u, ql[jj][1], 0u, b0, b1);
-        mma_bf16(s[n], qh[jj + 1][0], 0u, qh[jj + 1][1], 0u, b2, b3);
-        mma_bf16(s[n], ql[jj + 1][0], 0u, ql[jj + 1][1], 0u, b2, b3);
+        mma_bf16(s[n], qa[jj][0], qa[jj][1], qa[jj][2], qa[jj][3], b0, b1);
+        mma_bf16(s[n], qa[jj + 1][0], qa[jj + 1][1], qa[jj + 1][2], qa[jj + 1][3], b2, b3);
       }
     }
-    // online softmax over this tile
+    // online softmax over this tile (score of key 8n + 2t + e = s[n][e] + s[n][e+2])
+    float sv[2][2];
     float mt = -INFINITY;
 #pragma unroll
     for (int n = 0; n < 2; ++n)
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
         const int64_t key = 16 * (int64_t)i + 8 * n + 2 * t + e;
-        if (key > P.pos) s[n][e] = -INFINITY;
-        mt = fmaxf(mt, s[n][e]);
+        sv[n][e] = key > P.pos ? -INFINITY : s[n][e] + s[n][e + 2];
+        mt = fmaxf(mt, sv[n][e]);
       }
     mt = fmaxf(mt, __shfl_xor_sync(FULL, mt, 1));
     mt = fmaxf(mt, __shfl_xor_sync(FULL, mt, 2));
     const float mnew = fmaxf(mrun, mt);
     const float alpha = exp2f(mrun - mnew);
-    float p[2][2];
-    float psum = 0.f;
+    float ph[2][2], pl[2][2], psum = 0.f;
 #pragma unroll
     for (int n = 0; n < 2; ++n)
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
-        p[n][e] = exp2f(s[n][e] - mnew);
-        psum += p[n][e];
+        const float p = exp2f(sv[n][e] - mnew);
+        psum += p;
+        ph[n][e] = __bfloat162float(__float2bfloat16_rn(p));
+        pl[n][e] = p - ph[n][e];
       }
     lrun = lrun * alpha + psum;
     mrun = mnew;
@@ -679,32 +1035,25 @@ __device__ bool stage_att(const Params& P, int layer, Ring& R, Cursor& prod, int
     for (int nb = 0; nb < NB; ++nb) {
       o[nb][0] *= alpha;
       o[nb][1] *= alpha;
+      o[nb][2] *= alpha;
+      o[nb][3] *= alpha;
     }
-    float ph[2][2], pl[2][2];
-#pragma unroll
-    for (int n = 0; n < 2; ++n)
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        ph[n][e] = __bfloat162float(__float2bfloat16_rn(p[n][e]));
-        pl[n][e] = p[n][e] - ph[n][e];
-      }
-    const uint32_t pa0 = pack_bf16x2(ph[0][0], ph[0][1]), pa2 = pack_bf16x2(ph[1][0], ph[1][1]);
-    const uint32_t pb0 = pack_bf16x2(pl[0][0], pl[0][1]), pb2 = pack_bf16x2(pl[1][0], pl[1][1]);
-    // o[head g][d 8nb + 2t, +1] += P V
+    const uint32_t pa0 = pack_bf16x2(ph[0][0], ph[0][1]), pa1 = pack_bf16x2(pl[0][0], pl[0][1]);
+    const uint32_t pa2 = pack_bf16x2(ph[1][0], ph[1][1]), pa3 = pack_bf16x2(pl[1][0], pl[1][1]);
+    // o rows g += p_hi V, rows g+8 += p_lo V  (head dims 8nb + 2t, +1)
 #pragma unroll
     for (int nb = 0; nb < NB; nb += 2) {
       const int mat = lane >> 3, r = lane & 7;
       uint32_t b0, b1, b2, b3;
       ldsm_x4_t(vs + (8 * (mat & 1) + r) * ROWB + 8 * (nb + (mat >> 1)) * 2, b0, b1, b2, b3);
-      mma_bf16(o[nb], pa0, 0u, pa2, 0u, b0, b1);
-      mma_bf16(o[nb], pb0, 0u, pb2, 0u, b0, b1);
-      mma_bf16(o[nb + 1], pa0, 0u, pa2, 0u, b2, b3);
-      mma_bf16(o[nb + 1], pb0, 0u, pb2, 0u, b2, b3);
+      mma_bf16(o[nb], pa0, pa1, pa2, pa3, b0, b1);
+      mma_bf16(o[nb + 1], pa0, pa1, pa2, pa3, b2, b3);
     }
-    ring_advance<HD>(P, R, prod, wg, W, lane, policy);
-    ring_advance<HD>(P, R, prod, wg, W, lane, policy);
+    ring_advance<HD, WT>(P, R, prod, wg, W, lane, policy);
+    ring_advance<HD, WT>(P, R, prod, wg, W, lane, policy);
   }
-  if (ok && nseg > 0) flush(true);
+  if (ok && nseg > 0) att_flush<HD>(P, recs + (warp * 2 + (nseg == 1 ? 0 : 1)) * REC, o, mrun, lrun);
+  if (lane == 0) trace_stamp(P, layer * NSTAGE + ST_ATT, 2 + warp);
   if (lane == 0) {
     M.seg_n[warp] = ok ? nseg : 0;
     M.seg_first[warp] = first_seq;
@@ -713,21 +1062,6 @@ __device__ bool stage_att(const Params& P, int layer, Ring& R, Cursor& prod, int
   __syncthreads();
   if (M.abort) return false;
   // CTA merge: the warp where a sequence's run starts merges the run
-  auto chain = [&](int64_t seq, int rec_idx, bool continues) {
-    const float* list[NW + 1];
-    int n = 0;
-    list[n++] = recs + (warp * 2 + rec_idx) * REC;
-    if (continues) {
-      for (int v = warp + 1; v < NW; ++v) {
-        if (M.seg_n[v] == 0) continue;
-        if (M.seg_first[v] != seq) break;
-        list[n++] = recs + (v * 2 + 0) * REC;
-        if (M.seg_n[v] > 1) break;
-      }
-    }
-    float* out = P.apart + (seq * P.J_att + (blockIdx.x - owner_of(Ta, C, seq * nt))) * REC;
-    merge_records<HD>(list, n, out, GH);
-  };
   const int ns = M.seg_n[warp];
   if (ns > 0) {
     bool owner = true;
@@ -736,39 +1070,29 @@ __device__ bool stage_att(const Params& P, int layer, Ring& R, Cursor& prod, int
       owner = M.seg_last[v] != first_seq;
       break;
     }
-    if (owner) chain(first_seq, 0, ns == 1);
-    if (ns > 1) chain(cur, 1, true);
+    if (owner) att_chain<HD>(P, M, recs, first_seq, 0, ns == 1, Ta, C);
+    if (ns > 1) att_chain<HD>(P, M, recs, cur, 1, true, Ta, C);
+  }
+  // the last CTA to publish a sequence's record merges the sequence
+  __syncthreads();
+  const int64_t clo = range_lo(Ta, C, blockIdx.x), chi = range_lo(Ta, C, blockIdx.x + 1);
+  if (clo < chi) {
+    const int64_t s0 = clo / nt, s1 = (chi - 1) / nt;
+    if (threadIdx.x == 0) {
+      for (int64_t sq = s0; sq <= s1; ++sq) {
+        const int64_t cf = owner_of(Ta, C, sq * nt), cl = owner_of(Ta, C, sq * nt + nt - 1);
+        const uint32_t n = (uint32_t)(Ta >= C ? cl - cf + 1 : nt);
+        const uint32_t old = atom_add_acq_rel(P.seqcnt + sq, 1u);
+        M.mseq[(int)(sq - s0)] = old == n - 1 ? sq : -1;
+        if (old == n - 1) P.seqcnt[sq] = 0;
+      }
+    }
+    __syncthreads();
+    float* fac = recs + NW * 2 * REC;  // per (head, record) factors of the merge
+    for (int64_t sq = s0; sq <= s1; ++sq)
+      if (M.mseq[(int)(sq - s0)] == sq) merge_sequence<HD>(P, sq, Ta, C, fac);
   }
   return true;
-}
-
-// Merge the CTA partials of each (sequence, head) into attn [B][Hq*hd].
-template <int HD>
-__device__ void stage_comb(const Params& P, int64_t wg, int64_t W) {
-  const int lane = threadIdx.x & 31;
-  const int GH = P.GH, REC = GH * (HD + 2), nt = P.nt_att;
-  const int64_t Ta = (int64_t)P.B * P.Hkv * nt, C = gridDim.x;
-  const int64_t items = (int64_t)P.B * P.Hq * (HD / 32);
-  for (int64_t it = wg; it < items; it += W) {
-    const int qd = (int)(it % (HD / 32));
-    const int h = (int)((it / (HD / 32)) % P.Hq);
-    const int b = (int)(it / (HD / 32) / P.Hq);
-    const int64_t seq = (int64_t)b * P.Hkv + h / GH;
-    const int hl = h % GH, d = qd * 32 + lane;
-    const int64_t cf = owner_of(Ta, C, seq * nt), cl = owner_of(Ta, C, seq * nt + nt - 1);
-    float mx = -INFINITY, l = 0.f, o = 0.f;
-    for (int64_t jc = 0; jc <= cl - cf; ++jc) {
-      if (range_lo(Ta, C, cf + jc) == range_lo(Ta, C, cf + jc + 1)) continue;  // CTA with no tiles
-      const float* rec = P.apart + (seq * P.J_att + jc) * REC;
-      const float m = __ldcg(rec + GH * HD + hl), lj = __ldcg(rec + GH * HD + GH + hl);
-      const float oj = __ldcg(rec + hl * HD + d);
-      const float mn = fmaxf(mx, m), a0 = exp2f(mx - mn), a1 = exp2f(m - mn);
-      l = l * a0 + lj * a1;
-      o = o * a0 + oj * a1;
-      mx = mn;
-    }
-    P.attn[(int64_t)b * P.Hq * HD + (int64_t)h * HD + d] = o / l;
-  }
 }
 
 // ------------------------------------------------------------------ grid barrier
@@ -777,10 +1101,12 @@ __device__ bool grid_sync(const Params& P, uint32_t target, Misc& M) {
   if (threadIdx.x == 0) {
     __threadfence();
     atomicAdd(P.ctrl, 1u);
-    const uint64_t t0 = globaltimer();
-    while (ld_acquire_gpu(P.ctrl) < target) {
-      __nanosleep(64);
-      if (globaltimer() - t0 > WAIT_LIMIT_NS) {
+    uint64_t t0 = 0;
+    for (uint32_t it = 1; ld_acquire_gpu(P.ctrl) < target; ++it) {
+      if ((it & 255u) != 0) continue;
+      const uint64_t now = globaltimer();
+      if (t0 == 0) t0 = now;
+      else if (now - t0 > WAIT_LIMIT_NS) {
         atomicExch(P.ctrl + 1, STATUS_TIMEOUT);
         M.abort = 1;
         break;
@@ -804,17 +1130,21 @@ __global__ void __launch_bounds__(NTHREADS, 1) decode_kernel(const __grid_consta
   R.bar0 = smem_addr(smem + SM_BARS + warp * DEPTH * 8);
   R.n_issued = R.n_done = 0;
   if (lane < DEPTH) mbar_init(R.bar0 + lane * 8, 1);
-  if (threadIdx.x == 0) M.abort = 0;
+  if (threadIdx.x == 0) {
+    M.abort = 0;
+    M.pphase = 0;
+    mbar_init(smem_addr(smem + SM_PBAR), 1);
+  }
   mbar_init_fence();
   __syncthreads();
   const uint64_t policy = policy_evict_first();
   Cursor prod;
   prod.s = P.stage_begin;
-  cursor_range(P, prod.s, wg, W, prod.pos, prod.end);
+  cursor_enter<WT>(P, prod, wg, W);
   for (int k = 0; k < DEPTH; ++k) {
     SlotDesc d;
-    if (!cursor_next(P, prod, wg, W, d)) break;
-    issue_slot<HD>(P, d, R.slot(R.n_issued), R.bar(R.n_issued), lane, policy);
+    if (!cursor_next<WT>(P, prod, wg, W, d)) break;
+    issue_slot<HD, WT>(P, prod, d, R.slot(R.n_issued), R.bar(R.n_issued), lane, policy);
     R.n_issued++;
   }
   bool ok = true;
@@ -826,14 +1156,15 @@ __global__ void __launch_bounds__(NTHREADS, 1) decode_kernel(const __grid_consta
       }
     }
     const int layer = s / NSTAGE, st = s % NSTAGE;
+    if (threadIdx.x == 0) trace_stamp(P, s, 0);
     if (st == ST_ATT) {
-      ok = stage_att<HD>(P, layer, R, prod, wg, W, smem, M, policy);
-    } else if (st == ST_COMB) {
-      stage_comb<HD>(P, wg, W);
+      if (threadIdx.x == 0) trace_stamp(P, s, 1);
+      ok = stage_att<HD, WT>(P, layer, R, prod, wg, W, smem, M, policy);
     } else {
       stage_gemv<HD, WT>(P, layer, st, R, prod, wg, W, smem, M, policy);
     }
     __syncthreads();
+    if (threadIdx.x == 0) trace_stamp(P, s, NW + 2);
     if (M.abort) ok = false;
   }
   if (!ok) {  // let this warp's copies in flight land before the CTA exits (bounded)
@@ -854,6 +1185,8 @@ struct DevInfo {
 static std::mutex g_mu;
 static DevInfo g_dev[64];
 static int g_launch_mode = 0;  // 0 automatic, 1 one launch per stage
+static uint64_t* g_trace = nullptr;
+static size_t g_trace_bytes = 0;
 
 template <int HD, int WT>
 static int prepare_kernel() {
@@ -889,7 +1222,7 @@ static int device_info(DevInfo& out) {
 }
 
 struct WsLayout {
-  int64_t ctrl, cnt, gpart, apart, Z, q, attn, y, a, total;
+  int64_t ctrl, cnt, seqcnt, gpart, apart, Z, q, attn, y, a, total;
 };
 
 static int64_t att_J(int64_t seqs, int64_t nt, int64_t C) {
@@ -911,15 +1244,16 @@ static void ws_layout(const ddl_shape& s, int B, int64_t s_max, int C, const Mat
   const int64_t Jatt = C;
   int64_t gpart = 0, ntmax = 0;
   for (int k = 0; k < 4; ++k) {
-    const int64_t u = (int64_t)mg[k].Sk * mg[k].NT * mg[k].J * 32 * 2 * 4;
+    const int64_t u = (int64_t)mg[k].NT * mg[k].NP * mg[k].J * 32 * 2 * 4;
     if (u > gpart) gpart = u;
     if (mg[k].NT > ntmax) ntmax = mg[k].NT;
   }
   int64_t off = 0;
   w.ctrl = off;  off = align256(off + 256);
   w.cnt = off;   off = align256(off + ntmax * 4);
+  w.seqcnt = off; off = align256(off + (int64_t)B * s.H_kv * 4);
   w.gpart = off; off = align256(off + gpart);
-  w.apart = off; off = align256(off + (int64_t)B * s.H_kv * (Jatt + 1) * GH * (s.head_dim + 2) * 4);
+  w.apart = off; off = align256(off + (int64_t)B * s.H_kv * (Jatt + 1) * att_rec_floats(GH, s.head_dim) * 4);
   w.Z = off;     off = align256(off + 2 * (int64_t)B * s.D * 4);
   w.q = off;     off = align256(off + (int64_t)B * Nq * 4);
   w.attn = off;  off = align256(off + (int64_t)B * Nq * 4);
@@ -931,7 +1265,11 @@ static void ws_layout(const ddl_shape& s, int B, int64_t s_max, int C, const Mat
 static int plan(const ddl_shape* s, int wtype, int B, int64_t s_max, int C, MatGeom mg[4],
                 WsLayout& w) {
   make_geoms(*s, wtype, mg);
-  for (int k = 0; k < 4; ++k) mg[k].J = max_warps_per_unit(mg[k], (int64_t)C * NW);
+  for (int k = 0; k < 4; ++k) {
+    if (mg[k].T * (int64_t)C >= (int64_t(1) << 32) || mg[k].NT >= (1 << 20))
+      return DDL_ERR_UNSUPPORTED;  // 32-bit work-split arithmetic, 20-bit tile ids
+    if (!make_panels(mg[k], B, C)) return DDL_ERR_UNSUPPORTED;
+  }
   ws_layout(*s, B, s_max, C, mg, w);
   return DDL_OK;
 }
@@ -965,9 +1303,7 @@ static int decode(const ddl_shape* s, ddl_wtype wtype, const ddl_layer_w* layers
   Params P;
   memset(&P, 0, sizeof P);
   WsLayout w;
-  plan(s, wtype, B, s_max, C, P.mg, w);
-  for (int k = 0; k < 4; ++k)  // a CTA's share of a stream must touch at most two k-chunks
-    if ((P.mg[k].T + C - 1) / C > (int64_t)P.mg[k].NT * P.mg[k].Gc) return DDL_ERR_UNSUPPORTED;
+  if ((st = plan(s, wtype, B, s_max, C, P.mg, w))) return st;
   if ((int64_t)ws_bytes < w.total) return DDL_ERR_WORKSPACE;
   const int HD = s->head_dim;
   st = HD == 128 ? (wtype == DDL_W_INT4 ? prepare_kernel<128, DDL_W_INT4>() : prepare_kernel<128, DDL_W_BF16>())
@@ -978,14 +1314,26 @@ static int decode(const ddl_shape* s, ddl_wtype wtype, const ddl_layer_w* layers
   P.GH = s->H_q / s->H_kv; P.eps = s->eps; P.wtype = wtype; P.rope_base = s->rope_base;
   P.pos = pos; P.s_max = s_max;
   P.nt_att = (int32_t)((pos + 1 + 15) / 16);
+  for (int i = 0; i < HD / 2; ++i) {  // RoPE angles in fp64: pos * base^(-2i/hd)
+    const double phi = (double)pos * pow(s->rope_base, -2.0 * i / (double)HD);
+    P.rope[i][0] = (float)cos(phi);
+    P.rope[i][1] = (float)sin(phi);
+  }
   P.J_att = (int32_t)att_J((int64_t)B * s->H_kv, P.nt_att, C);
+  // shared scratch of the attention merges: 2 records per warp + the factors
+  if ((int64_t)(NW * 2 * att_rec_floats(P.GH, HD) + P.GH * P.J_att) * 4 > SM_SCR_BYTES) return DDL_ERR_UNSUPPORTED;
+  {  // a CTA's attention range may touch at most 8 sequences
+    const int64_t Ta = (int64_t)B * s->H_kv * P.nt_att, per = (Ta + C - 1) / C;
+    if ((per + P.nt_att - 1) / P.nt_att + 1 > 8) return DDL_ERR_UNSUPPORTED;
+  }
   P.resid_in = resid_in; P.x_bf16 = x_bf16; P.resid_out = resid_out; P.out_bf16 = out_bf16;
   P.ctrl = (uint32_t*)(ws + w.ctrl); P.cnt = (uint32_t*)(ws + w.cnt);
+  P.seqcnt = (uint32_t*)(ws + w.seqcnt);
   P.gpart = (float*)(ws + w.gpart); P.apart = (float*)(ws + w.apart); P.Z = (float*)(ws + w.Z);
   P.q = (float*)(ws + w.q); P.attn = (float*)(ws + w.attn); P.y = (float*)(ws + w.y);
   P.a = (float*)(ws + w.a);
   cudaStream_t cs = (cudaStream_t)stream;
-  cudaError_t e = cudaMemsetAsync(ws, 0, (size_t)w.gpart, cs);  // barrier, status, tile counters
+  cudaError_t e = cudaMemsetAsync(ws, 0, (size_t)w.gpart, cs);  // barrier, status, counters
   if (e != cudaSuccess) return cuda_status(e);
   const bool coop = di.coop && g_launch_mode == 0;
   void* fn = HD == 128 ? (wtype == DDL_W_INT4 ? (void*)decode_kernel<128, DDL_W_INT4> : (void*)decode_kernel<128, DDL_W_BF16>)
@@ -1002,6 +1350,8 @@ static int decode(const ddl_shape* s, ddl_wtype wtype, const ddl_layer_w* layers
       P.layers[l].kc = kv[l0 + l].k;
       P.layers[l].vc = kv[l0 + l].v;
     }
+    const size_t need_trace = (size_t)nL * NSTAGE * C * TRACE_WORDS * 8;
+    P.trace = (g_trace && g_trace_bytes >= need_trace && L <= MAX_LAYERS) ? g_trace : nullptr;
     if (coop) {
       if (l0 > 0 && (e = cudaMemsetAsync(ws + w.ctrl, 0, 4, cs)) != cudaSuccess) return cuda_status(e);
       P.stage_begin = 0;
@@ -1015,6 +1365,7 @@ static int decode(const ddl_shape* s, ddl_wtype wtype, const ddl_layer_w* layers
       for (int sidx = 0; sidx < nL * NSTAGE; ++sidx) {
         P.stage_begin = sidx;
         P.stage_end = sidx + 1;
+        if (P.trace) P.trace = g_trace + (size_t)sidx * C * TRACE_WORDS;
         void* args[] = {&P};
         e = cudaLaunchKernel(fn, dim3(C), dim3(NTHREADS), args, SM_TOTAL, cs);
         if (e != cudaSuccess) return cuda_status(e);
@@ -1034,10 +1385,10 @@ extern "C" size_t ddl_workspace_bytes(const ddl_shape* shape, int32_t B, int64_t
   if (device_info(di)) return 0;
   MatGeom mg[4];
   WsLayout w;
-  plan(shape, DDL_W_INT4, B, s_max, di.sms, mg, w);
+  if (plan(shape, DDL_W_INT4, B, s_max, di.sms, mg, w)) return 0;
   WsLayout w2;
   MatGeom mg2[4];
-  plan(shape, DDL_W_BF16, B, s_max, di.sms, mg2, w2);
+  if (plan(shape, DDL_W_BF16, B, s_max, di.sms, mg2, w2)) return 0;
   return (size_t)(w.total > w2.total ? w.total : w2.total);
 }
 
@@ -1050,7 +1401,7 @@ extern "C" int ddl_workspace_view(const ddl_shape* shape, int32_t B, int64_t s_m
   if ((st = device_info(di))) return st;
   MatGeom mg[4];
   WsLayout w;
-  plan(shape, DDL_W_INT4, B, s_max, di.sms, mg, w);
+  if ((st = plan(shape, DDL_W_INT4, B, s_max, di.sms, mg, w))) return st;
   out->q = (size_t)w.q;
   out->attn = (size_t)w.attn;
   out->y = (size_t)w.y;
@@ -1078,6 +1429,12 @@ extern "C" int ddl_stack_decode(const ddl_shape* shape, ddl_wtype wtype, const d
 extern "C" int ddl_set_launch_mode(int32_t mode) {
   if (mode != 0 && mode != 1) return DDL_ERR_ARG;
   g_launch_mode = mode;
+  return DDL_OK;
+}
+
+extern "C" int ddl_set_trace(void* device_buf, size_t bytes) {
+  g_trace = (uint64_t*)device_buf;
+  g_trace_bytes = device_buf ? bytes : 0;
   return DDL_OK;
 }
 

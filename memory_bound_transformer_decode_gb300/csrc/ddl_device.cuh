@@ -43,17 +43,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 // Warp-uniform wait for a barrier phase; false (and the status word set) if
-// it did not complete within WAIT_LIMIT_NS.
+// it did not complete within WAIT_LIMIT_NS.  The clock is read only every
+// 1024 polls, so a wait that succeeds soon costs no timer reads.
 __device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, uint32_t* status) {
-  if (__all_sync(FULL, mbar_try_wait(bar, parity))) return true;
-  uint64_t t0 = globaltimer();
-  while (true) {
-    for (int i = 0; i < 32; ++i)
-      if (__all_sync(FULL, mbar_try_wait(bar, parity))) return true;
-    uint64_t dt = __shfl_sync(FULL, globaltimer() - t0, 0);
-    if (dt > WAIT_LIMIT_NS) {
-      if ((threadIdx.x & 31) == 0) atomicExch(status, STATUS_TIMEOUT);
-      return false;
+  uint64_t t0 = 0;
+  for (uint32_t it = 1;; ++it) {
+    if (__all_sync(FULL, mbar_try_wait(bar, parity))) return true;
+    if ((it & 1023u) == 0) {
+      const uint64_t now = __shfl_sync(FULL, globaltimer(), 0);
+      if (t0 == 0) t0 = now;
+      else if (now - t0 > WAIT_LIMIT_NS) {
+        if ((threadIdx.x & 31) == 0) atomicExch(status, STATUS_TIMEOUT);
+        return false;
+      }
     }
   }
 }

@@ -57,16 +57,38 @@ inline int64_t make_geoms(const ddl_shape& s, int wtype, MatGeom mg[4]) {
   return off;
 }
 
-// Partial slots per (k-chunk, tile) unit when the blocks are split over W warps.
-inline int32_t max_warps_per_unit(const MatGeom& m, int64_t W) {
-  int32_t J = 1;
-  for (int kc = 0; kc < m.Sk; ++kc)
+// Panels of a matrix for batch B on C CTAs (see ddl_plan.h): at most
+// XF_CHUNKS / B k-chunks per panel, near-equal chunk counts, CTAs in
+// proportion to blocks (at least one each); then J, the largest number of
+// warps sharing a (tile, panel).  Returns false if the grid is too small.
+inline bool make_panels(MatGeom& m, int B, int C) {
+  int ch = XF_CHUNKS / B;
+  if (ch < 1) ch = 1;
+  int NP = (m.Sk + ch - 1) / ch;
+  if (NP > MAXP || NP > C) return false;
+  m.NP = NP;
+  for (int p = 0; p <= NP; ++p) m.pk[p] = (int16_t)((int64_t)m.Sk * p / NP);
+  int64_t acc = 0;
+  m.pc[0] = 0;
+  for (int p = 0; p < NP; ++p) {
+    acc += panel_blocks(m, p);
+    int c = (int)((acc * C + m.T / 2) / m.T);
+    if (c < m.pc[p] + 1) c = m.pc[p] + 1;
+    if (c > C - (NP - 1 - p)) c = C - (NP - 1 - p);
+    m.pc[p + 1] = (int16_t)c;
+  }
+  m.pc[NP] = (int16_t)C;
+  uint32_t J = 1;
+  for (int p = 0; p < NP; ++p) {
+    const uint32_t Gp = panel_groups(m, p);
     for (int T = 0; T < m.NT; ++T) {
-      int64_t s = unit_start(m, kc, T), e = s + chunk_groups(m, kc) - 1;
-      int64_t n = owner_of(m.T, W, e) - owner_of(m.T, W, s) + 1;
-      if (n > J) J = (int32_t)n;
+      const uint32_t n = work_owner(m, p, (uint32_t)(T + 1) * Gp - 1, NW) -
+                         work_owner(m, p, (uint32_t)T * Gp, NW) + 1;
+      if (n > J) J = n;
     }
-  return J;
+  }
+  m.J = (int32_t)J;
+  return true;
 }
 
 }  // namespace ddl

@@ -23,11 +23,10 @@
 // row j (rows 0-7) with up row j (rows 8-15); Wo and down tiles are 16
 // consecutive rows.
 //
-// Work split ("stream-K"): the blocks of a matrix are split into W contiguous
-// ranges, one per warp of the grid.  A (k-chunk, tile) unit covered by more
-// than one warp, or a tile with more than one k-chunk, is finished by the
-// last warp that contributes to it (an atomic counter per tile), which sums
-// the partial results in a fixed order: results do not depend on timing.
+// Work split: see panel_of_cta / warp_work below.  A tile covered by more
+// than one warp is finished by the last warp that contributes to it (an
+// atomic counter per tile), which sums the partial results in a fixed order:
+// results do not depend on timing.
 #pragma once
 #include <stdint.h>
 
@@ -52,9 +51,16 @@ constexpr int GC = 32;                // groups per k-chunk
 constexpr int MAX_LAYERS = 96;        // layers per launch (longer stacks use several launches)
 constexpr int MAX_B = 4;
 constexpr int MAX_GH = 8;             // query heads per KV head
-constexpr int NSTAGE = 6;
+constexpr int NSTAGE = 5;
+constexpr int MAXP = 16;              // k-chunk panels per matrix
+constexpr int XF_CHUNKS = 8;          // k-chunks of x one CTA can stage at batch 1 (x batch size <= 8)
+constexpr int TRACE_WORDS = NW + 7;   // per (stage, CTA) in the optional trace
 
-enum Stage { ST_QKV = 0, ST_ATT = 1, ST_COMB = 2, ST_WO = 3, ST_GU = 4, ST_DOWN = 5 };
+// Floats of one attention softmax record (o[GH][hd], m[GH], l[GH]), padded
+// to 16 bytes so that records can be read as float4.
+DDL_HD int att_rec_floats(int GH, int hd) { return (GH * (hd + 2) + 3) & ~3; }
+
+enum Stage { ST_QKV = 0, ST_ATT = 1, ST_WO = 2, ST_GU = 3, ST_DOWN = 4 };
 enum MatKind { MK_QKV = 0, MK_WO = 1, MK_GU = 2, MK_DOWN = 3 };
 
 DDL_HD int stage_mat(int st) {
@@ -65,10 +71,12 @@ struct MatGeom {
   int32_t N, K;       // rows of the (combined) matrix, input dimension
   int32_t NT, G;      // 16-row tiles, 64-column groups per row
   int32_t Gc, Sk;     // groups per full k-chunk, number of k-chunks
-  int32_t J;          // partial slots per (k-chunk, tile) unit
-  int32_t pad;
+  int32_t J;          // partial slots per (tile, panel)
+  int32_t NP;         // panels: k-chunks pk[p]..pk[p+1]-1, worked by CTAs pc[p]..pc[p+1]-1
   int64_t T;          // blocks
   int64_t woff, soff; // byte offsets of the code and scale streams in a packed layer
+  int16_t pk[MAXP + 1];
+  int16_t pc[MAXP + 1];
 };
 
 DDL_HD int32_t chunk_groups(const MatGeom& m, int kc) {
@@ -92,6 +100,61 @@ DDL_HD int64_t range_lo(int64_t total, int64_t parts, int64_t i) { return total 
 // The part owning item b (total > 0).
 DDL_HD int64_t owner_of(int64_t total, int64_t parts, int64_t b) {
   return ((b + 1) * parts - 1) / total;
+}
+
+// 32-bit forms for the kernels (the host checks T * W < 2^32).
+DDL_HD uint32_t owner32(uint32_t total, uint32_t parts, uint32_t b) {
+  return ((b + 1) * parts - 1) / total;
+}
+DDL_HD uint32_t lo32(uint32_t total, uint32_t parts, uint32_t i) { return total * i / parts; }
+DDL_HD uint32_t unit_start32(const MatGeom& m, int kc, int T) {
+  return (uint32_t)kc * (uint32_t)m.NT * (uint32_t)m.Gc + (uint32_t)T * (uint32_t)chunk_groups(m, kc);
+}
+
+// Work split.  The k-chunks are grouped into panels of at most as many
+// chunks as one CTA can stage; panel p gets CTAs pc[p]..pc[p+1]-1 in
+// proportion to its blocks.  Inside a panel the work order is tile-major
+// (tile, k-chunk, group), so a warp accumulates a whole tile across the
+// panel's chunks in registers; within a panel the CTAs, and within a CTA the
+// warps, take contiguous ranges of that order.  Only tiles split between
+// warps or panels leave partials: slot (tile, panel, j) for the j-th warp
+// (in panel order) owning blocks of the tile; each contributor adds its block
+// count to the tile's counter and the one that brings it to G finishes it.
+DDL_HD int panel_of_cta(const MatGeom& m, int c) {
+  int p = 0;
+  while (p + 1 < m.NP && c >= m.pc[p + 1]) ++p;
+  return p;
+}
+DDL_HD uint32_t panel_groups(const MatGeom& m, int p) {
+  const int k0 = m.pk[p], k1 = m.pk[p + 1];
+  return (uint32_t)((k1 - k0) * m.Gc - (k1 == m.Sk ? m.Sk * m.Gc - m.G : 0));
+}
+DDL_HD uint32_t panel_blocks(const MatGeom& m, int p) { return (uint32_t)m.NT * panel_groups(m, p); }
+// Range of panel work indices of warp w (0..NW-1) of panel-local CTA cl.
+DDL_HD void warp_work(const MatGeom& m, int p, int cl, int w, int nw, uint32_t& lo, uint32_t& hi) {
+  const uint32_t Tp = panel_blocks(m, p), Cp = (uint32_t)(m.pc[p + 1] - m.pc[p]);
+  const uint32_t clo = lo32(Tp, Cp, cl), R = lo32(Tp, Cp, cl + 1) - clo;
+  lo = clo + lo32(R, nw, w);
+  hi = clo + lo32(R, nw, w + 1);
+}
+// Panel-local warp index (cl * nw + w) owning panel work index i.
+DDL_HD uint32_t work_owner(const MatGeom& m, int p, uint32_t i, int nw) {
+  const uint32_t Tp = panel_blocks(m, p), Cp = (uint32_t)(m.pc[p + 1] - m.pc[p]);
+  const uint32_t cl = owner32(Tp, Cp, i), clo = lo32(Tp, Cp, cl), R = lo32(Tp, Cp, cl + 1) - clo;
+  return cl * nw + owner32(R, nw, i - clo);
+}
+DDL_HD bool warp_empty(const MatGeom& m, int p, uint32_t v, int nw) {
+  uint32_t lo, hi;
+  warp_work(m, p, (int)(v / nw), (int)(v % nw), nw, lo, hi);
+  return lo == hi;
+}
+// (tile, k-chunk, group) of panel work index i.
+DDL_HD void work_coord(const MatGeom& m, int p, uint32_t i, int& T, int& kc, int& gi) {
+  const uint32_t Gp = panel_groups(m, p);
+  T = (int)(i / Gp);
+  const uint32_t r = i - (uint32_t)T * Gp;
+  kc = m.pk[p] + (int)(r / (uint32_t)m.Gc);
+  gi = (int)(r - (uint32_t)(kc - m.pk[p]) * (uint32_t)m.Gc);
 }
 
 // Row of the combined matrix held by row r (0..15) of tile T.
@@ -125,6 +188,7 @@ struct Params {
   int32_t cooperative;
   int32_t nt_att;       // 16-key tiles per sequence
   int32_t J_att;        // attention partial slots per sequence
+  float rope[64][2];    // cos, sin of pos * base^(-2i/hd), i < hd/2 (computed in fp64 on the host)
   MatGeom mg[4];
   const float* resid_in;
   const uint16_t* x_bf16;
@@ -132,13 +196,15 @@ struct Params {
   uint16_t* out_bf16;
   uint32_t* ctrl;       // [0] grid barrier counter, [1] status word
   uint32_t* cnt;        // per-tile arrival counters
-  float* gpart;         // GEMV partials: [unit][J][32 lanes][2]
+  uint32_t* seqcnt;     // per-sequence arrival counters of the attention merge
+  float* gpart;         // GEMV partials: [tile][panel][J][32 lanes][2]
   float* apart;         // attention partials: [seq][J_att][GH*(hd+2)]
   float* Z;             // [2][B][D] residual ping-pong between layers
   float* q;             // [B][Hq*hd]
   float* attn;          // [B][Hq*hd]
   float* y;             // [B][D]
   float* a;             // [B][dff]
+  uint64_t* trace;      // optional: per stage, CTA: start, prologue end, NW warp ends, end, 4 prologue steps (ns)
   LayerDev layers[MAX_LAYERS];
 };
 

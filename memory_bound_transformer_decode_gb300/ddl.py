@@ -22,7 +22,7 @@ STATUS = {0: "DDL_OK", 1: "DDL_ERR_SHAPE", 2: "DDL_ERR_POS", 3: "DDL_ERR_ALIGN",
           7: "DDL_ERR_TIMEOUT", 8: "DDL_ERR_ARG"}
 EXPORTED = ("ddl_quantize_int4", "ddl_packed_layer_bytes", "ddl_pack_layer", "ddl_kv_append",
             "ddl_workspace_bytes", "ddl_workspace_view", "ddl_layer_decode", "ddl_stack_decode",
-            "ddl_stack_decode_noalloc", "ddl_set_launch_mode", "ddl_read_device_status", "ddl_status_string",
+            "ddl_stack_decode_noalloc", "ddl_set_launch_mode", "ddl_set_trace", "ddl_read_device_status", "ddl_status_string",
             "ddl_last_cuda_error")
 
 
@@ -101,6 +101,7 @@ def load(build_if_missing: bool = False):
         lib.ddl_stack_decode_noalloc.argtypes = [P(Shape), ctypes.c_int, P(LayerW), P(KV), i32, i32,
                                                  i64, vp, vp, vp, vp, vp]
         lib.ddl_set_launch_mode.argtypes = [i32]
+        lib.ddl_set_trace.argtypes = [vp, sz]
         lib.ddl_read_device_status.argtypes = [vp, P(Shape), i32, i64, P(i32), vp]
         lib.ddl_status_string.argtypes = [ctypes.c_int]
         lib.ddl_status_string.restype = ctypes.c_char_p
@@ -267,6 +268,15 @@ def ddl_layer_decode(shape: Shape, wtype: int, layer: dict, kv: tuple, pos: int,
 
 def ddl_set_launch_mode(mode: int):
     _check("ddl_set_launch_mode", load().ddl_set_launch_mode(mode))
+
+
+def ddl_set_trace(buf: torch.Tensor | None):
+    """Turn the per-(stage, CTA) %globaltimer trace on (a device tensor) or off."""
+    lib = load()
+    if buf is None:
+        _check("ddl_set_trace", lib.ddl_set_trace(None, 0))
+    else:
+        _check("ddl_set_trace", lib.ddl_set_trace(_ptr(buf), buf.numel() * buf.element_size()))
 
 
 def ddl_read_device_status(workspace: torch.Tensor, shape: Shape, B: int, s_max: int,

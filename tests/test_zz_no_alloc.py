@@ -48,9 +48,11 @@ def test_noalloc_matches_workspace_entry_point_twice():
 
 def test_noalloc_rejects_problems_larger_than_its_scratch():
     lib = ddl.load(build_if_missing=True)
-    big = ddl.Shape(8192, 64, 8, 128, 262144, 1e-6, 5e5)
-    need = ddl.ddl_workspace_bytes(big, 4, 1024)
-    assert need > (32 << 20)
+    # the first supported shape that needs more scratch than the static array
+    cands = [ddl.Shape(32768, 64, 8, 128, 65536, 1e-6, 5e5), ddl.Shape(16384, 64, 64, 128, 65536, 1e-6, 5e5),
+             ddl.Shape(32768, 128, 16, 128, 65536, 1e-6, 5e5)]
+    big = next((c for c in cands if lib.ddl_workspace_bytes(ctypes.byref(c), 4, 1024) > (32 << 20)), None)
+    assert big is not None
     lw = (ddl.LayerW * 1)(ddl.LayerW(256, 256, 256))
     kv = (ddl.KV * 1)(ddl.KV(256, 256, 1024))
     st = lib.ddl_stack_decode_noalloc(ctypes.byref(big), ddl.INT4, lw, kv, 1, 4, 0, None,
