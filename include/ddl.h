@@ -202,13 +202,14 @@ int ddl_stack_decode_noalloc(const ddl_shape* shape, ddl_wtype wtype, const ddl_
 int ddl_set_launch_mode(int32_t mode);
 
 /* Tracing: when device_buf (device memory) is not NULL, every later decode
- * call of at most 96 layers whose trace fits in `bytes` writes %globaltimer
- * stamps (uint64 ns) per (stage, CTA): stage start, end of the stage
- * prologue, end of each of the 8 warps' streams, stage end, then four steps
- * inside a weight stage's prologue (copies issued, sum of squares loaded,
- * copies landed, scale known) -- 15 words per (stage, CTA), stages in order
- * (layer * 5 + stage: QKV, ATT, WO, GU, DOWN).  Needs L * 5 * SMs * 15 * 8
- * bytes.  NULL turns tracing off. */
+ * call of at most 96 layers whose trace fits in `bytes` writes 16 uint64
+ * words per (stage, CTA), stages in order (layer * 5 + stage: QKV, ATT, WO,
+ * GU, DOWN): word 0 = %globaltimer (ns) at the stage start; words 1..14 =
+ * %clock64 (SM cycles) at the end of the stage prologue, the end of each of
+ * the 8 warps' streams, the stage end, and four steps inside a weight
+ * stage's prologue (copies issued, sum of squares loaded, copies landed,
+ * scale known); word 15 = %clock64 at the stage start.  Needs
+ * L * 5 * SMs * 16 * 8 bytes.  NULL turns tracing off. */
 int ddl_set_trace(void* device_buf, size_t bytes);
 
 /* Synchronize `stream` and read the device status word of the last decode

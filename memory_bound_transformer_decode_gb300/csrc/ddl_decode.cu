@@ -34,20 +34,35 @@
 namespace ddl {
 
 // ------------------------------------------------------------------ shared memory
+// The parameters that are read with a run-time index (per layer, per matrix,
+// per RoPE frequency) are copied to shared memory at launch, so that a stage
+// start does not wait on constant-cache misses.
+struct SParams {
+  MatGeom mg[4];
+  float rope[64][2];
+  LayerDev layers[MAX_LAYERS];
+};
+extern __shared__ __align__(1024) uint8_t g_smem[];
 constexpr int SM_RING = 0;
 constexpr int SM_RING_BYTES = NW * DEPTH * SLOT_BYTES;
 constexpr int SM_BARS = SM_RING_BYTES;
-constexpr int SM_PBAR = SM_BARS + NW * DEPTH * 8;  // the prologue's bulk-copy barrier
 constexpr int SM_SCR = SM_BARS + 512;
 constexpr int XF_BYTES = XF_CHUNKS * GC * 4 * 2 * 4 * 8;  // x fragments: chunks x batch <= 8
 constexpr int SX_BYTES = XF_CHUNKS * GC * MAX_B * 4;        // per-group sums of x
 constexpr int SM_SCR_BYTES = 70 * 1024;
-constexpr int SM_MISC = SM_SCR + SM_SCR_BYTES;
+constexpr int SM_NW = SM_SCR + SM_SCR_BYTES;               // the panel's norm weights (bf16)
+constexpr int SM_NW_BYTES = XF_CHUNKS * GC * DDL_GROUP * 2;
+constexpr int SM_MISC = SM_NW + SM_NW_BYTES;
 constexpr int SM_MISC_BYTES = 2048;
-constexpr int SM_TOTAL = SM_MISC + SM_MISC_BYTES;
+constexpr int SM_SPAR = SM_MISC + SM_MISC_BYTES;             // copies of the indexed parameters
+constexpr int SM_CTX = SM_SPAR + (((int)sizeof(SParams) + 255) & ~255);  // stage context, warp cursors
+constexpr int SM_CTX_BYTES = 2048;
+constexpr int SM_TOTAL = SM_CTX + SM_CTX_BYTES;
 static_assert(XF_BYTES + SX_BYTES + NW * 32 * 4 <= SM_SCR_BYTES, "x fragments do not fit");
 static_assert(NW * 2 * (MAX_GH * (128 + 2) + 3) * 4 <= SM_SCR_BYTES, "attention records do not fit");
 static_assert(SM_TOTAL <= 227 * 1024, "shared memory budget");
+static_assert(SM_SPAR % 16 == 0, "parameter copy alignment");
+__device__ __forceinline__ const SParams& sp() { return *reinterpret_cast<const SParams*>(g_smem + SM_SPAR); }
 
 struct Misc {
   float rnorm[MAX_B];
@@ -59,7 +74,6 @@ struct Misc {
   int seg_n[NW];
   long long seg_first[NW], seg_last[NW];
   long long mseq[8];       // sequences this CTA merges last
-  uint32_t pphase;         // completed phases of the prologue barrier
 };
 static_assert(sizeof(Misc) <= SM_MISC_BYTES, "misc");
 
@@ -90,6 +104,30 @@ struct Ring {
   __device__ __forceinline__ uint32_t parity(uint32_t n) const { return (n / DEPTH) & 1; }
 };
 
+// Per-stage constants of a GEMV stage, read once from the parameters.
+struct GemvCtx {
+  MatGeom m;
+  int st, layer, gl;
+  const float* xin32;     // layer input (fp32) or NULL
+  const uint16_t* xin16;  // layer input (bf16) when xin32 is NULL (QKV / WO of layer 0)
+  uint16_t* kc;           // K, V caches (QKV epilogue)
+  uint16_t* vc;
+  float* zout;            // residual output of this layer (DOWN)
+  bool final_layer;
+  int p, cl;              // this CTA's panel and its index among the panel's CTAs
+};
+
+// CTA-wide state in shared memory, so that nothing lives in local memory:
+// the current weight stage's context and each warp's ring and producer
+// cursor between stages.
+struct Ctx {
+  GemvCtx E;
+  Ring ring[NW];
+  Cursor cur[NW];
+};
+static_assert(sizeof(Ctx) <= SM_CTX_BYTES, "context");
+__device__ __forceinline__ Ctx& ctx() { return *reinterpret_cast<Ctx*>(g_smem + SM_CTX); }
+
 // ------------------------------------------------------------------ work split
 __device__ __forceinline__ void att_range(const Params& P, int64_t& lo, int64_t& hi) {
   const int64_t Ta = (int64_t)P.B * P.Hkv * P.nt_att, C = gridDim.x;
@@ -99,9 +137,9 @@ __device__ __forceinline__ void att_range(const Params& P, int64_t& lo, int64_t&
   hi = clo + range_lo(chi - clo, NW, w + 1);
 }
 template <int WT>
-__device__ __forceinline__ void cursor_enter(const Params& P, Cursor& c, int64_t wg, int64_t W) {
+__device__ __noinline__ void cursor_enter(const Params& P, Cursor& c, int64_t wg, int64_t W) {
   const int st = c.s % NSTAGE;
-  const LayerDev& Ld = P.layers[c.s / NSTAGE];
+  const LayerDev& Ld = sp().layers[c.s / NSTAGE];
   if (st == ST_ATT) {
     att_range(P, c.pos, c.end);
     c.pos *= 2;
@@ -109,7 +147,7 @@ __device__ __forceinline__ void cursor_enter(const Params& P, Cursor& c, int64_t
     c.kbase = Ld.kc;
     c.vbase = Ld.vc;
   } else {
-    const MatGeom& m = P.mg[stage_mat(st)];
+    const MatGeom& m = sp().mg[stage_mat(st)];
     const int p = panel_of_cta(m, blockIdx.x);
     uint32_t lo, hi;
     warp_work(m, p, blockIdx.x - m.pc[p], threadIdx.x >> 5, NW, lo, hi);
@@ -134,7 +172,15 @@ __device__ __forceinline__ bool cursor_next(const Params& P, Cursor& c, int64_t 
                                             SlotDesc& d) {
   while (c.pos >= c.end) {
     if (++c.s >= P.stage_end) return false;
-    cursor_enter<WT>(P, c, wg, W);
+    // through this warp's shared copy: a reference to registers would put
+    // the cursor in local memory
+    Cursor& cs = ctx().cur[threadIdx.x >> 5];
+    __syncwarp();
+    cs = c;
+    __syncwarp();
+    cursor_enter<WT>(P, cs, wg, W);
+    __syncwarp();
+    c = cs;
   }
   if (c.s % NSTAGE == ST_ATT) {
     const int64_t tile = c.pos >> 1;
@@ -219,25 +265,25 @@ __device__ __forceinline__ float4 bf16x4_f32(uint2 u) {
   return make_float4(bf16lo_f32(u.x), bf16hi_f32(u.x), bf16lo_f32(u.y), bf16hi_f32(u.y));
 }
 
-// Optional trace: %globaltimer stamps per (stage, CTA): start, end of the
-// prologue, end of each warp's stream, end of the stage.
+// Optional trace per (stage, CTA): word 0 is %globaltimer at the stage start
+// (comparable across SMs), the last word %clock64 at the same moment, and the
+// others %clock64 at later events (end of the prologue, end of each warp's
+// stream, end of the stage, prologue steps), so that intervals within a CTA
+// are exact to a cycle.
 __device__ __forceinline__ void trace_stamp(const Params& P, int s, int slot) {
-  if (P.trace)
-    P.trace[((int64_t)(s - P.stage_begin) * gridDim.x + blockIdx.x) * TRACE_WORDS + slot] = globaltimer();
+  if (P.trace) {
+    uint64_t* w = P.trace + ((int64_t)(s - P.stage_begin) * gridDim.x + blockIdx.x) * TRACE_WORDS;
+    if (slot == 0) {
+      const uint64_t c = clock64();
+      w[TRACE_WORDS - 1] = c;
+      w[0] = globaltimer();
+    } else {
+      w[slot] = clock64();
+    }
+  }
 }
 
-// Per-stage constants of a GEMV stage, read once from the parameters.
-struct GemvCtx {
-  MatGeom m;
-  int st, layer, gl;
-  const float* xin32;     // layer input (fp32) or NULL
-  const uint16_t* xin16;  // layer input (bf16) when xin32 is NULL (QKV / WO of layer 0)
-  uint16_t* kc;           // K, V caches (QKV epilogue)
-  uint16_t* vc;
-  float* zout;            // residual output of this layer (DOWN)
-  bool final_layer;
-  int p, cl;              // this CTA's panel and its index among the panel's CTAs
-};
+
 
 // ------------------------------------------------------------------ GEMV prologue
 // Stages this CTA's panel of the activation (k-chunks pk[p]..pk[p+1]-1) as
@@ -246,14 +292,16 @@ struct GemvCtx {
 // carried to ~22 bits.  Also computes the RMSNorm factor r (QKV, GU), the
 // power-of-two scale 2^e that brings the panel's largest |x| to [2^11, 2^12),
 // and, for INT4, the per-group sums of x used to remove the +8 code offset.
-// One round trip: every thread issues a 256-byte bulk copy of one (group,
-// sequence) of x into shared memory while the sum of squares is loaded; the
-// conversion then runs in place, group by group, from shared memory.
-// Shared layout of a group (B x 256 bytes): raw x[b][64] fp32, later the
-// fragments [j][column 2b+h][lane t][register half] of 2 x fp16.
+// One round trip: cp.async copies (through L1, so that they do not queue
+// behind the weight ring's bulk copies in the TMA unit) bring every (group,
+// sequence) of x into 256 bytes of shared memory and every group of norm
+// weights into 128 bytes.  When the panel is the whole vector the sum of
+// squares comes from the staged x; otherwise it is loaded meanwhile.  Item
+// it = ((group slot * B + b) * 16 + quad) is one four-column quad of x, at
+// byte it*16 of the staged x (fp32).  The conversion runs in rounds of whole
+// groups: read, block barrier, write the fragments in place.
 template <int HD, int WT>
-__device__ void gemv_prologue(const Params& P, const GemvCtx& E, uint8_t* smem, Misc& M,
-                              uint32_t pbar) {
+__device__ __noinline__ void gemv_prologue(const Params& P, const GemvCtx& E, uint8_t* smem, Misc& M) {
   const MatGeom& m = E.m;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int B = P.B;
@@ -261,7 +309,7 @@ __device__ void gemv_prologue(const Params& P, const GemvCtx& E, uint8_t* smem, 
   const float* x32 = nullptr;
   const uint16_t* x16 = nullptr;
   const uint16_t* nw = nullptr;
-  const LayerDev& Ld = P.layers[E.layer];
+  const LayerDev& Ld = sp().layers[E.layer];
   switch (E.st) {
     case ST_QKV: nw = Ld.norm1; x32 = E.xin32; x16 = E.xin16; break;
     case ST_WO: x32 = P.attn; break;
@@ -270,36 +318,39 @@ __device__ void gemv_prologue(const Params& P, const GemvCtx& E, uint8_t* smem, 
   }
   const int K = m.K;
   const int ngr = nkc * GC;  // group slots of the panel (the last chunk may use fewer)
+  const int n_items = ngr * B * 16;
+  const int kbase = kc_lo * GC * DDL_GROUP;
+  const bool whole = nkc == m.Sk;  // the panel is the whole vector
   uint8_t* raw = smem + SM_SCR;
-  const uint32_t gbytes = x32 ? 256u : 128u;  // bytes of one (group, sequence) of x in memory
-  // 1. bulk copies: item = (group slot, sequence).  Earlier generic accesses
-  //    to the scratch area (any thread) come before the copies overwrite it.
-  fence_proxy_async_smem();
+  uint8_t* nws = smem + SM_NW;
+  // 1. copies: 16-byte pieces of x (16 per (group, sequence) for fp32, 8 for
+  //    bf16) and of the norm weights (8 per group).  Earlier readers of the
+  //    areas (any thread) are done first.
   __syncthreads();
   {
-    uint32_t nbytes = 0;
-    for (int kcl = 0; kcl < nkc; ++kcl) nbytes += (uint32_t)chunk_groups(m, kc_lo + kcl) * gbytes * B;
-    if (tid == 0) mbar_arrive_expect_tx(pbar, nbytes);
-    for (int it = tid; it < ngr * B; it += NTHREADS) {
-      const int gs = it / B, b = it - gs * B, kcl = gs / GC, gi = gs - kcl * GC;
-      if (gi < chunk_groups(m, kc_lo + kcl)) {
-        const int64_t k = (int64_t)(kc_lo + kcl) * GC * DDL_GROUP + (int64_t)gi * DDL_GROUP;
-        const void* src = x32 ? (const void*)(x32 + (int64_t)b * K + k) : (const void*)(x16 + (int64_t)b * K + k);
-        bulk_g2s(smem_addr(raw + (size_t)it * 256), src, gbytes, pbar);
+    const int xp = x32 ? 16 : 8;  // pieces per (group, sequence)
+    const int nx = ngr * B * xp, nn = nw ? ngr * 8 : 0;
+    for (int i = tid; i < nx + nn; i += NTHREADS) {
+      if (i < nx) {
+        const int gsb = i / xp, q = i - gsb * xp, gs = gsb / B, b = gsb - gs * B;
+        if ((gs % GC) < chunk_groups(m, kc_lo + gs / GC)) {
+          const int64_t k = kbase + (int64_t)gs * DDL_GROUP;
+          const void* src = x32 ? (const void*)(x32 + (int64_t)b * K + k + q * 4)
+                                : (const void*)(x16 + (int64_t)b * K + k + q * 8);
+          cp_async16(smem_addr(raw + (size_t)gsb * 256 + q * 16), src);
+        }
+      } else {
+        const int j = i - nx, gs = j >> 3, q = j & 7;
+        if ((gs % GC) < chunk_groups(m, kc_lo + gs / GC))
+          cp_async16(smem_addr(nws + (size_t)gs * 128 + q * 16), nw + kbase + (int64_t)gs * DDL_GROUP + q * 8);
       }
     }
   }
   if (tid == 0) trace_stamp(P, E.layer * NSTAGE + E.st, NW + 3);
-  // 2. meanwhile: sum of squares over the whole vector (norm stages) and the
-  //    panel's norm weights into L1
-  if (nw) {
-    const int k0 = kc_lo * GC * DDL_GROUP, k1 = min(K, (kc_lo + nkc) * GC * DDL_GROUP);
-    for (int k = k0 + tid * 64; k < k1; k += NTHREADS * 64)
-      asm volatile("prefetch.global.L1 [%0];" ::"l"(nw + k));
-  }
-  for (int b = 0; b < B; ++b) {
-    float ss = 0.f;
-    if (nw) {
+  // 2. meanwhile (panel not the whole vector): the sum of squares
+  if (nw && !whole) {
+    for (int b = 0; b < B; ++b) {
+      float ss = 0.f;
       const int nq = K / 4;
       for (int q0 = tid; q0 < nq; q0 += 8 * NTHREADS) {
         float4 v[8];
@@ -314,63 +365,46 @@ __device__ void gemv_prologue(const Params& P, const GemvCtx& E, uint8_t* smem, 
         for (int u = 0; u < 8; ++u)
           ss = fmaf(v[u].x, v[u].x, fmaf(v[u].y, v[u].y, fmaf(v[u].z, v[u].z, fmaf(v[u].w, v[u].w, ss))));
       }
+      ss = warp_sum(ss);
+      if (lane == 0) M.red[warp][2 * b] = ss;
     }
-    ss = warp_sum(ss);
-    if (lane == 0) M.red[warp][2 * b] = ss;
   }
   if (tid == 0) trace_stamp(P, E.layer * NSTAGE + E.st, NW + 4);
-  const uint32_t parity = M.pphase & 1u;
-  if (!mbar_wait_warp(pbar, parity, P.ctrl + 1)) M.abort = 1;
+  cp_async_wait_all();
+  __syncthreads();
   if (tid == 0) trace_stamp(P, E.layer * NSTAGE + E.st, NW + 5);
-  // 3. pass A: x <- x * w in place (fp32), max |x| per sequence.  Lane l of
-  //    the warp owning a group handles columns 2l, 2l+1 of every sequence;
-  //    four groups per step keep their loads in flight together.
-  float mx[MAX_B] = {0.f, 0.f, 0.f, 0.f};
-  for (int gs0 = warp; gs0 < ngr; gs0 += 4 * NW) {
-    float2 w[4], v[4][MAX_B];
-    bool ok[4];
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int gs = gs0 + u * NW, kcl = gs / GC, gi = gs - kcl * GC;
-      ok[u] = gs < ngr && gi < chunk_groups(m, kc_lo + kcl);
-      w[u] = make_float2(1.f, 1.f);
-      if (ok[u] && nw) {
-        const int k = (kc_lo + kcl) * GC * DDL_GROUP + gi * DDL_GROUP + 2 * lane;
-        const uint32_t wb = __ldg(reinterpret_cast<const uint32_t*>(nw + k));
-        w[u] = make_float2(bf16lo_f32(wb), bf16hi_f32(wb));
-      }
-#pragma unroll
-      for (int b = 0; b < MAX_B; ++b) {
-        v[u][b] = make_float2(0.f, 0.f);
-        if (ok[u] && b < B) {
-          const uint8_t* g = raw + ((size_t)gs * B + b) * 256;
-          if (x32) v[u][b] = *reinterpret_cast<const float2*>(g + lane * 8);
-          else {
-            const uint32_t q = *reinterpret_cast<const uint32_t*>(g + lane * 4);
-            v[u][b] = make_float2(bf16lo_f32(q), bf16hi_f32(q));
-          }
-        }
-      }
+  // 3. max |x * w| per sequence over the panel (and the sum of squares of x
+  //    when the panel is the whole vector)
+  float mx[MAX_B] = {0.f, 0.f, 0.f, 0.f}, ssq[MAX_B] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
+  for (int it = tid; it < n_items; it += NTHREADS) {
+    const int gsb = it >> 4, q16 = it & 15, gs = gsb / B, b = gsb - gs * B;
+    if ((gs % GC) >= chunk_groups(m, kc_lo + gs / GC)) continue;
+    float4 x = x32 ? *reinterpret_cast<const float4*>(raw + (size_t)it * 16)
+                   : bf16x4_f32(*reinterpret_cast<const uint2*>(raw + (size_t)gsb * 256 + q16 * 8));
+    const float s2 = fmaf(x.x, x.x, fmaf(x.y, x.y, fmaf(x.z, x.z, x.w * x.w)));
+    if (nw) {
+      const float4 w = bf16x4_f32(*reinterpret_cast<const uint2*>(nws + (size_t)gs * 128 + q16 * 8));
+      x = make_float4(x.x * w.x, x.y * w.y, x.z * w.z, x.w * w.w);
     }
-    __syncwarp();
+    const float a = fmaxf(fmaxf(fabsf(x.x), fabsf(x.y)), fmaxf(fabsf(x.z), fabsf(x.w)));
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int gs = gs0 + u * NW;
-#pragma unroll
-      for (int b = 0; b < MAX_B; ++b) {
-        if (ok[u] && b < B) {
-          const float2 x = make_float2(v[u][b].x * w[u].x, v[u][b].y * w[u].y);
-          mx[b] = fmaxf(mx[b], fmaxf(fabsf(x.x), fabsf(x.y)));
-          *reinterpret_cast<float2*>(raw + ((size_t)gs * B + b) * 256 + lane * 8) = x;
-        }
+    for (int bb = 0; bb < MAX_B; ++bb) {
+      if (bb == b) {
+        mx[bb] = fmaxf(mx[bb], a);
+        ssq[bb] += s2;
       }
     }
   }
 #pragma unroll
   for (int b = 0; b < MAX_B; ++b) {
     if (b < B) {
-      const float v = warp_max(mx[b]);
-      if (lane == 0) M.red[warp][2 * b + 1] = v;
+      const float r = warp_max(mx[b]);
+      if (lane == 0) M.red[warp][2 * b + 1] = r;
+      if (nw && whole) {
+        const float q = warp_sum(ssq[b]);
+        if (lane == 0) M.red[warp][2 * b] = q;
+      }
     }
   }
   __syncthreads();
@@ -385,75 +419,64 @@ __device__ void gemv_prologue(const Params& P, const GemvCtx& E, uint8_t* smem, 
     M.escale[tid] = ldexpf(1.0f, e);
     M.edown[tid] = ldexpf(1.0f, -e);
   }
-  if (tid == 0) M.pphase++;
   __syncthreads();
   if (tid == 0) trace_stamp(P, E.layer * NSTAGE + E.st, NW + 6);
-  // 4. pass B: fragments in place.  Columns 2l, 2l+1 (MMA j = l/8) go to
-  //    lane t = l%4, register half (l%8)/4; Sx = sum of hi + lo per sequence.
-  //    Four groups per step.
+  // 4. fragments in place, in rounds of whole groups (up to 4 quads a thread).
+  //    Quad q16 holds columns 4 q16 .. 4 q16 + 3 of its group: MMA j = q16 / 4,
+  //    register half (q16 / 2) % 2, lanes t0 = 2 (q16 % 2) and t0 + 1.
+  //    Sx = sum of hi + lo over the group's 16 quads (16 consecutive lanes).
   float* Sx = reinterpret_cast<float*>(smem + SM_SCR + XF_BYTES);
-  const int j = lane >> 3, half = (lane >> 2) & 1, t = lane & 3;
-  for (int gs0 = warp; gs0 < ngr; gs0 += 4 * NW) {
-    float2 v[4][MAX_B];
+  constexpr bool f16 = WT == DDL_W_INT4;
+  const int ipr = (4 * NTHREADS / (16 * B)) * 16 * B;  // items per round: whole groups
+  for (int r0 = 0; r0 < n_items; r0 += ipr) {
+    float4 v[4];
     bool ok[4];
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
-      const int gs = gs0 + u * NW, kcl = gs / GC, gi = gs - kcl * GC;
-      ok[u] = gs < ngr && gi < chunk_groups(m, kc_lo + kcl);
-#pragma unroll
-      for (int b = 0; b < MAX_B; ++b)
-        v[u][b] = (ok[u] && b < B) ? *reinterpret_cast<const float2*>(raw + ((size_t)gs * B + b) * 256 + lane * 8)
-                                   : make_float2(0.f, 0.f);
+      const int iu = u * NTHREADS + tid, it = r0 + iu;
+      const int gsb = it >> 4, q16 = it & 15, gs = gsb / B;
+      ok[u] = iu < ipr && it < n_items && (gs % GC) < chunk_groups(m, kc_lo + gs / GC);
+      v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (ok[u]) {
+        const float sc = M.edown[gsb - gs * B];
+        float4 x = x32 ? *reinterpret_cast<const float4*>(raw + (size_t)it * 16)
+                       : bf16x4_f32(*reinterpret_cast<const uint2*>(raw + (size_t)gsb * 256 + q16 * 8));
+        const float4 w = nw ? bf16x4_f32(*reinterpret_cast<const uint2*>(nws + (size_t)gs * 128 + q16 * 8))
+                            : make_float4(1.f, 1.f, 1.f, 1.f);
+        v[u] = make_float4(x.x * w.x * sc, x.y * w.y * sc, x.z * w.z * sc, x.w * w.w * sc);
+      }
     }
-    __syncwarp();
-    float part[4][MAX_B];
+    __syncthreads();
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
-      const int gs = gs0 + u * NW;
-      uint32_t* f = reinterpret_cast<uint32_t*>(raw + (size_t)gs * B * 256);
+      const int it = r0 + u * NTHREADS + tid;
+      const int gsb = it >> 4, q16 = it & 15, gs = gsb / B, b = gsb - gs * B;
+      float part = 0.f;
+      if (ok[u]) {
+        const float xv[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+        float hi[4], lo[4];
 #pragma unroll
-      for (int b = 0; b < MAX_B; ++b) {
-        part[u][b] = 0.f;
-        if (ok[u] && b < B) {
-          const float sc = M.edown[b];
-          const float x0 = v[u][b].x * sc, x1 = v[u][b].y * sc;
-          float h0, h1, l0, l1;
-          uint32_t hw, lw;
-          if (WT == DDL_W_INT4) {
-            h0 = __half2float(__float2half_rn(x0));
-            h1 = __half2float(__float2half_rn(x1));
-            l0 = __half2float(__float2half_rn(x0 - h0));
-            l1 = __half2float(__float2half_rn(x1 - h1));
-            hw = pack_f16x2(h0, h1);
-            lw = pack_f16x2(l0, l1);
+        for (int e = 0; e < 4; ++e) {
+          if (f16) {
+            hi[e] = __half2float(__float2half_rn(xv[e]));
+            lo[e] = __half2float(__float2half_rn(xv[e] - hi[e]));
           } else {
-            h0 = __bfloat162float(__float2bfloat16_rn(x0));
-            h1 = __bfloat162float(__float2bfloat16_rn(x1));
-            l0 = __bfloat162float(__float2bfloat16_rn(x0 - h0));
-            l1 = __bfloat162float(__float2bfloat16_rn(x1 - h1));
-            hw = pack_bf16x2(h0, h1);
-            lw = pack_bf16x2(l0, l1);
+            hi[e] = __bfloat162float(__float2bfloat16_rn(xv[e]));
+            lo[e] = __bfloat162float(__float2bfloat16_rn(xv[e] - hi[e]));
           }
-          f[((j * 2 * B + 2 * b) * 4 + t) * 2 + half] = hw;
-          f[((j * 2 * B + 2 * b + 1) * 4 + t) * 2 + half] = lw;
-          part[u][b] = (h0 + l0) + (h1 + l1);
         }
+        part = ((hi[0] + lo[0]) + (hi[1] + lo[1])) + ((hi[2] + lo[2]) + (hi[3] + lo[3]));
+        const int j = q16 >> 2, half = (q16 >> 1) & 1, t0 = 2 * (q16 & 1);
+        uint32_t* f = reinterpret_cast<uint32_t*>(raw + (size_t)gs * B * 256);
+        const int ch = (j * 2 * B + 2 * b) * 4;  // (j, column 2b): 4 lanes x 2 halves
+        f[(ch + t0) * 2 + half] = f16 ? pack_f16x2(hi[0], hi[1]) : pack_bf16x2(hi[0], hi[1]);
+        f[(ch + t0 + 1) * 2 + half] = f16 ? pack_f16x2(hi[2], hi[3]) : pack_bf16x2(hi[2], hi[3]);
+        f[(ch + 4 + t0) * 2 + half] = f16 ? pack_f16x2(lo[0], lo[1]) : pack_bf16x2(lo[0], lo[1]);
+        f[(ch + 4 + t0 + 1) * 2 + half] = f16 ? pack_f16x2(lo[2], lo[3]) : pack_bf16x2(lo[2], lo[3]);
       }
-    }
 #pragma unroll
-    for (int o = 16; o; o >>= 1)
-#pragma unroll
-      for (int u = 0; u < 4; ++u)
-#pragma unroll
-        for (int b = 0; b < MAX_B; ++b) part[u][b] += __shfl_xor_sync(FULL, part[u][b], o);
-    if (lane == 0) {
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int gs = gs0 + u * NW;
-#pragma unroll
-        for (int b = 0; b < MAX_B; ++b)
-          if (ok[u] && b < B) Sx[gs * MAX_B + b] = part[u][b];
-      }
+      for (int o = 8; o; o >>= 1) part += __shfl_xor_sync(FULL, part, o);
+      if (q16 == 0 && ok[u]) Sx[gs * MAX_B + b] = part;
     }
   }
   __syncthreads();
@@ -462,7 +485,7 @@ __device__ void gemv_prologue(const Params& P, const GemvCtx& E, uint8_t* smem, 
 // ------------------------------------------------------------------ GEMV epilogues
 // Lane (g, t) holds rows g and g+8 of tile T for sequence t.
 template <int HD>
-__device__ void gemv_epilogue(const Params& P, const GemvCtx& E, int T, float v0, float v1,
+__device__ __noinline__ void gemv_epilogue(const Params& P, const GemvCtx& E, int T, float v0, float v1,
                               const Misc& M) {
   const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
   if (t >= P.B) return;
@@ -472,7 +495,7 @@ __device__ void gemv_epilogue(const Params& P, const GemvCtx& E, int T, float v0
     v1 *= r;
     const int tph = HD / 16, head = T / tph, i = 8 * (T % tph) + g;
     if (head < P.Hq + P.Hkv) {  // RoPE on q and k: pair (i, i + hd/2)
-      const float c = P.rope[i][0], s = P.rope[i][1], a = v0, b = v1;
+      const float c = sp().rope[i][0], s = sp().rope[i][1], a = v0, b = v1;
       v0 = a * c - b * s;
       v1 = a * s + b * c;
     }
@@ -521,27 +544,20 @@ __device__ void gemv_epilogue(const Params& P, const GemvCtx& E, int T, float v0
 template <int HD>
 __device__ __noinline__ void gemv_fixup(const Params& P, const GemvCtx& E, int T, const Misc& M) {
   const MatGeom& m = E.m;
-  const int lane = threadIdx.x & 31, nslot = m.NP * m.J;
-  const float2* part = reinterpret_cast<const float2*>(P.gpart) + (int64_t)T * nslot * 32 + lane;
+  const int lane = threadIdx.x & 31;
+  const float2* part = reinterpret_cast<const float2*>(P.gpart) + (int64_t)T * m.NP * m.J * 32 + lane;
   float s0 = 0.f, s1 = 0.f;
-  for (int f0 = 0; f0 < nslot; f0 += 8) {
-    float2 v[8];
-#pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const int f = f0 + u, p = f / m.J, j = f - p * m.J;
-      bool ok = f < nslot;
-      if (ok) {
-        const uint32_t Gp = panel_groups(m, p);
-        const uint32_t v0 = work_owner(m, p, (uint32_t)T * Gp, NW);
-        const uint32_t v1 = work_owner(m, p, (uint32_t)(T + 1) * Gp - 1, NW);
-        ok = v0 + j <= v1 && !warp_empty(m, p, v0 + j, NW);
-      }
-      v[u] = ok ? __ldcg(part + (int64_t)f * 32) : make_float2(0.f, 0.f);
-    }
-#pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      s0 += v[u].x;
-      s1 += v[u].y;
+  for (int p = 0; p < m.NP; ++p) {  // the tile's contributors in panel p: warps v0..v1
+    const uint32_t Gp = panel_groups(m, p);
+    const uint32_t v0 = work_owner(m, p, (uint32_t)T * Gp, NW);
+    const uint32_t v1 = work_owner(m, p, (uint32_t)(T + 1) * Gp - 1, NW);
+    const float2* pp = part + (int64_t)p * m.J * 32;
+#pragma unroll 4
+    for (uint32_t v = v0; v <= v1; ++v) {
+      if (warp_empty(m, p, v, NW)) continue;
+      const float2 x = __ldcg(pp + (int64_t)(v - v0) * 32);
+      s0 += x.x;
+      s1 += x.y;
     }
   }
   gemv_epilogue<HD>(P, E, T, s0, s1, M);
@@ -611,26 +627,29 @@ template <int HD, int WT>
 __device__ __noinline__ bool stage_gemv(const Params& P, int layer, int st, Ring& Rm, Cursor& prodm,
                                         int64_t wg, int64_t W, uint8_t* smem, Misc& M,
                                         uint64_t policy) {
+  __syncwarp();
   Ring R = Rm;
   Cursor prod = prodm;
   const bool ok = stage_gemv_body<HD, WT>(P, layer, st, R, prod, wg, W, smem, M, policy);
+  __syncwarp();
   Rm = R;
   prodm = prod;
+  __syncwarp();
   return ok;
 }
 template <int HD, int WT>
 __device__ __forceinline__ bool stage_gemv_body(const Params& P, int layer, int st, Ring& R,
                                                 Cursor& prod, int64_t wg, int64_t W, uint8_t* smem,
                                                 Misc& M, uint64_t policy) {
-  GemvCtx E;
-  E.m = P.mg[stage_mat(st)];
-  E.st = st;
-  E.layer = layer;
-  E.gl = P.l0 + layer;
-  E.p = panel_of_cta(E.m, blockIdx.x);
-  E.cl = blockIdx.x - E.m.pc[E.p];
-  {
-    const LayerDev& Ld = P.layers[layer];
+  GemvCtx& E = ctx().E;  // filled by thread 0; every warp reads it from shared memory
+  if (threadIdx.x == 0) {
+    E.m = sp().mg[stage_mat(st)];
+    E.st = st;
+    E.layer = layer;
+    E.gl = P.l0 + layer;
+    E.p = panel_of_cta(E.m, blockIdx.x);
+    E.cl = blockIdx.x - E.m.pc[E.p];
+    const LayerDev& Ld = sp().layers[layer];
     E.kc = Ld.kc;
     E.vc = Ld.vc;
     E.xin32 = nullptr;
@@ -644,8 +663,9 @@ __device__ __forceinline__ bool stage_gemv_body(const Params& P, int layer, int 
     E.zout = P.Z + (int64_t)(E.gl & 1) * P.B * P.D;
     E.final_layer = P.final_last && layer == P.L - 1;
   }
+  __syncthreads();
   const MatGeom& m = E.m;
-  gemv_prologue<HD, WT>(P, E, smem, M, smem_addr(smem + SM_PBAR));
+  gemv_prologue<HD, WT>(P, E, smem, M);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
   if (threadIdx.x == 0) trace_stamp(P, layer * NSTAGE + st, 1);
   uint32_t lo, hi;
@@ -667,7 +687,6 @@ __device__ __forceinline__ bool stage_gemv_body(const Params& P, int layer, int 
   float acc0 = 0.f, acc1 = 0.f, tac0 = 0.f, tac1 = 0.f;
   uint32_t nblk = 0;
   constexpr int PER = WT == DDL_W_INT4 ? BLKS_PER_SLOT : BF16_BLKS_PER_SLOT;
-  const uint32_t jst1 = jstride, jst2 = 2 * jstride, jst3 = 3 * jstride;
   for (uint32_t b = lo; b < hi;) {
     // a slot holds nb consecutive groups gi.. of unit (kc, T) (see cursor_next)
     int nb = (int)(hi - b < (uint32_t)PER ? hi - b : (uint32_t)PER);
@@ -680,51 +699,66 @@ __device__ __forceinline__ bool stage_gemv_body(const Params& P, int layer, int 
     const int kcl = kc - pk0;
     const uint32_t xb = xf_lane + kcl * kstride + gi * gstride;
     const uint32_t sb = sx_lane + ((kcl * GC + gi) * MAX_B) * 4;
+    // All shared loads of the slot first, then the MMAs in (j, block) order
+    // so that consecutive MMAs accumulate into different blocks.  Blocks
+    // i >= nb get zero x fragments (and zero scale and sum of x), so they add
+    // nothing whatever stale codes the slot holds.
     float c[PER][4];
+    uint2 bx[PER][4];
 #pragma unroll
     for (int i = 0; i < PER; ++i) {
       c[i][0] = c[i][1] = c[i][2] = c[i][3] = 0.f;
-      if (nb == PER || i < nb) {
-        const uint32_t xi = xb + i * gstride;
-        const uint32_t jo[4] = {0u, jst1, jst2, jst3};
-        if (WT == DDL_W_INT4) {
-          const uint4 wv = lds128(slot + i * BLK_BYTES + lane * 16);
-          const uint32_t ws[4] = {wv.x, wv.y, wv.z, wv.w};
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const uint32_t w = ws[j], w8 = w >> 8;
-            const uint32_t a0 = lop3_merge(w, 0x000F000Fu, 0x64086408u);
-            const uint32_t a1 = lop3_merge(w, 0x00F000F0u, 0x64806480u);
-            const uint32_t a2 = lop3_merge(w8, 0x000F000Fu, 0x64086408u);
-            const uint32_t a3 = lop3_merge(w8, 0x00F000F0u, 0x64806480u);
-            // lanes g >= 2B read unrelated fragments: they only feed C columns >= 2B, never used
-            const uint2 bf = lds64(xi + jo[j]);
-            mma_f16(c[i], a0, a1, a2, a3, bf.x, bf.y);
-          }
-        } else {
+      for (int j = 0; j < 4; ++j)
+        bx[i][j] = i < nb ? lds64(xb + i * gstride + j * jstride) : make_uint2(0u, 0u);
+    }
+    if (WT == DDL_W_INT4) {
+      uint4 wv[PER];
+      uint32_t sc[PER];
+      float sx[PER];
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const uint4 av = lds128(slot + i * BF16_BLK_BYTES + j * 512 + lane * 16);
-            const uint2 bf = lds64(xi + jo[j]);
-            mma_bf16(c[i], av.x, av.y, av.z, av.w, bf.x, bf.y);
-          }
+      for (int i = 0; i < PER; ++i) {
+        wv[i] = lds128(slot + i * BLK_BYTES + lane * 16);
+        sc[i] = i < nb ? lds32(slot + BLKS_PER_SLOT * BLK_BYTES + i * SCL_BYTES + g * 4) : 0u;
+        sx[i] = i < nb ? lds_f32(sb + i * (MAX_B * 4)) : 0.f;
+      }
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+#pragma unroll
+        for (int i = 0; i < PER; ++i) {
+          const uint32_t w = j == 0 ? wv[i].x : j == 1 ? wv[i].y : j == 2 ? wv[i].z : wv[i].w;
+          const uint32_t w8 = w >> 8;
+          const uint32_t a0 = lop3_merge(w, 0x000F000Fu, 0x64086408u);
+          const uint32_t a1 = lop3_merge(w, 0x00F000F0u, 0x64806480u);
+          const uint32_t a2 = lop3_merge(w8, 0x000F000Fu, 0x64086408u);
+          const uint32_t a3 = lop3_merge(w8, 0x00F000F0u, 0x64806480u);
+          // lanes g >= 2B read unrelated fragments: they only feed C columns >= 2B, never used
+          mma_f16(c[i], a0, a1, a2, a3, bx[i][j].x, bx[i][j].y);
         }
       }
-    }
+      // rows g hold 1024 + (q+8), rows g+8 hold 1024 + 16 (q+8):
+      // sum q x = v - 1032 Sx  and  (v - 1152 Sx) / 16
 #pragma unroll
-    for (int i = 0; i < PER; ++i) {
-      if (nb == PER || i < nb) {
-        if (WT == DDL_W_INT4) {
-          // rows g hold 1024 + (q+8), rows g+8 hold 1024 + 16 (q+8):
-          // sum q x = v - 1032 Sx  and  (v - 1152 Sx) / 16
-          const uint32_t sc = lds32(slot + BLKS_PER_SLOT * BLK_BYTES + i * SCL_BYTES + g * 4);
-          const float sx = lds_f32(sb + i * (MAX_B * 4));
-          acc0 = fmaf(bf16lo_f32(sc), (c[i][0] + c[i][1]) - 1032.f * sx, acc0);
-          acc1 = fmaf(bf16hi_f32(sc) * 0.0625f, (c[i][2] + c[i][3]) - 1152.f * sx, acc1);
-        } else {
-          acc0 += c[i][0] + c[i][1];
-          acc1 += c[i][2] + c[i][3];
-        }
+      for (int i = 0; i < PER; ++i) {
+        acc0 = fmaf(bf16lo_f32(sc[i]), (c[i][0] + c[i][1]) - 1032.f * sx[i], acc0);
+        acc1 = fmaf(bf16hi_f32(sc[i]) * 0.0625f, (c[i][2] + c[i][3]) - 1152.f * sx[i], acc1);
+      }
+    } else {
+      uint4 av[PER][4];
+#pragma unroll
+      for (int i = 0; i < PER; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j)  // stale bf16 codes could be NaN: zero them
+          av[i][j] = i < nb ? lds128(slot + i * BF16_BLK_BYTES + j * 512 + lane * 16) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+#pragma unroll
+        for (int i = 0; i < PER; ++i)
+          mma_bf16(c[i], av[i][j].x, av[i][j].y, av[i][j].z, av[i][j].w, bx[i][j].x, bx[i][j].y);
+#pragma unroll
+      for (int i = 0; i < PER; ++i) {
+        acc0 += c[i][0] + c[i][1];
+        acc1 += c[i][2] + c[i][3];
       }
     }
     b += nb;
@@ -754,41 +788,38 @@ __device__ __forceinline__ bool stage_gemv_body(const Params& P, int layer, int 
 }
 
 // ------------------------------------------------------------------ attention
-// Merge n <= NW+1 softmax states (m, l, o) into `out` (fp32 records of
-// GH*(hd+2)): per head the rescale factors exp2(m_k - max m) are computed once.
+// Merge softmax states (m, l, o) of the CTA's shared records into `out`
+// (fp32 records of GH*(hd+2) padded to REC floats): record `first`, then
+// record 2v of every warp v in vmask.  Head by head: M = max m_k,
+// f_k = exp2(m_k - M), l = sum f_k l_k, o = sum f_k o_k.  Lane d handles
+// head dims d, d+32, ...
 template <int HD>
-__device__ void merge_records(const float* const* recs, int n, float* out, int GH) {
+__device__ __noinline__ void merge_records(const float* recs, int REC, int first, uint32_t vmask,
+                                           float* out, int GH) {
   const int lane = threadIdx.x & 31;
-  float f[NW + 1][MAX_GH];
-  float mxh[MAX_GH];
+  for (int h = 0; h < GH; ++h) {
+    float mx = recs[first * REC + GH * HD + h];
+    for (uint32_t mm = vmask; mm; mm &= mm - 1)
+      mx = fmaxf(mx, recs[2 * (__ffs(mm) - 1) * REC + GH * HD + h]);
+    float acc[HD / 32], l = 0.f;
 #pragma unroll
-  for (int h = 0; h < MAX_GH; ++h) {
-    mxh[h] = -INFINITY;
-    if (h < GH)
-      for (int k = 0; k < n; ++k) mxh[h] = fmaxf(mxh[h], recs[k][GH * HD + h]);
-  }
+    for (int dd = 0; dd < HD / 32; ++dd) acc[dd] = 0.f;
+    int ri = first;
+    for (uint32_t mm = vmask;;) {
+      const float* r = recs + ri * REC;
+      const float f = exp2f(r[GH * HD + h] - mx);
+      l = fmaf(f, r[GH * HD + GH + h], l);
 #pragma unroll
-  for (int k = 0; k < NW + 1; ++k)
+      for (int dd = 0; dd < HD / 32; ++dd) acc[dd] = fmaf(f, r[h * HD + lane + 32 * dd], acc[dd]);
+      if (!mm) break;
+      ri = 2 * (__ffs(mm) - 1);
+      mm &= mm - 1;
+    }
 #pragma unroll
-    for (int h = 0; h < MAX_GH; ++h)
-      f[k][h] = (k < n && h < GH) ? exp2f(recs[k][GH * HD + h] - mxh[h]) : 0.f;
-  if (lane < GH) {
-    float l = 0.f;
-#pragma unroll
-    for (int k = 0; k < NW + 1; ++k)
-      if (k < n) l += f[k][lane] * recs[k][GH * HD + GH + lane];
-    out[GH * HD + lane] = mxh[lane];
-    out[GH * HD + GH + lane] = l;
-  }
-#pragma unroll
-  for (int h = 0; h < MAX_GH; ++h) {
-    if (h >= GH) break;
-    for (int d = lane; d < HD; d += 32) {
-      float o = 0.f;
-#pragma unroll
-      for (int k = 0; k < NW + 1; ++k)
-        if (k < n) o += f[k][h] * recs[k][h * HD + d];
-      out[h * HD + d] = o;
+    for (int dd = 0; dd < HD / 32; ++dd) out[h * HD + lane + 32 * dd] = acc[dd];
+    if (lane == 0) {
+      out[GH * HD + h] = mx;
+      out[GH * HD + GH + h] = l;
     }
   }
 }
@@ -796,10 +827,10 @@ __device__ void merge_records(const float* const* recs, int n, float* out, int G
 // Final merge of all CTA records of one sequence into attn, by the last CTA
 // to finish it.  Phase 1: warp h < GH folds every record's (m, l) of head h
 // into per-record factors exp2(m_j - M) / L (one record per lane per step).
-// Phase 2: thread (h, d-quad) sums factor * o over the records, 16 loads in
+// Phase 2: thread (h, d-quad) sums factor * o over the records, 8 loads in
 // flight.
 template <int HD>
-__device__ void merge_sequence(const Params& P, int64_t seq, int64_t Ta, int64_t C, float* fac) {
+__device__ __noinline__ void merge_sequence(const Params& P, int64_t seq, int64_t Ta, int64_t C, float* fac) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int GH = P.GH, REC = att_rec_floats(GH, HD), nt = P.nt_att;
   const int64_t cf = owner_of(Ta, C, seq * nt), cl = owner_of(Ta, C, seq * nt + nt - 1);
@@ -832,14 +863,15 @@ __device__ void merge_sequence(const Params& P, int64_t seq, int64_t Ta, int64_t
   for (int e = threadIdx.x; e < GH * DQ; e += NTHREADS) {
     const int h = e / DQ, dq = e - h * DQ;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int j0 = 0; j0 < n; j0 += 16) {
-      float4 v[16];
+#pragma unroll 1
+    for (int j0 = 0; j0 < n; j0 += 8) {
+      float4 v[8];
 #pragma unroll
-      for (int u = 0; u < 16; ++u)
+      for (int u = 0; u < 8; ++u)
         v[u] = j0 + u < n ? __ldcg(reinterpret_cast<const float4*>(base + (int64_t)(j0 + u) * REC + h * HD) + dq)
                           : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-      for (int u = 0; u < 16; ++u) {
+      for (int u = 0; u < 8; ++u) {
         const float fj = j0 + u < n ? fac[h * P.J_att + j0 + u] : 0.f;
         acc.x = fmaf(fj, v[u].x, acc.x);
         acc.y = fmaf(fj, v[u].y, acc.y);
@@ -879,22 +911,20 @@ __device__ __forceinline__ void att_flush(const Params& P, float* rec, const flo
 // record slot rec_idx (continuing into later warps when the run does) into
 // the sequence's partial of this CTA.
 template <int HD>
-__device__ void att_chain(const Params& P, const Misc& M, const float* recs, int64_t seq,
+__device__ __noinline__ void att_chain(const Params& P, const Misc& M, const float* recs, int64_t seq,
                           int rec_idx, bool continues, int64_t Ta, int64_t C) {
   const int warp = threadIdx.x >> 5, GH = P.GH, REC = att_rec_floats(GH, HD), nt = P.nt_att;
-  const float* list[NW + 1];
-  int n = 0;
-  list[n++] = recs + (warp * 2 + rec_idx) * REC;
+  uint32_t vmask = 0;
   if (continues) {
     for (int v = warp + 1; v < NW; ++v) {
       if (M.seg_n[v] == 0) continue;
       if (M.seg_first[v] != seq) break;
-      list[n++] = recs + (v * 2 + 0) * REC;
+      vmask |= 1u << v;
       if (M.seg_n[v] > 1) break;
     }
   }
   float* out = P.apart + (seq * P.J_att + (blockIdx.x - owner_of(Ta, C, seq * nt))) * REC;
-  merge_records<HD>(list, n, out, GH);
+  merge_records<HD>(recs, REC, warp * 2 + rec_idx, vmask, out, GH);
 }
 
 template <int HD, int WT>
@@ -905,11 +935,14 @@ template <int HD, int WT>
 __device__ __noinline__ bool stage_att(const Params& P, int layer, Ring& Rm, Cursor& prodm,
                                        int64_t wg, int64_t W, uint8_t* smem, Misc& M,
                                        uint64_t policy) {
+  __syncwarp();
   Ring R = Rm;
   Cursor prod = prodm;
   const bool ok = stage_att_body<HD, WT>(P, layer, R, prod, wg, W, smem, M, policy);
+  __syncwarp();
   Rm = R;
   prodm = prod;
+  __syncwarp();
   return ok;
 }
 template <int HD, int WT>
@@ -920,7 +953,7 @@ __device__ __forceinline__ bool stage_att_body(const Params& P, int layer, Ring&
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
   const int GH = P.GH, REC = att_rec_floats(GH, HD), nt = P.nt_att;
   const int64_t Ta = (int64_t)P.B * P.Hkv * nt, C = gridDim.x;
-  const LayerDev& Ld = P.layers[layer];
+  const LayerDev& Ld = sp().layers[layer];
   float* recs = reinterpret_cast<float*>(smem + SM_SCR);
   int64_t lo, hi;
   att_range(P, lo, hi);
@@ -1121,31 +1154,54 @@ __device__ bool grid_sync(const Params& P, uint32_t target, Misc& M) {
 // ------------------------------------------------------------------ the kernel
 template <int HD, int WT>
 __global__ void __launch_bounds__(NTHREADS, 1) decode_kernel(const __grid_constant__ Params P) {
-  extern __shared__ __align__(1024) uint8_t smem[];
+  uint8_t* smem = g_smem;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  {  // indexed parameters to shared memory (read after the barrier below)
+    SParams& S = *reinterpret_cast<SParams*>(smem + SM_SPAR);
+    const uint32_t* src = reinterpret_cast<const uint32_t*>(P.mg);
+    uint32_t* dst = reinterpret_cast<uint32_t*>(S.mg);
+    for (int i = threadIdx.x; i < (int)(sizeof(S.mg) / 4); i += NTHREADS) dst[i] = src[i];
+    src = reinterpret_cast<const uint32_t*>(P.rope);
+    dst = reinterpret_cast<uint32_t*>(S.rope);
+    for (int i = threadIdx.x; i < (int)(sizeof(S.rope) / 4); i += NTHREADS) dst[i] = src[i];
+    src = reinterpret_cast<const uint32_t*>(P.layers);
+    dst = reinterpret_cast<uint32_t*>(S.layers);
+    const int nw32 = P.L * (int)(sizeof(LayerDev) / 4);
+    for (int i = threadIdx.x; i < nw32; i += NTHREADS) dst[i] = src[i];
+  }
   const int64_t W = (int64_t)gridDim.x * NW, wg = (int64_t)blockIdx.x * NW + warp;
   Misc& M = *reinterpret_cast<Misc*>(smem + SM_MISC);
-  Ring R;
+  Ring& R = ctx().ring[warp];  // warp-uniform: every lane writes the same values
+  Cursor& prod = ctx().cur[warp];
   R.slot0 = smem_addr(smem + SM_RING + warp * DEPTH * SLOT_BYTES);
   R.bar0 = smem_addr(smem + SM_BARS + warp * DEPTH * 8);
   R.n_issued = R.n_done = 0;
   if (lane < DEPTH) mbar_init(R.bar0 + lane * 8, 1);
   if (threadIdx.x == 0) {
     M.abort = 0;
-    M.pphase = 0;
-    mbar_init(smem_addr(smem + SM_PBAR), 1);
   }
   mbar_init_fence();
   __syncthreads();
   const uint64_t policy = policy_evict_first();
-  Cursor prod;
-  prod.s = P.stage_begin;
-  cursor_enter<WT>(P, prod, wg, W);
-  for (int k = 0; k < DEPTH; ++k) {
-    SlotDesc d;
-    if (!cursor_next<WT>(P, prod, wg, W, d)) break;
-    issue_slot<HD, WT>(P, prod, d, R.slot(R.n_issued), R.bar(R.n_issued), lane, policy);
-    R.n_issued++;
+  {
+    Cursor c;
+    c.s = P.stage_begin;
+    prod.s = P.stage_begin;
+    __syncwarp();
+    cursor_enter<WT>(P, prod, wg, W);
+    __syncwarp();
+    c = prod;
+    Ring r = R;
+    for (int k = 0; k < DEPTH; ++k) {
+      SlotDesc d;
+      if (!cursor_next<WT>(P, c, wg, W, d)) break;
+      issue_slot<HD, WT>(P, c, d, r.slot(r.n_issued), r.bar(r.n_issued), lane, policy);
+      r.n_issued++;
+    }
+    __syncwarp();
+    prod = c;
+    R = r;
+    __syncwarp();
   }
   bool ok = true;
   for (int s = P.stage_begin; s < P.stage_end && ok; ++s) {
@@ -1168,8 +1224,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) decode_kernel(const __grid_consta
     if (M.abort) ok = false;
   }
   if (!ok) {  // let this warp's copies in flight land before the CTA exits (bounded)
-    for (uint32_t n = R.n_done; n < R.n_issued; ++n)
-      if (!mbar_wait_warp(R.bar(n), R.parity(n), P.ctrl + 1)) break;
+    __syncwarp();
+    const Ring r = R;
+    for (uint32_t n = r.n_done; n < r.n_issued; ++n)
+      if (!mbar_wait_warp(r.bar(n), r.parity(n), P.ctrl + 1)) break;
   }
 }
 

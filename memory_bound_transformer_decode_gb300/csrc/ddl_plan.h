@@ -40,7 +40,7 @@ namespace ddl {
 
 constexpr int NW = 8;                 // warps per CTA (each streams its own ring)
 constexpr int NTHREADS = NW * 32;
-constexpr int DEPTH = 4;              // ring slots per warp
+constexpr int DEPTH = 3;              // ring slots per warp
 constexpr int SLOT_BYTES = 4352;      // 8 INT4 blocks + their scales, or 16 padded KV rows
 constexpr int BLK_BYTES = 512;        // one INT4 block: 16 rows x 64 columns
 constexpr int SCL_BYTES = 32;         // scales of one block
@@ -54,7 +54,7 @@ constexpr int MAX_GH = 8;             // query heads per KV head
 constexpr int NSTAGE = 5;
 constexpr int MAXP = 16;              // k-chunk panels per matrix
 constexpr int XF_CHUNKS = 8;          // k-chunks of x one CTA can stage at batch 1 (x batch size <= 8)
-constexpr int TRACE_WORDS = NW + 7;   // per (stage, CTA) in the optional trace
+constexpr int TRACE_WORDS = NW + 8;   // per (stage, CTA) in the optional trace
 
 // Floats of one attention softmax record (o[GH][hd], m[GH], l[GH]), padded
 // to 16 bytes so that records can be read as float4.

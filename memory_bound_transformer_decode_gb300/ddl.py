@@ -271,7 +271,7 @@ def ddl_set_launch_mode(mode: int):
 
 
 def ddl_set_trace(buf: torch.Tensor | None):
-    """Turn the per-(stage, CTA) %globaltimer trace on (a device tensor) or off."""
+    """Turn the per-(stage, CTA) timing trace on (a device tensor) or off."""
     lib = load()
     if buf is None:
         _check("ddl_set_trace", lib.ddl_set_trace(None, 0))
