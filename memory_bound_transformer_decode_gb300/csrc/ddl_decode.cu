@@ -58,7 +58,9 @@ constexpr int SM_SPAR = SM_MISC + SM_MISC_BYTES;             // copies of the in
 constexpr int SM_CTX = SM_SPAR + (((int)sizeof(SParams) + 255) & ~255);  // stage context, warp cursors
 constexpr int SM_CTX_BYTES = 2048;
 constexpr int SM_TOTAL = SM_CTX + SM_CTX_BYTES;
-static_assert(XF_BYTES + SX_BYTES + NW * 32 * 4 <= SM_SCR_BYTES, "x fragments do not fit");
+constexpr int XZ_OFF = XF_BYTES + SX_BYTES + NW * 32 * 4;  // zero x fragments for blocks past a slot's end
+constexpr int XZ_BYTES = 3 * 2 * MAX_B * 32 + 256;          // 3 j-strides + one lane span
+static_assert(XZ_OFF + XZ_BYTES <= SM_SCR_BYTES, "x fragments do not fit");
 static_assert(NW * 2 * (MAX_GH * (128 + 2) + 3) * 4 <= SM_SCR_BYTES, "attention records do not fit");
 static_assert(SM_TOTAL <= 227 * 1024, "shared memory budget");
 static_assert(SM_SPAR % 16 == 0, "parameter copy alignment");
@@ -239,7 +241,6 @@ __device__ __forceinline__ void ring_advance(const Params& P, Ring& R, Cursor& p
   __syncwarp();
   SlotDesc d;
   if (cursor_next<WT>(P, prod, wg, W, d)) {
-    fence_proxy_async_smem();  // every issuing lane: earlier generic smem accesses first
     issue_slot<HD, WT>(P, prod, d, R.slot(R.n_issued), R.bar(R.n_issued), lane, policy);
     R.n_issued++;
   }
@@ -479,6 +480,9 @@ __device__ __noinline__ void gemv_prologue(const Params& P, const GemvCtx& E, ui
       if (q16 == 0 && ok[u]) Sx[gs * MAX_B + b] = part;
     }
   }
+  // zero fragments that the stream reads for blocks past a slot's end (the
+  // attention stage uses this memory too)
+  for (int i = tid; i < XZ_BYTES / 4; i += NTHREADS) reinterpret_cast<uint32_t*>(smem + SM_SCR + XZ_OFF)[i] = 0u;
   __syncthreads();
 }
 
@@ -679,6 +683,7 @@ __device__ __forceinline__ bool stage_gemv_body(const Params& P, int layer, int 
   const int B = P.B, B2 = 2 * B, Sk = m.Sk, pk0 = m.pk[E.p], pk1 = m.pk[E.p + 1];
   const uint32_t jstride = B2 * 32, gstride = 4 * jstride, kstride = GC * gstride;
   const uint32_t xf_lane = smem_addr(smem + SM_SCR) + (g * 4 + t) * 8;
+  const uint32_t xz = smem_addr(smem + SM_SCR + XZ_OFF) + (g * 4 + t) * 8;
   const uint32_t sx_lane = smem_addr(smem + SM_SCR + XF_BYTES) + t * 4;
   const float esc = M.escale[t < B ? t : 0];
   int kc, T, gi;
@@ -699,68 +704,77 @@ __device__ __forceinline__ bool stage_gemv_body(const Params& P, int layer, int 
     const int kcl = kc - pk0;
     const uint32_t xb = xf_lane + kcl * kstride + gi * gstride;
     const uint32_t sb = sx_lane + ((kcl * GC + gi) * MAX_B) * 4;
-    // All shared loads of the slot first, then the MMAs in (j, block) order
-    // so that consecutive MMAs accumulate into different blocks.  Blocks
-    // i >= nb get zero x fragments (and zero scale and sum of x), so they add
-    // nothing whatever stale codes the slot holds.
-    float c[PER][4];
-    uint2 bx[PER][4];
+    // The slot's blocks in two halves (a rolled loop: the stream loop's code
+    // has to stay in the instruction cache).  Per half, all shared loads
+    // first, then the MMAs in (j, block) order so that consecutive MMAs
+    // accumulate into different blocks.  Blocks i >= nb get zero x fragments
+    // (and zero scale and sum of x), so they add nothing whatever stale codes
+    // the slot holds.
+    constexpr int HB = PER / 2;
+#pragma unroll 1
+    for (int h0 = 0; h0 < PER; h0 += HB) {
+      float c[HB][4];
+      uint2 bx[HB][4];
 #pragma unroll
-    for (int i = 0; i < PER; ++i) {
-      c[i][0] = c[i][1] = c[i][2] = c[i][3] = 0.f;
+      for (int ii = 0; ii < HB; ++ii) {
+        const int i = h0 + ii;
+        c[ii][0] = c[ii][1] = c[ii][2] = c[ii][3] = 0.f;
+        const uint32_t xi = i < nb ? xb + i * gstride : xz;  // past the slot's end: zeros
 #pragma unroll
-      for (int j = 0; j < 4; ++j)
-        bx[i][j] = i < nb ? lds64(xb + i * gstride + j * jstride) : make_uint2(0u, 0u);
-    }
-    if (WT == DDL_W_INT4) {
-      uint4 wv[PER];
-      uint32_t sc[PER];
-      float sx[PER];
-#pragma unroll
-      for (int i = 0; i < PER; ++i) {
-        wv[i] = lds128(slot + i * BLK_BYTES + lane * 16);
-        sc[i] = i < nb ? lds32(slot + BLKS_PER_SLOT * BLK_BYTES + i * SCL_BYTES + g * 4) : 0u;
-        sx[i] = i < nb ? lds_f32(sb + i * (MAX_B * 4)) : 0.f;
+        for (int j = 0; j < 4; ++j) bx[ii][j] = lds64(xi + j * jstride);
       }
+      if (WT == DDL_W_INT4) {
+        uint4 wv[HB];
+        uint32_t sc[HB];
+        float sx[HB];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
+        for (int ii = 0; ii < HB; ++ii) {
+          const int i = h0 + ii;
+          wv[ii] = lds128(slot + i * BLK_BYTES + lane * 16);
+          const uint32_t scw = lds32(slot + BLKS_PER_SLOT * BLK_BYTES + i * SCL_BYTES + g * 4);
+          const float sxv = lds_f32(sb + i * (MAX_B * 4));
+          sc[ii] = i < nb ? scw : 0u;  // stale scale and sum words are finite-safe only as 0
+          sx[ii] = i < nb ? sxv : 0.f;
+        }
 #pragma unroll
-        for (int i = 0; i < PER; ++i) {
-          const uint32_t w = j == 0 ? wv[i].x : j == 1 ? wv[i].y : j == 2 ? wv[i].z : wv[i].w;
-          const uint32_t w8 = w >> 8;
-          const uint32_t a0 = lop3_merge(w, 0x000F000Fu, 0x64086408u);
-          const uint32_t a1 = lop3_merge(w, 0x00F000F0u, 0x64806480u);
-          const uint32_t a2 = lop3_merge(w8, 0x000F000Fu, 0x64086408u);
-          const uint32_t a3 = lop3_merge(w8, 0x00F000F0u, 0x64806480u);
-          // lanes g >= 2B read unrelated fragments: they only feed C columns >= 2B, never used
-          mma_f16(c[i], a0, a1, a2, a3, bx[i][j].x, bx[i][j].y);
+        for (int j = 0; j < 4; ++j) {
+#pragma unroll
+          for (int ii = 0; ii < HB; ++ii) {
+            const uint32_t w = j == 0 ? wv[ii].x : j == 1 ? wv[ii].y : j == 2 ? wv[ii].z : wv[ii].w;
+            const uint32_t w8 = w >> 8;
+            const uint32_t a0 = lop3_merge(w, 0x000F000Fu, 0x64086408u);
+            const uint32_t a1 = lop3_merge(w, 0x00F000F0u, 0x64806480u);
+            const uint32_t a2 = lop3_merge(w8, 0x000F000Fu, 0x64086408u);
+            const uint32_t a3 = lop3_merge(w8, 0x00F000F0u, 0x64806480u);
+            // lanes g >= 2B read unrelated fragments: they only feed C columns >= 2B, never used
+            mma_f16(c[ii], a0, a1, a2, a3, bx[ii][j].x, bx[ii][j].y);
+          }
+        }
+        // rows g hold 1024 + (q+8), rows g+8 hold 1024 + 16 (q+8):
+        // sum q x = v - 1032 Sx  and  (v - 1152 Sx) / 16
+#pragma unroll
+        for (int ii = 0; ii < HB; ++ii) {
+          acc0 = fmaf(bf16lo_f32(sc[ii]), (c[ii][0] + c[ii][1]) - 1032.f * sx[ii], acc0);
+          acc1 = fmaf(bf16hi_f32(sc[ii]) * 0.0625f, (c[ii][2] + c[ii][3]) - 1152.f * sx[ii], acc1);
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+#pragma unroll
+          for (int ii = 0; ii < HB; ++ii) {
+            const int i = h0 + ii;  // stale bf16 codes could be NaN: zero them
+            const uint4 av = lds128(slot + i * BF16_BLK_BYTES + j * 512 + lane * 16);
+            const uint4 aq = i < nb ? av : make_uint4(0u, 0u, 0u, 0u);
+            mma_bf16(c[ii], aq.x, aq.y, aq.z, aq.w, bx[ii][j].x, bx[ii][j].y);
+          }
+#pragma unroll
+        for (int ii = 0; ii < HB; ++ii) {
+          acc0 += c[ii][0] + c[ii][1];
+          acc1 += c[ii][2] + c[ii][3];
         }
       }
-      // rows g hold 1024 + (q+8), rows g+8 hold 1024 + 16 (q+8):
-      // sum q x = v - 1032 Sx  and  (v - 1152 Sx) / 16
-#pragma unroll
-      for (int i = 0; i < PER; ++i) {
-        acc0 = fmaf(bf16lo_f32(sc[i]), (c[i][0] + c[i][1]) - 1032.f * sx[i], acc0);
-        acc1 = fmaf(bf16hi_f32(sc[i]) * 0.0625f, (c[i][2] + c[i][3]) - 1152.f * sx[i], acc1);
-      }
-    } else {
-      uint4 av[PER][4];
-#pragma unroll
-      for (int i = 0; i < PER; ++i)
-#pragma unroll
-        for (int j = 0; j < 4; ++j)  // stale bf16 codes could be NaN: zero them
-          av[i][j] = i < nb ? lds128(slot + i * BF16_BLK_BYTES + j * 512 + lane * 16) : make_uint4(0u, 0u, 0u, 0u);
-#pragma unroll
-      for (int j = 0; j < 4; ++j)
-#pragma unroll
-        for (int i = 0; i < PER; ++i)
-          mma_bf16(c[i], av[i][j].x, av[i][j].y, av[i][j].z, av[i][j].w, bx[i][j].x, bx[i][j].y);
-#pragma unroll
-      for (int i = 0; i < PER; ++i) {
-        acc0 += c[i][0] + c[i][1];
-        acc1 += c[i][2] + c[i][3];
-      }
     }
+    ring_advance<HD, WT>(P, R, prod, wg, W, lane, policy);
     b += nb;
     gi += nb;
     nblk += nb;
@@ -778,7 +792,6 @@ __device__ __forceinline__ bool stage_gemv_body(const Params& P, int layer, int 
       }
       gk = kc < Sk ? chunk_groups(m, kc) : 1;
     }
-    ring_advance<HD, WT>(P, R, prod, wg, W, lane, policy);
   }
   if (nblk != 0)
     tile_finish<HD>(P, E, M, T, nblk, fmaf(acc0, esc, tac0), fmaf(acc1, esc, tac1), pend, npend);
