@@ -76,6 +76,7 @@ struct Misc {
   int seg_n[NW];
   long long seg_first[NW], seg_last[NW];
   long long mseq[8];       // sequences this CTA merges last
+  uint32_t cmax[MAX_B];    // running max |output * consumer norm weight| of this stage (float bits)
 };
 static_assert(sizeof(Misc) <= SM_MISC_BYTES, "misc");
 
@@ -290,17 +291,19 @@ __device__ __forceinline__ void trace_stamp(const Params& P, int s, int slot) {
 // Stages this CTA's panel of the activation (k-chunks pk[p]..pk[p+1]-1) as
 // m16n8k16 B fragments: column 2b is the fp16 "high" part of sequence b's x
 // (times the norm weight and 2^-e), column 2b+1 the fp16 remainder, so x is
-// carried to ~22 bits.  Also computes the RMSNorm factor r (QKV, GU), the
-// power-of-two scale 2^e that brings the panel's largest |x| to [2^11, 2^12),
-// and, for INT4, the per-group sums of x used to remove the +8 code offset.
-// One round trip: cp.async copies (through L1, so that they do not queue
-// behind the weight ring's bulk copies in the TMA unit) bring every (group,
-// sequence) of x into 256 bytes of shared memory and every group of norm
-// weights into 128 bytes.  When the panel is the whole vector the sum of
-// squares comes from the staged x; otherwise it is loaded meanwhile.  Item
-// it = ((group slot * B + b) * 16 + quad) is one four-column quad of x, at
-// byte it*16 of the staged x (fp32).  The conversion runs in rounds of whole
-// groups: read, block barrier, write the fragments in place.
+// carried to ~22 bits.  Also the RMSNorm factor r (QKV, GU) and, for INT4,
+// the per-group sums of x used to remove the +8 code offset.  The power-of-two
+// scale 2^e brings the largest |x * w| to [2^11, 2^12); that maximum is
+// recorded by the stage that produced x (one word per sequence), so one pass
+// over the panel suffices; only the first layer of a launch has no producer
+// and measures its panel.
+// cp.async copies (through L1, so that they do not queue behind the weight
+// ring's bulk copies in the TMA unit) bring every (group, sequence) of x into
+// 256 bytes of shared memory and every group of norm weights into 128 bytes;
+// the Wo and down stages also stage the next weight stage's norm vector for
+// their epilogue maxima.  Item it = ((group slot * B + b) * 16 + quad) is one
+// four-column quad of x at byte it*16 of the staged x (fp32).  The conversion
+// runs in rounds of whole groups: read, block barrier, write in place.
 template <int HD, int WT>
 __device__ __noinline__ void gemv_prologue(const Params& P, const GemvCtx& E, uint8_t* smem, Misc& M) {
   const MatGeom& m = E.m;
@@ -309,46 +312,54 @@ __device__ __noinline__ void gemv_prologue(const Params& P, const GemvCtx& E, ui
   const int kc_lo = m.pk[E.p], nkc = m.pk[E.p + 1] - kc_lo;
   const float* x32 = nullptr;
   const uint16_t* x16 = nullptr;
-  const uint16_t* nw = nullptr;
+  const uint16_t* nw = nullptr;       // this stage's norm weights (QKV, GU)
+  const uint16_t* nw_next = nullptr;  // the next weight stage's (Wo, down), for the maxima
   const LayerDev& Ld = sp().layers[E.layer];
   switch (E.st) {
     case ST_QKV: nw = Ld.norm1; x32 = E.xin32; x16 = E.xin16; break;
-    case ST_WO: x32 = P.attn; break;
+    case ST_WO: x32 = P.attn; nw_next = Ld.norm2; break;
     case ST_GU: x32 = P.y; nw = Ld.norm2; break;
-    default: x32 = P.a; break;
+    default: x32 = P.a; nw_next = E.layer + 1 < P.L ? sp().layers[E.layer + 1].norm1 : nullptr; break;
   }
+  if ((int64_t)P.D * 2 > SM_NW_BYTES) nw_next = nullptr;  // the epilogue reads it from memory
   const int K = m.K;
-  const int ngr = nkc * GC;  // group slots of the panel (the last chunk may use fewer)
+  const int ngr = nkc * GC;                                                   // group slots
+  const int ngv = (nkc - 1) * GC + chunk_groups(m, kc_lo + nkc - 1);          // ... holding data
   const int n_items = ngr * B * 16;
   const int kbase = kc_lo * GC * DDL_GROUP;
   const bool whole = nkc == m.Sk;  // the panel is the whole vector
+  const bool have_max = !(E.st == ST_QKV && E.layer == 0);
+  const uint64_t invB = ((1ull << 32) + B - 1) / B;  // g / B == (g * invB) >> 32 for the indices here
   uint8_t* raw = smem + SM_SCR;
   uint8_t* nws = smem + SM_NW;
-  // 1. copies: 16-byte pieces of x (16 per (group, sequence) for fp32, 8 for
-  //    bf16) and of the norm weights (8 per group).  Earlier readers of the
-  //    areas (any thread) are done first.
+  // 1. copies (earlier readers of these areas, any thread, are done first)
   __syncthreads();
   {
-    const int xp = x32 ? 16 : 8;  // pieces per (group, sequence)
-    const int nx = ngr * B * xp, nn = nw ? ngr * 8 : 0;
-    for (int i = tid; i < nx + nn; i += NTHREADS) {
+    const int xsh = x32 ? 4 : 3;  // log2 of the 16-byte pieces of one (group, sequence)
+    const int nx = (ngr * B) << xsh, nn = nw ? ngr * 8 : 0, nnx = nw_next ? P.D / 8 : 0;
+    for (int i = tid; i < nx + nn + nnx; i += NTHREADS) {
       if (i < nx) {
-        const int gsb = i / xp, q = i - gsb * xp, gs = gsb / B, b = gsb - gs * B;
-        if ((gs % GC) < chunk_groups(m, kc_lo + gs / GC)) {
+        const int gsb = i >> xsh, q = i & ((1 << xsh) - 1);
+        const int gs = (int)(((uint64_t)gsb * invB) >> 32), b = gsb - gs * B;
+        if (gs < ngv) {
           const int64_t k = kbase + (int64_t)gs * DDL_GROUP;
           const void* src = x32 ? (const void*)(x32 + (int64_t)b * K + k + q * 4)
                                 : (const void*)(x16 + (int64_t)b * K + k + q * 8);
           cp_async16(smem_addr(raw + (size_t)gsb * 256 + q * 16), src);
         }
-      } else {
+      } else if (i < nx + nn) {
         const int j = i - nx, gs = j >> 3, q = j & 7;
-        if ((gs % GC) < chunk_groups(m, kc_lo + gs / GC))
-          cp_async16(smem_addr(nws + (size_t)gs * 128 + q * 16), nw + kbase + (int64_t)gs * DDL_GROUP + q * 8);
+        if (gs < ngv) cp_async16(smem_addr(nws + (size_t)gs * 128 + q * 16), nw + kbase + (int64_t)gs * DDL_GROUP + q * 8);
+      } else {
+        const int j = i - nx - nn;
+        cp_async16(smem_addr(nws + (size_t)j * 16), nw_next + (int64_t)j * 8);
       }
     }
   }
+  float xm = 0.f;  // thread b < B: the producer's max for sequence b
+  if (have_max && tid < B) xm = __uint_as_float(__ldcg(P.xmax + (E.layer * NSTAGE + E.st) * MAX_B + tid));
   if (tid == 0) trace_stamp(P, E.layer * NSTAGE + E.st, NW + 3);
-  // 2. meanwhile (panel not the whole vector): the sum of squares
+  // 2. meanwhile (a norm stage whose panel is not the whole vector): the sum of squares
   if (nw && !whole) {
     for (int b = 0; b < B; ++b) {
       float ss = 0.f;
@@ -374,60 +385,52 @@ __device__ __noinline__ void gemv_prologue(const Params& P, const GemvCtx& E, ui
   cp_async_wait_all();
   __syncthreads();
   if (tid == 0) trace_stamp(P, E.layer * NSTAGE + E.st, NW + 5);
-  // 3. max |x * w| per sequence over the panel (and the sum of squares of x
-  //    when the panel is the whole vector)
-  float mx[MAX_B] = {0.f, 0.f, 0.f, 0.f}, ssq[MAX_B] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 4
-  for (int it = tid; it < n_items; it += NTHREADS) {
-    const int gsb = it >> 4, q16 = it & 15, gs = gsb / B, b = gsb - gs * B;
-    if ((gs % GC) >= chunk_groups(m, kc_lo + gs / GC)) continue;
-    float4 x = x32 ? *reinterpret_cast<const float4*>(raw + (size_t)it * 16)
-                   : bf16x4_f32(*reinterpret_cast<const uint2*>(raw + (size_t)gsb * 256 + q16 * 8));
-    const float s2 = fmaf(x.x, x.x, fmaf(x.y, x.y, fmaf(x.z, x.z, x.w * x.w)));
-    if (nw) {
-      const float4 w = bf16x4_f32(*reinterpret_cast<const uint2*>(nws + (size_t)gs * 128 + q16 * 8));
-      x = make_float4(x.x * w.x, x.y * w.y, x.z * w.z, x.w * w.w);
-    }
-    const float a = fmaxf(fmaxf(fabsf(x.x), fabsf(x.y)), fmaxf(fabsf(x.z), fabsf(x.w)));
+  // 3. the scale: the producer's max, or (first layer of a launch) the panel's
+  if (!have_max) {
+    float mx[MAX_B] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 2
+    for (int it = tid; it < n_items; it += NTHREADS) {
+      const int gsb = it >> 4, q16 = it & 15;
+      const int gs = (int)(((uint64_t)gsb * invB) >> 32), b = gsb - gs * B;
+      if (gs >= ngv) continue;
+      float4 x = x32 ? *reinterpret_cast<const float4*>(raw + (size_t)it * 16)
+                     : bf16x4_f32(*reinterpret_cast<const uint2*>(raw + (size_t)gsb * 256 + q16 * 8));
+      if (nw) {
+        const float4 w = bf16x4_f32(*reinterpret_cast<const uint2*>(nws + (size_t)gs * 128 + q16 * 8));
+        x = make_float4(x.x * w.x, x.y * w.y, x.z * w.z, x.w * w.w);
+      }
+      const float a = fmaxf(fmaxf(fabsf(x.x), fabsf(x.y)), fmaxf(fabsf(x.z), fabsf(x.w)));
 #pragma unroll
-    for (int bb = 0; bb < MAX_B; ++bb) {
-      if (bb == b) {
-        mx[bb] = fmaxf(mx[bb], a);
-        ssq[bb] += s2;
+      for (int bb = 0; bb < MAX_B; ++bb)
+        if (bb == b) mx[bb] = fmaxf(mx[bb], a);
+    }
+#pragma unroll
+    for (int b = 0; b < MAX_B; ++b) {
+      if (b < B) {
+        const float r = warp_max(mx[b]);
+        if (lane == 0) M.red[warp][2 * b + 1] = r;
       }
     }
+    __syncthreads();
+    if (tid < B)
+      for (int w = 0; w < NW; ++w) xm = fmaxf(xm, M.red[w][2 * tid + 1]);
   }
-#pragma unroll
-  for (int b = 0; b < MAX_B; ++b) {
-    if (b < B) {
-      const float r = warp_max(mx[b]);
-      if (lane == 0) M.red[warp][2 * b + 1] = r;
-      if (nw && whole) {
-        const float q = warp_sum(ssq[b]);
-        if (lane == 0) M.red[warp][2 * b] = q;
-      }
-    }
-  }
-  __syncthreads();
   if (tid < B) {
-    float ss = 0.f, mxa = 0.f;
-    for (int w = 0; w < NW; ++w) {
-      ss += M.red[w][2 * tid];
-      mxa = fmaxf(mxa, M.red[w][2 * tid + 1]);
-    }
-    M.rnorm[tid] = nw ? 1.0f / sqrtf(ss / (float)K + P.eps) : 1.0f;
-    const int e = mxa > 0.f ? ilogbf(mxa) - 11 : 0;
+    const int e = xm > 0.f ? ilogbf(xm) - 11 : 0;
     M.escale[tid] = ldexpf(1.0f, e);
     M.edown[tid] = ldexpf(1.0f, -e);
   }
   __syncthreads();
   if (tid == 0) trace_stamp(P, E.layer * NSTAGE + E.st, NW + 6);
-  // 4. fragments in place, in rounds of whole groups (up to 4 quads a thread).
-  //    Quad q16 holds columns 4 q16 .. 4 q16 + 3 of its group: MMA j = q16 / 4,
+  // 4. fragments in place, in rounds of whole groups (up to 4 quads a thread),
+  //    and the sum of squares of x when the panel is the whole vector.  Quad
+  //    q16 holds columns 4 q16 .. 4 q16 + 3 of its group: MMA j = q16 / 4,
   //    register half (q16 / 2) % 2, lanes t0 = 2 (q16 % 2) and t0 + 1.
   //    Sx = sum of hi + lo over the group's 16 quads (16 consecutive lanes).
   float* Sx = reinterpret_cast<float*>(smem + SM_SCR + XF_BYTES);
   constexpr bool f16 = WT == DDL_W_INT4;
+  const bool want_ss = nw && whole;
+  float ssq[MAX_B] = {0.f, 0.f, 0.f, 0.f};
   const int ipr = (4 * NTHREADS / (16 * B)) * 16 * B;  // items per round: whole groups
   for (int r0 = 0; r0 < n_items; r0 += ipr) {
     float4 v[4];
@@ -435,13 +438,20 @@ __device__ __noinline__ void gemv_prologue(const Params& P, const GemvCtx& E, ui
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       const int iu = u * NTHREADS + tid, it = r0 + iu;
-      const int gsb = it >> 4, q16 = it & 15, gs = gsb / B;
-      ok[u] = iu < ipr && it < n_items && (gs % GC) < chunk_groups(m, kc_lo + gs / GC);
+      const int gsb = it >> 4, q16 = it & 15;
+      const int gs = (int)(((uint64_t)gsb * invB) >> 32), b = gsb - gs * B;
+      ok[u] = iu < ipr && it < n_items && gs < ngv;
       v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
       if (ok[u]) {
-        const float sc = M.edown[gsb - gs * B];
         float4 x = x32 ? *reinterpret_cast<const float4*>(raw + (size_t)it * 16)
                        : bf16x4_f32(*reinterpret_cast<const uint2*>(raw + (size_t)gsb * 256 + q16 * 8));
+        if (want_ss) {
+          const float s2 = fmaf(x.x, x.x, fmaf(x.y, x.y, fmaf(x.z, x.z, x.w * x.w)));
+#pragma unroll
+          for (int bb = 0; bb < MAX_B; ++bb)
+            if (bb == b) ssq[bb] += s2;
+        }
+        const float sc = M.edown[b];
         const float4 w = nw ? bf16x4_f32(*reinterpret_cast<const uint2*>(nws + (size_t)gs * 128 + q16 * 8))
                             : make_float4(1.f, 1.f, 1.f, 1.f);
         v[u] = make_float4(x.x * w.x * sc, x.y * w.y * sc, x.z * w.z * sc, x.w * w.w * sc);
@@ -451,29 +461,47 @@ __device__ __noinline__ void gemv_prologue(const Params& P, const GemvCtx& E, ui
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       const int it = r0 + u * NTHREADS + tid;
-      const int gsb = it >> 4, q16 = it & 15, gs = gsb / B, b = gsb - gs * B;
+      const int gsb = it >> 4, q16 = it & 15;
+      const int gs = (int)(((uint64_t)gsb * invB) >> 32), b = gsb - gs * B;
       float part = 0.f;
       if (ok[u]) {
-        const float xv[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
-        float hi[4], lo[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          if (f16) {
-            hi[e] = __half2float(__float2half_rn(xv[e]));
-            lo[e] = __half2float(__float2half_rn(xv[e] - hi[e]));
-          } else {
-            hi[e] = __bfloat162float(__float2bfloat16_rn(xv[e]));
-            lo[e] = __bfloat162float(__float2bfloat16_rn(xv[e] - hi[e]));
-          }
+        uint32_t h01, h23, l01, l23;
+        float2 hf01, hf23, lf01, lf23;
+        if (f16) {
+          const __half2 a = __float22half2_rn(make_float2(v[u].x, v[u].y));
+          const __half2 c = __float22half2_rn(make_float2(v[u].z, v[u].w));
+          hf01 = __half22float2(a);
+          hf23 = __half22float2(c);
+          const __half2 la = __float22half2_rn(make_float2(v[u].x - hf01.x, v[u].y - hf01.y));
+          const __half2 lc = __float22half2_rn(make_float2(v[u].z - hf23.x, v[u].w - hf23.y));
+          lf01 = __half22float2(la);
+          lf23 = __half22float2(lc);
+          h01 = *reinterpret_cast<const uint32_t*>(&a);
+          h23 = *reinterpret_cast<const uint32_t*>(&c);
+          l01 = *reinterpret_cast<const uint32_t*>(&la);
+          l23 = *reinterpret_cast<const uint32_t*>(&lc);
+        } else {
+          const __nv_bfloat162 a = __float22bfloat162_rn(make_float2(v[u].x, v[u].y));
+          const __nv_bfloat162 c = __float22bfloat162_rn(make_float2(v[u].z, v[u].w));
+          hf01 = __bfloat1622float2(a);
+          hf23 = __bfloat1622float2(c);
+          const __nv_bfloat162 la = __float22bfloat162_rn(make_float2(v[u].x - hf01.x, v[u].y - hf01.y));
+          const __nv_bfloat162 lc = __float22bfloat162_rn(make_float2(v[u].z - hf23.x, v[u].w - hf23.y));
+          lf01 = __bfloat1622float2(la);
+          lf23 = __bfloat1622float2(lc);
+          h01 = *reinterpret_cast<const uint32_t*>(&a);
+          h23 = *reinterpret_cast<const uint32_t*>(&c);
+          l01 = *reinterpret_cast<const uint32_t*>(&la);
+          l23 = *reinterpret_cast<const uint32_t*>(&lc);
         }
-        part = ((hi[0] + lo[0]) + (hi[1] + lo[1])) + ((hi[2] + lo[2]) + (hi[3] + lo[3]));
+        part = ((hf01.x + lf01.x) + (hf01.y + lf01.y)) + ((hf23.x + lf23.x) + (hf23.y + lf23.y));
         const int j = q16 >> 2, half = (q16 >> 1) & 1, t0 = 2 * (q16 & 1);
         uint32_t* f = reinterpret_cast<uint32_t*>(raw + (size_t)gs * B * 256);
         const int ch = (j * 2 * B + 2 * b) * 4;  // (j, column 2b): 4 lanes x 2 halves
-        f[(ch + t0) * 2 + half] = f16 ? pack_f16x2(hi[0], hi[1]) : pack_bf16x2(hi[0], hi[1]);
-        f[(ch + t0 + 1) * 2 + half] = f16 ? pack_f16x2(hi[2], hi[3]) : pack_bf16x2(hi[2], hi[3]);
-        f[(ch + 4 + t0) * 2 + half] = f16 ? pack_f16x2(lo[0], lo[1]) : pack_bf16x2(lo[0], lo[1]);
-        f[(ch + 4 + t0 + 1) * 2 + half] = f16 ? pack_f16x2(lo[2], lo[3]) : pack_bf16x2(lo[2], lo[3]);
+        f[(ch + t0) * 2 + half] = h01;
+        f[(ch + t0 + 1) * 2 + half] = h23;
+        f[(ch + 4 + t0) * 2 + half] = l01;
+        f[(ch + 4 + t0 + 1) * 2 + half] = l23;
       }
 #pragma unroll
       for (int o = 8; o; o >>= 1) part += __shfl_xor_sync(FULL, part, o);
@@ -483,14 +511,38 @@ __device__ __noinline__ void gemv_prologue(const Params& P, const GemvCtx& E, ui
   // zero fragments that the stream reads for blocks past a slot's end (the
   // attention stage uses this memory too)
   for (int i = tid; i < XZ_BYTES / 4; i += NTHREADS) reinterpret_cast<uint32_t*>(smem + SM_SCR + XZ_OFF)[i] = 0u;
+  // 5. the RMSNorm factor
+  if (want_ss) {
+#pragma unroll
+    for (int b = 0; b < MAX_B; ++b) {
+      if (b < B) {
+        const float r = warp_sum(ssq[b]);
+        if (lane == 0) M.red[warp][2 * b] = r;
+      }
+    }
+  }
+  __syncthreads();
+  if (tid < B) {
+    float ss = 0.f;
+    if (nw)
+      for (int w = 0; w < NW; ++w) ss += M.red[w][2 * tid];
+    M.rnorm[tid] = nw ? 1.0f / sqrtf(ss / (float)K + P.eps) : 1.0f;
+  }
   __syncthreads();
 }
 
 // ------------------------------------------------------------------ GEMV epilogues
+// Norm weight r of the next weight stage, for the output maxima: from the copy
+// that this stage's prologue staged in shared memory when the vector fits.
+__device__ __forceinline__ float epi_norm(const Params& P, const uint16_t* w, int r) {
+  return (int64_t)P.D * 2 <= SM_NW_BYTES ? bf16_bits_to_f32(reinterpret_cast<const uint16_t*>(g_smem + SM_NW)[r])
+                                         : bf16_bits_to_f32(__ldg(w + r));
+}
+
 // Lane (g, t) holds rows g and g+8 of tile T for sequence t.
 template <int HD>
 __device__ __noinline__ void gemv_epilogue(const Params& P, const GemvCtx& E, int T, float v0, float v1,
-                              const Misc& M) {
+                              Misc& M) {
   const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
   if (t >= P.B) return;
   if (E.st == ST_QKV) {
@@ -519,17 +571,29 @@ __device__ __noinline__ void gemv_epilogue(const Params& P, const GemvCtx& E, in
     const int64_t o = (int64_t)t * P.D;
     const float x0 = E.xin32 ? __ldcg(E.xin32 + o + r0) : bf16_bits_to_f32(E.xin16[o + r0]);
     const float x1 = E.xin32 ? __ldcg(E.xin32 + o + r1) : bf16_bits_to_f32(E.xin16[o + r1]);
-    P.y[o + r0] = x0 + v0;
-    P.y[o + r1] = x1 + v1;
+    const float y0 = x0 + v0, y1 = x1 + v1;
+    P.y[o + r0] = y0;
+    P.y[o + r1] = y1;
+    // the gate/up stage scales its staged x by this max of |y * norm2|
+    const uint16_t* w2 = sp().layers[E.layer].norm2;
+    const float m = fmaxf(fabsf(y0 * epi_norm(P, w2, r0)), fabsf(y1 * epi_norm(P, w2, r1)));
+    atomicMax(&M.cmax[t], __float_as_uint(m));
   } else if (E.st == ST_GU) {
     const float r = M.rnorm[t], gt = v0 * r, up = v1 * r;
-    P.a[(int64_t)t * P.dff + 8 * T + g] = gt / (1.0f + expf(-gt)) * up;
+    const float av = gt / (1.0f + expf(-gt)) * up;
+    P.a[(int64_t)t * P.dff + 8 * T + g] = av;
+    atomicMax(&M.cmax[t], __float_as_uint(fabsf(av)));
   } else {
     const int r0 = 16 * T + g, r1 = r0 + 8;
     const int64_t o = (int64_t)t * P.D;
     const float z0 = __ldcg(P.y + o + r0) + v0, z1 = __ldcg(P.y + o + r1) + v1;
     E.zout[o + r0] = z0;
     E.zout[o + r1] = z1;
+    if (E.layer + 1 < P.L) {  // the next layer's QKV scales its staged x by max |z * norm1|
+      const uint16_t* w1 = sp().layers[E.layer + 1].norm1;
+      const float m = fmaxf(fabsf(z0 * epi_norm(P, w1, r0)), fabsf(z1 * epi_norm(P, w1, r1)));
+      atomicMax(&M.cmax[t], __float_as_uint(m));
+    }
     if (E.final_layer) {
       if (P.resid_out) {
         P.resid_out[o + r0] = z0;
@@ -546,7 +610,7 @@ __device__ __noinline__ void gemv_epilogue(const Params& P, const GemvCtx& E, in
 // Sum the partials of tile T in slot order (panel, then warp; 8 loads in
 // flight) and run its epilogue.
 template <int HD>
-__device__ __noinline__ void gemv_fixup(const Params& P, const GemvCtx& E, int T, const Misc& M) {
+__device__ __noinline__ void gemv_fixup(const Params& P, const GemvCtx& E, int T, Misc& M) {
   const MatGeom& m = E.m;
   const int lane = threadIdx.x & 31;
   const float2* part = reinterpret_cast<const float2*>(P.gpart) + (int64_t)T * m.NP * m.J * 32 + lane;
@@ -573,7 +637,7 @@ __device__ __noinline__ void gemv_fixup(const Params& P, const GemvCtx& E, int T
 // that brings a counter to G finishes that tile.
 template <int HD>
 __device__ __noinline__ void gemv_publish(const Params& P, const GemvCtx& E, const uint32_t* pend,
-                                          int npend, const Misc& M) {
+                                          int npend, Misc& M) {
   const int lane = threadIdx.x & 31;
   __syncwarp();
   __threadfence();
@@ -596,7 +660,7 @@ __device__ __noinline__ void gemv_publish(const Params& P, const GemvCtx& E, con
 // otherwise the partial goes to slot (T, panel, warp - first warp of the tile
 // in the panel) and the tile is queued for publication.
 template <int HD>
-__device__ __forceinline__ void tile_finish(const Params& P, const GemvCtx& E, const Misc& M, int T,
+__device__ __forceinline__ void tile_finish(const Params& P, const GemvCtx& E, Misc& M, int T,
                                             uint32_t nblk, float v0, float v1, uint32_t* pend,
                                             int& npend) {
   const MatGeom& m = E.m;
@@ -843,7 +907,8 @@ __device__ __noinline__ void merge_records(const float* recs, int REC, int first
 // Phase 2: thread (h, d-quad) sums factor * o over the records, 8 loads in
 // flight.
 template <int HD>
-__device__ __noinline__ void merge_sequence(const Params& P, int64_t seq, int64_t Ta, int64_t C, float* fac) {
+__device__ __noinline__ void merge_sequence(const Params& P, int64_t seq, int64_t Ta, int64_t C, float* fac,
+                                            Misc& M) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int GH = P.GH, REC = att_rec_floats(GH, HD), nt = P.nt_att;
   const int64_t cf = owner_of(Ta, C, seq * nt), cl = owner_of(Ta, C, seq * nt + nt - 1);
@@ -894,6 +959,8 @@ __device__ __noinline__ void merge_sequence(const Params& P, int64_t seq, int64_
     }
     float* dst = P.attn + b * P.Hq * HD + (kvh * GH + h) * HD;
     reinterpret_cast<float4*>(dst)[dq] = acc;
+    const float m = fmaxf(fmaxf(fabsf(acc.x), fabsf(acc.y)), fmaxf(fabsf(acc.z), fabsf(acc.w)));
+    atomicMax(&M.cmax[b], __float_as_uint(m));  // the Wo stage scales its staged x by this
   }
   __syncthreads();
 }
@@ -924,7 +991,7 @@ __device__ __forceinline__ void att_flush(const Params& P, float* rec, const flo
 // record slot rec_idx (continuing into later warps when the run does) into
 // the sequence's partial of this CTA.
 template <int HD>
-__device__ __noinline__ void att_chain(const Params& P, const Misc& M, const float* recs, int64_t seq,
+__device__ __noinline__ void att_chain(const Params& P, Misc& M, const float* recs, int64_t seq,
                           int rec_idx, bool continues, int64_t Ta, int64_t C) {
   const int warp = threadIdx.x >> 5, GH = P.GH, REC = att_rec_floats(GH, HD), nt = P.nt_att;
   uint32_t vmask = 0;
@@ -1136,9 +1203,19 @@ __device__ __forceinline__ bool stage_att_body(const Params& P, int layer, Ring&
     __syncthreads();
     float* fac = recs + NW * 2 * REC;  // per (head, record) factors of the merge
     for (int64_t sq = s0; sq <= s1; ++sq)
-      if (M.mseq[(int)(sq - s0)] == sq) merge_sequence<HD>(P, sq, Ta, C, fac);
+      if (M.mseq[(int)(sq - s0)] == sq) merge_sequence<HD>(P, sq, Ta, C, fac, M);
   }
   return true;
+}
+
+// This CTA's maximum of its stage output (times the consumer's norm weight)
+// to the consumer stage's word, for sequence threadIdx.x.
+__device__ __noinline__ void flush_cmax(const Params& P, Misc& M, int layer, int st) {
+  const int cl = st == ST_DOWN ? layer + 1 : layer;
+  const int cs = st == ST_ATT ? ST_WO : st == ST_WO ? ST_GU : st == ST_GU ? ST_DOWN : ST_QKV;
+  if (st != ST_QKV && cl < P.L && M.cmax[threadIdx.x] != 0u)
+    atomicMax(P.xmax + (cl * NSTAGE + cs) * MAX_B + threadIdx.x, M.cmax[threadIdx.x]);
+  M.cmax[threadIdx.x] = 0u;
 }
 
 // ------------------------------------------------------------------ grid barrier
@@ -1193,6 +1270,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) decode_kernel(const __grid_consta
   if (threadIdx.x == 0) {
     M.abort = 0;
   }
+  if (threadIdx.x < MAX_B) M.cmax[threadIdx.x] = 0u;
   mbar_init_fence();
   __syncthreads();
   const uint64_t policy = policy_evict_first();
@@ -1235,6 +1313,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) decode_kernel(const __grid_consta
     __syncthreads();
     if (threadIdx.x == 0) trace_stamp(P, s, NW + 2);
     if (M.abort) ok = false;
+    if (threadIdx.x < P.B) flush_cmax(P, M, layer, st);
   }
   if (!ok) {  // let this warp's copies in flight land before the CTA exits (bounded)
     __syncwarp();
@@ -1293,7 +1372,7 @@ static int device_info(DevInfo& out) {
 }
 
 struct WsLayout {
-  int64_t ctrl, cnt, seqcnt, gpart, apart, Z, q, attn, y, a, total;
+  int64_t ctrl, cnt, seqcnt, xmax, gpart, apart, Z, q, attn, y, a, total;
 };
 
 static int64_t att_J(int64_t seqs, int64_t nt, int64_t C) {
@@ -1323,6 +1402,7 @@ static void ws_layout(const ddl_shape& s, int B, int64_t s_max, int C, const Mat
   w.ctrl = off;  off = align256(off + 256);
   w.cnt = off;   off = align256(off + ntmax * 4);
   w.seqcnt = off; off = align256(off + (int64_t)B * s.H_kv * 4);
+  w.xmax = off;  off = align256(off + (int64_t)MAX_LAYERS * NSTAGE * MAX_B * 4);
   w.gpart = off; off = align256(off + gpart);
   w.apart = off; off = align256(off + (int64_t)B * s.H_kv * (Jatt + 1) * att_rec_floats(GH, s.head_dim) * 4);
   w.Z = off;     off = align256(off + 2 * (int64_t)B * s.D * 4);
@@ -1400,6 +1480,7 @@ static int decode(const ddl_shape* s, ddl_wtype wtype, const ddl_layer_w* layers
   P.resid_in = resid_in; P.x_bf16 = x_bf16; P.resid_out = resid_out; P.out_bf16 = out_bf16;
   P.ctrl = (uint32_t*)(ws + w.ctrl); P.cnt = (uint32_t*)(ws + w.cnt);
   P.seqcnt = (uint32_t*)(ws + w.seqcnt);
+  P.xmax = (uint32_t*)(ws + w.xmax);
   P.gpart = (float*)(ws + w.gpart); P.apart = (float*)(ws + w.apart); P.Z = (float*)(ws + w.Z);
   P.q = (float*)(ws + w.q); P.attn = (float*)(ws + w.attn); P.y = (float*)(ws + w.y);
   P.a = (float*)(ws + w.a);
@@ -1423,6 +1504,8 @@ static int decode(const ddl_shape* s, ddl_wtype wtype, const ddl_layer_w* layers
     }
     const size_t need_trace = (size_t)nL * NSTAGE * C * TRACE_WORDS * 8;
     P.trace = (g_trace && g_trace_bytes >= need_trace && L <= MAX_LAYERS) ? g_trace : nullptr;
+    if (l0 > 0 && (e = cudaMemsetAsync(ws + w.xmax, 0, (size_t)(w.gpart - w.xmax), cs)) != cudaSuccess)
+      return cuda_status(e);  // maxima are per launch (its first layer finds its own)
     if (coop) {
       if (l0 > 0 && (e = cudaMemsetAsync(ws + w.ctrl, 0, 4, cs)) != cudaSuccess) return cuda_status(e);
       P.stage_begin = 0;

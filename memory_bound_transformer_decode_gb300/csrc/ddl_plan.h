@@ -197,6 +197,7 @@ struct Params {
   uint32_t* ctrl;       // [0] grid barrier counter, [1] status word
   uint32_t* cnt;        // per-tile arrival counters
   uint32_t* seqcnt;     // per-sequence arrival counters of the attention merge
+  uint32_t* xmax;       // [layer][stage][MAX_B] bits of max |x * norm weight| of a stage's input, from its producer
   float* gpart;         // GEMV partials: [tile][panel][J][32 lanes][2]
   float* apart;         // attention partials: [seq][J_att][GH*(hd+2)]
   float* Z;             // [2][B][D] residual ping-pong between layers
