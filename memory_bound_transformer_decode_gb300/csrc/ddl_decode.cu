@@ -56,7 +56,7 @@ constexpr int SM_MISC = SM_NW + SM_NW_BYTES;
 constexpr int SM_MISC_BYTES = 2048;
 constexpr int SM_SPAR = SM_MISC + SM_MISC_BYTES;             // copies of the indexed parameters
 constexpr int SM_CTX = SM_SPAR + (((int)sizeof(SParams) + 255) & ~255);  // stage context, warp cursors
-constexpr int SM_CTX_BYTES = 2048;
+constexpr int SM_CTX_BYTES = 4096;
 constexpr int SM_TOTAL = SM_CTX + SM_CTX_BYTES;
 constexpr int XZ_OFF = XF_BYTES + SX_BYTES + NW * 32 * 4;  // zero x fragments for blocks past a slot's end
 constexpr int XZ_BYTES = 3 * 2 * MAX_B * 32 + 256;          // 3 j-strides + one lane span
@@ -123,10 +123,18 @@ struct GemvCtx {
 // CTA-wide state in shared memory, so that nothing lives in local memory:
 // the current weight stage's context and each warp's ring and producer
 // cursor between stages.
+// A warp's place in each stage kind, the same for every layer of a launch:
+// computed once at launch so that entering a stage costs no divisions.
+struct Entry {
+  uint32_t lo, hi;           // work range: GEMV panel work indices, ATT 16-key tiles
+  int32_t T, kc, gi, gk;     // GEMV: (tile, k-chunk, group) at lo and the chunk's groups
+  int16_t p, cl, pk0, pk1;   // GEMV: panel, CTA index in the panel, the panel's k-chunks
+};
 struct Ctx {
   GemvCtx E;
   Ring ring[NW];
   Cursor cur[NW];
+  Entry ent[NW][NSTAGE];
 };
 static_assert(sizeof(Ctx) <= SM_CTX_BYTES, "context");
 __device__ __forceinline__ Ctx& ctx() { return *reinterpret_cast<Ctx*>(g_smem + SM_CTX); }
@@ -139,35 +147,69 @@ __device__ __forceinline__ void att_range(const Params& P, int64_t& lo, int64_t&
   lo = clo + range_lo(chi - clo, NW, w);
   hi = clo + range_lo(chi - clo, NW, w + 1);
 }
+// Compute this warp's entry for every stage kind (once per launch).
+__device__ __noinline__ void compute_entries(const Params& P) {
+  const int warp = threadIdx.x >> 5;
+  for (int st = 0; st < NSTAGE; ++st) {
+    Entry e;
+    if (st == ST_ATT) {
+      int64_t lo, hi;
+      att_range(P, lo, hi);
+      e.lo = (uint32_t)lo;
+      e.hi = (uint32_t)hi;
+      e.T = e.kc = e.gi = e.gk = 0;
+      e.p = e.cl = e.pk0 = e.pk1 = 0;
+    } else {
+      const MatGeom& m = sp().mg[stage_mat(st)];
+      const int p = panel_of_cta(m, blockIdx.x);
+      uint32_t lo, hi;
+      warp_work(m, p, blockIdx.x - m.pc[p], warp, NW, lo, hi);
+      e.lo = lo;
+      e.hi = hi;
+      e.p = (int16_t)p;
+      e.cl = (int16_t)(blockIdx.x - m.pc[p]);
+      e.pk0 = m.pk[p];
+      e.pk1 = m.pk[p + 1];
+      e.T = e.kc = e.gi = 0;
+      e.gk = 1;
+      if (lo < hi) {
+        int T, kc, gi;
+        work_coord(m, p, lo, T, kc, gi);
+        e.T = T;
+        e.kc = kc;
+        e.gi = gi;
+        e.gk = chunk_groups(m, kc);
+      }
+    }
+    if ((threadIdx.x & 31) == 0) ctx().ent[warp][st] = e;
+  }
+}
 template <int WT>
-__device__ __noinline__ void cursor_enter(const Params& P, Cursor& c, int64_t wg, int64_t W) {
+__device__ __forceinline__ void cursor_enter(const Params& P, Cursor& c) {
   const int st = c.s % NSTAGE;
   const LayerDev& Ld = sp().layers[c.s / NSTAGE];
+  const Entry& e = ctx().ent[threadIdx.x >> 5][st];
+  c.pos = e.lo;
+  c.end = e.hi;
   if (st == ST_ATT) {
-    att_range(P, c.pos, c.end);
     c.pos *= 2;
     c.end *= 2;
     c.kbase = Ld.kc;
     c.vbase = Ld.vc;
   } else {
     const MatGeom& m = sp().mg[stage_mat(st)];
-    const int p = panel_of_cta(m, blockIdx.x);
-    uint32_t lo, hi;
-    warp_work(m, p, blockIdx.x - m.pc[p], threadIdx.x >> 5, NW, lo, hi);
-    c.pos = lo;
-    c.end = hi;
     c.wbase = Ld.packed + m.woff;
     c.sbase = Ld.packed + m.soff;
     c.NT = m.NT;
     c.Sk = m.Sk;
     c.Gc = m.Gc;
     c.G = m.G;
-    c.pk0 = m.pk[p];
-    c.pk1 = m.pk[p + 1];
-    if (lo < hi) {
-      work_coord(m, p, lo, c.T, c.kc, c.gi);
-      c.gk = chunk_groups(m, c.kc);
-    }
+    c.pk0 = e.pk0;
+    c.pk1 = e.pk1;
+    c.T = e.T;
+    c.kc = e.kc;
+    c.gi = e.gi;
+    c.gk = e.gk;
   }
 }
 template <int WT>
@@ -175,15 +217,7 @@ __device__ __forceinline__ bool cursor_next(const Params& P, Cursor& c, int64_t 
                                             SlotDesc& d) {
   while (c.pos >= c.end) {
     if (++c.s >= P.stage_end) return false;
-    // through this warp's shared copy: a reference to registers would put
-    // the cursor in local memory
-    Cursor& cs = ctx().cur[threadIdx.x >> 5];
-    __syncwarp();
-    cs = c;
-    __syncwarp();
-    cursor_enter<WT>(P, cs, wg, W);
-    __syncwarp();
-    c = cs;
+    cursor_enter<WT>(P, c);
   }
   if (c.s % NSTAGE == ST_ATT) {
     const int64_t tile = c.pos >> 1;
@@ -715,8 +749,8 @@ __device__ __forceinline__ bool stage_gemv_body(const Params& P, int layer, int 
     E.st = st;
     E.layer = layer;
     E.gl = P.l0 + layer;
-    E.p = panel_of_cta(E.m, blockIdx.x);
-    E.cl = blockIdx.x - E.m.pc[E.p];
+    E.p = ctx().ent[0][st].p;
+    E.cl = ctx().ent[0][st].cl;
     const LayerDev& Ld = sp().layers[layer];
     E.kc = Ld.kc;
     E.vc = Ld.vc;
@@ -736,8 +770,8 @@ __device__ __forceinline__ bool stage_gemv_body(const Params& P, int layer, int 
   gemv_prologue<HD, WT>(P, E, smem, M);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
   if (threadIdx.x == 0) trace_stamp(P, layer * NSTAGE + st, 1);
-  uint32_t lo, hi;
-  warp_work(m, E.p, E.cl, warp, NW, lo, hi);
+  const Entry& en = ctx().ent[warp][st];
+  const uint32_t lo = en.lo, hi = en.hi;
   if (lo >= hi) {
     if (lane == 0) trace_stamp(P, layer * NSTAGE + st, 2 + warp);
     return true;
@@ -750,9 +784,7 @@ __device__ __forceinline__ bool stage_gemv_body(const Params& P, int layer, int 
   const uint32_t xz = smem_addr(smem + SM_SCR + XZ_OFF) + (g * 4 + t) * 8;
   const uint32_t sx_lane = smem_addr(smem + SM_SCR + XF_BYTES) + t * 4;
   const float esc = M.escale[t < B ? t : 0];
-  int kc, T, gi;
-  work_coord(m, E.p, lo, T, kc, gi);
-  int gk = chunk_groups(m, kc);
+  int kc = en.kc, T = en.T, gi = en.gi, gk = en.gk;
   float acc0 = 0.f, acc1 = 0.f, tac0 = 0.f, tac1 = 0.f;
   uint32_t nblk = 0;
   constexpr int PER = WT == DDL_W_INT4 ? BLKS_PER_SLOT : BF16_BLKS_PER_SLOT;
@@ -1035,8 +1067,7 @@ __device__ __forceinline__ bool stage_att_body(const Params& P, int layer, Ring&
   const int64_t Ta = (int64_t)P.B * P.Hkv * nt, C = gridDim.x;
   const LayerDev& Ld = sp().layers[layer];
   float* recs = reinterpret_cast<float*>(smem + SM_SCR);
-  int64_t lo, hi;
-  att_range(P, lo, hi);
+  const int64_t lo = ctx().ent[warp][ST_ATT].lo, hi = ctx().ent[warp][ST_ATT].hi;
   const float qscale = 1.4426950408889634f / sqrtf((float)HD);  // log2(e) / sqrt(hd)
   int nseg = 0;
   int64_t first_seq = -1, cur = -1;
@@ -1274,14 +1305,12 @@ __global__ void __launch_bounds__(NTHREADS, 1) decode_kernel(const __grid_consta
   mbar_init_fence();
   __syncthreads();
   const uint64_t policy = policy_evict_first();
+  compute_entries(P);
+  __syncwarp();
   {
     Cursor c;
     c.s = P.stage_begin;
-    prod.s = P.stage_begin;
-    __syncwarp();
-    cursor_enter<WT>(P, prod, wg, W);
-    __syncwarp();
-    c = prod;
+    cursor_enter<WT>(P, c);
     Ring r = R;
     for (int k = 0; k < DEPTH; ++k) {
       SlotDesc d;
