@@ -1253,8 +1253,10 @@ __device__ __noinline__ void flush_cmax(const Params& P, Misc& M, int layer, int
 __device__ bool grid_sync(const Params& P, uint32_t target, Misc& M) {
   __syncthreads();
   if (threadIdx.x == 0) {
-    __threadfence();
-    atomicAdd(P.ctrl, 1u);
+    // release: the CTA's writes of this stage (ordered before by the block
+    // barrier) become visible no later than the arrival; the acquiring poll
+    // below orders the next stage's reads after every CTA's arrival
+    red_release_gpu_add(P.ctrl, 1u);
     uint64_t t0 = 0;
     for (uint32_t it = 1; ld_acquire_gpu(P.ctrl) < target; ++it) {
       if ((it & 255u) != 0) continue;
@@ -1266,7 +1268,6 @@ __device__ bool grid_sync(const Params& P, uint32_t target, Misc& M) {
         break;
       }
     }
-    __threadfence();
   }
   __syncthreads();
   return !M.abort;

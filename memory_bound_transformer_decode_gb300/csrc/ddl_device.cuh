@@ -125,6 +125,11 @@ __device__ __forceinline__ float ldcg_f32(const float* p) { return __ldcg(p); }
 __device__ __forceinline__ uint4 ldcg_u128(const void* p) {
   return __ldcg(reinterpret_cast<const uint4*>(p));
 }
+// Add with release semantics at GPU scope, no value returned (the issuing
+// thread does not wait for it).
+__device__ __forceinline__ void red_release_gpu_add(uint32_t* p, uint32_t v) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
 __device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
   uint32_t v;
   asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
