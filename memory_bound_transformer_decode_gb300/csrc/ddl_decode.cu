@@ -935,7 +935,8 @@ __device__ __noinline__ void merge_records(const float* recs, int REC, int first
 
 // Final merge of all CTA records of one sequence into attn, by the last CTA
 // to finish it.  Phase 1: warp h < GH folds every record's (m, l) of head h
-// into per-record factors exp2(m_j - M) / L (one record per lane per step).
+// into per-record factors exp2(m_j - M) / L (one load round trip for up to 64
+// records).
 // Phase 2: thread (h, d-quad) sums factor * o over the records, 8 loads in
 // flight.
 template <int HD>
@@ -946,21 +947,36 @@ __device__ __noinline__ void merge_sequence(const Params& P, int64_t seq, int64_
   const int64_t cf = owner_of(Ta, C, seq * nt), cl = owner_of(Ta, C, seq * nt + nt - 1);
   const int n = (int)(cl - cf + 1);
   const float* base = P.apart + seq * P.J_att * REC;
+  // with more tiles than CTAs every CTA of the sequence holds a record; with
+  // fewer, a CTA whose tile range is empty holds none
+  const bool all_full = Ta >= C;
   if (warp < GH) {
-    float mx = -INFINITY;
-    for (int j = lane; j < n; j += 32) {
-      const bool ok = range_lo(Ta, C, cf + j) != range_lo(Ta, C, cf + j + 1);
-      if (ok) mx = fmaxf(mx, __ldcg(base + (int64_t)j * REC + GH * HD + warp));
+    // one round trip for the (m, l) of up to 64 records per lane pair
+    float mj[2], lj[2];
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const int j = lane + 32 * u;
+      const bool ok = j < n && (all_full || range_lo(Ta, C, cf + j) != range_lo(Ta, C, cf + j + 1));
+      mj[u] = ok ? __ldcg(base + (int64_t)j * REC + GH * HD + warp) : -INFINITY;
+      lj[u] = ok ? __ldcg(base + (int64_t)j * REC + GH * HD + GH + warp) : 0.f;
     }
-    mx = warp_max(mx);
+    for (int j0 = 64; j0 < n; j0 += 32) {  // more than 64 CTAs per sequence: the rest
+      const int j = j0 + lane;
+      const bool ok = j < n && (all_full || range_lo(Ta, C, cf + j) != range_lo(Ta, C, cf + j + 1));
+      if (ok) mj[0] = fmaxf(mj[0], __ldcg(base + (int64_t)j * REC + GH * HD + warp));
+    }
+    const float mx = warp_max(fmaxf(mj[0], mj[1]));
     float l = 0.f;
     for (int j = lane; j < n; j += 32) {
-      const bool ok = range_lo(Ta, C, cf + j) != range_lo(Ta, C, cf + j + 1);
       float fj = 0.f;
-      if (ok) {
+      if (j < 64) {
+        const float m = j < 32 ? mj[0] : mj[1];
+        fj = m == -INFINITY ? 0.f : exp2f(m - mx);
+        l = fmaf(fj, j < 32 ? lj[0] : lj[1], l);
+      } else if (all_full || range_lo(Ta, C, cf + j) != range_lo(Ta, C, cf + j + 1)) {
         const float* rec = base + (int64_t)j * REC;
         fj = exp2f(__ldcg(rec + GH * HD + warp) - mx);
-        l += fj * __ldcg(rec + GH * HD + GH + warp);
+        l = fmaf(fj, __ldcg(rec + GH * HD + GH + warp), l);
       }
       fac[warp * P.J_att + j] = fj;
     }
@@ -1222,14 +1238,13 @@ __device__ __forceinline__ bool stage_att_body(const Params& P, int layer, Ring&
   const int64_t clo = range_lo(Ta, C, blockIdx.x), chi = range_lo(Ta, C, blockIdx.x + 1);
   if (clo < chi) {
     const int64_t s0 = clo / nt, s1 = (chi - 1) / nt;
-    if (threadIdx.x == 0) {
-      for (int64_t sq = s0; sq <= s1; ++sq) {
-        const int64_t cf = owner_of(Ta, C, sq * nt), cl = owner_of(Ta, C, sq * nt + nt - 1);
-        const uint32_t n = (uint32_t)(Ta >= C ? cl - cf + 1 : nt);
-        const uint32_t old = atom_add_acq_rel(P.seqcnt + sq, 1u);
-        M.mseq[(int)(sq - s0)] = old == n - 1 ? sq : -1;
-        if (old == n - 1) P.seqcnt[sq] = 0;
-      }
+    if (threadIdx.x <= s1 - s0) {  // one thread per sequence: the arrivals in flight together
+      const int64_t sq = s0 + threadIdx.x;
+      const int64_t cf = owner_of(Ta, C, sq * nt), cl = owner_of(Ta, C, sq * nt + nt - 1);
+      const uint32_t n = (uint32_t)(Ta >= C ? cl - cf + 1 : nt);
+      const uint32_t old = atom_add_acq_rel(P.seqcnt + sq, 1u);
+      M.mseq[threadIdx.x] = old == n - 1 ? sq : -1;
+      if (old == n - 1) P.seqcnt[sq] = 0;
     }
     __syncthreads();
     float* fac = recs + NW * 2 * REC;  // per (head, record) factors of the merge
