@@ -76,6 +76,10 @@ struct Misc {
   int seg_n[NW];
   long long seg_first[NW], seg_last[NW];
   long long mseq[8];       // sequences this CTA merges last
+  int nruns;               // CTA merge: runs of warp records of one sequence
+  int run_first[2 * NW];
+  uint32_t run_vmask[2 * NW];
+  long long run_seq[2 * NW], run_out[2 * NW];
   uint32_t cmax[MAX_B];    // running max |output * consumer norm weight| of this stage (float bits)
 };
 static_assert(sizeof(Misc) <= SM_MISC_BYTES, "misc");
@@ -897,39 +901,36 @@ __device__ __forceinline__ bool stage_gemv_body(const Params& P, int layer, int 
 }
 
 // ------------------------------------------------------------------ attention
-// Merge softmax states (m, l, o) of the CTA's shared records into `out`
-// (fp32 records of GH*(hd+2) padded to REC floats): record `first`, then
-// record 2v of every warp v in vmask.  Head by head: M = max m_k,
-// f_k = exp2(m_k - M), l = sum f_k l_k, o = sum f_k o_k.  Lane d handles
-// head dims d, d+32, ...
+// Merge head h of the CTA's shared softmax records (m, l, o; fp32 records of
+// GH*(hd+2) padded to REC floats) into `out`: record `first`, then record 2v
+// of every warp v in vmask.  M = max m_k, f_k = exp2(m_k - M),
+// l = sum f_k l_k, o = sum f_k o_k.  Lane d handles head dims d, d+32, ...
 template <int HD>
-__device__ __noinline__ void merge_records(const float* recs, int REC, int first, uint32_t vmask,
-                                           float* out, int GH) {
+__device__ __forceinline__ void merge_head(const float* recs, int REC, int first, uint32_t vmask,
+                                           float* out, int GH, int h) {
   const int lane = threadIdx.x & 31;
-  for (int h = 0; h < GH; ++h) {
-    float mx = recs[first * REC + GH * HD + h];
-    for (uint32_t mm = vmask; mm; mm &= mm - 1)
-      mx = fmaxf(mx, recs[2 * (__ffs(mm) - 1) * REC + GH * HD + h]);
-    float acc[HD / 32], l = 0.f;
+  float mx = recs[first * REC + GH * HD + h];
+  for (uint32_t mm = vmask; mm; mm &= mm - 1)
+    mx = fmaxf(mx, recs[2 * (__ffs(mm) - 1) * REC + GH * HD + h]);
+  float acc[HD / 32], l = 0.f;
 #pragma unroll
-    for (int dd = 0; dd < HD / 32; ++dd) acc[dd] = 0.f;
-    int ri = first;
-    for (uint32_t mm = vmask;;) {
-      const float* r = recs + ri * REC;
-      const float f = exp2f(r[GH * HD + h] - mx);
-      l = fmaf(f, r[GH * HD + GH + h], l);
+  for (int dd = 0; dd < HD / 32; ++dd) acc[dd] = 0.f;
+  int ri = first;
+  for (uint32_t mm = vmask;;) {
+    const float* r = recs + ri * REC;
+    const float f = exp2f(r[GH * HD + h] - mx);
+    l = fmaf(f, r[GH * HD + GH + h], l);
 #pragma unroll
-      for (int dd = 0; dd < HD / 32; ++dd) acc[dd] = fmaf(f, r[h * HD + lane + 32 * dd], acc[dd]);
-      if (!mm) break;
-      ri = 2 * (__ffs(mm) - 1);
-      mm &= mm - 1;
-    }
+    for (int dd = 0; dd < HD / 32; ++dd) acc[dd] = fmaf(f, r[h * HD + lane + 32 * dd], acc[dd]);
+    if (!mm) break;
+    ri = 2 * (__ffs(mm) - 1);
+    mm &= mm - 1;
+  }
 #pragma unroll
-    for (int dd = 0; dd < HD / 32; ++dd) out[h * HD + lane + 32 * dd] = acc[dd];
-    if (lane == 0) {
-      out[GH * HD + h] = mx;
-      out[GH * HD + GH + h] = l;
-    }
+  for (int dd = 0; dd < HD / 32; ++dd) out[h * HD + lane + 32 * dd] = acc[dd];
+  if (lane == 0) {
+    out[GH * HD + h] = mx;
+    out[GH * HD + GH + h] = l;
   }
 }
 
@@ -1033,26 +1034,6 @@ __device__ __forceinline__ void att_flush(const Params& P, float* rec, const flo
       rec[GH * HD + GH + g] = ls;
     }
   }
-}
-
-// Merge the run of CTA records of sequence `seq` that starts at this warp's
-// record slot rec_idx (continuing into later warps when the run does) into
-// the sequence's partial of this CTA.
-template <int HD>
-__device__ __noinline__ void att_chain(const Params& P, Misc& M, const float* recs, int64_t seq,
-                          int rec_idx, bool continues, int64_t Ta, int64_t C) {
-  const int warp = threadIdx.x >> 5, GH = P.GH, REC = att_rec_floats(GH, HD), nt = P.nt_att;
-  uint32_t vmask = 0;
-  if (continues) {
-    for (int v = warp + 1; v < NW; ++v) {
-      if (M.seg_n[v] == 0) continue;
-      if (M.seg_first[v] != seq) break;
-      vmask |= 1u << v;
-      if (M.seg_n[v] > 1) break;
-    }
-  }
-  float* out = P.apart + (seq * P.J_att + (blockIdx.x - owner_of(Ta, C, seq * nt))) * REC;
-  merge_records<HD>(recs, REC, warp * 2 + rec_idx, vmask, out, GH);
 }
 
 template <int HD, int WT>
@@ -1221,18 +1202,36 @@ __device__ __forceinline__ bool stage_att_body(const Params& P, int layer, Ring&
   }
   __syncthreads();
   if (M.abort) return false;
-  // CTA merge: the warp where a sequence's run starts merges the run
-  const int ns = M.seg_n[warp];
-  if (ns > 0) {
-    bool owner = true;
-    for (int v = warp - 1; v >= 0; --v) {
-      if (M.seg_n[v] == 0) continue;
-      owner = M.seg_last[v] != first_seq;
-      break;
+  // CTA merge: runs of consecutive warp records of one sequence (found by
+  // thread 0), each merged head by head with the heads spread over the warps
+  if (threadIdx.x == 0) {
+    int nr = 0;
+    for (int w = 0; w < NW; ++w) {
+      const int n = M.seg_n[w];
+      if (n == 0) continue;
+      if (nr > 0 && M.run_seq[nr - 1] == M.seg_first[w]) {
+        M.run_vmask[nr - 1] |= 1u << w;  // record 2w continues the open run
+      } else {
+        M.run_seq[nr] = M.seg_first[w];
+        M.run_first[nr] = 2 * w;
+        M.run_vmask[nr] = 0u;
+        ++nr;
+      }
+      if (n > 1) {  // the warp's last segment starts a new run (record 2w+1)
+        M.run_seq[nr] = M.seg_last[w];
+        M.run_first[nr] = 2 * w + 1;
+        M.run_vmask[nr] = 0u;
+        ++nr;
+      }
     }
-    if (owner) att_chain<HD>(P, M, recs, first_seq, 0, ns == 1, Ta, C);
-    if (ns > 1) att_chain<HD>(P, M, recs, cur, 1, true, Ta, C);
+    for (int r = 0; r < nr; ++r)
+      M.run_out[r] = (M.run_seq[r] * P.J_att + (blockIdx.x - owner_of(Ta, C, M.run_seq[r] * nt))) * REC;
+    M.nruns = nr;
   }
+  __syncthreads();
+  for (int r = 0; r < M.nruns; ++r)
+    for (int h = warp; h < GH; h += NW)
+      merge_head<HD>(recs, REC, M.run_first[r], M.run_vmask[r], P.apart + M.run_out[r], GH, h);
   // the last CTA to publish a sequence's record merges the sequence
   __syncthreads();
   const int64_t clo = range_lo(Ta, C, blockIdx.x), chi = range_lo(Ta, C, blockIdx.x + 1);
