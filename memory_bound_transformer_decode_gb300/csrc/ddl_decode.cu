@@ -28,6 +28,8 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <cudaTypedefs.h>
+
 #include "ddl_device.cuh"
 #include "ddl_internal.h"
 
@@ -64,6 +66,8 @@ static_assert(XZ_OFF + XZ_BYTES <= SM_SCR_BYTES, "x fragments do not fit");
 static_assert(NW * 2 * (MAX_GH * (128 + 2) + 3) * 4 <= SM_SCR_BYTES, "attention records do not fit");
 static_assert(SM_TOTAL <= 227 * 1024, "shared memory budget");
 static_assert(SM_SPAR % 16 == 0, "parameter copy alignment");
+static_assert(sizeof(Params) <= 32000, "kernel parameters (with the K/V tensor maps) exceed the launch limit");
+static_assert(SLOT_BYTES % 1024 == 512 || SLOT_BYTES % 1024 == 0, "K/V boxes need 512-byte aligned slots");
 __device__ __forceinline__ const SParams& sp() { return *reinterpret_cast<const SParams*>(g_smem + SM_SPAR); }
 
 struct Misc {
@@ -100,6 +104,8 @@ struct Cursor {
   const uint8_t* sbase;   // GEMV: scale stream (INT4)
   const uint16_t* kbase;  // ATT: K cache of the layer
   const uint16_t* vbase;  // ATT: V cache of the layer
+  const void* kmap;       // ATT: tensor maps of the layer's caches
+  const void* vmap;
   int kc, T, gi, gk;      // GEMV: (k-chunk, tile, group) of work index `pos`
   int NT, Sk, Gc, G;      // GEMV: geometry of the matrix
   int pk0, pk1;           // GEMV: k-chunks of this CTA's panel
@@ -200,6 +206,8 @@ __device__ __forceinline__ void cursor_enter(const Params& P, Cursor& c) {
     c.end *= 2;
     c.kbase = Ld.kc;
     c.vbase = Ld.vc;
+    c.kmap = &P.kmap[c.s / NSTAGE];
+    c.vmap = &P.vmap[c.s / NSTAGE];
   } else {
     const MatGeom& m = sp().mg[stage_mat(st)];
     c.wbase = Ld.packed + m.woff;
@@ -252,10 +260,15 @@ __device__ __forceinline__ bool cursor_next(const Params& P, Cursor& c, int64_t 
   return true;
 }
 
+// Shared address of 16-byte chunk `ch` (head dims 8ch..8ch+7) of row r of a
+// K/V slot: quarter ch/4 of the row sits in its own 1 KB box of 16 rows x 64
+// bytes, chunk ch%4 XOR-ed with bits 1-2 of the row (the 64-byte swizzle).
+__device__ __forceinline__ uint32_t kv_addr(uint32_t slot, int r, int ch) {
+  return slot + (ch >> 2) * 1024 + r * 64 + (((ch & 3) ^ ((r >> 1) & 3)) << 4);
+}
 template <int HD, int WT>
 __device__ __forceinline__ void issue_slot(const Params& P, const Cursor& c, const SlotDesc& d,
                                            uint32_t slot, uint32_t bar, int lane, uint64_t policy) {
-  constexpr int ROWB = HD * 2 + 16;
   if (d.kind == SK_GEMV) {
     if (lane == 0) {
       constexpr bool q4 = WT == DDL_W_INT4;
@@ -265,11 +278,12 @@ __device__ __forceinline__ void issue_slot(const Params& P, const Cursor& c, con
       bulk_g2s_evict_first(slot, c.wbase + d.a * BB, wb, bar, policy);
       if (q4) bulk_g2s_evict_first(slot + BLKS_PER_SLOT * BLK_BYTES, c.sbase + d.a * SCL_BYTES, sb, bar, policy);
     }
-  } else {
+  } else {  // 16 rows of K or V: HD/32 boxes of 16 rows x 64 bytes, swizzled (kv_addr)
     const uint32_t seq = (uint32_t)d.a / (uint32_t)P.nt_att, i = (uint32_t)d.a - seq * (uint32_t)P.nt_att;
-    const uint16_t* base = (d.kind == SK_K ? c.kbase : c.vbase) + ((int64_t)seq * P.s_max + 16 * i) * HD;
-    if (lane == 0) mbar_arrive_expect_tx(bar, d.cnt * HD * 2);
-    if (lane < d.cnt) bulk_g2s_evict_first(slot + lane * ROWB, base + lane * HD, HD * 2, bar, policy);
+    const int y = (int)((int64_t)seq * P.s_max + 16 * i);
+    if (lane == 0) mbar_arrive_expect_tx(bar, 16 * HD * 2);
+    if (lane < HD / 32)
+      tensor2d_g2s(slot + lane * 1024, d.kind == SK_K ? c.kmap : c.vmap, lane * 32, y, bar, policy);
   }
 }
 
@@ -1058,7 +1072,7 @@ template <int HD, int WT>
 __device__ __forceinline__ bool stage_att_body(const Params& P, int layer, Ring& R, Cursor& prod,
                                                int64_t wg, int64_t W, uint8_t* smem, Misc& M,
                                                uint64_t policy) {
-  constexpr int ROWB = HD * 2 + 16, KS = HD / 16, NB = HD / 8;
+  constexpr int KS = HD / 16, NB = HD / 8;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
   const int GH = P.GH, REC = att_rec_floats(GH, HD), nt = P.nt_att;
   const int64_t Ta = (int64_t)P.B * P.Hkv * nt, C = gridDim.x;
@@ -1121,14 +1135,16 @@ __device__ __forceinline__ bool stage_att_body(const Params& P, int layer, Ring&
       const int rnew = (int)(P.pos - 16 * (int64_t)i);
       const int b = (int)(seq / P.Hkv), kvh = (int)(seq % P.Hkv);
       const int64_t ro = (((int64_t)b * P.Hkv + kvh) * P.s_max + P.pos) * HD;
-      if (lane < HD / 8) sts128(ks + rnew * ROWB + lane * 16, ldcg_u128(Ld.kc + ro + lane * 8));
+      if (lane < HD / 8) sts128(kv_addr(ks, rnew, lane), ldcg_u128(Ld.kc + ro + lane * 8));
       else if (lane >= 16 && lane < 16 + HD / 8)
-        sts128(vs + rnew * ROWB + (lane - 16) * 16, ldcg_u128(Ld.vc + ro + (lane - 16) * 8));
+        sts128(kv_addr(vs, rnew, lane - 16), ldcg_u128(Ld.vc + ro + (lane - 16) * 8));
       const int nz = (15 - rnew) * (HD / 8);
       for (int z = lane; z < 2 * nz; z += 32) {
         const int zz = z % nz, row = rnew + 1 + zz / (HD / 8), col = zz % (HD / 8);
-        sts128((z < nz ? ks : vs) + row * ROWB + col * 16, make_uint4(0u, 0u, 0u, 0u));
+        sts128(kv_addr(z < nz ? ks : vs, row, col), make_uint4(0u, 0u, 0u, 0u));
       }
+      // these generic writes come before the slots' next bulk (async-proxy) fill
+      fence_proxy_async_smem();
       __syncwarp();
     }
     // scores: rows g = high-part dot products, rows g+8 = low-part ones
@@ -1140,7 +1156,7 @@ __device__ __forceinline__ bool stage_att_body(const Params& P, int layer, Ring&
       for (int jj = 0; jj < KS; jj += 2) {
         const int mat = lane >> 3, r = lane & 7;
         uint32_t b0, b1, b2, b3;
-        ldsm_x4(ks + (8 * n + r) * ROWB + (16 * (jj + (mat >> 1)) + 8 * (mat & 1)) * 2, b0, b1, b2, b3);
+        ldsm_x4(kv_addr(ks, 8 * n + r, 2 * (jj + (mat >> 1)) + (mat & 1)), b0, b1, b2, b3);
         mma_bf16(s[n], qa[jj][0], qa[jj][1], qa[jj][2], qa[jj][3], b0, b1);
         mma_bf16(s[n], qa[jj + 1][0], qa[jj + 1][1], qa[jj + 1][2], qa[jj + 1][3], b2, b3);
       }
@@ -1186,7 +1202,7 @@ __device__ __forceinline__ bool stage_att_body(const Params& P, int layer, Ring&
     for (int nb = 0; nb < NB; nb += 2) {
       const int mat = lane >> 3, r = lane & 7;
       uint32_t b0, b1, b2, b3;
-      ldsm_x4_t(vs + (8 * (mat & 1) + r) * ROWB + 8 * (nb + (mat >> 1)) * 2, b0, b1, b2, b3);
+      ldsm_x4_t(kv_addr(vs, 8 * (mat & 1) + r, nb + (mat >> 1)), b0, b1, b2, b3);
       mma_bf16(o[nb], pa0, pa1, pa2, pa3, b0, b1);
       mma_bf16(o[nb + 1], pa0, pa1, pa2, pa3, b2, b3);
     }
@@ -1469,6 +1485,35 @@ static int plan(const ddl_shape* s, int wtype, int B, int64_t s_max, int C, MatG
   return DDL_OK;
 }
 
+// cuTensorMapEncodeTiled from the driver, found once through the runtime.
+static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    cudaDriverEntryPointQueryResult q;
+    void* f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = (PFN_cuTensorMapEncodeTiled_v12000)f;
+  });
+  return fn;
+}
+// The [rows][hd] bf16 view of a K or V cache for 16-row x 32-column boxes
+// with the 64-byte swizzle (rows = B * H_kv * s_max).
+static int encode_kv_map(CUtensorMap* m, const uint16_t* base, int64_t rows, int hd) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (!enc) return DDL_ERR_CUDA;
+  const cuuint64_t dims[2] = {(cuuint64_t)hd, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)hd * 2};
+  const cuuint32_t box[2] = {32, 16};
+  const cuuint32_t es[2] = {1, 1};
+  const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(base), dims, strides,
+                         box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? DDL_OK : DDL_ERR_CUDA;
+}
+
 static int decode(const ddl_shape* s, ddl_wtype wtype, const ddl_layer_w* layers, const ddl_kv* kv,
                   int32_t L, int32_t B, int64_t pos, const float* resid_in, const uint16_t* x_bf16,
                   float* resid_out, uint16_t* out_bf16, void* workspace, size_t ws_bytes,
@@ -1545,6 +1590,10 @@ static int decode(const ddl_shape* s, ddl_wtype wtype, const ddl_layer_w* layers
       P.layers[l].norm2 = layers[l0 + l].norm2;
       P.layers[l].kc = kv[l0 + l].k;
       P.layers[l].vc = kv[l0 + l].v;
+      const int64_t rows = (int64_t)B * s->H_kv * s_max;
+      if ((st = encode_kv_map(&P.kmap[l], kv[l0 + l].k, rows, HD)) != DDL_OK ||
+          (st = encode_kv_map(&P.vmap[l], kv[l0 + l].v, rows, HD)) != DDL_OK)
+        return st;
     }
     const size_t need_trace = (size_t)nL * NSTAGE * C * TRACE_WORDS * 8;
     P.trace = (g_trace && g_trace_bytes >= need_trace && L <= MAX_LAYERS) ? g_trace : nullptr;

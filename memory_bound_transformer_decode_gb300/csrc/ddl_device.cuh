@@ -76,6 +76,16 @@ __device__ __forceinline__ void bulk_g2s_evict_first(uint32_t dst, const void* s
       "l"(src), "r"(bytes), "r"(bar), "l"(policy)
       : "memory");
 }
+// 2-D tensor copy of one box at (x, y) (x in elements; x times the element
+// size is a multiple of 16 bytes) into shared memory, completing on `bar`.
+__device__ __forceinline__ void tensor2d_g2s(uint32_t dst, const void* tmap, int x, int y, uint32_t bar,
+                                             uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+      "l"(tmap), "r"(x), "r"(y), "r"(bar), "l"(policy)
+      : "memory");
+}
 __device__ __forceinline__ uint64_t policy_evict_first() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));

@@ -28,6 +28,7 @@
 // atomic counter per tile), which sums the partial results in a fixed order:
 // results do not depend on timing.
 #pragma once
+#include <cuda.h>
 #include <stdint.h>
 
 #if defined(__CUDACC__)
@@ -41,7 +42,7 @@ namespace ddl {
 constexpr int NW = 8;                 // warps per CTA (each streams its own ring)
 constexpr int NTHREADS = NW * 32;
 constexpr int DEPTH = 3;              // ring slots per warp
-constexpr int SLOT_BYTES = 4352;      // 8 INT4 blocks + their scales, or 16 padded KV rows
+constexpr int SLOT_BYTES = 4608;      // 8 INT4 blocks + their scales, or 16 KV rows (512-byte aligned)
 constexpr int BLK_BYTES = 512;        // one INT4 block: 16 rows x 64 columns
 constexpr int SCL_BYTES = 32;         // scales of one block
 constexpr int BLKS_PER_SLOT = 8;
@@ -207,6 +208,10 @@ struct Params {
   float* a;             // [B][dff]
   uint64_t* trace;      // optional: per stage, CTA: start, prologue end, NW warp ends, end, 4 prologue steps (ns)
   LayerDev layers[MAX_LAYERS];
+  // 2-D views [B * H_kv * s_max rows][hd] of each layer's K and V caches for
+  // TMA tensor copies of 16 rows x 32 columns with the 64-byte swizzle
+  CUtensorMap kmap[MAX_LAYERS];
+  CUtensorMap vmap[MAX_LAYERS];
 };
 
 }  // namespace ddl
