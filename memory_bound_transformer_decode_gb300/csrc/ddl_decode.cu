@@ -707,6 +707,56 @@ __device__ __noinline__ void gemv_publish(const Params& P, const GemvCtx& E, con
   }
 }
 
+// Cooperative launch: tile T's owner (the warp holding its first blocks in
+// panel 0) finishes it.  It waits (bounded) until every other contributor has
+// released its partial, then sums all partials in slot order with its own in
+// its slot's place (deterministic) and runs the epilogue.
+template <int HD>
+__device__ __noinline__ void owner_fixup(const Params& P, const GemvCtx& E, int T, float o0, float o1,
+                                         Misc& M) {
+  const MatGeom& m = E.m;
+  const int lane = threadIdx.x & 31;
+  uint32_t expected = 0;
+  for (int p = 0; p < m.NP; ++p) {
+    const uint32_t Gp = panel_groups(m, p);
+    const uint32_t v0 = work_owner(m, p, (uint32_t)T * Gp, NW), v1 = work_owner(m, p, (uint32_t)(T + 1) * Gp - 1, NW);
+    for (uint32_t v = v0; v <= v1; ++v)
+      if ((p != 0 || v != v0) && !warp_empty(m, p, v, NW)) ++expected;
+  }
+  if (lane == 0) {
+    uint64_t t0 = 0;
+    for (uint32_t it = 1; ld_acquire_gpu(P.cnt + T) < expected; ++it) {
+      if ((it & 255u) != 0) continue;
+      const uint64_t now = globaltimer();
+      if (t0 == 0) t0 = now;
+      else if (now - t0 > WAIT_LIMIT_NS) {
+        atomicExch(P.ctrl + 1, STATUS_TIMEOUT);
+        M.abort = 1;
+        break;
+      }
+    }
+  }
+  __syncwarp();
+  const float2* part = reinterpret_cast<const float2*>(P.gpart) + (int64_t)T * m.NP * m.J * 32 + lane;
+  float s0 = 0.f, s1 = 0.f;
+  for (int p = 0; p < m.NP; ++p) {
+    const uint32_t Gp = panel_groups(m, p);
+    const uint32_t v0 = work_owner(m, p, (uint32_t)T * Gp, NW), v1 = work_owner(m, p, (uint32_t)(T + 1) * Gp - 1, NW);
+    for (uint32_t v = v0; v <= v1; ++v) {
+      if (p == 0 && v == v0) {
+        s0 += o0;
+        s1 += o1;
+      } else if (!warp_empty(m, p, v, NW)) {
+        const float2 x = __ldcg(part + ((int64_t)p * m.J + (v - v0)) * 32);
+        s0 += x.x;
+        s1 += x.y;
+      }
+    }
+  }
+  gemv_epilogue<HD>(P, E, T, s0, s1, M);
+  if (lane == 0) P.cnt[T] = 0;
+}
+
 // Finish this warp's share of tile T (nblk of its blocks, sums v0, v1 in true
 // scale): a warp that covered the whole tile runs the epilogue directly;
 // otherwise the partial goes to slot (T, panel, warp - first warp of the tile
@@ -714,7 +764,8 @@ __device__ __noinline__ void gemv_publish(const Params& P, const GemvCtx& E, con
 template <int HD>
 __device__ __forceinline__ void tile_finish(const Params& P, const GemvCtx& E, Misc& M, int T,
                                             uint32_t nblk, float v0, float v1, uint32_t* pend,
-                                            int& npend) {
+                                            int& npend, int& nown, int& oT0, float& oa0, float& ob0,
+                                            int& oT1, float& oa1, float& ob1) {
   const MatGeom& m = E.m;
   const int lane = threadIdx.x & 31;
   if (nblk == (uint32_t)m.G) {
@@ -723,8 +774,25 @@ __device__ __forceinline__ void tile_finish(const Params& P, const GemvCtx& E, M
   }
   const uint32_t me = (uint32_t)E.cl * NW + (threadIdx.x >> 5);
   const uint32_t first = work_owner(m, E.p, (uint32_t)T * panel_groups(m, E.p), NW);
+  if (P.cooperative && E.p == 0 && me == first) {  // the tile's owner: finish it at the end
+    if (nown == 0) {
+      oT0 = T; oa0 = v0; ob0 = v1;
+    } else if (nown == 1) {
+      oT1 = T; oa1 = v0; ob1 = v1;
+    } else {
+      owner_fixup<HD>(P, E, T, v0, v1, M);  // more than two: finish this one now
+      return;
+    }
+    ++nown;
+    return;
+  }
   const int64_t slot = ((int64_t)T * m.NP + E.p) * m.J + (me - first);
   reinterpret_cast<float2*>(P.gpart)[slot * 32 + lane] = make_float2(v0, v1);
+  if (P.cooperative) {  // release the partial to the tile's owner
+    __syncwarp();
+    if (lane == 0) red_release_gpu_add(P.cnt + T, 1u);
+    return;
+  }
   if (lane == 0) pend[npend] = (uint32_t)T | (nblk << 20);
   if (++npend == 32) {
     gemv_publish<HD>(P, E, pend, npend, M);
@@ -805,6 +873,8 @@ __device__ __forceinline__ bool stage_gemv_body(const Params& P, int layer, int 
   int kc = en.kc, T = en.T, gi = en.gi, gk = en.gk;
   float acc0 = 0.f, acc1 = 0.f, tac0 = 0.f, tac1 = 0.f;
   uint32_t nblk = 0;
+  int nown = 0, oT0 = 0, oT1 = 0;  // tiles this warp owns (cooperative launch), finished at the end
+  float oa0 = 0.f, ob0 = 0.f, oa1 = 0.f, ob1 = 0.f;
   constexpr int PER = WT == DDL_W_INT4 ? BLKS_PER_SLOT : BF16_BLKS_PER_SLOT;
   for (uint32_t b = lo; b < hi;) {
     // a slot holds nb consecutive groups gi.. of unit (kc, T) (see cursor_next)
@@ -898,7 +968,7 @@ __device__ __forceinline__ bool stage_gemv_body(const Params& P, int layer, int 
       acc0 = acc1 = 0.f;
       gi = 0;
       if (++kc == pk1) {  // end of the tile in this panel
-        tile_finish<HD>(P, E, M, T, nblk, tac0, tac1, pend, npend);
+        tile_finish<HD>(P, E, M, T, nblk, tac0, tac1, pend, npend, nown, oT0, oa0, ob0, oT1, oa1, ob1);
         tac0 = tac1 = 0.f;
         nblk = 0;
         kc = pk0;
@@ -908,8 +978,11 @@ __device__ __forceinline__ bool stage_gemv_body(const Params& P, int layer, int 
     }
   }
   if (nblk != 0)
-    tile_finish<HD>(P, E, M, T, nblk, fmaf(acc0, esc, tac0), fmaf(acc1, esc, tac1), pend, npend);
+    tile_finish<HD>(P, E, M, T, nblk, fmaf(acc0, esc, tac0), fmaf(acc1, esc, tac1), pend, npend, nown, oT0,
+                    oa0, ob0, oT1, oa1, ob1);
   if (npend) gemv_publish<HD>(P, E, pend, npend, M);
+  if (nown > 0) owner_fixup<HD>(P, E, oT0, oa0, ob0, M);
+  if (nown > 1) owner_fixup<HD>(P, E, oT1, oa1, ob1, M);
   if (lane == 0) trace_stamp(P, layer * NSTAGE + st, 2 + warp);
   return true;
 }
