@@ -38,7 +38,7 @@ extern "C" {
 #endif
 
 #define DDL_GROUP 64      /* INT4 scale group along the input dimension K */
-#define DDL_MAX_BATCH 4   /* sequences per step on the batch <= 4 path */
+#define DDL_MAX_BATCH 16  /* sequences per step (bf16 weights: 4) */
 #define DDL_MAX_GROUP_HEADS 8 /* H_q / H_kv */
 
 typedef enum {
@@ -149,7 +149,8 @@ typedef struct {
 } ddl_ws_view;
 int ddl_workspace_view(const ddl_shape* shape, int32_t B, int64_t s_max, ddl_ws_view* out);
 
-/* One decode step of one layer for B <= 4 sequences, all at position pos:
+/* One decode step of one layer for B <= DDL_MAX_BATCH sequences (INT4
+ * weights; bf16 weights: B <= 4, else DDL_ERR_UNSUPPORTED), all at position pos:
  * writes KV slot pos and attends over slots 0..pos (the caller keeps slots
  * < pos filled).  Input: resid_in [B][D] fp32, or x_bf16 [B][D] bf16 when
  * resid_in is NULL.  Output: resid_out [B][D] fp32 (may be NULL) and

@@ -50,8 +50,8 @@ constexpr int SM_RING_BYTES = NW * DEPTH * SLOT_BYTES;
 constexpr int SM_BARS = SM_RING_BYTES;
 constexpr int SM_SCR = SM_BARS + 512;
 constexpr int XF_BYTES = XF_CHUNKS * GC * 4 * 2 * 4 * 8;  // x fragments: chunks x batch <= 8
-constexpr int SX_BYTES = XF_CHUNKS * GC * MAX_B * 4;        // per-group sums of x
-constexpr int SM_SCR_BYTES = 70 * 1024;
+constexpr int SX_BYTES = XF_CHUNKS * GC * NARROW_B * 4;     // per-group sums of x (wide: 2 chunks x 16)
+constexpr int SM_SCR_BYTES = 71 * 1024;
 constexpr int SM_NW = SM_SCR + SM_SCR_BYTES;               // the panel's norm weights (bf16)
 constexpr int SM_NW_BYTES = XF_CHUNKS * GC * DDL_GROUP * 2;
 constexpr int SM_MISC = SM_NW + SM_NW_BYTES;
@@ -61,7 +61,7 @@ constexpr int SM_CTX = SM_SPAR + (((int)sizeof(SParams) + 255) & ~255);  // stag
 constexpr int SM_CTX_BYTES = 4096;
 constexpr int SM_TOTAL = SM_CTX + SM_CTX_BYTES;
 constexpr int XZ_OFF = XF_BYTES + SX_BYTES + NW * 32 * 4;  // zero x fragments for blocks past a slot's end
-constexpr int XZ_BYTES = 3 * 2 * MAX_B * 32 + 256;          // 3 j-strides + one lane span
+constexpr int XZ_BYTES = 2048;                             // covers both fragment layouts
 static_assert(XZ_OFF + XZ_BYTES <= SM_SCR_BYTES, "x fragments do not fit");
 static_assert(NW * 2 * (MAX_GH * (128 + 2) + 3) * 4 <= SM_SCR_BYTES, "attention records do not fit");
 static_assert(SM_TOTAL <= 227 * 1024, "shared memory budget");
@@ -439,7 +439,7 @@ __device__ __noinline__ void gemv_prologue(const Params& P, const GemvCtx& E, ui
   if (tid == 0) trace_stamp(P, E.layer * NSTAGE + E.st, NW + 5);
   // 3. the scale: the producer's max, or (first layer of a launch) the panel's
   if (!have_max) {
-    float mx[MAX_B] = {0.f, 0.f, 0.f, 0.f};
+    float mx[NARROW_B] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll 2
     for (int it = tid; it < n_items; it += NTHREADS) {
       const int gsb = it >> 4, q16 = it & 15;
@@ -453,11 +453,11 @@ __device__ __noinline__ void gemv_prologue(const Params& P, const GemvCtx& E, ui
       }
       const float a = fmaxf(fmaxf(fabsf(x.x), fabsf(x.y)), fmaxf(fabsf(x.z), fabsf(x.w)));
 #pragma unroll
-      for (int bb = 0; bb < MAX_B; ++bb)
+      for (int bb = 0; bb < NARROW_B; ++bb)
         if (bb == b) mx[bb] = fmaxf(mx[bb], a);
     }
 #pragma unroll
-    for (int b = 0; b < MAX_B; ++b) {
+    for (int b = 0; b < NARROW_B; ++b) {
       if (b < B) {
         const float r = warp_max(mx[b]);
         if (lane == 0) M.red[warp][2 * b + 1] = r;
@@ -482,7 +482,7 @@ __device__ __noinline__ void gemv_prologue(const Params& P, const GemvCtx& E, ui
   float* Sx = reinterpret_cast<float*>(smem + SM_SCR + XF_BYTES);
   constexpr bool f16 = WT == DDL_W_INT4;
   const bool want_ss = nw && whole;
-  float ssq[MAX_B] = {0.f, 0.f, 0.f, 0.f};
+  float ssq[NARROW_B] = {0.f, 0.f, 0.f, 0.f};
   const int ipr = (4 * NTHREADS / (16 * B)) * 16 * B;  // items per round: whole groups
   for (int r0 = 0; r0 < n_items; r0 += ipr) {
     float4 v[4];
@@ -500,7 +500,7 @@ __device__ __noinline__ void gemv_prologue(const Params& P, const GemvCtx& E, ui
         if (want_ss) {
           const float s2 = fmaf(x.x, x.x, fmaf(x.y, x.y, fmaf(x.z, x.z, x.w * x.w)));
 #pragma unroll
-          for (int bb = 0; bb < MAX_B; ++bb)
+          for (int bb = 0; bb < NARROW_B; ++bb)
             if (bb == b) ssq[bb] += s2;
         }
         const float sc = M.edown[b];
@@ -557,7 +557,7 @@ __device__ __noinline__ void gemv_prologue(const Params& P, const GemvCtx& E, ui
       }
 #pragma unroll
       for (int o = 8; o; o >>= 1) part += __shfl_xor_sync(FULL, part, o);
-      if (q16 == 0 && ok[u]) Sx[gs * MAX_B + b] = part;
+      if (q16 == 0 && ok[u]) Sx[gs * NARROW_B + b] = part;
     }
   }
   // zero fragments that the stream reads for blocks past a slot's end (the
@@ -566,7 +566,7 @@ __device__ __noinline__ void gemv_prologue(const Params& P, const GemvCtx& E, ui
   // 5. the RMSNorm factor
   if (want_ss) {
 #pragma unroll
-    for (int b = 0; b < MAX_B; ++b) {
+    for (int b = 0; b < NARROW_B; ++b) {
       if (b < B) {
         const float r = warp_sum(ssq[b]);
         if (lane == 0) M.red[warp][2 * b] = r;
@@ -591,12 +591,11 @@ __device__ __forceinline__ float epi_norm(const Params& P, const uint16_t* w, in
                                          : bf16_bits_to_f32(__ldg(w + r));
 }
 
-// Lane (g, t) holds rows g and g+8 of tile T for sequence t.
+// Rows g and g+8 of tile T for sequence t (narrow batches: t = lane % 4).
 template <int HD>
-__device__ __noinline__ void gemv_epilogue(const Params& P, const GemvCtx& E, int T, float v0, float v1,
-                              Misc& M) {
-  const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
-  if (t >= P.B) return;
+__device__ __noinline__ void gemv_epilogue(const Params& P, const GemvCtx& E, int T, int t, float v0,
+                                           float v1, Misc& M) {
+  const int lane = threadIdx.x & 31, g = lane >> 2;  // rows g, g+8 of tile T for sequence t
   if (E.st == ST_QKV) {
     const float r = M.rnorm[t];
     v0 *= r;
@@ -680,7 +679,7 @@ __device__ __noinline__ void gemv_fixup(const Params& P, const GemvCtx& E, int T
       s1 += x.y;
     }
   }
-  gemv_epilogue<HD>(P, E, T, s0, s1, M);
+  if ((threadIdx.x & 3) < P.B) gemv_epilogue<HD>(P, E, T, threadIdx.x & 3, s0, s1, M);
   if (lane == 0) P.cnt[T] = 0;
 }
 
@@ -753,7 +752,7 @@ __device__ __noinline__ void owner_fixup(const Params& P, const GemvCtx& E, int 
       }
     }
   }
-  gemv_epilogue<HD>(P, E, T, s0, s1, M);
+  if ((threadIdx.x & 3) < P.B) gemv_epilogue<HD>(P, E, T, threadIdx.x & 3, s0, s1, M);
   if (lane == 0) P.cnt[T] = 0;
 }
 
@@ -769,7 +768,7 @@ __device__ __forceinline__ void tile_finish(const Params& P, const GemvCtx& E, M
   const MatGeom& m = E.m;
   const int lane = threadIdx.x & 31;
   if (nblk == (uint32_t)m.G) {
-    gemv_epilogue<HD>(P, E, T, v0, v1, M);
+    if ((threadIdx.x & 3) < P.B) gemv_epilogue<HD>(P, E, T, threadIdx.x & 3, v0, v1, M);
     return;
   }
   const uint32_t me = (uint32_t)E.cl * NW + (threadIdx.x >> 5);
@@ -800,36 +799,9 @@ __device__ __forceinline__ void tile_finish(const Params& P, const GemvCtx& E, M
   }
 }
 
-// ------------------------------------------------------------------ GEMV stage
-// The warp walks its range of the panel's work order (tile, k-chunk, group).
-// Per ring slot (up to 8 groups of one (k-chunk, tile) unit): the 8 blocks'
-// MMAs run as 8 independent chains, then fold into the unit sums; a unit's
-// sums join the tile sums in true scale, and a tile is finished when the
-// warp leaves it.
-template <int HD, int WT>
-__device__ __forceinline__ bool stage_gemv_body(const Params& P, int layer, int st, Ring& R,
-                                                Cursor& prod, int64_t wg, int64_t W, uint8_t* smem,
-                                                Misc& M, uint64_t policy);
-// The ring and the cursor live in registers while the stage runs.
-template <int HD, int WT>
-__device__ __noinline__ bool stage_gemv(const Params& P, int layer, int st, Ring& Rm, Cursor& prodm,
-                                        int64_t wg, int64_t W, uint8_t* smem, Misc& M,
-                                        uint64_t policy) {
-  __syncwarp();
-  Ring R = Rm;
-  Cursor prod = prodm;
-  const bool ok = stage_gemv_body<HD, WT>(P, layer, st, R, prod, wg, W, smem, M, policy);
-  __syncwarp();
-  Rm = R;
-  prodm = prod;
-  __syncwarp();
-  return ok;
-}
-template <int HD, int WT>
-__device__ __forceinline__ bool stage_gemv_body(const Params& P, int layer, int st, Ring& R,
-                                                Cursor& prod, int64_t wg, int64_t W, uint8_t* smem,
-                                                Misc& M, uint64_t policy) {
-  GemvCtx& E = ctx().E;  // filled by thread 0; every warp reads it from shared memory
+// Fill the CTA's stage context (thread 0), then a block barrier.
+__device__ __noinline__ void fill_gemv_ctx(const Params& P, int layer, int st) {
+  GemvCtx& E = ctx().E;
   if (threadIdx.x == 0) {
     E.m = sp().mg[stage_mat(st)];
     E.st = st;
@@ -852,6 +824,44 @@ __device__ __forceinline__ bool stage_gemv_body(const Params& P, int layer, int 
     E.final_layer = P.final_last && layer == P.L - 1;
   }
   __syncthreads();
+}
+
+// ------------------------------------------------------------------ GEMV stage
+// The warp walks its range of the panel's work order (tile, k-chunk, group).
+// Per ring slot (up to 8 groups of one (k-chunk, tile) unit): the 8 blocks'
+// MMAs run as 8 independent chains, then fold into the unit sums; a unit's
+// sums join the tile sums in true scale, and a tile is finished when the
+// warp leaves it.
+template <int HD, int WT>
+__device__ __forceinline__ bool stage_gemv_body(const Params& P, int layer, int st, Ring& R,
+                                                Cursor& prod, int64_t wg, int64_t W, uint8_t* smem,
+                                                Misc& M, uint64_t policy);
+// The ring and the cursor live in registers while the stage runs.
+template <int HD, int WT>
+__device__ __noinline__ bool stage_gemv_wide(const Params& P, int layer, int st, Ring& Rm, Cursor& prodm,
+                                             int64_t wg, int64_t W, uint8_t* smem, Misc& M,
+                                             uint64_t policy);
+template <int HD, int WT>
+__device__ __noinline__ bool stage_gemv(const Params& P, int layer, int st, Ring& Rm, Cursor& prodm,
+                                        int64_t wg, int64_t W, uint8_t* smem, Misc& M,
+                                        uint64_t policy) {
+  if (P.B > NARROW_B) return stage_gemv_wide<HD, WT>(P, layer, st, Rm, prodm, wg, W, smem, M, policy);
+  __syncwarp();
+  Ring R = Rm;
+  Cursor prod = prodm;
+  const bool ok = stage_gemv_body<HD, WT>(P, layer, st, R, prod, wg, W, smem, M, policy);
+  __syncwarp();
+  Rm = R;
+  prodm = prod;
+  __syncwarp();
+  return ok;
+}
+template <int HD, int WT>
+__device__ __forceinline__ bool stage_gemv_body(const Params& P, int layer, int st, Ring& R,
+                                                Cursor& prod, int64_t wg, int64_t W, uint8_t* smem,
+                                                Misc& M, uint64_t policy) {
+  fill_gemv_ctx(P, layer, st);
+  GemvCtx& E = ctx().E;
   const MatGeom& m = E.m;
   gemv_prologue<HD, WT>(P, E, smem, M);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
@@ -887,7 +897,7 @@ __device__ __forceinline__ bool stage_gemv_body(const Params& P, int layer, int 
     }
     const int kcl = kc - pk0;
     const uint32_t xb = xf_lane + kcl * kstride + gi * gstride;
-    const uint32_t sb = sx_lane + ((kcl * GC + gi) * MAX_B) * 4;
+    const uint32_t sb = sx_lane + ((kcl * GC + gi) * NARROW_B) * 4;
     // The slot's blocks in two halves (a rolled loop: the stream loop's code
     // has to stay in the instruction cache).  Per half, all shared loads
     // first, then the MMAs in (j, block) order so that consecutive MMAs
@@ -916,7 +926,7 @@ __device__ __forceinline__ bool stage_gemv_body(const Params& P, int layer, int 
           const int i = h0 + ii;
           wv[ii] = lds128(slot + i * BLK_BYTES + lane * 16);
           const uint32_t scw = lds32(slot + BLKS_PER_SLOT * BLK_BYTES + i * SCL_BYTES + g * 4);
-          const float sxv = lds_f32(sb + i * (MAX_B * 4));
+          const float sxv = lds_f32(sb + i * (NARROW_B * 4));
           sc[ii] = i < nb ? scw : 0u;  // stale scale and sum words are finite-safe only as 0
           sx[ii] = i < nb ? sxv : 0.f;
         }
@@ -985,6 +995,472 @@ __device__ __forceinline__ bool stage_gemv_body(const Params& P, int layer, int 
   if (nown > 1) owner_fixup<HD>(P, E, oT1, oa1, ob1, M);
   if (lane == 0) trace_stamp(P, layer * NSTAGE + st, 2 + warp);
   return true;
+}
+
+// ------------------------------------------------------------------ wide batches
+// Batches of NARROW_B+1..MAX_B sequences: x is carried in fp16 without the
+// low part (one column per sequence, n-tile b / 8 of ntn = ceil(B / 8)), so a
+// group's fragments are 4 x ntn records of 256 bytes: [j][n-tile][lane (g,t)]
+// [register r] holding rows 2t, 2t+1 (r = 0) and 2t+8, 2t+9 (r = 1) of k-slice
+// j for column (sequence) 8 n-tile + g.  Lane (g, t) of a tile's MMA result
+// holds rows g, g+8 of sequences 8 n-tile + 2t and + 2t + 1.  The staged
+// panel is at most 2 k-chunks (one for ntn = 2); per-group sums of x have a
+// stride of MAX_B.  Split tiles keep 8 values per lane.
+__device__ __forceinline__ int wide_ntn(int B) { return (B + 7) >> 3; }
+
+template <int HD, int WT>
+__device__ __noinline__ void gemv_prologue_wide(const Params& P, const GemvCtx& E, uint8_t* smem, Misc& M) {
+  const MatGeom& m = E.m;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int B = P.B, ntn = wide_ntn(B);
+  const int kc_lo = m.pk[E.p], nkc = m.pk[E.p + 1] - kc_lo;
+  const float* x32 = nullptr;
+  const uint16_t* x16 = nullptr;
+  const uint16_t* nw = nullptr;
+  const uint16_t* nw_next = nullptr;
+  const LayerDev& Ld = sp().layers[E.layer];
+  switch (E.st) {
+    case ST_QKV: nw = Ld.norm1; x32 = E.xin32; x16 = E.xin16; break;
+    case ST_WO: x32 = P.attn; nw_next = Ld.norm2; break;
+    case ST_GU: x32 = P.y; nw = Ld.norm2; break;
+    default: x32 = P.a; nw_next = E.layer + 1 < P.L ? sp().layers[E.layer + 1].norm1 : nullptr; break;
+  }
+  if ((int64_t)P.D * 2 > SM_NW_BYTES) nw_next = nullptr;
+  const int K = m.K;
+  const int ngr = nkc * GC;
+  const int ngv = (nkc - 1) * GC + chunk_groups(m, kc_lo + nkc - 1);
+  const int kbase = kc_lo * GC * DDL_GROUP;
+  const bool whole = nkc == m.Sk;
+  const bool have_max = !(E.st == ST_QKV && E.layer == 0);
+  uint8_t* nws = smem + SM_NW;
+  __syncthreads();
+  {  // norm weights of the panel and the next stage's norm vector
+    const int nn = nw ? ngr * 8 : 0, nnx = nw_next ? P.D / 8 : 0;
+    for (int i = tid; i < nn + nnx; i += NTHREADS) {
+      if (i < nn) {
+        const int gs = i >> 3, q = i & 7;
+        if (gs < ngv) cp_async16(smem_addr(nws + (size_t)gs * 128 + q * 16), nw + kbase + (int64_t)gs * DDL_GROUP + q * 8);
+      } else {
+        const int j = i - nn;
+        cp_async16(smem_addr(nws + (size_t)j * 16), nw_next + (int64_t)j * 8);
+      }
+    }
+  }
+  float xm = 0.f;
+  if (have_max && tid < B) xm = __uint_as_float(__ldcg(P.xmax + (E.layer * NSTAGE + E.st) * MAX_B + tid));
+  if (nw && !whole) {
+    for (int b = 0; b < B; ++b) {
+      float ss = 0.f;
+      for (int q = tid; q < K / 4; q += NTHREADS) {
+        const float4 v = x32 ? __ldcg(reinterpret_cast<const float4*>(x32 + (int64_t)b * K) + q)
+                             : bf16x4_f32(__ldcg(reinterpret_cast<const uint2*>(x16 + (int64_t)b * K) + q));
+        ss = fmaf(v.x, v.x, fmaf(v.y, v.y, fmaf(v.z, v.z, fmaf(v.w, v.w, ss))));
+      }
+      ss = warp_sum(ss);
+      if (lane == 0) M.red[warp][2 * b] = ss;
+    }
+  }
+  cp_async_wait_all();
+  __syncthreads();
+  // item it = ((group slot * B + b) * 16 + quad): four columns of sequence b, read from memory
+#define WIDE_X(it_, gs_, b_, q16_)                                                                         \
+  (x32 ? __ldcg(reinterpret_cast<const float4*>(x32 + (int64_t)(b_) * K + kbase + (gs_) * DDL_GROUP) + (q16_)) \
+       : bf16x4_f32(__ldcg(reinterpret_cast<const uint2*>(x16 + (int64_t)(b_) * K + kbase + (gs_) * DDL_GROUP) + (q16_))))
+  if (!have_max) {  // first layer of a launch: the panel's max per sequence
+    for (int b = 0; b < B; ++b) {
+      float mx = 0.f;
+      for (int it = tid; it < ngr * 16; it += NTHREADS) {
+        const int gs = it >> 4, q16 = it & 15;
+        if (gs >= ngv) continue;
+        float4 x = WIDE_X(it, gs, b, q16);
+        if (nw) {
+          const float4 w = bf16x4_f32(*reinterpret_cast<const uint2*>(nws + (size_t)gs * 128 + q16 * 8));
+          x = make_float4(x.x * w.x, x.y * w.y, x.z * w.z, x.w * w.w);
+        }
+        mx = fmaxf(mx, fmaxf(fmaxf(fabsf(x.x), fabsf(x.y)), fmaxf(fabsf(x.z), fabsf(x.w))));
+      }
+      mx = warp_max(mx);
+      if (lane == 0) M.red[warp][2 * b + 1] = mx;
+    }
+    __syncthreads();
+    if (tid < B)
+      for (int w = 0; w < NW; ++w) xm = fmaxf(xm, M.red[w][2 * tid + 1]);
+  }
+  if (tid < B) {
+    const int e = xm > 0.f ? ilogbf(xm) - 11 : 0;
+    M.escale[tid] = ldexpf(1.0f, e);
+    M.edown[tid] = ldexpf(1.0f, -e);
+  }
+  __syncthreads();
+  // fragments (fp16 of x * w * 2^-e) and the sum of x per (group, sequence);
+  // the sum of squares per sequence when the panel is the whole vector
+  uint32_t* xf = reinterpret_cast<uint32_t*>(smem + SM_SCR);
+  float* Sx = reinterpret_cast<float*>(smem + SM_SCR + XF_BYTES);
+  constexpr bool f16 = WT == DDL_W_INT4;
+  const bool want_ss = nw && whole;
+  const int gwords = 4 * ntn * 64;  // 32-bit words of one group's fragments
+  // sequence by sequence (item = group slot * 16 + quad), so that the sums
+  // of squares reduce in a fixed order
+  for (int b = 0; b < B; ++b) {
+    const float sc = M.edown[b];
+    float ssb = 0.f;
+    for (int base = warp * 32; base < ngr * 16; base += 4 * NTHREADS) {
+      float4 x[4];
+      bool ok[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int it = base + u * NTHREADS + lane, gs = it >> 4, q16 = it & 15;
+        ok[u] = it < ngr * 16 && gs < ngv;
+        x[u] = ok[u] ? WIDE_X(it, gs, b, q16) : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int it = base + u * NTHREADS + lane, gs = it >> 4, q16 = it & 15;
+        float part = 0.f;
+        if (ok[u]) {
+          if (want_ss) ssb = fmaf(x[u].x, x[u].x, fmaf(x[u].y, x[u].y, fmaf(x[u].z, x[u].z, fmaf(x[u].w, x[u].w, ssb))));
+          const float4 w = nw ? bf16x4_f32(*reinterpret_cast<const uint2*>(nws + (size_t)gs * 128 + q16 * 8))
+                              : make_float4(1.f, 1.f, 1.f, 1.f);
+          const float v0 = x[u].x * w.x * sc, v1 = x[u].y * w.y * sc, v2 = x[u].z * w.z * sc, v3 = x[u].w * w.w * sc;
+          uint32_t h01, h23;
+          float2 f01, f23;
+          if (f16) {
+            const __half2 a = __float22half2_rn(make_float2(v0, v1)), c = __float22half2_rn(make_float2(v2, v3));
+            f01 = __half22float2(a);
+            f23 = __half22float2(c);
+            h01 = *reinterpret_cast<const uint32_t*>(&a);
+            h23 = *reinterpret_cast<const uint32_t*>(&c);
+          } else {
+            const __nv_bfloat162 a = __float22bfloat162_rn(make_float2(v0, v1));
+            const __nv_bfloat162 c = __float22bfloat162_rn(make_float2(v2, v3));
+            f01 = __bfloat1622float2(a);
+            f23 = __bfloat1622float2(c);
+            h01 = *reinterpret_cast<const uint32_t*>(&a);
+            h23 = *reinterpret_cast<const uint32_t*>(&c);
+          }
+          part = (f01.x + f01.y) + (f23.x + f23.y);
+          const int j = q16 >> 2, reg = (q16 >> 1) & 1, t0 = 2 * (q16 & 1), nt = b >> 3, g = b & 7;
+          uint32_t* f = xf + gs * gwords + (j * ntn + nt) * 64;
+          f[(g * 4 + t0) * 2 + reg] = h01;
+          f[(g * 4 + t0 + 1) * 2 + reg] = h23;
+        }
+#pragma unroll
+        for (int o = 8; o; o >>= 1) part += __shfl_xor_sync(FULL, part, o);
+        if (q16 == 0 && ok[u]) Sx[gs * MAX_B + b] = part;
+      }
+    }
+    if (want_ss) {
+      ssb = warp_sum(ssb);
+      if (lane == 0) M.red[warp][2 * b] = ssb;
+    }
+  }
+#undef WIDE_X
+  for (int i = tid; i < XZ_BYTES / 4; i += NTHREADS) reinterpret_cast<uint32_t*>(smem + SM_SCR + XZ_OFF)[i] = 0u;
+  __syncthreads();
+  if (tid < B) {
+    float ss = 0.f;
+    if (nw)
+      for (int w = 0; w < NW; ++w) ss += M.red[w][2 * tid];
+    M.rnorm[tid] = nw ? 1.0f / sqrtf(ss / (float)K + P.eps) : 1.0f;
+  }
+  __syncthreads();
+}
+
+// Split tiles of a wide batch: 8 values per lane, float4 x 2 at [slot][lane].
+template <int HD>
+__device__ __forceinline__ void wide_epilogues(const Params& P, const GemvCtx& E, int T, const float (&v)[8],
+                                               Misc& M) {
+  const int t = threadIdx.x & 3;
+#pragma unroll
+  for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+    for (int s = 0; s < 2; ++s) {
+      const int b = nt * 8 + 2 * t + s;
+      if (b < P.B) gemv_epilogue<HD>(P, E, T, b, v[nt * 4 + s], v[nt * 4 + 2 + s], M);
+    }
+}
+template <int HD>
+__device__ __forceinline__ void wide_sum_slots(const Params& P, const GemvCtx& E, int T, float (&v)[8]) {
+  const MatGeom& m = E.m;
+  const int lane = threadIdx.x & 31;
+  const float4* part = reinterpret_cast<const float4*>(P.gpart) + (int64_t)T * m.NP * m.J * 64 + lane * 2;
+#pragma unroll
+  for (int k = 0; k < 8; ++k) v[k] = 0.f;
+  for (int p = 0; p < m.NP; ++p) {
+    const uint32_t Gp = panel_groups(m, p);
+    const uint32_t v0 = work_owner(m, p, (uint32_t)T * Gp, NW), v1 = work_owner(m, p, (uint32_t)(T + 1) * Gp - 1, NW);
+    for (uint32_t w = v0; w <= v1; ++w) {
+      if (warp_empty(m, p, w, NW)) continue;
+      const float4* q = part + ((int64_t)p * m.J + (w - v0)) * 64;
+      const float4 a = __ldcg(q), c = __ldcg(q + 1);
+      v[0] += a.x; v[1] += a.y; v[2] += a.z; v[3] += a.w;
+      v[4] += c.x; v[5] += c.y; v[6] += c.z; v[7] += c.w;
+    }
+  }
+}
+// Cooperative launch: the owner waits for the other contributors' releases.
+template <int HD>
+__device__ __noinline__ void wide_owner_fixup(const Params& P, const GemvCtx& E, int T, Misc& M) {
+  const MatGeom& m = E.m;
+  const int lane = threadIdx.x & 31;
+  uint32_t expected = 0;
+  for (int p = 0; p < m.NP; ++p) {
+    const uint32_t Gp = panel_groups(m, p);
+    const uint32_t v0 = work_owner(m, p, (uint32_t)T * Gp, NW), v1 = work_owner(m, p, (uint32_t)(T + 1) * Gp - 1, NW);
+    for (uint32_t v = v0; v <= v1; ++v)
+      if ((p != 0 || v != v0) && !warp_empty(m, p, v, NW)) ++expected;
+  }
+  if (lane == 0) {
+    uint64_t t0 = 0;
+    for (uint32_t it = 1; ld_acquire_gpu(P.cnt + T) < expected; ++it) {
+      if ((it & 255u) != 0) continue;
+      const uint64_t now = globaltimer();
+      if (t0 == 0) t0 = now;
+      else if (now - t0 > WAIT_LIMIT_NS) {
+        atomicExch(P.ctrl + 1, STATUS_TIMEOUT);
+        M.abort = 1;
+        break;
+      }
+    }
+  }
+  __syncwarp();
+  float v[8];
+  wide_sum_slots<HD>(P, E, T, v);
+  wide_epilogues<HD>(P, E, T, v, M);
+  if (lane == 0) P.cnt[T] = 0;
+}
+// One launch per stage: the warp whose arrival completes the tile finishes it.
+template <int HD>
+__device__ __noinline__ void wide_publish(const Params& P, const GemvCtx& E, const uint32_t* pend, int npend,
+                                          Misc& M) {
+  const int lane = threadIdx.x & 31;
+  __syncwarp();
+  __threadfence();
+  uint32_t last = 0;
+  if (lane < npend) {
+    const uint32_t T = pend[lane] & 0xFFFFFu, nblk = pend[lane] >> 20;
+    last = atomicAdd(P.cnt + T, nblk) + nblk == (uint32_t)E.m.G;
+  }
+  uint32_t mask = __ballot_sync(FULL, last);
+  if (mask) __threadfence();
+  while (mask) {
+    const int l = __ffs(mask) - 1;
+    mask &= mask - 1;
+    const int T = (int)(pend[l] & 0xFFFFFu);
+    float v[8];
+    wide_sum_slots<HD>(P, E, T, v);
+    wide_epilogues<HD>(P, E, T, v, M);
+    if (lane == 0) P.cnt[T] = 0;
+  }
+}
+template <int HD>
+__device__ __forceinline__ void wide_tile_finish(const Params& P, const GemvCtx& E, Misc& M, int T, uint32_t nblk,
+                                                 const float (&v)[8], uint32_t* pend, int& npend, int& nown,
+                                                 int& oT0, int& oT1) {
+  const MatGeom& m = E.m;
+  const int lane = threadIdx.x & 31;
+  if (nblk == (uint32_t)m.G) {
+    wide_epilogues<HD>(P, E, T, v, M);
+    return;
+  }
+  const uint32_t me = (uint32_t)E.cl * NW + (threadIdx.x >> 5);
+  const uint32_t first = work_owner(m, E.p, (uint32_t)T * panel_groups(m, E.p), NW);
+  const int64_t slot = ((int64_t)T * m.NP + E.p) * m.J + (me - first);
+  float4* q = reinterpret_cast<float4*>(P.gpart) + slot * 64 + lane * 2;
+  q[0] = make_float4(v[0], v[1], v[2], v[3]);
+  q[1] = make_float4(v[4], v[5], v[6], v[7]);
+  if (P.cooperative) {
+    if (E.p == 0 && me == first) {  // the owner: finish at the end (its own partial is in its slot)
+      if (nown == 0) oT0 = T;
+      else if (nown == 1) oT1 = T;
+      if (nown >= 2) {
+        __syncwarp();
+        wide_owner_fixup<HD>(P, E, T, M);
+        return;
+      }
+      ++nown;
+      return;
+    }
+    __syncwarp();
+    if (lane == 0) red_release_gpu_add(P.cnt + T, 1u);
+    return;
+  }
+  if (lane == 0) pend[npend] = (uint32_t)T | (nblk << 20);
+  if (++npend == 32) {
+    wide_publish<HD>(P, E, pend, npend, M);
+    npend = 0;
+  }
+}
+
+template <int HD, int WT>
+__device__ __noinline__ bool stage_gemv_wide(const Params& P, int layer, int st, Ring& Rm, Cursor& prodm,
+                                             int64_t wg, int64_t W, uint8_t* smem, Misc& M,
+                                             uint64_t policy) {
+  __syncwarp();
+  Ring R = Rm;
+  Cursor prod = prodm;
+  fill_gemv_ctx(P, layer, st);
+  GemvCtx& E = ctx().E;
+  const MatGeom& m = E.m;
+  gemv_prologue_wide<HD, WT>(P, E, smem, M);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+  if (threadIdx.x == 0) trace_stamp(P, layer * NSTAGE + st, 1);
+  const Entry& en = ctx().ent[warp][st];
+  const uint32_t lo = en.lo, hi = en.hi;
+  bool ok = true;
+  if (lo < hi) {
+    uint32_t* pend = reinterpret_cast<uint32_t*>(smem + SM_SCR + XF_BYTES + SX_BYTES) + warp * 32;
+    int npend = 0;
+    const int B = P.B, ntn = wide_ntn(B), Sk = m.Sk, pk0 = m.pk[E.p], pk1 = m.pk[E.p + 1];
+    const uint32_t jstride = ntn * 256, gstride = 4 * jstride, kstride = GC * gstride;
+    const uint32_t xf_lane = smem_addr(smem + SM_SCR) + (g * 4 + t) * 8;
+    const uint32_t xz = smem_addr(smem + SM_SCR + XZ_OFF) + (g * 4 + t) * 8;
+    const uint32_t sx0 = smem_addr(smem + SM_SCR + XF_BYTES);
+    float esc[2][2];
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+      for (int s = 0; s < 2; ++s) {
+        const int b = nt * 8 + 2 * t + s;
+        esc[nt][s] = b < B ? M.escale[b] : 0.f;
+      }
+    int kc = en.kc, T = en.T, gi = en.gi, gk = en.gk;
+    float acc[8], tac[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) acc[k] = tac[k] = 0.f;
+    uint32_t nblk = 0;
+    int nown = 0, oT0 = 0, oT1 = 0;
+    constexpr int PER = WT == DDL_W_INT4 ? BLKS_PER_SLOT : BF16_BLKS_PER_SLOT;
+    constexpr int HB = PER >= 4 ? 2 : 1;
+    for (uint32_t b = lo; b < hi;) {
+      int nb = (int)(hi - b < (uint32_t)PER ? hi - b : (uint32_t)PER);
+      if (nb > gk - gi) nb = gk - gi;
+      const uint32_t slot = R.slot(R.n_done);
+      if (!mbar_wait_warp(R.bar(R.n_done), R.parity(R.n_done), P.ctrl + 1)) {
+        M.abort = 1;
+        ok = false;
+        break;
+      }
+      const int kcl = kc - pk0;
+      const uint32_t xb = xf_lane + kcl * kstride + gi * gstride;
+      const int gsl = kcl * GC + gi;  // group slot of the slot's first block
+#pragma unroll 1
+      for (int h0 = 0; h0 < PER; h0 += HB) {
+        float c[HB][2][4];
+        uint2 bx[HB][4][2];
+#pragma unroll
+        for (int ii = 0; ii < HB; ++ii) {
+          const int i = h0 + ii;
+          const uint32_t xi = i < nb ? xb + i * gstride : xz;
+#pragma unroll
+          for (int nt = 0; nt < 2; ++nt) {
+            c[ii][nt][0] = c[ii][nt][1] = c[ii][nt][2] = c[ii][nt][3] = 0.f;
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              bx[ii][j][nt] = nt < ntn ? lds64(xi + (j * ntn + nt) * 256) : make_uint2(0u, 0u);
+          }
+        }
+        if (WT == DDL_W_INT4) {
+          uint4 wv[HB];
+          uint32_t sc[HB];
+          float sx[HB][2][2];
+#pragma unroll
+          for (int ii = 0; ii < HB; ++ii) {
+            const int i = h0 + ii;
+            wv[ii] = lds128(slot + i * BLK_BYTES + lane * 16);
+            const uint32_t scw = lds32(slot + BLKS_PER_SLOT * BLK_BYTES + i * SCL_BYTES + g * 4);
+            sc[ii] = i < nb ? scw : 0u;
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+              for (int s = 0; s < 2; ++s) {
+                const int bq = nt * 8 + 2 * t + s;
+                const float v = lds_f32(sx0 + ((gsl + (i < nb ? i : 0)) * MAX_B + bq) * 4);
+                sx[ii][nt][s] = (i < nb && bq < B) ? v : 0.f;
+              }
+          }
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+#pragma unroll
+            for (int ii = 0; ii < HB; ++ii) {
+              const uint32_t w = j == 0 ? wv[ii].x : j == 1 ? wv[ii].y : j == 2 ? wv[ii].z : wv[ii].w;
+              const uint32_t w8 = w >> 8;
+              const uint32_t a0 = lop3_merge(w, 0x000F000Fu, 0x64086408u);
+              const uint32_t a1 = lop3_merge(w, 0x00F000F0u, 0x64806480u);
+              const uint32_t a2 = lop3_merge(w8, 0x000F000Fu, 0x64086408u);
+              const uint32_t a3 = lop3_merge(w8, 0x00F000F0u, 0x64806480u);
+              mma_f16(c[ii][0], a0, a1, a2, a3, bx[ii][j][0].x, bx[ii][j][0].y);
+              if (ntn > 1) mma_f16(c[ii][1], a0, a1, a2, a3, bx[ii][j][1].x, bx[ii][j][1].y);
+            }
+          }
+#pragma unroll
+          for (int ii = 0; ii < HB; ++ii) {
+            const float slo = bf16lo_f32(sc[ii]), shi = bf16hi_f32(sc[ii]) * 0.0625f;
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+              for (int s = 0; s < 2; ++s) {
+                acc[nt * 4 + s] = fmaf(slo, c[ii][nt][s] - 1032.f * sx[ii][nt][s], acc[nt * 4 + s]);
+                acc[nt * 4 + 2 + s] = fmaf(shi, c[ii][nt][2 + s] - 1152.f * sx[ii][nt][s], acc[nt * 4 + 2 + s]);
+              }
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+#pragma unroll
+            for (int ii = 0; ii < HB; ++ii) {
+              const int i = h0 + ii;
+              const uint4 av = lds128(slot + i * BF16_BLK_BYTES + j * 512 + lane * 16);
+              const uint4 aq = i < nb ? av : make_uint4(0u, 0u, 0u, 0u);
+              mma_bf16(c[ii][0], aq.x, aq.y, aq.z, aq.w, bx[ii][j][0].x, bx[ii][j][0].y);
+              if (ntn > 1) mma_bf16(c[ii][1], aq.x, aq.y, aq.z, aq.w, bx[ii][j][1].x, bx[ii][j][1].y);
+            }
+#pragma unroll
+          for (int ii = 0; ii < HB; ++ii)
+#pragma unroll
+            for (int k = 0; k < 8; ++k) acc[k] += c[ii][k >> 2][k & 3];
+        }
+      }
+      ring_advance<HD, WT>(P, R, prod, wg, W, lane, policy);
+      b += nb;
+      gi += nb;
+      nblk += nb;
+      if (gi == gk) {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          tac[k] = fmaf(acc[k], esc[k >> 2][k & 1], tac[k]);
+          acc[k] = 0.f;
+        }
+        gi = 0;
+        if (++kc == pk1) {
+          wide_tile_finish<HD>(P, E, M, T, nblk, tac, pend, npend, nown, oT0, oT1);
+#pragma unroll
+          for (int k = 0; k < 8; ++k) tac[k] = 0.f;
+          nblk = 0;
+          kc = pk0;
+          ++T;
+        }
+        gk = kc < Sk ? chunk_groups(m, kc) : 1;
+      }
+    }
+    if (ok) {
+      if (nblk != 0) {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) tac[k] = fmaf(acc[k], esc[k >> 2][k & 1], tac[k]);
+        wide_tile_finish<HD>(P, E, M, T, nblk, tac, pend, npend, nown, oT0, oT1);
+      }
+      if (npend) wide_publish<HD>(P, E, pend, npend, M);
+      __syncwarp();
+      if (nown > 0) wide_owner_fixup<HD>(P, E, oT0, M);
+      if (nown > 1) wide_owner_fixup<HD>(P, E, oT1, M);
+    }
+  }
+  if (lane == 0) trace_stamp(P, layer * NSTAGE + st, 2 + warp);
+  __syncwarp();
+  Rm = R;
+  prodm = prod;
+  __syncwarp();
+  return ok;
 }
 
 // ------------------------------------------------------------------ attention
@@ -1527,7 +2003,7 @@ static void ws_layout(const ddl_shape& s, int B, int64_t s_max, int C, const Mat
   const int64_t Jatt = C;
   int64_t gpart = 0, ntmax = 0;
   for (int k = 0; k < 4; ++k) {
-    const int64_t u = (int64_t)mg[k].NT * mg[k].NP * mg[k].J * 32 * 2 * 4;
+    const int64_t u = (int64_t)mg[k].NT * mg[k].NP * mg[k].J * 32 * (B > NARROW_B ? 8 : 2) * 4;
     if (u > gpart) gpart = u;
     if (mg[k].NT > ntmax) ntmax = mg[k].NT;
   }
@@ -1596,6 +2072,9 @@ static int decode(const ddl_shape* s, ddl_wtype wtype, const ddl_layer_w* layers
   if (!layers || !kv || L <= 0 || !workspace) return !workspace ? DDL_ERR_WORKSPACE : DDL_ERR_ARG;
   if (B < 1 || B > MAX_B) return DDL_ERR_UNSUPPORTED;
   if (wtype != DDL_W_INT4 && wtype != DDL_W_BF16) return DDL_ERR_UNSUPPORTED;
+  // bf16 weights need bf16 activations in the MMA; past NARROW_B sequences
+  // there is no room for their low parts, and 8 bits alone miss the tolerance
+  if (wtype == DDL_W_BF16 && B > NARROW_B) return DDL_ERR_UNSUPPORTED;
   if (!resid_in && !x_bf16) return DDL_ERR_ARG;
   const int64_t s_max = kv[0].s_max;
   if (pos < 0 || pos >= s_max) return DDL_ERR_POS;

@@ -62,7 +62,9 @@ inline int64_t make_geoms(const ddl_shape& s, int wtype, MatGeom mg[4]) {
 // proportion to blocks (at least one each); then J, the largest number of
 // warps sharing a (tile, panel).  Returns false if the grid is too small.
 inline bool make_panels(MatGeom& m, int B, int C) {
-  int ch = XF_CHUNKS / B;
+  // narrow batches: 2B fp16 columns per group; wider ones: 8 per n-tile of
+  // ceil(B / 8) (fp16 without the low part), 4 x 256 bytes each
+  int ch = B <= NARROW_B ? XF_CHUNKS / B : XF_CHUNKS / (4 * ((B + 7) / 8));
   if (ch < 1) ch = 1;
   int NP = (m.Sk + ch - 1) / ch;
   if (NP > MAXP || NP > C) return false;

@@ -50,7 +50,8 @@ constexpr int BF16_BLK_BYTES = 2048;  // one bf16 block: 16 rows x 64 columns
 constexpr int BF16_BLKS_PER_SLOT = 2;
 constexpr int GC = 32;                // groups per k-chunk
 constexpr int MAX_LAYERS = 96;        // layers per launch (longer stacks use several launches)
-constexpr int MAX_B = 4;
+constexpr int MAX_B = 16;             // sequences of a batch
+constexpr int NARROW_B = 4;           // up to this batch x is carried as fp16 hi/lo columns
 constexpr int MAX_GH = 8;             // query heads per KV head
 constexpr int NSTAGE = 5;
 constexpr int MAXP = 16;              // k-chunk panels per matrix

@@ -9,8 +9,8 @@ stack per step).
   oracle run untethered over all 64 layers (each layer takes the oracle's own
   residual; rel-L2 of the output held to the step's bar, the residual's drift
   reported).
-* the same stack at batch 4 with a 4096-token cache: teacher-forced layers
-  {0, 63} plus two seeded others.
+* the same stack at batches 4 and 16 with a 4096-token cache: teacher-forced
+  layers {0, 63} plus two seeded others.
 * Llama-3-70B-shaped stack, 80 layers, KV 32768: the device step over all 80
   layers and teacher-forced layers {0, 1, 40, 79} plus two seeded others.
 
@@ -114,9 +114,10 @@ def test_27b_stack_64_layers_full_and_teacher_forced():
     assert e_res <= 1e-3 * float(np.max(np.abs(x)))
 
 
-def test_27b_stack_batch4_teacher_forced():
+@pytest.mark.parametrize("B", [4, 16])
+def test_27b_stack_batch_teacher_forced(B):
     cfg = configs.STACK27B_SWEEP
-    st = workload.build_stack(cfg, batch=4)
+    st = workload.build_stack(cfg, batch=B)
     errs = {}
     for l in _sampled(cfg.layers, (0, cfg.layers - 1), 2, seed=12):
         errs[f"layer {l}"] = _teacher_forced(st, l, host_layer(cfg, l, st.wtype))
