@@ -845,7 +845,6 @@ template <int HD, int WT>
 __device__ __noinline__ bool stage_gemv(const Params& P, int layer, int st, Ring& Rm, Cursor& prodm,
                                         int64_t wg, int64_t W, uint8_t* smem, Misc& M,
                                         uint64_t policy) {
-  if (P.B > NARROW_B) return stage_gemv_wide<HD, WT>(P, layer, st, Rm, prodm, wg, W, smem, M, policy);
   __syncwarp();
   Ring R = Rm;
   Cursor prod = prodm;
@@ -1853,7 +1852,7 @@ __device__ bool grid_sync(const Params& P, uint32_t target, Misc& M) {
 }
 
 // ------------------------------------------------------------------ the kernel
-template <int HD, int WT>
+template <int HD, int WT, bool WIDE>
 __global__ void __launch_bounds__(NTHREADS, 1) decode_kernel(const __grid_constant__ Params P) {
   uint8_t* smem = g_smem;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -1917,7 +1916,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) decode_kernel(const __grid_consta
       if (threadIdx.x == 0) trace_stamp(P, s, 1);
       ok = stage_att<HD, WT>(P, layer, R, prod, wg, W, smem, M, policy);
     } else {
-      stage_gemv<HD, WT>(P, layer, st, R, prod, wg, W, smem, M, policy);
+      if constexpr (WIDE) stage_gemv_wide<HD, WT>(P, layer, st, R, prod, wg, W, smem, M, policy);
+      else stage_gemv<HD, WT>(P, layer, st, R, prod, wg, W, smem, M, policy);
     }
     __syncthreads();
     if (threadIdx.x == 0) trace_stamp(P, s, NW + 2);
@@ -1953,7 +1953,12 @@ static int prepare_kernel() {
   int dev = 0;
   cudaGetDevice(&dev);
   if (done[dev]) return DDL_OK;
-  cudaError_t e = cudaFuncSetAttribute(decode_kernel<HD, WT>,
+  if constexpr (WT == DDL_W_INT4) {  // the wide-batch variant
+    cudaError_t e = cudaFuncSetAttribute(decode_kernel<HD, WT, true>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, SM_TOTAL);
+    if (e != cudaSuccess) return cuda_status(e);
+  }
+  cudaError_t e = cudaFuncSetAttribute(decode_kernel<HD, WT, false>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, SM_TOTAL);
   if (e != cudaSuccess) return cuda_status(e);
   done[dev] = true;
@@ -2129,8 +2134,13 @@ static int decode(const ddl_shape* s, ddl_wtype wtype, const ddl_layer_w* layers
   cudaError_t e = cudaMemsetAsync(ws, 0, (size_t)w.gpart, cs);  // barrier, status, counters
   if (e != cudaSuccess) return cuda_status(e);
   const bool coop = di.coop && g_launch_mode == 0;
-  void* fn = HD == 128 ? (wtype == DDL_W_INT4 ? (void*)decode_kernel<128, DDL_W_INT4> : (void*)decode_kernel<128, DDL_W_BF16>)
-                       : (wtype == DDL_W_INT4 ? (void*)decode_kernel<64, DDL_W_INT4> : (void*)decode_kernel<64, DDL_W_BF16>);
+  const bool wide = B > NARROW_B;  // INT4 only (checked above)
+  void* fn = HD == 128 ? (wtype == DDL_W_INT4 ? (wide ? (void*)decode_kernel<128, DDL_W_INT4, true>
+                                                      : (void*)decode_kernel<128, DDL_W_INT4, false>)
+                                              : (void*)decode_kernel<128, DDL_W_BF16, false>)
+                       : (wtype == DDL_W_INT4 ? (wide ? (void*)decode_kernel<64, DDL_W_INT4, true>
+                                                      : (void*)decode_kernel<64, DDL_W_INT4, false>)
+                                              : (void*)decode_kernel<64, DDL_W_BF16, false>);
   for (int l0 = 0; l0 < L; l0 += MAX_LAYERS) {
     const int nL = L - l0 < MAX_LAYERS ? L - l0 : MAX_LAYERS;
     P.L = nL;
