@@ -773,7 +773,7 @@ __device__ __forceinline__ void tile_finish(const Params& P, const GemvCtx& E, M
   }
   const uint32_t me = (uint32_t)E.cl * NW + (threadIdx.x >> 5);
   const uint32_t first = work_owner(m, E.p, (uint32_t)T * panel_groups(m, E.p), NW);
-  if (P.cooperative && E.p == 0 && me == first) {  // the tile's owner: finish it at the end
+  if (P.cooperative && m.own_ok && E.p == 0 && me == first) {  // the tile's owner: finish it at the end
     if (nown == 0) {
       oT0 = T; oa0 = v0; ob0 = v1;
     } else if (nown == 1) {
@@ -787,7 +787,7 @@ __device__ __forceinline__ void tile_finish(const Params& P, const GemvCtx& E, M
   }
   const int64_t slot = ((int64_t)T * m.NP + E.p) * m.J + (me - first);
   reinterpret_cast<float2*>(P.gpart)[slot * 32 + lane] = make_float2(v0, v1);
-  if (P.cooperative) {  // release the partial to the tile's owner
+  if (P.cooperative && m.own_ok) {  // release the partial to the tile's owner
     __syncwarp();
     if (lane == 0) red_release_gpu_add(P.cnt + T, 1u);
     return;
@@ -1268,7 +1268,7 @@ __device__ __forceinline__ void wide_tile_finish(const Params& P, const GemvCtx&
   float4* q = reinterpret_cast<float4*>(P.gpart) + slot * 64 + lane * 2;
   q[0] = make_float4(v[0], v[1], v[2], v[3]);
   q[1] = make_float4(v[4], v[5], v[6], v[7]);
-  if (P.cooperative) {
+  if (P.cooperative && m.own_ok) {
     if (E.p == 0 && me == first) {  // the owner: finish at the end (its own partial is in its slot)
       if (nown == 0) oT0 = T;
       else if (nown == 1) oT1 = T;

@@ -90,6 +90,19 @@ inline bool make_panels(MatGeom& m, int B, int C) {
     }
   }
   m.J = (int32_t)J;
+  // a warp owns the split tiles whose first panel-0 block it holds; with more
+  // than two it would wait for other contributors in mid-stream
+  int maxown = 0;
+  const uint32_t Gp0 = panel_groups(m, 0);
+  for (int v = 0; v < (m.pc[1] - m.pc[0]) * NW; ++v) {
+    uint32_t lo, hi;
+    warp_work(m, 0, v / NW, v % NW, NW, lo, hi);
+    int own = 0;
+    for (uint32_t T = (lo + Gp0 - 1) / Gp0; T * Gp0 < hi; ++T)
+      if (m.NP > 1 || (T + 1) * Gp0 > hi) ++own;
+    if (own > maxown) maxown = own;
+  }
+  m.own_ok = maxown <= 2;
   return true;
 }
 

@@ -75,6 +75,7 @@ struct MatGeom {
   int32_t Gc, Sk;     // groups per full k-chunk, number of k-chunks
   int32_t J;          // partial slots per (tile, panel)
   int32_t NP;         // panels: k-chunks pk[p]..pk[p+1]-1, worked by CTAs pc[p]..pc[p+1]-1
+  int32_t own_ok;     // split tiles may be finished by their owners: no warp owns more than two
   int64_t T;          // blocks
   int64_t woff, soff; // byte offsets of the code and scale streams in a packed layer
   int16_t pk[MAXP + 1];
