@@ -92,14 +92,16 @@ enum SlotKind { SK_GEMV = 0, SK_K = 1, SK_V = 2 };
 
 struct SlotDesc {
   int kind, cnt;
-  int64_t a;
+  uint32_t a;  // GEMV: stream block index; K/V: first row of the tile in the [rows][hd] cache view
 };
 // Producer cursor over this warp's slots of every stage of the launch; it
 // caches the current stage's stream bases so that issuing a slot reads no
 // per-layer parameter with a run-time index.
 struct Cursor {
-  int s;
-  int64_t pos, end;
+  int s, st;              // flattened stage and its kind
+  uint32_t pos, end;      // work index and end: GEMV panel blocks, ATT 2 x tiles (K, V)
+  uint32_t a;             // GEMV: stream block index of pos; ATT: cache-view row of the tile
+  int aseq, ai;           // ATT: sequence and tile index of the tile
   const uint8_t* wbase;   // GEMV: code (or bf16) stream of the matrix
   const uint8_t* sbase;   // GEMV: scale stream (INT4)
   const uint16_t* kbase;  // ATT: K cache of the layer
@@ -197,11 +199,15 @@ __device__ __noinline__ void compute_entries(const Params& P) {
 template <int WT>
 __device__ __forceinline__ void cursor_enter(const Params& P, Cursor& c) {
   const int st = c.s % NSTAGE;
+  c.st = st;
   const LayerDev& Ld = sp().layers[c.s / NSTAGE];
   const Entry& e = ctx().ent[threadIdx.x >> 5][st];
   c.pos = e.lo;
   c.end = e.hi;
   if (st == ST_ATT) {
+    c.aseq = (int)(e.lo / (uint32_t)P.nt_att);
+    c.ai = (int)(e.lo - (uint32_t)c.aseq * (uint32_t)P.nt_att);
+    c.a = (uint32_t)((int64_t)c.aseq * P.s_max + 16 * c.ai);
     c.pos *= 2;
     c.end *= 2;
     c.kbase = Ld.kc;
@@ -222,6 +228,7 @@ __device__ __forceinline__ void cursor_enter(const Params& P, Cursor& c) {
     c.kc = e.kc;
     c.gi = e.gi;
     c.gk = e.gk;
+    c.a = (uint32_t)c.kc * (uint32_t)c.NT * (uint32_t)c.Gc + (uint32_t)c.T * (uint32_t)c.gk + (uint32_t)c.gi;
   }
 }
 template <int WT>
@@ -231,23 +238,31 @@ __device__ __forceinline__ bool cursor_next(const Params& P, Cursor& c, int64_t 
     if (++c.s >= P.stage_end) return false;
     cursor_enter<WT>(P, c);
   }
-  if (c.s % NSTAGE == ST_ATT) {
-    const int64_t tile = c.pos >> 1;
+  if (c.st == ST_ATT) {  // K then V of one 16-key tile
     d.kind = (c.pos & 1) ? SK_V : SK_K;
-    d.a = tile;
-    const int64_t rows = P.pos - 16 * (int64_t)((uint32_t)tile % (uint32_t)P.nt_att);
-    d.cnt = (int)(rows < 0 ? 0 : rows > 16 ? 16 : rows);
+    d.a = c.a;
+    d.cnt = 16;
+    if (c.pos & 1) {  // the next tile
+      if (++c.ai == P.nt_att) {
+        c.ai = 0;
+        ++c.aseq;
+        c.a = (uint32_t)((int64_t)c.aseq * P.s_max);
+      } else {
+        c.a += 16;
+      }
+    }
     c.pos += 1;
   } else {  // up to PER blocks of one (k-chunk, tile) unit, in panel work order
     constexpr int PER = WT == DDL_W_INT4 ? BLKS_PER_SLOT : BF16_BLKS_PER_SLOT;
     d.kind = SK_GEMV;
-    const int64_t left = c.end - c.pos;
-    int n = (int)(left < PER ? left : PER);
+    const uint32_t left = c.end - c.pos;
+    int n = left < (uint32_t)PER ? (int)left : PER;
     if (n > c.gk - c.gi) n = c.gk - c.gi;
-    d.a = (int64_t)c.kc * c.NT * c.Gc + (int64_t)c.T * c.gk + c.gi;  // stream block index
+    d.a = c.a;
     d.cnt = n;
     c.pos += n;
     c.gi += n;
+    c.a += n;
     if (c.gi == c.gk) {
       c.gi = 0;
       if (++c.kc == c.pk1) {
@@ -255,6 +270,7 @@ __device__ __forceinline__ bool cursor_next(const Params& P, Cursor& c, int64_t 
         ++c.T;
       }
       c.gk = c.kc == c.Sk - 1 ? c.G - (c.Sk - 1) * c.Gc : c.Gc;
+      c.a = (uint32_t)c.kc * (uint32_t)c.NT * (uint32_t)c.Gc + (uint32_t)c.T * (uint32_t)c.gk;
     }
   }
   return true;
@@ -275,15 +291,13 @@ __device__ __forceinline__ void issue_slot(const Params& P, const Cursor& c, con
       constexpr uint32_t BB = q4 ? BLK_BYTES : BF16_BLK_BYTES;
       const uint32_t wb = d.cnt * BB, sb = q4 ? d.cnt * SCL_BYTES : 0;
       mbar_arrive_expect_tx(bar, wb + sb);
-      bulk_g2s_evict_first(slot, c.wbase + d.a * BB, wb, bar, policy);
-      if (q4) bulk_g2s_evict_first(slot + BLKS_PER_SLOT * BLK_BYTES, c.sbase + d.a * SCL_BYTES, sb, bar, policy);
+      bulk_g2s_evict_first(slot, c.wbase + (uint64_t)d.a * BB, wb, bar, policy);
+      if (q4) bulk_g2s_evict_first(slot + BLKS_PER_SLOT * BLK_BYTES, c.sbase + (uint64_t)d.a * SCL_BYTES, sb, bar, policy);
     }
   } else {  // 16 rows of K or V: HD/32 boxes of 16 rows x 64 bytes, swizzled (kv_addr)
-    const uint32_t seq = (uint32_t)d.a / (uint32_t)P.nt_att, i = (uint32_t)d.a - seq * (uint32_t)P.nt_att;
-    const int y = (int)((int64_t)seq * P.s_max + 16 * i);
     if (lane == 0) mbar_arrive_expect_tx(bar, 16 * HD * 2);
     if (lane < HD / 32)
-      tensor2d_g2s(slot + lane * 1024, d.kind == SK_K ? c.kmap : c.vmap, lane * 32, y, bar, policy);
+      tensor2d_g2s(slot + lane * 1024, d.kind == SK_K ? c.kmap : c.vmap, lane * 32, (int)d.a, bar, policy);
   }
 }
 
@@ -2082,6 +2096,7 @@ static int decode(const ddl_shape* s, ddl_wtype wtype, const ddl_layer_w* layers
   if (wtype == DDL_W_BF16 && B > NARROW_B) return DDL_ERR_UNSUPPORTED;
   if (!resid_in && !x_bf16) return DDL_ERR_ARG;
   const int64_t s_max = kv[0].s_max;
+  if ((int64_t)B * s->H_kv * s_max >= (1ll << 31)) return DDL_ERR_UNSUPPORTED;  // K/V tensor-map rows
   if (pos < 0 || pos >= s_max) return DDL_ERR_POS;
   for (int l = 0; l < L; ++l) {
     if (!layers[l].packed || !layers[l].norm1 || !layers[l].norm2 || !kv[l].k || !kv[l].v)
