@@ -400,25 +400,17 @@ __device__ __noinline__ void gemv_prologue(const Params& P, const GemvCtx& E, ui
   uint8_t* nws = smem + SM_NW;
   // 1. copies (earlier readers of these areas, any thread, are done first)
   __syncthreads();
-  {
+  {  // (the norm weights are already on their way: gemv_prep, before the barrier)
     const int xsh = x32 ? 4 : 3;  // log2 of the 16-byte pieces of one (group, sequence)
-    const int nx = (ngr * B) << xsh, nn = nw ? ngr * 8 : 0, nnx = nw_next ? P.D / 8 : 0;
-    for (int i = tid; i < nx + nn + nnx; i += NTHREADS) {
-      if (i < nx) {
-        const int gsb = i >> xsh, q = i & ((1 << xsh) - 1);
-        const int gs = (int)(((uint64_t)gsb * invB) >> 32), b = gsb - gs * B;
-        if (gs < ngv) {
-          const int64_t k = kbase + (int64_t)gs * DDL_GROUP;
-          const void* src = x32 ? (const void*)(x32 + (int64_t)b * K + k + q * 4)
-                                : (const void*)(x16 + (int64_t)b * K + k + q * 8);
-          cp_async16(smem_addr(raw + (size_t)gsb * 256 + q * 16), src);
-        }
-      } else if (i < nx + nn) {
-        const int j = i - nx, gs = j >> 3, q = j & 7;
-        if (gs < ngv) cp_async16(smem_addr(nws + (size_t)gs * 128 + q * 16), nw + kbase + (int64_t)gs * DDL_GROUP + q * 8);
-      } else {
-        const int j = i - nx - nn;
-        cp_async16(smem_addr(nws + (size_t)j * 16), nw_next + (int64_t)j * 8);
+    const int nx = (ngr * B) << xsh;
+    for (int i = tid; i < nx; i += NTHREADS) {
+      const int gsb = i >> xsh, q = i & ((1 << xsh) - 1);
+      const int gs = (int)(((uint64_t)gsb * invB) >> 32), b = gsb - gs * B;
+      if (gs < ngv) {
+        const int64_t k = kbase + (int64_t)gs * DDL_GROUP;
+        const void* src = x32 ? (const void*)(x32 + (int64_t)b * K + k + q * 4)
+                              : (const void*)(x16 + (int64_t)b * K + k + q * 8);
+        cp_async16(smem_addr(raw + (size_t)gsb * 256 + q * 16), src);
       }
     }
   }
@@ -840,6 +832,34 @@ __device__ __noinline__ void fill_gemv_ctx(const Params& P, int layer, int st) {
   __syncthreads();
 }
 
+// Before a weight stage's barrier: its context and the copies that do not
+// depend on the previous stage (the panel's norm weights, and for Wo and down
+// the next stage's norm vector for the epilogue maxima).
+__device__ __noinline__ void gemv_prep(const Params& P, int layer, int st, uint8_t* smem) {
+  fill_gemv_ctx(P, layer, st);
+  const GemvCtx& E = ctx().E;
+  const MatGeom& m = E.m;
+  const LayerDev& Ld = sp().layers[layer];
+  const uint16_t* nw = st == ST_QKV ? Ld.norm1 : st == ST_GU ? Ld.norm2 : nullptr;
+  const uint16_t* nw_next = st == ST_WO ? Ld.norm2
+                            : (st == ST_DOWN && layer + 1 < P.L) ? sp().layers[layer + 1].norm1 : nullptr;
+  if ((int64_t)P.D * 2 > SM_NW_BYTES) nw_next = nullptr;
+  const int kc_lo = m.pk[E.p], nkc = m.pk[E.p + 1] - kc_lo;
+  const int ngr = nkc * GC, ngv = (nkc - 1) * GC + chunk_groups(m, kc_lo + nkc - 1);
+  const int kbase = kc_lo * GC * DDL_GROUP;
+  uint8_t* nws = smem + SM_NW;
+  const int nn = nw ? ngr * 8 : 0, nnx = nw_next ? P.D / 8 : 0;
+  for (int i = threadIdx.x; i < nn + nnx; i += NTHREADS) {
+    if (i < nn) {
+      const int gs = i >> 3, q = i & 7;
+      if (gs < ngv) cp_async16(smem_addr(nws + (size_t)gs * 128 + q * 16), nw + kbase + (int64_t)gs * DDL_GROUP + q * 8);
+    } else {
+      const int j = i - nn;
+      cp_async16(smem_addr(nws + (size_t)j * 16), nw_next + (int64_t)j * 8);
+    }
+  }
+}
+
 // ------------------------------------------------------------------ GEMV stage
 // The warp walks its range of the panel's work order (tile, k-chunk, group).
 // Per ring slot (up to 8 groups of one (k-chunk, tile) unit): the 8 blocks'
@@ -873,8 +893,7 @@ template <int HD, int WT>
 __device__ __forceinline__ bool stage_gemv_body(const Params& P, int layer, int st, Ring& R,
                                                 Cursor& prod, int64_t wg, int64_t W, uint8_t* smem,
                                                 Misc& M, uint64_t policy) {
-  fill_gemv_ctx(P, layer, st);
-  GemvCtx& E = ctx().E;
+  GemvCtx& E = ctx().E;  // filled by gemv_prep
   const MatGeom& m = E.m;
   gemv_prologue<HD, WT>(P, E, smem, M);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
@@ -1047,18 +1066,6 @@ __device__ __noinline__ void gemv_prologue_wide(const Params& P, const GemvCtx& 
   const bool have_max = !(E.st == ST_QKV && E.layer == 0);
   uint8_t* nws = smem + SM_NW;
   __syncthreads();
-  {  // norm weights of the panel and the next stage's norm vector
-    const int nn = nw ? ngr * 8 : 0, nnx = nw_next ? P.D / 8 : 0;
-    for (int i = tid; i < nn + nnx; i += NTHREADS) {
-      if (i < nn) {
-        const int gs = i >> 3, q = i & 7;
-        if (gs < ngv) cp_async16(smem_addr(nws + (size_t)gs * 128 + q * 16), nw + kbase + (int64_t)gs * DDL_GROUP + q * 8);
-      } else {
-        const int j = i - nn;
-        cp_async16(smem_addr(nws + (size_t)j * 16), nw_next + (int64_t)j * 8);
-      }
-    }
-  }
   float xm = 0.f;
   if (have_max && tid < B) xm = __uint_as_float(__ldcg(P.xmax + (E.layer * NSTAGE + E.st) * MAX_B + tid));
   if (nw && !whole) {
@@ -1312,8 +1319,7 @@ __device__ __noinline__ bool stage_gemv_wide(const Params& P, int layer, int st,
   __syncwarp();
   Ring R = Rm;
   Cursor prod = prodm;
-  fill_gemv_ctx(P, layer, st);
-  GemvCtx& E = ctx().E;
+  GemvCtx& E = ctx().E;  // filled by gemv_prep
   const MatGeom& m = E.m;
   gemv_prologue_wide<HD, WT>(P, E, smem, M);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
@@ -1842,13 +1848,16 @@ __device__ __noinline__ void flush_cmax(const Params& P, Misc& M, int layer, int
 }
 
 // ------------------------------------------------------------------ grid barrier
-__device__ bool grid_sync(const Params& P, uint32_t target, Misc& M) {
+// Arrival: the CTA's writes of this stage (ordered before by the block
+// barrier) become visible no later than the release.  The wait (acquiring
+// polls) orders the next stage's reads after every CTA's arrival; between
+// the two the CTA prepares its next stage.
+__device__ void grid_arrive(const Params& P) {
   __syncthreads();
+  if (threadIdx.x == 0) red_release_gpu_add(P.ctrl, 1u);
+}
+__device__ bool grid_wait(const Params& P, uint32_t target, Misc& M) {
   if (threadIdx.x == 0) {
-    // release: the CTA's writes of this stage (ordered before by the block
-    // barrier) become visible no later than the arrival; the acquiring poll
-    // below orders the next stage's reads after every CTA's arrival
-    red_release_gpu_add(P.ctrl, 1u);
     uint64_t t0 = 0;
     for (uint32_t it = 1; ld_acquire_gpu(P.ctrl) < target; ++it) {
       if ((it & 255u) != 0) continue;
@@ -1918,13 +1927,14 @@ __global__ void __launch_bounds__(NTHREADS, 1) decode_kernel(const __grid_consta
   }
   bool ok = true;
   for (int s = P.stage_begin; s < P.stage_end && ok; ++s) {
+    const int layer = s / NSTAGE, st = s % NSTAGE;
+    if (st != ST_ATT) gemv_prep(P, layer, st, smem);
     if (s != P.stage_begin && P.cooperative) {
-      if (!grid_sync(P, (uint32_t)(s - P.stage_begin) * gridDim.x, M)) {
+      if (!grid_wait(P, (uint32_t)(s - P.stage_begin) * gridDim.x, M)) {
         ok = false;
         break;
       }
     }
-    const int layer = s / NSTAGE, st = s % NSTAGE;
     if (threadIdx.x == 0) trace_stamp(P, s, 0);
     if (st == ST_ATT) {
       if (threadIdx.x == 0) trace_stamp(P, s, 1);
@@ -1937,6 +1947,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) decode_kernel(const __grid_consta
     if (threadIdx.x == 0) trace_stamp(P, s, NW + 2);
     if (M.abort) ok = false;
     if (threadIdx.x < P.B) flush_cmax(P, M, layer, st);
+    if (P.cooperative && s + 1 < P.stage_end) grid_arrive(P);
   }
   if (!ok) {  // let this warp's copies in flight land before the CTA exits (bounded)
     __syncwarp();
