@@ -600,7 +600,8 @@ __device__ __forceinline__ float epi_norm(const Params& P, const uint16_t* w, in
 // Rows g and g+8 of tile T for sequence t (narrow batches: t = lane % 4).
 template <int HD>
 __device__ __noinline__ void gemv_epilogue(const Params& P, const GemvCtx& E, int T, int t, float v0,
-                                           float v1, Misc& M) {
+                                           float v1, Misc& M, bool have_res = false, float res0 = 0.f,
+                                           float res1 = 0.f) {
   const int lane = threadIdx.x & 31, g = lane >> 2;  // rows g, g+8 of tile T for sequence t
   if (E.st == ST_QKV) {
     const float r = M.rnorm[t];
@@ -626,8 +627,8 @@ __device__ __noinline__ void gemv_epilogue(const Params& P, const GemvCtx& E, in
   } else if (E.st == ST_WO) {
     const int r0 = 16 * T + g, r1 = r0 + 8;
     const int64_t o = (int64_t)t * P.D;
-    const float x0 = E.xin32 ? __ldcg(E.xin32 + o + r0) : bf16_bits_to_f32(E.xin16[o + r0]);
-    const float x1 = E.xin32 ? __ldcg(E.xin32 + o + r1) : bf16_bits_to_f32(E.xin16[o + r1]);
+    const float x0 = have_res ? res0 : E.xin32 ? __ldcg(E.xin32 + o + r0) : bf16_bits_to_f32(E.xin16[o + r0]);
+    const float x1 = have_res ? res1 : E.xin32 ? __ldcg(E.xin32 + o + r1) : bf16_bits_to_f32(E.xin16[o + r1]);
     const float y0 = x0 + v0, y1 = x1 + v1;
     P.y[o + r0] = y0;
     P.y[o + r1] = y1;
@@ -643,7 +644,7 @@ __device__ __noinline__ void gemv_epilogue(const Params& P, const GemvCtx& E, in
   } else {
     const int r0 = 16 * T + g, r1 = r0 + 8;
     const int64_t o = (int64_t)t * P.D;
-    const float z0 = __ldcg(P.y + o + r0) + v0, z1 = __ldcg(P.y + o + r1) + v1;
+    const float z0 = (have_res ? res0 : __ldcg(P.y + o + r0)) + v0, z1 = (have_res ? res1 : __ldcg(P.y + o + r1)) + v1;
     E.zout[o + r0] = z0;
     E.zout[o + r1] = z1;
     if (E.layer + 1 < P.L) {  // the next layer's QKV scales its staged x by max |z * norm1|
@@ -712,25 +713,57 @@ __device__ __noinline__ void gemv_publish(const Params& P, const GemvCtx& E, con
   }
 }
 
-// Cooperative launch: tile T's owner (the warp holding its first blocks in
-// panel 0) finishes it.  It waits (bounded) until every other contributor has
-// released its partial, then sums all partials in slot order with its own in
-// its slot's place (deterministic) and runs the epilogue.
-template <int HD>
-__device__ __noinline__ void owner_fixup(const Params& P, const GemvCtx& E, int T, float o0, float o1,
-                                         Misc& M) {
-  const MatGeom& m = E.m;
-  const int lane = threadIdx.x & 31;
-  uint32_t expected = 0;
+// Cooperative launch: a tile's owner (the warp holding its first blocks in
+// panel 0) finishes it.  For the warp's one or two owned tiles together: wait
+// (bounded) until every other contributor has released its partial, then load
+// all partials and the epilogue's residual values in one round trip, sum the
+// partials in slot order with the owner's own in its slot's place
+// (deterministic), and run the epilogues.
+__device__ __forceinline__ uint32_t owned_slots(const MatGeom& m, int T) {  // bit f = p * J + j
+  uint32_t mask = 0;
   for (int p = 0; p < m.NP; ++p) {
     const uint32_t Gp = panel_groups(m, p);
     const uint32_t v0 = work_owner(m, p, (uint32_t)T * Gp, NW), v1 = work_owner(m, p, (uint32_t)(T + 1) * Gp - 1, NW);
     for (uint32_t v = v0; v <= v1; ++v)
-      if ((p != 0 || v != v0) && !warp_empty(m, p, v, NW)) ++expected;
+      if (!warp_empty(m, p, v, NW)) mask |= 1u << (p * m.J + (v - v0));
   }
+  return mask;
+}
+template <int HD>
+__device__ __forceinline__ void owned_sum(const Params& P, const GemvCtx& E, int T, uint32_t mask, float o0,
+                                          float o1, float& s0, float& s1) {
+  const float2* part = reinterpret_cast<const float2*>(P.gpart) + (int64_t)T * E.m.NP * E.m.J * 32 +
+                       (threadIdx.x & 31);
+  float2 x[8];
+#pragma unroll
+  for (int f = 0; f < 8; ++f)
+    x[f] = (f > 0 && (mask >> f & 1u)) ? __ldcg(part + f * 32) : make_float2(0.f, 0.f);
+  s0 = o0;
+  s1 = o1;
+#pragma unroll
+  for (int f = 1; f < 8; ++f) {
+    s0 += x[f].x;
+    s1 += x[f].y;
+  }
+  for (int f = 8; f < 32; ++f)
+    if (mask >> f & 1u) {
+      const float2 y = __ldcg(part + f * 32);
+      s0 += y.x;
+      s1 += y.y;
+    }
+}
+template <int HD>
+__device__ __noinline__ void owner_fixup(const Params& P, const GemvCtx& E, int n, int T0, float a0,
+                                         float b0, int T1, float a1, float b1, Misc& M) {
+  const MatGeom& m = E.m;
+  const int lane = threadIdx.x & 31, t = lane & 3, g = lane >> 2;
+  const uint32_t mk0 = owned_slots(m, T0), mk1 = n > 1 ? owned_slots(m, T1) : 1u;
+  const uint32_t e0 = __popc(mk0) - 1, e1 = __popc(mk1) - 1;
   if (lane == 0) {
     uint64_t t0 = 0;
-    for (uint32_t it = 1; ld_acquire_gpu(P.cnt + T) < expected; ++it) {
+    for (uint32_t it = 1;; ++it) {
+      const uint32_t c0 = ld_acquire_gpu(P.cnt + T0), c1 = n > 1 ? ld_acquire_gpu(P.cnt + T1) : e1;
+      if (c0 >= e0 && c1 >= e1) break;
       if ((it & 255u) != 0) continue;
       const uint64_t now = globaltimer();
       if (t0 == 0) t0 = now;
@@ -742,24 +775,30 @@ __device__ __noinline__ void owner_fixup(const Params& P, const GemvCtx& E, int 
     }
   }
   __syncwarp();
-  const float2* part = reinterpret_cast<const float2*>(P.gpart) + (int64_t)T * m.NP * m.J * 32 + lane;
-  float s0 = 0.f, s1 = 0.f;
-  for (int p = 0; p < m.NP; ++p) {
-    const uint32_t Gp = panel_groups(m, p);
-    const uint32_t v0 = work_owner(m, p, (uint32_t)T * Gp, NW), v1 = work_owner(m, p, (uint32_t)(T + 1) * Gp - 1, NW);
-    for (uint32_t v = v0; v <= v1; ++v) {
-      if (p == 0 && v == v0) {
-        s0 += o0;
-        s1 += o1;
-      } else if (!warp_empty(m, p, v, NW)) {
-        const float2 x = __ldcg(part + ((int64_t)p * m.J + (v - v0)) * 32);
-        s0 += x.x;
-        s1 += x.y;
-      }
+  // the residual inputs of the Wo / down epilogues, loaded with the partials
+  const bool res = (E.st == ST_WO || E.st == ST_DOWN) && t < P.B && (E.st == ST_DOWN || E.xin32);
+  const float* rb = E.st == ST_DOWN ? P.y : E.xin32;
+  float r00 = 0.f, r01 = 0.f, r10 = 0.f, r11 = 0.f;
+  if (res) {
+    const int64_t o = (int64_t)t * P.D;
+    r00 = __ldcg(rb + o + 16 * T0 + g);
+    r01 = __ldcg(rb + o + 16 * T0 + g + 8);
+    if (n > 1) {
+      r10 = __ldcg(rb + o + 16 * T1 + g);
+      r11 = __ldcg(rb + o + 16 * T1 + g + 8);
     }
   }
-  if ((threadIdx.x & 3) < P.B) gemv_epilogue<HD>(P, E, T, threadIdx.x & 3, s0, s1, M);
-  if (lane == 0) P.cnt[T] = 0;
+  float s0, s1, u0 = 0.f, u1 = 0.f;
+  owned_sum<HD>(P, E, T0, mk0, a0, b0, s0, s1);
+  if (n > 1) owned_sum<HD>(P, E, T1, mk1, a1, b1, u0, u1);
+  if (t < P.B) {
+    gemv_epilogue<HD>(P, E, T0, t, s0, s1, M, res, r00, r01);
+    if (n > 1) gemv_epilogue<HD>(P, E, T1, t, u0, u1, M, res, r10, r11);
+  }
+  if (lane == 0) {
+    P.cnt[T0] = 0;
+    if (n > 1) P.cnt[T1] = 0;
+  }
 }
 
 // Finish this warp's share of tile T (nblk of its blocks, sums v0, v1 in true
@@ -785,7 +824,7 @@ __device__ __forceinline__ void tile_finish(const Params& P, const GemvCtx& E, M
     } else if (nown == 1) {
       oT1 = T; oa1 = v0; ob1 = v1;
     } else {
-      owner_fixup<HD>(P, E, T, v0, v1, M);  // more than two: finish this one now
+      owner_fixup<HD>(P, E, 1, T, v0, v1, 0, 0.f, 0.f, M);  // more than two: finish this one now
       return;
     }
     ++nown;
@@ -1023,8 +1062,7 @@ __device__ __forceinline__ bool stage_gemv_body(const Params& P, int layer, int 
     tile_finish<HD>(P, E, M, T, nblk, fmaf(acc0, esc, tac0), fmaf(acc1, esc, tac1), pend, npend, nown, oT0,
                     oa0, ob0, oT1, oa1, ob1);
   if (npend) gemv_publish<HD>(P, E, pend, npend, M);
-  if (nown > 0) owner_fixup<HD>(P, E, oT0, oa0, ob0, M);
-  if (nown > 1) owner_fixup<HD>(P, E, oT1, oa1, ob1, M);
+  if (nown > 0) owner_fixup<HD>(P, E, nown, oT0, oa0, ob0, oT1, oa1, ob1, M);
   if (lane == 0) trace_stamp(P, layer * NSTAGE + st, 2 + warp);
   return true;
 }

@@ -102,7 +102,7 @@ inline bool make_panels(MatGeom& m, int B, int C) {
       if (m.NP > 1 || (T + 1) * Gp0 > hi) ++own;
     if (own > maxown) maxown = own;
   }
-  m.own_ok = maxown <= 2;
+  m.own_ok = maxown <= 2 && NP * (int)J <= 32;  // owners track a tile's slots in a 32-bit mask
   return true;
 }
 
