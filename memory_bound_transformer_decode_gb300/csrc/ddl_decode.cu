@@ -363,13 +363,19 @@ __device__ __forceinline__ void trace_stamp(const Params& P, int s, int slot) {
 // recorded by the stage that produced x (one word per sequence), so one pass
 // over the panel suffices; only the first layer of a launch has no producer
 // and measures its panel.
-// cp.async copies (through L1, so that they do not queue behind the weight
-// ring's bulk copies in the TMA unit) bring every (group, sequence) of x into
-// 256 bytes of shared memory and every group of norm weights into 128 bytes;
-// the Wo and down stages also stage the next weight stage's norm vector for
-// their epilogue maxima.  Item it = ((group slot * B + b) * 16 + quad) is one
-// four-column quad of x at byte it*16 of the staged x (fp32).  The conversion
-// runs in rounds of whole groups: read, block barrier, write in place.
+// A unit (group slot gs, sequence b, k-slice j) is 16 values of x.  Its
+// fragments fill 64 bytes: words 4 (r % 2) + 2 k + r / 2 (high parts) and 8 +
+// the same (low parts) for pair k of quad r (values 4 r + 2 k, +1).  cp.async
+// copies (through L1, so that they do not queue behind the weight ring's bulk
+// copies in the TMA unit) put the unit's four fp32 quads in those same 64
+// bytes, so one thread converts a unit in place, with no barrier between
+// units.  This code runs once per stage: its loops are rolled, because each
+// new instruction is fetched while the memory system carries the weight
+// stream.  The panel's norm weights were copied before the stage's grid
+// barrier (gemv_prep).
+__device__ __forceinline__ uint32_t unit_offset(int gs, int b, int j, int B) {  // bytes
+  return (uint32_t)gs * B * 256 + (uint32_t)(j * 2 * B + 2 * b) * 32;
+}
 template <int HD, int WT>
 __device__ __noinline__ void gemv_prologue(const Params& P, const GemvCtx& E, uint8_t* smem, Misc& M) {
   const MatGeom& m = E.m;
@@ -378,193 +384,186 @@ __device__ __noinline__ void gemv_prologue(const Params& P, const GemvCtx& E, ui
   const int kc_lo = m.pk[E.p], nkc = m.pk[E.p + 1] - kc_lo;
   const float* x32 = nullptr;
   const uint16_t* x16 = nullptr;
-  const uint16_t* nw = nullptr;       // this stage's norm weights (QKV, GU)
-  const uint16_t* nw_next = nullptr;  // the next weight stage's (Wo, down), for the maxima
+  const uint16_t* nw = nullptr;  // this stage's norm weights (QKV, GU)
   const LayerDev& Ld = sp().layers[E.layer];
   switch (E.st) {
     case ST_QKV: nw = Ld.norm1; x32 = E.xin32; x16 = E.xin16; break;
-    case ST_WO: x32 = P.attn; nw_next = Ld.norm2; break;
+    case ST_WO: x32 = P.attn; break;
     case ST_GU: x32 = P.y; nw = Ld.norm2; break;
-    default: x32 = P.a; nw_next = E.layer + 1 < P.L ? sp().layers[E.layer + 1].norm1 : nullptr; break;
+    default: x32 = P.a; break;
   }
-  if ((int64_t)P.D * 2 > SM_NW_BYTES) nw_next = nullptr;  // the epilogue reads it from memory
   const int K = m.K;
-  const int ngr = nkc * GC;                                                   // group slots
-  const int ngv = (nkc - 1) * GC + chunk_groups(m, kc_lo + nkc - 1);          // ... holding data
-  const int n_items = ngr * B * 16;
+  const int ngv = (nkc - 1) * GC + chunk_groups(m, kc_lo + nkc - 1);  // group slots holding data
+  const int n_units = ngv * B * 4;
   const int kbase = kc_lo * GC * DDL_GROUP;
   const bool whole = nkc == m.Sk;  // the panel is the whole vector
   const bool have_max = !(E.st == ST_QKV && E.layer == 0);
-  const uint64_t invB = ((1ull << 32) + B - 1) / B;  // g / B == (g * invB) >> 32 for the indices here
-  uint8_t* raw = smem + SM_SCR;
-  uint8_t* nws = smem + SM_NW;
-  // 1. copies (earlier readers of these areas, any thread, are done first)
+  const uint32_t invB = (65536u + B - 1) / B;  // g / B == (g * invB) >> 16 for g < 2^15
+  const uint32_t raw = smem_addr(smem + SM_SCR);
+  const uint32_t nws = smem_addr(smem + SM_NW);
+  // 1. copies (earlier readers of these areas, any thread, are done first):
+  //    quad i = (gs * B + b) * 16 + q16 of x to quad q16 % 4 of its unit
   __syncthreads();
-  {  // (the norm weights are already on their way: gemv_prep, before the barrier)
-    const int xsh = x32 ? 4 : 3;  // log2 of the 16-byte pieces of one (group, sequence)
-    const int nx = (ngr * B) << xsh;
-    for (int i = tid; i < nx; i += NTHREADS) {
-      const int gsb = i >> xsh, q = i & ((1 << xsh) - 1);
-      const int gs = (int)(((uint64_t)gsb * invB) >> 32), b = gsb - gs * B;
-      if (gs < ngv) {
-        const int64_t k = kbase + (int64_t)gs * DDL_GROUP;
-        const void* src = x32 ? (const void*)(x32 + (int64_t)b * K + k + q * 4)
-                              : (const void*)(x16 + (int64_t)b * K + k + q * 8);
-        cp_async16(smem_addr(raw + (size_t)gsb * 256 + q * 16), src);
-      }
-    }
+#pragma unroll 1
+  for (int i = tid; i < n_units * 4; i += NTHREADS) {
+    const int gsb = i >> 4, q16 = i & 15;
+    const int gs = (int)(((uint32_t)gsb * invB) >> 16), b = gsb - gs * B;
+    const int64_t o = (int64_t)b * K + kbase + gs * DDL_GROUP + q16 * 4;
+    const uint32_t dst = raw + unit_offset(gs, b, q16 >> 2, B) + (q16 & 3) * 16;
+    if (x32) cp_async16(dst, x32 + o);
+    else cp_async8(dst, x16 + o);
   }
-  float xm = 0.f;  // thread b < B: the producer's max for sequence b
-  if (have_max && tid < B) xm = __uint_as_float(__ldcg(P.xmax + (E.layer * NSTAGE + E.st) * MAX_B + tid));
+  float xm[NARROW_B] = {0.f, 0.f, 0.f, 0.f};
+  if (have_max) {
+#pragma unroll
+    for (int b = 0; b < NARROW_B; ++b)
+      if (b < B) xm[b] = __uint_as_float(__ldcg(P.xmax + (E.layer * NSTAGE + E.st) * MAX_B + b));
+  }
   if (tid == 0) trace_stamp(P, E.layer * NSTAGE + E.st, NW + 3);
   // 2. meanwhile (a norm stage whose panel is not the whole vector): the sum of squares
   if (nw && !whole) {
+#pragma unroll 1
     for (int b = 0; b < B; ++b) {
       float ss = 0.f;
-      const int nq = K / 4;
-      for (int q0 = tid; q0 < nq; q0 += 8 * NTHREADS) {
-        float4 v[8];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const int q = q0 + u * NTHREADS;
-          if (q >= nq) v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-          else if (x32) v[u] = __ldcg(reinterpret_cast<const float4*>(x32 + (int64_t)b * K) + q);
-          else v[u] = bf16x4_f32(__ldcg(reinterpret_cast<const uint2*>(x16 + (int64_t)b * K) + q));
-        }
-#pragma unroll
-        for (int u = 0; u < 8; ++u)
-          ss = fmaf(v[u].x, v[u].x, fmaf(v[u].y, v[u].y, fmaf(v[u].z, v[u].z, fmaf(v[u].w, v[u].w, ss))));
+#pragma unroll 4
+      for (int q = tid; q < K / 4; q += NTHREADS) {
+        const float4 x = x32 ? __ldcg(reinterpret_cast<const float4*>(x32 + (int64_t)b * K) + q)
+                             : bf16x4_f32(__ldcg(reinterpret_cast<const uint2*>(x16 + (int64_t)b * K) + q));
+        ss = fmaf(x.x, x.x, fmaf(x.y, x.y, fmaf(x.z, x.z, fmaf(x.w, x.w, ss))));
       }
       ss = warp_sum(ss);
       if (lane == 0) M.red[warp][2 * b] = ss;
     }
   }
-  if (tid == 0) trace_stamp(P, E.layer * NSTAGE + E.st, NW + 4);
   cp_async_wait_all();
   __syncthreads();
   if (tid == 0) trace_stamp(P, E.layer * NSTAGE + E.st, NW + 5);
+  // the 16 values of unit u (fp32 x, norm weights) from shared memory
+  auto unit_load = [&](int u, float (&x)[16], float (&w)[16], int& gs, int& b, int& j) {
+    const int gsb = u >> 2;
+    j = u & 3;
+    gs = (int)(((uint32_t)gsb * invB) >> 16);
+    b = gsb - gs * B;
+    const uint32_t a = raw + unit_offset(gs, b, j, B);
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      float4 v;
+      if (x32) {
+        const uint4 q = lds128(a + r * 16);
+        v = make_float4(__uint_as_float(q.x), __uint_as_float(q.y), __uint_as_float(q.z), __uint_as_float(q.w));
+      } else {
+        v = bf16x4_f32(lds64(a + r * 16));
+      }
+      x[4 * r] = v.x;
+      x[4 * r + 1] = v.y;
+      x[4 * r + 2] = v.z;
+      x[4 * r + 3] = v.w;
+    }
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const uint4 q = nw ? lds128(nws + gs * 128 + j * 32 + h * 16) : make_uint4(0x3f803f80u, 0x3f803f80u, 0x3f803f80u, 0x3f803f80u);
+      w[8 * h] = bf16lo_f32(q.x);
+      w[8 * h + 1] = bf16hi_f32(q.x);
+      w[8 * h + 2] = bf16lo_f32(q.y);
+      w[8 * h + 3] = bf16hi_f32(q.y);
+      w[8 * h + 4] = bf16lo_f32(q.z);
+      w[8 * h + 5] = bf16hi_f32(q.z);
+      w[8 * h + 6] = bf16lo_f32(q.w);
+      w[8 * h + 7] = bf16hi_f32(q.w);
+    }
+  };
   // 3. the scale: the producer's max, or (first layer of a launch) the panel's
   if (!have_max) {
-    float mx[NARROW_B] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 2
-    for (int it = tid; it < n_items; it += NTHREADS) {
-      const int gsb = it >> 4, q16 = it & 15;
-      const int gs = (int)(((uint64_t)gsb * invB) >> 32), b = gsb - gs * B;
-      if (gs >= ngv) continue;
-      float4 x = x32 ? *reinterpret_cast<const float4*>(raw + (size_t)it * 16)
-                     : bf16x4_f32(*reinterpret_cast<const uint2*>(raw + (size_t)gsb * 256 + q16 * 8));
-      if (nw) {
-        const float4 w = bf16x4_f32(*reinterpret_cast<const uint2*>(nws + (size_t)gs * 128 + q16 * 8));
-        x = make_float4(x.x * w.x, x.y * w.y, x.z * w.z, x.w * w.w);
-      }
-      const float a = fmaxf(fmaxf(fabsf(x.x), fabsf(x.y)), fmaxf(fabsf(x.z), fabsf(x.w)));
+#pragma unroll 1
+    for (int u = tid; u < n_units; u += NTHREADS) {
+      float x[16], w[16];
+      int gs, b, j;
+      unit_load(u, x, w, gs, b, j);
+      float a = 0.f;
+#pragma unroll
+      for (int e = 0; e < 16; ++e) a = fmaxf(a, fabsf(x[e] * w[e]));
 #pragma unroll
       for (int bb = 0; bb < NARROW_B; ++bb)
-        if (bb == b) mx[bb] = fmaxf(mx[bb], a);
+        if (bb == b) xm[bb] = fmaxf(xm[bb], a);
     }
 #pragma unroll
     for (int b = 0; b < NARROW_B; ++b) {
-      if (b < B) {
-        const float r = warp_max(mx[b]);
-        if (lane == 0) M.red[warp][2 * b + 1] = r;
-      }
+      const float r = warp_max(xm[b]);
+      if (lane == 0 && b < B) M.red[warp][2 * b + 1] = r;
     }
     __syncthreads();
-    if (tid < B)
-      for (int w = 0; w < NW; ++w) xm = fmaxf(xm, M.red[w][2 * tid + 1]);
+#pragma unroll
+    for (int b = 0; b < NARROW_B; ++b) {
+      xm[b] = 0.f;
+      if (b < B)
+        for (int w = 0; w < NW; ++w) xm[b] = fmaxf(xm[b], M.red[w][2 * b + 1]);
+    }
   }
-  if (tid < B) {
-    const int e = xm > 0.f ? ilogbf(xm) - 11 : 0;
-    M.escale[tid] = ldexpf(1.0f, e);
-    M.edown[tid] = ldexpf(1.0f, -e);
+  float sdn[NARROW_B];  // 2^-e of each sequence
+#pragma unroll
+  for (int b = 0; b < NARROW_B; ++b) {
+    const int e = xm[b] > 0.f ? ilogbf(xm[b]) - 11 : 0;
+    sdn[b] = ldexpf(1.0f, -e);
+    if (tid == b && b < B) M.escale[b] = ldexpf(1.0f, e);
   }
-  __syncthreads();
-  if (tid == 0) trace_stamp(P, E.layer * NSTAGE + E.st, NW + 6);
-  // 4. fragments in place, in rounds of whole groups (up to 4 quads a thread),
-  //    and the sum of squares of x when the panel is the whole vector.  Quad
-  //    q16 holds columns 4 q16 .. 4 q16 + 3 of its group: MMA j = q16 / 4,
-  //    register half (q16 / 2) % 2, lanes t0 = 2 (q16 % 2) and t0 + 1.
-  //    Sx = sum of hi + lo over the group's 16 quads (16 consecutive lanes).
+  // 4. fragments, one unit per thread and trip; Sx = sum of hi + lo over the
+  //    group's four units (four consecutive lanes)
   float* Sx = reinterpret_cast<float*>(smem + SM_SCR + XF_BYTES);
   constexpr bool f16 = WT == DDL_W_INT4;
   const bool want_ss = nw && whole;
   float ssq[NARROW_B] = {0.f, 0.f, 0.f, 0.f};
-  const int ipr = (4 * NTHREADS / (16 * B)) * 16 * B;  // items per round: whole groups
-  for (int r0 = 0; r0 < n_items; r0 += ipr) {
-    float4 v[4];
-    bool ok[4];
+#pragma unroll 1
+  for (int u0 = 0; u0 < n_units; u0 += NTHREADS) {
+    const int u = u0 + tid;
+    float part = 0.f;
+    int gs = 0, b = 0, j = 0;
+    if (u < n_units) {
+      float x[16], w[16];
+      unit_load(u, x, w, gs, b, j);
+      if (want_ss) {
+        float s2 = 0.f;
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int iu = u * NTHREADS + tid, it = r0 + iu;
-      const int gsb = it >> 4, q16 = it & 15;
-      const int gs = (int)(((uint64_t)gsb * invB) >> 32), b = gsb - gs * B;
-      ok[u] = iu < ipr && it < n_items && gs < ngv;
-      v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (ok[u]) {
-        float4 x = x32 ? *reinterpret_cast<const float4*>(raw + (size_t)it * 16)
-                       : bf16x4_f32(*reinterpret_cast<const uint2*>(raw + (size_t)gsb * 256 + q16 * 8));
-        if (want_ss) {
-          const float s2 = fmaf(x.x, x.x, fmaf(x.y, x.y, fmaf(x.z, x.z, x.w * x.w)));
+        for (int e = 0; e < 16; ++e) s2 = fmaf(x[e], x[e], s2);
 #pragma unroll
-          for (int bb = 0; bb < NARROW_B; ++bb)
-            if (bb == b) ssq[bb] += s2;
-        }
-        const float sc = M.edown[b];
-        const float4 w = nw ? bf16x4_f32(*reinterpret_cast<const uint2*>(nws + (size_t)gs * 128 + q16 * 8))
-                            : make_float4(1.f, 1.f, 1.f, 1.f);
-        v[u] = make_float4(x.x * w.x * sc, x.y * w.y * sc, x.z * w.z * sc, x.w * w.w * sc);
+        for (int bb = 0; bb < NARROW_B; ++bb)
+          if (bb == b) ssq[bb] += s2;
       }
-    }
-    __syncthreads();
+      const float sc = b == 0 ? sdn[0] : b == 1 ? sdn[1] : b == 2 ? sdn[2] : sdn[3];
+      uint32_t o[16];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int it = r0 + u * NTHREADS + tid;
-      const int gsb = it >> 4, q16 = it & 15;
-      const int gs = (int)(((uint64_t)gsb * invB) >> 32), b = gsb - gs * B;
-      float part = 0.f;
-      if (ok[u]) {
-        uint32_t h01, h23, l01, l23;
-        float2 hf01, hf23, lf01, lf23;
-        if (f16) {
-          const __half2 a = __float22half2_rn(make_float2(v[u].x, v[u].y));
-          const __half2 c = __float22half2_rn(make_float2(v[u].z, v[u].w));
-          hf01 = __half22float2(a);
-          hf23 = __half22float2(c);
-          const __half2 la = __float22half2_rn(make_float2(v[u].x - hf01.x, v[u].y - hf01.y));
-          const __half2 lc = __float22half2_rn(make_float2(v[u].z - hf23.x, v[u].w - hf23.y));
-          lf01 = __half22float2(la);
-          lf23 = __half22float2(lc);
-          h01 = *reinterpret_cast<const uint32_t*>(&a);
-          h23 = *reinterpret_cast<const uint32_t*>(&c);
-          l01 = *reinterpret_cast<const uint32_t*>(&la);
-          l23 = *reinterpret_cast<const uint32_t*>(&lc);
-        } else {
-          const __nv_bfloat162 a = __float22bfloat162_rn(make_float2(v[u].x, v[u].y));
-          const __nv_bfloat162 c = __float22bfloat162_rn(make_float2(v[u].z, v[u].w));
-          hf01 = __bfloat1622float2(a);
-          hf23 = __bfloat1622float2(c);
-          const __nv_bfloat162 la = __float22bfloat162_rn(make_float2(v[u].x - hf01.x, v[u].y - hf01.y));
-          const __nv_bfloat162 lc = __float22bfloat162_rn(make_float2(v[u].z - hf23.x, v[u].w - hf23.y));
-          lf01 = __bfloat1622float2(la);
-          lf23 = __bfloat1622float2(lc);
-          h01 = *reinterpret_cast<const uint32_t*>(&a);
-          h23 = *reinterpret_cast<const uint32_t*>(&c);
-          l01 = *reinterpret_cast<const uint32_t*>(&la);
-          l23 = *reinterpret_cast<const uint32_t*>(&lc);
+      for (int r = 0; r < 4; ++r)
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+          const int e = 4 * r + 2 * k;
+          const float2 pv = make_float2(x[e] * w[e] * sc, x[e + 1] * w[e + 1] * sc);
+          float2 hf, lf;
+          uint32_t hw, lw;
+          if (f16) {
+            const __half2 h = __float22half2_rn(pv);
+            hf = __half22float2(h);
+            const __half2 l = __float22half2_rn(make_float2(pv.x - hf.x, pv.y - hf.y));
+            lf = __half22float2(l);
+            hw = *reinterpret_cast<const uint32_t*>(&h);
+            lw = *reinterpret_cast<const uint32_t*>(&l);
+          } else {
+            const __nv_bfloat162 h = __float22bfloat162_rn(pv);
+            hf = __bfloat1622float2(h);
+            const __nv_bfloat162 l = __float22bfloat162_rn(make_float2(pv.x - hf.x, pv.y - hf.y));
+            lf = __bfloat1622float2(l);
+            hw = *reinterpret_cast<const uint32_t*>(&h);
+            lw = *reinterpret_cast<const uint32_t*>(&l);
+          }
+          part += (hf.x + lf.x) + (hf.y + lf.y);
+          o[4 * (r & 1) + 2 * k + (r >> 1)] = hw;
+          o[8 + 4 * (r & 1) + 2 * k + (r >> 1)] = lw;
         }
-        part = ((hf01.x + lf01.x) + (hf01.y + lf01.y)) + ((hf23.x + lf23.x) + (hf23.y + lf23.y));
-        const int j = q16 >> 2, half = (q16 >> 1) & 1, t0 = 2 * (q16 & 1);
-        uint32_t* f = reinterpret_cast<uint32_t*>(raw + (size_t)gs * B * 256);
-        const int ch = (j * 2 * B + 2 * b) * 4;  // (j, column 2b): 4 lanes x 2 halves
-        f[(ch + t0) * 2 + half] = h01;
-        f[(ch + t0 + 1) * 2 + half] = h23;
-        f[(ch + 4 + t0) * 2 + half] = l01;
-        f[(ch + 4 + t0 + 1) * 2 + half] = l23;
-      }
+      const uint32_t a = raw + unit_offset(gs, b, j, B);
 #pragma unroll
-      for (int o = 8; o; o >>= 1) part += __shfl_xor_sync(FULL, part, o);
-      if (q16 == 0 && ok[u]) Sx[gs * NARROW_B + b] = part;
+      for (int q = 0; q < 4; ++q) sts128(a + q * 16, make_uint4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]));
     }
+    part += __shfl_xor_sync(FULL, part, 1);
+    part += __shfl_xor_sync(FULL, part, 2);
+    if (j == 0 && u < n_units) Sx[gs * NARROW_B + b] = part;
   }
   // zero fragments that the stream reads for blocks past a slot's end (the
   // attention stage uses this memory too)
@@ -573,10 +572,8 @@ __device__ __noinline__ void gemv_prologue(const Params& P, const GemvCtx& E, ui
   if (want_ss) {
 #pragma unroll
     for (int b = 0; b < NARROW_B; ++b) {
-      if (b < B) {
-        const float r = warp_sum(ssq[b]);
-        if (lane == 0) M.red[warp][2 * b] = r;
-      }
+      const float r = warp_sum(ssq[b]);
+      if (lane == 0 && b < B) M.red[warp][2 * b] = r;
     }
   }
   __syncthreads();
@@ -586,6 +583,7 @@ __device__ __noinline__ void gemv_prologue(const Params& P, const GemvCtx& E, ui
       for (int w = 0; w < NW; ++w) ss += M.red[w][2 * tid];
     M.rnorm[tid] = nw ? 1.0f / sqrtf(ss / (float)K + P.eps) : 1.0f;
   }
+  if (tid == 0) trace_stamp(P, E.layer * NSTAGE + E.st, NW + 6);
   __syncthreads();
 }
 
