@@ -141,6 +141,8 @@ struct Entry {
   uint32_t lo, hi;           // work range: GEMV panel work indices, ATT 16-key tiles
   int32_t T, kc, gi, gk;     // GEMV: (tile, k-chunk, group) at lo and the chunk's groups
   int16_t p, cl, pk0, pk1;   // GEMV: panel, CTA index in the panel, the panel's k-chunks
+  uint32_t first;            // GEMV: panel-local index of the first warp holding tile T in this panel
+  uint32_t omask[2];         // GEMV: partial slots (bit p J + j) of the first two tiles this warp owns
 };
 struct Ctx {
   GemvCtx E;
@@ -158,6 +160,18 @@ __device__ __forceinline__ void att_range(const Params& P, int64_t& lo, int64_t&
   const int w = threadIdx.x >> 5;
   lo = clo + range_lo(chi - clo, NW, w);
   hi = clo + range_lo(chi - clo, NW, w + 1);
+}
+// Partial slots of split tile T (bit p J + j: the j-th warp holding blocks of
+// T in panel p), read by the tile's owner.
+__device__ __noinline__ uint32_t owned_slots(const MatGeom& m, int T) {  // bit f = p * J + j
+  uint32_t mask = 0;
+  for (int p = 0; p < m.NP; ++p) {
+    const uint32_t Gp = panel_groups(m, p);
+    const uint32_t v0 = work_owner(m, p, (uint32_t)T * Gp, NW), v1 = work_owner(m, p, (uint32_t)(T + 1) * Gp - 1, NW);
+    for (uint32_t v = v0; v <= v1; ++v)
+      if (!warp_empty(m, p, v, NW)) mask |= 1u << (p * m.J + (v - v0));
+  }
+  return mask;
 }
 // Compute this warp's entry for every stage kind (once per launch).
 __device__ __noinline__ void compute_entries(const Params& P) {
@@ -184,6 +198,8 @@ __device__ __noinline__ void compute_entries(const Params& P) {
       e.pk1 = m.pk[p + 1];
       e.T = e.kc = e.gi = 0;
       e.gk = 1;
+      e.first = 0;
+      e.omask[0] = e.omask[1] = 0u;
       if (lo < hi) {
         int T, kc, gi;
         work_coord(m, p, lo, T, kc, gi);
@@ -191,6 +207,19 @@ __device__ __noinline__ void compute_entries(const Params& P) {
         e.kc = kc;
         e.gi = gi;
         e.gk = chunk_groups(m, kc);
+        const uint32_t Gp = panel_groups(m, p);
+        e.first = work_owner(m, p, (uint32_t)T * Gp, NW);  // later tiles of the range start in it
+        if (p == 0) {  // owned: split tiles whose first panel-0 block is in the range
+          uint32_t mk[2] = {0u, 0u};
+          for (uint32_t t = (lo + Gp - 1) / Gp; t * Gp < hi && mk[1] == 0u; ++t)
+            if (m.NP > 1 || (t + 1) * Gp > hi) {
+              const uint32_t k = owned_slots(m, (int)t);
+              if (mk[0] == 0u) mk[0] = k;
+              else mk[1] = k;
+            }
+          e.omask[0] = mk[0];
+          e.omask[1] = mk[1];
+        }
       }
     }
     if ((threadIdx.x & 31) == 0) ctx().ent[warp][st] = e;
@@ -717,16 +746,6 @@ __device__ __noinline__ void gemv_publish(const Params& P, const GemvCtx& E, con
 // all partials and the epilogue's residual values in one round trip, sum the
 // partials in slot order with the owner's own in its slot's place
 // (deterministic), and run the epilogues.
-__device__ __forceinline__ uint32_t owned_slots(const MatGeom& m, int T) {  // bit f = p * J + j
-  uint32_t mask = 0;
-  for (int p = 0; p < m.NP; ++p) {
-    const uint32_t Gp = panel_groups(m, p);
-    const uint32_t v0 = work_owner(m, p, (uint32_t)T * Gp, NW), v1 = work_owner(m, p, (uint32_t)(T + 1) * Gp - 1, NW);
-    for (uint32_t v = v0; v <= v1; ++v)
-      if (!warp_empty(m, p, v, NW)) mask |= 1u << (p * m.J + (v - v0));
-  }
-  return mask;
-}
 template <int HD>
 __device__ __forceinline__ void owned_sum(const Params& P, const GemvCtx& E, int T, uint32_t mask, float o0,
                                           float o1, float& s0, float& s1) {
@@ -751,11 +770,11 @@ __device__ __forceinline__ void owned_sum(const Params& P, const GemvCtx& E, int
     }
 }
 template <int HD>
-__device__ __noinline__ void owner_fixup(const Params& P, const GemvCtx& E, int n, int T0, float a0,
-                                         float b0, int T1, float a1, float b1, Misc& M) {
-  const MatGeom& m = E.m;
+__device__ __noinline__ void owner_fixup(const Params& P, const GemvCtx& E, int n, int T0, uint32_t mk0,
+                                         float a0, float b0, int T1, uint32_t mk1, float a1, float b1,
+                                         Misc& M) {
   const int lane = threadIdx.x & 31, t = lane & 3, g = lane >> 2;
-  const uint32_t mk0 = owned_slots(m, T0), mk1 = n > 1 ? owned_slots(m, T1) : 1u;
+  if (n < 2) mk1 = 1u;
   const uint32_t e0 = __popc(mk0) - 1, e1 = __popc(mk1) - 1;
   if (lane == 0) {
     uint64_t t0 = 0;
@@ -804,7 +823,7 @@ __device__ __noinline__ void owner_fixup(const Params& P, const GemvCtx& E, int 
 // otherwise the partial goes to slot (T, panel, warp - first warp of the tile
 // in the panel) and the tile is queued for publication.
 template <int HD>
-__device__ __forceinline__ void tile_finish(const Params& P, const GemvCtx& E, Misc& M, int T,
+__device__ __forceinline__ void tile_finish(const Params& P, const GemvCtx& E, const Entry& en, Misc& M, int T,
                                             uint32_t nblk, float v0, float v1, uint32_t* pend,
                                             int& npend, int& nown, int& oT0, float& oa0, float& ob0,
                                             int& oT1, float& oa1, float& ob1) {
@@ -815,14 +834,14 @@ __device__ __forceinline__ void tile_finish(const Params& P, const GemvCtx& E, M
     return;
   }
   const uint32_t me = (uint32_t)E.cl * NW + (threadIdx.x >> 5);
-  const uint32_t first = work_owner(m, E.p, (uint32_t)T * panel_groups(m, E.p), NW);
+  const uint32_t first = T == en.T ? en.first : me;  // a later tile of the range starts in it
   if (P.cooperative && m.own_ok && E.p == 0 && me == first) {  // the tile's owner: finish it at the end
     if (nown == 0) {
       oT0 = T; oa0 = v0; ob0 = v1;
     } else if (nown == 1) {
       oT1 = T; oa1 = v0; ob1 = v1;
-    } else {
-      owner_fixup<HD>(P, E, 1, T, v0, v1, 0, 0.f, 0.f, M);  // more than two: finish this one now
+    } else {  // more than two (not planned for the owner path): finish this one now
+      owner_fixup<HD>(P, E, 1, T, owned_slots(m, T), v0, v1, 0, 0u, 0.f, 0.f, M);
       return;
     }
     ++nown;
@@ -1047,7 +1066,7 @@ __device__ __forceinline__ bool stage_gemv_body(const Params& P, int layer, int 
       acc0 = acc1 = 0.f;
       gi = 0;
       if (++kc == pk1) {  // end of the tile in this panel
-        tile_finish<HD>(P, E, M, T, nblk, tac0, tac1, pend, npend, nown, oT0, oa0, ob0, oT1, oa1, ob1);
+        tile_finish<HD>(P, E, en, M, T, nblk, tac0, tac1, pend, npend, nown, oT0, oa0, ob0, oT1, oa1, ob1);
         tac0 = tac1 = 0.f;
         nblk = 0;
         kc = pk0;
@@ -1057,10 +1076,10 @@ __device__ __forceinline__ bool stage_gemv_body(const Params& P, int layer, int 
     }
   }
   if (nblk != 0)
-    tile_finish<HD>(P, E, M, T, nblk, fmaf(acc0, esc, tac0), fmaf(acc1, esc, tac1), pend, npend, nown, oT0,
+    tile_finish<HD>(P, E, en, M, T, nblk, fmaf(acc0, esc, tac0), fmaf(acc1, esc, tac1), pend, npend, nown, oT0,
                     oa0, ob0, oT1, oa1, ob1);
   if (npend) gemv_publish<HD>(P, E, pend, npend, M);
-  if (nown > 0) owner_fixup<HD>(P, E, nown, oT0, oa0, ob0, oT1, oa1, ob1, M);
+  if (nown > 0) owner_fixup<HD>(P, E, nown, oT0, en.omask[0], oa0, ob0, oT1, en.omask[1], oa1, ob1, M);
   if (lane == 0) trace_stamp(P, layer * NSTAGE + st, 2 + warp);
   return true;
 }
@@ -1254,18 +1273,13 @@ __device__ __forceinline__ void wide_sum_slots(const Params& P, const GemvCtx& E
     }
   }
 }
-// Cooperative launch: the owner waits for the other contributors' releases.
+// Cooperative launch: the owner waits for the other contributors' releases,
+// then sums the partial slots in `mask` (its own included) in slot order.
 template <int HD>
-__device__ __noinline__ void wide_owner_fixup(const Params& P, const GemvCtx& E, int T, Misc& M) {
+__device__ __noinline__ void wide_owner_fixup(const Params& P, const GemvCtx& E, int T, uint32_t mask, Misc& M) {
   const MatGeom& m = E.m;
   const int lane = threadIdx.x & 31;
-  uint32_t expected = 0;
-  for (int p = 0; p < m.NP; ++p) {
-    const uint32_t Gp = panel_groups(m, p);
-    const uint32_t v0 = work_owner(m, p, (uint32_t)T * Gp, NW), v1 = work_owner(m, p, (uint32_t)(T + 1) * Gp - 1, NW);
-    for (uint32_t v = v0; v <= v1; ++v)
-      if ((p != 0 || v != v0) && !warp_empty(m, p, v, NW)) ++expected;
-  }
+  const uint32_t expected = __popc(mask) - 1;
   if (lane == 0) {
     uint64_t t0 = 0;
     for (uint32_t it = 1; ld_acquire_gpu(P.cnt + T) < expected; ++it) {
@@ -1281,7 +1295,15 @@ __device__ __noinline__ void wide_owner_fixup(const Params& P, const GemvCtx& E,
   }
   __syncwarp();
   float v[8];
-  wide_sum_slots<HD>(P, E, T, v);
+#pragma unroll
+  for (int k = 0; k < 8; ++k) v[k] = 0.f;
+  const float4* part = reinterpret_cast<const float4*>(P.gpart) + (int64_t)T * m.NP * m.J * 64 + lane * 2;
+  for (uint32_t r = mask; r; r &= r - 1) {
+    const float4* q = part + (int64_t)(__ffs(r) - 1) * 64;
+    const float4 a = __ldcg(q), c = __ldcg(q + 1);
+    v[0] += a.x; v[1] += a.y; v[2] += a.z; v[3] += a.w;
+    v[4] += c.x; v[5] += c.y; v[6] += c.z; v[7] += c.w;
+  }
   wide_epilogues<HD>(P, E, T, v, M);
   if (lane == 0) P.cnt[T] = 0;
 }
@@ -1310,7 +1332,8 @@ __device__ __noinline__ void wide_publish(const Params& P, const GemvCtx& E, con
   }
 }
 template <int HD>
-__device__ __forceinline__ void wide_tile_finish(const Params& P, const GemvCtx& E, Misc& M, int T, uint32_t nblk,
+__device__ __forceinline__ void wide_tile_finish(const Params& P, const GemvCtx& E, const Entry& en, Misc& M, int T,
+                                                 uint32_t nblk,
                                                  const float (&v)[8], uint32_t* pend, int& npend, int& nown,
                                                  int& oT0, int& oT1) {
   const MatGeom& m = E.m;
@@ -1320,7 +1343,7 @@ __device__ __forceinline__ void wide_tile_finish(const Params& P, const GemvCtx&
     return;
   }
   const uint32_t me = (uint32_t)E.cl * NW + (threadIdx.x >> 5);
-  const uint32_t first = work_owner(m, E.p, (uint32_t)T * panel_groups(m, E.p), NW);
+  const uint32_t first = T == en.T ? en.first : me;  // a later tile of the range starts in it
   const int64_t slot = ((int64_t)T * m.NP + E.p) * m.J + (me - first);
   float4* q = reinterpret_cast<float4*>(P.gpart) + slot * 64 + lane * 2;
   q[0] = make_float4(v[0], v[1], v[2], v[3]);
@@ -1329,9 +1352,9 @@ __device__ __forceinline__ void wide_tile_finish(const Params& P, const GemvCtx&
     if (E.p == 0 && me == first) {  // the owner: finish at the end (its own partial is in its slot)
       if (nown == 0) oT0 = T;
       else if (nown == 1) oT1 = T;
-      if (nown >= 2) {
+      if (nown >= 2) {  // more than two (not planned for the owner path): finish this one now
         __syncwarp();
-        wide_owner_fixup<HD>(P, E, T, M);
+        wide_owner_fixup<HD>(P, E, T, owned_slots(m, T), M);
         return;
       }
       ++nown;
@@ -1488,7 +1511,7 @@ __device__ __noinline__ bool stage_gemv_wide(const Params& P, int layer, int st,
         }
         gi = 0;
         if (++kc == pk1) {
-          wide_tile_finish<HD>(P, E, M, T, nblk, tac, pend, npend, nown, oT0, oT1);
+          wide_tile_finish<HD>(P, E, en, M, T, nblk, tac, pend, npend, nown, oT0, oT1);
 #pragma unroll
           for (int k = 0; k < 8; ++k) tac[k] = 0.f;
           nblk = 0;
@@ -1502,12 +1525,12 @@ __device__ __noinline__ bool stage_gemv_wide(const Params& P, int layer, int st,
       if (nblk != 0) {
 #pragma unroll
         for (int k = 0; k < 8; ++k) tac[k] = fmaf(acc[k], esc[k >> 2][k & 1], tac[k]);
-        wide_tile_finish<HD>(P, E, M, T, nblk, tac, pend, npend, nown, oT0, oT1);
+        wide_tile_finish<HD>(P, E, en, M, T, nblk, tac, pend, npend, nown, oT0, oT1);
       }
       if (npend) wide_publish<HD>(P, E, pend, npend, M);
       __syncwarp();
-      if (nown > 0) wide_owner_fixup<HD>(P, E, oT0, M);
-      if (nown > 1) wide_owner_fixup<HD>(P, E, oT1, M);
+      if (nown > 0) wide_owner_fixup<HD>(P, E, oT0, en.omask[0], M);
+      if (nown > 1) wide_owner_fixup<HD>(P, E, oT1, en.omask[1], M);
     }
   }
   if (lane == 0) trace_stamp(P, layer * NSTAGE + st, 2 + warp);
