@@ -144,8 +144,19 @@ struct Entry {
   uint32_t first;            // GEMV: panel-local index of the first warp holding tile T in this panel
   uint32_t omask[2];         // GEMV: partial slots (bit p J + j) of the first two tiles this warp owns
 };
+// This CTA's part of the attention stage, the same for every layer of a
+// launch: its range of (sequence, 16-key tile) work and, per sequence it
+// touches, the first CTA holding a tile of it and how many CTAs do.
+struct AttCta {
+  int32_t clo, chi;  // tiles [clo, chi) of the B * H_kv * nt work order
+  int32_t s0, ns;    // sequences s0 .. s0 + ns - 1 (ns <= 8, checked by the host)
+  int32_t cf[8];
+  int32_t span[8];  // CTAs cf .. cf + span - 1 (with fewer tiles than CTAs some hold none)
+  uint32_t n[8];    // the CTAs that hold a tile of it: arrivals before its merge
+};
 struct Ctx {
   GemvCtx E;
+  AttCta att;
   Ring ring[NW];
   Cursor cur[NW];
   Entry ent[NW][NSTAGE];
@@ -223,6 +234,23 @@ __device__ __noinline__ void compute_entries(const Params& P) {
       }
     }
     if ((threadIdx.x & 31) == 0) ctx().ent[warp][st] = e;
+  }
+  AttCta& A = ctx().att;
+  const int64_t Ta = (int64_t)P.B * P.Hkv * P.nt_att, C = gridDim.x, nt = P.nt_att;
+  const int64_t clo = range_lo(Ta, C, blockIdx.x), chi = range_lo(Ta, C, blockIdx.x + 1);
+  const int64_t s0 = clo / nt, ns = clo < chi ? (chi - 1) / nt - s0 + 1 : 0;
+  if (threadIdx.x == 0) {
+    A.clo = (int32_t)clo;
+    A.chi = (int32_t)chi;
+    A.s0 = (int32_t)s0;
+    A.ns = (int32_t)ns;
+  }
+  if (threadIdx.x < ns && threadIdx.x < 8) {
+    const int64_t sq = s0 + threadIdx.x;
+    const int64_t cf = owner_of(Ta, C, sq * nt), cl = owner_of(Ta, C, sq * nt + nt - 1);
+    A.cf[threadIdx.x] = (int32_t)cf;
+    A.span[threadIdx.x] = (int32_t)(cl - cf + 1);
+    A.n[threadIdx.x] = (uint32_t)(Ta >= C ? cl - cf + 1 : nt);
   }
 }
 template <int WT>
@@ -1582,12 +1610,10 @@ __device__ __forceinline__ void merge_head(const float* recs, int REC, int first
 // Phase 2: thread (h, d-quad) sums factor * o over the records, 8 loads in
 // flight.
 template <int HD>
-__device__ __noinline__ void merge_sequence(const Params& P, int64_t seq, int64_t Ta, int64_t C, float* fac,
-                                            Misc& M) {
+__device__ __noinline__ void merge_sequence(const Params& P, int64_t seq, int64_t Ta, int64_t C, int64_t cf,
+                                            int n, float* fac, Misc& M) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int GH = P.GH, REC = att_rec_floats(GH, HD), nt = P.nt_att;
-  const int64_t cf = owner_of(Ta, C, seq * nt), cl = owner_of(Ta, C, seq * nt + nt - 1);
-  const int n = (int)(cl - cf + 1);
+  const int GH = P.GH, REC = att_rec_floats(GH, HD);
   const float* base = P.apart + seq * P.J_att * REC;
   // with more tiles than CTAs every CTA of the sequence holds a record; with
   // fewer, a CTA whose tile range is empty holds none
@@ -1704,6 +1730,7 @@ __device__ __forceinline__ bool stage_att_body(const Params& P, int layer, Ring&
   const int GH = P.GH, REC = att_rec_floats(GH, HD), nt = P.nt_att;
   const int64_t Ta = (int64_t)P.B * P.Hkv * nt, C = gridDim.x;
   const LayerDev& Ld = sp().layers[layer];
+  const AttCta& A = ctx().att;
   float* recs = reinterpret_cast<float*>(smem + SM_SCR);
   const int64_t lo = ctx().ent[warp][ST_ATT].lo, hi = ctx().ent[warp][ST_ATT].hi;
   const float qscale = 1.4426950408889634f / sqrtf((float)HD);  // log2(e) / sqrt(hd)
@@ -1720,7 +1747,7 @@ __device__ __forceinline__ bool stage_att_body(const Params& P, int layer, Ring&
     if (seq != cur) {
       if (cur >= 0)  // a segment wholly inside this warp (or the warp's first)
         att_flush<HD>(P, nseg == 1 ? recs + (warp * 2) * REC
-                                   : P.apart + (cur * P.J_att + (blockIdx.x - owner_of(Ta, C, cur * nt))) * REC,
+                                   : P.apart + (cur * P.J_att + (blockIdx.x - A.cf[cur - A.s0])) * REC,
                       o, mrun, lrun);
       cur = seq;
       ++nseg;
@@ -1868,7 +1895,7 @@ __device__ __forceinline__ bool stage_att_body(const Params& P, int layer, Ring&
       }
     }
     for (int r = 0; r < nr; ++r)
-      M.run_out[r] = (M.run_seq[r] * P.J_att + (blockIdx.x - owner_of(Ta, C, M.run_seq[r] * nt))) * REC;
+      M.run_out[r] = (M.run_seq[r] * P.J_att + (blockIdx.x - A.cf[M.run_seq[r] - A.s0])) * REC;
     M.nruns = nr;
   }
   __syncthreads();
@@ -1877,13 +1904,11 @@ __device__ __forceinline__ bool stage_att_body(const Params& P, int layer, Ring&
       merge_head<HD>(recs, REC, M.run_first[r], M.run_vmask[r], P.apart + M.run_out[r], GH, h);
   // the last CTA to publish a sequence's record merges the sequence
   __syncthreads();
-  const int64_t clo = range_lo(Ta, C, blockIdx.x), chi = range_lo(Ta, C, blockIdx.x + 1);
-  if (clo < chi) {
-    const int64_t s0 = clo / nt, s1 = (chi - 1) / nt;
+  if (A.ns > 0) {
+    const int64_t s0 = A.s0, s1 = A.s0 + A.ns - 1;
     if (threadIdx.x <= s1 - s0) {  // one thread per sequence: the arrivals in flight together
       const int64_t sq = s0 + threadIdx.x;
-      const int64_t cf = owner_of(Ta, C, sq * nt), cl = owner_of(Ta, C, sq * nt + nt - 1);
-      const uint32_t n = (uint32_t)(Ta >= C ? cl - cf + 1 : nt);
+      const uint32_t n = A.n[threadIdx.x];
       const uint32_t old = atom_add_acq_rel(P.seqcnt + sq, 1u);
       M.mseq[threadIdx.x] = old == n - 1 ? sq : -1;
       if (old == n - 1) P.seqcnt[sq] = 0;
@@ -1891,7 +1916,8 @@ __device__ __forceinline__ bool stage_att_body(const Params& P, int layer, Ring&
     __syncthreads();
     float* fac = recs + NW * 2 * REC;  // per (head, record) factors of the merge
     for (int64_t sq = s0; sq <= s1; ++sq)
-      if (M.mseq[(int)(sq - s0)] == sq) merge_sequence<HD>(P, sq, Ta, C, fac, M);
+      if (M.mseq[(int)(sq - s0)] == sq)
+        merge_sequence<HD>(P, sq, Ta, C, A.cf[sq - s0], A.span[sq - s0], fac, M);
   }
   return true;
 }
