@@ -70,6 +70,10 @@ static_assert(sizeof(Params) <= 32000, "kernel parameters (with the K/V tensor m
 static_assert(SLOT_BYTES % 1024 == 512 || SLOT_BYTES % 1024 == 0, "K/V boxes need 512-byte aligned slots");
 __device__ __forceinline__ const SParams& sp() { return *reinterpret_cast<const SParams*>(g_smem + SM_SPAR); }
 
+// An empty partial slot word: two all-ones NaNs, a pattern that fp32
+// arithmetic does not produce (its NaN results are canonical).
+constexpr uint64_t PART_EMPTY = ~0ull;
+
 struct Misc {
   float rnorm[MAX_B];
   float escale[MAX_B];     // 2^e of the staged x of each sequence
@@ -739,6 +743,7 @@ __device__ __noinline__ void gemv_fixup(const Params& P, const GemvCtx& E, int T
       const float2 x = __ldcg(pp + (int64_t)(v - v0) * 32);
       s0 += x.x;
       s1 += x.y;
+      *reinterpret_cast<uint64_t*>(const_cast<float2*>(pp + (int64_t)(v - v0) * 32)) = PART_EMPTY;
     }
   }
   if ((threadIdx.x & 3) < P.B) gemv_epilogue<HD>(P, E, T, threadIdx.x & 3, s0, s1, M);
@@ -769,58 +774,22 @@ __device__ __noinline__ void gemv_publish(const Params& P, const GemvCtx& E, con
 }
 
 // Cooperative launch: a tile's owner (the warp holding its first blocks in
-// panel 0) finishes it.  For the warp's one or two owned tiles together: wait
-// (bounded) until every other contributor has released its partial, then load
-// all partials and the epilogue's residual values in one round trip, sum the
-// partials in slot order with the owner's own in its slot's place
-// (deterministic), and run the epilogues.
-template <int HD>
-__device__ __forceinline__ void owned_sum(const Params& P, const GemvCtx& E, int T, uint32_t mask, float o0,
-                                          float o1, float& s0, float& s1) {
-  const float2* part = reinterpret_cast<const float2*>(P.gpart) + (int64_t)T * E.m.NP * E.m.J * 32 +
-                       (threadIdx.x & 31);
-  float2 x[8];
-#pragma unroll
-  for (int f = 0; f < 8; ++f)
-    x[f] = (f > 0 && (mask >> f & 1u)) ? __ldcg(part + f * 32) : make_float2(0.f, 0.f);
-  s0 = o0;
-  s1 = o1;
-#pragma unroll
-  for (int f = 1; f < 8; ++f) {
-    s0 += x[f].x;
-    s1 += x[f].y;
-  }
-  for (int f = 8; f < 32; ++f)
-    if (mask >> f & 1u) {
-      const float2 y = __ldcg(part + f * 32);
-      s0 += y.x;
-      s1 += y.y;
-    }
-}
+// panel 0) finishes it.  Each other contributor stores its partial (one
+// 8-byte word per lane) into a slot that holds PART_EMPTY until then, so the
+// owner's polls of the slots return the partials themselves: for the warp's
+// one or two owned tiles together, every lane polls its word of each
+// contributor slot (bounded) until none is empty, sums the partials in slot
+// order with the owner's own in its slot's place (deterministic), empties the
+// slots for the next stage and runs the epilogues, whose residual inputs were
+// loaded before the wait.
 template <int HD>
 __device__ __noinline__ void owner_fixup(const Params& P, const GemvCtx& E, int n, int T0, uint32_t mk0,
                                          float a0, float b0, int T1, uint32_t mk1, float a1, float b1,
                                          Misc& M) {
+  const MatGeom& m = E.m;
   const int lane = threadIdx.x & 31, t = lane & 3, g = lane >> 2;
-  if (n < 2) mk1 = 1u;
-  const uint32_t e0 = __popc(mk0) - 1, e1 = __popc(mk1) - 1;
-  if (lane == 0) {
-    uint64_t t0 = 0;
-    for (uint32_t it = 1;; ++it) {
-      const uint32_t c0 = ld_acquire_gpu(P.cnt + T0), c1 = n > 1 ? ld_acquire_gpu(P.cnt + T1) : e1;
-      if (c0 >= e0 && c1 >= e1) break;
-      if ((it & 255u) != 0) continue;
-      const uint64_t now = globaltimer();
-      if (t0 == 0) t0 = now;
-      else if (now - t0 > WAIT_LIMIT_NS) {
-        atomicExch(P.ctrl + 1, STATUS_TIMEOUT);
-        M.abort = 1;
-        break;
-      }
-    }
-  }
-  __syncwarp();
-  // the residual inputs of the Wo / down epilogues, loaded with the partials
+  if (n < 2) mk1 = 1u;  // (the owner's own slot only)
+  // the residual inputs of the Wo / down epilogues
   const bool res = (E.st == ST_WO || E.st == ST_DOWN) && t < P.B && (E.st == ST_DOWN || E.xin32);
   const float* rb = E.st == ST_DOWN ? P.y : E.xin32;
   float r00 = 0.f, r01 = 0.f, r10 = 0.f, r11 = 0.f;
@@ -833,16 +802,85 @@ __device__ __noinline__ void owner_fixup(const Params& P, const GemvCtx& E, int 
       r11 = __ldcg(rb + o + 16 * T1 + g + 8);
     }
   }
-  float s0, s1, u0 = 0.f, u1 = 0.f;
-  owned_sum<HD>(P, E, T0, mk0, a0, b0, s0, s1);
-  if (n > 1) owned_sum<HD>(P, E, T1, mk1, a1, b1, u0, u1);
+  const int64_t tstride = (int64_t)m.NP * m.J * 32;
+  uint64_t* p0 = reinterpret_cast<uint64_t*>(P.gpart) + (int64_t)T0 * tstride + lane;
+  uint64_t* p1 = reinterpret_cast<uint64_t*>(P.gpart) + (int64_t)(n > 1 ? T1 : T0) * tstride + lane;
+  // slots 1..7 (the usual case) are polled together and kept in registers
+  uint64_t x0[8], x1[8];
+#pragma unroll
+  for (int f = 0; f < 8; ++f) x0[f] = x1[f] = PART_EMPTY;
+  uint32_t w0 = mk0 & 0xFEu, w1 = mk1 & 0xFEu;
+  uint64_t tw = 0;
+  for (uint32_t it = 1; w0 | w1; ++it) {
+#pragma unroll
+    for (int f = 1; f < 8; ++f) {
+      if (w0 >> f & 1u) x0[f] = ld_relaxed_gpu_u64(p0 + f * 32);
+      if (w1 >> f & 1u) x1[f] = ld_relaxed_gpu_u64(p1 + f * 32);
+    }
+#pragma unroll
+    for (int f = 1; f < 8; ++f) {
+      if (x0[f] != PART_EMPTY) w0 &= ~(1u << f);
+      if (x1[f] != PART_EMPTY) w1 &= ~(1u << f);
+    }
+    if (!(w0 | w1) || (it & 63u) != 0) continue;
+    const uint64_t now = globaltimer();
+    if (tw == 0) tw = now;
+    else if (now - tw > WAIT_LIMIT_NS) {
+      atomicExch(P.ctrl + 1, STATUS_TIMEOUT);
+      M.abort = 1;
+      break;
+    }
+  }
+  // slots 8.. (many panels): one at a time
+  for (int k = 0; k < 2; ++k) {
+    const uint64_t* pk = k ? p1 : p0;
+    for (uint32_t r = (k ? mk1 : mk0) & ~0xFFu; r && !M.abort; r &= r - 1) {
+      const int f = __ffs(r) - 1;
+      for (uint32_t it = 1; ld_relaxed_gpu_u64(pk + f * 32) == PART_EMPTY; ++it) {
+        if ((it & 63u) != 0) continue;
+        const uint64_t now = globaltimer();
+        if (tw == 0) tw = now;
+        else if (now - tw > WAIT_LIMIT_NS) {
+          atomicExch(P.ctrl + 1, STATUS_TIMEOUT);
+          M.abort = 1;
+          break;
+        }
+      }
+    }
+  }
+  // sums in slot order, then the slots are emptied for the next stage
+  float s0 = a0, s1 = b0, u0 = a1, u1 = b1;
+#pragma unroll
+  for (int f = 1; f < 8; ++f) {
+    if (mk0 >> f & 1u) {
+      s0 += __uint_as_float((uint32_t)x0[f]);
+      s1 += __uint_as_float((uint32_t)(x0[f] >> 32));
+      p0[f * 32] = PART_EMPTY;
+    }
+    if (n > 1 && (mk1 >> f & 1u)) {
+      u0 += __uint_as_float((uint32_t)x1[f]);
+      u1 += __uint_as_float((uint32_t)(x1[f] >> 32));
+      p1[f * 32] = PART_EMPTY;
+    }
+  }
+  for (uint32_t r = mk0 & ~0xFFu; r; r &= r - 1) {
+    const int f = __ffs(r) - 1;
+    const uint64_t y = ld_relaxed_gpu_u64(p0 + f * 32);
+    s0 += __uint_as_float((uint32_t)y);
+    s1 += __uint_as_float((uint32_t)(y >> 32));
+    p0[f * 32] = PART_EMPTY;
+  }
+  for (uint32_t r = n > 1 ? mk1 & ~0xFFu : 0u; r; r &= r - 1) {
+    const int f = __ffs(r) - 1;
+    const uint64_t y = ld_relaxed_gpu_u64(p1 + f * 32);
+    u0 += __uint_as_float((uint32_t)y);
+    u1 += __uint_as_float((uint32_t)(y >> 32));
+    p1[f * 32] = PART_EMPTY;
+  }
+  __syncwarp();
   if (t < P.B) {
     gemv_epilogue<HD>(P, E, T0, t, s0, s1, M, res, r00, r01);
     if (n > 1) gemv_epilogue<HD>(P, E, T1, t, u0, u1, M, res, r10, r11);
-  }
-  if (lane == 0) {
-    P.cnt[T0] = 0;
-    if (n > 1) P.cnt[T1] = 0;
   }
 }
 
@@ -876,12 +914,12 @@ __device__ __forceinline__ void tile_finish(const Params& P, const GemvCtx& E, c
     return;
   }
   const int64_t slot = ((int64_t)T * m.NP + E.p) * m.J + (me - first);
-  reinterpret_cast<float2*>(P.gpart)[slot * 32 + lane] = make_float2(v0, v1);
-  if (P.cooperative && m.own_ok) {  // release the partial to the tile's owner
-    __syncwarp();
-    if (lane == 0) red_release_gpu_add(P.cnt + T, 1u);
+  if (P.cooperative && m.own_ok) {  // the tile's owner polls the slot for it
+    st_relaxed_gpu_u64(reinterpret_cast<uint64_t*>(P.gpart) + slot * 32 + lane,
+                       (uint64_t)__float_as_uint(v1) << 32 | __float_as_uint(v0));
     return;
   }
+  reinterpret_cast<float2*>(P.gpart)[slot * 32 + lane] = make_float2(v0, v1);
   if (lane == 0) pend[npend] = (uint32_t)T | (nblk << 20);
   if (++npend == 32) {
     gemv_publish<HD>(P, E, pend, npend, M);
@@ -2244,6 +2282,10 @@ static int decode(const ddl_shape* s, ddl_wtype wtype, const ddl_layer_w* layers
   cudaStream_t cs = (cudaStream_t)stream;
   cudaError_t e = cudaMemsetAsync(ws, 0, (size_t)w.gpart, cs);  // barrier, status, counters
   if (e != cudaSuccess) return cuda_status(e);
+  // empty partial slots (each reader empties the slots it consumed, so they
+  // stay empty from stage to stage within a launch)
+  if ((e = cudaMemsetAsync(ws + w.gpart, 0xFF, (size_t)(w.apart - w.gpart), cs)) != cudaSuccess)
+    return cuda_status(e);
   const bool coop = di.coop && g_launch_mode == 0;
   const bool wide = B > NARROW_B;  // INT4 only (checked above)
   void* fn = HD == 128 ? (wtype == DDL_W_INT4 ? (wide ? (void*)decode_kernel<128, DDL_W_INT4, true>
@@ -2272,6 +2314,8 @@ static int decode(const ddl_shape* s, ddl_wtype wtype, const ddl_layer_w* layers
     P.trace = (g_trace && g_trace_bytes >= need_trace && L <= MAX_LAYERS) ? g_trace : nullptr;
     if (l0 > 0 && (e = cudaMemsetAsync(ws + w.xmax, 0, (size_t)(w.gpart - w.xmax), cs)) != cudaSuccess)
       return cuda_status(e);  // maxima are per launch (its first layer finds its own)
+    if (l0 > 0 && (e = cudaMemsetAsync(ws + w.gpart, 0xFF, (size_t)(w.apart - w.gpart), cs)) != cudaSuccess)
+      return cuda_status(e);
     if (coop) {
       if (l0 > 0 && (e = cudaMemsetAsync(ws + w.ctrl, 0, 4, cs)) != cudaSuccess) return cuda_status(e);
       P.stage_begin = 0;
