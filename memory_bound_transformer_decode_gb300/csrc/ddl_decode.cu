@@ -499,53 +499,51 @@ __device__ __noinline__ void gemv_prologue(const Params& P, const GemvCtx& E, ui
   cp_async_wait_all();
   __syncthreads();
   if (tid == 0) trace_stamp(P, E.layer * NSTAGE + E.st, NW + 5);
-  // the 16 values of unit u (fp32 x, norm weights) from shared memory
-  auto unit_load = [&](int u, float (&x)[16], float (&w)[16], int& gs, int& b, int& j) {
-    const int gsb = u >> 2;
+  // Half unit h = 2 u + p of unit u: quads p and p + 2 (values 4p..4p+3 and
+  // 4p+8..4p+11), read from bytes 16p and 32 + 16p of the unit; their high
+  // parts fill bytes 16p.. and their low parts bytes 32 + 16p.., the same
+  // bytes, so the two halves of a unit are converted independently.
+  auto half_load = [&](int h, float (&x)[8], float (&w)[8], int& gs, int& b, int& j, uint32_t& a) {
+    const int u = h >> 1, p = h & 1, gsb = u >> 2;
     j = u & 3;
     gs = (int)(((uint32_t)gsb * invB) >> 16);
     b = gsb - gs * B;
-    const uint32_t a = raw + unit_offset(gs, b, j, B);
+    a = raw + unit_offset(gs, b, j, B) + 16 * p;
 #pragma unroll
-    for (int r = 0; r < 4; ++r) {
+    for (int q = 0; q < 2; ++q) {
       float4 v;
       if (x32) {
-        const uint4 q = lds128(a + r * 16);
-        v = make_float4(__uint_as_float(q.x), __uint_as_float(q.y), __uint_as_float(q.z), __uint_as_float(q.w));
+        const uint4 r = lds128(a + 32 * q);
+        v = make_float4(__uint_as_float(r.x), __uint_as_float(r.y), __uint_as_float(r.z), __uint_as_float(r.w));
       } else {
-        v = bf16x4_f32(lds64(a + r * 16));
+        v = bf16x4_f32(lds64(a + 32 * q));
       }
-      x[4 * r] = v.x;
-      x[4 * r + 1] = v.y;
-      x[4 * r + 2] = v.z;
-      x[4 * r + 3] = v.w;
-    }
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const uint4 q = nw ? lds128(nws + gs * 128 + j * 32 + h * 16) : make_uint4(0x3f803f80u, 0x3f803f80u, 0x3f803f80u, 0x3f803f80u);
-      w[8 * h] = bf16lo_f32(q.x);
-      w[8 * h + 1] = bf16hi_f32(q.x);
-      w[8 * h + 2] = bf16lo_f32(q.y);
-      w[8 * h + 3] = bf16hi_f32(q.y);
-      w[8 * h + 4] = bf16lo_f32(q.z);
-      w[8 * h + 5] = bf16hi_f32(q.z);
-      w[8 * h + 6] = bf16lo_f32(q.w);
-      w[8 * h + 7] = bf16hi_f32(q.w);
+      x[4 * q] = v.x;
+      x[4 * q + 1] = v.y;
+      x[4 * q + 2] = v.z;
+      x[4 * q + 3] = v.w;
+      const uint2 wq = nw ? lds64(nws + gs * 128 + j * 32 + p * 8 + q * 16) : make_uint2(0x3f803f80u, 0x3f803f80u);
+      w[4 * q] = bf16lo_f32(wq.x);
+      w[4 * q + 1] = bf16hi_f32(wq.x);
+      w[4 * q + 2] = bf16lo_f32(wq.y);
+      w[4 * q + 3] = bf16hi_f32(wq.y);
     }
   };
+  const int n_half = 2 * n_units;
   // 3. the scale: the producer's max, or (first layer of a launch) the panel's
   if (!have_max) {
 #pragma unroll 1
-    for (int u = tid; u < n_units; u += NTHREADS) {
-      float x[16], w[16];
+    for (int h = tid; h < n_half; h += NTHREADS) {
+      float x[8], w[8];
       int gs, b, j;
-      unit_load(u, x, w, gs, b, j);
-      float a = 0.f;
+      uint32_t a;
+      half_load(h, x, w, gs, b, j, a);
+      float m = 0.f;
 #pragma unroll
-      for (int e = 0; e < 16; ++e) a = fmaxf(a, fabsf(x[e] * w[e]));
+      for (int e = 0; e < 8; ++e) m = fmaxf(m, fabsf(x[e] * w[e]));
 #pragma unroll
       for (int bb = 0; bb < NARROW_B; ++bb)
-        if (bb == b) xm[bb] = fmaxf(xm[bb], a);
+        if (bb == b) xm[bb] = fmaxf(xm[bb], m);
     }
 #pragma unroll
     for (int b = 0; b < NARROW_B; ++b) {
@@ -567,64 +565,62 @@ __device__ __noinline__ void gemv_prologue(const Params& P, const GemvCtx& E, ui
     sdn[b] = ldexpf(1.0f, -e);
     if (tid == b && b < B) M.escale[b] = ldexpf(1.0f, e);
   }
-  // 4. fragments, one unit per thread and trip; Sx = sum of hi + lo over the
-  //    group's four units (four consecutive lanes)
+  // 4. fragments, one half unit per thread and trip; Sx = sum of hi + lo
+  //    over the group's eight half units (eight consecutive lanes)
   float* Sx = reinterpret_cast<float*>(smem + SM_SCR + XF_BYTES);
   constexpr bool f16 = WT == DDL_W_INT4;
   const bool want_ss = nw && whole;
   float ssq[NARROW_B] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll 1
-  for (int u0 = 0; u0 < n_units; u0 += NTHREADS) {
-    const int u = u0 + tid;
+  for (int h0 = 0; h0 < n_half; h0 += NTHREADS) {
+    const int h = h0 + tid;
     float part = 0.f;
     int gs = 0, b = 0, j = 0;
-    if (u < n_units) {
-      float x[16], w[16];
-      unit_load(u, x, w, gs, b, j);
+    if (h < n_half) {
+      float x[8], w[8];
+      uint32_t a;
+      half_load(h, x, w, gs, b, j, a);
       if (want_ss) {
         float s2 = 0.f;
 #pragma unroll
-        for (int e = 0; e < 16; ++e) s2 = fmaf(x[e], x[e], s2);
+        for (int e = 0; e < 8; ++e) s2 = fmaf(x[e], x[e], s2);
 #pragma unroll
         for (int bb = 0; bb < NARROW_B; ++bb)
           if (bb == b) ssq[bb] += s2;
       }
       const float sc = b == 0 ? sdn[0] : b == 1 ? sdn[1] : b == 2 ? sdn[2] : sdn[3];
-      uint32_t o[16];
+      uint32_t hw[4], lw[4];  // word 2k + q: pair k of quad p + 2q
 #pragma unroll
-      for (int r = 0; r < 4; ++r)
+      for (int q = 0; q < 2; ++q)
 #pragma unroll
         for (int k = 0; k < 2; ++k) {
-          const int e = 4 * r + 2 * k;
+          const int e = 4 * q + 2 * k;
           const float2 pv = make_float2(x[e] * w[e] * sc, x[e + 1] * w[e + 1] * sc);
           float2 hf, lf;
-          uint32_t hw, lw;
           if (f16) {
-            const __half2 h = __float22half2_rn(pv);
-            hf = __half22float2(h);
-            const __half2 l = __float22half2_rn(make_float2(pv.x - hf.x, pv.y - hf.y));
-            lf = __half22float2(l);
-            hw = *reinterpret_cast<const uint32_t*>(&h);
-            lw = *reinterpret_cast<const uint32_t*>(&l);
+            const __half2 hh = __float22half2_rn(pv);
+            hf = __half22float2(hh);
+            const __half2 ll = __float22half2_rn(make_float2(pv.x - hf.x, pv.y - hf.y));
+            lf = __half22float2(ll);
+            hw[2 * k + q] = *reinterpret_cast<const uint32_t*>(&hh);
+            lw[2 * k + q] = *reinterpret_cast<const uint32_t*>(&ll);
           } else {
-            const __nv_bfloat162 h = __float22bfloat162_rn(pv);
-            hf = __bfloat1622float2(h);
-            const __nv_bfloat162 l = __float22bfloat162_rn(make_float2(pv.x - hf.x, pv.y - hf.y));
-            lf = __bfloat1622float2(l);
-            hw = *reinterpret_cast<const uint32_t*>(&h);
-            lw = *reinterpret_cast<const uint32_t*>(&l);
+            const __nv_bfloat162 hh = __float22bfloat162_rn(pv);
+            hf = __bfloat1622float2(hh);
+            const __nv_bfloat162 ll = __float22bfloat162_rn(make_float2(pv.x - hf.x, pv.y - hf.y));
+            lf = __bfloat1622float2(ll);
+            hw[2 * k + q] = *reinterpret_cast<const uint32_t*>(&hh);
+            lw[2 * k + q] = *reinterpret_cast<const uint32_t*>(&ll);
           }
           part += (hf.x + lf.x) + (hf.y + lf.y);
-          o[4 * (r & 1) + 2 * k + (r >> 1)] = hw;
-          o[8 + 4 * (r & 1) + 2 * k + (r >> 1)] = lw;
         }
-      const uint32_t a = raw + unit_offset(gs, b, j, B);
-#pragma unroll
-      for (int q = 0; q < 4; ++q) sts128(a + q * 16, make_uint4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]));
+      sts128(a, make_uint4(hw[0], hw[1], hw[2], hw[3]));
+      sts128(a + 32, make_uint4(lw[0], lw[1], lw[2], lw[3]));
     }
     part += __shfl_xor_sync(FULL, part, 1);
     part += __shfl_xor_sync(FULL, part, 2);
-    if (j == 0 && u < n_units) Sx[gs * NARROW_B + b] = part;
+    part += __shfl_xor_sync(FULL, part, 4);
+    if ((h & 7) == 0 && h < n_half) Sx[gs * NARROW_B + b] = part;
   }
   // zero fragments that the stream reads for blocks past a slot's end (the
   // attention stage uses this memory too)
@@ -1052,13 +1048,14 @@ __device__ __forceinline__ bool stage_gemv_body(const Params& P, int layer, int 
     const int kcl = kc - pk0;
     const uint32_t xb = xf_lane + kcl * kstride + gi * gstride;
     const uint32_t sb = sx_lane + ((kcl * GC + gi) * NARROW_B) * 4;
-    // The slot's blocks in two halves (a rolled loop: the stream loop's code
-    // has to stay in the instruction cache).  Per half, all shared loads
-    // first, then the MMAs in (j, block) order so that consecutive MMAs
-    // accumulate into different blocks.  Blocks i >= nb get zero x fragments
+    // The slot's blocks (PER independent MMA chains for latency hiding: with
+    // one CTA of 8 warps per SM each warp's slot time is its dependency
+    // chains, not issue bandwidth): all shared loads first, then the MMAs in
+    // (j, block) order so that consecutive MMAs accumulate into different
+    // blocks.  Blocks i >= nb get zero x fragments
     // (and zero scale and sum of x), so they add nothing whatever stale codes
     // the slot holds.
-    constexpr int HB = PER / 2;
+    constexpr int HB = PER;
 #pragma unroll 1
     for (int h0 = 0; h0 < PER; h0 += HB) {
       float c[HB][4];
