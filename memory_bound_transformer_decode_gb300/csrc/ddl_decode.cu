@@ -67,7 +67,9 @@ static_assert(NW * 2 * (MAX_GH * (128 + 2) + 3) * 4 <= SM_SCR_BYTES, "attention 
 static_assert(SM_TOTAL <= 227 * 1024, "shared memory budget");
 static_assert(SM_SPAR % 16 == 0, "parameter copy alignment");
 static_assert(sizeof(Params) <= 32000, "kernel parameters (with the K/V tensor maps) exceed the launch limit");
-static_assert(SLOT_BYTES % 1024 == 512 || SLOT_BYTES % 1024 == 0, "K/V boxes need 512-byte aligned slots");
+static_assert((SLOT_BYTES % 1024 == 512 && SLOT_BYTES >= 512 + 16 * 128 * 2) ||
+                  (SLOT_BYTES % 1024 == 0 && SLOT_BYTES >= 16 * 128 * 2),
+              "K/V boxes need 1024-byte boundaries inside 512-byte aligned slots");
 __device__ __forceinline__ const SParams& sp() { return *reinterpret_cast<const SParams*>(g_smem + SM_SPAR); }
 
 // An empty partial slot word: two all-ones NaNs, a pattern that fp32
@@ -337,11 +339,15 @@ __device__ __forceinline__ bool cursor_next(const Params& P, Cursor& c, int64_t 
   return true;
 }
 
-// Shared address of 16-byte chunk `ch` (head dims 8ch..8ch+7) of row r of a
-// K/V slot: quarter ch/4 of the row sits in its own 1 KB box of 16 rows x 64
-// bytes, chunk ch%4 XOR-ed with bits 1-2 of the row (the 64-byte swizzle).
+// A K/V slot holds 16 rows of hd bf16 as hd/64 boxes of 16 rows x 128 bytes
+// with the 128-byte swizzle, which wants each box at a 1024-byte boundary:
+// ring slots are 512-byte aligned, and one that starts 512 bytes past a
+// boundary puts its boxes 512 bytes in (4608-byte slots: they end at its end).
+__device__ __forceinline__ uint32_t kv_base(uint32_t slot) { return (slot + 1023u) & ~1023u; }
+// Shared address of 16-byte chunk `ch` (head dims 8ch..8ch+7) of row r: half
+// ch/8 of the row in its own 2 KB box, chunk ch%8 XOR-ed with row%8.
 __device__ __forceinline__ uint32_t kv_addr(uint32_t slot, int r, int ch) {
-  return slot + (ch >> 2) * 1024 + r * 64 + (((ch & 3) ^ ((r >> 1) & 3)) << 4);
+  return kv_base(slot) + (ch >> 3) * 2048 + r * 128 + (((ch & 7) ^ (r & 7)) << 4);
 }
 template <int HD, int WT>
 __device__ __forceinline__ void issue_slot(const Params& P, const Cursor& c, const SlotDesc& d,
@@ -355,10 +361,10 @@ __device__ __forceinline__ void issue_slot(const Params& P, const Cursor& c, con
       bulk_g2s_evict_first(slot, c.wbase + (uint64_t)d.a * BB, wb, bar, policy);
       if (q4) bulk_g2s_evict_first(slot + BLKS_PER_SLOT * BLK_BYTES, c.sbase + (uint64_t)d.a * SCL_BYTES, sb, bar, policy);
     }
-  } else {  // 16 rows of K or V: HD/32 boxes of 16 rows x 64 bytes, swizzled (kv_addr)
+  } else {  // 16 rows of K or V: HD/64 boxes of 16 rows x 128 bytes, swizzled (kv_addr)
     if (lane == 0) mbar_arrive_expect_tx(bar, 16 * HD * 2);
-    if (lane < HD / 32)
-      tensor2d_g2s(slot + lane * 1024, d.kind == SK_K ? c.kmap : c.vmap, lane * 32, (int)d.a, bar, policy);
+    if (lane < HD / 64)
+      tensor2d_g2s(kv_base(slot) + lane * 2048, d.kind == SK_K ? c.kmap : c.vmap, lane * 64, (int)d.a, bar, policy);
   }
 }
 
@@ -2198,17 +2204,17 @@ static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   });
   return fn;
 }
-// The [rows][hd] bf16 view of a K or V cache for 16-row x 32-column boxes
-// with the 64-byte swizzle (rows = B * H_kv * s_max).
+// The [rows][hd] bf16 view of a K or V cache for 16-row x 64-column boxes
+// with the 128-byte swizzle (rows = B * H_kv * s_max).
 static int encode_kv_map(CUtensorMap* m, const uint16_t* base, int64_t rows, int hd) {
   PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
   if (!enc) return DDL_ERR_CUDA;
   const cuuint64_t dims[2] = {(cuuint64_t)hd, (cuuint64_t)rows};
   const cuuint64_t strides[1] = {(cuuint64_t)hd * 2};
-  const cuuint32_t box[2] = {32, 16};
+  const cuuint32_t box[2] = {64, 16};  // 16 rows x 128 bytes: one half of an hd-128 row (all of hd 64)
   const cuuint32_t es[2] = {1, 1};
   const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(base), dims, strides,
-                         box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                         box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                          CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? DDL_OK : DDL_ERR_CUDA;
 }

@@ -211,7 +211,7 @@ struct Params {
   uint64_t* trace;      // optional: per stage, CTA: start, prologue end, NW warp ends, end, 4 prologue steps (ns)
   LayerDev layers[MAX_LAYERS];
   // 2-D views [B * H_kv * s_max rows][hd] of each layer's K and V caches for
-  // TMA tensor copies of 16 rows x 32 columns with the 64-byte swizzle
+  // TMA tensor copies of 16 rows x 64 columns with the 128-byte swizzle
   CUtensorMap kmap[MAX_LAYERS];
   CUtensorMap vmap[MAX_LAYERS];
 };
