@@ -108,8 +108,8 @@ struct Cursor {
   uint32_t pos, end;      // work index and end: GEMV panel blocks, ATT 2 x tiles (K, V)
   uint32_t a;             // GEMV: stream block index of pos; ATT: cache-view row of the tile
   int aseq, ai;           // ATT: sequence and tile index of the tile
-  const uint8_t* wbase;   // GEMV: code (or bf16) stream of the matrix
-  const uint8_t* sbase;   // GEMV: scale stream (INT4)
+  const uint8_t* wbase;   // GEMV: block stream of the matrix (INT4: codes and scales)
+  const uint8_t* sbase;   // GEMV: scales of the stream's first block (INT4)
   const uint16_t* kbase;  // ATT: K cache of the layer
   const uint16_t* vbase;  // ATT: V cache of the layer
   const void* kmap;       // ATT: tensor maps of the layer's caches
@@ -355,11 +355,10 @@ __device__ __forceinline__ void issue_slot(const Params& P, const Cursor& c, con
   if (d.kind == SK_GEMV) {
     if (lane == 0) {
       constexpr bool q4 = WT == DDL_W_INT4;
-      constexpr uint32_t BB = q4 ? BLK_BYTES : BF16_BLK_BYTES;
-      const uint32_t wb = d.cnt * BB, sb = q4 ? d.cnt * SCL_BYTES : 0;
-      mbar_arrive_expect_tx(bar, wb + sb);
+      constexpr uint32_t BB = q4 ? QBLK_BYTES : BF16_BLK_BYTES;  // INT4: codes and scales together
+      const uint32_t wb = d.cnt * BB;
+      mbar_arrive_expect_tx(bar, wb);
       bulk_g2s_evict_first(slot, c.wbase + (uint64_t)d.a * BB, wb, bar, policy);
-      if (q4) bulk_g2s_evict_first(slot + BLKS_PER_SLOT * BLK_BYTES, c.sbase + (uint64_t)d.a * SCL_BYTES, sb, bar, policy);
     }
   } else {  // 16 rows of K or V: HD/64 boxes of 16 rows x 128 bytes, swizzled (kv_addr)
     if (lane == 0) mbar_arrive_expect_tx(bar, 16 * HD * 2);
@@ -1081,8 +1080,8 @@ __device__ __forceinline__ bool stage_gemv_body(const Params& P, int layer, int 
 #pragma unroll
         for (int ii = 0; ii < HB; ++ii) {
           const int i = h0 + ii;
-          wv[ii] = lds128(slot + i * BLK_BYTES + lane * 16);
-          const uint32_t scw = lds32(slot + BLKS_PER_SLOT * BLK_BYTES + i * SCL_BYTES + g * 4);
+          wv[ii] = lds128(slot + i * QBLK_BYTES + lane * 16);
+          const uint32_t scw = lds32(slot + i * QBLK_BYTES + BLK_BYTES + g * 4);
           const float sxv = lds_f32(sb + i * (NARROW_B * 4));
           sc[ii] = i < nb ? scw : 0u;  // stale scale and sum words are finite-safe only as 0
           sx[ii] = i < nb ? sxv : 0.f;
@@ -1514,8 +1513,8 @@ __device__ __noinline__ bool stage_gemv_wide(const Params& P, int layer, int st,
 #pragma unroll
           for (int ii = 0; ii < HB; ++ii) {
             const int i = h0 + ii;
-            wv[ii] = lds128(slot + i * BLK_BYTES + lane * 16);
-            const uint32_t scw = lds32(slot + BLKS_PER_SLOT * BLK_BYTES + i * SCL_BYTES + g * 4);
+            wv[ii] = lds128(slot + i * QBLK_BYTES + lane * 16);
+            const uint32_t scw = lds32(slot + i * QBLK_BYTES + BLK_BYTES + g * 4);
             sc[ii] = i < nb ? scw : 0u;
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt)

@@ -49,10 +49,9 @@ inline int64_t make_geoms(const ddl_shape& s, int wtype, MatGeom mg[4]) {
     m.Gc = m.G < GC ? m.G : GC;
     m.Sk = (m.G + m.Gc - 1) / m.Gc;
     m.T = (int64_t)m.NT * m.G;
-    m.woff = off;
-    off = align256(off + m.T * (wtype == DDL_W_INT4 ? BLK_BYTES : BF16_BLK_BYTES));
-    m.soff = off;
-    if (wtype == DDL_W_INT4) off = align256(off + m.T * SCL_BYTES);
+    m.woff = off;  // INT4: one stream of blocks, each its codes then its scales (one copy per slot)
+    off = align256(off + m.T * (wtype == DDL_W_INT4 ? QBLK_BYTES : BF16_BLK_BYTES));
+    m.soff = wtype == DDL_W_INT4 ? m.woff + BLK_BYTES : off;
   }
   return off;
 }

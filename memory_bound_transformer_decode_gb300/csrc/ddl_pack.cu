@@ -88,7 +88,7 @@ __global__ void pack_int4_kernel(MatGeom m, int kind, int hd, SrcRows src,
       wd |= nib(src, mh, rh, m.K, k0 + 1) << 20;
       wd |= nib(src, mg_, rg, m.K, k0 + 9) << 24;
       wd |= nib(src, mh, rh, m.K, k0 + 9) << 28;
-      wout[b * 128 + lane * 4 + j] = wd;
+      wout[b * (QBLK_BYTES / 4) + lane * 4 + j] = wd;
     } else {
       const int64_t si = i - nw, b = si / 8;
       const int g = (int)(si % 8);
@@ -98,7 +98,7 @@ __global__ void pack_int4_kernel(MatGeom m, int kind, int hd, SrcRows src,
       int rg, rh;
       const int mg_ = src_of(src, kind, T, g, hd, rg), mh = src_of(src, kind, T, g + 8, hd, rh);
       const uint32_t lo = src.s[mg_][(int64_t)rg * m.G + grp], hi = src.s[mh][(int64_t)rh * m.G + grp];
-      sout[b * 8 + g] = lo | (hi << 16);
+      sout[b * (QBLK_BYTES / 4) + g] = lo | (hi << 16);
     }
   }
 }

@@ -42,9 +42,10 @@ namespace ddl {
 constexpr int NW = 8;                 // warps per CTA (each streams its own ring)
 constexpr int NTHREADS = NW * 32;
 constexpr int DEPTH = 3;              // ring slots per warp
-constexpr int SLOT_BYTES = 4608;      // 8 INT4 blocks + their scales, or 16 KV rows (512-byte aligned)
+constexpr int SLOT_BYTES = 4608;      // 8 INT4 blocks with their scales, or 16 KV rows (512-byte aligned)
 constexpr int BLK_BYTES = 512;        // one INT4 block: 16 rows x 64 columns
 constexpr int SCL_BYTES = 32;         // scales of one block
+constexpr int QBLK_BYTES = BLK_BYTES + SCL_BYTES;  // an INT4 block's codes followed by its scales
 constexpr int BLKS_PER_SLOT = 8;
 constexpr int BF16_BLK_BYTES = 2048;  // one bf16 block: 16 rows x 64 columns
 constexpr int BF16_BLKS_PER_SLOT = 2;
@@ -77,7 +78,8 @@ struct MatGeom {
   int32_t NP;         // panels: k-chunks pk[p]..pk[p+1]-1, worked by CTAs pc[p]..pc[p+1]-1
   int32_t own_ok;     // split tiles may be finished by their owners: no warp owns more than two
   int64_t T;          // blocks
-  int64_t woff, soff; // byte offsets of the code and scale streams in a packed layer
+  int64_t woff, soff; // packed layer: INT4 block b's codes at woff + b * QBLK_BYTES, its scales at
+                      // soff + b * QBLK_BYTES (soff = woff + BLK_BYTES); bf16 block b at woff + b * 2048
   int16_t pk[MAXP + 1];
   int16_t pc[MAXP + 1];
 };

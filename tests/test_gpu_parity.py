@@ -72,10 +72,7 @@ def _geoms(cfg, wtype):
         G = K // 64
         Gc = min(G, 32)
         g = dict(N=N, K=K, NT=N // 16, G=G, Gc=Gc, Sk=-(-G // Gc), T=(N // 16) * G, woff=off)
-        off = al(off + g["T"] * (512 if wtype == ddl.INT4 else 2048))
-        g["soff"] = off
-        if wtype == ddl.INT4:
-            off = al(off + g["T"] * 32)
+        off = al(off + g["T"] * (544 if wtype == ddl.INT4 else 2048))  # INT4: 512 B codes + 32 B scales
         out.append(g)
     return out, off
 
@@ -119,8 +116,9 @@ def test_pack_layer_is_the_documented_permutation(cfg):
     gg, tt = lanes // 4, lanes % 4
     for kind, g in enumerate(geoms):
         kc, T, gi = _block_coords(g)
-        words = blob[g["woff"]: g["woff"] + g["T"] * 512].view(np.uint32).reshape(-1, 32, 4)
-        sw = blob[g["soff"]: g["soff"] + g["T"] * 32].view(np.uint32).reshape(-1, 8)
+        blocks = blob[g["woff"]: g["woff"] + g["T"] * 544].view(np.uint32).reshape(-1, 136)
+        words = blocks[:, :128].reshape(-1, 32, 4)
+        sw = blocks[:, 128:]
         for b in range(0, g["T"], max(1, g["T"] // 97)):  # a spread sample of blocks
             rows = _tile_rows(kind, T[b], cfg.head_dim)
             if kind == 2:
