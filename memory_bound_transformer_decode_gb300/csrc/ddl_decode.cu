@@ -1644,20 +1644,31 @@ __device__ __forceinline__ void merge_head(const float* recs, int REC, int first
 }
 
 // Final merge of all CTA records of one sequence into attn, by the last CTA
-// to finish it.  Phase 1: warp h < GH folds every record's (m, l) of head h
-// into per-record factors exp2(m_j - M) / L (one load round trip for up to 64
-// records).
-// Phase 2: thread (h, d-quad) sums factor * o over the records, 8 loads in
-// flight.
+// to finish it; it is on the stage's critical path, so its loads go out in
+// one round trip.  Thread (h, d-quad) first copies (cp.async) its o column of
+// the first 2 NW records into the CTA's record area of shared memory, free by
+// now; meanwhile (phase 1) warp h < GH folds every record's (m, l) of head h
+// into per-record factors exp2(m_j - M) / L (one round trip for up to 64
+// records).  Phase 2: the thread sums factor * o over the records (any past
+// 2 NW from global memory in rounds of 8).  A record whose factor is 0 (a
+// CTA without tiles holds none) is skipped, whatever its memory holds.
 template <int HD>
 __device__ __noinline__ void merge_sequence(const Params& P, int64_t seq, int64_t Ta, int64_t C, int64_t cf,
-                                            int n, float* fac, Misc& M) {
+                                            int n, float* stage, float* fac, Misc& M) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int GH = P.GH, REC = att_rec_floats(GH, HD);
   const float* base = P.apart + seq * P.J_att * REC;
   // with more tiles than CTAs every CTA of the sequence holds a record; with
   // fewer, a CTA whose tile range is empty holds none
   const bool all_full = Ta >= C;
+  constexpr int DQ = HD / 4;  // float4 columns of a head; GH * DQ <= NTHREADS (MAX_GH = 8)
+  constexpr int MV = 2 * NW;  // records staged in shared memory (their o parts fill <= 2 NW REC floats)
+  const int e = threadIdx.x, h = e / DQ, dq = e - h * DQ;
+  const bool act = h < GH;
+  const int nst = n < MV ? n : MV;
+  if (act)
+    for (int u = 0; u < nst; ++u)
+      cp_async16(smem_addr(stage + (u * GH + h) * HD + 4 * dq), base + (int64_t)u * REC + h * HD + 4 * dq);
   if (warp < GH) {
     // one round trip for the (m, l) of up to 64 records per lane pair
     float mj[2], lj[2];
@@ -1691,27 +1702,31 @@ __device__ __noinline__ void merge_sequence(const Params& P, int64_t seq, int64_
     l = warp_sum(l);
     for (int j = lane; j < n; j += 32) fac[warp * P.J_att + j] /= l;
   }
+  cp_async_wait_all();
   __syncthreads();
-  constexpr int DQ = HD / 4;  // float4 columns of a head
   const int64_t b = seq / P.Hkv, kvh = seq % P.Hkv;
-  for (int e = threadIdx.x; e < GH * DQ; e += NTHREADS) {
-    const int h = e / DQ, dq = e - h * DQ;
+  if (act) {
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    auto add = [&](float fj, float4 x) {
+      if (fj != 0.f) {
+        acc.x = fmaf(fj, x.x, acc.x);
+        acc.y = fmaf(fj, x.y, acc.y);
+        acc.z = fmaf(fj, x.z, acc.z);
+        acc.w = fmaf(fj, x.w, acc.w);
+      }
+    };
+#pragma unroll 4
+    for (int u = 0; u < nst; ++u)
+      add(fac[h * P.J_att + u], *reinterpret_cast<const float4*>(stage + (u * GH + h) * HD + 4 * dq));
 #pragma unroll 1
-    for (int j0 = 0; j0 < n; j0 += 8) {
-      float4 v[8];
+    for (int j0 = MV; j0 < n; j0 += 8) {
+      float4 w[8];
 #pragma unroll
       for (int u = 0; u < 8; ++u)
-        v[u] = j0 + u < n ? __ldcg(reinterpret_cast<const float4*>(base + (int64_t)(j0 + u) * REC + h * HD) + dq)
+        w[u] = j0 + u < n ? __ldcg(reinterpret_cast<const float4*>(base + (int64_t)(j0 + u) * REC + h * HD) + dq)
                           : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const float fj = j0 + u < n ? fac[h * P.J_att + j0 + u] : 0.f;
-        acc.x = fmaf(fj, v[u].x, acc.x);
-        acc.y = fmaf(fj, v[u].y, acc.y);
-        acc.z = fmaf(fj, v[u].z, acc.z);
-        acc.w = fmaf(fj, v[u].w, acc.w);
-      }
+      for (int u = 0; u < 8; ++u) add(j0 + u < n ? fac[h * P.J_att + j0 + u] : 0.f, w[u]);
     }
     float* dst = P.attn + b * P.Hq * HD + (kvh * GH + h) * HD;
     reinterpret_cast<float4*>(dst)[dq] = acc;
@@ -1957,7 +1972,7 @@ __device__ __forceinline__ bool stage_att_body(const Params& P, int layer, Ring&
     float* fac = recs + NW * 2 * REC;  // per (head, record) factors of the merge
     for (int64_t sq = s0; sq <= s1; ++sq)
       if (M.mseq[(int)(sq - s0)] == sq)
-        merge_sequence<HD>(P, sq, Ta, C, A.cf[sq - s0], A.span[sq - s0], fac, M);
+        merge_sequence<HD>(P, sq, Ta, C, A.cf[sq - s0], A.span[sq - s0], recs, fac, M);
   }
   return true;
 }
