@@ -969,6 +969,12 @@ __device__ __noinline__ void gemv_prep(const Params& P, int layer, int st, uint8
   if ((int64_t)P.D * 2 > SM_NW_BYTES) nw_next = nullptr;
   const int kc_lo = m.pk[E.p], nkc = m.pk[E.p + 1] - kc_lo;
   const int ngr = nkc * GC, ngv = (nkc - 1) * GC + chunk_groups(m, kc_lo + nkc - 1);
+  // A whole-vector panel of QKV (after the previous layer's down stage) or of
+  // gate/up (after Wo) finds its norm vector already staged, in the same
+  // layout, by that weight stage's preparation for its epilogue maxima.
+  if (nw && P.cooperative && nkc == m.Sk && (int64_t)P.D * 2 <= SM_NW_BYTES &&
+      (st == ST_GU || layer * NSTAGE + st > P.stage_begin))
+    nw = nullptr;
   const int kbase = kc_lo * GC * DDL_GROUP;
   uint8_t* nws = smem + SM_NW;
   const int nn = nw ? ngr * 8 : 0, nnx = nw_next ? P.D / 8 : 0;
