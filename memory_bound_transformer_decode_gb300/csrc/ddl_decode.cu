@@ -928,7 +928,8 @@ __device__ __forceinline__ void tile_finish(const Params& P, const GemvCtx& E, c
   }
 }
 
-// Fill the CTA's stage context (thread 0), then a block barrier.
+// Fill the CTA's stage context (thread 0); the block barrier that follows
+// (the grid barrier's wait, or the one after the preparation) publishes it.
 __device__ __noinline__ void fill_gemv_ctx(const Params& P, int layer, int st) {
   GemvCtx& E = ctx().E;
   if (threadIdx.x == 0) {
@@ -952,22 +953,23 @@ __device__ __noinline__ void fill_gemv_ctx(const Params& P, int layer, int st) {
     E.zout = P.Z + (int64_t)(E.gl & 1) * P.B * P.D;
     E.final_layer = P.final_last && layer == P.L - 1;
   }
-  __syncthreads();
 }
 
 // Before a weight stage's barrier: its context and the copies that do not
 // depend on the previous stage (the panel's norm weights, and for Wo and down
-// the next stage's norm vector for the epilogue maxima).
+// the next stage's norm vector for the epilogue maxima).  The copies are
+// issued by warps 0..NW-2: the last warp's lane 0 made the CTA's grid-barrier
+// arrival, whose release waits for the stage's writes to land.
 __device__ __noinline__ void gemv_prep(const Params& P, int layer, int st, uint8_t* smem) {
   fill_gemv_ctx(P, layer, st);
-  const GemvCtx& E = ctx().E;
-  const MatGeom& m = E.m;
+  const MatGeom& m = sp().mg[stage_mat(st)];
+  const int pnl = ctx().ent[0][st].p;
   const LayerDev& Ld = sp().layers[layer];
   const uint16_t* nw = st == ST_QKV ? Ld.norm1 : st == ST_GU ? Ld.norm2 : nullptr;
   const uint16_t* nw_next = st == ST_WO ? Ld.norm2
                             : (st == ST_DOWN && layer + 1 < P.L) ? sp().layers[layer + 1].norm1 : nullptr;
   if ((int64_t)P.D * 2 > SM_NW_BYTES) nw_next = nullptr;
-  const int kc_lo = m.pk[E.p], nkc = m.pk[E.p + 1] - kc_lo;
+  const int kc_lo = m.pk[pnl], nkc = m.pk[pnl + 1] - kc_lo;
   const int ngr = nkc * GC, ngv = (nkc - 1) * GC + chunk_groups(m, kc_lo + nkc - 1);
   // A whole-vector panel of QKV (after the previous layer's down stage) or of
   // gate/up (after Wo) finds its norm vector already staged, in the same
@@ -978,7 +980,7 @@ __device__ __noinline__ void gemv_prep(const Params& P, int layer, int st, uint8
   const int kbase = kc_lo * GC * DDL_GROUP;
   uint8_t* nws = smem + SM_NW;
   const int nn = nw ? ngr * 8 : 0, nnx = nw_next ? P.D / 8 : 0;
-  for (int i = threadIdx.x; i < nn + nnx; i += NTHREADS) {
+  for (int i = threadIdx.x; i < nn + nnx && threadIdx.x < NTHREADS - 32; i += NTHREADS - 32) {
     if (i < nn) {
       const int gs = i >> 3, q = i & 7;
       if (gs < ngv) cp_async16(smem_addr(nws + (size_t)gs * 128 + q * 16), nw + kbase + (int64_t)gs * DDL_GROUP + q * 8);
@@ -2000,7 +2002,7 @@ __device__ __noinline__ void flush_cmax(const Params& P, Misc& M, int layer, int
 // the two the CTA prepares its next stage.
 __device__ void grid_arrive(const Params& P) {
   __syncthreads();
-  if (threadIdx.x == 0) red_release_gpu_add(P.ctrl, 1u);
+  if (threadIdx.x == NTHREADS - 32) red_release_gpu_add(P.ctrl, 1u);  // not thread 0: see gemv_prep
 }
 __device__ bool grid_wait(const Params& P, uint32_t target, Misc& M) {
   if (threadIdx.x == 0) {
@@ -2080,6 +2082,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) decode_kernel(const __grid_consta
         ok = false;
         break;
       }
+    } else {
+      __syncthreads();  // the stage context
     }
     if (threadIdx.x == 0) trace_stamp(P, s, 0);
     if (st == ST_ATT) {
