@@ -85,34 +85,50 @@ def _traffic(workload: str):
 
 
 class Clocks:
-    """nvidia-smi samples during the timed region."""
+    """nvidia-smi samples (every 50 ms) kept for the timed region: the sampler
+    is started before the warm-up and each line is stamped on arrival, so a
+    short timed region still has its own samples (the nearest one on each
+    side when it is shorter than the sampling period)."""
 
     Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, index: int):
+    def __init__(self, index: int, period_ms: int = 50):
         self.index = index
+        self.period_ms = period_ms
         self.proc = None
-        self.lines = []
+        self.lines = []  # (monotonic seconds at arrival, line)
+        self.t0 = self.t1 = None
 
-    def __enter__(self):
+    def start(self):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", str(self.period_ms)],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
+            deadline = time.monotonic() + 5.0
+            while not self.lines and time.monotonic() < deadline and self.proc.poll() is None:
+                time.sleep(0.01)
         except Exception:
             self.proc = None
         return self
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.monotonic(), line.strip()))
 
-    def __exit__(self, *a):
+    def begin(self):
+        self.t0 = time.monotonic()
+
+    def end(self):
+        self.t1 = time.monotonic()
+        if self.proc:  # one more period, so that a sample after the region exists
+            time.sleep(1.5 * self.period_ms / 1000)
+
+    def stop(self):
         if self.proc:
             self.proc.terminate()
             try:
@@ -121,9 +137,16 @@ class Clocks:
                 self.proc.kill()
 
     def summary(self):
+        if self.t0 is None or self.t1 is None:
+            return None
+        inside = [ln for t, ln in self.lines if self.t0 <= t <= self.t1]
+        if not inside:  # a region shorter than the period: the samples around it
+            before = [ln for t, ln in self.lines if t < self.t0][-1:]
+            after = [ln for t, ln in self.lines if t > self.t1][:1]
+            inside = before + after
         sm, mx, reasons = [], None, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        for ln in inside:
             f = [x.strip() for x in ln.split(",")]
             if len(f) < 9:
                 continue
@@ -138,7 +161,8 @@ class Clocks:
         if not sm:
             return None
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
-                "samples": len(sm)}
+                "samples": len(sm), "period_ms": self.period_ms,
+                "region_s": round(self.t1 - self.t0, 4)}
 
 
 def _cpu_baseline(cfg, target_s: float = 12.0):
@@ -242,16 +266,19 @@ def run_ours(args):
             torch.distributed.barrier()
         torch.cuda.synchronize()
 
+    clk = Clocks(local).start()
     for _ in range(max(3, args.warmup)):
         st.decode(out_bf16=out)
     barrier()
     status = ddl.ddl_read_device_status(st.workspace, st.shape, B, st.s_max)
     if status != 0:
+        clk.stop()
         raise RuntimeError(f"device status {status} after warm-up")
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(args.steps)]
-    with Clocks(local) as clk:
+    try:
         barrier()
+        clk.begin()
         t_all0 = torch.cuda.Event(enable_timing=True)
         t_all1 = torch.cuda.Event(enable_timing=True)
         t_all0.record(stream)
@@ -261,6 +288,9 @@ def run_ours(args):
             ev[i][1].record(stream)
         t_all1.record(stream)
         barrier()
+        clk.end()
+    finally:
+        clk.stop()
     total_ms = t_all0.elapsed_time(t_all1)
     per_ms = [a.elapsed_time(b) for a, b in ev]
     ms = total_ms / args.steps
