@@ -48,6 +48,7 @@ extern __shared__ __align__(1024) uint8_t g_smem[];
 constexpr int SM_RING = 0;
 constexpr int SM_RING_BYTES = NW * DEPTH * SLOT_BYTES;
 constexpr int SM_BARS = SM_RING_BYTES;
+constexpr int SM_XBAR = SM_BARS + NW * DEPTH * 8;  // the batch-1 prologue's x copy
 constexpr int SM_SCR = SM_BARS + 512;
 constexpr int XF_BYTES = XF_CHUNKS * GC * 4 * 2 * 4 * 8;  // x fragments: chunks x batch <= 8
 constexpr int SX_BYTES = XF_CHUNKS * GC * NARROW_B * 4;     // per-group sums of x (wide: 2 chunks x 16)
@@ -63,6 +64,7 @@ constexpr int SM_TOTAL = SM_CTX + SM_CTX_BYTES;
 constexpr int XZ_OFF = XF_BYTES + SX_BYTES + NW * 32 * 4;  // zero x fragments for blocks past a slot's end
 constexpr int XZ_BYTES = 2048;                             // covers both fragment layouts
 static_assert(XZ_OFF + XZ_BYTES <= SM_SCR_BYTES, "x fragments do not fit");
+static_assert(SM_XBAR + 8 <= SM_SCR, "barriers");
 static_assert(NW * 2 * (MAX_GH * (128 + 2) + 3) * 4 <= SM_SCR_BYTES, "attention records do not fit");
 static_assert(SM_TOTAL <= 227 * 1024, "shared memory budget");
 static_assert(SM_SPAR % 16 == 0, "parameter copy alignment");
@@ -86,6 +88,7 @@ struct Misc {
   int seg_n[NW];
   long long seg_first[NW], seg_last[NW];
   long long mseq[8];       // sequences this CTA merges last
+  uint32_t xuse;           // batch-1 prologue copies completed on the x barrier so far (its phase)
   int nruns;               // CTA merge: runs of warp records of one sequence
   int run_first[2 * NW];
   uint32_t run_vmask[2 * NW];
@@ -468,10 +471,20 @@ __device__ __noinline__ void gemv_prologue(const Params& P, const GemvCtx& E, ui
   const uint32_t raw = smem_addr(smem + SM_SCR);
   const uint32_t nws = smem_addr(smem + SM_NW);
   // 1. copies (earlier readers of these areas, any thread, are done first):
-  //    quad i = (gs * B + b) * 16 + q16 of x to quad q16 % 4 of its unit
+  //    quad i = (gs * B + b) * 16 + q16 of x to quad q16 % 4 of its unit.  At
+  //    batch 1 that is the panel of x as it lies in memory: one bulk copy
+  //    (thread 0; the ring's copies were issued long before the barrier, so
+  //    it does not queue behind them), completed on the x barrier.
   __syncthreads();
+  const bool bulk = B == 1 && x32 != nullptr;
+  const uint32_t xbar = smem_addr(smem + SM_XBAR), xpar = M.xuse & 1u;
+  if (bulk && tid == 0) {
+    fence_proxy_async_smem();  // the previous stage's generic accesses to this area come first
+    mbar_arrive_expect_tx(xbar, (uint32_t)n_units * 64);
+    bulk_g2s(raw, x32 + kbase, (uint32_t)n_units * 64, xbar);
+  }
 #pragma unroll 1
-  for (int i = tid; i < n_units * 4; i += NTHREADS) {
+  for (int i = tid; i < (bulk ? 0 : n_units * 4); i += NTHREADS) {
     const int gsb = i >> 4, q16 = i & 15;
     const int gs = (int)(((uint32_t)gsb * invB) >> 16), b = gsb - gs * B;
     const int64_t o = (int64_t)b * K + kbase + gs * DDL_GROUP + q16 * 4;
@@ -502,7 +515,9 @@ __device__ __noinline__ void gemv_prologue(const Params& P, const GemvCtx& E, ui
     }
   }
   cp_async_wait_all();
+  if (bulk && !mbar_wait_warp(xbar, xpar, P.ctrl + 1)) M.abort = 1;
   __syncthreads();
+  if (bulk && tid == 0) M.xuse += 1;
   if (tid == 0) trace_stamp(P, E.layer * NSTAGE + E.st, NW + 5);
   // Half unit h = 2 u + p of unit u: quads p and p + 2 (values 4p..4p+3 and
   // 4p+8..4p+11), read from bytes 16p and 32 + 16p of the unit; their high
@@ -2050,6 +2065,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) decode_kernel(const __grid_consta
   if (lane < DEPTH) mbar_init(R.bar0 + lane * 8, 1);
   if (threadIdx.x == 0) {
     M.abort = 0;
+    M.xuse = 0;
+    mbar_init(smem_addr(smem + SM_XBAR), 1);
   }
   if (threadIdx.x < MAX_B) M.cmax[threadIdx.x] = 0u;
   mbar_init_fence();
