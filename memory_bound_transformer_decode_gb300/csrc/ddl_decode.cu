@@ -479,7 +479,8 @@ __device__ __noinline__ void gemv_prologue(const Params& P, const GemvCtx& E, ui
   const bool bulk = B == 1 && x32 != nullptr;
   const uint32_t xbar = smem_addr(smem + SM_XBAR), xpar = M.xuse & 1u;
   if (bulk && tid == 0) {
-    fence_proxy_async_smem();  // the previous stage's generic accesses to this area come first
+    fence_proxy_async_global();  // x: the previous stage's generic stores, read by the copy
+    fence_proxy_async_smem();    // the previous stage's generic accesses to this area come first
     mbar_arrive_expect_tx(xbar, (uint32_t)n_units * 64);
     bulk_g2s(raw, x32 + kbase, (uint32_t)n_units * 64, xbar);
   }

@@ -96,6 +96,11 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
+// Generic-proxy writes to global memory (this CTA's own, or other CTAs'
+// acquired through the grid barrier) before a later async-proxy (TMA) read.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
 
 // ---------------------------------------------------------------- cp.async (through L1, not the TMA unit)
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
