@@ -434,11 +434,12 @@ __device__ __forceinline__ void trace_stamp(const Params& P, int s, int slot) {
 // and measures its panel.
 // A unit (group slot gs, sequence b, k-slice j) is 16 values of x.  Its
 // fragments fill 64 bytes: words 4 (r % 2) + 2 k + r / 2 (high parts) and 8 +
-// the same (low parts) for pair k of quad r (values 4 r + 2 k, +1).  cp.async
-// copies (through L1, so that they do not queue behind the weight ring's bulk
-// copies in the TMA unit) put the unit's four fp32 quads in those same 64
-// bytes, so one thread converts a unit in place, with no barrier between
-// units.  This code runs once per stage: its loops are rolled, because each
+// the same (low parts) for pair k of quad r (values 4 r + 2 k, +1).  The
+// unit's four fp32 quads are first staged in those same 64 bytes, so one
+// thread converts (half) a unit in place, with no barrier between units: at
+// batch 1 the staging layout is x itself and arrives by one bulk copy; wider
+// batches interleave sequences and use cp.async (through L1).  This code
+// runs once per stage: its loops are rolled, because each
 // new instruction is fetched while the memory system carries the weight
 // stream.  The panel's norm weights were copied before the stage's grid
 // barrier (gemv_prep).
