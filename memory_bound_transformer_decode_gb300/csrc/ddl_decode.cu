@@ -823,77 +823,53 @@ __device__ __noinline__ void owner_fixup(const Params& P, const GemvCtx& E, int 
   const int64_t tstride = (int64_t)m.NP * m.J * 32;
   uint64_t* p0 = reinterpret_cast<uint64_t*>(P.gpart) + (int64_t)T0 * tstride + lane;
   uint64_t* p1 = reinterpret_cast<uint64_t*>(P.gpart) + (int64_t)(n > 1 ? T1 : T0) * tstride + lane;
-  // slots 1..7 (the usual case) are polled together and kept in registers
-  uint64_t x0[8], x1[8];
-#pragma unroll
-  for (int f = 0; f < 8; ++f) x0[f] = x1[f] = PART_EMPTY;
-  uint32_t w0 = mk0 & 0xFEu, w1 = mk1 & 0xFEu;
+  // Slots in chunks of 8 (one chunk at batch 1, more with many panels): the
+  // chunk's slots are polled together and kept in registers, then summed in
+  // slot order (the owner's own first) and emptied for the next stage.
+  float s0 = a0, s1 = b0, u0 = a1, u1 = b1;
+  const uint32_t all = mk0 | (n > 1 ? mk1 : 0u);
   uint64_t tw = 0;
-  for (uint32_t it = 1; w0 | w1; ++it) {
+#pragma unroll 1
+  for (int c = 0; c < 32 && !M.abort && (all >> c) != 0u; c += 8) {
+    const uint32_t own = c == 0 ? 0xFEu : 0xFFu;
+    const uint32_t c0 = (mk0 >> c) & own, c1 = n > 1 ? (mk1 >> c) & own : 0u;
+    uint64_t x0[8], x1[8];
 #pragma unroll
-    for (int f = 1; f < 8; ++f) {
-      if (w0 >> f & 1u) x0[f] = ld_relaxed_gpu_u64(p0 + f * 32);
-      if (w1 >> f & 1u) x1[f] = ld_relaxed_gpu_u64(p1 + f * 32);
-    }
+    for (int f = 0; f < 8; ++f) x0[f] = x1[f] = PART_EMPTY;
+    uint32_t w0 = c0, w1 = c1;
+    for (uint32_t it = 1; w0 | w1; ++it) {
 #pragma unroll
-    for (int f = 1; f < 8; ++f) {
-      if (x0[f] != PART_EMPTY) w0 &= ~(1u << f);
-      if (x1[f] != PART_EMPTY) w1 &= ~(1u << f);
-    }
-    if (!(w0 | w1) || (it & 63u) != 0) continue;
-    const uint64_t now = globaltimer();
-    if (tw == 0) tw = now;
-    else if (now - tw > WAIT_LIMIT_NS) {
-      atomicExch(P.ctrl + 1, STATUS_TIMEOUT);
-      M.abort = 1;
-      break;
-    }
-  }
-  // slots 8.. (many panels): one at a time
-  for (int k = 0; k < 2; ++k) {
-    const uint64_t* pk = k ? p1 : p0;
-    for (uint32_t r = (k ? mk1 : mk0) & ~0xFFu; r && !M.abort; r &= r - 1) {
-      const int f = __ffs(r) - 1;
-      for (uint32_t it = 1; ld_relaxed_gpu_u64(pk + f * 32) == PART_EMPTY; ++it) {
-        if ((it & 63u) != 0) continue;
-        const uint64_t now = globaltimer();
-        if (tw == 0) tw = now;
-        else if (now - tw > WAIT_LIMIT_NS) {
-          atomicExch(P.ctrl + 1, STATUS_TIMEOUT);
-          M.abort = 1;
-          break;
-        }
+      for (int f = 0; f < 8; ++f) {
+        if (w0 >> f & 1u) x0[f] = ld_relaxed_gpu_u64(p0 + (c + f) * 32);
+        if (w1 >> f & 1u) x1[f] = ld_relaxed_gpu_u64(p1 + (c + f) * 32);
+      }
+#pragma unroll
+      for (int f = 0; f < 8; ++f) {
+        if (x0[f] != PART_EMPTY) w0 &= ~(1u << f);
+        if (x1[f] != PART_EMPTY) w1 &= ~(1u << f);
+      }
+      if (!(w0 | w1) || (it & 63u) != 0) continue;
+      const uint64_t now = globaltimer();
+      if (tw == 0) tw = now;
+      else if (now - tw > WAIT_LIMIT_NS) {
+        atomicExch(P.ctrl + 1, STATUS_TIMEOUT);
+        M.abort = 1;
+        break;
       }
     }
-  }
-  // sums in slot order, then the slots are emptied for the next stage
-  float s0 = a0, s1 = b0, u0 = a1, u1 = b1;
 #pragma unroll
-  for (int f = 1; f < 8; ++f) {
-    if (mk0 >> f & 1u) {
-      s0 += __uint_as_float((uint32_t)x0[f]);
-      s1 += __uint_as_float((uint32_t)(x0[f] >> 32));
-      p0[f * 32] = PART_EMPTY;
+    for (int f = 0; f < 8; ++f) {
+      if (c0 >> f & 1u) {
+        s0 += __uint_as_float((uint32_t)x0[f]);
+        s1 += __uint_as_float((uint32_t)(x0[f] >> 32));
+        p0[(c + f) * 32] = PART_EMPTY;
+      }
+      if (c1 >> f & 1u) {
+        u0 += __uint_as_float((uint32_t)x1[f]);
+        u1 += __uint_as_float((uint32_t)(x1[f] >> 32));
+        p1[(c + f) * 32] = PART_EMPTY;
+      }
     }
-    if (n > 1 && (mk1 >> f & 1u)) {
-      u0 += __uint_as_float((uint32_t)x1[f]);
-      u1 += __uint_as_float((uint32_t)(x1[f] >> 32));
-      p1[f * 32] = PART_EMPTY;
-    }
-  }
-  for (uint32_t r = mk0 & ~0xFFu; r; r &= r - 1) {
-    const int f = __ffs(r) - 1;
-    const uint64_t y = ld_relaxed_gpu_u64(p0 + f * 32);
-    s0 += __uint_as_float((uint32_t)y);
-    s1 += __uint_as_float((uint32_t)(y >> 32));
-    p0[f * 32] = PART_EMPTY;
-  }
-  for (uint32_t r = n > 1 ? mk1 & ~0xFFu : 0u; r; r &= r - 1) {
-    const int f = __ffs(r) - 1;
-    const uint64_t y = ld_relaxed_gpu_u64(p1 + f * 32);
-    u0 += __uint_as_float((uint32_t)y);
-    u1 += __uint_as_float((uint32_t)(y >> 32));
-    p1[f * 32] = PART_EMPTY;
   }
   __syncwarp();
   if (t < P.B) {
