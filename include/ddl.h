@@ -206,10 +206,11 @@ int ddl_set_launch_mode(int32_t mode);
  * call of at most 96 layers whose trace fits in `bytes` writes 16 uint64
  * words per (stage, CTA), stages in order (layer * 5 + stage: QKV, ATT, WO,
  * GU, DOWN): word 0 = %globaltimer (ns) at the stage start; words 1..14 =
- * %clock64 (SM cycles) at the end of the stage prologue, the end of each of
- * the 8 warps' streams, the stage end, and four steps inside a weight
- * stage's prologue (copies issued, sum of squares loaded, copies landed,
- * scale known); word 15 = %clock64 at the stage start.  Needs
+ * %clock64 (SM cycles) at the end of the stage prologue (word 1), the end
+ * of each of the 8 warps' streams (words 2..9), the stage end (word 10), and
+ * inside a weight stage's prologue: x copies issued (word 11), x landed
+ * (word 13), fragments and RMSNorm factor done (word 14); word 12 is not
+ * written; word 15 = %clock64 at the stage start.  Needs
  * L * 5 * SMs * 16 * 8 bytes.  NULL turns tracing off. */
 int ddl_set_trace(void* device_buf, size_t bytes);
 
