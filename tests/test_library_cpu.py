@@ -44,9 +44,7 @@ def _geom_bytes(cfg, int4: bool) -> int:
     off = 0
     for N, K in dims:
         T = (N // 16) * (K // 64)
-        off = al(off + T * (512 if int4 else 2048))
-        if int4:
-            off = al(off + T * 32)
+        off = al(off + T * (544 if int4 else 2048))  # INT4 block: 512 B of codes, then its 32 B of scales
     return off
 
 
