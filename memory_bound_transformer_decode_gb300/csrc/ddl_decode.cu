@@ -16,10 +16,11 @@
 //   GU   : rmsnorm(y) folded into the gate/up GEMV, silu(g) * u in the epilogue
 //          (Unsloth/Qwen-27B article §二.1 fused SwiGLU)
 //   DOWN : z = y + a Wd
-// Every warp owns a ring of DEPTH shared-memory slots filled by 1-D TMA bulk
-// copies; its lane 0 keeps DEPTH slots in flight, running ahead across stage
-// (and layer) boundaries because weights and the KV history do not depend on
-// the token being decoded.  Stages are separated by a grid-wide barrier (one
+// Every warp owns a ring of DEPTH shared-memory slots filled by TMA (1-D bulk
+// copies of weight blocks, 2-D tensor copies of K/V tiles); its lane 0 keeps
+// DEPTH slots in flight, running ahead across stage (and layer) boundaries
+// because weights and the KV history do not depend on the token being
+// decoded.  Stages are separated by a grid-wide barrier (one
 // cooperative launch for the whole stack) or by kernel boundaries (one launch
 // per stage).  All waits are bounded: a wait that gives up sets the status
 // word in the workspace and the kernel returns.
