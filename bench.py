@@ -53,6 +53,24 @@ def _dist():
     return rank, world, local
 
 
+def _slowest(ms: float, world: int, device: str) -> float:
+    """The slowest rank's time (max over ranks); every rank gets it."""
+    if world <= 1:
+        return ms
+    import torch
+    import torch.distributed
+
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def _job_rate(world: int, batch: int, ms: float) -> float:
+    """Whole-job tokens/s: each rank decodes `batch` tokens a step and the
+    job's step takes the slowest rank's time."""
+    return world * batch / (ms * 1e-3)
+
+
 def _peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -293,11 +311,7 @@ def run_ours(args):
         clk.stop()
     total_ms = t_all0.elapsed_time(t_all1)
     per_ms = [a.elapsed_time(b) for a, b in ev]
-    ms = total_ms / args.steps
-    if world > 1:
-        t = torch.tensor([ms], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = _slowest(total_ms / args.steps, world, "cuda")
     status = ddl.ddl_read_device_status(st.workspace, st.shape, B, st.s_max)
     if status != 0:
         raise RuntimeError(f"device status {status} in the timed region")
@@ -316,11 +330,7 @@ def run_ours(args):
         out_host.copy_(out, non_blocking=True)
     e1.record(stream)
     barrier()
-    e2e_ms = e0.elapsed_time(e1) / args.steps
-    if world > 1:
-        t = torch.tensor([e2e_ms], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = _slowest(e0.elapsed_time(e1) / args.steps, world, "cuda")
 
     nbytes = roofline.step_bytes(cfg)
     peak, peak_kind = _peaks()
@@ -329,7 +339,7 @@ def run_ours(args):
     launches_per_step = (L + 95) // 96 if args.mode == 0 else L * 6
     line = {
         "metric": METRIC,
-        "value": world * B / (ms * 1e-3),
+        "value": _job_rate(world, B, ms),
         "unit": "tokens/s",
         "n_gpus": world,
         "steps": args.steps,
@@ -349,7 +359,7 @@ def run_ours(args):
                      "frac": achieved / peak, "peak_source": f"hbm_gbs of {peak_kind}",
                      "traffic": _traffic(cfg.name),
                      "kernel": "decode_kernel (one persistent launch per step)"},
-        "e2e": {"value": world * B / (e2e_ms * 1e-3), "unit": "tokens/s",
+        "e2e": {"value": _job_rate(world, B, e2e_ms), "unit": "tokens/s",
                 "h2d_bytes_per_step": B * cfg.D * 2, "d2h_bytes_per_step": B * cfg.D * 2},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk.summary(),
