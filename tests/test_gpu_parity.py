@@ -247,6 +247,24 @@ def test_stack_parity_small_and_launch_modes_agree():
     assert np.max(np.abs(res_c - z)) <= MAX_ABS
 
 
+def test_stack_longer_than_one_launch():
+    """100 layers: two cooperative launches of at most 96 layers, the second
+    starting with its own maxima, counters and empty partial slots; bit-equal
+    to one launch per stage, and to the oracle run untethered over all 100
+    layers (output rel-L2 at the step's bar; the fp32 residual held to 1e-3 of
+    the largest |z|, as for the 64-layer stack)."""
+    cfg = EDGE.with_(layers=100, kv_len=45, D=256, H_q=8, H_kv=2, head_dim=128, d_ff=320, name="s100")
+    st = workload.build_stack(cfg, batch=1)
+    kv0 = [(synth.bits(k).copy(), synth.bits(v).copy()) for k, v in st.kvs]
+    out_c, res_c, _ = device_outputs(st, mode=0)
+    out_s, res_s, _ = device_outputs(st, mode=1)
+    np.testing.assert_array_equal(out_c, out_s)
+    np.testing.assert_array_equal(res_c, res_s)
+    z, _, _, _ = oracle_stack(st, kv0)
+    assert rel_l2(oracle.bf16_to_f64(out_c), z) <= REL_L2
+    assert np.max(np.abs(res_c - z)) <= 1e-3 * np.max(np.abs(z))
+
+
 def test_bf16_weight_layer_parity():
     st = workload.build_stack(EDGE.with_(kv_len=24, D=256, d_ff=320), wtype=ddl.BF16, batch=2)
     _check_layer(st)
