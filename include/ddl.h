@@ -191,8 +191,9 @@ int ddl_stack_decode(const ddl_shape* shape, ddl_wtype wtype, const ddl_layer_w*
  *    more scratch than DDL_NOALLOC_SCRATCH_BYTES (ddl_workspace_bytes tells).
  *  - All calls share the array and a call leaves its contents behind; calls
  *    that overlap on the GPU (other streams, other threads) race on it, so
- *    order them on one stream.  The device status word of these calls is
- *    not readable through ddl_read_device_status. */
+ *    order them on one stream.
+ *  - The device status word of the last call (DDL_OK or DDL_ERR_TIMEOUT) is
+ *    read with ddl_read_device_status(NULL, ...). */
 int ddl_stack_decode_noalloc(const ddl_shape* shape, ddl_wtype wtype, const ddl_layer_w* layers,
                              const ddl_kv* kv, int32_t L, int32_t B, int64_t pos,
                              const float* resid_in, const uint16_t* x_bf16, float* resid_out,
@@ -215,7 +216,9 @@ int ddl_set_launch_mode(int32_t mode);
 int ddl_set_trace(void* device_buf, size_t bytes);
 
 /* Synchronize `stream` and read the device status word of the last decode
- * call that used `workspace` (DDL_OK or DDL_ERR_TIMEOUT); host-blocking. */
+ * call that used `workspace` (DDL_OK or DDL_ERR_TIMEOUT); host-blocking.
+ * workspace NULL reads the status word of the last ddl_stack_decode_noalloc
+ * call (its static scratch).  shape, B and s_max are those of that call. */
 int ddl_read_device_status(const void* workspace, const ddl_shape* shape, int32_t B,
                            int64_t s_max, int32_t* status_out, void* stream);
 

@@ -2427,10 +2427,15 @@ extern "C" int ddl_set_trace(void* device_buf, size_t bytes) {
 
 extern "C" int ddl_read_device_status(const void* workspace, const ddl_shape* shape, int32_t B,
                                       int64_t s_max, int32_t* status_out, void* stream) {
-  if (!workspace || !status_out) return DDL_ERR_ARG;
+  if (!status_out) return DDL_ERR_ARG;
   ddl_ws_view v;
   int st = ddl_workspace_view(shape, B, s_max, &v);
   if (st) return st;
+  if (!workspace) {  // the static scratch of ddl_stack_decode_noalloc
+    void* p = nullptr;
+    if ((st = noalloc_scratch(&p)) != DDL_OK) return st;
+    workspace = p;
+  }
   cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
   if (e != cudaSuccess) return cuda_status(e);
   uint32_t word = 0;

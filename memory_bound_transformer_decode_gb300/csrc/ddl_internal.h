@@ -11,6 +11,7 @@
 namespace ddl {
 
 void set_cuda_error(cudaError_t e);  // records cudaGetErrorString(e) for ddl_last_cuda_error
+int noalloc_scratch(void** out);     // device address of ddl_stack_decode_noalloc's static scratch
 
 inline int cuda_status(cudaError_t e) {
   if (e == cudaSuccess) return DDL_OK;

@@ -12,37 +12,32 @@
 // start at zero itself), and calls that overlap on the GPU race on it.
 #include <cuda_runtime.h>
 
-#include <mutex>
-
 #include "ddl_internal.h"
 
 namespace {
 
 __device__ __align__(256) unsigned char g_noalloc_scratch[DDL_NOALLOC_SCRATCH_BYTES];
 
-std::mutex g_noalloc_mu;
-void* g_noalloc_ptr[64] = {nullptr};
-
-// Device address of the scratch array on the current device, looked up once
-// per device (in host code the array's name is only a stand-in, not a device
-// address).
+// Device address of the scratch array on the current device (in host code
+// the array's name is only a stand-in, not a device address).  It is looked up
+// on every call, not cached: after cudaDeviceReset the module loads again and
+// the array may move, and once the module is loaded the lookup is cheap.  The
+// first lookup on a device loads the module, which is why the first call
+// should come before any stream capture.
 int scratch_address(void** out) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  void* p = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
   if (e != cudaSuccess) return ddl::cuda_status(e);
-  if (dev < 0 || dev >= 64) return DDL_ERR_UNSUPPORTED;
-  std::lock_guard<std::mutex> lk(g_noalloc_mu);
-  if (!g_noalloc_ptr[dev]) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-    if (e != cudaSuccess) return ddl::cuda_status(e);
-    g_noalloc_ptr[dev] = p;
-  }
-  *out = g_noalloc_ptr[dev];
+  *out = p;
   return DDL_OK;
 }
 
 }  // namespace
+
+namespace ddl {
+// The scratch array's address for ddl_read_device_status (workspace NULL).
+int noalloc_scratch(void** out) { return scratch_address(out); }
+}  // namespace ddl
 
 extern "C" int ddl_stack_decode_noalloc(const ddl_shape* shape, ddl_wtype wtype,
                                         const ddl_layer_w* layers, const ddl_kv* kv, int32_t L,

@@ -279,8 +279,10 @@ def ddl_set_trace(buf: torch.Tensor | None):
         _check("ddl_set_trace", lib.ddl_set_trace(_ptr(buf), buf.numel() * buf.element_size()))
 
 
-def ddl_read_device_status(workspace: torch.Tensor, shape: Shape, B: int, s_max: int,
+def ddl_read_device_status(workspace: torch.Tensor | None, shape: Shape, B: int, s_max: int,
                            stream=None) -> int:
+    """Status word of the last decode call on `workspace` (None: the static
+    scratch of ddl_stack_decode_noalloc)."""
     out = ctypes.c_int32(0)
     _check("ddl_read_device_status",
            load().ddl_read_device_status(_ptr(workspace), ctypes.byref(shape), B, s_max,
