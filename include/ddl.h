@@ -203,16 +203,34 @@ int ddl_stack_decode_noalloc(const ddl_shape* shape, ddl_wtype wtype, const ddl_
  * kernel when possible), 1 = one launch per fused stage. */
 int ddl_set_launch_mode(int32_t mode);
 
+/* Limit of every bounded wait inside the decode kernels (a wait for a TMA
+ * copy, a grid barrier, another CTA's partial sums): a wait that gives up sets
+ * the device status word to DDL_ERR_TIMEOUT and the kernel returns without
+ * faulting; later calls on the same context work.  Applies to later calls;
+ * ns = 0 restores the default of 2 s. */
+int ddl_set_wait_limit_ns(uint64_t ns);
+
+/* Test hook for the timeout path: when stage >= 0, the grid barrier in front
+ * of flattened stage `stage` (layer * 5 + stage kind; QKV, ATT, WO, GU, DOWN)
+ * of later cooperative decode calls waits for one arrival more than the grid
+ * makes, so every CTA's bounded wait gives up (after the wait limit) and the
+ * call reports DDL_ERR_TIMEOUT through ddl_read_device_status.  No fault, trap
+ * or unbounded wait is involved.  -1 turns it off (the default); stage 0 has
+ * no barrier in front of it. */
+int ddl_test_hold_barrier(int32_t stage);
+
 /* Tracing: when device_buf (device memory) is not NULL, every later decode
- * call of at most 96 layers whose trace fits in `bytes` writes 16 uint64
+ * call of at most 96 layers whose trace fits in `bytes` writes 32 uint64
  * words per (stage, CTA), stages in order (layer * 5 + stage: QKV, ATT, WO,
  * GU, DOWN): word 0 = %globaltimer (ns) at the stage start; words 1..14 =
  * %clock64 (SM cycles) at the end of the stage prologue (word 1), the end
- * of each of the 8 warps' streams (words 2..9), the stage end (word 10), and
- * inside a weight stage's prologue: x copies issued (word 11), x landed
- * (word 13), fragments and RMSNorm factor done (word 14); word 12 is not
- * written; word 15 = %clock64 at the stage start.  Needs
- * L * 5 * SMs * 16 * 8 bytes.  NULL turns tracing off. */
+ * of each of the 8 consumer warps' streams (words 2..9), the stage end (word
+ * 10), and inside a weight stage's prologue: x copies issued (word 11), x
+ * landed (word 13), fragments and RMSNorm factor done (word 14); word 12 is
+ * not written; word 15 = %clock64 at the stage start; words 16..23 = the
+ * cycles each consumer warp waited for its ring's data, words 24..31 = the
+ * ring slots it consumed.  Needs L * 5 * SMs * 32 * 8 bytes.  NULL turns
+ * tracing off. */
 int ddl_set_trace(void* device_buf, size_t bytes);
 
 /* Synchronize `stream` and read the device status word of the last decode

@@ -16,11 +16,13 @@
 //   GU   : rmsnorm(y) folded into the gate/up GEMV, silu(g) * u in the epilogue
 //          (Unsloth/Qwen-27B article §二.1 fused SwiGLU)
 //   DOWN : z = y + a Wd
-// Every warp owns a ring of DEPTH shared-memory slots filled by TMA (1-D bulk
-// copies of weight blocks, 2-D tensor copies of K/V tiles); its lane 0 keeps
-// DEPTH slots in flight, running ahead across stage (and layer) boundaries
-// because weights and the KV history do not depend on the token being
-// decoded.  Stages are separated by a grid-wide barrier (one
+// Every consumer warp owns a ring of DEPTH shared-memory slots filled by TMA
+// (1-D bulk copies of weight blocks, 2-D tensor copies of K/V tiles).  One
+// producer warp keeps all the rings full: its lane w walks consumer warp w's
+// work and refills a slot as soon as the consumer hands it back (an "empty"
+// mbarrier), running ahead across stage (and layer) boundaries because
+// weights and the KV history do not depend on the token being decoded; the
+// consumers only wait for data, compute and hand slots back.  Stages are separated by a grid-wide barrier (one
 // cooperative launch for the whole stack) or by kernel boundaries (one launch
 // per stage).  All waits are bounded: a wait that gives up sets the status
 // word in the workspace and the kernel returns.
@@ -48,8 +50,9 @@ struct SParams {
 extern __shared__ __align__(1024) uint8_t g_smem[];
 constexpr int SM_RING = 0;
 constexpr int SM_RING_BYTES = NW * DEPTH * SLOT_BYTES;
-constexpr int SM_BARS = SM_RING_BYTES;
-constexpr int SM_XBAR = SM_BARS + NW * DEPTH * 8;  // the batch-1 prologue's x copy
+constexpr int SM_BARS = SM_RING_BYTES;                // "full" barriers: a slot's copy landed
+constexpr int SM_EBARS = SM_BARS + NW * DEPTH * 8;    // "empty" barriers: the consumer handed a slot back
+constexpr int SM_XBAR = SM_EBARS + NW * DEPTH * 8;    // the batch-1 prologue's x copy
 constexpr int SM_SCR = SM_BARS + 512;
 constexpr int XF_BYTES = XF_CHUNKS * GC * 4 * 2 * 4 * 8;  // x fragments: chunks x batch <= 8
 constexpr int SX_BYTES = XF_CHUNKS * GC * NARROW_B * 4;     // per-group sums of x (wide: 2 chunks x 16)
@@ -104,29 +107,42 @@ struct SlotDesc {
   int kind, cnt;
   uint32_t a;  // GEMV: stream block index; K/V: first row of the tile in the [rows][hd] cache view
 };
-// Producer cursor over this warp's slots of every stage of the launch; it
-// caches the current stage's stream bases so that issuing a slot reads no
-// per-layer parameter with a run-time index.
+// Producer cursor over one consumer warp's slots of every stage of the
+// launch (held by the producer lane serving that warp); it caches the current
+// stage's stream bases so that issuing a slot reads no per-layer parameter
+// with a run-time index.
 struct Cursor {
   int s, st;              // flattened stage and its kind
   uint32_t pos, end;      // work index and end: GEMV panel blocks, ATT 2 x tiles (K, V)
   uint32_t a;             // GEMV: stream block index of pos; ATT: cache-view row of the tile
   int aseq, ai;           // ATT: sequence and tile index of the tile
   const uint8_t* wbase;   // GEMV: block stream of the matrix (INT4: codes and scales)
-  const uint8_t* sbase;   // GEMV: scales of the stream's first block (INT4)
-  const uint16_t* kbase;  // ATT: K cache of the layer
-  const uint16_t* vbase;  // ATT: V cache of the layer
   const void* kmap;       // ATT: tensor maps of the layer's caches
   const void* vmap;
   int kc, T, gi, gk;      // GEMV: (k-chunk, tile, group) of work index `pos`
   int NT, Sk, Gc, G;      // GEMV: geometry of the matrix
   int pk0, pk1;           // GEMV: k-chunks of this CTA's panel
 };
+// A consumer warp's view of its ring: the next slot to consume sits at
+// slot(), lands on full barrier bar() with phase parity `phase`, and is
+// handed back on empty barrier ebar(); advance() steps to the slot after it.
 struct Ring {
-  uint32_t slot0, bar0, n_issued, n_done;
-  __device__ __forceinline__ uint32_t slot(uint32_t n) const { return slot0 + (n % DEPTH) * SLOT_BYTES; }
-  __device__ __forceinline__ uint32_t bar(uint32_t n) const { return bar0 + (n % DEPTH) * 8; }
-  __device__ __forceinline__ uint32_t parity(uint32_t n) const { return (n / DEPTH) & 1; }
+  uint32_t slot0, bar0, ebar0;
+  uint32_t idx, phase;
+  __device__ __forceinline__ uint32_t slot() const { return slot0 + idx * SLOT_BYTES; }
+  __device__ __forceinline__ uint32_t bar() const { return bar0 + idx * 8; }
+  __device__ __forceinline__ uint32_t ebar() const { return ebar0 + idx * 8; }
+  __device__ __forceinline__ void advance() {
+    if (++idx == DEPTH) {
+      idx = 0;
+      phase ^= 1u;
+    }
+  }
+  __device__ __forceinline__ Ring next() const {
+    Ring r = *this;
+    r.advance();
+    return r;
+  }
 };
 
 // Per-stage constants of a GEMV stage, read once from the parameters.
@@ -143,8 +159,8 @@ struct GemvCtx {
 };
 
 // CTA-wide state in shared memory, so that nothing lives in local memory:
-// the current weight stage's context and each warp's ring and producer
-// cursor between stages.
+// the current weight stage's context and each consumer warp's ring between
+// stages.
 // A warp's place in each stage kind, the same for every layer of a launch:
 // computed once at launch so that entering a stage costs no divisions.
 struct Entry {
@@ -168,7 +184,6 @@ struct Ctx {
   GemvCtx E;
   AttCta att;
   Ring ring[NW];
-  Cursor cur[NW];
   Entry ent[NW][NSTAGE];
 };
 static_assert(sizeof(Ctx) <= SM_CTX_BYTES, "context");
@@ -243,7 +258,7 @@ __device__ __noinline__ void compute_entries(const Params& P) {
         }
       }
     }
-    if ((threadIdx.x & 31) == 0) ctx().ent[warp][st] = e;
+    if ((threadIdx.x & 31) == 0 && warp < NW) ctx().ent[warp][st] = e;
   }
   AttCta& A = ctx().att;
   const int64_t Ta = (int64_t)P.B * P.Hkv * P.nt_att, C = gridDim.x, nt = P.nt_att;
@@ -264,11 +279,11 @@ __device__ __noinline__ void compute_entries(const Params& P) {
   }
 }
 template <int WT>
-__device__ __forceinline__ void cursor_enter(const Params& P, Cursor& c) {
+__device__ __forceinline__ void cursor_enter(const Params& P, Cursor& c, int w) {
   const int st = c.s % NSTAGE;
   c.st = st;
   const LayerDev& Ld = sp().layers[c.s / NSTAGE];
-  const Entry& e = ctx().ent[threadIdx.x >> 5][st];
+  const Entry& e = ctx().ent[w][st];
   c.pos = e.lo;
   c.end = e.hi;
   if (st == ST_ATT) {
@@ -277,14 +292,11 @@ __device__ __forceinline__ void cursor_enter(const Params& P, Cursor& c) {
     c.a = (uint32_t)((int64_t)c.aseq * P.s_max + 16 * c.ai);
     c.pos *= 2;
     c.end *= 2;
-    c.kbase = Ld.kc;
-    c.vbase = Ld.vc;
     c.kmap = &P.kmap[c.s / NSTAGE];
     c.vmap = &P.vmap[c.s / NSTAGE];
   } else {
     const MatGeom& m = sp().mg[stage_mat(st)];
     c.wbase = Ld.packed + m.woff;
-    c.sbase = Ld.packed + m.soff;
     c.NT = m.NT;
     c.Sk = m.Sk;
     c.Gc = m.Gc;
@@ -299,11 +311,10 @@ __device__ __forceinline__ void cursor_enter(const Params& P, Cursor& c) {
   }
 }
 template <int WT>
-__device__ __forceinline__ bool cursor_next(const Params& P, Cursor& c, int64_t wg, int64_t W,
-                                            SlotDesc& d) {
+__device__ __forceinline__ bool cursor_next(const Params& P, Cursor& c, int w, SlotDesc& d) {
   while (c.pos >= c.end) {
     if (++c.s >= P.stage_end) return false;
-    cursor_enter<WT>(P, c);
+    cursor_enter<WT>(P, c, w);
   }
   if (c.st == ST_ATT) {  // K then V of one 16-key tile
     d.kind = (c.pos & 1) ? SK_V : SK_K;
@@ -353,35 +364,32 @@ __device__ __forceinline__ uint32_t kv_base(uint32_t slot) { return (slot + 1023
 __device__ __forceinline__ uint32_t kv_addr(uint32_t slot, int r, int ch) {
   return kv_base(slot) + (ch >> 3) * 2048 + r * 128 + (((ch & 7) ^ (r & 7)) << 4);
 }
+// Issue one slot's copies (by one producer lane).
 template <int HD, int WT>
-__device__ __forceinline__ void issue_slot(const Params& P, const Cursor& c, const SlotDesc& d,
-                                           uint32_t slot, uint32_t bar, int lane, uint64_t policy) {
+__device__ __forceinline__ void issue_slot(const Cursor& c, const SlotDesc& d, uint32_t slot, uint32_t bar,
+                                           uint64_t policy) {
   if (d.kind == SK_GEMV) {
-    if (lane == 0) {
-      constexpr bool q4 = WT == DDL_W_INT4;
-      constexpr uint32_t BB = q4 ? QBLK_BYTES : BF16_BLK_BYTES;  // INT4: codes and scales together
-      const uint32_t wb = d.cnt * BB;
-      mbar_arrive_expect_tx(bar, wb);
-      bulk_g2s_evict_first(slot, c.wbase + (uint64_t)d.a * BB, wb, bar, policy);
-    }
+    constexpr bool q4 = WT == DDL_W_INT4;
+    constexpr uint32_t BB = q4 ? QBLK_BYTES : BF16_BLK_BYTES;  // INT4: codes and scales together
+    const uint32_t wb = d.cnt * BB;
+    mbar_arrive_expect_tx(bar, wb);
+    bulk_g2s_evict_first(slot, c.wbase + (uint64_t)d.a * BB, wb, bar, policy);
   } else {  // 16 rows of K or V: HD/64 boxes of 16 rows x 128 bytes, swizzled (kv_addr)
-    if (lane == 0) mbar_arrive_expect_tx(bar, 16 * HD * 2);
-    if (lane < HD / 64)
-      tensor2d_g2s(kv_base(slot) + lane * 2048, d.kind == SK_K ? c.kmap : c.vmap, lane * 64, (int)d.a, bar, policy);
+    mbar_arrive_expect_tx(bar, 16 * HD * 2);
+#pragma unroll
+    for (int b = 0; b < HD / 64; ++b)
+      tensor2d_g2s(kv_base(slot) + b * 2048, d.kind == SK_K ? c.kmap : c.vmap, b * 64, (int)d.a, bar, policy);
   }
 }
 
-// Release the slot just consumed and refill the ring from the cursor.
-template <int HD, int WT>
-__device__ __forceinline__ void ring_advance(const Params& P, Ring& R, Cursor& prod, int64_t wg,
-                                             int64_t W, int lane, uint64_t policy) {
+// Hand the slot just consumed back to the producer.  The warp's reads of it
+// are ordered before the arrival by the warp barrier and the arrival's
+// release; a warp that wrote into the slot fenced those writes for the async
+// proxy first.
+__device__ __forceinline__ void ring_advance(Ring& R, int lane) {
   __syncwarp();
-  SlotDesc d;
-  if (cursor_next<WT>(P, prod, wg, W, d)) {
-    issue_slot<HD, WT>(P, prod, d, R.slot(R.n_issued), R.bar(R.n_issued), lane, policy);
-    R.n_issued++;
-  }
-  R.n_done++;
+  if (lane == 0) mbar_arrive(R.ebar());
+  R.advance();
 }
 
 // ------------------------------------------------------------------ small helpers
@@ -404,16 +412,24 @@ __device__ __forceinline__ float4 bf16x4_f32(uint2 u) {
 }
 
 // Optional trace per (stage, CTA): word 0 is %globaltimer at the stage start
-// (comparable across SMs), the last word %clock64 at the same moment, and the
-// others %clock64 at later events (end of the prologue, end of each warp's
+// (comparable across SMs), word 15 %clock64 at the same moment, and words
+// 1..14 %clock64 at later events (end of the prologue, end of each warp's
 // stream, end of the stage, prologue steps), so that intervals within a CTA
-// are exact to a cycle.
+// are exact to a cycle; words 16 + w and 24 + w hold the cycles consumer warp
+// w spent waiting for its ring's data and the slots it consumed.
+__device__ __forceinline__ void trace_ring(const Params& P, int s, uint64_t wait_cycles, uint32_t slots) {
+  if (P.trace && (threadIdx.x & 31) == 0) {
+    uint64_t* w = P.trace + ((int64_t)(s - P.stage_begin) * gridDim.x + blockIdx.x) * TRACE_WORDS;
+    w[16 + (threadIdx.x >> 5)] = wait_cycles;
+    w[24 + (threadIdx.x >> 5)] = slots;
+  }
+}
 __device__ __forceinline__ void trace_stamp(const Params& P, int s, int slot) {
   if (P.trace) {
     uint64_t* w = P.trace + ((int64_t)(s - P.stage_begin) * gridDim.x + blockIdx.x) * TRACE_WORDS;
     if (slot == 0) {
       const uint64_t c = clock64();
-      w[TRACE_WORDS - 1] = c;
+      w[15] = c;
       w[0] = globaltimer();
     } else {
       w[slot] = clock64();
@@ -477,7 +493,7 @@ __device__ __noinline__ void gemv_prologue(const Params& P, const GemvCtx& E, ui
   //    batch 1 that is the panel of x as it lies in memory: one bulk copy
   //    (thread 0; the ring's copies were issued long before the barrier, so
   //    it does not queue behind them), completed on the x barrier.
-  __syncthreads();
+  csync();
   const bool bulk = B == 1 && x32 != nullptr;
   const uint32_t xbar = smem_addr(smem + SM_XBAR), xpar = M.xuse & 1u;
   if (bulk && tid == 0) {
@@ -518,8 +534,8 @@ __device__ __noinline__ void gemv_prologue(const Params& P, const GemvCtx& E, ui
     }
   }
   cp_async_wait_all();
-  if (bulk && !mbar_wait_warp(xbar, xpar, P.ctrl + 1)) M.abort = 1;
-  __syncthreads();
+  if (bulk && !mbar_wait_warp(xbar, xpar, P.ctrl + 1, P.wait_ns)) M.abort = 1;
+  csync();
   if (bulk && tid == 0) M.xuse += 1;
   if (tid == 0) trace_stamp(P, E.layer * NSTAGE + E.st, NW + 5);
   // Half unit h = 2 u + p of unit u: quads p and p + 2 (values 4p..4p+3 and
@@ -573,7 +589,7 @@ __device__ __noinline__ void gemv_prologue(const Params& P, const GemvCtx& E, ui
       const float r = warp_max(xm[b]);
       if (lane == 0 && b < B) M.red[warp][2 * b + 1] = r;
     }
-    __syncthreads();
+    csync();
 #pragma unroll
     for (int b = 0; b < NARROW_B; ++b) {
       xm[b] = 0.f;
@@ -656,7 +672,7 @@ __device__ __noinline__ void gemv_prologue(const Params& P, const GemvCtx& E, ui
       if (lane == 0 && b < B) M.red[warp][2 * b] = r;
     }
   }
-  __syncthreads();
+  csync();
   if (tid < B) {
     float ss = 0.f;
     if (nw)
@@ -664,7 +680,7 @@ __device__ __noinline__ void gemv_prologue(const Params& P, const GemvCtx& E, ui
     M.rnorm[tid] = nw ? 1.0f / sqrtf(ss / (float)K + P.eps) : 1.0f;
   }
   if (tid == 0) trace_stamp(P, E.layer * NSTAGE + E.st, NW + 6);
-  __syncthreads();
+  csync();
 }
 
 // ------------------------------------------------------------------ GEMV epilogues
@@ -852,7 +868,7 @@ __device__ __noinline__ void owner_fixup(const Params& P, const GemvCtx& E, int 
       if (!(w0 | w1) || (it & 63u) != 0) continue;
       const uint64_t now = globaltimer();
       if (tw == 0) tw = now;
-      else if (now - tw > WAIT_LIMIT_NS) {
+      else if (now - tw > P.wait_ns) {
         atomicExch(P.ctrl + 1, STATUS_TIMEOUT);
         M.abort = 1;
         break;
@@ -985,39 +1001,117 @@ __device__ __noinline__ void gemv_prep(const Params& P, int layer, int st, uint8
   }
 }
 
+// One ring slot of a narrow-batch GEMV stage: nb blocks (groups gi.. of one
+// (k-chunk, tile) unit) as PER independent MMA chains for latency hiding: the
+// codes, scales and sums of x of every block first, then per k-slice j the
+// blocks' x fragments and their MMAs in block order, so that consecutive MMAs
+// accumulate into different blocks.  A FULL slot has PER blocks; in a partial
+// one, blocks i >= nb get zero x fragments (and zero scale and sum of x), so
+// they add nothing whatever stale codes the slot holds.  When another slot
+// follows (`more`), its wait is made while this slot's MMAs drain.
+template <int WT, int NB, bool FULL, class Wait>
+__device__ __forceinline__ bool gemv_slot(const Params& P, const Ring& R, uint32_t xb, uint32_t xz, uint32_t sb,
+                                          int lane, int g, int nb, bool more, float& acc0, float& acc1,
+                                          Wait& wait_slot) {
+  constexpr int PER = WT == DDL_W_INT4 ? BLKS_PER_SLOT : BF16_BLKS_PER_SLOT;
+  constexpr uint32_t jstride = 2 * NB * 32, gstride = 4 * jstride;
+  const uint32_t slot = R.slot();
+  if (WT == DDL_W_INT4) {
+    float c[PER][4];
+    uint4 wv[PER];
+    uint32_t sc[PER], xi[PER];
+    float sx[PER];
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+      c[i][0] = c[i][1] = c[i][2] = c[i][3] = 0.f;
+      xi[i] = FULL || i < nb ? xb + i * gstride : xz;  // past the slot's end: zeros
+      wv[i] = lds128(slot + i * QBLK_BYTES + lane * 16);
+      const uint32_t scw = lds32(slot + i * QBLK_BYTES + BLK_BYTES + g * 4);
+      const float sxv = lds_f32(sb + i * (NARROW_B * 4));
+      sc[i] = FULL || i < nb ? scw : 0u;  // stale scale and sum words are finite-safe only as 0
+      sx[i] = FULL || i < nb ? sxv : 0.f;
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      uint2 bx[PER];
+#pragma unroll
+      for (int i = 0; i < PER; ++i) bx[i] = lds64(xi[i] + j * jstride);
+#pragma unroll
+      for (int i = 0; i < PER; ++i) {
+        const uint32_t w = j == 0 ? wv[i].x : j == 1 ? wv[i].y : j == 2 ? wv[i].z : wv[i].w;
+        const uint32_t w8 = w >> 8;
+        const uint32_t a0 = lop3_merge(w, 0x000F000Fu, 0x64086408u);
+        const uint32_t a1 = lop3_merge(w, 0x00F000F0u, 0x64806480u);
+        const uint32_t a2 = lop3_merge(w8, 0x000F000Fu, 0x64086408u);
+        const uint32_t a3 = lop3_merge(w8, 0x00F000F0u, 0x64806480u);
+        // lanes g >= 2B read unrelated fragments: they only feed C columns >= 2B, never used
+        mma_f16(c[i], a0, a1, a2, a3, bx[i].x, bx[i].y);
+      }
+    }
+    if (more && !wait_slot(R.next())) return false;
+    // rows g hold 1024 + (q+8), rows g+8 hold 1024 + 16 (q+8):
+    // sum q x = v - 1032 Sx  and  (v - 1152 Sx) / 16
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+      acc0 = fmaf(bf16lo_f32(sc[i]), (c[i][0] + c[i][1]) - 1032.f * sx[i], acc0);
+      acc1 = fmaf(bf16hi_f32(sc[i]) * 0.0625f, (c[i][2] + c[i][3]) - 1152.f * sx[i], acc1);
+    }
+  } else {
+    float c[PER][4];
+    uint2 bx[PER][4];
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+      c[i][0] = c[i][1] = c[i][2] = c[i][3] = 0.f;
+      const uint32_t xi = FULL || i < nb ? xb + i * gstride : xz;  // past the slot's end: zeros
+#pragma unroll
+      for (int j = 0; j < 4; ++j) bx[i][j] = lds64(xi + j * jstride);
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+#pragma unroll
+      for (int i = 0; i < PER; ++i) {  // stale bf16 codes could be NaN: zero them
+        const uint4 av = lds128(slot + i * BF16_BLK_BYTES + j * 512 + lane * 16);
+        const uint4 aq = FULL || i < nb ? av : make_uint4(0u, 0u, 0u, 0u);
+        mma_bf16(c[i], aq.x, aq.y, aq.z, aq.w, bx[i][j].x, bx[i][j].y);
+      }
+    if (more && !wait_slot(R.next())) return false;
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+      acc0 += c[i][0] + c[i][1];
+      acc1 += c[i][2] + c[i][3];
+    }
+  }
+  return true;
+}
+
 // ------------------------------------------------------------------ GEMV stage
 // The warp walks its range of the panel's work order (tile, k-chunk, group).
 // Per ring slot (up to 8 groups of one (k-chunk, tile) unit): the 8 blocks'
 // MMAs run as 8 independent chains, then fold into the unit sums; a unit's
 // sums join the tile sums in true scale, and a tile is finished when the
 // warp leaves it.
+template <int HD, int WT, int NB>
+__device__ __forceinline__ bool stage_gemv_body(const Params& P, int layer, int st, Ring& R, uint8_t* smem, Misc& M);
+// The ring lives in registers while the stage runs.
 template <int HD, int WT>
-__device__ __forceinline__ bool stage_gemv_body(const Params& P, int layer, int st, Ring& R,
-                                                Cursor& prod, int64_t wg, int64_t W, uint8_t* smem,
-                                                Misc& M, uint64_t policy);
-// The ring and the cursor live in registers while the stage runs.
+__device__ __noinline__ bool stage_gemv_wide(const Params& P, int layer, int st, Ring& Rm, uint8_t* smem, Misc& M);
 template <int HD, int WT>
-__device__ __noinline__ bool stage_gemv_wide(const Params& P, int layer, int st, Ring& Rm, Cursor& prodm,
-                                             int64_t wg, int64_t W, uint8_t* smem, Misc& M,
-                                             uint64_t policy);
-template <int HD, int WT>
-__device__ __noinline__ bool stage_gemv(const Params& P, int layer, int st, Ring& Rm, Cursor& prodm,
-                                        int64_t wg, int64_t W, uint8_t* smem, Misc& M,
-                                        uint64_t policy) {
+__device__ __noinline__ bool stage_gemv(const Params& P, int layer, int st, Ring& Rm, uint8_t* smem, Misc& M) {
   __syncwarp();
   Ring R = Rm;
-  Cursor prod = prodm;
-  const bool ok = stage_gemv_body<HD, WT>(P, layer, st, R, prod, wg, W, smem, M, policy);
+  // the batch is a template parameter of the stream, so that the x fragments'
+  // strides are constants
+  const bool ok = P.B == 1   ? stage_gemv_body<HD, WT, 1>(P, layer, st, R, smem, M)
+                  : P.B == 2 ? stage_gemv_body<HD, WT, 2>(P, layer, st, R, smem, M)
+                  : P.B == 3 ? stage_gemv_body<HD, WT, 3>(P, layer, st, R, smem, M)
+                             : stage_gemv_body<HD, WT, 4>(P, layer, st, R, smem, M);
   __syncwarp();
   Rm = R;
-  prodm = prod;
   __syncwarp();
   return ok;
 }
-template <int HD, int WT>
-__device__ __forceinline__ bool stage_gemv_body(const Params& P, int layer, int st, Ring& R,
-                                                Cursor& prod, int64_t wg, int64_t W, uint8_t* smem,
-                                                Misc& M, uint64_t policy) {
+template <int HD, int WT, int NB>
+__device__ __forceinline__ bool stage_gemv_body(const Params& P, int layer, int st, Ring& R, uint8_t* smem, Misc& M) {
   GemvCtx& E = ctx().E;  // filled by gemv_prep
   const MatGeom& m = E.m;
   gemv_prologue<HD, WT>(P, E, smem, M);
@@ -1031,7 +1125,8 @@ __device__ __forceinline__ bool stage_gemv_body(const Params& P, int layer, int 
   }
   uint32_t* pend = reinterpret_cast<uint32_t*>(smem + SM_SCR + XF_BYTES + SX_BYTES) + warp * 32;
   int npend = 0;
-  const int B = P.B, B2 = 2 * B, Sk = m.Sk, pk0 = m.pk[E.p], pk1 = m.pk[E.p + 1];
+  constexpr int B = NB, B2 = 2 * B;
+  const int Sk = m.Sk, pk0 = m.pk[E.p], pk1 = m.pk[E.p + 1];
   const uint32_t jstride = B2 * 32, gstride = 4 * jstride, kstride = GC * gstride;
   const uint32_t xf_lane = smem_addr(smem + SM_SCR) + (g * 4 + t) * 8;
   const uint32_t xz = smem_addr(smem + SM_SCR + XZ_OFF) + (g * 4 + t) * 8;
@@ -1042,94 +1137,48 @@ __device__ __forceinline__ bool stage_gemv_body(const Params& P, int layer, int 
   uint32_t nblk = 0;
   int nown = 0, oT0 = 0, oT1 = 0;  // tiles this warp owns (cooperative launch), finished at the end
   float oa0 = 0.f, ob0 = 0.f, oa1 = 0.f, ob1 = 0.f;
+  uint64_t wcyc = 0;  // traced: cycles waiting for the ring, slots consumed
+  uint32_t nslots = 0;
+  const bool tr = P.trace != nullptr;
   constexpr int PER = WT == DDL_W_INT4 ? BLKS_PER_SLOT : BF16_BLKS_PER_SLOT;
-  for (uint32_t b = lo; b < hi;) {
-    // a slot holds nb consecutive groups gi.. of unit (kc, T) (see cursor_next)
-    int nb = (int)(hi - b < (uint32_t)PER ? hi - b : (uint32_t)PER);
-    if (nb > gk - gi) nb = gk - gi;
-    const uint32_t slot = R.slot(R.n_done);
-    if (!mbar_wait_warp(R.bar(R.n_done), R.parity(R.n_done), P.ctrl + 1)) {
+  const int glast = m.G - (Sk - 1) * m.Gc, Gc = m.Gc;  // groups of the last / other k-chunks
+  // The wait for slot k + 1 is made while slot k's MMAs drain (after its
+  // k-slice loop), so that a slot boundary costs no pipeline bubble.
+  auto wait_slot = [&](const Ring& r) -> bool {
+    const uint64_t tw = tr ? clock64() : 0;
+    if (!mbar_wait_warp(r.bar(), r.phase, P.ctrl + 1, P.wait_ns)) {
       M.abort = 1;
       return false;
     }
+    if (tr) wcyc += clock64() - tw;
+    return true;
+  };
+  if (!wait_slot(R)) return false;
+  // The producer cuts a unit (k-chunk kc, tile T) of the warp's range into
+  // slots of PER groups from the range's first group in the unit, and a last
+  // partial slot; full slots take the lean path.
+  for (uint32_t b = lo; b < hi;) {
+    int ng = gk - gi;  // groups of this unit in the range
+    if (hi - b < (uint32_t)ng) ng = (int)(hi - b);
     const int kcl = kc - pk0;
-    const uint32_t xb = xf_lane + kcl * kstride + gi * gstride;
-    const uint32_t sb = sx_lane + ((kcl * GC + gi) * NARROW_B) * 4;
-    // The slot's blocks (PER independent MMA chains for latency hiding: with
-    // one CTA of 8 warps per SM each warp's slot time is its dependency
-    // chains, not issue bandwidth): all shared loads first, then the MMAs in
-    // (j, block) order so that consecutive MMAs accumulate into different
-    // blocks.  Blocks i >= nb get zero x fragments
-    // (and zero scale and sum of x), so they add nothing whatever stale codes
-    // the slot holds.
-    constexpr int HB = PER;
+    uint32_t xb = xf_lane + kcl * kstride + gi * gstride;
+    uint32_t sb = sx_lane + ((kcl * GC + gi) * NARROW_B) * 4;
 #pragma unroll 1
-    for (int h0 = 0; h0 < PER; h0 += HB) {
-      float c[HB][4];
-      uint2 bx[HB][4];
-#pragma unroll
-      for (int ii = 0; ii < HB; ++ii) {
-        const int i = h0 + ii;
-        c[ii][0] = c[ii][1] = c[ii][2] = c[ii][3] = 0.f;
-        const uint32_t xi = i < nb ? xb + i * gstride : xz;  // past the slot's end: zeros
-#pragma unroll
-        for (int j = 0; j < 4; ++j) bx[ii][j] = lds64(xi + j * jstride);
-      }
-      if (WT == DDL_W_INT4) {
-        uint4 wv[HB];
-        uint32_t sc[HB];
-        float sx[HB];
-#pragma unroll
-        for (int ii = 0; ii < HB; ++ii) {
-          const int i = h0 + ii;
-          wv[ii] = lds128(slot + i * QBLK_BYTES + lane * 16);
-          const uint32_t scw = lds32(slot + i * QBLK_BYTES + BLK_BYTES + g * 4);
-          const float sxv = lds_f32(sb + i * (NARROW_B * 4));
-          sc[ii] = i < nb ? scw : 0u;  // stale scale and sum words are finite-safe only as 0
-          sx[ii] = i < nb ? sxv : 0.f;
-        }
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-#pragma unroll
-          for (int ii = 0; ii < HB; ++ii) {
-            const uint32_t w = j == 0 ? wv[ii].x : j == 1 ? wv[ii].y : j == 2 ? wv[ii].z : wv[ii].w;
-            const uint32_t w8 = w >> 8;
-            const uint32_t a0 = lop3_merge(w, 0x000F000Fu, 0x64086408u);
-            const uint32_t a1 = lop3_merge(w, 0x00F000F0u, 0x64806480u);
-            const uint32_t a2 = lop3_merge(w8, 0x000F000Fu, 0x64086408u);
-            const uint32_t a3 = lop3_merge(w8, 0x00F000F0u, 0x64806480u);
-            // lanes g >= 2B read unrelated fragments: they only feed C columns >= 2B, never used
-            mma_f16(c[ii], a0, a1, a2, a3, bx[ii][j].x, bx[ii][j].y);
-          }
-        }
-        // rows g hold 1024 + (q+8), rows g+8 hold 1024 + 16 (q+8):
-        // sum q x = v - 1032 Sx  and  (v - 1152 Sx) / 16
-#pragma unroll
-        for (int ii = 0; ii < HB; ++ii) {
-          acc0 = fmaf(bf16lo_f32(sc[ii]), (c[ii][0] + c[ii][1]) - 1032.f * sx[ii], acc0);
-          acc1 = fmaf(bf16hi_f32(sc[ii]) * 0.0625f, (c[ii][2] + c[ii][3]) - 1152.f * sx[ii], acc1);
-        }
-      } else {
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-#pragma unroll
-          for (int ii = 0; ii < HB; ++ii) {
-            const int i = h0 + ii;  // stale bf16 codes could be NaN: zero them
-            const uint4 av = lds128(slot + i * BF16_BLK_BYTES + j * 512 + lane * 16);
-            const uint4 aq = i < nb ? av : make_uint4(0u, 0u, 0u, 0u);
-            mma_bf16(c[ii], aq.x, aq.y, aq.z, aq.w, bx[ii][j].x, bx[ii][j].y);
-          }
-#pragma unroll
-        for (int ii = 0; ii < HB; ++ii) {
-          acc0 += c[ii][0] + c[ii][1];
-          acc1 += c[ii][2] + c[ii][3];
-        }
-      }
+    for (; ng > 0;) {
+      const int nb = ng < PER ? ng : PER;
+      const bool more = b + nb < hi;  // another slot of this stage follows
+      if (tr) ++nslots;
+      const bool ok = nb == PER ? gemv_slot<WT, NB, true>(P, R, xb, xz, sb, lane, g, PER, more, acc0, acc1, wait_slot)
+                                : gemv_slot<WT, NB, false>(P, R, xb, xz, sb, lane, g, nb, more, acc0, acc1, wait_slot);
+      if (!ok) return false;
+      ring_advance(R, lane);
+      b += nb;
+      gi += nb;
+      nblk += nb;
+      ng -= nb;
+      xb += nb * gstride;
+      sb += nb * (NARROW_B * 4);
     }
-    ring_advance<HD, WT>(P, R, prod, wg, W, lane, policy);
-    b += nb;
-    gi += nb;
-    nblk += nb;
     if (gi == gk) {  // end of the unit: its sums join the tile's
       tac0 = fmaf(acc0, esc, tac0);
       tac1 = fmaf(acc1, esc, tac1);
@@ -1142,7 +1191,7 @@ __device__ __forceinline__ bool stage_gemv_body(const Params& P, int layer, int 
         kc = pk0;
         ++T;
       }
-      gk = kc < Sk ? chunk_groups(m, kc) : 1;
+      gk = kc < Sk - 1 ? Gc : kc == Sk - 1 ? glast : 1;
     }
   }
   if (nblk != 0)
@@ -1151,6 +1200,7 @@ __device__ __forceinline__ bool stage_gemv_body(const Params& P, int layer, int 
   if (npend) gemv_publish<HD>(P, E, pend, npend, M);
   if (nown > 0) owner_fixup<HD>(P, E, nown, oT0, en.omask[0], oa0, ob0, oT1, en.omask[1], oa1, ob1, M);
   if (lane == 0) trace_stamp(P, layer * NSTAGE + st, 2 + warp);
+  trace_ring(P, layer * NSTAGE + st, wcyc, nslots);
   return true;
 }
 
@@ -1190,7 +1240,7 @@ __device__ __noinline__ void gemv_prologue_wide(const Params& P, const GemvCtx& 
   const bool whole = nkc == m.Sk;
   const bool have_max = !(E.st == ST_QKV && E.layer == 0);
   uint8_t* nws = smem + SM_NW;
-  __syncthreads();
+  csync();
   float xm = 0.f;
   if (have_max && tid < B) xm = __uint_as_float(__ldcg(P.xmax + (E.layer * NSTAGE + E.st) * MAX_B + tid));
   if (nw && !whole) {
@@ -1206,7 +1256,7 @@ __device__ __noinline__ void gemv_prologue_wide(const Params& P, const GemvCtx& 
     }
   }
   cp_async_wait_all();
-  __syncthreads();
+  csync();
   // item it = ((group slot * B + b) * 16 + quad): four columns of sequence b, read from memory
 #define WIDE_X(it_, gs_, b_, q16_)                                                                         \
   (x32 ? __ldcg(reinterpret_cast<const float4*>(x32 + (int64_t)(b_) * K + kbase + (gs_) * DDL_GROUP) + (q16_)) \
@@ -1227,7 +1277,7 @@ __device__ __noinline__ void gemv_prologue_wide(const Params& P, const GemvCtx& 
       mx = warp_max(mx);
       if (lane == 0) M.red[warp][2 * b + 1] = mx;
     }
-    __syncthreads();
+    csync();
     if (tid < B)
       for (int w = 0; w < NW; ++w) xm = fmaxf(xm, M.red[w][2 * tid + 1]);
   }
@@ -1236,7 +1286,7 @@ __device__ __noinline__ void gemv_prologue_wide(const Params& P, const GemvCtx& 
     M.escale[tid] = ldexpf(1.0f, e);
     M.edown[tid] = ldexpf(1.0f, -e);
   }
-  __syncthreads();
+  csync();
   // fragments (fp16 of x * w * 2^-e) and the sum of x per (group, sequence);
   // the sum of squares per sequence when the panel is the whole vector
   uint32_t* xf = reinterpret_cast<uint32_t*>(smem + SM_SCR);
@@ -1301,14 +1351,14 @@ __device__ __noinline__ void gemv_prologue_wide(const Params& P, const GemvCtx& 
   }
 #undef WIDE_X
   for (int i = tid; i < XZ_BYTES / 4; i += NTHREADS) reinterpret_cast<uint32_t*>(smem + SM_SCR + XZ_OFF)[i] = 0u;
-  __syncthreads();
+  csync();
   if (tid < B) {
     float ss = 0.f;
     if (nw)
       for (int w = 0; w < NW; ++w) ss += M.red[w][2 * tid];
     M.rnorm[tid] = nw ? 1.0f / sqrtf(ss / (float)K + P.eps) : 1.0f;
   }
-  __syncthreads();
+  csync();
 }
 
 // Split tiles of a wide batch: 8 values per lane, float4 x 2 at [slot][lane].
@@ -1356,7 +1406,7 @@ __device__ __noinline__ void wide_owner_fixup(const Params& P, const GemvCtx& E,
       if ((it & 255u) != 0) continue;
       const uint64_t now = globaltimer();
       if (t0 == 0) t0 = now;
-      else if (now - t0 > WAIT_LIMIT_NS) {
+      else if (now - t0 > P.wait_ns) {
         atomicExch(P.ctrl + 1, STATUS_TIMEOUT);
         M.abort = 1;
         break;
@@ -1442,12 +1492,9 @@ __device__ __forceinline__ void wide_tile_finish(const Params& P, const GemvCtx&
 }
 
 template <int HD, int WT>
-__device__ __noinline__ bool stage_gemv_wide(const Params& P, int layer, int st, Ring& Rm, Cursor& prodm,
-                                             int64_t wg, int64_t W, uint8_t* smem, Misc& M,
-                                             uint64_t policy) {
+__device__ __noinline__ bool stage_gemv_wide(const Params& P, int layer, int st, Ring& Rm, uint8_t* smem, Misc& M) {
   __syncwarp();
   Ring R = Rm;
-  Cursor prod = prodm;
   GemvCtx& E = ctx().E;  // filled by gemv_prep
   const MatGeom& m = E.m;
   gemv_prologue_wide<HD, WT>(P, E, smem, M);
@@ -1483,8 +1530,8 @@ __device__ __noinline__ bool stage_gemv_wide(const Params& P, int layer, int st,
     for (uint32_t b = lo; b < hi;) {
       int nb = (int)(hi - b < (uint32_t)PER ? hi - b : (uint32_t)PER);
       if (nb > gk - gi) nb = gk - gi;
-      const uint32_t slot = R.slot(R.n_done);
-      if (!mbar_wait_warp(R.bar(R.n_done), R.parity(R.n_done), P.ctrl + 1)) {
+      const uint32_t slot = R.slot();
+      if (!mbar_wait_warp(R.bar(), R.phase, P.ctrl + 1, P.wait_ns)) {
         M.abort = 1;
         ok = false;
         break;
@@ -1569,7 +1616,7 @@ __device__ __noinline__ bool stage_gemv_wide(const Params& P, int layer, int st,
             for (int k = 0; k < 8; ++k) acc[k] += c[ii][k >> 2][k & 3];
         }
       }
-      ring_advance<HD, WT>(P, R, prod, wg, W, lane, policy);
+      ring_advance(R, lane);
       b += nb;
       gi += nb;
       nblk += nb;
@@ -1606,7 +1653,6 @@ __device__ __noinline__ bool stage_gemv_wide(const Params& P, int layer, int st,
   if (lane == 0) trace_stamp(P, layer * NSTAGE + st, 2 + warp);
   __syncwarp();
   Rm = R;
-  prodm = prod;
   __syncwarp();
   return ok;
 }
@@ -1705,7 +1751,7 @@ __device__ __noinline__ void merge_sequence(const Params& P, int64_t seq, int64_
     for (int j = lane; j < n; j += 32) fac[warp * P.J_att + j] /= l;
   }
   cp_async_wait_all();
-  __syncthreads();
+  csync();
   const int64_t b = seq / P.Hkv, kvh = seq % P.Hkv;
   if (act) {
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -1735,7 +1781,7 @@ __device__ __noinline__ void merge_sequence(const Params& P, int64_t seq, int64_
     const float m = fmaxf(fmaxf(fabsf(acc.x), fabsf(acc.y)), fmaxf(fabsf(acc.z), fabsf(acc.w)));
     atomicMax(&M.cmax[b], __float_as_uint(m));  // the Wo stage scales its staged x by this
   }
-  __syncthreads();
+  csync();
 }
 
 // Write one warp's softmax state (m, l, o) for its current sequence segment:
@@ -1761,27 +1807,19 @@ __device__ __forceinline__ void att_flush(const Params& P, float* rec, const flo
 }
 
 template <int HD, int WT>
-__device__ __forceinline__ bool stage_att_body(const Params& P, int layer, Ring& R, Cursor& prod,
-                                               int64_t wg, int64_t W, uint8_t* smem, Misc& M,
-                                               uint64_t policy);
+__device__ __forceinline__ bool stage_att_body(const Params& P, int layer, Ring& R, uint8_t* smem, Misc& M);
 template <int HD, int WT>
-__device__ __noinline__ bool stage_att(const Params& P, int layer, Ring& Rm, Cursor& prodm,
-                                       int64_t wg, int64_t W, uint8_t* smem, Misc& M,
-                                       uint64_t policy) {
+__device__ __noinline__ bool stage_att(const Params& P, int layer, Ring& Rm, uint8_t* smem, Misc& M) {
   __syncwarp();
   Ring R = Rm;
-  Cursor prod = prodm;
-  const bool ok = stage_att_body<HD, WT>(P, layer, R, prod, wg, W, smem, M, policy);
+  const bool ok = stage_att_body<HD, WT>(P, layer, R, smem, M);
   __syncwarp();
   Rm = R;
-  prodm = prod;
   __syncwarp();
   return ok;
 }
 template <int HD, int WT>
-__device__ __forceinline__ bool stage_att_body(const Params& P, int layer, Ring& R, Cursor& prod,
-                                               int64_t wg, int64_t W, uint8_t* smem, Misc& M,
-                                               uint64_t policy) {
+__device__ __forceinline__ bool stage_att_body(const Params& P, int layer, Ring& R, uint8_t* smem, Misc& M) {
   constexpr int KS = HD / 16, NB = HD / 8;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
   const int GH = P.GH, REC = att_rec_floats(GH, HD), nt = P.nt_att;
@@ -1796,7 +1834,9 @@ __device__ __forceinline__ bool stage_att_body(const Params& P, int layer, Ring&
   uint32_t qa[KS][4];
   float mrun = -INFINITY, lrun = 0.f;
   float o[NB][4];
-  bool ok = true;
+  bool ok = true, kready = false;
+  uint64_t wcyc = 0;  // traced: cycles waiting for the ring, slots consumed
+  uint32_t nslots = 0;
 
   for (int64_t it = lo; it < hi && ok; ++it) {
     const int64_t seq = (uint32_t)it / (uint32_t)nt;
@@ -1835,29 +1875,35 @@ __device__ __forceinline__ bool stage_att_body(const Params& P, int layer, Ring&
 #pragma unroll
       for (int nb = 0; nb < NB; ++nb) o[nb][0] = o[nb][1] = o[nb][2] = o[nb][3] = 0.f;
     }
-    const uint32_t ks = R.slot(R.n_done), vs = R.slot(R.n_done + 1);
-    if (!mbar_wait_warp(R.bar(R.n_done), R.parity(R.n_done), P.ctrl + 1) ||
-        !mbar_wait_warp(R.bar(R.n_done + 1), R.parity(R.n_done + 1), P.ctrl + 1)) {
-      M.abort = 1;
-      ok = false;
-      break;
-    }
-    if (i == nt - 1) {  // the tile holding the new token: its row from the cache, zero rows after it
-      const int rnew = (int)(P.pos - 16 * (int64_t)i);
-      const int b = (int)(seq / P.Hkv), kvh = (int)(seq % P.Hkv);
-      const int64_t ro = (((int64_t)b * P.Hkv + kvh) * P.s_max + P.pos) * HD;
-      if (lane < HD / 8) sts128(kv_addr(ks, rnew, lane), ldcg_u128(Ld.kc + ro + lane * 8));
-      else if (lane >= 16 && lane < 16 + HD / 8)
-        sts128(kv_addr(vs, rnew, lane - 16), ldcg_u128(Ld.vc + ro + (lane - 16) * 8));
-      const int nz = (15 - rnew) * (HD / 8);
-      for (int z = lane; z < 2 * nz; z += 32) {
-        const int zz = z % nz, row = rnew + 1 + zz / (HD / 8), col = zz % (HD / 8);
-        sts128(kv_addr(z < nz ? ks : vs, row, col), make_uint4(0u, 0u, 0u, 0u));
+    // K of this tile in slot R, V in the slot after it.  The K slot goes back
+    // to the producer once the scores are computed, and the wait for the
+    // next tile's K is made while the P.V MMAs drain.
+    const uint32_t ks = R.slot();
+    if (!kready) {
+      const uint64_t tw = P.trace ? clock64() : 0;
+      if (!mbar_wait_warp(R.bar(), R.phase, P.ctrl + 1, P.wait_ns)) {
+        M.abort = 1;
+        ok = false;
+        break;
       }
-      // these generic writes come before the slots' next bulk (async-proxy) fill
+      if (P.trace) wcyc += clock64() - tw;
+    }
+    if (P.trace) nslots += 2;
+    const bool newtok = i == nt - 1;  // the tile holding the new token
+    const int rnew = (int)(P.pos - 16 * (int64_t)i);
+    const int64_t ro = ((seq * P.s_max) + P.pos) * HD;  // its row in the cache ([seq][s_max][hd])
+    // the new token's row from the cache (written by the QKV stage after the
+    // copy may have been made) and zero rows after it; these generic writes
+    // come before the slot's next bulk (async-proxy) fill
+    auto patch = [&](uint32_t sl, const uint16_t* cache) {
+      if (lane < HD / 8) sts128(kv_addr(sl, rnew, lane), ldcg_u128(cache + ro + lane * 8));
+      const int nz = (15 - rnew) * (HD / 8);
+      for (int z = lane; z < nz; z += 32)
+        sts128(kv_addr(sl, rnew + 1 + z / (HD / 8), z % (HD / 8)), make_uint4(0u, 0u, 0u, 0u));
       fence_proxy_async_smem();
       __syncwarp();
-    }
+    };
+    if (newtok) patch(ks, Ld.kc);
     // scores: rows g = high-part dot products, rows g+8 = low-part ones
     float s[2][4];
 #pragma unroll
@@ -1872,6 +1918,18 @@ __device__ __forceinline__ bool stage_att_body(const Params& P, int layer, Ring&
         mma_bf16(s[n], qa[jj + 1][0], qa[jj + 1][1], qa[jj + 1][2], qa[jj + 1][3], b2, b3);
       }
     }
+    ring_advance(R, lane);  // the K slot: its rows are in registers now
+    const uint32_t vs = R.slot();
+    {
+      const uint64_t tw = P.trace ? clock64() : 0;
+      if (!mbar_wait_warp(R.bar(), R.phase, P.ctrl + 1, P.wait_ns)) {
+        M.abort = 1;
+        ok = false;
+        break;
+      }
+      if (P.trace) wcyc += clock64() - tw;
+    }
+    if (newtok) patch(vs, Ld.vc);
     // online softmax over this tile (score of key 8n + 2t + e = s[n][e] + s[n][e+2])
     float sv[2][2];
     float mt = -INFINITY;
@@ -1917,17 +1975,29 @@ __device__ __forceinline__ bool stage_att_body(const Params& P, int layer, Ring&
       mma_bf16(o[nb], pa0, pa1, pa2, pa3, b0, b1);
       mma_bf16(o[nb + 1], pa0, pa1, pa2, pa3, b2, b3);
     }
-    ring_advance<HD, WT>(P, R, prod, wg, W, lane, policy);
-    ring_advance<HD, WT>(P, R, prod, wg, W, lane, policy);
+    kready = false;
+    if (it + 1 < hi) {  // the next tile's K, while these MMAs drain
+      const Ring Rk = R.next();
+      const uint64_t tw = P.trace ? clock64() : 0;
+      if (!mbar_wait_warp(Rk.bar(), Rk.phase, P.ctrl + 1, P.wait_ns)) {
+        M.abort = 1;
+        ok = false;
+        break;
+      }
+      if (P.trace) wcyc += clock64() - tw;
+      kready = true;
+    }
+    ring_advance(R, lane);  // the V slot
   }
   if (ok && nseg > 0) att_flush<HD>(P, recs + (warp * 2 + (nseg == 1 ? 0 : 1)) * REC, o, mrun, lrun);
   if (lane == 0) trace_stamp(P, layer * NSTAGE + ST_ATT, 2 + warp);
+  trace_ring(P, layer * NSTAGE + ST_ATT, wcyc, nslots);
   if (lane == 0) {
     M.seg_n[warp] = ok ? nseg : 0;
     M.seg_first[warp] = first_seq;
     M.seg_last[warp] = cur;
   }
-  __syncthreads();
+  csync();
   if (M.abort) return false;
   // CTA merge: runs of consecutive warp records of one sequence (found by
   // thread 0), each merged head by head with the heads spread over the warps
@@ -1955,12 +2025,12 @@ __device__ __forceinline__ bool stage_att_body(const Params& P, int layer, Ring&
       M.run_out[r] = (M.run_seq[r] * P.J_att + (blockIdx.x - A.cf[M.run_seq[r] - A.s0])) * REC;
     M.nruns = nr;
   }
-  __syncthreads();
+  csync();
   for (int r = 0; r < M.nruns; ++r)
     for (int h = warp; h < GH; h += NW)
       merge_head<HD>(recs, REC, M.run_first[r], M.run_vmask[r], P.apart + M.run_out[r], GH, h);
   // the last CTA to publish a sequence's record merges the sequence
-  __syncthreads();
+  csync();
   if (A.ns > 0) {
     const int64_t s0 = A.s0, s1 = A.s0 + A.ns - 1;
     if (threadIdx.x <= s1 - s0) {  // one thread per sequence: the arrivals in flight together
@@ -1970,7 +2040,7 @@ __device__ __forceinline__ bool stage_att_body(const Params& P, int layer, Ring&
       M.mseq[threadIdx.x] = old == n - 1 ? sq : -1;
       if (old == n - 1) P.seqcnt[sq] = 0;
     }
-    __syncthreads();
+    csync();
     float* fac = recs + NW * 2 * REC;  // per (head, record) factors of the merge
     for (int64_t sq = s0; sq <= s1; ++sq)
       if (M.mseq[(int)(sq - s0)] == sq)
@@ -1995,7 +2065,7 @@ __device__ __noinline__ void flush_cmax(const Params& P, Misc& M, int layer, int
 // polls) orders the next stage's reads after every CTA's arrival; between
 // the two the CTA prepares its next stage.
 __device__ void grid_arrive(const Params& P) {
-  __syncthreads();
+  csync();
   if (threadIdx.x == NTHREADS - 32) red_release_gpu_add(P.ctrl, 1u);  // not thread 0: see gemv_prep
 }
 __device__ bool grid_wait(const Params& P, uint32_t target, Misc& M) {
@@ -2005,43 +2075,109 @@ __device__ bool grid_wait(const Params& P, uint32_t target, Misc& M) {
       if ((it & 255u) != 0) continue;
       const uint64_t now = globaltimer();
       if (t0 == 0) t0 = now;
-      else if (now - t0 > WAIT_LIMIT_NS) {
+      else if (now - t0 > P.wait_ns) {
         atomicExch(P.ctrl + 1, STATUS_TIMEOUT);
         M.abort = 1;
         break;
       }
     }
   }
-  __syncthreads();
+  csync();
   return !M.abort;
+}
+
+// ------------------------------------------------------------------ producer
+// Lane w (< NW) of the producer warp fills consumer warp w's ring: it walks
+// the warp's slots of every stage of the launch with its own cursor and
+// issues slot n as soon as the consumer handed slot n - DEPTH back.  It polls
+// without blocking (the lanes' rings advance independently) and naps between
+// rounds that find nothing to do, stops when the consumers abort or when no
+// ring advanced for the wait limit, and before leaving waits for its copies
+// in flight, so that none lands after the CTA has gone.
+template <int HD, int WT>
+__device__ __noinline__ void producer(const Params& P, uint8_t* smem, Misc& M) {
+  const int lane = threadIdx.x & 31;
+  const uint64_t policy = policy_evict_first();
+  const uint32_t slot0 = smem_addr(smem + SM_RING + lane * DEPTH * SLOT_BYTES);
+  const uint32_t fbar0 = smem_addr(smem + SM_BARS + lane * DEPTH * 8);
+  const uint32_t ebar0 = smem_addr(smem + SM_EBARS + lane * DEPTH * 8);
+  Cursor c;
+  SlotDesc d;
+  bool have = false;
+  if (lane < NW) {
+    c.s = P.stage_begin;
+    cursor_enter<WT>(P, c, lane);
+    have = cursor_next<WT>(P, c, lane, d);
+  }
+  uint32_t n = 0;  // slots issued
+  uint64_t t0 = 0;
+  bool stop = false;
+#pragma unroll 1
+  for (uint32_t it = 1; __any_sync(FULL, have); ++it) {
+    bool moved = false;
+    if (have && (n < DEPTH || mbar_test_wait(ebar0 + (n % DEPTH) * 8, ((n / DEPTH) + 1) & 1))) {
+      issue_slot<HD, WT>(c, d, slot0 + (n % DEPTH) * SLOT_BYTES, fbar0 + (n % DEPTH) * 8, policy);
+      ++n;
+      have = cursor_next<WT>(P, c, lane, d);
+      moved = true;
+    }
+    if (__any_sync(FULL, moved)) {
+      t0 = 0;
+      continue;
+    }
+    // Nothing to issue: a short pause, so that the polling takes few issue
+    // slots from the consumer warps that share this warp's scheduler.
+    __nanosleep(PRODUCER_NAP_NS);
+    if ((it & 15u) != 0) continue;
+    if (*reinterpret_cast<volatile int*>(&M.abort)) stop = true;
+    const uint64_t now = globaltimer();
+    if (t0 == 0) t0 = now;
+    else if (now - t0 > P.wait_ns) {
+      if (lane == 0) atomicExch(P.ctrl + 1, STATUS_TIMEOUT);
+      stop = true;
+    }
+    if (__any_sync(FULL, stop)) break;
+  }
+  // copies in flight: the last DEPTH slots issued on each ring (bounded)
+  if (lane < NW) {
+    const uint64_t t1 = globaltimer();
+    for (uint32_t k = n > DEPTH ? n - DEPTH : 0; k < n; ++k)
+      while (!mbar_test_wait(fbar0 + (k % DEPTH) * 8, (k / DEPTH) & 1))
+        if (globaltimer() - t1 > P.wait_ns) break;
+  }
 }
 
 // ------------------------------------------------------------------ the kernel
 template <int HD, int WT, bool WIDE>
-__global__ void __launch_bounds__(NTHREADS, 1) decode_kernel(const __grid_constant__ Params P) {
+__global__ void __launch_bounds__(NTHREADS_ALL, 1) decode_kernel(const __grid_constant__ Params P) {
   uint8_t* smem = g_smem;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   {  // indexed parameters to shared memory (read after the barrier below)
     SParams& S = *reinterpret_cast<SParams*>(smem + SM_SPAR);
     const uint32_t* src = reinterpret_cast<const uint32_t*>(P.mg);
     uint32_t* dst = reinterpret_cast<uint32_t*>(S.mg);
-    for (int i = threadIdx.x; i < (int)(sizeof(S.mg) / 4); i += NTHREADS) dst[i] = src[i];
+    for (int i = threadIdx.x; i < (int)(sizeof(S.mg) / 4); i += NTHREADS_ALL) dst[i] = src[i];
     src = reinterpret_cast<const uint32_t*>(P.rope);
     dst = reinterpret_cast<uint32_t*>(S.rope);
-    for (int i = threadIdx.x; i < (int)(sizeof(S.rope) / 4); i += NTHREADS) dst[i] = src[i];
+    for (int i = threadIdx.x; i < (int)(sizeof(S.rope) / 4); i += NTHREADS_ALL) dst[i] = src[i];
     src = reinterpret_cast<const uint32_t*>(P.layers);
     dst = reinterpret_cast<uint32_t*>(S.layers);
     const int nw32 = P.L * (int)(sizeof(LayerDev) / 4);
-    for (int i = threadIdx.x; i < nw32; i += NTHREADS) dst[i] = src[i];
+    for (int i = threadIdx.x; i < nw32; i += NTHREADS_ALL) dst[i] = src[i];
   }
-  const int64_t W = (int64_t)gridDim.x * NW, wg = (int64_t)blockIdx.x * NW + warp;
   Misc& M = *reinterpret_cast<Misc*>(smem + SM_MISC);
-  Ring& R = ctx().ring[warp];  // warp-uniform: every lane writes the same values
-  Cursor& prod = ctx().cur[warp];
-  R.slot0 = smem_addr(smem + SM_RING + warp * DEPTH * SLOT_BYTES);
-  R.bar0 = smem_addr(smem + SM_BARS + warp * DEPTH * 8);
-  R.n_issued = R.n_done = 0;
-  if (lane < DEPTH) mbar_init(R.bar0 + lane * 8, 1);
+  if (warp < NW) {
+    Ring& R = ctx().ring[warp];  // warp-uniform: every lane writes the same values
+    R.slot0 = smem_addr(smem + SM_RING + warp * DEPTH * SLOT_BYTES);
+    R.bar0 = smem_addr(smem + SM_BARS + warp * DEPTH * 8);
+    R.ebar0 = smem_addr(smem + SM_EBARS + warp * DEPTH * 8);
+    R.idx = 0;
+    R.phase = 0;
+    if (lane < DEPTH) {
+      mbar_init(R.bar0 + lane * 8, 1);
+      mbar_init(R.ebar0 + lane * 8, 1);
+    }
+  }
   if (threadIdx.x == 0) {
     M.abort = 0;
     M.xuse = 0;
@@ -2050,56 +2186,53 @@ __global__ void __launch_bounds__(NTHREADS, 1) decode_kernel(const __grid_consta
   if (threadIdx.x < MAX_B) M.cmax[threadIdx.x] = 0u;
   mbar_init_fence();
   __syncthreads();
-  const uint64_t policy = policy_evict_first();
-  compute_entries(P);
-  __syncwarp();
-  {
-    Cursor c;
-    c.s = P.stage_begin;
-    cursor_enter<WT>(P, c);
-    Ring r = R;
-    for (int k = 0; k < DEPTH; ++k) {
-      SlotDesc d;
-      if (!cursor_next<WT>(P, c, wg, W, d)) break;
-      issue_slot<HD, WT>(P, c, d, r.slot(r.n_issued), r.bar(r.n_issued), lane, policy);
-      r.n_issued++;
+  // Roles.  A non-inlined function must not be called on both sides of the
+  // register split, so the consumers compute the work entries after theirs
+  // and publish them to the producer through barrier 2.
+  if (warp >= NW) {  // the producer warpgroup
+    regs_dec<PRODUCER_REGS>();
+    if (warp == NW) {
+      asm volatile("bar.sync 2, %0;" ::"n"(NTHREADS + 32) : "memory");
+      producer<HD, WT>(P, smem, M);
     }
-    __syncwarp();
-    prod = c;
-    R = r;
-    __syncwarp();
+    return;
   }
+  regs_inc<CONSUMER_REGS>();
+  compute_entries(P);
+  asm volatile("bar.arrive 2, %0;" ::"n"(NTHREADS + 32) : "memory");
+  Ring& R = ctx().ring[warp];
   bool ok = true;
   for (int s = P.stage_begin; s < P.stage_end && ok; ++s) {
     const int layer = s / NSTAGE, st = s % NSTAGE;
     if (st != ST_ATT) gemv_prep(P, layer, st, smem);
     if (s != P.stage_begin && P.cooperative) {
-      if (!grid_wait(P, (uint32_t)(s - P.stage_begin) * gridDim.x, M)) {
+      // (a held barrier waits for one arrival more than the grid makes: its
+      // bounded wait gives up and the call reports a timeout)
+      const uint32_t target = (uint32_t)(s - P.stage_begin) * gridDim.x + (P.l0 * NSTAGE + s == P.hold_stage);
+      if (!grid_wait(P, target, M)) {
         ok = false;
         break;
       }
     } else {
-      __syncthreads();  // the stage context
+      csync();  // the stage context
     }
     if (threadIdx.x == 0) trace_stamp(P, s, 0);
     if (st == ST_ATT) {
       if (threadIdx.x == 0) trace_stamp(P, s, 1);
-      ok = stage_att<HD, WT>(P, layer, R, prod, wg, W, smem, M, policy);
+      ok = stage_att<HD, WT>(P, layer, R, smem, M);
     } else {
-      if constexpr (WIDE) stage_gemv_wide<HD, WT>(P, layer, st, R, prod, wg, W, smem, M, policy);
-      else stage_gemv<HD, WT>(P, layer, st, R, prod, wg, W, smem, M, policy);
+      if constexpr (WIDE) stage_gemv_wide<HD, WT>(P, layer, st, R, smem, M);
+      else stage_gemv<HD, WT>(P, layer, st, R, smem, M);
     }
-    __syncthreads();
+    csync();
     if (threadIdx.x == 0) trace_stamp(P, s, NW + 2);
     if (M.abort) ok = false;
     if (threadIdx.x < P.B) flush_cmax(P, M, layer, st);
     if (P.cooperative && s + 1 < P.stage_end) grid_arrive(P);
   }
-  if (!ok) {  // let this warp's copies in flight land before the CTA exits (bounded)
-    __syncwarp();
-    const Ring r = R;
-    for (uint32_t n = r.n_done; n < r.n_issued; ++n)
-      if (!mbar_wait_warp(r.bar(n), r.parity(n), P.ctrl + 1)) break;
+  if (!ok) {
+    cp_async_wait_all();  // this thread's copies in flight (the stage preparation's) land first
+    if (threadIdx.x == 0) M.abort = 1;  // the producer stops and waits for its copies
   }
 }
 
@@ -2115,6 +2248,8 @@ struct DevInfo {
 static std::mutex g_mu;
 static DevInfo g_dev[64];
 static int g_launch_mode = 0;  // 0 automatic, 1 one launch per stage
+static uint64_t g_wait_ns = WAIT_LIMIT_NS;  // limit of every bounded device wait
+static int g_hold_stage = -1;  // test hook: the grid barrier before this flattened stage never completes
 static uint64_t* g_trace = nullptr;
 static size_t g_trace_bytes = 0;
 
@@ -2282,6 +2417,8 @@ static int decode(const ddl_shape* s, ddl_wtype wtype, const ddl_layer_w* layers
   P.D = s->D; P.Hq = s->H_q; P.Hkv = s->H_kv; P.hd = HD; P.dff = s->d_ff; P.B = B;
   P.GH = s->H_q / s->H_kv; P.eps = s->eps; P.wtype = wtype; P.rope_base = s->rope_base;
   P.pos = pos; P.s_max = s_max;
+  P.wait_ns = g_wait_ns;
+  P.hold_stage = g_hold_stage;
   P.nt_att = (int32_t)((pos + 1 + 15) / 16);
   for (int i = 0; i < HD / 2; ++i) {  // RoPE angles in fp64: pos * base^(-2i/hd)
     const double phi = (double)pos * pow(s->rope_base, -2.0 * i / (double)HD);
@@ -2345,7 +2482,7 @@ static int decode(const ddl_shape* s, ddl_wtype wtype, const ddl_layer_w* layers
       P.stage_end = nL * NSTAGE;
       P.cooperative = 1;
       void* args[] = {&P};
-      e = cudaLaunchCooperativeKernel(fn, dim3(C), dim3(NTHREADS), args, SM_TOTAL, cs);
+      e = cudaLaunchCooperativeKernel(fn, dim3(C), dim3(NTHREADS_ALL), args, SM_TOTAL, cs);
       if (e != cudaSuccess) return cuda_status(e);
     } else {
       P.cooperative = 0;
@@ -2354,7 +2491,7 @@ static int decode(const ddl_shape* s, ddl_wtype wtype, const ddl_layer_w* layers
         P.stage_end = sidx + 1;
         if (P.trace) P.trace = g_trace + (size_t)sidx * C * TRACE_WORDS;
         void* args[] = {&P};
-        e = cudaLaunchKernel(fn, dim3(C), dim3(NTHREADS), args, SM_TOTAL, cs);
+        e = cudaLaunchKernel(fn, dim3(C), dim3(NTHREADS_ALL), args, SM_TOTAL, cs);
         if (e != cudaSuccess) return cuda_status(e);
       }
     }
@@ -2416,6 +2553,17 @@ extern "C" int ddl_stack_decode(const ddl_shape* shape, ddl_wtype wtype, const d
 extern "C" int ddl_set_launch_mode(int32_t mode) {
   if (mode != 0 && mode != 1) return DDL_ERR_ARG;
   g_launch_mode = mode;
+  return DDL_OK;
+}
+
+extern "C" int ddl_set_wait_limit_ns(uint64_t ns) {
+  g_wait_ns = ns ? ns : WAIT_LIMIT_NS;
+  return DDL_OK;
+}
+
+extern "C" int ddl_test_hold_barrier(int32_t stage) {
+  if (stage < -1) return DDL_ERR_ARG;
+  g_hold_stage = stage;
   return DDL_OK;
 }
 

@@ -8,7 +8,7 @@
 namespace ddl {
 
 constexpr unsigned FULL = 0xffffffffu;
-constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;  // a bounded wait gives up after 2 s
+constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;  // default: a bounded wait gives up after 2 s
 constexpr uint32_t STATUS_TIMEOUT = 7;               // == DDL_ERR_TIMEOUT
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
@@ -42,23 +42,50 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
+// Non-blocking test of a barrier phase (the producer polls several rings).
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Plain arrival (release at CTA scope): a consumer warp hands a slot back.
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
 // Warp-uniform wait for a barrier phase; false (and the status word set) if
-// it did not complete within WAIT_LIMIT_NS.  The clock is read only every
+// it did not complete within limit_ns.  The clock is read only every
 // 1024 polls, so a wait that succeeds soon costs no timer reads.
-__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, uint32_t* status) {
+__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, uint32_t* status,
+                                               uint64_t limit_ns) {
   uint64_t t0 = 0;
   for (uint32_t it = 1;; ++it) {
     if (__all_sync(FULL, mbar_try_wait(bar, parity))) return true;
     if ((it & 1023u) == 0) {
       const uint64_t now = __shfl_sync(FULL, globaltimer(), 0);
       if (t0 == 0) t0 = now;
-      else if (now - t0 > WAIT_LIMIT_NS) {
+      else if (now - t0 > limit_ns) {
         if ((threadIdx.x & 31) == 0) atomicExch(status, STATUS_TIMEOUT);
         return false;
       }
     }
   }
 }
+
+// ---------------------------------------------------------------- roles
+// Block barrier of the consumer warps only (barrier 1, 256 threads); the
+// producer warp never takes part.
+__device__ __forceinline__ void csync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+// Per-warpgroup register budgets (all four warps of a warpgroup execute it).
+template <int N>
+__device__ __forceinline__ void regs_dec() { asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N)); }
+template <int N>
+__device__ __forceinline__ void regs_inc() { asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N)); }
 
 // ---------------------------------------------------------------- TMA (1-D bulk)
 __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,

@@ -39,8 +39,18 @@
 
 namespace ddl {
 
-constexpr int NW = 8;                 // warps per CTA (each streams its own ring)
-constexpr int NTHREADS = NW * 32;
+constexpr int NW = 8;                 // consumer warps per CTA (each consumes its own ring)
+constexpr int NTHREADS = NW * 32;     // consumer threads
+// A CTA is three warpgroups: the consumer warps (warpgroups 0 and 1) and a
+// third whose first warp fills every consumer warp's ring (its other three
+// warps leave at once).  setmaxnreg moves registers from the producer
+// warpgroup to the consumers: PRODUCER_REGS * 128 + CONSUMER_REGS * 256 must
+// not exceed the launch's 384 threads x 168 registers.
+constexpr int NTHREADS_ALL = 384;
+constexpr int PRODUCER_REGS = 40;
+constexpr int CONSUMER_REGS = 232;
+constexpr int PRODUCER_NAP_NS = 100;  // the producer's pause after a round with nothing to issue
+static_assert(PRODUCER_REGS * 128 + CONSUMER_REGS * 256 <= NTHREADS_ALL * 168, "register split");
 constexpr int DEPTH = 3;              // ring slots per warp
 constexpr int SLOT_BYTES = 4608;      // 8 INT4 blocks with their scales, or 16 KV rows (512-byte aligned)
 constexpr int BLK_BYTES = 512;        // one INT4 block: 16 rows x 64 columns
@@ -57,7 +67,7 @@ constexpr int MAX_GH = 8;             // query heads per KV head
 constexpr int NSTAGE = 5;
 constexpr int MAXP = 16;              // k-chunk panels per matrix
 constexpr int XF_CHUNKS = 8;          // k-chunks of x one CTA can stage at batch 1 (x batch size <= 8)
-constexpr int TRACE_WORDS = NW + 8;   // per (stage, CTA) in the optional trace
+constexpr int TRACE_WORDS = 2 * NW + 16;  // per (stage, CTA) in the optional trace
 
 // Floats of one attention softmax record (o[GH][hd], m[GH], l[GH]), padded
 // to 16 bytes so that records can be read as float4.
@@ -193,6 +203,8 @@ struct Params {
   int32_t cooperative;
   int32_t nt_att;       // 16-key tiles per sequence
   int32_t J_att;        // attention partial slots per sequence
+  int32_t hold_stage;   // test hook: the grid barrier before this flattened stage of the step waits for ever (-1: none)
+  uint64_t wait_ns;     // limit of every bounded wait
   float rope[64][2];    // cos, sin of pos * base^(-2i/hd), i < hd/2 (computed in fp64 on the host)
   MatGeom mg[4];
   const float* resid_in;

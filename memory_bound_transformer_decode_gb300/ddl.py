@@ -22,7 +22,8 @@ STATUS = {0: "DDL_OK", 1: "DDL_ERR_SHAPE", 2: "DDL_ERR_POS", 3: "DDL_ERR_ALIGN",
           7: "DDL_ERR_TIMEOUT", 8: "DDL_ERR_ARG"}
 EXPORTED = ("ddl_quantize_int4", "ddl_packed_layer_bytes", "ddl_pack_layer", "ddl_kv_append",
             "ddl_workspace_bytes", "ddl_workspace_view", "ddl_layer_decode", "ddl_stack_decode",
-            "ddl_stack_decode_noalloc", "ddl_set_launch_mode", "ddl_set_trace", "ddl_read_device_status", "ddl_status_string",
+            "ddl_stack_decode_noalloc", "ddl_set_launch_mode", "ddl_set_wait_limit_ns",
+            "ddl_test_hold_barrier", "ddl_set_trace", "ddl_read_device_status", "ddl_status_string",
             "ddl_last_cuda_error")
 
 
@@ -101,6 +102,8 @@ def load(build_if_missing: bool = False):
         lib.ddl_stack_decode_noalloc.argtypes = [P(Shape), ctypes.c_int, P(LayerW), P(KV), i32, i32,
                                                  i64, vp, vp, vp, vp, vp]
         lib.ddl_set_launch_mode.argtypes = [i32]
+        lib.ddl_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
+        lib.ddl_test_hold_barrier.argtypes = [i32]
         lib.ddl_set_trace.argtypes = [vp, sz]
         lib.ddl_read_device_status.argtypes = [vp, P(Shape), i32, i64, P(i32), vp]
         lib.ddl_status_string.argtypes = [ctypes.c_int]
@@ -268,6 +271,17 @@ def ddl_layer_decode(shape: Shape, wtype: int, layer: dict, kv: tuple, pos: int,
 
 def ddl_set_launch_mode(mode: int):
     _check("ddl_set_launch_mode", load().ddl_set_launch_mode(mode))
+
+
+def ddl_set_wait_limit_ns(ns: int):
+    """Limit of every bounded device wait (0: the default of 2 s)."""
+    _check("ddl_set_wait_limit_ns", load().ddl_set_wait_limit_ns(int(ns)))
+
+
+def ddl_test_hold_barrier(stage: int):
+    """Test hook: hold the grid barrier in front of flattened stage `stage`
+    (-1: off), so that the bounded waits give up and report a timeout."""
+    _check("ddl_test_hold_barrier", load().ddl_test_hold_barrier(int(stage)))
 
 
 def ddl_set_trace(buf: torch.Tensor | None):

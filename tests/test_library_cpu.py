@@ -75,6 +75,10 @@ def test_shape_rules(lib):
 def test_host_argument_checks(lib):
     assert lib.ddl_set_launch_mode(7) == 8
     assert lib.ddl_set_launch_mode(0) == 0
+    assert lib.ddl_test_hold_barrier(-2) == 8
+    assert lib.ddl_test_hold_barrier(-1) == 0
+    assert lib.ddl_set_wait_limit_ns(5_000_000) == 0
+    assert lib.ddl_set_wait_limit_ns(0) == 0
     assert lib.ddl_quantize_int4(None, 4, 64, None, None, None) == 8
     kv = ddl.KV(16, 16, 10)
     assert lib.ddl_kv_append(ctypes.byref(kv), 1, 1, 64, 10, ctypes.c_void_p(16),
