@@ -38,7 +38,7 @@ extern "C" {
 #endif
 
 #define DDL_GROUP 64      /* INT4 scale group along the input dimension K */
-#define DDL_MAX_BATCH 16  /* sequences per step (bf16 weights: 4) */
+#define DDL_MAX_BATCH 64  /* sequences per step */
 #define DDL_MAX_GROUP_HEADS 8 /* H_q / H_kv */
 
 typedef enum {
@@ -149,8 +149,12 @@ typedef struct {
 } ddl_ws_view;
 int ddl_workspace_view(const ddl_shape* shape, int32_t B, int64_t s_max, ddl_ws_view* out);
 
-/* One decode step of one layer for B <= DDL_MAX_BATCH sequences (INT4
- * weights; bf16 weights: B <= 4, else DDL_ERR_UNSUPPORTED), all at position pos:
+/* One decode step of one layer for B <= DDL_MAX_BATCH sequences, all at
+ * position pos.  INT4 weights at B >= 16 and bf16 weights at B >= 5 run their
+ * matrix products on the tcgen05 tensor cores (weights as fp16 code * scale,
+ * exact for group scales in [2^-17, 9357]; bf16 weights converted to fp16,
+ * exact for |w| >= 2^-17; activations as three fp16 limbs), smaller batches on
+ * warp-level tensor-core MMAs inside one persistent kernel.  The step:
  * writes KV slot pos and attends over slots 0..pos (the caller keeps slots
  * < pos filled).  Input: resid_in [B][D] fp32, or x_bf16 [B][D] bf16 when
  * resid_in is NULL.  Output: resid_out [B][D] fp32 (may be NULL) and

@@ -35,6 +35,7 @@
 
 #include "ddl_device.cuh"
 #include "ddl_internal.h"
+#include "ddl_tc.h"
 
 namespace ddl {
 
@@ -1779,7 +1780,7 @@ __device__ __noinline__ void merge_sequence(const Params& P, int64_t seq, int64_
     float* dst = P.attn + b * P.Hq * HD + (kvh * GH + h) * HD;
     reinterpret_cast<float4*>(dst)[dq] = acc;
     const float m = fmaxf(fmaxf(fabsf(acc.x), fabsf(acc.y)), fmaxf(fabsf(acc.z), fabsf(acc.w)));
-    atomicMax(&M.cmax[b], __float_as_uint(m));  // the Wo stage scales its staged x by this
+    if (b < MAX_B) atomicMax(&M.cmax[b], __float_as_uint(m));  // the Wo stage scales its staged x by this
   }
   csync();
 }
@@ -2227,7 +2228,7 @@ __global__ void __launch_bounds__(NTHREADS_ALL, 1) decode_kernel(const __grid_co
     csync();
     if (threadIdx.x == 0) trace_stamp(P, s, NW + 2);
     if (M.abort) ok = false;
-    if (threadIdx.x < P.B) flush_cmax(P, M, layer, st);
+    if (threadIdx.x < P.B && threadIdx.x < MAX_B) flush_cmax(P, M, layer, st);
     if (P.cooperative && s + 1 < P.stage_end) grid_arrive(P);
   }
   if (!ok) {
@@ -2292,7 +2293,7 @@ static int device_info(DevInfo& out) {
 }
 
 struct WsLayout {
-  int64_t ctrl, cnt, seqcnt, xmax, gpart, apart, Z, q, attn, y, a, total;
+  int64_t ctrl, cnt, seqcnt, xmax, gpart, apart, Z, q, attn, y, a, tc, total;
 };
 
 static int64_t att_J(int64_t seqs, int64_t nt, int64_t C) {
@@ -2330,6 +2331,8 @@ static void ws_layout(const ddl_shape& s, int B, int64_t s_max, int C, const Mat
   w.attn = off;  off = align256(off + (int64_t)B * Nq * 4);
   w.y = off;     off = align256(off + (int64_t)B * s.D * 4);
   w.a = off;     off = align256(off + (int64_t)B * s.d_ff * 4);
+  w.tc = off;  // the tensor-core path's partials, operand images and sums (batches past NARROW_B)
+  if (B > NARROW_B) off = align256(off + tc_workspace_bytes(s, B, DDL_W_INT4));
   w.total = off;
 }
 
@@ -2381,11 +2384,12 @@ static int decode(const ddl_shape* s, ddl_wtype wtype, const ddl_layer_w* layers
   int st = check_shape(s);
   if (st) return st;
   if (!layers || !kv || L <= 0 || !workspace) return !workspace ? DDL_ERR_WORKSPACE : DDL_ERR_ARG;
-  if (B < 1 || B > MAX_B) return DDL_ERR_UNSUPPORTED;
+  if (B < 1 || B > TC_MAX_B) return DDL_ERR_UNSUPPORTED;
   if (wtype != DDL_W_INT4 && wtype != DDL_W_BF16) return DDL_ERR_UNSUPPORTED;
-  // bf16 weights need bf16 activations in the MMA; past NARROW_B sequences
-  // there is no room for their low parts, and 8 bits alone miss the tolerance
-  if (wtype == DDL_W_BF16 && B > NARROW_B) return DDL_ERR_UNSUPPORTED;
+  // the weight stages on the tcgen05 tensor cores: INT4 from TC_MIN_B
+  // sequences on, bf16 past NARROW_B (whose warp-level MMAs would need bf16
+  // activations, 8 bits, which miss the tolerance)
+  const bool use_tc = (wtype == DDL_W_INT4 && B >= TC_MIN_B) || (wtype == DDL_W_BF16 && B > NARROW_B);
   if (!resid_in && !x_bf16) return DDL_ERR_ARG;
   const int64_t s_max = kv[0].s_max;
   if ((int64_t)B * s->H_kv * s_max >= (1ll << 31)) return DDL_ERR_UNSUPPORTED;  // K/V tensor-map rows
@@ -2413,6 +2417,8 @@ static int decode(const ddl_shape* s, ddl_wtype wtype, const ddl_layer_w* layers
   st = HD == 128 ? (wtype == DDL_W_INT4 ? prepare_kernel<128, DDL_W_INT4>() : prepare_kernel<128, DDL_W_BF16>())
                  : (wtype == DDL_W_INT4 ? prepare_kernel<64, DDL_W_INT4>() : prepare_kernel<64, DDL_W_BF16>());
   if (st) return st;
+  if (use_tc && wtype == DDL_W_BF16)  // its attention stage runs on the INT4 wide-batch instance
+    if ((st = HD == 128 ? prepare_kernel<128, DDL_W_INT4>() : prepare_kernel<64, DDL_W_INT4>())) return st;
   uint8_t* ws = (uint8_t*)workspace;
   P.D = s->D; P.Hq = s->H_q; P.Hkv = s->H_kv; P.hd = HD; P.dff = s->d_ff; P.B = B;
   P.GH = s->H_q / s->H_kv; P.eps = s->eps; P.wtype = wtype; P.rope_base = s->rope_base;
@@ -2446,14 +2452,16 @@ static int decode(const ddl_shape* s, ddl_wtype wtype, const ddl_layer_w* layers
   // stay empty from stage to stage within a launch)
   if ((e = cudaMemsetAsync(ws + w.gpart, 0xFF, (size_t)(w.apart - w.gpart), cs)) != cudaSuccess)
     return cuda_status(e);
-  const bool coop = di.coop && g_launch_mode == 0;
-  const bool wide = B > NARROW_B;  // INT4 only (checked above)
+  const bool coop = di.coop && g_launch_mode == 0 && !use_tc;
+  const bool wide = B > NARROW_B;  // INT4, or only the attention stage (tensor-core path)
   void* fn = HD == 128 ? (wtype == DDL_W_INT4 ? (wide ? (void*)decode_kernel<128, DDL_W_INT4, true>
                                                       : (void*)decode_kernel<128, DDL_W_INT4, false>)
-                                              : (void*)decode_kernel<128, DDL_W_BF16, false>)
+                                              : (wide ? (void*)decode_kernel<128, DDL_W_INT4, true>
+                                                      : (void*)decode_kernel<128, DDL_W_BF16, false>))
                        : (wtype == DDL_W_INT4 ? (wide ? (void*)decode_kernel<64, DDL_W_INT4, true>
                                                       : (void*)decode_kernel<64, DDL_W_INT4, false>)
-                                              : (void*)decode_kernel<64, DDL_W_BF16, false>);
+                                              : (wide ? (void*)decode_kernel<64, DDL_W_INT4, true>
+                                                      : (void*)decode_kernel<64, DDL_W_BF16, false>));
   for (int l0 = 0; l0 < L; l0 += MAX_LAYERS) {
     const int nL = L - l0 < MAX_LAYERS ? L - l0 : MAX_LAYERS;
     P.L = nL;
@@ -2476,7 +2484,35 @@ static int decode(const ddl_shape* s, ddl_wtype wtype, const ddl_layer_w* layers
       return cuda_status(e);  // maxima are per launch (its first layer finds its own)
     if (l0 > 0 && (e = cudaMemsetAsync(ws + w.gpart, 0xFF, (size_t)(w.apart - w.gpart), cs)) != cudaSuccess)
       return cuda_status(e);
-    if (coop) {
+    if (use_tc) {  // weight stages on the tensor cores, attention by the decode kernel
+      TcLayer tl[MAX_LAYERS];
+      for (int l = 0; l < nL; ++l)
+        tl[l] = TcLayer{P.layers[l].packed, P.layers[l].norm1, P.layers[l].norm2, P.layers[l].kc, P.layers[l].vc};
+      TcRun R;
+      memset(&R, 0, sizeof R);
+      R.D = P.D; R.Hq = P.Hq; R.Hkv = P.Hkv; R.hd = HD; R.dff = P.dff; R.B = B; R.GH = P.GH;
+      R.wtype = wtype; R.C = C; R.eps = P.eps; R.pos = pos; R.s_max = s_max;
+      memcpy(R.rope, P.rope, sizeof R.rope);
+      make_geoms(*s, wtype, R.mg);
+      R.layers = tl; R.L = nL; R.l0 = l0; R.final_last = P.final_last;
+      R.resid_in = resid_in; R.x_bf16 = x_bf16; R.resid_out = resid_out; R.out_bf16 = out_bf16;
+      R.status = P.ctrl + 1; R.wait_ns = g_wait_ns;
+      R.q = P.q; R.attn = P.attn; R.y = P.y; R.a = P.a; R.Z = P.Z;
+      tc_workspace_carve(*s, B, wtype, ws + w.tc, R);
+      if ((st = tc_begin(R, stream))) return st;
+      P.cooperative = 0;
+      P.trace = nullptr;
+      for (int l = 0; l < nL; ++l) {
+        if ((st = tc_stage(R, l, ST_QKV, stream))) return st;
+        P.stage_begin = l * NSTAGE + ST_ATT;
+        P.stage_end = P.stage_begin + 1;
+        void* args[] = {&P};
+        if ((e = cudaLaunchKernel(fn, dim3(C), dim3(NTHREADS_ALL), args, SM_TOTAL, cs)) != cudaSuccess)
+          return cuda_status(e);
+        for (int stg : {ST_WO, ST_GU, ST_DOWN})
+          if ((st = tc_stage(R, l, stg, stream))) return st;
+      }
+    } else if (coop) {
       if (l0 > 0 && (e = cudaMemsetAsync(ws + w.ctrl, 0, 4, cs)) != cudaSuccess) return cuda_status(e);
       P.stage_begin = 0;
       P.stage_end = nL * NSTAGE;
@@ -2504,7 +2540,7 @@ static int decode(const ddl_shape* s, ddl_wtype wtype, const ddl_layer_w* layers
 using namespace ddl;
 
 extern "C" size_t ddl_workspace_bytes(const ddl_shape* shape, int32_t B, int64_t s_max) {
-  if (check_shape(shape) || B < 1 || B > MAX_B || s_max < 1) return 0;
+  if (check_shape(shape) || B < 1 || B > TC_MAX_B || s_max < 1) return 0;
   DevInfo di;
   if (device_info(di)) return 0;
   MatGeom mg[4];
@@ -2520,7 +2556,7 @@ extern "C" int ddl_workspace_view(const ddl_shape* shape, int32_t B, int64_t s_m
                                   ddl_ws_view* out) {
   int st = check_shape(shape);
   if (st) return st;
-  if (!out || B < 1 || B > MAX_B || s_max < 1) return DDL_ERR_ARG;
+  if (!out || B < 1 || B > TC_MAX_B || s_max < 1) return DDL_ERR_ARG;
   DevInfo di;
   if ((st = device_info(di))) return st;
   MatGeom mg[4];

@@ -1,0 +1,621 @@
+// ddl_tc.cu -- the batched decode step's weight stages on the tcgen05 tensor
+// cores (batches of 16-64 sequences with INT4 weights, 5-64 with bf16), where
+// the step's matrix products are real dense contractions ("把基础打牢"
+// primer §1.3: batching raises the intensity; roofline reply §七).
+//
+// GEMM kernel (one launch per weight stage): a CTA takes units of 128 weight
+// rows (eight of the packed stream's 16-row tiles) by a range of 64-wide
+// groups of the input dimension.  Warp 0 copies each group's eight packed
+// blocks and the group's B-operand image (the activations as fp16 limbs, laid
+// out as the tensor core reads them) into a ring of shared-memory stages with
+// TMA bulk copies; warps 4-7 expand the 4-bit codes in registers to fp16
+// code * scale and store them into tensor memory as the A operand (one 32-lane
+// quarter each; the tcgen05.st 16x256b shape takes the tensor-core fragment
+// registers as they are); one thread of warp 1 issues the tcgen05.mma of the
+// group's four 16-wide slices into an fp32 accumulator in tensor memory and
+// commits them to mbarriers that hand the stage and the A buffer back.  At a
+// unit's end warps 4-7 read the accumulator (tcgen05.ld), combine the three
+// limb columns of each sequence and store the unit's partial sums.
+//
+// Epilogue kernel (one launch per stage): sums a stage's split-K partials in a
+// fixed order and applies what the layer does to that stage's output (RMSNorm
+// factor, RoPE, the K/V append, the residual adds, SwiGLU), and writes the
+// B-operand image of the next GEMM's input (the activations times the next
+// RMSNorm weight, three fp16 limbs each) with per-CTA sums of squares.
+#include <math.h>
+
+#include <cuda_fp16.h>
+
+#include "ddl_device.cuh"
+#include "ddl_internal.h"
+#include "ddl_tc.h"
+
+namespace ddl {
+
+namespace {
+
+constexpr int GT = 256;          // GEMM threads: warp 0 copies, warp 1 issues MMAs, warps 4-7 expand / read out
+constexpr int STAGES = 4;
+constexpr int TMEM_COLS = 256;
+constexpr int A_COLS = 32;       // one group of A: four 16-wide slices of 8 columns
+constexpr int D_COL0 = 2 * A_COLS;
+constexpr int LBO = 128, SBO = 1024;  // B-operand image: k-cores of 8 x 16 B, 8 k-cores per column group of 8
+
+struct TcGemm {
+  int32_t N, NT, G, Sk, Gc, glast, S, NR, units, NP, B;
+  uint32_t wbytes, stage_bytes;  // bytes of a stage's weights area (aligned), of a whole stage
+  const uint8_t* w;              // the matrix's block stream
+  const uint8_t* xl;             // B-operand images, NP * 128 bytes per group
+  float* part;                   // [S][N][B] partial sums, rows in the packed (tile) order
+  uint32_t* status;
+  uint64_t wait_ns;
+};
+
+__device__ __forceinline__ int64_t block_index(const TcGemm& P, int T, int g) {
+  const int kc = g / P.Gc, gi = g - kc * P.Gc, gk = kc == P.Sk - 1 ? P.glast : P.Gc;
+  return (int64_t)kc * P.NT * P.Gc + (int64_t)T * gk + gi;
+}
+
+__device__ __forceinline__ uint32_t h2u(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
+__device__ __forceinline__ __half2 u2h(uint32_t u) { return *reinterpret_cast<__half2*>(&u); }
+
+// fp16 code * scale of one 32-bit word of packed nibbles (the eight codes of
+// rows g, g+8 at k 2t, 2t+1, 2t+8, 2t+9 of a 16-wide slice): r0 = row g,
+// k (2t, 2t+1); r1 = row g, k (2t+8, 2t+9); r2, r3 the same for row g+8.
+// (1032 + code) comes out exact from the fp16 pattern 0x6408 | (code ^ 8);
+// minus 1032 gives the code, times the fp16 scale the exact product.
+__device__ __forceinline__ void expand_int4(uint32_t w, __half2 s0, __half2 s1, uint32_t& r0, uint32_t& r1,
+                                            uint32_t& r2, uint32_t& r3) {
+  const __half2 off = u2h(0x64086408u);
+  const __half2 c0 = __hsub2(u2h(lop3_merge(w, 0x000F000Fu, 0x64086408u)), off);
+  const __half2 c1 = __hsub2(u2h(lop3_merge(w >> 4, 0x000F000Fu, 0x64086408u)), off);
+  const __half2 c2 = __hsub2(u2h(lop3_merge(w >> 8, 0x000F000Fu, 0x64086408u)), off);
+  const __half2 c3 = __hsub2(u2h(lop3_merge(w >> 12, 0x000F000Fu, 0x64086408u)), off);
+  r0 = h2u(__hmul2(c0, s0));
+  r1 = h2u(__hmul2(c2, s0));
+  r2 = h2u(__hmul2(c1, s1));
+  r3 = h2u(__hmul2(c3, s1));
+}
+__device__ __forceinline__ uint32_t bf16pair_to_f16pair(uint32_t v) {
+  return h2u(__floats2half2_rn(bf16lo_f32(v), bf16hi_f32(v)));
+}
+
+template <int WT>
+__global__ void __launch_bounds__(GT, 1) tc_gemm_kernel(const __grid_constant__ TcGemm P) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  constexpr uint32_t BB = WT == DDL_W_INT4 ? QBLK_BYTES : BF16_BLK_BYTES;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * P.stage_bytes);
+  const uint32_t full0 = smem_addr(bars), empty0 = full0 + STAGES * 8;
+  const uint32_t aready0 = empty0 + STAGES * 8, afree0 = aready0 + 16, dready = afree0 + 16, dfree = dready + 8;
+  const uint32_t fin = dfree + 8;
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 7);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tslot + 1);
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < STAGES; ++i) {
+      mbar_init(full0 + i * 8, 1);
+      mbar_init(empty0 + i * 8, 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(aready0 + i * 8, 4);
+      mbar_init(afree0 + i * 8, 1);
+    }
+    mbar_init(dready, 1);
+    mbar_init(dfree, 4);
+    mbar_init(fin, 1);
+    *abort_flag = 0;
+  }
+  mbar_init_fence();
+  __syncthreads();
+  if (warp == 1) tmem_alloc(smem_addr(tslot), TMEM_COLS);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tm = *tslot;
+  const uint32_t sbase = smem_addr(smem);
+  auto fail = [&]() {
+    if ((threadIdx.x & 31) == 0) atomicExch(P.status, STATUS_TIMEOUT);
+    *abort_flag = 1;
+  };
+
+  if (warp == 0) {  // ------------------------------------------------ copies
+    const uint64_t policy = policy_evict_first();
+    uint32_t it = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < P.units && ok; u += gridDim.x) {
+      const int rt = u % P.NR, s = u / P.NR, T0 = rt * 8;
+      const int nt = P.NT - T0 < 8 ? P.NT - T0 : 8;
+      const int g0 = (int)((int64_t)P.G * s / P.S), g1 = (int)((int64_t)P.G * (s + 1) / P.S);
+      for (int g = g0; g < g1; ++g, ++it) {
+        const uint32_t st = it % STAGES, k = it / STAGES;
+        if (k > 0 && !mbar_wait_warp(empty0 + st * 8, (k - 1) & 1, P.status, P.wait_ns)) {
+          fail();
+          ok = false;
+          break;
+        }
+        const uint32_t slot = sbase + st * P.stage_bytes;
+        if (lane == 0) mbar_arrive_expect_tx(full0 + st * 8, nt * BB + P.NP * 128u);
+        __syncwarp();
+        if (lane < nt) bulk_g2s_evict_first(slot + lane * BB, P.w + block_index(P, T0 + lane, g) * BB, BB,
+                                            full0 + st * 8, policy);
+        if (lane == 8) bulk_g2s(slot + P.wbytes, P.xl + (int64_t)g * P.NP * 128, P.NP * 128u, full0 + st * 8);
+      }
+      if (*abort_flag) ok = false;
+    }
+    // copies in flight land before the CTA leaves (bounded)
+    if (lane == 0)
+      for (uint32_t j = it > STAGES ? it - STAGES : 0; j < it; ++j)
+        if (!mbar_wait_thread(full0 + (j % STAGES) * 8, (j / STAGES) & 1, P.wait_ns)) break;
+  } else if (warp == 1) {  // ------------------------------------ MMA issue
+    if (lane == 0) {
+      const uint32_t idesc = umma_idesc_f16(128, P.NP);
+      uint32_t it = 0, ai = 0, ui = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < P.units && ok; u += gridDim.x, ++ui) {
+        const int s = u / P.NR;
+        const int g0 = (int)((int64_t)P.G * s / P.S), g1 = (int)((int64_t)P.G * (s + 1) / P.S);
+        if (ui > 0 && !mbar_wait_thread(dfree, (ui - 1) & 1, P.wait_ns)) {
+          fail();
+          break;
+        }
+        tc_fence_after();
+        for (int g = g0; g < g1; ++g, ++it, ++ai) {
+          const uint32_t st = it % STAGES, k = it / STAGES, ab = ai & 1, ka = ai >> 1;
+          if (!mbar_wait_thread(full0 + st * 8, k & 1, P.wait_ns) ||
+              !mbar_wait_thread(aready0 + ab * 8, ka & 1, P.wait_ns)) {
+            fail();
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t xs = sbase + st * P.stage_bytes + P.wbytes;
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            umma_f16_ts(tm + D_COL0, tm + ab * A_COLS + 8 * j, umma_sdesc(xs + j * 2 * LBO, LBO, SBO), idesc,
+                        (g > g0 || j > 0) ? 1u : 0u);
+          umma_commit(empty0 + st * 8);
+          umma_commit(afree0 + ab * 8);
+        }
+        if (ok) umma_commit(dready);
+      }
+      // every MMA issued has completed before tensor memory is released
+      umma_commit(fin);
+      mbar_wait_thread(fin, 0, P.wait_ns);
+    }
+  } else if (warp >= 4) {  // --------------------------- A operand, read-out
+    const int q = warp - 4, g = lane >> 2;
+    uint32_t it = 0, ai = 0, ui = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < P.units && ok; u += gridDim.x, ++ui) {
+      const int rt = u % P.NR, s = u / P.NR, T0 = rt * 8;
+      const int nt = P.NT - T0 < 8 ? P.NT - T0 : 8;
+      const int g0 = (int)((int64_t)P.G * s / P.S), g1 = (int)((int64_t)P.G * (s + 1) / P.S);
+      for (int gg = g0; gg < g1; ++gg, ++it, ++ai) {
+        const uint32_t st = it % STAGES, k = it / STAGES, ab = ai & 1, ka = ai >> 1;
+        if (!mbar_wait_warp(full0 + st * 8, k & 1, P.status, P.wait_ns) ||
+            (ka > 0 && !mbar_wait_warp(afree0 + ab * 8, (ka - 1) & 1, P.status, P.wait_ns))) {
+          fail();
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t slot = sbase + st * P.stage_bytes;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int tile = 2 * q + h;
+          const uint32_t ta = tm + ((uint32_t)(32 * q + 16 * h) << 16) + ab * A_COLS;
+          if (tile < nt) {
+            const uint32_t blk = slot + tile * BB;
+            if (WT == DDL_W_INT4) {
+              const uint4 wv = lds128(blk + lane * 16);
+              const uint32_t sw = lds32(blk + BLK_BYTES + g * 4);
+              const __half2 s0 = __float2half2_rn(bf16lo_f32(sw)), s1 = __float2half2_rn(bf16hi_f32(sw));
+              uint32_t r[4][4];
+              expand_int4(wv.x, s0, s1, r[0][0], r[0][1], r[0][2], r[0][3]);
+              expand_int4(wv.y, s0, s1, r[1][0], r[1][1], r[1][2], r[1][3]);
+              expand_int4(wv.z, s0, s1, r[2][0], r[2][1], r[2][2], r[2][3]);
+              expand_int4(wv.w, s0, s1, r[3][0], r[3][1], r[3][2], r[3][3]);
+#pragma unroll
+              for (int j = 0; j < 4; ++j) tmem_st_16x256b(ta + 8 * j, r[j][0], r[j][1], r[j][2], r[j][3]);
+            } else {
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {  // a0..a3 of the fragment: (g, lo k), (g+8, lo k), (g, hi k), (g+8, hi k)
+                const uint4 av = lds128(blk + j * 512 + lane * 16);
+                tmem_st_16x256b(ta + 8 * j, bf16pair_to_f16pair(av.x), bf16pair_to_f16pair(av.z),
+                                bf16pair_to_f16pair(av.y), bf16pair_to_f16pair(av.w));
+              }
+            }
+          } else {  // rows past the matrix's end: zero
+#pragma unroll
+            for (int j = 0; j < 4; ++j) tmem_st_16x256b(ta + 8 * j, 0u, 0u, 0u, 0u);
+          }
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_local(aready0 + ab * 8);
+      }
+      if (!ok) break;
+      // the unit's accumulator: row 32 q + lane, limb columns l * B + b
+      if (!mbar_wait_warp(dready, ui & 1, P.status, P.wait_ns)) {
+        fail();
+        break;
+      }
+      tc_fence_after();
+      const int n = rt * 128 + 32 * q + lane;
+      const uint32_t tr = tm + ((uint32_t)(32 * q) << 16) + D_COL0;
+      for (int b0 = 0; b0 < P.B; b0 += 16) {
+        uint32_t v0[16], v1[16], v2[16];
+        tmem_ld_32x32b_x16(tr + b0, v0);
+        tmem_ld_32x32b_x16(tr + P.B + b0, v1);
+        tmem_ld_32x32b_x16(tr + 2 * P.B + b0, v2);
+        tmem_ld_wait();
+        if (n < P.N) {
+          float* dst = P.part + ((int64_t)s * P.N + n) * P.B;
+#pragma unroll
+          for (int j = 0; j < 16; ++j)
+            if (b0 + j < P.B)
+              dst[b0 + j] = fmaf(4096.f, __uint_as_float(v0[j]),
+                                 fmaf(1.0f / 4096.f, __uint_as_float(v2[j]), __uint_as_float(v1[j])));
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_local(dfree);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tm, TMEM_COLS);
+  }
+}
+
+// ------------------------------------------------------------------ epilogues
+enum EpiKind { EK_QKV = 0, EK_WO = 2, EK_GU = 3, EK_DOWN = 4, EK_PREP_X = 5, EK_PREP_ATT = 6 };
+
+struct TcEpi {
+  int32_t kind, N, S, B, D, Hq, Hkv, hd, dff, NP;
+  float eps;
+  int64_t pos, s_max;
+  const float* part;
+  const float* xin32;        // WO: the layer's input residual (fp32) ...
+  const uint16_t* xin16;     // ... or bf16; PREP_X: the vector
+  const float* vec;          // DOWN: y; PREP_ATT: the attention output
+  float* out;                // QKV: q; WO: y; GU: a; DOWN: z
+  uint16_t* kc;
+  uint16_t* vc;
+  const uint16_t* nw;        // RMSNorm weight the limbs are multiplied by (WO: norm2, DOWN: next norm1, PREP_X: norm1)
+  uint8_t* xl;               // limb images written (NULL: none)
+  const float* ss_in;        // QKV, GU: sums of squares of the stage's input, per epilogue CTA
+  float* ss_out;             // WO, DOWN, PREP_X: of the vector written
+  int32_t ss_K;              // length of the vector of ss_in
+  float* resid_out;          // DOWN of the stack's last layer
+  uint16_t* out_bf16;
+  float rope[64][2];
+};
+
+// Position of element k, limb column c of a group's B-operand image.  Inside
+// each 16-wide slice the order of k follows the A operand's tensor-memory
+// columns: (0,1) (8,9) (2,3) (10,11) (4,5) (12,13) (6,7) (14,15).
+__device__ __forceinline__ int64_t limb_offset(int NP, int k, int c) {
+  const int kk = k & 63, j = kk >> 4, k16 = kk & 15;
+  const int kap = (k16 < 8 ? 4 * (k16 >> 1) + (k16 & 1) : 4 * ((k16 - 8) >> 1) + 2 + (k16 & 1)) + 16 * j;
+  return (int64_t)(k >> 6) * NP * 128 + (c >> 3) * SBO + (kap >> 3) * LBO + (c & 7) * 16 + (kap & 7) * 2;
+}
+__device__ __forceinline__ void put_limbs(uint8_t* xl, int NP, int B, int k, int b, float v) {
+  const __half h0 = __float2half_rn(v * (1.0f / 4096.f));
+  const float r1 = v - 4096.f * __half2float(h0);
+  const __half h1 = __float2half_rn(r1);
+  const __half h2 = __float2half_rn((r1 - __half2float(h1)) * 4096.f);
+  *reinterpret_cast<__half*>(xl + limb_offset(NP, k, b)) = h0;
+  *reinterpret_cast<__half*>(xl + limb_offset(NP, k, B + b)) = h1;
+  *reinterpret_cast<__half*>(xl + limb_offset(NP, k, 2 * B + b)) = h2;
+}
+
+__global__ void __launch_bounds__(256) tc_epi_kernel(const __grid_constant__ TcEpi E) {
+  __shared__ float red[256];
+  __shared__ float rfac[TC_MAX_B];
+  const int tid = threadIdx.x, B = E.B, RR = 256 / B, rr = tid / B, b = tid - rr * B;
+  const bool act = rr < RR;
+  // RMSNorm factor of the stage's input, per sequence, from the sums of squares
+  // of the CTAs that wrote it (in CTA order)
+  if (E.ss_in && tid < B) {
+    float ss = 0.f;
+    for (int c = 0; c < TC_EPI_CTAS; ++c) ss += E.ss_in[c * B + tid];
+    rfac[tid] = 1.0f / sqrtf(ss / (float)E.ss_K + E.eps);
+  }
+  __syncthreads();
+  const int64_t items = (E.kind == EK_QKV || E.kind == EK_GU) ? (int64_t)(E.N / 16) * 8 : E.N;
+  const int64_t i0 = items * blockIdx.x / gridDim.x, i1 = items * (blockIdx.x + 1) / gridDim.x;
+  float ss = 0.f;
+  auto psum = [&](int row) {  // split-K partials of packed row `row`, sequence b, in split order
+    float v = 0.f;
+    for (int s = 0; s < E.S; ++s) v += __ldcg(E.part + ((int64_t)s * E.N + row) * B + b);
+    return v;
+  };
+  if (act)
+    for (int64_t it = i0 + rr; it < i1; it += RR) {
+      const int i = (int)it;
+      switch (E.kind) {
+        case EK_QKV: {
+          const int T = i >> 3, gg = i & 7, tph = E.hd / 16, head = T / tph, ii = 8 * (T % tph) + gg;
+          const float r = rfac[b];
+          float v0 = psum(16 * T + gg) * r, v1 = psum(16 * T + gg + 8) * r;
+          if (head < E.Hq + E.Hkv) {  // RoPE on q and k: pair (ii, ii + hd/2)
+            const float c = E.rope[ii][0], sn = E.rope[ii][1], x0 = v0, x1 = v1;
+            v0 = x0 * c - x1 * sn;
+            v1 = x0 * sn + x1 * c;
+          }
+          if (head < E.Hq) {
+            float* qp = E.out + (int64_t)b * E.Hq * E.hd + (int64_t)head * E.hd;
+            qp[ii] = v0;
+            qp[ii + E.hd / 2] = v1;
+          } else {
+            const bool is_k = head < E.Hq + E.Hkv;
+            const int kvh = is_k ? head - E.Hq : head - E.Hq - E.Hkv;
+            uint16_t* row = (is_k ? E.kc : E.vc) + (((int64_t)b * E.Hkv + kvh) * E.s_max + E.pos) * E.hd;
+            row[ii] = f32_to_bf16_bits(v0);
+            row[ii + E.hd / 2] = f32_to_bf16_bits(v1);
+          }
+          break;
+        }
+        case EK_GU: {
+          const int T = i >> 3, gg = i & 7, j = 8 * T + gg;
+          const float r = rfac[b], gt = psum(16 * T + gg) * r, up = psum(16 * T + gg + 8) * r;
+          const float av = gt / (1.0f + expf(-gt)) * up;
+          E.out[(int64_t)b * E.dff + j] = av;
+          if (E.xl) put_limbs(E.xl, E.NP, B, j, b, av);
+          break;
+        }
+        case EK_WO: {
+          const int64_t o = (int64_t)b * E.D + i;
+          const float x = E.xin32 ? __ldcg(E.xin32 + o) : bf16_bits_to_f32(E.xin16[o]);
+          const float y = x + psum(i);
+          E.out[o] = y;
+          ss = fmaf(y, y, ss);
+          if (E.xl) put_limbs(E.xl, E.NP, B, i, b, y * bf16_bits_to_f32(E.nw[i]));
+          break;
+        }
+        case EK_DOWN: {
+          const int64_t o = (int64_t)b * E.D + i;
+          const float z = __ldcg(E.vec + o) + psum(i);
+          E.out[o] = z;
+          ss = fmaf(z, z, ss);
+          if (E.xl) put_limbs(E.xl, E.NP, B, i, b, z * bf16_bits_to_f32(E.nw[i]));
+          if (E.resid_out) E.resid_out[o] = z;
+          if (E.out_bf16) E.out_bf16[o] = f32_to_bf16_bits(z);
+          break;
+        }
+        case EK_PREP_X: {
+          const int64_t o = (int64_t)b * E.D + i;
+          const float x = E.xin32 ? __ldcg(E.xin32 + o) : bf16_bits_to_f32(E.xin16[o]);
+          ss = fmaf(x, x, ss);
+          put_limbs(E.xl, E.NP, B, i, b, x * bf16_bits_to_f32(E.nw[i]));
+          break;
+        }
+        default: {  // EK_PREP_ATT: the attention output, no norm
+          put_limbs(E.xl, E.NP, B, i, b, __ldcg(E.vec + (int64_t)b * E.N + i));
+          break;
+        }
+      }
+    }
+  if (E.ss_out) {  // this CTA's sums of squares per sequence, reduced in a fixed order
+    red[tid] = act ? ss : 0.f;
+    __syncthreads();
+    if (tid < B) {
+      float t = 0.f;
+      for (int k = 0; k < RR; ++k) t += red[k * B + tid];
+      E.ss_out[blockIdx.x * B + tid] = t;
+    }
+  }
+}
+
+// ------------------------------------------------------------------ host
+int g_tc_ready[64] = {0};
+
+int prepare(int wtype) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_status(e);
+  if (dev < 0 || dev >= 64) return DDL_ERR_UNSUPPORTED;
+  const int bit = wtype == DDL_W_INT4 ? 1 : 2;
+  if (g_tc_ready[dev] & bit) return DDL_OK;
+  e = cudaFuncSetAttribute(wtype == DDL_W_INT4 ? (const void*)tc_gemm_kernel<DDL_W_INT4>
+                                               : (const void*)tc_gemm_kernel<DDL_W_BF16>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+  if (e != cudaSuccess) return cuda_status(e);
+  g_tc_ready[dev] |= bit;
+  return DDL_OK;
+}
+
+int64_t al256(int64_t x) { return (x + 255) & ~int64_t(255); }
+uint32_t al1024(uint32_t x) { return (x + 1023u) & ~1023u; }
+
+int split_of(const MatGeom& m, int C) {
+  const int NR = (m.NT + 7) / 8;
+  int S = (C + NR / 2) / NR;
+  if (S < 1) S = 1;
+  if (S > TC_MAX_SPLIT) S = TC_MAX_SPLIT;
+  if (S > m.G) S = m.G;
+  return S;
+}
+
+void tc_sizes(const ddl_shape& s, int B, int C, int64_t& part_floats, int64_t& xl_bytes) {
+  MatGeom mg[4];
+  make_geoms(s, DDL_W_INT4, mg);
+  part_floats = 0;
+  xl_bytes = 0;
+  for (int k = 0; k < 4; ++k) {
+    const int64_t p = (int64_t)split_of(mg[k], C) * mg[k].N * B;
+    if (p > part_floats) part_floats = p;
+    const int64_t x = (int64_t)mg[k].G * tc_ncols(B) * 128;
+    if (x > xl_bytes) xl_bytes = x;
+  }
+}
+
+int launch_epi(const TcEpi& E, cudaStream_t cs) {
+  void* args[] = {const_cast<TcEpi*>(&E)};
+  return cuda_status(cudaLaunchKernel((const void*)tc_epi_kernel, dim3(TC_EPI_CTAS), dim3(256), args, 0, cs));
+}
+
+TcEpi epi_base(const TcRun& R) {
+  TcEpi E;
+  memset(&E, 0, sizeof E);
+  E.B = R.B;
+  E.D = R.D;
+  E.Hq = R.Hq;
+  E.Hkv = R.Hkv;
+  E.hd = R.hd;
+  E.dff = R.dff;
+  E.NP = tc_ncols(R.B);
+  E.eps = R.eps;
+  E.pos = R.pos;
+  E.s_max = R.s_max;
+  E.part = R.part;
+  E.ss_K = R.D;
+  memcpy(E.rope, R.rope, sizeof E.rope);
+  return E;
+}
+
+}  // namespace
+
+int64_t tc_workspace_bytes(const ddl_shape& s, int B, int wtype) {
+  (void)wtype;
+  int dev = 0, C = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&C, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return -1;
+  int64_t pf, xb;
+  tc_sizes(s, B, C, pf, xb);
+  return al256(pf * 4) + al256(xb) + al256((int64_t)2 * TC_EPI_CTAS * B * 4);
+}
+
+void tc_workspace_carve(const ddl_shape& s, int B, int wtype, uint8_t* base, TcRun& R) {
+  (void)wtype;
+  int64_t pf, xb;
+  tc_sizes(s, B, R.C, pf, xb);
+  R.part = reinterpret_cast<float*>(base);
+  R.xl = base + al256(pf * 4);
+  R.ss = reinterpret_cast<float*>(R.xl + al256(xb));
+}
+
+int tc_begin(const TcRun& R, void* stream) {
+  cudaStream_t cs = (cudaStream_t)stream;
+  int st = prepare(R.wtype);
+  if (st) return st;
+  int64_t pf, xb;
+  ddl_shape sh;
+  sh.D = R.D; sh.H_q = R.Hq; sh.H_kv = R.Hkv; sh.head_dim = R.hd; sh.d_ff = R.dff; sh.eps = R.eps; sh.rope_base = 1.0;
+  tc_sizes(sh, R.B, R.C, pf, xb);
+  cudaError_t e = cudaMemsetAsync(R.xl, 0, (size_t)xb, cs);  // padding columns stay zero
+  if (e != cudaSuccess) return cuda_status(e);
+  // the first layer's QKV operands and the sums of squares of its input
+  TcEpi E = epi_base(R);
+  E.kind = EK_PREP_X;
+  E.N = R.D;
+  if (R.l0 == 0) {
+    E.xin32 = R.resid_in;
+    E.xin16 = R.resid_in ? nullptr : R.x_bf16;
+  } else {
+    E.xin32 = R.Z + (int64_t)((R.l0 - 1) & 1) * R.B * R.D;
+  }
+  E.nw = R.layers[0].norm1;
+  E.xl = R.xl;
+  E.ss_out = R.ss;
+  return launch_epi(E, cs);
+}
+
+int tc_stage(const TcRun& R, int layer, int st, void* stream) {
+  cudaStream_t cs = (cudaStream_t)stream;
+  const int gl = R.l0 + layer, B = R.B, NP = tc_ncols(B);
+  const TcLayer& Ly = R.layers[layer];
+  int rc;
+  if (st == ST_WO) {  // the attention output becomes the Wo operands
+    TcEpi E = epi_base(R);
+    E.kind = EK_PREP_ATT;
+    E.N = R.Hq * R.hd;
+    E.vec = R.attn;
+    E.xl = R.xl;
+    if ((rc = launch_epi(E, cs))) return rc;
+  }
+  const MatGeom& m = R.mg[stage_mat(st)];
+  TcGemm G;
+  memset(&G, 0, sizeof G);
+  G.N = m.N;
+  G.NT = m.NT;
+  G.G = m.G;
+  G.Sk = m.Sk;
+  G.Gc = m.Gc;
+  G.glast = m.G - (m.Sk - 1) * m.Gc;
+  G.S = split_of(m, R.C);
+  G.NR = (m.NT + 7) / 8;
+  G.units = G.NR * G.S;
+  G.NP = NP;
+  G.B = B;
+  const uint32_t BB = R.wtype == DDL_W_INT4 ? QBLK_BYTES : BF16_BLK_BYTES;
+  G.wbytes = al1024(8 * BB);
+  G.stage_bytes = G.wbytes + al1024((uint32_t)NP * 128);
+  G.w = Ly.packed + m.woff;
+  G.xl = R.xl;
+  G.part = R.part;
+  G.status = R.status;
+  G.wait_ns = R.wait_ns;
+  // (at least half of an SM's shared memory, so that no two CTAs share an SM
+  // and its 512 tensor-memory columns)
+  size_t smem = (size_t)STAGES * G.stage_bytes + 1024;
+  if (smem < 116 * 1024) smem = 116 * 1024;
+  if (smem > 227 * 1024) return DDL_ERR_UNSUPPORTED;
+  {
+    void* args[] = {&G};
+    const int grid = G.units < R.C ? G.units : R.C;
+    const void* fn = R.wtype == DDL_W_INT4 ? (const void*)tc_gemm_kernel<DDL_W_INT4> : (const void*)tc_gemm_kernel<DDL_W_BF16>;
+    if ((rc = cuda_status(cudaLaunchKernel(fn, dim3(grid), dim3(GT), args, smem, cs)))) return rc;
+  }
+  TcEpi E = epi_base(R);
+  E.kind = st;
+  E.N = m.N;
+  E.S = G.S;
+  switch (st) {
+    case ST_QKV:
+      E.out = R.q;
+      E.kc = Ly.kc;
+      E.vc = Ly.vc;
+      E.ss_in = R.ss;
+      break;
+    case ST_WO:
+      if (gl == 0) {
+        E.xin32 = R.resid_in;
+        E.xin16 = R.resid_in ? nullptr : R.x_bf16;
+      } else {
+        E.xin32 = R.Z + (int64_t)((gl - 1) & 1) * B * R.D;
+      }
+      E.out = R.y;
+      E.nw = Ly.norm2;
+      E.xl = R.xl;
+      E.ss_out = R.ss + TC_EPI_CTAS * B;
+      break;
+    case ST_GU:
+      E.out = R.a;
+      E.xl = R.xl;
+      E.ss_in = R.ss + TC_EPI_CTAS * B;
+      break;
+    default: {  // ST_DOWN
+      E.vec = R.y;
+      E.out = R.Z + (int64_t)(gl & 1) * B * R.D;
+      if (layer + 1 < R.L) {  // the next layer's QKV operands
+        E.nw = R.layers[layer + 1].norm1;
+        E.xl = R.xl;
+        E.ss_out = R.ss;
+      }
+      if (R.final_last && layer == R.L - 1) {
+        E.resid_out = R.resid_out;
+        E.out_bf16 = R.out_bf16;
+      }
+      break;
+    }
+  }
+  return launch_epi(E, cs);
+}
+
+}  // namespace ddl

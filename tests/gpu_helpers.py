@@ -22,6 +22,12 @@ REL_L2 = 2e-3
 MAX_ABS = 2e-2
 
 
+def tensor_core_path(st) -> bool:
+    """The batched path on the tcgen05 tensor cores: INT4 from 16 sequences,
+    bf16 weights from 5."""
+    return (st.wtype == ddl.INT4 and st.batch >= 16) or (st.wtype == ddl.BF16 and st.batch > 4)
+
+
 def rel_l2(a, b) -> float:
     a = np.asarray(a, np.float64)
     b = np.asarray(b, np.float64)

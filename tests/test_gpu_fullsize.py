@@ -11,8 +11,9 @@ stack per step).
   reported).
 * the same stack at batches 4 and 16 with a 4096-token cache: teacher-forced
   layers {0, 63} plus two seeded others.
-* Llama-3-70B-shaped stack, 80 layers, KV 32768: the device step over all 80
-  layers and teacher-forced layers {0, 1, 40, 79} plus two seeded others.
+* Llama-3-70B-shaped stack, 80 layers, KV 32768: the device step against the
+  oracle run untethered over all 80 layers, and teacher-forced layers
+  {0, 1, 40, 79} plus two seeded others.
 
 Tolerances are those of the decode step (gpu_helpers): rel-L2 of the bf16
 output vs the oracle's fp64 z <= 2e-3 and max-abs of the fp32 residual <= 2e-2.
@@ -126,13 +127,29 @@ def test_27b_stack_batch_teacher_forced(B):
     _check(errs)
 
 
-def test_70b_stack_80_layers_teacher_forced():
+def test_70b_stack_80_layers_full_and_teacher_forced():
+    """The full 80-layer step against the oracle run untethered over all 80
+    layers (output rel-L2 at the step's bar, the fp32 residual within 1e-3 of
+    the largest |z|, as for the 64-layer stack), and teacher-forced layers."""
     cfg = configs.LLAMA70B_STACK
     st = workload.build_stack(cfg)
-    _device_run(st, 0, cfg.layers)  # the full step runs clean (status checked)
+    out, res = _device_run(st, 0, cfg.layers)
+    out = oracle.bf16_to_f64(synth.bits(out))
+    res = res.cpu().numpy().astype(np.float64)
+    sampled = _sampled(cfg.layers, (0, 1, cfg.layers // 2, cfg.layers - 1), 2, seed=13)
     errs = {}
-    for l in _sampled(cfg.layers, (0, 1, cfg.layers // 2, cfg.layers - 1), 2, seed=13):
-        errs[f"layer {l}"] = _teacher_forced(st, l, host_layer(cfg, l, st.wtype))
+    x = oracle.bf16_to_f64(synth.bits(st.x))
+    for l in range(cfg.layers):
+        lw = host_layer(cfg, l, st.wtype)
+        kc, vc = _host_cache(st, l)
+        x = oracle.layer_decode(cfg, lw, kc, vc, st.pos, x)  # untethered
+        if l in sampled:
+            errs[f"layer {l}"] = _teacher_forced(st, l, lw)
+        del lw
     del st
     torch.cuda.empty_cache()
     _check(errs)
+    e_out, e_res = rel_l2(out, x), float(np.max(np.abs(res - x)))
+    print(f"untethered 80-layer stack: rel-L2 {e_out:.3e}, max-abs {e_res:.3e} (max |z| {np.max(np.abs(x)):.1f})")
+    assert e_out <= REL_L2
+    assert e_res <= 1e-3 * float(np.max(np.abs(x)))
