@@ -34,16 +34,22 @@ namespace ddl {
 
 namespace {
 
-constexpr int GT = 256;          // GEMM threads: warp 0 copies, warp 1 issues MMAs, warps 4-7 expand / read out
-constexpr int STAGES = 4;
-constexpr int TMEM_COLS = 256;
+// GEMM CTA: warp 0 copies, warp 1 issues the MMAs, NDW warpgroups from warp
+// 4 on expand A, the last warpgroup reads the accumulators out.
+constexpr int NDW = 3;
+constexpr int GT = 32 * (4 + 4 * NDW + 4);
+constexpr int MAX_STAGES = 8;
+constexpr int NA = 4;            // A buffers in tensor memory
+constexpr int TMEM_COLS = 512;
 constexpr int A_COLS = 32;       // one group of A: four 16-wide slices of 8 columns
-constexpr int D_COL0 = 2 * A_COLS;
+constexpr int D_COL0 = NA * A_COLS;  // two accumulators of NP <= 192 columns follow
 constexpr int LBO = 128, SBO = 1024;  // B-operand image: k-cores of 8 x 16 B, 8 k-cores per column group of 8
 
 struct TcGemm {
   int32_t N, NT, G, Sk, Gc, glast, S, NR, units, NP, B;
   uint32_t wbytes, stage_bytes;  // bytes of a stage's weights area (aligned), of a whole stage
+  int32_t stages;                // shared-memory ring depth
+  int32_t gs;                    // groups per ring stage (at most)
   const uint8_t* w;              // the matrix's block stream
   const uint8_t* xl;             // B-operand images, NP * 128 bytes per group
   float* part;                   // [S][N][B] partial sums, rows in the packed (tile) order
@@ -80,28 +86,42 @@ __device__ __forceinline__ uint32_t bf16pair_to_f16pair(uint32_t v) {
   return h2u(__floats2half2_rn(bf16lo_f32(v), bf16hi_f32(v)));
 }
 
+// A unit's k-range [g0, g1) is cut into ring stages of up to P.gs groups that
+// stay inside one k-chunk, so that each tile's blocks of a stage are one
+// contiguous run of the stream (one bulk copy per tile and stage).
+__device__ __forceinline__ int stage_groups(const TcGemm& P, int g, int g1) {
+  const int cend = (g / P.Gc + 1) * P.Gc;
+  int e = g + P.gs;
+  if (e > cend) e = cend;
+  if (e > g1) e = g1;
+  return e - g;
+}
+
 template <int WT>
 __global__ void __launch_bounds__(GT, 1) tc_gemm_kernel(const __grid_constant__ TcGemm P) {
   extern __shared__ __align__(1024) uint8_t smem[];
   constexpr uint32_t BB = WT == DDL_W_INT4 ? QBLK_BYTES : BF16_BLK_BYTES;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * P.stage_bytes);
-  const uint32_t full0 = smem_addr(bars), empty0 = full0 + STAGES * 8;
-  const uint32_t aready0 = empty0 + STAGES * 8, afree0 = aready0 + 16, dready = afree0 + 16, dfree = dready + 8;
-  const uint32_t fin = dfree + 8;
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 7);
+  const int NS = P.stages;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + NS * P.stage_bytes);
+  const uint32_t full0 = smem_addr(bars), empty0 = full0 + MAX_STAGES * 8;
+  const uint32_t aready0 = empty0 + MAX_STAGES * 8, afree0 = aready0 + NA * 8;
+  const uint32_t dready0 = afree0 + NA * 8, dfree0 = dready0 + 16, fin = dfree0 + 16;
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 2 * MAX_STAGES + 2 * NA + 5);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tslot + 1);
   if (threadIdx.x == 0) {
-    for (int i = 0; i < STAGES; ++i) {
+    for (int i = 0; i < NS; ++i) {
       mbar_init(full0 + i * 8, 1);
       mbar_init(empty0 + i * 8, 1);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < NA; ++i) {
       mbar_init(aready0 + i * 8, 4);
       mbar_init(afree0 + i * 8, 1);
     }
-    mbar_init(dready, 1);
-    mbar_init(dfree, 4);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(dready0 + i * 8, 1);
+      mbar_init(dfree0 + i * 8, 4);
+    }
     mbar_init(fin, 1);
     *abort_flag = 0;
   }
@@ -117,133 +137,171 @@ __global__ void __launch_bounds__(GT, 1) tc_gemm_kernel(const __grid_constant__ 
     if ((threadIdx.x & 31) == 0) atomicExch(P.status, STATUS_TIMEOUT);
     *abort_flag = 1;
   };
+  auto unit_groups = [&](int u, int& g0, int& g1) {
+    const int s = u / P.NR;
+    g0 = (int)((int64_t)P.G * s / P.S);
+    g1 = (int)((int64_t)P.G * (s + 1) / P.S);
+  };
 
   if (warp == 0) {  // ------------------------------------------------ copies
     const uint64_t policy = policy_evict_first();
-    uint32_t it = 0;
+    uint32_t sc = 0;  // stages issued
     bool ok = true;
     for (int u = blockIdx.x; u < P.units && ok; u += gridDim.x) {
-      const int rt = u % P.NR, s = u / P.NR, T0 = rt * 8;
-      const int nt = P.NT - T0 < 8 ? P.NT - T0 : 8;
-      const int g0 = (int)((int64_t)P.G * s / P.S), g1 = (int)((int64_t)P.G * (s + 1) / P.S);
-      for (int g = g0; g < g1; ++g, ++it) {
-        const uint32_t st = it % STAGES, k = it / STAGES;
+      const int T0 = (u % P.NR) * 8, nt = P.NT - T0 < 8 ? P.NT - T0 : 8;
+      int g0, g1;
+      unit_groups(u, g0, g1);
+      for (int g = g0; g < g1; ++sc) {
+        const int ng = stage_groups(P, g, g1);
+        const uint32_t st = sc % NS, k = sc / NS;
         if (k > 0 && !mbar_wait_warp(empty0 + st * 8, (k - 1) & 1, P.status, P.wait_ns)) {
           fail();
           ok = false;
           break;
         }
         const uint32_t slot = sbase + st * P.stage_bytes;
-        if (lane == 0) mbar_arrive_expect_tx(full0 + st * 8, nt * BB + P.NP * 128u);
+        if (lane == 0) mbar_arrive_expect_tx(full0 + st * 8, (uint32_t)(nt * ng) * BB + (uint32_t)ng * P.NP * 128u);
         __syncwarp();
-        if (lane < nt) bulk_g2s_evict_first(slot + lane * BB, P.w + block_index(P, T0 + lane, g) * BB, BB,
-                                            full0 + st * 8, policy);
-        if (lane == 8) bulk_g2s(slot + P.wbytes, P.xl + (int64_t)g * P.NP * 128, P.NP * 128u, full0 + st * 8);
+        if (lane < nt)  // tile T0 + lane, groups g .. g + ng - 1: one run of the stream
+          bulk_g2s_evict_first(slot + lane * (P.gs * BB), P.w + block_index(P, T0 + lane, g) * BB, ng * BB,
+                               full0 + st * 8, policy);
+        if (lane == 8)
+          bulk_g2s(slot + P.wbytes, P.xl + (int64_t)g * P.NP * 128, (uint32_t)ng * P.NP * 128u, full0 + st * 8);
+        g += ng;
       }
       if (*abort_flag) ok = false;
     }
     // copies in flight land before the CTA leaves (bounded)
     if (lane == 0)
-      for (uint32_t j = it > STAGES ? it - STAGES : 0; j < it; ++j)
-        if (!mbar_wait_thread(full0 + (j % STAGES) * 8, (j / STAGES) & 1, P.wait_ns)) break;
+      for (uint32_t j = sc > (uint32_t)NS ? sc - NS : 0; j < sc; ++j)
+        if (!mbar_wait_thread(full0 + (j % NS) * 8, (j / NS) & 1, P.wait_ns)) break;
   } else if (warp == 1) {  // ------------------------------------ MMA issue
     if (lane == 0) {
       const uint32_t idesc = umma_idesc_f16(128, P.NP);
-      uint32_t it = 0, ai = 0, ui = 0;
+      uint32_t sc = 0, it = 0, ui = 0;
       bool ok = true;
       for (int u = blockIdx.x; u < P.units && ok; u += gridDim.x, ++ui) {
-        const int s = u / P.NR;
-        const int g0 = (int)((int64_t)P.G * s / P.S), g1 = (int)((int64_t)P.G * (s + 1) / P.S);
-        if (ui > 0 && !mbar_wait_thread(dfree, (ui - 1) & 1, P.wait_ns)) {
+        int g0, g1;
+        unit_groups(u, g0, g1);
+        const uint32_t db = ui & 1, dk = ui >> 1, dcol = D_COL0 + db * P.NP;
+        if (dk > 0 && !mbar_wait_thread(dfree0 + db * 8, (dk - 1) & 1, P.wait_ns)) {
           fail();
           break;
         }
         tc_fence_after();
-        for (int g = g0; g < g1; ++g, ++it, ++ai) {
-          const uint32_t st = it % STAGES, k = it / STAGES, ab = ai & 1, ka = ai >> 1;
-          if (!mbar_wait_thread(full0 + st * 8, k & 1, P.wait_ns) ||
-              !mbar_wait_thread(aready0 + ab * 8, ka & 1, P.wait_ns)) {
+        for (int g = g0; g < g1 && ok; ++sc) {
+          const int ng = stage_groups(P, g, g1);
+          const uint32_t st = sc % NS, k = sc / NS;
+          if (!mbar_wait_thread(full0 + st * 8, k & 1, P.wait_ns)) {
             fail();
             ok = false;
             break;
           }
-          tc_fence_after();
           const uint32_t xs = sbase + st * P.stage_bytes + P.wbytes;
+          for (int gi = 0; gi < ng; ++gi, ++it) {
+            const uint32_t ab = it % NA, ka = it / NA;
+            if (!mbar_wait_thread(aready0 + ab * 8, ka & 1, P.wait_ns)) {
+              fail();
+              ok = false;
+              break;
+            }
+            tc_fence_after();
 #pragma unroll
-          for (int j = 0; j < 4; ++j)
-            umma_f16_ts(tm + D_COL0, tm + ab * A_COLS + 8 * j, umma_sdesc(xs + j * 2 * LBO, LBO, SBO), idesc,
-                        (g > g0 || j > 0) ? 1u : 0u);
+            for (int j = 0; j < 4; ++j)
+              umma_f16_ts(tm + dcol, tm + ab * A_COLS + 8 * j,
+                          umma_sdesc(xs + gi * P.NP * 128 + j * 2 * LBO, LBO, SBO), idesc,
+                          (g + gi > g0 || j > 0) ? 1u : 0u);
+            umma_commit(afree0 + ab * 8);
+          }
+          if (!ok) break;
           umma_commit(empty0 + st * 8);
-          umma_commit(afree0 + ab * 8);
+          g += ng;
         }
-        if (ok) umma_commit(dready);
+        if (ok) umma_commit(dready0 + db * 8);
       }
       // every MMA issued has completed before tensor memory is released
       umma_commit(fin);
       mbar_wait_thread(fin, 0, P.wait_ns);
     }
-  } else if (warp >= 4) {  // --------------------------- A operand, read-out
-    const int q = warp - 4, g = lane >> 2;
-    uint32_t it = 0, ai = 0, ui = 0;
+  } else if (warp >= 4 && warp < 4 + 4 * NDW) {  // ------------------ A operand
+    // expansion warpgroup d takes the CTA's groups it, it + NDW, ...; warp q
+    // of it writes tensor-memory lanes 32 q .. 32 q + 31 (tiles 2q, 2q+1)
+    const int d = (warp - 4) >> 2, q = warp & 3, g = lane >> 2;
+    uint32_t sc = 0, it = 0;
     bool ok = true;
-    for (int u = blockIdx.x; u < P.units && ok; u += gridDim.x, ++ui) {
-      const int rt = u % P.NR, s = u / P.NR, T0 = rt * 8;
-      const int nt = P.NT - T0 < 8 ? P.NT - T0 : 8;
-      const int g0 = (int)((int64_t)P.G * s / P.S), g1 = (int)((int64_t)P.G * (s + 1) / P.S);
-      for (int gg = g0; gg < g1; ++gg, ++it, ++ai) {
-        const uint32_t st = it % STAGES, k = it / STAGES, ab = ai & 1, ka = ai >> 1;
-        if (!mbar_wait_warp(full0 + st * 8, k & 1, P.status, P.wait_ns) ||
-            (ka > 0 && !mbar_wait_warp(afree0 + ab * 8, (ka - 1) & 1, P.status, P.wait_ns))) {
-          fail();
-          ok = false;
-          break;
-        }
-        tc_fence_after();
+    for (int u = blockIdx.x; u < P.units && ok; u += gridDim.x) {
+      const int T0 = (u % P.NR) * 8, nt = P.NT - T0 < 8 ? P.NT - T0 : 8;
+      int g0, g1;
+      unit_groups(u, g0, g1);
+      for (int gs = g0; gs < g1 && ok; ++sc) {
+        const int ng = stage_groups(P, gs, g1);
+        const uint32_t st = sc % NS, k = sc / NS;
         const uint32_t slot = sbase + st * P.stage_bytes;
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int tile = 2 * q + h;
-          const uint32_t ta = tm + ((uint32_t)(32 * q + 16 * h) << 16) + ab * A_COLS;
-          if (tile < nt) {
-            const uint32_t blk = slot + tile * BB;
-            if (WT == DDL_W_INT4) {
-              const uint4 wv = lds128(blk + lane * 16);
-              const uint32_t sw = lds32(blk + BLK_BYTES + g * 4);
-              const __half2 s0 = __float2half2_rn(bf16lo_f32(sw)), s1 = __float2half2_rn(bf16hi_f32(sw));
-              uint32_t r[4][4];
-              expand_int4(wv.x, s0, s1, r[0][0], r[0][1], r[0][2], r[0][3]);
-              expand_int4(wv.y, s0, s1, r[1][0], r[1][1], r[1][2], r[1][3]);
-              expand_int4(wv.z, s0, s1, r[2][0], r[2][1], r[2][2], r[2][3]);
-              expand_int4(wv.w, s0, s1, r[3][0], r[3][1], r[3][2], r[3][3]);
-#pragma unroll
-              for (int j = 0; j < 4; ++j) tmem_st_16x256b(ta + 8 * j, r[j][0], r[j][1], r[j][2], r[j][3]);
-            } else {
-#pragma unroll
-              for (int j = 0; j < 4; ++j) {  // a0..a3 of the fragment: (g, lo k), (g+8, lo k), (g, hi k), (g+8, hi k)
-                const uint4 av = lds128(blk + j * 512 + lane * 16);
-                tmem_st_16x256b(ta + 8 * j, bf16pair_to_f16pair(av.x), bf16pair_to_f16pair(av.z),
-                                bf16pair_to_f16pair(av.y), bf16pair_to_f16pair(av.w));
-              }
-            }
-          } else {  // rows past the matrix's end: zero
-#pragma unroll
-            for (int j = 0; j < 4; ++j) tmem_st_16x256b(ta + 8 * j, 0u, 0u, 0u, 0u);
+        bool waited = false;
+        for (int gi = 0; gi < ng; ++gi, ++it) {
+          if ((int)(it % NDW) != d) continue;
+          const uint32_t ab = it % NA, ka = it / NA;
+          if ((!waited && !mbar_wait_warp(full0 + st * 8, k & 1, P.status, P.wait_ns)) ||
+              (ka > 0 && !mbar_wait_warp(afree0 + ab * 8, (ka - 1) & 1, P.status, P.wait_ns))) {
+            fail();
+            ok = false;
+            break;
           }
+          waited = true;
+          tc_fence_after();
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int tile = 2 * q + h;
+            const uint32_t ta = tm + ((uint32_t)(32 * q + 16 * h) << 16) + ab * A_COLS;
+            if (tile < nt) {
+              const uint32_t blk = slot + tile * (P.gs * BB) + gi * BB;
+              if (WT == DDL_W_INT4) {
+                const uint4 wv = lds128(blk + lane * 16);
+                const uint32_t sw = lds32(blk + BLK_BYTES + g * 4);
+                const __half2 s0 = __float2half2_rn(bf16lo_f32(sw)), s1 = __float2half2_rn(bf16hi_f32(sw));
+                uint32_t r[4][4];
+                expand_int4(wv.x, s0, s1, r[0][0], r[0][1], r[0][2], r[0][3]);
+                expand_int4(wv.y, s0, s1, r[1][0], r[1][1], r[1][2], r[1][3]);
+                expand_int4(wv.z, s0, s1, r[2][0], r[2][1], r[2][2], r[2][3]);
+                expand_int4(wv.w, s0, s1, r[3][0], r[3][1], r[3][2], r[3][3]);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) tmem_st_16x256b(ta + 8 * j, r[j][0], r[j][1], r[j][2], r[j][3]);
+              } else {
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {  // a0..a3 of the fragment: (g, lo k), (g+8, lo k), (g, hi k), (g+8, hi k)
+                  const uint4 av = lds128(blk + j * 512 + lane * 16);
+                  tmem_st_16x256b(ta + 8 * j, bf16pair_to_f16pair(av.x), bf16pair_to_f16pair(av.z),
+                                  bf16pair_to_f16pair(av.y), bf16pair_to_f16pair(av.w));
+                }
+              }
+            } else {  // rows past the matrix's end: zero
+#pragma unroll
+              for (int j = 0; j < 4; ++j) tmem_st_16x256b(ta + 8 * j, 0u, 0u, 0u, 0u);
+            }
+          }
+          tmem_st_wait();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive_local(aready0 + ab * 8);
         }
-        tmem_st_wait();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive_local(aready0 + ab * 8);
+        gs += ng;
       }
-      if (!ok) break;
-      // the unit's accumulator: row 32 q + lane, limb columns l * B + b
-      if (!mbar_wait_warp(dready, ui & 1, P.status, P.wait_ns)) {
+      if (*abort_flag) ok = false;
+    }
+  } else if (warp >= 4 + 4 * NDW) {  // --------------------------- read-out
+    // the accumulator of each unit: row 32 q + lane, limb columns l * B + b
+    const int q = warp & 3;
+    uint32_t ui = 0;
+    for (int u = blockIdx.x; u < P.units; u += gridDim.x, ++ui) {
+      const int rt = u % P.NR, s = u / P.NR;
+      const uint32_t db = ui & 1, dk = ui >> 1;
+      if (!mbar_wait_warp(dready0 + db * 8, dk & 1, P.status, P.wait_ns)) {
         fail();
         break;
       }
       tc_fence_after();
       const int n = rt * 128 + 32 * q + lane;
-      const uint32_t tr = tm + ((uint32_t)(32 * q) << 16) + D_COL0;
+      const uint32_t tr = tm + ((uint32_t)(32 * q) << 16) + D_COL0 + db * P.NP;
       for (int b0 = 0; b0 < P.B; b0 += 16) {
         uint32_t v0[16], v1[16], v2[16];
         tmem_ld_32x32b_x16(tr + b0, v0);
@@ -261,7 +319,7 @@ __global__ void __launch_bounds__(GT, 1) tc_gemm_kernel(const __grid_constant__ 
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive_local(dfree);
+      if (lane == 0) mbar_arrive_local(dfree0 + db * 8);
     }
   }
   tc_fence_before();
@@ -554,16 +612,23 @@ int tc_stage(const TcRun& R, int layer, int st, void* stream) {
   G.NP = NP;
   G.B = B;
   const uint32_t BB = R.wtype == DDL_W_INT4 ? QBLK_BYTES : BF16_BLK_BYTES;
-  G.wbytes = al1024(8 * BB);
-  G.stage_bytes = G.wbytes + al1024((uint32_t)NP * 128);
+  // groups per stage: as many as keep three stages within 200 KB (at most 8)
+  G.gs = 8;
+  while (G.gs > 1 && 3 * (al1024(8 * BB * G.gs) + al1024((uint32_t)NP * 128 * G.gs)) > 200u * 1024u) --G.gs;
+  G.wbytes = al1024(8 * BB * G.gs);
+  G.stage_bytes = G.wbytes + al1024((uint32_t)NP * 128 * G.gs);
   G.w = Ly.packed + m.woff;
   G.xl = R.xl;
   G.part = R.part;
   G.status = R.status;
   G.wait_ns = R.wait_ns;
-  // (at least half of an SM's shared memory, so that no two CTAs share an SM
-  // and its 512 tensor-memory columns)
-  size_t smem = (size_t)STAGES * G.stage_bytes + 1024;
+  // as many ring stages as fit (at most MAX_STAGES); at least half of an SM's
+  // shared memory, so that no two CTAs share an SM and its 512 tensor-memory
+  // columns
+  G.stages = (int32_t)((200u * 1024u) / G.stage_bytes);
+  if (G.stages > MAX_STAGES) G.stages = MAX_STAGES;
+  if (G.stages < 2) return DDL_ERR_UNSUPPORTED;
+  size_t smem = (size_t)G.stages * G.stage_bytes + 1024;
   if (smem < 116 * 1024) smem = 116 * 1024;
   if (smem > 227 * 1024) return DDL_ERR_UNSUPPORTED;
   {
