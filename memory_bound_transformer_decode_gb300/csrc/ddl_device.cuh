@@ -255,6 +255,13 @@ __device__ __forceinline__ void umma_f16_ts(uint32_t d, uint32_t a, uint64_t bde
       "r"(a), "l"(bdesc), "r"(idesc), "r"(acc)
       : "memory");
 }
+// One lane of a converged warp (the MMA instructions want warp-uniform
+// operands, so the whole warp runs the issue loop and one lane issues).
+__device__ __forceinline__ bool elect_one() {
+  uint32_t p = 0;
+  asm volatile("{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\tselp.u32 %0, 1, 0, e;\n\t}" : "=r"(p));
+  return p != 0;
+}
 // Arrive on an mbarrier once every MMA this thread issued so far has completed.
 __device__ __forceinline__ void umma_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)

@@ -39,10 +39,9 @@ namespace {
 constexpr int NDW = 3;
 constexpr int GT = 32 * (4 + 4 * NDW + 4);
 constexpr int MAX_STAGES = 8;
-constexpr int NA = 4;            // A buffers in tensor memory
+constexpr int MAX_NA = 12;       // A buffers in tensor memory (barrier slots)
 constexpr int TMEM_COLS = 512;
 constexpr int A_COLS = 32;       // one group of A: four 16-wide slices of 8 columns
-constexpr int D_COL0 = NA * A_COLS;  // two accumulators of NP <= 192 columns follow
 constexpr int LBO = 128, SBO = 1024;  // B-operand image: k-cores of 8 x 16 B, 8 k-cores per column group of 8
 
 struct TcGemm {
@@ -50,6 +49,8 @@ struct TcGemm {
   uint32_t wbytes, stage_bytes;  // bytes of a stage's weights area (aligned), of a whole stage
   int32_t stages;                // shared-memory ring depth
   int32_t gs;                    // groups per ring stage (at most)
+  int32_t na, nd;                // A buffers (32 columns each, from column 0), accumulators (after them)
+  int32_t dstride;               // columns of an accumulator: NP + 16 (the read-out takes 16 at a time)
   const uint8_t* w;              // the matrix's block stream
   const uint8_t* xl;             // B-operand images, NP * 128 bytes per group
   float* part;                   // [S][N][B] partial sums, rows in the packed (tile) order
@@ -105,9 +106,11 @@ __global__ void __launch_bounds__(GT, 1) tc_gemm_kernel(const __grid_constant__ 
   const int NS = P.stages;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + NS * P.stage_bytes);
   const uint32_t full0 = smem_addr(bars), empty0 = full0 + MAX_STAGES * 8;
-  const uint32_t aready0 = empty0 + MAX_STAGES * 8, afree0 = aready0 + NA * 8;
-  const uint32_t dready0 = afree0 + NA * 8, dfree0 = dready0 + 16, fin = dfree0 + 16;
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 2 * MAX_STAGES + 2 * NA + 5);
+  const int NA = P.na, ND = P.nd;
+  const uint32_t D_COL0 = (uint32_t)NA * A_COLS;
+  const uint32_t aready0 = empty0 + MAX_STAGES * 8, afree0 = aready0 + MAX_NA * 8;
+  const uint32_t dready0 = afree0 + MAX_NA * 8, dfree0 = dready0 + 16, fin = dfree0 + 16;
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 2 * MAX_STAGES + 2 * MAX_NA + 5);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tslot + 1);
   if (threadIdx.x == 0) {
     for (int i = 0; i < NS; ++i) {
@@ -118,7 +121,7 @@ __global__ void __launch_bounds__(GT, 1) tc_gemm_kernel(const __grid_constant__ 
       mbar_init(aready0 + i * 8, 4);
       mbar_init(afree0 + i * 8, 1);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < ND; ++i) {
       mbar_init(dready0 + i * 8, 1);
       mbar_init(dfree0 + i * 8, 4);
     }
@@ -176,53 +179,62 @@ __global__ void __launch_bounds__(GT, 1) tc_gemm_kernel(const __grid_constant__ 
       for (uint32_t j = sc > (uint32_t)NS ? sc - NS : 0; j < sc; ++j)
         if (!mbar_wait_thread(full0 + (j % NS) * 8, (j / NS) & 1, P.wait_ns)) break;
   } else if (warp == 1) {  // ------------------------------------ MMA issue
-    if (lane == 0) {
-      const uint32_t idesc = umma_idesc_f16(128, P.NP);
-      uint32_t sc = 0, it = 0, ui = 0;
-      bool ok = true;
-      for (int u = blockIdx.x; u < P.units && ok; u += gridDim.x, ++ui) {
-        int g0, g1;
-        unit_groups(u, g0, g1);
-        const uint32_t db = ui & 1, dk = ui >> 1, dcol = D_COL0 + db * P.NP;
-        if (dk > 0 && !mbar_wait_thread(dfree0 + db * 8, (dk - 1) & 1, P.wait_ns)) {
+    // the whole warp runs the loop (warp-uniform operands); one lane issues
+    const uint32_t idesc = umma_idesc_f16(128, P.NP);
+    const uint64_t xdesc0 = umma_sdesc(sbase + P.wbytes, LBO, SBO);  // stage 0's first group, slice 0
+    const uint32_t gstep = (uint32_t)P.NP * 128u >> 4, sstep = P.stage_bytes >> 4;  // descriptor address units
+    uint32_t sc = 0, it = 0, ui = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < P.units && ok; u += gridDim.x, ++ui) {
+      int g0, g1;
+      unit_groups(u, g0, g1);
+      const uint32_t db = ui % ND, dk = ui / ND, dcol = tm + D_COL0 + db * P.dstride;
+      if (dk > 0 && !mbar_wait_warp(dfree0 + db * 8, (dk - 1) & 1, P.status, P.wait_ns)) {
+        fail();
+        break;
+      }
+      tc_fence_after();
+      bool first = true;
+      for (int g = g0; g < g1 && ok; ++sc) {
+        const int ng = stage_groups(P, g, g1);
+        const uint32_t st = sc % NS, k = sc / NS;
+        if (!mbar_wait_warp(full0 + st * 8, k & 1, P.status, P.wait_ns)) {
           fail();
+          ok = false;
           break;
         }
-        tc_fence_after();
-        for (int g = g0; g < g1 && ok; ++sc) {
-          const int ng = stage_groups(P, g, g1);
-          const uint32_t st = sc % NS, k = sc / NS;
-          if (!mbar_wait_thread(full0 + st * 8, k & 1, P.wait_ns)) {
+        uint64_t xd = xdesc0 + (uint64_t)(st * sstep);
+        for (int gi = 0; gi < ng; ++gi, ++it, xd += gstep) {
+          const uint32_t ab = it % NA, ka = it / NA;
+          if (!mbar_wait_warp(aready0 + ab * 8, ka & 1, P.status, P.wait_ns)) {
             fail();
             ok = false;
             break;
           }
-          const uint32_t xs = sbase + st * P.stage_bytes + P.wbytes;
-          for (int gi = 0; gi < ng; ++gi, ++it) {
-            const uint32_t ab = it % NA, ka = it / NA;
-            if (!mbar_wait_thread(aready0 + ab * 8, ka & 1, P.wait_ns)) {
-              fail();
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-              umma_f16_ts(tm + dcol, tm + ab * A_COLS + 8 * j,
-                          umma_sdesc(xs + gi * P.NP * 128 + j * 2 * LBO, LBO, SBO), idesc,
-                          (g + gi > g0 || j > 0) ? 1u : 0u);
+          tc_fence_after();
+          if (elect_one()) {
+            const uint32_t aa = tm + ab * A_COLS;
+            umma_f16_ts(dcol, aa, xd, idesc, first ? 0u : 1u);
+            umma_f16_ts(dcol, aa + 8, xd + (2 * LBO >> 4), idesc, 1u);
+            umma_f16_ts(dcol, aa + 16, xd + (4 * LBO >> 4), idesc, 1u);
+            umma_f16_ts(dcol, aa + 24, xd + (6 * LBO >> 4), idesc, 1u);
             umma_commit(afree0 + ab * 8);
           }
-          if (!ok) break;
-          umma_commit(empty0 + st * 8);
-          g += ng;
+          __syncwarp();
+          first = false;
         }
-        if (ok) umma_commit(dready0 + db * 8);
+        if (!ok) break;
+        if (elect_one()) umma_commit(empty0 + st * 8);
+        __syncwarp();
+        g += ng;
       }
-      // every MMA issued has completed before tensor memory is released
-      umma_commit(fin);
-      mbar_wait_thread(fin, 0, P.wait_ns);
+      if (ok && elect_one()) umma_commit(dready0 + db * 8);
+      __syncwarp();
     }
+    // every MMA issued has completed before tensor memory is released
+    if (elect_one()) umma_commit(fin);
+    __syncwarp();
+    mbar_wait_warp(fin, 0, P.status, P.wait_ns);
   } else if (warp >= 4 && warp < 4 + 4 * NDW) {  // ------------------ A operand
     // expansion warpgroup d takes the CTA's groups it, it + NDW, ...; warp q
     // of it writes tensor-memory lanes 32 q .. 32 q + 31 (tiles 2q, 2q+1)
@@ -294,14 +306,14 @@ __global__ void __launch_bounds__(GT, 1) tc_gemm_kernel(const __grid_constant__ 
     uint32_t ui = 0;
     for (int u = blockIdx.x; u < P.units; u += gridDim.x, ++ui) {
       const int rt = u % P.NR, s = u / P.NR;
-      const uint32_t db = ui & 1, dk = ui >> 1;
+      const uint32_t db = ui % ND, dk = ui / ND;
       if (!mbar_wait_warp(dready0 + db * 8, dk & 1, P.status, P.wait_ns)) {
         fail();
         break;
       }
       tc_fence_after();
       const int n = rt * 128 + 32 * q + lane;
-      const uint32_t tr = tm + ((uint32_t)(32 * q) << 16) + D_COL0 + db * P.NP;
+      const uint32_t tr = tm + ((uint32_t)(32 * q) << 16) + D_COL0 + db * P.dstride;
       for (int b0 = 0; b0 < P.B; b0 += 16) {
         uint32_t v0[16], v1[16], v2[16];
         tmem_ld_32x32b_x16(tr + b0, v0);
@@ -615,6 +627,12 @@ int tc_stage(const TcRun& R, int layer, int st, void* stream) {
   // groups per stage: as many as keep three stages within 200 KB (at most 8)
   G.gs = 8;
   while (G.gs > 1 && 3 * (al1024(8 * BB * G.gs) + al1024((uint32_t)NP * 128 * G.gs)) > 200u * 1024u) --G.gs;
+  // four A buffers (a deeper A ring measured slower), then accumulators of
+  // NP columns plus 16 of headroom (the read-out loads 16 columns at a time,
+  // up to column 3B + 14): two when they fit, else one
+  G.dstride = NP + 16;
+  G.na = 4;
+  G.nd = G.na * A_COLS + 2 * G.dstride <= TMEM_COLS ? 2 : 1;
   G.wbytes = al1024(8 * BB * G.gs);
   G.stage_bytes = G.wbytes + al1024((uint32_t)NP * 128 * G.gs);
   G.w = Ly.packed + m.woff;
