@@ -9,8 +9,9 @@ stack per step).
   oracle run untethered over all 64 layers (each layer takes the oracle's own
   residual; rel-L2 of the output held to the step's bar, the residual's drift
   reported).
-* the same stack at batches 4 and 16 with a 4096-token cache: teacher-forced
-  layers {0, 63} plus two seeded others.
+* the same stack with a 4096-token cache per sequence, INT4 at batches 4, 16
+  and 64 and bf16 weights at batches 1, 16 and 64: the full step, and
+  teacher-forced layers {0, 63} plus two seeded others.
 * Llama-3-70B-shaped stack, 80 layers, KV 32768: the device step against the
   oracle run untethered over all 80 layers, and teacher-forced layers
   {0, 1, 40, 79} plus two seeded others.
@@ -115,10 +116,15 @@ def test_27b_stack_64_layers_full_and_teacher_forced():
     assert e_res <= 1e-3 * float(np.max(np.abs(x)))
 
 
-@pytest.mark.parametrize("B", [4, 16])
-def test_27b_stack_batch_teacher_forced(B):
+@pytest.mark.parametrize("wtype,B", [(ddl.INT4, 4), (ddl.INT4, 16), (ddl.INT4, 64), (ddl.BF16, 1),
+                                     (ddl.BF16, 16), (ddl.BF16, 64)])
+def test_27b_stack_batch_teacher_forced(wtype, B):
+    """The 64-layer batch/weight sweep shape (4096-token caches): batches on the
+    warp-level path (4 INT4, 1 bf16) and on the tcgen05 path (16 and 64, INT4
+    and bf16 weights), the full step's status and teacher-forced layers."""
     cfg = configs.STACK27B_SWEEP
-    st = workload.build_stack(cfg, batch=B)
+    st = workload.build_stack(cfg, batch=B, wtype=wtype)
+    _device_run(st, 0, cfg.layers)  # the full step runs clean (status checked)
     errs = {}
     for l in _sampled(cfg.layers, (0, cfg.layers - 1), 2, seed=12):
         errs[f"layer {l}"] = _teacher_forced(st, l, host_layer(cfg, l, st.wtype))
