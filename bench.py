@@ -80,10 +80,14 @@ def _peaks():
         return 6800.0, "fallback"
 
 
+# The sources the batch-1 decode kernel is compiled from.
+_DECODE_SOURCES = ("ddl_decode.cu", "ddl_device.cuh", "ddl_plan.h")
+
+
 def _source_hash() -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "memory_bound_transformer_decode_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
+    for f in _DECODE_SOURCES:
         h.update(open(os.path.join(csrc, f), "rb").read())
     return h.hexdigest()[:16]
 
@@ -336,7 +340,14 @@ def run_ours(args):
     peak, peak_kind = _peaks()
     kernel_ms = statistics.mean(per_ms)
     achieved = nbytes / (kernel_ms * 1e-3) / 1e9
-    launches_per_step = (L + 95) // 96 if args.mode == 0 else L * 6
+    tc = (wname == "int4" and B >= 16) or (wname == "bf16" and B > 4)
+    if tc:  # per layer: 4 tensor-core GEMMs, 4 epilogues, the attention operands, the attention stage
+        launches_per_step = L * 10 + (L + 95) // 96
+        kernel = ("tc_gemm_kernel + tc_epi_kernel per weight stage, decode_kernel for attention "
+                  "(step-level roofline over all launches)")
+    else:
+        launches_per_step = (L + 95) // 96 if args.mode == 0 else L * 5
+        kernel = "decode_kernel (one persistent launch per step)"
     line = {
         "metric": METRIC,
         "value": _job_rate(world, B, ms),
@@ -358,7 +369,7 @@ def run_ours(args):
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_source": f"hbm_gbs of {peak_kind}",
                      "traffic": _traffic(cfg.name),
-                     "kernel": "decode_kernel (one persistent launch per step)"},
+                     "kernel": kernel},
         "e2e": {"value": _job_rate(world, B, e2e_ms), "unit": "tokens/s",
                 "h2d_bytes_per_step": B * cfg.D * 2, "d2h_bytes_per_step": B * cfg.D * 2},
         "gpu_launches": launches_per_step * args.steps,
