@@ -273,3 +273,90 @@ def layer_decode(shape, layer: dict, kc, vc, pos: int, x, stages: bool = False):
     if rc != 0:
         raise ValueError(f"oracle rejected the shape/position (rc={rc})")
     return (z, st_arrays) if stages else z
+
+
+# ---------------------------------------------------------------- token step
+# The steps on either side of the layer stack in the primer's §1.2
+# decode_step: `embed(last_token_id)` before it and `sample(x @ W_emb.T)`
+# after it, with the Unsloth/Qwen-27B article's §三 vocabulary of about
+# 152 thousand entries.  Readings where the pages are silent: the output
+# matrix is the (tied) embedding table, in the same weight format as the
+# layers (INT4 quantized from the bf16 table, or the bf16 table itself); an
+# optional final RMSNorm weight (the pages show none; the Qwen/Llama models of
+# the workload shapes apply one before the output matrix); greedy decoding
+# takes the lowest id among equal maxima; top-k sampling is inverse-CDF
+# sampling over the k largest logits (equal logits at the boundary: lower ids
+# first) with weights exp((l - l_max) / T) and a caller-drawn uniform u.
+
+def embed(table_bf16, tokens) -> np.ndarray:
+    """Rows `tokens` of the embedding table (primer §1.2 `embed`).
+
+    table_bf16: uint16 [V, D] bf16 bits.  tokens: int [B].  Returns a uint16
+    [B, D] copy.  Ids outside [0, V) raise ValueError."""
+    table = np.asarray(table_bf16, np.uint16)
+    ids = np.asarray(tokens, np.int64).reshape(-1)
+    if np.any((ids < 0) | (ids >= table.shape[0])):
+        raise ValueError("token id outside the vocabulary")
+    out = np.empty((ids.size, table.shape[1]), np.uint16)
+    for b, t in enumerate(ids):
+        out[b] = table[t]
+    return out
+
+
+def lm_head_logits(x, head: OracleMat, norm_w=None, eps: float = 0.0) -> np.ndarray:
+    """Logits over the vocabulary of B hidden states (primer §1.2
+    `x[:, -1] @ W_emb.T`): l = W h with h = rmsnorm(x, norm_w) when a final
+    norm weight is given, else h = x.
+
+    x: fp64 [B, D].  head: OracleMat [V, D], INT4 (q, s) or bf16 (w).
+    Returns fp64 [B, V]."""
+    x = np.atleast_2d(np.asarray(x, np.float64))
+    rows = []
+    for b in range(x.shape[0]):
+        h = rmsnorm(x[b], norm_w, eps) if norm_w is not None else x[b]
+        rows.append(gemv_int4(head.q, head.s, h) if head.w is None else gemv_bf16(head.w, h))
+    return np.stack(rows)
+
+
+def greedy_token(logits) -> np.ndarray:
+    """Greedy decoding: the id of the largest logit, the lowest id among
+    equal maxima.  logits: [B, V] (or [V]).  Returns int64 [B]."""
+    l = np.atleast_2d(np.asarray(logits, np.float64))
+    return np.argmax(l, axis=1).astype(np.int64)  # first occurrence of the maximum
+
+
+def logsumexp(logits) -> np.ndarray:
+    """log sum_v exp(l_v) per row, with the maximum taken out first."""
+    l = np.atleast_2d(np.asarray(logits, np.float64))
+    m = l.max(axis=1, keepdims=True)
+    return (m + np.log(np.exp(l - m).sum(axis=1, keepdims=True)))[:, 0]
+
+
+def top_k_cdf(logits_row, k: int, temperature: float):
+    """The k candidates of top-k sampling in draw order (logit descending, id
+    ascending among equal logits) and their cumulative weights divided by the
+    total: candidate j is drawn for u in [cdf[j-1], cdf[j])."""
+    l = np.asarray(logits_row, np.float64).reshape(-1)
+    if temperature <= 0:
+        raise ValueError("temperature must be positive")
+    k = max(1, min(int(k), l.size))
+    order = np.lexsort((np.arange(l.size), -l))[:k]  # sort by -l, then by id
+    w = np.exp((l[order] - l[order[0]]) / temperature)
+    c = np.cumsum(w)
+    return order.astype(np.int64), c / c[-1]
+
+
+def sample_top_k(logits, k: int, temperature: float, u) -> np.ndarray:
+    """Top-k sampling (primer §1.2 `sample`) by inverse CDF with one uniform
+    u in [0, 1) per sequence; k <= 1 is greedy decoding.  logits: [B, V].
+    Returns int64 [B]."""
+    l = np.atleast_2d(np.asarray(logits, np.float64))
+    u = np.asarray(u, np.float64).reshape(-1)
+    if k <= 1:
+        return greedy_token(l)
+    out = np.empty(l.shape[0], np.int64)
+    for b in range(l.shape[0]):
+        ids, cdf = top_k_cdf(l[b], k, temperature)
+        j = int(np.searchsorted(cdf, u[b], side="right"))  # first j with cdf[j] > u
+        out[b] = ids[min(j, ids.size - 1)]
+    return out

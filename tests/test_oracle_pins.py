@@ -376,3 +376,108 @@ def test_layer_rejects_bad_position():
     wb, kc, vc, x = _tiny_inputs(cfg, cfg.kv_len)
     with pytest.raises(ValueError):
         oracle.layer_decode(cfg, oracle.quantized_layer(wb), kc, vc, cfg.kv_len, x)
+
+
+# ------------------------------------------------------------------ token step
+
+
+def test_embed_is_the_table_rows():
+    # hand example: row v of the table holds the bf16 value v + 1 everywhere
+    V, D = 5, 64
+    table = np.stack([_bits_of(np.full(D, v + 1.0)) for v in range(V)])
+    got = oracle.embed(table, [4, 0, 4, 2])
+    np.testing.assert_array_equal(oracle.bf16_to_f64(got)[:, 0], [5.0, 1.0, 5.0, 3.0])
+    np.testing.assert_array_equal(got[1], table[0])
+    for bad in ([-1], [V]):
+        with pytest.raises(ValueError):
+            oracle.embed(table, bad)
+
+
+@pytest.mark.parametrize("V,D", [(300, 128), (17, 64)])
+@pytest.mark.parametrize("with_norm", [False, True])
+def test_lm_head_logits_vs_library_routines(V, D, with_norm):
+    # W from the independently unpacked codes times the scales, the norm from
+    # torch's rms_norm, the product from numpy's matmul
+    w_bits = synth.bits(synth.normal_bf16((V, D), seed=V + D, std=0.02))
+    q, s = oracle.quantize_int4(w_bits)
+    x = RNG.standard_normal((3, D)) * 7.0
+    nw = synth.bits(synth.normal_bf16((D,), seed=5, mean=1.0, std=0.1)) if with_norm else None
+    eps = 1e-6
+    if with_norm:
+        h = F.rms_norm(torch.from_numpy(x), (D,), torch.from_numpy(oracle.bf16_to_f64(nw)), eps).numpy()
+    else:
+        h = x
+    W4 = _numpy_codes(q).astype(np.float64) * np.repeat(oracle.bf16_to_f64(s), 64, axis=1)
+    got = oracle.lm_head_logits(x, oracle.OracleMat(q=q, s=s), nw, eps)
+    np.testing.assert_allclose(got, h @ W4.T, rtol=1e-10, atol=1e-12)
+    gotb = oracle.lm_head_logits(x, oracle.OracleMat(w=w_bits), nw, eps)
+    np.testing.assert_allclose(gotb, h @ oracle.bf16_to_f64(w_bits).T, rtol=1e-10, atol=1e-12)
+
+
+def test_greedy_token_ties_and_brute_force():
+    assert oracle.greedy_token([[1.0, 3.0, 3.0, 2.0]])[0] == 1  # lowest id among equal maxima
+    assert oracle.greedy_token([[-5.0, -2.0, -9.0]])[0] == 1
+    l = RNG.standard_normal((4, 1000))
+    for b in range(4):
+        best = 0
+        for i in range(1000):
+            if l[b, i] > l[b, best]:
+                best = i
+        assert oracle.greedy_token(l)[b] == best
+
+
+def test_logsumexp_closed_forms_and_scipy():
+    scipy_special = pytest.importorskip("scipy.special")
+    l = RNG.standard_normal((3, 5000)) * 4.0
+    np.testing.assert_allclose(oracle.logsumexp(l), scipy_special.logsumexp(l, axis=1), rtol=1e-14)
+    # all equal: c + log V; shift: lse(l + c) = lse(l) + c (no overflow at 1e3)
+    np.testing.assert_allclose(oracle.logsumexp(np.full((1, 152064), 2.5)), 2.5 + math.log(152064), rtol=1e-14)
+    np.testing.assert_allclose(oracle.logsumexp(l + 1000.0), oracle.logsumexp(l) + 1000.0, rtol=1e-14)
+    assert oracle.logsumexp([[7.25]])[0] == 7.25
+
+
+def test_top_k_candidates_and_order():
+    l = np.array([5.0, 2.0, 2.0, 2.0, 1.0, 6.0])
+    ids, cdf = oracle.top_k_cdf(l, 3, 1.0)
+    np.testing.assert_array_equal(ids, [5, 0, 1])  # descending; the tie at the boundary takes the lower id
+    w = np.exp(np.array([6.0, 5.0, 2.0]) - 6.0)
+    np.testing.assert_allclose(cdf, np.cumsum(w) / w.sum(), rtol=1e-15)
+    ids, _ = oracle.top_k_cdf(l, 100, 1.0)  # k beyond V: every id
+    np.testing.assert_array_equal(ids, [5, 0, 1, 2, 3, 4])
+    r = RNG.standard_normal(2000)
+    ids, _ = oracle.top_k_cdf(r, 50, 0.7)
+    np.testing.assert_array_equal(np.sort(ids), np.sort(np.argsort(-r)[:50]))
+
+
+def test_sample_top_k_special_cases():
+    l = RNG.standard_normal((2, 3000)) * 2.0
+    g = oracle.greedy_token(l)
+    for u in (0.0, 0.3, 0.999):
+        np.testing.assert_array_equal(oracle.sample_top_k(l, 1, 1.0, [u, u]), g)  # k = 1: greedy
+    np.testing.assert_array_equal(oracle.sample_top_k(l, 40, 1.0, [0.0, 0.0]), g)  # u = 0: the largest
+    last = [oracle.top_k_cdf(l[b], 40, 1.0)[0][-1] for b in range(2)]
+    np.testing.assert_array_equal(oracle.sample_top_k(l, 40, 1.0, [1 - 1e-15] * 2), last)
+    # a tiny temperature is greedy; a huge one is uniform over the k candidates
+    np.testing.assert_array_equal(oracle.sample_top_k(l, 40, 1e-6, [0.9, 0.9]), g)
+    ids, cdf = oracle.top_k_cdf(l[0], 8, 1e9)
+    np.testing.assert_allclose(cdf, np.arange(1, 9) / 8.0, rtol=1e-8)
+    # candidate j is drawn for u in [cdf[j-1], cdf[j]): at u = 1/2 exactly, two
+    # equal logits give the second candidate
+    two = np.array([[0.0, 0.0, -50.0]])
+    assert oracle.sample_top_k(two, 2, 1.0, [0.5])[0] == 1
+    assert oracle.sample_top_k(two, 2, 1.0, [0.5 - 2 ** -53])[0] == 0
+
+
+def test_sample_top_k_frequencies_match_softmax():
+    # draws at the midpoints of a fine grid of u land on each candidate in
+    # proportion to its softmax weight over the top k (scipy's softmax)
+    scipy_special = pytest.importorskip("scipy.special")
+    l = RNG.standard_normal(500) * 1.5
+    k, T, n = 12, 0.8, 20000
+    u = (np.arange(n) + 0.5) / n
+    toks = np.array([oracle.sample_top_k(l[None, :], k, T, [ui])[0] for ui in u])
+    top = np.argsort(-l)[:k]
+    p = scipy_special.softmax(l[top] / T)
+    for j, v in enumerate(top):
+        assert abs(np.count_nonzero(toks == v) / n - p[j]) <= 1.0 / n + 1e-12
+    assert set(np.unique(toks)) <= set(top.tolist())
