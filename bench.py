@@ -43,6 +43,8 @@ def _args():
     p.add_argument("--layers", type=int, default=None)
     p.add_argument("--mode", type=int, default=0, help="0 persistent kernel, 1 launch per stage")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-token-step", action="store_true",
+                   help="skip the token step (embedding + stack + LM head + greedy id)")
     return p.parse_args()
 
 
@@ -260,6 +262,63 @@ def run_reference(args):
     }))
 
 
+def _token_step(args, cfg, st, wname, world, barrier, stream):
+    """The whole token step on the device: embedding rows of the previous
+    step's ids -> the layer stack -> the LM head over the vocabulary (the tied
+    table, with a final RMSNorm) -> greedy ids, fed back to the next step."""
+    import torch
+
+    from memory_bound_transformer_decode_gb300 import configs, ddl, synth
+
+    B, D, V = cfg.batch, cfg.D, configs.VOCAB
+    wt = ddl.INT4 if wname == "int4" else ddl.BF16
+    hw = synth.head_weights(cfg, V, device="cuda")
+    if wt == ddl.INT4:
+        q, s = ddl.ddl_quantize_int4(hw["embed"])
+        packed = ddl.ddl_pack_head((q, s), D, V, wt)
+        del q, s
+    else:
+        packed = ddl.ddl_pack_head(hw["embed"], D, V, wt)
+    table, norm_f = hw["embed"], hw["norm_f"]
+    ws = torch.empty(ddl.ddl_head_workspace_bytes(D, V, B), dtype=torch.uint8, device="cuda")
+    tok = torch.zeros(B, dtype=torch.int32, device="cuda")
+    x = torch.empty((B, D), dtype=torch.bfloat16, device="cuda")
+    res = torch.empty((B, D), dtype=torch.float32, device="cuda")
+
+    def step(ev=None):
+        ddl.ddl_embed(table, tok, out=x)
+        st.decode(resid_out=res, x=x)
+        if ev:
+            ev[0].record(stream)
+        ddl.ddl_lm_head(D, V, wt, packed, res, norm_f=norm_f, eps=cfg.eps, tokens=tok, workspace=ws)
+        if ev:
+            ev[1].record(stream)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    barrier()
+    hev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(args.steps):
+        step(hev[i])
+    e1.record(stream)
+    barrier()
+    status = ddl.ddl_read_device_status(st.workspace, st.shape, B, st.s_max)
+    if status != 0:
+        raise RuntimeError(f"device status {status} in the token step")
+    ms = _slowest(e0.elapsed_time(e1) / args.steps, world, "cuda")
+    head_ms = statistics.mean(a.elapsed_time(b) for a, b in hev)
+    head_bytes = ddl.ddl_packed_head_bytes(D, V, wt)
+    return {"value": _job_rate(world, B, ms), "unit": "tokens/s", "ms_per_step": ms, "vocab": V,
+            "sampling": "greedy", "head_ms": head_ms,
+            "head_roofline": {"bound": "hbm", "achieved": head_bytes / (head_ms * 1e-3) / 1e9,
+                              "unit": "GB/s", "traffic": None,
+                              "kernel": "head_prep + head_gemv + head_select (one step's LM head)"}}
+
+
 def run_ours(args):
     import torch
 
@@ -336,6 +395,8 @@ def run_ours(args):
     barrier()
     e2e_ms = _slowest(e0.elapsed_time(e1) / args.steps, world, "cuda")
 
+    token = None if args.no_token_step else _token_step(args, cfg, st, wname, world, barrier, stream)
+
     nbytes = roofline.step_bytes(cfg)
     peak, peak_kind = _peaks()
     kernel_ms = statistics.mean(per_ms)
@@ -375,6 +436,10 @@ def run_ours(args):
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk.summary(),
     }
+    if token is not None:
+        token["head_roofline"]["frac"] = token["head_roofline"]["achieved"] / peak
+        token["head_roofline"]["peak"] = peak
+        line["token_step"] = token
     if rank == 0 and not args.no_cpu_baseline:
         cb, _ = _cpu_baseline(cfg)
         line["cpu_baseline"] = cb

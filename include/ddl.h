@@ -203,6 +203,61 @@ int ddl_stack_decode_noalloc(const ddl_shape* shape, ddl_wtype wtype, const ddl_
                              const float* resid_in, const uint16_t* x_bf16, float* resid_out,
                              uint16_t* out_bf16, void* stream);
 
+/* ------------------------------------------------------------ token step
+ * The steps on either side of the layer stack in the primer's §1.2
+ * decode_step: `embed(last_token_id)` before it and `sample(x @ W_emb.T)`
+ * after it, for a vocabulary of V entries (Unsloth/Qwen-27B article §三:
+ * about 152 thousand, reduced chunk by chunk without forming the
+ * distribution over the whole vocabulary). */
+
+#define DDL_MAX_TOP_K 1024  /* largest k of top-k sampling */
+
+/* Rows of the bf16 embedding table: x_out[b] = table[tokens[b]].
+ * table: device [V][D] bf16 (D a multiple of 64).  tokens: device int32 [B],
+ * B <= DDL_MAX_BATCH.  x_out: device [B][D] bf16 (the x_bf16 input of
+ * ddl_stack_decode).  A token id outside [0, V) gives a zero row and, when
+ * bad_out (device int32, may be NULL) is given, sets *bad_out to 1 (the call
+ * never clears it). */
+int ddl_embed(const uint16_t* table, int64_t V, int32_t D, const int32_t* tokens, int32_t B,
+              uint16_t* x_out, int32_t* bad_out, void* stream);
+
+/* Bytes of a packed output matrix [V][D] (0 if the arguments are invalid). */
+size_t ddl_packed_head_bytes(int32_t D, int64_t V, ddl_wtype wtype);
+
+/* Pack the output matrix (the tied embedding table: INT4 codes and scales
+ * from ddl_quantize_int4, or the bf16 table) into the layout ddl_lm_head
+ * streams: 16-row x 64-column blocks in the layers' block format, ordered
+ * (16-row tile, group); rows past V in the last tile are zero.  Setup only. */
+int ddl_pack_head(const ddl_mat* w, int32_t D, int64_t V, ddl_wtype wtype, void* packed_out,
+                  void* stream);
+
+/* Workspace bytes of ddl_lm_head for (D, V, B) on the current device. */
+size_t ddl_head_workspace_bytes(int32_t D, int64_t V, int32_t B);
+
+/* The LM head and the choice of the next token for B <= DDL_MAX_BATCH
+ * sequences:  l = W h  with  h = rmsnorm(x, norm_f) when norm_f is given
+ * (eps inside the square root, as the layers' RMSNorm), else h = x.
+ *  x: device [B][D] fp32 (the stack's resid_out).  norm_f: device bf16 [D]
+ *    or NULL.  head_packed: from ddl_pack_head.
+ *  top_k <= 1: greedy, token_out[b] = the id of the largest logit (the
+ *    lowest id among equal maxima).
+ *  1 < top_k <= DDL_MAX_TOP_K: top-k sampling: the min(top_k, V) largest
+ *    logits (equal logits at the boundary: lower ids first) in the order
+ *    (logit descending, id ascending) with weights exp((l - l_max) / T),
+ *    T = temperature > 0; token_out[b] is the first candidate whose
+ *    cumulative weight exceeds u[b] * total (u: device fp32 [B] in [0, 1),
+ *    drawn by the caller).
+ *  logits_out: device fp32 [B][V] or NULL.  lse_out: device fp32 [B]
+ *    (log sum_v exp(l_v)) or NULL.  token_out: device int32 [B].
+ *  workspace: device, >= ddl_head_workspace_bytes(D, V, B).
+ * Errors: DDL_ERR_ARG (NULL pointer, top_k < 0, temperature or u missing
+ * for sampling), DDL_ERR_SHAPE (D not a multiple of 64), DDL_ERR_UNSUPPORTED
+ * (B or top_k too large), DDL_ERR_ALIGN, DDL_ERR_WORKSPACE. */
+int ddl_lm_head(int32_t D, int64_t V, ddl_wtype wtype, const void* head_packed, const uint16_t* norm_f,
+                float eps, int32_t B, const float* x, int32_t top_k, float temperature, const float* u,
+                int32_t* token_out, float* logits_out, float* lse_out, void* workspace, size_t ws_bytes,
+                void* stream);
+
 /* Launch mode of the decode calls: 0 = automatic (persistent cooperative
  * kernel when possible), 1 = one launch per fused stage. */
 int ddl_set_launch_mode(int32_t mode);

@@ -70,5 +70,9 @@ LLAMA70B_STACK = DecodeConfig("llama3-70b-80L-int4-kv32768-b1", D=8192, H_q=64, 
                               head_dim=128, d_ff=28672, rope_base=5e5, kv_len=32768, layers=80,
                               seed=4)
 
+# Vocabulary of the LM head: the Qwen-class vocabulary of about 152 thousand
+# entries (Unsloth/Qwen-27B article §三), 152064 = 16 x 9504.
+VOCAB = 152064
+
 ALL = (SMALL_LAYER, QWEN7B_LAYER, STACK27B, STACK27B_SWEEP, LLAMA70B_STACK)
 BY_NAME = {c.name: c for c in ALL}

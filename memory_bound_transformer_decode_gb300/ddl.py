@@ -24,7 +24,8 @@ EXPORTED = ("ddl_quantize_int4", "ddl_packed_layer_bytes", "ddl_pack_layer", "dd
             "ddl_workspace_bytes", "ddl_workspace_view", "ddl_layer_decode", "ddl_stack_decode",
             "ddl_stack_decode_noalloc", "ddl_set_launch_mode", "ddl_set_wait_limit_ns",
             "ddl_test_hold_barrier", "ddl_set_trace", "ddl_read_device_status", "ddl_status_string",
-            "ddl_last_cuda_error")
+            "ddl_last_cuda_error", "ddl_embed", "ddl_packed_head_bytes", "ddl_pack_head",
+            "ddl_head_workspace_bytes", "ddl_lm_head")
 
 
 class DDLError(RuntimeError):
@@ -109,6 +110,14 @@ def load(build_if_missing: bool = False):
         lib.ddl_status_string.argtypes = [ctypes.c_int]
         lib.ddl_status_string.restype = ctypes.c_char_p
         lib.ddl_last_cuda_error.restype = ctypes.c_char_p
+        lib.ddl_embed.argtypes = [vp, i64, i32, vp, i32, vp, vp, vp]
+        lib.ddl_packed_head_bytes.argtypes = [i32, i64, ctypes.c_int]
+        lib.ddl_packed_head_bytes.restype = sz
+        lib.ddl_pack_head.argtypes = [P(Mat), i32, i64, ctypes.c_int, vp, vp]
+        lib.ddl_head_workspace_bytes.argtypes = [i32, i64, i32]
+        lib.ddl_head_workspace_bytes.restype = sz
+        lib.ddl_lm_head.argtypes = [i32, i64, ctypes.c_int, vp, vp, ctypes.c_float, i32, vp, i32,
+                                    ctypes.c_float, vp, vp, vp, vp, vp, sz, vp]
         for name in EXPORTED:
             if not hasattr(lib, name):
                 raise RuntimeError(f"{path} does not export {name}")
@@ -308,3 +317,69 @@ def ws_tensor(workspace: torch.Tensor, offset: int, n: int) -> torch.Tensor:
     """fp32 view of n floats at byte offset `offset` of a workspace tensor."""
     assert offset % 4 == 0
     return workspace.view(torch.uint8)[offset: offset + 4 * n].view(torch.float32)
+
+
+# ------------------------------------------------------------------ token step
+
+def ddl_embed(table: torch.Tensor, tokens: torch.Tensor, out: torch.Tensor | None = None,
+              bad: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Rows tokens (int32 [B], device) of the bf16 table [V, D] -> bf16 [B, D].
+    bad: optional int32 [1] device flag set to 1 by an id outside [0, V)."""
+    lib = load()
+    V, D = table.shape
+    B = tokens.numel()
+    if out is None:
+        out = torch.empty((B, D), dtype=torch.bfloat16, device=table.device)
+    _check("ddl_embed", lib.ddl_embed(_ptr(table), V, D, _ptr(tokens), B, _ptr(out), _ptr(bad),
+                                      _stream(stream)))
+    return out
+
+
+def ddl_packed_head_bytes(D: int, V: int, wtype: int) -> int:
+    return int(load().ddl_packed_head_bytes(D, V, wtype))
+
+
+def ddl_pack_head(w, D: int, V: int, wtype: int, out: torch.Tensor | None = None,
+                  stream=None) -> torch.Tensor:
+    """Pack the output matrix [V, D]: (q, scale) for INT4 or a bf16 tensor."""
+    lib = load()
+    n = ddl_packed_head_bytes(D, V, wtype)
+    if n == 0:
+        raise DDLError("ddl_packed_head_bytes", 1, lib)
+    if wtype == INT4:
+        q, s = w
+        m, dev = Mat(q.data_ptr(), s.data_ptr(), None), q.device
+    else:
+        m, dev = Mat(None, None, w.data_ptr()), w.device
+    if out is None:
+        out = torch.empty(n, dtype=torch.uint8, device=dev)
+    _check("ddl_pack_head", lib.ddl_pack_head(ctypes.byref(m), D, V, wtype, _ptr(out), _stream(stream)))
+    return out
+
+
+def ddl_head_workspace_bytes(D: int, V: int, B: int) -> int:
+    n = int(load().ddl_head_workspace_bytes(D, V, B))
+    if n == 0:
+        raise DDLError("ddl_head_workspace_bytes", 1, _lib)
+    return n
+
+
+def ddl_lm_head(D: int, V: int, wtype: int, head_packed: torch.Tensor, x: torch.Tensor,
+                norm_f: torch.Tensor | None = None, eps: float = 0.0, top_k: int = 1,
+                temperature: float = 1.0, u: torch.Tensor | None = None,
+                tokens: torch.Tensor | None = None, logits: torch.Tensor | None = None,
+                lse: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
+                stream=None) -> torch.Tensor:
+    """Next-token ids (int32 [B]) from the fp32 hidden states x [B, D]: greedy
+    for top_k <= 1, else top-k sampling with the uniforms u (fp32 [B])."""
+    lib = load()
+    B = x.shape[0]
+    if tokens is None:
+        tokens = torch.empty(B, dtype=torch.int32, device=x.device)
+    if workspace is None:
+        workspace = torch.empty(ddl_head_workspace_bytes(D, V, B), dtype=torch.uint8, device=x.device)
+    _check("ddl_lm_head", lib.ddl_lm_head(D, V, wtype, _ptr(head_packed), _ptr(norm_f), float(eps), B,
+                                          _ptr(x), int(top_k), float(temperature), _ptr(u),
+                                          _ptr(tokens), _ptr(logits), _ptr(lse), _ptr(workspace),
+                                          workspace.numel(), _stream(stream)))
+    return tokens

@@ -7,7 +7,8 @@ share).  Every tensor has its own sub-seed
     seed * 2**32 + (layer + 1) * 64 + tensor_id
 
 with tensor ids norm1 0, wq 1, wk 2, wv 3, wo 4, norm2 5, wg 6, wu 7, wd 8,
-K cache 9, V cache 10; the input x uses layer = -1.  Values are drawn as fp32
+K cache 9, V cache 10; the input x (id 0), the embedding table (id 11) and
+the final norm weight (id 12) use layer = -1.  Values are drawn as fp32
 normals (mean + std * N(0, 1)) and rounded to bf16 by PyTorch's
 round-to-nearest-even conversion.
 
@@ -22,7 +23,7 @@ import numpy as np
 import torch
 
 TENSOR_IDS = {"norm1": 0, "wq": 1, "wk": 2, "wv": 3, "wo": 4, "norm2": 5, "wg": 6,
-              "wu": 7, "wd": 8, "kcache": 9, "vcache": 10}
+              "wu": 7, "wd": 8, "kcache": 9, "vcache": 10, "embed": 11, "norm_f": 12}
 WEIGHT_STD = 0.02
 NORM_STD = 0.1
 
@@ -88,6 +89,15 @@ def input_x(cfg, device="cpu", batch=None) -> torch.Tensor:
     """Layer-0 input x [B, D] bf16, N(0, 1)."""
     B = cfg.batch if batch is None else batch
     return normal_bf16((B, cfg.D), seed=subseed(cfg.seed, -1, 0), device=device)
+
+
+def head_weights(cfg, vocab: int, device="cpu") -> dict:
+    """The embedding table [vocab, D] (N(0, 0.02), also the output matrix) and
+    the final norm weight [D] (1 + N(0, 0.1)), bf16."""
+    return {"embed": normal_bf16((vocab, cfg.D), seed=subseed(cfg.seed, -1, TENSOR_IDS["embed"]),
+                                 std=WEIGHT_STD, device=device),
+            "norm_f": normal_bf16((cfg.D,), seed=subseed(cfg.seed, -1, TENSOR_IDS["norm_f"]),
+                                  mean=1.0, std=NORM_STD, device=device)}
 
 
 def bits(t: torch.Tensor) -> np.ndarray:

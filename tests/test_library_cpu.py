@@ -83,3 +83,29 @@ def test_host_argument_checks(lib):
     kv = ddl.KV(16, 16, 10)
     assert lib.ddl_kv_append(ctypes.byref(kv), 1, 1, 64, 10, ctypes.c_void_p(16),
                              ctypes.c_void_p(16), None) == 2
+
+
+def test_token_step_host_checks(lib):
+    # sizes: INT4 blocks of 544 bytes, bf16 of 2048, over ceil(V / 16) tiles x D / 64 groups
+    assert lib.ddl_packed_head_bytes(512, 1000, ddl.INT4) == 63 * 8 * 544
+    assert lib.ddl_packed_head_bytes(512, 1008, ddl.BF16) == 63 * 8 * 2048
+    assert lib.ddl_packed_head_bytes(500, 1000, ddl.INT4) == 0
+    assert lib.ddl_packed_head_bytes(512, 0, ddl.INT4) == 0
+    m = ddl.Mat(None, None, None)
+    assert lib.ddl_pack_head(ctypes.byref(m), 512, 1000, ddl.INT4, ctypes.c_void_p(256), None) == 8
+    assert lib.ddl_pack_head(ctypes.byref(m), 500, 1000, ddl.INT4, ctypes.c_void_p(256), None) == 1
+    p = ctypes.c_void_p(256)
+    assert lib.ddl_embed(None, 10, 64, p, 1, p, None, None) == 8
+    assert lib.ddl_embed(p, 10, 100, p, 1, p, None, None) == 1
+    assert lib.ddl_embed(p, 10, 64, p, 65, p, None, None) == 5
+    assert lib.ddl_embed(ctypes.c_void_p(258), 10, 64, p, 1, p, None, None) == 3
+    head = lambda **kw: lib.ddl_lm_head(  # noqa: E731
+        kw.get("D", 512), kw.get("V", 1000), ddl.INT4, p, None, 1e-6, kw.get("B", 1), p, kw.get("k", 1),
+        ctypes.c_float(kw.get("T", 1.0)), kw.get("u", None), p, None, None, kw.get("ws", p), 1 << 30, None)
+    assert head(D=500) == 1
+    assert head(B=65) == 5
+    assert head(k=1025, u=p) == 5
+    assert head(k=-1) == 8
+    assert head(k=4) == 8             # sampling without uniforms
+    assert head(k=4, u=p, T=0.0) == 8
+    assert head(ws=None) == 8
