@@ -442,28 +442,70 @@ __device__ __forceinline__ void trace_stamp(const Params& P, int s, int slot) {
 
 // ------------------------------------------------------------------ GEMV prologue
 // Stages this CTA's panel of the activation (k-chunks pk[p]..pk[p+1]-1) as
-// m16n8k16 B fragments: column 2b is the fp16 "high" part of sequence b's x
-// (times the norm weight and 2^-e), column 2b+1 the fp16 remainder, so x is
-// carried to ~22 bits.  Also the RMSNorm factor r (QKV, GU) and, for INT4,
-// the per-group sums of x used to remove the +8 code offset.  The power-of-two
-// scale 2^e brings the largest |x * w| to [2^11, 2^12); that maximum is
-// recorded by the stage that produced x (one word per sequence), so one pass
-// over the panel suffices; only the first layer of a launch has no producer
-// and measures its panel.
-// A unit (group slot gs, sequence b, k-slice j) is 16 values of x.  Its
-// fragments fill 64 bytes: words 4 (r % 2) + 2 k + r / 2 (high parts) and 8 +
-// the same (low parts) for pair k of quad r (values 4 r + 2 k, +1).  The
-// unit's four fp32 quads are first staged in those same 64 bytes, so one
-// thread converts (half) a unit in place, with no barrier between units: at
-// batch 1 the staging layout is x itself and arrives by one bulk copy; wider
-// batches interleave sequences and use cp.async (through L1).  This code
-// runs once per stage: its loops are rolled, because each
-// new instruction is fetched while the memory system carries the weight
-// stream.  The panel's norm weights were copied before the stage's grid
-// barrier (gemv_prep).
+// m16n8k16 B fragments: column 2b is the fp16 "high" part of sequence b's
+// x * norm weight * 2^-8, column 2b+1 the fp16 remainder, so x is carried to
+// ~22 significant bits for |x w| >= 32 and to an absolute 2^-17 below (range
+// |x w| < 2^24 with no per-vector scale).  Also the RMSNorm factor r (QKV,
+// GU) and the per-group sums of x used to remove the +8 code offset.
+// A unit (group slot gs, sequence b, k-slice j) is 16 values of x; its
+// fragments fill 64 bytes: lane (c, t) of the MMA reads bytes 8 (4 c + t) of
+// the slice's 64 B-byte block (c = 2b: high parts, 2b + 1: remainders), word
+// 0 holding values 2t, 2t+1 and word 1 values 2t+8, 2t+9.  With INT4 weights
+// every weight stage after the first of a launch finds this image already
+// written by the epilogues of the stage that produced x (img_put below) and
+// fetches its panel with one bulk copy; otherwise the panel's x is staged in
+// the fragments' bytes and converted in place (one thread per half unit: the
+// even and the odd quads of a unit read and write disjoint bytes).  This code
+// runs once per stage: its loops are rolled, because each new instruction is
+// fetched while the memory system carries the weight stream.  The panel's
+// norm weights were copied before the stage's grid barrier (gemv_prep).
 __device__ __forceinline__ uint32_t unit_offset(int gs, int b, int j, int B) {  // bytes
   return (uint32_t)gs * B * 256 + (uint32_t)(j * 2 * B + 2 * b) * 32;
 }
+constexpr float X_SCALE = 256.f;  // x is carried as x * 2^-8
+// With an image, the norm-weight area holds the half-slice sums of the panel
+// (from NW_HS_OFF, <= 8 KB) and the sums of squares of the vector (from 0,
+// <= NW_HS_OFF), or the next stage's norm weights (from 0, D * 2 bytes).
+constexpr int NW_HS_OFF = 24576;
+static_assert(NW_HS_OFF + XF_CHUNKS * GC * 8 * 4 <= SM_NW_BYTES, "half-slice sums");
+
+// fp16 high part and remainder of v * 2^-8 at element k of sequence b of a
+// fragment image (the layout above, B sequences, slice-major).
+// Returns high part + remainder (what the MMAs multiply), for the sums below.
+__device__ __forceinline__ float img_put(uint8_t* img, int B, int64_t k, int b, float v) {
+  const int p = (int)(k & 15), tq = (p & 7) >> 1;
+  const float sv = v * (1.0f / X_SCALE);
+  const __half hi = __float2half_rn(sv);
+  const __half lo = __float2half_rn(sv - __half2float(hi));
+  uint8_t* base = img + (k >> 4) * 64 * B + (p >> 3) * 4 + (p & 1) * 2 + tq * 8;
+  *reinterpret_cast<__half*>(base + 2 * b * 32) = hi;
+  *reinterpret_cast<__half*>(base + (2 * b + 1) * 32) = lo;
+  return __half2float(hi) + __half2float(lo);
+}
+// Beside an image of K elements: per 8-element half slice and sequence, the
+// sum of the fragments (high part + remainder) and the sum of squares of the
+// vector itself (before the norm weight), [K / 8][B] floats each.
+__device__ __forceinline__ float* img_hsum(uint8_t* img, int B, int K) {
+  return reinterpret_cast<float*>(img + (((int64_t)K * 4 * B + 255) & ~int64_t(255)));
+}
+__device__ __forceinline__ float* img_hsq(uint8_t* img, int B, int K) { return img_hsum(img, B, K) + (K / 8) * B; }
+// An epilogue's lanes (g, t), t < B, hold rows g (half slice 0) and g + 8
+// (half slice 1) of a 16-row tile: the half slices' sums over g.
+__device__ __forceinline__ float tile_half_sum(float v, int B) {
+  const uint32_t mask = 0x11111111u * ((1u << B) - 1u);
+  v += __shfl_xor_sync(mask, v, 4);
+  v += __shfl_xor_sync(mask, v, 8);
+  v += __shfl_xor_sync(mask, v, 16);
+  return v;
+}
+// The image a stage writes for the next weight stage, and the one it reads.
+__device__ __forceinline__ uint8_t* img_out(const Params& P, int layer, int st) {
+  return P.ximg[(layer * NSTAGE + st) & 1];
+}
+__device__ __forceinline__ bool img_in(const Params& P, int layer, int st) {
+  return P.ximg[0] != nullptr && P.wtype == DDL_W_INT4 && layer * NSTAGE + st > 0;
+}
+
 template <int HD, int WT>
 __device__ __noinline__ void gemv_prologue(const Params& P, const GemvCtx& E, uint8_t* smem, Misc& M) {
   const MatGeom& m = E.m;
@@ -484,24 +526,33 @@ __device__ __noinline__ void gemv_prologue(const Params& P, const GemvCtx& E, ui
   const int ngv = (nkc - 1) * GC + chunk_groups(m, kc_lo + nkc - 1);  // group slots holding data
   const int n_units = ngv * B * 4;
   const int kbase = kc_lo * GC * DDL_GROUP;
-  const bool whole = nkc == m.Sk;  // the panel is the whole vector
-  const bool have_max = !(E.st == ST_QKV && E.layer == 0);
+  const bool from_img = WT == DDL_W_INT4 && img_in(P, E.layer, E.st);
   const uint32_t invB = (65536u + B - 1) / B;  // g / B == (g * invB) >> 16 for g < 2^15
   const uint32_t raw = smem_addr(smem + SM_SCR);
   const uint32_t nws = smem_addr(smem + SM_NW);
   // 1. copies (earlier readers of these areas, any thread, are done first):
-  //    quad i = (gs * B + b) * 16 + q16 of x to quad q16 % 4 of its unit.  At
-  //    batch 1 that is the panel of x as it lies in memory: one bulk copy
-  //    (thread 0; the ring's copies were issued long before the barrier, so
-  //    it does not queue behind them), completed on the x barrier.
+  //    the panel of the image, or at batch 1 the panel of x as it lies in
+  //    memory: one bulk copy (thread 0; the ring's copies were issued long
+  //    before the barrier, so it does not queue behind them), completed on
+  //    the x barrier; else quad i = (gs * B + b) * 16 + q16 of x to quad
+  //    q16 % 4 of its unit.
   csync();
-  const bool bulk = B == 1 && x32 != nullptr;
+  const bool bulk = from_img || (B == 1 && x32 != nullptr);
   const uint32_t xbar = smem_addr(smem + SM_XBAR), xpar = M.xuse & 1u;
   if (bulk && tid == 0) {
-    fence_proxy_async_global();  // x: the previous stage's generic stores, read by the copy
+    fence_proxy_async_global();  // the previous stage's generic stores, read by the copy
     fence_proxy_async_smem();    // the previous stage's generic accesses to this area come first
-    mbar_arrive_expect_tx(xbar, (uint32_t)n_units * 64);
-    bulk_g2s(raw, x32 + kbase, (uint32_t)n_units * 64, xbar);
+    if (from_img) {  // the panel's fragments, its half-slice sums and (norm stages) the sums of squares
+      uint8_t* src = P.ximg[(E.layer * NSTAGE + E.st - 1) & 1];
+      const uint32_t ib = (uint32_t)n_units * 64, hb = (uint32_t)ngv * 8 * B * 4, qb = nw ? (uint32_t)(K / 8) * B * 4 : 0u;
+      mbar_arrive_expect_tx(xbar, ib + hb + qb);
+      bulk_g2s(raw, src + (int64_t)(kbase / 16) * 64 * B, ib, xbar);
+      bulk_g2s(nws + NW_HS_OFF, img_hsum(src, B, K) + (int64_t)(kbase / 8) * B, hb, xbar);
+      if (qb) bulk_g2s(nws, img_hsq(src, B, K), qb, xbar);
+    } else {
+      mbar_arrive_expect_tx(xbar, (uint32_t)n_units * 64);
+      bulk_g2s(raw, x32 + kbase, (uint32_t)n_units * 64, xbar);
+    }
   }
 #pragma unroll 1
   for (int i = tid; i < (bulk ? 0 : n_units * 4); i += NTHREADS) {
@@ -512,15 +563,11 @@ __device__ __noinline__ void gemv_prologue(const Params& P, const GemvCtx& E, ui
     if (x32) cp_async16(dst, x32 + o);
     else cp_async8(dst, x16 + o);
   }
-  float xm[NARROW_B] = {0.f, 0.f, 0.f, 0.f};
-  if (have_max) {
-#pragma unroll
-    for (int b = 0; b < NARROW_B; ++b)
-      if (b < B) xm[b] = __uint_as_float(__ldcg(P.xmax + (E.layer * NSTAGE + E.st) * MAX_B + b));
-  }
   if (tid == 0) trace_stamp(P, E.layer * NSTAGE + E.st, NW + 3);
-  // 2. meanwhile (a norm stage whose panel is not the whole vector): the sum of squares
-  if (nw && !whole) {
+  // 2. meanwhile (norm stages without an image): the sum of squares of the
+  //    whole input vector
+  float* Sx = reinterpret_cast<float*>(smem + SM_SCR + XF_BYTES);
+  if (nw && !from_img) {
 #pragma unroll 1
     for (int b = 0; b < B; ++b) {
       float ss = 0.f;
@@ -539,16 +586,39 @@ __device__ __noinline__ void gemv_prologue(const Params& P, const GemvCtx& E, ui
   csync();
   if (bulk && tid == 0) M.xuse += 1;
   if (tid == 0) trace_stamp(P, E.layer * NSTAGE + E.st, NW + 5);
-  // Half unit h = 2 u + p of unit u: quads p and p + 2 (values 4p..4p+3 and
-  // 4p+8..4p+11), read from bytes 16p and 32 + 16p of the unit; their high
-  // parts fill bytes 16p.. and their low parts bytes 32 + 16p.., the same
-  // bytes, so the two halves of a unit are converted independently.
-  auto half_load = [&](int h, float (&x)[8], float (&w)[8], int& gs, int& b, int& j, uint32_t& a) {
-    const int u = h >> 1, p = h & 1, gsb = u >> 2;
-    j = u & 3;
-    gs = (int)(((uint32_t)gsb * invB) >> 16);
-    b = gsb - gs * B;
-    a = raw + unit_offset(gs, b, j, B) + 16 * p;
+  if (from_img) {  // per (group slot, sequence) the sum of its eight half slices, in order; the sum of squares
+    const float* hs = reinterpret_cast<const float*>(smem + SM_NW + NW_HS_OFF);
+#pragma unroll 1
+    for (int i = tid; i < ngv * B; i += NTHREADS) {
+      const int gs = (int)(((uint32_t)i * invB) >> 16), b = i - gs * B;
+      float sum = 0.f;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) sum += hs[(8 * gs + q) * B + b];
+      Sx[gs * NARROW_B + b] = sum;
+    }
+    if (nw) {
+      const float* hq = reinterpret_cast<const float*>(smem + SM_NW);
+#pragma unroll 1
+      for (int b = 0; b < B; ++b) {
+        float ss = 0.f;
+        for (int q = tid; q < K / 8; q += NTHREADS) ss += hq[q * B + b];
+        ss = warp_sum(ss);
+        if (lane == 0) M.red[warp][2 * b] = ss;
+      }
+    }
+  }
+  // 3. conversion in place (no image): half unit h = 2 u + p of unit u holds
+  //    quads p and p + 2 (values 4p..4p+3 and 4p+8..4p+11), read from bytes
+  //    16p and 32 + 16p of the unit; their high parts fill bytes 16p.. and
+  //    their remainders bytes 32 + 16p.., the same bytes.
+  const int n_half = 2 * n_units;
+  constexpr bool f16 = WT == DDL_W_INT4;
+#pragma unroll 1
+  for (int h = tid; h < (from_img ? 0 : n_half); h += NTHREADS) {
+    const int u = h >> 1, pp = h & 1, gsb = u >> 2, j = u & 3;
+    const int gs = (int)(((uint32_t)gsb * invB) >> 16);
+    const uint32_t a = raw + unit_offset(gs, gsb - gs * B, j, B) + 16 * pp;
+    float x[8], w[8];
 #pragma unroll
     for (int q = 0; q < 2; ++q) {
       float4 v;
@@ -562,117 +632,73 @@ __device__ __noinline__ void gemv_prologue(const Params& P, const GemvCtx& E, ui
       x[4 * q + 1] = v.y;
       x[4 * q + 2] = v.z;
       x[4 * q + 3] = v.w;
-      const uint2 wq = nw ? lds64(nws + gs * 128 + j * 32 + p * 8 + q * 16) : make_uint2(0x3f803f80u, 0x3f803f80u);
+      const uint2 wq = nw ? lds64(nws + gs * 128 + j * 32 + pp * 8 + q * 16) : make_uint2(0x3f803f80u, 0x3f803f80u);
       w[4 * q] = bf16lo_f32(wq.x);
       w[4 * q + 1] = bf16hi_f32(wq.x);
       w[4 * q + 2] = bf16lo_f32(wq.y);
       w[4 * q + 3] = bf16hi_f32(wq.y);
     }
-  };
-  const int n_half = 2 * n_units;
-  // 3. the scale: the producer's max, or (first layer of a launch) the panel's
-  if (!have_max) {
-#pragma unroll 1
-    for (int h = tid; h < n_half; h += NTHREADS) {
-      float x[8], w[8];
-      int gs, b, j;
-      uint32_t a;
-      half_load(h, x, w, gs, b, j, a);
-      float m = 0.f;
+    uint32_t hw[4], lw[4];  // word 2k + q: pair k of quad p + 2q
 #pragma unroll
-      for (int e = 0; e < 8; ++e) m = fmaxf(m, fabsf(x[e] * w[e]));
+    for (int q = 0; q < 2; ++q)
 #pragma unroll
-      for (int bb = 0; bb < NARROW_B; ++bb)
-        if (bb == b) xm[bb] = fmaxf(xm[bb], m);
-    }
-#pragma unroll
-    for (int b = 0; b < NARROW_B; ++b) {
-      const float r = warp_max(xm[b]);
-      if (lane == 0 && b < B) M.red[warp][2 * b + 1] = r;
-    }
-    csync();
-#pragma unroll
-    for (int b = 0; b < NARROW_B; ++b) {
-      xm[b] = 0.f;
-      if (b < B)
-        for (int w = 0; w < NW; ++w) xm[b] = fmaxf(xm[b], M.red[w][2 * b + 1]);
-    }
-  }
-  float sdn[NARROW_B];  // 2^-e of each sequence
-#pragma unroll
-  for (int b = 0; b < NARROW_B; ++b) {
-    const int e = xm[b] > 0.f ? ilogbf(xm[b]) - 11 : 0;
-    sdn[b] = ldexpf(1.0f, -e);
-    if (tid == b && b < B) M.escale[b] = ldexpf(1.0f, e);
-  }
-  // 4. fragments, one half unit per thread and trip; Sx = sum of hi + lo
-  //    over the group's eight half units (eight consecutive lanes)
-  float* Sx = reinterpret_cast<float*>(smem + SM_SCR + XF_BYTES);
-  constexpr bool f16 = WT == DDL_W_INT4;
-  const bool want_ss = nw && whole;
-  float ssq[NARROW_B] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 1
-  for (int h0 = 0; h0 < n_half; h0 += NTHREADS) {
-    const int h = h0 + tid;
-    float part = 0.f;
-    int gs = 0, b = 0, j = 0;
-    if (h < n_half) {
-      float x[8], w[8];
-      uint32_t a;
-      half_load(h, x, w, gs, b, j, a);
-      if (want_ss) {
-        float s2 = 0.f;
-#pragma unroll
-        for (int e = 0; e < 8; ++e) s2 = fmaf(x[e], x[e], s2);
-#pragma unroll
-        for (int bb = 0; bb < NARROW_B; ++bb)
-          if (bb == b) ssq[bb] += s2;
-      }
-      const float sc = b == 0 ? sdn[0] : b == 1 ? sdn[1] : b == 2 ? sdn[2] : sdn[3];
-      uint32_t hw[4], lw[4];  // word 2k + q: pair k of quad p + 2q
-#pragma unroll
-      for (int q = 0; q < 2; ++q)
-#pragma unroll
-        for (int k = 0; k < 2; ++k) {
-          const int e = 4 * q + 2 * k;
-          const float2 pv = make_float2(x[e] * w[e] * sc, x[e + 1] * w[e + 1] * sc);
-          float2 hf, lf;
-          if (f16) {
-            const __half2 hh = __float22half2_rn(pv);
-            hf = __half22float2(hh);
-            const __half2 ll = __float22half2_rn(make_float2(pv.x - hf.x, pv.y - hf.y));
-            lf = __half22float2(ll);
-            hw[2 * k + q] = *reinterpret_cast<const uint32_t*>(&hh);
-            lw[2 * k + q] = *reinterpret_cast<const uint32_t*>(&ll);
-          } else {
-            const __nv_bfloat162 hh = __float22bfloat162_rn(pv);
-            hf = __bfloat1622float2(hh);
-            const __nv_bfloat162 ll = __float22bfloat162_rn(make_float2(pv.x - hf.x, pv.y - hf.y));
-            lf = __bfloat1622float2(ll);
-            hw[2 * k + q] = *reinterpret_cast<const uint32_t*>(&hh);
-            lw[2 * k + q] = *reinterpret_cast<const uint32_t*>(&ll);
-          }
-          part += (hf.x + lf.x) + (hf.y + lf.y);
+      for (int k = 0; k < 2; ++k) {
+        const int e = 4 * q + 2 * k;
+        const float2 pv = make_float2(x[e] * w[e] * (1.0f / X_SCALE), x[e + 1] * w[e + 1] * (1.0f / X_SCALE));
+        if (f16) {
+          const __half2 hh = __float22half2_rn(pv);
+          const float2 hf = __half22float2(hh);
+          const __half2 ll = __float22half2_rn(make_float2(pv.x - hf.x, pv.y - hf.y));
+          hw[2 * k + q] = *reinterpret_cast<const uint32_t*>(&hh);
+          lw[2 * k + q] = *reinterpret_cast<const uint32_t*>(&ll);
+        } else {
+          const __nv_bfloat162 hh = __float22bfloat162_rn(pv);
+          const float2 hf = __bfloat1622float2(hh);
+          const __nv_bfloat162 ll = __float22bfloat162_rn(make_float2(pv.x - hf.x, pv.y - hf.y));
+          hw[2 * k + q] = *reinterpret_cast<const uint32_t*>(&hh);
+          lw[2 * k + q] = *reinterpret_cast<const uint32_t*>(&ll);
         }
-      sts128(a, make_uint4(hw[0], hw[1], hw[2], hw[3]));
-      sts128(a + 32, make_uint4(lw[0], lw[1], lw[2], lw[3]));
-    }
-    part += __shfl_xor_sync(FULL, part, 1);
-    part += __shfl_xor_sync(FULL, part, 2);
-    part += __shfl_xor_sync(FULL, part, 4);
-    if ((h & 7) == 0 && h < n_half) Sx[gs * NARROW_B + b] = part;
+      }
+    sts128(a, make_uint4(hw[0], hw[1], hw[2], hw[3]));
+    sts128(a + 32, make_uint4(lw[0], lw[1], lw[2], lw[3]));
   }
+  if (!from_img) csync();
+  // 4. (no image) per (group slot, sequence): the sum of every high part and
+  //    remainder, one unit per thread, the four units of a group in adjacent
+  //    lanes
+#pragma unroll 1
+  for (int u0 = 0; u0 < (from_img ? 0 : n_units); u0 += NTHREADS) {
+    const int u = u0 + tid;
+    float sum = 0.f;
+    if (u < n_units) {
+      const int gsb = u >> 2, gs = (int)(((uint32_t)gsb * invB) >> 16);
+      const uint32_t a = raw + unit_offset(gs, gsb - gs * B, u & 3, B);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint4 r = lds128(a + 16 * q);
+        const uint32_t wd[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          float2 f;
+          if (f16) f = __half22float2(*reinterpret_cast<const __half2*>(&wd[e]));
+          else f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wd[e]));
+          sum += f.x + f.y;
+        }
+      }
+    }
+    sum += __shfl_xor_sync(FULL, sum, 1);
+    sum += __shfl_xor_sync(FULL, sum, 2);
+    if ((u & 3) == 0 && u < n_units) {
+      const int gsb = u >> 2, gs = (int)(((uint32_t)gsb * invB) >> 16);
+      Sx[gs * NARROW_B + (gsb - gs * B)] = sum;
+    }
+  }
+  if (tid < B) M.escale[tid] = X_SCALE;
   // zero fragments that the stream reads for blocks past a slot's end (the
   // attention stage uses this memory too)
   for (int i = tid; i < XZ_BYTES / 4; i += NTHREADS) reinterpret_cast<uint32_t*>(smem + SM_SCR + XZ_OFF)[i] = 0u;
+  if (tid == 0) trace_stamp(P, E.layer * NSTAGE + E.st, NW + 6);
   // 5. the RMSNorm factor
-  if (want_ss) {
-#pragma unroll
-    for (int b = 0; b < NARROW_B; ++b) {
-      const float r = warp_sum(ssq[b]);
-      if (lane == 0 && b < B) M.red[warp][2 * b] = r;
-    }
-  }
   csync();
   if (tid < B) {
     float ss = 0.f;
@@ -680,7 +706,6 @@ __device__ __noinline__ void gemv_prologue(const Params& P, const GemvCtx& E, ui
       for (int w = 0; w < NW; ++w) ss += M.red[w][2 * tid];
     M.rnorm[tid] = nw ? 1.0f / sqrtf(ss / (float)K + P.eps) : 1.0f;
   }
-  if (tid == 0) trace_stamp(P, E.layer * NSTAGE + E.st, NW + 6);
   csync();
 }
 
@@ -688,7 +713,7 @@ __device__ __noinline__ void gemv_prologue(const Params& P, const GemvCtx& E, ui
 // Norm weight r of the next weight stage, for the output maxima: from the copy
 // that this stage's prologue staged in shared memory when the vector fits.
 __device__ __forceinline__ float epi_norm(const Params& P, const uint16_t* w, int r) {
-  return (int64_t)P.D * 2 <= SM_NW_BYTES ? bf16_bits_to_f32(reinterpret_cast<const uint16_t*>(g_smem + SM_NW)[r])
+  return (int64_t)P.D * 2 <= NW_HS_OFF ? bf16_bits_to_f32(reinterpret_cast<const uint16_t*>(g_smem + SM_NW)[r])
                                          : bf16_bits_to_f32(__ldg(w + r));
 }
 
@@ -727,25 +752,60 @@ __device__ __noinline__ void gemv_epilogue(const Params& P, const GemvCtx& E, in
     const float y0 = x0 + v0, y1 = x1 + v1;
     P.y[o + r0] = y0;
     P.y[o + r1] = y1;
-    // the gate/up stage scales its staged x by this max of |y * norm2|
     const uint16_t* w2 = sp().layers[E.layer].norm2;
-    const float m = fmaxf(fabsf(y0 * epi_norm(P, w2, r0)), fabsf(y1 * epi_norm(P, w2, r1)));
-    atomicMax(&M.cmax[t], __float_as_uint(m));
+    const float yw0 = y0 * epi_norm(P, w2, r0), yw1 = y1 * epi_norm(P, w2, r1);
+    if (P.ximg[0]) {  // the gate/up stage's fragments of y * norm2, their sums, sums of y^2
+      uint8_t* img = img_out(P, E.layer, E.st);
+      const float f0 = tile_half_sum(img_put(img, P.B, r0, t, yw0), P.B);
+      const float f1 = tile_half_sum(img_put(img, P.B, r1, t, yw1), P.B);
+      const float q0 = tile_half_sum(y0 * y0, P.B), q1 = tile_half_sum(y1 * y1, P.B);
+      if (g == 0) {
+        float* hs = img_hsum(img, P.B, P.D);
+        float* hq = img_hsq(img, P.B, P.D);
+        hs[(2 * T) * P.B + t] = f0;
+        hs[(2 * T + 1) * P.B + t] = f1;
+        hq[(2 * T) * P.B + t] = q0;
+        hq[(2 * T + 1) * P.B + t] = q1;
+      }
+    } else if (P.B > NARROW_B) {  // the gate/up stage scales its staged x by this max of |y * norm2|
+      atomicMax(&M.cmax[t], __float_as_uint(fmaxf(fabsf(yw0), fabsf(yw1))));
+    }
   } else if (E.st == ST_GU) {
     const float r = M.rnorm[t], gt = v0 * r, up = v1 * r;
     const float av = gt / (1.0f + expf(-gt)) * up;
     P.a[(int64_t)t * P.dff + 8 * T + g] = av;
-    atomicMax(&M.cmax[t], __float_as_uint(fabsf(av)));
+    if (P.ximg[0]) {  // the down stage's fragments of a and their sums (half slice T)
+      uint8_t* img = img_out(P, E.layer, E.st);
+      const float f = tile_half_sum(img_put(img, P.B, 8 * T + g, t, av), P.B);
+      if (g == 0) img_hsum(img, P.B, P.dff)[T * P.B + t] = f;
+    } else if (P.B > NARROW_B) {
+      atomicMax(&M.cmax[t], __float_as_uint(fabsf(av)));
+    }
   } else {
     const int r0 = 16 * T + g, r1 = r0 + 8;
     const int64_t o = (int64_t)t * P.D;
     const float z0 = (have_res ? res0 : __ldcg(P.y + o + r0)) + v0, z1 = (have_res ? res1 : __ldcg(P.y + o + r1)) + v1;
     E.zout[o + r0] = z0;
     E.zout[o + r1] = z1;
-    if (E.layer + 1 < P.L) {  // the next layer's QKV scales its staged x by max |z * norm1|
+    if (E.layer + 1 < P.L) {  // the next layer's QKV input: fragments of z * norm1, or their max
       const uint16_t* w1 = sp().layers[E.layer + 1].norm1;
-      const float m = fmaxf(fabsf(z0 * epi_norm(P, w1, r0)), fabsf(z1 * epi_norm(P, w1, r1)));
-      atomicMax(&M.cmax[t], __float_as_uint(m));
+      const float zw0 = z0 * epi_norm(P, w1, r0), zw1 = z1 * epi_norm(P, w1, r1);
+      if (P.ximg[0]) {
+        uint8_t* img = img_out(P, E.layer, E.st);
+        const float f0 = tile_half_sum(img_put(img, P.B, r0, t, zw0), P.B);
+        const float f1 = tile_half_sum(img_put(img, P.B, r1, t, zw1), P.B);
+        const float q0 = tile_half_sum(z0 * z0, P.B), q1 = tile_half_sum(z1 * z1, P.B);
+        if (g == 0) {
+          float* hs = img_hsum(img, P.B, P.D);
+          float* hq = img_hsq(img, P.B, P.D);
+          hs[(2 * T) * P.B + t] = f0;
+          hs[(2 * T + 1) * P.B + t] = f1;
+          hq[(2 * T) * P.B + t] = q0;
+          hq[(2 * T + 1) * P.B + t] = q1;
+        }
+      } else if (P.B > NARROW_B) {
+        atomicMax(&M.cmax[t], __float_as_uint(fmaxf(fabsf(zw0), fabsf(zw1))));
+      }
     }
     if (E.final_layer) {
       if (P.resid_out) {
@@ -979,7 +1039,8 @@ __device__ __noinline__ void gemv_prep(const Params& P, int layer, int st, uint8
   const uint16_t* nw = st == ST_QKV ? Ld.norm1 : st == ST_GU ? Ld.norm2 : nullptr;
   const uint16_t* nw_next = st == ST_WO ? Ld.norm2
                             : (st == ST_DOWN && layer + 1 < P.L) ? sp().layers[layer + 1].norm1 : nullptr;
-  if ((int64_t)P.D * 2 > SM_NW_BYTES) nw_next = nullptr;
+  if ((int64_t)P.D * 2 > NW_HS_OFF) nw_next = nullptr;
+  if (img_in(P, layer, st)) nw = nullptr;  // the image carries x * norm weight already
   const int kc_lo = m.pk[pnl], nkc = m.pk[pnl + 1] - kc_lo;
   const int ngr = nkc * GC, ngv = (nkc - 1) * GC + chunk_groups(m, kc_lo + nkc - 1);
   // A whole-vector panel of QKV (after the previous layer's down stage) or of
@@ -1233,7 +1294,7 @@ __device__ __noinline__ void gemv_prologue_wide(const Params& P, const GemvCtx& 
     case ST_GU: x32 = P.y; nw = Ld.norm2; break;
     default: x32 = P.a; nw_next = E.layer + 1 < P.L ? sp().layers[E.layer + 1].norm1 : nullptr; break;
   }
-  if ((int64_t)P.D * 2 > SM_NW_BYTES) nw_next = nullptr;
+  if ((int64_t)P.D * 2 > NW_HS_OFF) nw_next = nullptr;
   const int K = m.K;
   const int ngr = nkc * GC;
   const int ngv = (nkc - 1) * GC + chunk_groups(m, kc_lo + nkc - 1);
@@ -1702,8 +1763,8 @@ __device__ __forceinline__ void merge_head(const float* recs, int REC, int first
 // 2 NW from global memory in rounds of 8).  A record whose factor is 0 (a
 // CTA without tiles holds none) is skipped, whatever its memory holds.
 template <int HD>
-__device__ __noinline__ void merge_sequence(const Params& P, int64_t seq, int64_t Ta, int64_t C, int64_t cf,
-                                            int n, float* stage, float* fac, Misc& M) {
+__device__ __noinline__ void merge_sequence(const Params& P, int layer, int64_t seq, int64_t Ta, int64_t C,
+                                            int64_t cf, int n, float* stage, float* fac, Misc& M) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int GH = P.GH, REC = att_rec_floats(GH, HD);
   const float* base = P.apart + seq * P.J_att * REC;
@@ -1754,6 +1815,7 @@ __device__ __noinline__ void merge_sequence(const Params& P, int64_t seq, int64_
   cp_async_wait_all();
   csync();
   const int64_t b = seq / P.Hkv, kvh = seq % P.Hkv;
+  float fsum = 0.f;
   if (act) {
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     auto add = [&](float fj, float4 x) {
@@ -1779,8 +1841,24 @@ __device__ __noinline__ void merge_sequence(const Params& P, int64_t seq, int64_
     }
     float* dst = P.attn + b * P.Hq * HD + (kvh * GH + h) * HD;
     reinterpret_cast<float4*>(dst)[dq] = acc;
-    const float m = fmaxf(fmaxf(fabsf(acc.x), fabsf(acc.y)), fmaxf(fabsf(acc.z), fabsf(acc.w)));
-    if (b < MAX_B) atomicMax(&M.cmax[b], __float_as_uint(m));  // the Wo stage scales its staged x by this
+    if (P.ximg[0]) {  // the Wo stage's fragments of the attention output
+      uint8_t* img = img_out(P, layer, ST_ATT);
+      const int64_t k = (kvh * GH + h) * HD + 4 * dq;
+      float f = img_put(img, P.B, k, (int)b, acc.x);
+      f += img_put(img, P.B, k + 1, (int)b, acc.y);
+      f += img_put(img, P.B, k + 2, (int)b, acc.z);
+      f += img_put(img, P.B, k + 3, (int)b, acc.w);
+      fsum = f;
+    } else if (P.B > NARROW_B) {  // the Wo stage scales its staged x by this
+      const float m = fmaxf(fmaxf(fabsf(acc.x), fabsf(acc.y)), fmaxf(fabsf(acc.z), fabsf(acc.w)));
+      if (b < MAX_B) atomicMax(&M.cmax[b], __float_as_uint(m));
+    }
+  }
+  // the half slice's other four elements are thread dq ^ 1's (the next lane)
+  fsum += __shfl_xor_sync(FULL, fsum, 1);
+  if (P.ximg[0] && act && (dq & 1) == 0) {
+    const int64_t k = (kvh * GH + h) * HD + 4 * dq;
+    img_hsum(img_out(P, layer, ST_ATT), P.B, P.Hq * HD)[(k >> 3) * P.B + b] = fsum;
   }
   csync();
 }
@@ -2045,7 +2123,7 @@ __device__ __forceinline__ bool stage_att_body(const Params& P, int layer, Ring&
     float* fac = recs + NW * 2 * REC;  // per (head, record) factors of the merge
     for (int64_t sq = s0; sq <= s1; ++sq)
       if (M.mseq[(int)(sq - s0)] == sq)
-        merge_sequence<HD>(P, sq, Ta, C, A.cf[sq - s0], A.span[sq - s0], recs, fac, M);
+        merge_sequence<HD>(P, layer, sq, Ta, C, A.cf[sq - s0], A.span[sq - s0], recs, fac, M);
   }
   return true;
 }
@@ -2293,7 +2371,7 @@ static int device_info(DevInfo& out) {
 }
 
 struct WsLayout {
-  int64_t ctrl, cnt, seqcnt, xmax, gpart, apart, Z, q, attn, y, a, tc, total;
+  int64_t ctrl, cnt, seqcnt, xmax, gpart, apart, Z, q, attn, y, a, ximg, ximg_bytes, tc, total;
 };
 
 static int64_t att_J(int64_t seqs, int64_t nt, int64_t C) {
@@ -2331,6 +2409,13 @@ static void ws_layout(const ddl_shape& s, int B, int64_t s_max, int C, const Mat
   w.attn = off;  off = align256(off + (int64_t)B * Nq * 4);
   w.y = off;     off = align256(off + (int64_t)B * s.D * 4);
   w.a = off;     off = align256(off + (int64_t)B * s.d_ff * 4);
+  // fragment images of a weight stage's input (fp16 high part and remainder
+  // per element), two by stage parity; batches up to NARROW_B
+  int64_t kmax = s.D > s.d_ff ? s.D : s.d_ff;
+  if (Nq > kmax) kmax = Nq;
+  w.ximg = off;
+  w.ximg_bytes = B <= NARROW_B ? align256(kmax * 4 * B) + align256(2 * (kmax / 8) * B * 4) : 0;
+  off += 2 * w.ximg_bytes;
   w.tc = off;  // the tensor-core path's partials, operand images and sums (batches past NARROW_B)
   if (B > NARROW_B) off = align256(off + tc_workspace_bytes(s, B, DDL_W_INT4));
   w.total = off;
@@ -2445,6 +2530,11 @@ static int decode(const ddl_shape* s, ddl_wtype wtype, const ddl_layer_w* layers
   P.gpart = (float*)(ws + w.gpart); P.apart = (float*)(ws + w.apart); P.Z = (float*)(ws + w.Z);
   P.q = (float*)(ws + w.q); P.attn = (float*)(ws + w.attn); P.y = (float*)(ws + w.y);
   P.a = (float*)(ws + w.a);
+  P.ximg[0] = P.ximg[1] = nullptr;
+  if (wtype == DDL_W_INT4 && w.ximg_bytes > 0 && (int64_t)s->D / 8 * B * 4 <= NW_HS_OFF) {
+    P.ximg[0] = ws + w.ximg;
+    P.ximg[1] = ws + w.ximg + w.ximg_bytes;
+  }
   cudaStream_t cs = (cudaStream_t)stream;
   cudaError_t e = cudaMemsetAsync(ws, 0, (size_t)w.gpart, cs);  // barrier, status, counters
   if (e != cudaSuccess) return cuda_status(e);

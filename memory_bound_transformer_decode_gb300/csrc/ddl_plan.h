@@ -222,6 +222,7 @@ struct Params {
   float* attn;          // [B][Hq*hd]
   float* y;             // [B][D]
   float* a;             // [B][dff]
+  uint8_t* ximg[2];     // INT4, B <= 4: fp16 fragment images of the next weight stage's input, by stage parity (or NULL)
   uint64_t* trace;      // optional: per stage, CTA: start, prologue end, NW warp ends, end, 4 prologue steps (ns)
   LayerDev layers[MAX_LAYERS];
   // 2-D views [B * H_kv * s_max rows][hd] of each layer's K and V caches for
