@@ -285,8 +285,8 @@ int ddl_test_hold_barrier(int32_t stage);
  * %clock64 (SM cycles) at the end of the stage prologue (word 1), the end
  * of each of the 8 consumer warps' streams (words 2..9), the stage end (word
  * 10), and inside a weight stage's prologue: x copies issued (word 11), x
- * landed (word 13), fragments and RMSNorm factor done (word 14); word 12 is
- * not written; word 15 = %clock64 at the stage start; words 16..23 = the
+ * landed (word 13), fragments and RMSNorm factor done (word 14), the
+ * prologue's entry (word 12); word 15 = %clock64 at the stage start; words 16..23 = the
  * cycles each consumer warp waited for its ring's data, words 24..31 = the
  * ring slots it consumed.  Needs L * 5 * SMs * 32 * 8 bytes.  NULL turns
  * tracing off. */

@@ -440,6 +440,33 @@ __device__ __forceinline__ void trace_stamp(const Params& P, int s, int slot) {
 
 
 
+// ------------------------------------------------------------------ grid barrier
+// Arrival: the CTA's writes of this stage (ordered before by the block
+// barrier) become visible no later than the release.  The wait (acquiring
+// polls) orders the next stage's reads after every CTA's arrival; between
+// the two the CTA prepares its next stage.
+__device__ void grid_arrive(const Params& P) {
+  csync();
+  if (threadIdx.x == NTHREADS - 32) red_release_gpu_add(P.ctrl, 1u);  // not thread 0: see gemv_prep
+}
+__device__ __forceinline__ bool grid_wait(const Params& P, uint32_t target, Misc& M) {
+  if (threadIdx.x == 0) {
+    uint64_t t0 = 0;
+    for (uint32_t it = 1; ld_acquire_gpu(P.ctrl) < target; ++it) {
+      if ((it & 255u) != 0) continue;
+      const uint64_t now = globaltimer();
+      if (t0 == 0) t0 = now;
+      else if (now - t0 > P.wait_ns) {
+        atomicExch(P.ctrl + 1, STATUS_TIMEOUT);
+        M.abort = 1;
+        break;
+      }
+    }
+  }
+  csync();
+  return !M.abort;
+}
+
 // ------------------------------------------------------------------ GEMV prologue
 // Stages this CTA's panel of the activation (k-chunks pk[p]..pk[p+1]-1) as
 // m16n8k16 B fragments: column 2b is the fp16 "high" part of sequence b's
@@ -507,7 +534,7 @@ __device__ __forceinline__ bool img_in(const Params& P, int layer, int st) {
 }
 
 template <int HD, int WT>
-__device__ __noinline__ void gemv_prologue(const Params& P, const GemvCtx& E, uint8_t* smem, Misc& M) {
+__device__ __forceinline__ void gemv_prologue(const Params& P, const GemvCtx& E, uint8_t* smem, Misc& M) {
   const MatGeom& m = E.m;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int B = P.B;
@@ -536,6 +563,7 @@ __device__ __noinline__ void gemv_prologue(const Params& P, const GemvCtx& E, ui
   //    before the barrier, so it does not queue behind them), completed on
   //    the x barrier; else quad i = (gs * B + b) * 16 + q16 of x to quad
   //    q16 % 4 of its unit.
+  if (tid == 0) trace_stamp(P, E.layer * NSTAGE + E.st, NW + 4);
   csync();
   const bool bulk = from_img || (B == 1 && x32 != nullptr);
   const uint32_t xbar = smem_addr(smem + SM_XBAR), xpar = M.xuse & 1u;
@@ -1153,27 +1181,39 @@ __device__ __forceinline__ bool gemv_slot(const Params& P, const Ring& R, uint32
 // sums join the tile sums in true scale, and a tile is finished when the
 // warp leaves it.
 template <int HD, int WT, int NB>
-__device__ __forceinline__ bool stage_gemv_body(const Params& P, int layer, int st, Ring& R, uint8_t* smem, Misc& M);
+__device__ __forceinline__ bool stage_gemv_body(const Params& P, int layer, int st, Ring& R, uint8_t* smem, Misc& M,
+                                                bool wait, uint32_t target);
 // The ring lives in registers while the stage runs.
 template <int HD, int WT>
 __device__ __noinline__ bool stage_gemv_wide(const Params& P, int layer, int st, Ring& Rm, uint8_t* smem, Misc& M);
 template <int HD, int WT>
-__device__ __noinline__ bool stage_gemv(const Params& P, int layer, int st, Ring& Rm, uint8_t* smem, Misc& M) {
+__device__ __noinline__ bool stage_gemv(const Params& P, int layer, int st, Ring& Rm, uint8_t* smem, Misc& M,
+                                        bool wait, uint32_t target) {
   __syncwarp();
   Ring R = Rm;
   // the batch is a template parameter of the stream, so that the x fragments'
   // strides are constants
-  const bool ok = P.B == 1   ? stage_gemv_body<HD, WT, 1>(P, layer, st, R, smem, M)
-                  : P.B == 2 ? stage_gemv_body<HD, WT, 2>(P, layer, st, R, smem, M)
-                  : P.B == 3 ? stage_gemv_body<HD, WT, 3>(P, layer, st, R, smem, M)
-                             : stage_gemv_body<HD, WT, 4>(P, layer, st, R, smem, M);
+  const bool ok = P.B == 1   ? stage_gemv_body<HD, WT, 1>(P, layer, st, R, smem, M, wait, target)
+                  : P.B == 2 ? stage_gemv_body<HD, WT, 2>(P, layer, st, R, smem, M, wait, target)
+                  : P.B == 3 ? stage_gemv_body<HD, WT, 3>(P, layer, st, R, smem, M, wait, target)
+                             : stage_gemv_body<HD, WT, 4>(P, layer, st, R, smem, M, wait, target);
   __syncwarp();
   Rm = R;
   __syncwarp();
   return ok;
 }
 template <int HD, int WT, int NB>
-__device__ __forceinline__ bool stage_gemv_body(const Params& P, int layer, int st, Ring& R, uint8_t* smem, Misc& M) {
+__device__ __forceinline__ bool stage_gemv_body(const Params& P, int layer, int st, Ring& R, uint8_t* smem, Misc& M,
+                                                bool wait, uint32_t target) {
+  // The grid barrier in front of the stage is waited for here, so that the
+  // code after it (the prologue's copies) follows the polling loop in
+  // instruction memory instead of being fetched cold once the barrier opens.
+  if (wait) {
+    if (!grid_wait(P, target, M)) return false;
+  } else {
+    csync();  // the stage context
+  }
+  if (threadIdx.x == 0) trace_stamp(P, layer * NSTAGE + st, 0);
   GemvCtx& E = ctx().E;  // filled by gemv_prep
   const MatGeom& m = E.m;
   gemv_prologue<HD, WT>(P, E, smem, M);
@@ -2138,33 +2178,6 @@ __device__ __noinline__ void flush_cmax(const Params& P, Misc& M, int layer, int
   M.cmax[threadIdx.x] = 0u;
 }
 
-// ------------------------------------------------------------------ grid barrier
-// Arrival: the CTA's writes of this stage (ordered before by the block
-// barrier) become visible no later than the release.  The wait (acquiring
-// polls) orders the next stage's reads after every CTA's arrival; between
-// the two the CTA prepares its next stage.
-__device__ void grid_arrive(const Params& P) {
-  csync();
-  if (threadIdx.x == NTHREADS - 32) red_release_gpu_add(P.ctrl, 1u);  // not thread 0: see gemv_prep
-}
-__device__ bool grid_wait(const Params& P, uint32_t target, Misc& M) {
-  if (threadIdx.x == 0) {
-    uint64_t t0 = 0;
-    for (uint32_t it = 1; ld_acquire_gpu(P.ctrl) < target; ++it) {
-      if ((it & 255u) != 0) continue;
-      const uint64_t now = globaltimer();
-      if (t0 == 0) t0 = now;
-      else if (now - t0 > P.wait_ns) {
-        atomicExch(P.ctrl + 1, STATUS_TIMEOUT);
-        M.abort = 1;
-        break;
-      }
-    }
-  }
-  csync();
-  return !M.abort;
-}
-
 // ------------------------------------------------------------------ producer
 // Lane w (< NW) of the producer warp fills consumer warp w's ring: it walks
 // the warp's slots of every stage of the launch with its own cursor and
@@ -2284,24 +2297,32 @@ __global__ void __launch_bounds__(NTHREADS_ALL, 1) decode_kernel(const __grid_co
   for (int s = P.stage_begin; s < P.stage_end && ok; ++s) {
     const int layer = s / NSTAGE, st = s % NSTAGE;
     if (st != ST_ATT) gemv_prep(P, layer, st, smem);
-    if (s != P.stage_begin && P.cooperative) {
-      // (a held barrier waits for one arrival more than the grid makes: its
-      // bounded wait gives up and the call reports a timeout)
-      const uint32_t target = (uint32_t)(s - P.stage_begin) * gridDim.x + (P.l0 * NSTAGE + s == P.hold_stage);
-      if (!grid_wait(P, target, M)) {
+    // (a held barrier waits for one arrival more than the grid makes: its
+    // bounded wait gives up and the call reports a timeout)
+    const bool wait = s != P.stage_begin && P.cooperative;
+    const uint32_t target = (uint32_t)(s - P.stage_begin) * gridDim.x + (P.l0 * NSTAGE + s == P.hold_stage);
+    if (st != ST_ATT && !WIDE) {  // the narrow GEMV stage waits for its barrier itself
+      stage_gemv<HD, WT>(P, layer, st, R, smem, M, wait, target);
+      if (M.abort) {
         ok = false;
         break;
       }
     } else {
-      csync();  // the stage context
-    }
-    if (threadIdx.x == 0) trace_stamp(P, s, 0);
-    if (st == ST_ATT) {
-      if (threadIdx.x == 0) trace_stamp(P, s, 1);
-      ok = stage_att<HD, WT>(P, layer, R, smem, M);
-    } else {
-      if constexpr (WIDE) stage_gemv_wide<HD, WT>(P, layer, st, R, smem, M);
-      else stage_gemv<HD, WT>(P, layer, st, R, smem, M);
+      if (wait) {
+        if (!grid_wait(P, target, M)) {
+          ok = false;
+          break;
+        }
+      } else {
+        csync();  // the stage context
+      }
+      if (threadIdx.x == 0) trace_stamp(P, s, 0);
+      if (st == ST_ATT) {
+        if (threadIdx.x == 0) trace_stamp(P, s, 1);
+        ok = stage_att<HD, WT>(P, layer, R, smem, M);
+      } else {
+        stage_gemv_wide<HD, WT>(P, layer, st, R, smem, M);
+      }
     }
     csync();
     if (threadIdx.x == 0) trace_stamp(P, s, NW + 2);
