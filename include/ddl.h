@@ -153,7 +153,7 @@ int ddl_workspace_view(const ddl_shape* shape, int32_t B, int64_t s_max, ddl_ws_
  * position pos.  INT4 weights at B >= 16 and bf16 weights at B >= 5 run their
  * matrix products on the tcgen05 tensor cores (weights as fp16 code * scale,
  * exact for group scales in [2^-17, 9357]; bf16 weights converted to fp16,
- * exact for |w| >= 2^-17; activations as three fp16 limbs), smaller batches on
+ * exact for |w| >= 2^-17; activations as two fp16 limbs), smaller batches on
  * warp-level tensor-core MMAs inside one persistent kernel.  The step:
  * writes KV slot pos and attends over slots 0..pos (the caller keeps slots
  * < pos filled).  Input: resid_in [B][D] fp32, or x_bf16 [B][D] bf16 when

@@ -77,6 +77,26 @@ __device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, ui
   }
 }
 
+// The same wait with a pause of about nap_ns between polls, for warps whose
+// wait is long and off the critical path (their polls would take issue slots
+// from the warps doing the work).
+__device__ __forceinline__ bool mbar_wait_warp_nap(uint32_t bar, uint32_t parity, uint32_t* status,
+                                                   uint64_t limit_ns, uint32_t nap_ns) {
+  uint64_t t0 = 0;
+  for (uint32_t it = 1;; ++it) {
+    if (__all_sync(FULL, mbar_try_wait(bar, parity))) return true;
+    __nanosleep(nap_ns);
+    if ((it & 63u) == 0) {
+      const uint64_t now = __shfl_sync(FULL, globaltimer(), 0);
+      if (t0 == 0) t0 = now;
+      else if (now - t0 > limit_ns) {
+        if ((threadIdx.x & 31) == 0) atomicExch(status, STATUS_TIMEOUT);
+        return false;
+      }
+    }
+  }
+}
+
 // ---------------------------------------------------------------- roles
 // Block barrier of the consumer warps only (barrier 1, 256 threads); the
 // producer warp never takes part.

@@ -6,7 +6,7 @@
 // GEMM kernel (one launch per weight stage): a CTA takes units of 128 weight
 // rows (eight of the packed stream's 16-row tiles) by a range of 64-wide
 // groups of the input dimension.  Warp 0 copies each group's eight packed
-// blocks and the group's B-operand image (the activations as fp16 limbs, laid
+// blocks and the group's B-operand image (the activations as two fp16 limbs, laid
 // out as the tensor core reads them) into a ring of shared-memory stages with
 // TMA bulk copies; warps 4-7 expand the 4-bit codes in registers to fp16
 // code * scale and store them into tensor memory as the A operand (one 32-lane
@@ -14,14 +14,14 @@
 // registers as they are); one thread of warp 1 issues the tcgen05.mma of the
 // group's four 16-wide slices into an fp32 accumulator in tensor memory and
 // commits them to mbarriers that hand the stage and the A buffer back.  At a
-// unit's end warps 4-7 read the accumulator (tcgen05.ld), combine the three
+// unit's end warps 4-7 read the accumulator (tcgen05.ld), combine the two
 // limb columns of each sequence and store the unit's partial sums.
 //
 // Epilogue kernel (one launch per stage): sums a stage's split-K partials in a
 // fixed order and applies what the layer does to that stage's output (RMSNorm
 // factor, RoPE, the K/V append, the residual adds, SwiGLU), and writes the
 // B-operand image of the next GEMM's input (the activations times the next
-// RMSNorm weight, three fp16 limbs each) with per-CTA sums of squares.
+// RMSNorm weight, as two fp16 limbs) with per-CTA sums of squares.
 #include <math.h>
 
 #include <cuda_fp16.h>
@@ -301,13 +301,13 @@ __global__ void __launch_bounds__(GT, 1) tc_gemm_kernel(const __grid_constant__ 
       if (*abort_flag) ok = false;
     }
   } else if (warp >= 4 + 4 * NDW) {  // --------------------------- read-out
-    // the accumulator of each unit: row 32 q + lane, limb columns l * B + b
+    // the accumulator of each unit: row 32 q + lane, limb columns l * B + b (l = 0, 1)
     const int q = warp & 3;
     uint32_t ui = 0;
     for (int u = blockIdx.x; u < P.units; u += gridDim.x, ++ui) {
       const int rt = u % P.NR, s = u / P.NR;
       const uint32_t db = ui % ND, dk = ui / ND;
-      if (!mbar_wait_warp(dready0 + db * 8, dk & 1, P.status, P.wait_ns)) {
+      if (!mbar_wait_warp_nap(dready0 + db * 8, dk & 1, P.status, P.wait_ns, 500)) {  // a unit takes many us
         fail();
         break;
       }
@@ -315,18 +315,15 @@ __global__ void __launch_bounds__(GT, 1) tc_gemm_kernel(const __grid_constant__ 
       const int n = rt * 128 + 32 * q + lane;
       const uint32_t tr = tm + ((uint32_t)(32 * q) << 16) + D_COL0 + db * P.dstride;
       for (int b0 = 0; b0 < P.B; b0 += 16) {
-        uint32_t v0[16], v1[16], v2[16];
+        uint32_t v0[16], v1[16];
         tmem_ld_32x32b_x16(tr + b0, v0);
         tmem_ld_32x32b_x16(tr + P.B + b0, v1);
-        tmem_ld_32x32b_x16(tr + 2 * P.B + b0, v2);
         tmem_ld_wait();
         if (n < P.N) {
           float* dst = P.part + ((int64_t)s * P.N + n) * P.B;
 #pragma unroll
           for (int j = 0; j < 16; ++j)
-            if (b0 + j < P.B)
-              dst[b0 + j] = fmaf(4096.f, __uint_as_float(v0[j]),
-                                 fmaf(1.0f / 4096.f, __uint_as_float(v2[j]), __uint_as_float(v1[j])));
+            if (b0 + j < P.B) dst[b0 + j] = 256.f * (__uint_as_float(v0[j]) + __uint_as_float(v1[j]));
         }
       }
       tc_fence_before();
@@ -374,14 +371,13 @@ __device__ __forceinline__ int64_t limb_offset(int NP, int k, int c) {
   const int kap = (k16 < 8 ? 4 * (k16 >> 1) + (k16 & 1) : 4 * ((k16 - 8) >> 1) + 2 + (k16 & 1)) + 16 * j;
   return (int64_t)(k >> 6) * NP * 128 + (c >> 3) * SBO + (kap >> 3) * LBO + (c & 7) * 16 + (kap & 7) * 2;
 }
+// v * 2^-8 as an fp16 high part (column b) and remainder (column B + b).
 __device__ __forceinline__ void put_limbs(uint8_t* xl, int NP, int B, int k, int b, float v) {
-  const __half h0 = __float2half_rn(v * (1.0f / 4096.f));
-  const float r1 = v - 4096.f * __half2float(h0);
-  const __half h1 = __float2half_rn(r1);
-  const __half h2 = __float2half_rn((r1 - __half2float(h1)) * 4096.f);
+  const float sv = v * (1.0f / 256.f);
+  const __half h0 = __float2half_rn(sv);
+  const __half h1 = __float2half_rn(sv - __half2float(h0));
   *reinterpret_cast<__half*>(xl + limb_offset(NP, k, b)) = h0;
   *reinterpret_cast<__half*>(xl + limb_offset(NP, k, B + b)) = h1;
-  *reinterpret_cast<__half*>(xl + limb_offset(NP, k, 2 * B + b)) = h2;
 }
 
 __global__ void __launch_bounds__(256) tc_epi_kernel(const __grid_constant__ TcEpi E) {
@@ -629,7 +625,7 @@ int tc_stage(const TcRun& R, int layer, int st, void* stream) {
   while (G.gs > 1 && 3 * (al1024(8 * BB * G.gs) + al1024((uint32_t)NP * 128 * G.gs)) > 200u * 1024u) --G.gs;
   // four A buffers (a deeper A ring measured slower), then accumulators of
   // NP columns plus 16 of headroom (the read-out loads 16 columns at a time,
-  // up to column 3B + 14): two when they fit, else one
+  // up to column 2B + 14): two when they fit, else one
   G.dstride = NP + 16;
   G.na = 4;
   G.nd = G.na * A_COLS + 2 * G.dstride <= TMEM_COLS ? 2 : 1;

@@ -12,11 +12,12 @@
 // Numerics.  A (weights) is fp16 holding code * scale exactly: |code| <= 7 is
 // 3 bits and the bf16 scale 8, so the product has at most 11 significant bits
 // (exact for scales in [2^-17, 9357]; bf16 weights are converted to fp16,
-// exact for |w| >= 2^-17).  B (activations) is three fp16 limbs per value at
-// the fixed scales 2^12, 1, 2^-12 (v = 4096 l0 + l1 + l2 / 4096), at least 22
-// significant bits for |v| in [2^-16, 2^27] with no per-vector scale, so the
-// producing epilogue writes them directly.  Products accumulate in fp32 in
-// tensor memory; split-K partials are summed in a fixed order.
+// exact for |w| >= 2^-17).  B (activations) is two fp16 limbs per value at
+// the fixed scale 2^-8 (v = 256 (l0 + l1), l0 the fp16 rounding of v / 256,
+// l1 that of the remainder): ~22 significant bits for |v| >= 32, an absolute
+// 2^-17 below, |v| < 2^24, with no per-vector scale, so the producing
+// epilogue writes them directly.  Products accumulate in fp32 in tensor
+// memory; split-K partials are summed in a fixed order.
 #pragma once
 #include <stdint.h>
 
@@ -30,8 +31,8 @@ constexpr int TC_MAX_B = 64;   // largest batch of the library
 constexpr int TC_EPI_CTAS = 304;
 constexpr int TC_MAX_SPLIT = 8;
 
-// Padded B-operand columns: three limbs per sequence, a multiple of 16.
-inline int tc_ncols(int B) { return (3 * B + 15) & ~15; }
+// Padded B-operand columns: two limbs per sequence, a multiple of 16.
+inline int tc_ncols(int B) { return (2 * B + 15) & ~15; }
 
 struct TcLayer {
   const uint8_t* packed;
