@@ -177,6 +177,19 @@ int ddl_stack_decode(const ddl_shape* shape, ddl_wtype wtype, const ddl_layer_w*
                      const float* resid_in, const uint16_t* x_bf16, float* resid_out,
                      uint16_t* out_bf16, void* workspace, size_t ws_bytes, void* stream);
 
+/* ddl_stack_decode for sequences at their own positions (continuous
+ * batching: sequences that joined at different times decode together; the
+ * primer's §1.3 batching with a per-sequence history): sequence b writes KV
+ * slot pos[b] of its own cache, attends over its slots 0..pos[b] and rotates
+ * q, k by position pos[b].  pos: host array of B positions, each in
+ * [0, s_max) (DDL_ERR_POS otherwise).  Slots past pos[b] may hold anything:
+ * they are neither read into the result nor written.  Other arguments as
+ * ddl_stack_decode; the workspace is sized by ddl_workspace_bytes. */
+int ddl_stack_decode_ragged(const ddl_shape* shape, ddl_wtype wtype, const ddl_layer_w* layers,
+                            const ddl_kv* kv, int32_t L, int32_t B, const int64_t* pos,
+                            const float* resid_in, const uint16_t* x_bf16, float* resid_out,
+                            uint16_t* out_bf16, void* workspace, size_t ws_bytes, void* stream);
+
 /* Size of the library's own static scratch array (32 MiB), used only by
  * ddl_stack_decode_noalloc. */
 #define DDL_NOALLOC_SCRATCH_BYTES (32u << 20)

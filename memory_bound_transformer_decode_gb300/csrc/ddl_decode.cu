@@ -79,6 +79,17 @@ static_assert((SLOT_BYTES % 1024 == 512 && SLOT_BYTES >= 512 + 16 * 128 * 2) ||
               "K/V boxes need 1024-byte boundaries inside 512-byte aligned slots");
 __device__ __forceinline__ const SParams& sp() { return *reinterpret_cast<const SParams*>(g_smem + SM_SPAR); }
 
+// Position of sequence b's new token, its 16-key tiles (the last holds the new
+// token), and the RoPE (cos, sin) of head-dimension pair i at that position.
+__device__ __forceinline__ int64_t seq_pos(const Params& P, int b) { return P.ragged ? P.posb[b] : P.pos; }
+__device__ __forceinline__ int att_tiles(const Params& P, int64_t seq) {
+  return P.ragged ? (int)(P.posb[seq / P.Hkv] / 16) + 1 : P.nt_att;
+}
+__device__ __forceinline__ float2 rope_cs(const Params& P, int b, int i) {
+  if (P.ragged) return *reinterpret_cast<const float2*>(P.rope_b + ((int64_t)b * 64 + i) * 2);
+  return make_float2(sp().rope[i][0], sp().rope[i][1]);
+}
+
 // An empty partial slot word: two all-ones NaNs, a pattern that fp32
 // arithmetic does not produce (its NaN results are canonical).
 constexpr uint64_t PART_EMPTY = ~0ull;
@@ -313,9 +324,22 @@ __device__ __forceinline__ void cursor_enter(const Params& P, Cursor& c, int w) 
 }
 template <int WT>
 __device__ __forceinline__ bool cursor_next(const Params& P, Cursor& c, int w, SlotDesc& d) {
-  while (c.pos >= c.end) {
-    if (++c.s >= P.stage_end) return false;
-    cursor_enter<WT>(P, c, w);
+  for (;;) {
+    while (c.pos >= c.end) {
+      if (++c.s >= P.stage_end) return false;
+      cursor_enter<WT>(P, c, w);
+    }
+    // a sequence whose new token sits before the tile: its remaining tiles
+    // carry no keys, the consumer skips them too (the next sequence's first
+    // tile always holds keys)
+    if (c.st == ST_ATT && P.ragged && (c.pos & 1) == 0 && c.ai >= att_tiles(P, c.aseq)) {
+      c.pos += 2u * (uint32_t)(P.nt_att - c.ai);
+      c.ai = 0;
+      ++c.aseq;
+      c.a = (uint32_t)((int64_t)c.aseq * P.s_max);
+      continue;
+    }
+    break;
   }
   if (c.st == ST_ATT) {  // K then V of one 16-key tile
     d.kind = (c.pos & 1) ? SK_V : SK_K;
@@ -757,7 +781,8 @@ __device__ __noinline__ void gemv_epilogue(const Params& P, const GemvCtx& E, in
     v1 *= r;
     const int tph = HD / 16, head = T / tph, i = 8 * (T % tph) + g;
     if (head < P.Hq + P.Hkv) {  // RoPE on q and k: pair (i, i + hd/2)
-      const float c = sp().rope[i][0], s = sp().rope[i][1], a = v0, b = v1;
+      const float2 cs = rope_cs(P, t, i);
+      const float c = cs.x, s = cs.y, a = v0, b = v1;
       v0 = a * c - b * s;
       v1 = a * s + b * c;
     }
@@ -768,7 +793,7 @@ __device__ __noinline__ void gemv_epilogue(const Params& P, const GemvCtx& E, in
     } else {
       const bool is_k = head < P.Hq + P.Hkv;
       const int kvh = is_k ? head - P.Hq : head - P.Hq - P.Hkv;
-      uint16_t* row = (is_k ? E.kc : E.vc) + (((int64_t)t * P.Hkv + kvh) * P.s_max + P.pos) * HD;
+      uint16_t* row = (is_k ? E.kc : E.vc) + (((int64_t)t * P.Hkv + kvh) * P.s_max + seq_pos(P, t)) * HD;
       row[i] = f32_to_bf16_bits(v0);
       row[i + HD / 2] = f32_to_bf16_bits(v1);
     }
@@ -1771,13 +1796,14 @@ __device__ __forceinline__ void merge_head(const float* recs, int REC, int first
   float mx = recs[first * REC + GH * HD + h];
   for (uint32_t mm = vmask; mm; mm &= mm - 1)
     mx = fmaxf(mx, recs[2 * (__ffs(mm) - 1) * REC + GH * HD + h]);
+  const float mref = mx == -INFINITY ? 0.f : mx;  // records without keys (m = -inf) weigh 0
   float acc[HD / 32], l = 0.f;
 #pragma unroll
   for (int dd = 0; dd < HD / 32; ++dd) acc[dd] = 0.f;
   int ri = first;
   for (uint32_t mm = vmask;;) {
     const float* r = recs + ri * REC;
-    const float f = exp2f(r[GH * HD + h] - mx);
+    const float f = exp2f(r[GH * HD + h] - mref);
     l = fmaf(f, r[GH * HD + GH + h], l);
 #pragma unroll
     for (int dd = 0; dd < HD / 32; ++dd) acc[dd] = fmaf(f, r[h * HD + lane + 32 * dd], acc[dd]);
@@ -1960,6 +1986,7 @@ __device__ __forceinline__ bool stage_att_body(const Params& P, int layer, Ring&
   for (int64_t it = lo; it < hi && ok; ++it) {
     const int64_t seq = (uint32_t)it / (uint32_t)nt;
     const int i = (int)((uint32_t)it - (uint32_t)seq * (uint32_t)nt);
+    const int ntq = att_tiles(P, seq);  // tiles of this sequence holding keys
     if (seq != cur) {
       if (cur >= 0)  // a segment wholly inside this warp (or the warp's first)
         att_flush<HD>(P, nseg == 1 ? recs + (warp * 2) * REC
@@ -1994,6 +2021,10 @@ __device__ __forceinline__ bool stage_att_body(const Params& P, int layer, Ring&
 #pragma unroll
       for (int nb = 0; nb < NB; ++nb) o[nb][0] = o[nb][1] = o[nb][2] = o[nb][3] = 0.f;
     }
+    if (i >= ntq) {  // past the sequence's new token (its record stays empty): the next sequence
+      it = (seq + 1) * nt - 1;
+      continue;
+    }
     // K of this tile in slot R, V in the slot after it.  The K slot goes back
     // to the producer once the scores are computed, and the wait for the
     // next tile's K is made while the P.V MMAs drain.
@@ -2008,9 +2039,10 @@ __device__ __forceinline__ bool stage_att_body(const Params& P, int layer, Ring&
       if (P.trace) wcyc += clock64() - tw;
     }
     if (P.trace) nslots += 2;
-    const bool newtok = i == nt - 1;  // the tile holding the new token
-    const int rnew = (int)(P.pos - 16 * (int64_t)i);
-    const int64_t ro = ((seq * P.s_max) + P.pos) * HD;  // its row in the cache ([seq][s_max][hd])
+    const int64_t pq = seq_pos(P, (int)(seq / P.Hkv));
+    const bool newtok = i == ntq - 1;  // the tile holding the new token
+    const int rnew = (int)(pq - 16 * (int64_t)i);
+    const int64_t ro = ((seq * P.s_max) + pq) * HD;  // its row in the cache ([seq][s_max][hd])
     // the new token's row from the cache (written by the QKV stage after the
     // copy may have been made) and zero rows after it; these generic writes
     // come before the slot's next bulk (async-proxy) fill
@@ -2057,7 +2089,7 @@ __device__ __forceinline__ bool stage_att_body(const Params& P, int layer, Ring&
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
         const int64_t key = 16 * (int64_t)i + 8 * n + 2 * t + e;
-        sv[n][e] = key > P.pos ? -INFINITY : s[n][e] + s[n][e + 2];
+        sv[n][e] = key > pq ? -INFINITY : s[n][e] + s[n][e + 2];
         mt = fmaxf(mt, sv[n][e]);
       }
     mt = fmaxf(mt, __shfl_xor_sync(FULL, mt, 1));
@@ -2095,7 +2127,9 @@ __device__ __forceinline__ bool stage_att_body(const Params& P, int layer, Ring&
       mma_bf16(o[nb + 1], pa0, pa1, pa2, pa3, b2, b3);
     }
     kready = false;
-    if (it + 1 < hi) {  // the next tile's K, while these MMAs drain
+    int64_t nx = it + 1;  // the next tile holding keys: the next one, or the next sequence's first
+    if (P.ragged && nx < hi && nx - seq * nt >= ntq) nx = (seq + 1) * nt;
+    if (nx < hi) {  // the next tile's K, while these MMAs drain
       const Ring Rk = R.next();
       const uint64_t tw = P.trace ? clock64() : 0;
       if (!mbar_wait_warp(Rk.bar(), Rk.phase, P.ctrl + 1, P.wait_ns)) {
@@ -2392,7 +2426,7 @@ static int device_info(DevInfo& out) {
 }
 
 struct WsLayout {
-  int64_t ctrl, cnt, seqcnt, xmax, gpart, apart, Z, q, attn, y, a, ximg, ximg_bytes, tc, total;
+  int64_t ctrl, cnt, seqcnt, xmax, gpart, apart, Z, q, attn, y, a, rope, ximg, ximg_bytes, tc, total;
 };
 
 static int64_t att_J(int64_t seqs, int64_t nt, int64_t C) {
@@ -2430,6 +2464,7 @@ static void ws_layout(const ddl_shape& s, int B, int64_t s_max, int C, const Mat
   w.attn = off;  off = align256(off + (int64_t)B * Nq * 4);
   w.y = off;     off = align256(off + (int64_t)B * s.D * 4);
   w.a = off;     off = align256(off + (int64_t)B * s.d_ff * 4);
+  w.rope = off;  off = align256(off + (int64_t)B * (64 * 2 * 4 + 4));  // ragged positions: RoPE table, positions
   // fragment images of a weight stage's input (fp16 high part and remainder
   // per element), two by stage parity; batches up to NARROW_B
   int64_t kmax = s.D > s.d_ff ? s.D : s.d_ff;
@@ -2483,10 +2518,31 @@ static int encode_kv_map(CUtensorMap* m, const uint16_t* base, int64_t rows, int
   return r == CUDA_SUCCESS ? DDL_OK : DDL_ERR_CUDA;
 }
 
+// RoPE table of sequences at their own positions (fp64 angles, as the host
+// computes the shared one), and the positions as int32 for the epilogues.
+struct RopeFill {
+  int32_t posb[64];
+  double base;
+  int32_t hd, B;
+  float* table;   // [B][64][2]
+  int32_t* pos;   // [B]
+};
+__global__ void rope_fill_kernel(const __grid_constant__ RopeFill R) {
+  const int b = blockIdx.x, i = threadIdx.x;
+  if (b >= R.B) return;
+  if (i < R.hd / 2) {
+    const double phi = (double)R.posb[b] * pow(R.base, -2.0 * i / (double)R.hd);
+    R.table[((int64_t)b * 64 + i) * 2] = (float)cos(phi);
+    R.table[((int64_t)b * 64 + i) * 2 + 1] = (float)sin(phi);
+  }
+  if (i == 0) R.pos[b] = R.posb[b];
+}
+
+// posv: NULL (every sequence at pos) or a host array of B positions (pos unused).
 static int decode(const ddl_shape* s, ddl_wtype wtype, const ddl_layer_w* layers, const ddl_kv* kv,
                   int32_t L, int32_t B, int64_t pos, const float* resid_in, const uint16_t* x_bf16,
                   float* resid_out, uint16_t* out_bf16, void* workspace, size_t ws_bytes,
-                  void* stream) {
+                  void* stream, const int64_t* posv = nullptr) {
   int st = check_shape(s);
   if (st) return st;
   if (!layers || !kv || L <= 0 || !workspace) return !workspace ? DDL_ERR_WORKSPACE : DDL_ERR_ARG;
@@ -2499,6 +2555,13 @@ static int decode(const ddl_shape* s, ddl_wtype wtype, const ddl_layer_w* layers
   if (!resid_in && !x_bf16) return DDL_ERR_ARG;
   const int64_t s_max = kv[0].s_max;
   if ((int64_t)B * s->H_kv * s_max >= (1ll << 31)) return DDL_ERR_UNSUPPORTED;  // K/V tensor-map rows
+  if (posv) {  // the largest position sets the attention's tile count
+    pos = 0;
+    for (int b = 0; b < B; ++b) {
+      if (posv[b] < 0 || posv[b] >= s_max) return DDL_ERR_POS;
+      if (posv[b] > pos) pos = posv[b];
+    }
+  }
   if (pos < 0 || pos >= s_max) return DDL_ERR_POS;
   for (int l = 0; l < L; ++l) {
     if (!layers[l].packed || !layers[l].norm1 || !layers[l].norm2 || !kv[l].k || !kv[l].v)
@@ -2559,6 +2622,21 @@ static int decode(const ddl_shape* s, ddl_wtype wtype, const ddl_layer_w* layers
   cudaStream_t cs = (cudaStream_t)stream;
   cudaError_t e = cudaMemsetAsync(ws, 0, (size_t)w.gpart, cs);  // barrier, status, counters
   if (e != cudaSuccess) return cuda_status(e);
+  if (posv) {
+    RopeFill rf;
+    memset(&rf, 0, sizeof rf);
+    for (int b = 0; b < B; ++b) rf.posb[b] = (int32_t)posv[b];
+    rf.base = s->rope_base;
+    rf.hd = HD;
+    rf.B = B;
+    rf.table = (float*)(ws + w.rope);
+    rf.pos = (int32_t*)(ws + w.rope + (int64_t)B * 64 * 2 * 4);
+    rope_fill_kernel<<<B, 64, 0, cs>>>(rf);
+    if ((e = cudaGetLastError()) != cudaSuccess) return cuda_status(e);
+    P.ragged = 1;
+    for (int b = 0; b < B; ++b) P.posb[b] = (int32_t)posv[b];
+    P.rope_b = rf.table;
+  }
   // empty partial slots (each reader empties the slots it consumed, so they
   // stay empty from stage to stage within a launch)
   if ((e = cudaMemsetAsync(ws + w.gpart, 0xFF, (size_t)(w.apart - w.gpart), cs)) != cudaSuccess)
@@ -2604,6 +2682,8 @@ static int decode(const ddl_shape* s, ddl_wtype wtype, const ddl_layer_w* layers
       R.D = P.D; R.Hq = P.Hq; R.Hkv = P.Hkv; R.hd = HD; R.dff = P.dff; R.B = B; R.GH = P.GH;
       R.wtype = wtype; R.C = C; R.eps = P.eps; R.pos = pos; R.s_max = s_max;
       memcpy(R.rope, P.rope, sizeof R.rope);
+      R.posb = posv ? (const int32_t*)(ws + w.rope + (int64_t)B * 64 * 2 * 4) : nullptr;
+      R.rope_b = posv ? (const float*)(ws + w.rope) : nullptr;
       make_geoms(*s, wtype, R.mg);
       R.layers = tl; R.L = nL; R.l0 = l0; R.final_last = P.final_last;
       R.resid_in = resid_in; R.x_bf16 = x_bf16; R.resid_out = resid_out; R.out_bf16 = out_bf16;
@@ -2695,6 +2775,16 @@ extern "C" int ddl_stack_decode(const ddl_shape* shape, ddl_wtype wtype, const d
                                 uint16_t* out_bf16, void* workspace, size_t ws_bytes, void* stream) {
   return decode(shape, wtype, layers, kv, L, B, pos, resid_in, x_bf16, resid_out, out_bf16,
                 workspace, ws_bytes, stream);
+}
+
+extern "C" int ddl_stack_decode_ragged(const ddl_shape* shape, ddl_wtype wtype, const ddl_layer_w* layers,
+                                       const ddl_kv* kv, int32_t L, int32_t B, const int64_t* pos,
+                                       const float* resid_in, const uint16_t* x_bf16, float* resid_out,
+                                       uint16_t* out_bf16, void* workspace, size_t ws_bytes, void* stream) {
+  if (!pos) return DDL_ERR_ARG;
+  if (B < 1 || B > TC_MAX_B) return DDL_ERR_UNSUPPORTED;
+  return decode(shape, wtype, layers, kv, L, B, 0, resid_in, x_bf16, resid_out, out_bf16, workspace, ws_bytes,
+                stream, pos);
 }
 
 extern "C" int ddl_set_launch_mode(int32_t mode) {

@@ -234,6 +234,9 @@ struct Params {
   float* y;             // [B][D]
   float* a;             // [B][dff]
   uint8_t* ximg[2];     // INT4, B <= 4: fp16 fragment images of the next weight stage's input, by stage parity (or NULL)
+  int32_t ragged;       // sequences at their own positions: posb, rope_b (else every sequence at pos, rope)
+  int32_t posb[64];     // position of sequence b (ragged)
+  const float* rope_b;  // [B][64][2] cos, sin of posb[b] * base^(-2i/hd) (ragged)
   uint64_t* trace;      // optional: per stage, CTA: start, prologue end, NW warp ends, end, 4 prologue steps (ns)
   LayerDev layers[MAX_LAYERS];
   // 2-D views [B * H_kv * s_max rows][hd] of each layer's K and V caches for

@@ -361,6 +361,8 @@ struct TcEpi {
   float* resid_out;          // DOWN of the stack's last layer
   uint16_t* out_bf16;
   float rope[64][2];
+  const int32_t* posb;       // ragged positions: posb[b] (device copy in the run's parameters) or NULL
+  const float* rope_b;       // [B][64][2] with posb
 };
 
 // Position of element k, limb column c of a group's B-operand image.  Inside
@@ -410,7 +412,9 @@ __global__ void __launch_bounds__(256) tc_epi_kernel(const __grid_constant__ TcE
           const float r = rfac[b];
           float v0 = psum(16 * T + gg) * r, v1 = psum(16 * T + gg + 8) * r;
           if (head < E.Hq + E.Hkv) {  // RoPE on q and k: pair (ii, ii + hd/2)
-            const float c = E.rope[ii][0], sn = E.rope[ii][1], x0 = v0, x1 = v1;
+            const float c = E.rope_b ? E.rope_b[((int64_t)b * 64 + ii) * 2] : E.rope[ii][0];
+            const float sn = E.rope_b ? E.rope_b[((int64_t)b * 64 + ii) * 2 + 1] : E.rope[ii][1];
+            const float x0 = v0, x1 = v1;
             v0 = x0 * c - x1 * sn;
             v1 = x0 * sn + x1 * c;
           }
@@ -421,7 +425,8 @@ __global__ void __launch_bounds__(256) tc_epi_kernel(const __grid_constant__ TcE
           } else {
             const bool is_k = head < E.Hq + E.Hkv;
             const int kvh = is_k ? head - E.Hq : head - E.Hq - E.Hkv;
-            uint16_t* row = (is_k ? E.kc : E.vc) + (((int64_t)b * E.Hkv + kvh) * E.s_max + E.pos) * E.hd;
+            const int64_t pb = E.posb ? (int64_t)E.posb[b] : E.pos;
+            uint16_t* row = (is_k ? E.kc : E.vc) + (((int64_t)b * E.Hkv + kvh) * E.s_max + pb) * E.hd;
             row[ii] = f32_to_bf16_bits(v0);
             row[ii + E.hd / 2] = f32_to_bf16_bits(v1);
           }
@@ -542,6 +547,8 @@ TcEpi epi_base(const TcRun& R) {
   E.part = R.part;
   E.ss_K = R.D;
   memcpy(E.rope, R.rope, sizeof E.rope);
+  E.posb = R.posb;
+  E.rope_b = R.rope_b;
   return E;
 }
 

@@ -25,7 +25,7 @@ EXPORTED = ("ddl_quantize_int4", "ddl_packed_layer_bytes", "ddl_pack_layer", "dd
             "ddl_stack_decode_noalloc", "ddl_set_launch_mode", "ddl_set_wait_limit_ns",
             "ddl_test_hold_barrier", "ddl_set_trace", "ddl_read_device_status", "ddl_status_string",
             "ddl_last_cuda_error", "ddl_embed", "ddl_packed_head_bytes", "ddl_pack_head",
-            "ddl_head_workspace_bytes", "ddl_lm_head")
+            "ddl_head_workspace_bytes", "ddl_lm_head", "ddl_stack_decode_ragged")
 
 
 class DDLError(RuntimeError):
@@ -100,6 +100,8 @@ def load(build_if_missing: bool = False):
                                          vp, vp, vp, sz, vp]
         lib.ddl_stack_decode.argtypes = [P(Shape), ctypes.c_int, P(LayerW), P(KV), i32, i32, i64,
                                          vp, vp, vp, vp, vp, sz, vp]
+        lib.ddl_stack_decode_ragged.argtypes = [P(Shape), ctypes.c_int, P(LayerW), P(KV), i32, i32, P(i64),
+                                                vp, vp, vp, vp, vp, sz, vp]
         lib.ddl_stack_decode_noalloc.argtypes = [P(Shape), ctypes.c_int, P(LayerW), P(KV), i32, i32,
                                                  i64, vp, vp, vp, vp, vp]
         lib.ddl_set_launch_mode.argtypes = [i32]
@@ -248,6 +250,22 @@ def ddl_stack_decode(shape: Shape, wtype: int, layers: list, kvs: list, pos: int
                               _ptr(workspace), workspace.numel() * workspace.element_size(),
                               _stream(stream))
     _check("ddl_stack_decode", st)
+
+
+def ddl_stack_decode_ragged(shape: Shape, wtype: int, layers: list, kvs: list, pos, *,
+                            x_bf16: torch.Tensor | None = None, resid_in: torch.Tensor | None = None,
+                            resid_out: torch.Tensor | None = None, out_bf16: torch.Tensor | None = None,
+                            workspace: torch.Tensor, stream=None):
+    """ddl_stack_decode with sequence b at its own position pos[b]."""
+    lib = load()
+    B = (x_bf16 if x_bf16 is not None else resid_in).shape[0]
+    lw, kv = _layers_and_kv(layers, kvs)
+    pv = (ctypes.c_int64 * B)(*[int(p) for p in pos])
+    st = lib.ddl_stack_decode_ragged(ctypes.byref(shape), wtype, lw, kv, len(layers), B, pv,
+                                     _ptr(resid_in), _ptr(x_bf16), _ptr(resid_out), _ptr(out_bf16),
+                                     _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                     _stream(stream))
+    _check("ddl_stack_decode_ragged", st)
 
 
 def ddl_stack_decode_noalloc(shape: Shape, wtype: int, layers: list, kvs: list, pos: int, *,

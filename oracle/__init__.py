@@ -360,3 +360,33 @@ def sample_top_k(logits, k: int, temperature: float, u) -> np.ndarray:
         j = int(np.searchsorted(cdf, u[b], side="right"))  # first j with cdf[j] > u
         out[b] = ids[min(j, ids.size - 1)]
     return out
+
+
+def layer_decode_ragged(shape, layer: dict, kc, vc, pos, x, stages: bool = False):
+    """One decode step of one layer for B sequences each at its own position
+    pos[b] (the primer's §1.2 decode_step per sequence; §1.3 batching of
+    sequences of different lengths): sequence b is the plain step on its own
+    cache, its own input row and its position, independently of the others.
+
+    kc, vc: uint16 [B, H_kv, s_max, hd], slot pos[b] of sequence b written in
+    place.  x: fp64 [B, D].  Returns z [B, D] (and the per-sequence stage
+    outputs stacked, as layer_decode)."""
+    x = np.atleast_2d(np.asarray(x, np.float64))
+    B = x.shape[0]
+    pos = [int(p) for p in pos]
+    zs, sts = [], []
+    for b in range(B):
+        kb = np.ascontiguousarray(kc[b:b + 1])
+        vb = np.ascontiguousarray(vc[b:b + 1])
+        r = layer_decode(shape, layer, kb, vb, pos[b], x[b:b + 1], stages=stages)
+        kc[b:b + 1] = kb
+        vc[b:b + 1] = vb
+        if stages:
+            zs.append(r[0])
+            sts.append(r[1])
+        else:
+            zs.append(r)
+    z = np.concatenate(zs)
+    if not stages:
+        return z
+    return z, {k: np.concatenate([s[k] for s in sts]) for k in sts[0]}

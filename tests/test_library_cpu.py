@@ -109,3 +109,13 @@ def test_token_step_host_checks(lib):
     assert head(k=4) == 8             # sampling without uniforms
     assert head(k=4, u=p, T=0.0) == 8
     assert head(ws=None) == 8
+
+
+def test_ragged_decode_host_checks(lib):
+    s = ddl.Shape(512, 8, 2, 64, 1408, 1e-6, 1e4)
+    p = ctypes.c_void_p(256)
+    pos = (ctypes.c_int64 * 2)(3, 4)
+    assert lib.ddl_stack_decode_ragged(ctypes.byref(s), ddl.INT4, None, None, 1, 2, None, None, p, None, p,
+                                       p, 1 << 20, None) == 8  # no positions
+    assert lib.ddl_stack_decode_ragged(ctypes.byref(s), ddl.INT4, None, None, 1, 65, pos, None, p, None, p,
+                                       p, 1 << 20, None) == 5  # batch past the limit

@@ -481,3 +481,44 @@ def test_sample_top_k_frequencies_match_softmax():
     for j, v in enumerate(top):
         assert abs(np.count_nonzero(toks == v) / n - p[j]) <= 1.0 / n + 1e-12
     assert set(np.unique(toks)) <= set(top.tolist())
+
+
+# ------------------------------------------------------------------ sequences at their own positions
+
+
+def _small_batch(B, S):
+    cfg = configs.SMALL_LAYER.with_(kv_len=S)
+    w = {k: synth.bits(v) for k, v in synth.layer_weights(cfg, 0).items()}
+    lw = oracle.quantized_layer(w)
+    kc, vc = (synth.bits(t).copy() for t in synth.kv_cache(cfg, 0, S + 1, batch=B))
+    x = oracle.bf16_to_f64(synth.bits(synth.input_x(cfg, batch=B)))
+    return cfg, lw, kc, vc, x
+
+
+def test_ragged_equal_positions_is_the_batched_step():
+    cfg, lw, kc, vc, x = _small_batch(3, 40)
+    k1, v1, k2, v2 = kc.copy(), vc.copy(), kc.copy(), vc.copy()
+    z1, s1 = oracle.layer_decode(cfg, lw, k1, v1, 40, x, stages=True)
+    z2, s2 = oracle.layer_decode_ragged(cfg, lw, k2, v2, [40, 40, 40], x, stages=True)
+    np.testing.assert_array_equal(z1, z2)
+    for k in s1:
+        np.testing.assert_array_equal(s1[k], s2[k])
+    np.testing.assert_array_equal(k1, k2)
+    np.testing.assert_array_equal(v1, v2)
+
+
+def test_ragged_sequences_are_independent_and_ignore_slots_past_their_position():
+    cfg, lw, kc, vc, x = _small_batch(3, 40)
+    pos = [0, 17, 40]
+    z = oracle.layer_decode_ragged(cfg, lw, kc.copy(), vc.copy(), pos, x)
+    # junk in the slots past each position changes nothing
+    kj, vj = kc.copy(), vc.copy()
+    for b, p in enumerate(pos):
+        kj[b, :, p + 1:] = 0x7F7F  # a large bf16 value
+        vj[b, :, p + 1:] = 0xFF7F
+    zj = oracle.layer_decode_ragged(cfg, lw, kj, vj, pos, x)
+    np.testing.assert_array_equal(z, zj)
+    # moving sequence 1 changes only sequence 1
+    z2 = oracle.layer_decode_ragged(cfg, lw, kc.copy(), vc.copy(), [0, 30, 40], x)
+    np.testing.assert_array_equal(z[[0, 2]], z2[[0, 2]])
+    assert not np.array_equal(z[1], z2[1])
