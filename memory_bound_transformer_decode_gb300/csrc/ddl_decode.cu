@@ -290,7 +290,9 @@ __device__ __noinline__ void compute_entries(const Params& P) {
     A.n[threadIdx.x] = (uint32_t)(Ta >= C ? cl - cf + 1 : nt);
   }
 }
-template <int WT>
+// RAG: sequences at their own positions (a separate kernel instance, so that
+// the shared-position step carries none of its code).
+template <int WT, bool RAG>
 __device__ __forceinline__ void cursor_enter(const Params& P, Cursor& c, int w) {
   const int st = c.s % NSTAGE;
   c.st = st;
@@ -304,6 +306,12 @@ __device__ __forceinline__ void cursor_enter(const Params& P, Cursor& c, int w) 
     c.a = (uint32_t)((int64_t)c.aseq * P.s_max + 16 * c.ai);
     c.pos *= 2;
     c.end *= 2;
+    if (RAG && c.ai >= att_tiles(P, c.aseq)) {  // the range starts past a sequence's new token
+      c.pos += 2u * (uint32_t)(P.nt_att - c.ai);
+      c.ai = 0;
+      ++c.aseq;
+      c.a = (uint32_t)((int64_t)c.aseq * P.s_max);
+    }
     c.kmap = &P.kmap[c.s / NSTAGE];
     c.vmap = &P.vmap[c.s / NSTAGE];
   } else {
@@ -322,31 +330,21 @@ __device__ __forceinline__ void cursor_enter(const Params& P, Cursor& c, int w) 
     c.a = (uint32_t)c.kc * (uint32_t)c.NT * (uint32_t)c.Gc + (uint32_t)c.T * (uint32_t)c.gk + (uint32_t)c.gi;
   }
 }
-template <int WT>
+template <int WT, bool RAG>
 __device__ __forceinline__ bool cursor_next(const Params& P, Cursor& c, int w, SlotDesc& d) {
-  for (;;) {
-    while (c.pos >= c.end) {
-      if (++c.s >= P.stage_end) return false;
-      cursor_enter<WT>(P, c, w);
-    }
-    // a sequence whose new token sits before the tile: its remaining tiles
-    // carry no keys, the consumer skips them too (the next sequence's first
-    // tile always holds keys)
-    if (c.st == ST_ATT && P.ragged && (c.pos & 1) == 0 && c.ai >= att_tiles(P, c.aseq)) {
-      c.pos += 2u * (uint32_t)(P.nt_att - c.ai);
-      c.ai = 0;
-      ++c.aseq;
-      c.a = (uint32_t)((int64_t)c.aseq * P.s_max);
-      continue;
-    }
-    break;
+  while (c.pos >= c.end) {
+    if (++c.s >= P.stage_end) return false;
+    cursor_enter<WT, RAG>(P, c, w);
   }
   if (c.st == ST_ATT) {  // K then V of one 16-key tile
     d.kind = (c.pos & 1) ? SK_V : SK_K;
     d.a = c.a;
     d.cnt = 16;
     if (c.pos & 1) {  // the next tile
-      if (++c.ai == P.nt_att) {
+      // (sequences at their own positions: tiles past a sequence's new token
+      // hold no keys, and the consumer skips them too)
+      if (++c.ai == P.nt_att || (RAG && c.ai >= att_tiles(P, c.aseq))) {
+        c.pos += 2u * (uint32_t)(P.nt_att - c.ai);
         c.ai = 0;
         ++c.aseq;
         c.a = (uint32_t)((int64_t)c.aseq * P.s_max);
@@ -1951,19 +1949,19 @@ __device__ __forceinline__ void att_flush(const Params& P, float* rec, const flo
   }
 }
 
-template <int HD, int WT>
+template <int HD, int WT, bool RAG>
 __device__ __forceinline__ bool stage_att_body(const Params& P, int layer, Ring& R, uint8_t* smem, Misc& M);
-template <int HD, int WT>
+template <int HD, int WT, bool RAG>
 __device__ __noinline__ bool stage_att(const Params& P, int layer, Ring& Rm, uint8_t* smem, Misc& M) {
   __syncwarp();
   Ring R = Rm;
-  const bool ok = stage_att_body<HD, WT>(P, layer, R, smem, M);
+  const bool ok = stage_att_body<HD, WT, RAG>(P, layer, R, smem, M);
   __syncwarp();
   Rm = R;
   __syncwarp();
   return ok;
 }
-template <int HD, int WT>
+template <int HD, int WT, bool RAG>
 __device__ __forceinline__ bool stage_att_body(const Params& P, int layer, Ring& R, uint8_t* smem, Misc& M) {
   constexpr int KS = HD / 16, NB = HD / 8;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
@@ -1982,11 +1980,12 @@ __device__ __forceinline__ bool stage_att_body(const Params& P, int layer, Ring&
   bool ok = true, kready = false;
   uint64_t wcyc = 0;  // traced: cycles waiting for the ring, slots consumed
   uint32_t nslots = 0;
+  int64_t pq = P.pos;  // the current sequence's position and its tiles holding keys
+  int ntq = nt;
 
   for (int64_t it = lo; it < hi && ok; ++it) {
     const int64_t seq = (uint32_t)it / (uint32_t)nt;
     const int i = (int)((uint32_t)it - (uint32_t)seq * (uint32_t)nt);
-    const int ntq = att_tiles(P, seq);  // tiles of this sequence holding keys
     if (seq != cur) {
       if (cur >= 0)  // a segment wholly inside this warp (or the warp's first)
         att_flush<HD>(P, nseg == 1 ? recs + (warp * 2) * REC
@@ -1994,6 +1993,10 @@ __device__ __forceinline__ bool stage_att_body(const Params& P, int layer, Ring&
                       o, mrun, lrun);
       cur = seq;
       ++nseg;
+      if constexpr (RAG) {  // this sequence's position and tiles holding keys
+        pq = P.posb[seq / P.Hkv];
+        ntq = (int)(pq / 16) + 1;
+      }
       if (first_seq < 0) first_seq = seq;
       const int b = (int)(seq / P.Hkv), kvh = (int)(seq % P.Hkv);
       const float* qp = P.q + (int64_t)b * P.Hq * HD + (int64_t)(kvh * GH + g) * HD;
@@ -2039,7 +2042,6 @@ __device__ __forceinline__ bool stage_att_body(const Params& P, int layer, Ring&
       if (P.trace) wcyc += clock64() - tw;
     }
     if (P.trace) nslots += 2;
-    const int64_t pq = seq_pos(P, (int)(seq / P.Hkv));
     const bool newtok = i == ntq - 1;  // the tile holding the new token
     const int rnew = (int)(pq - 16 * (int64_t)i);
     const int64_t ro = ((seq * P.s_max) + pq) * HD;  // its row in the cache ([seq][s_max][hd])
@@ -2128,7 +2130,7 @@ __device__ __forceinline__ bool stage_att_body(const Params& P, int layer, Ring&
     }
     kready = false;
     int64_t nx = it + 1;  // the next tile holding keys: the next one, or the next sequence's first
-    if (P.ragged && nx < hi && nx - seq * nt >= ntq) nx = (seq + 1) * nt;
+    if (RAG && nx < hi && nx - seq * nt >= ntq) nx = (seq + 1) * nt;
     if (nx < hi) {  // the next tile's K, while these MMAs drain
       const Ring Rk = R.next();
       const uint64_t tw = P.trace ? clock64() : 0;
@@ -2220,7 +2222,7 @@ __device__ __noinline__ void flush_cmax(const Params& P, Misc& M, int layer, int
 // rounds that find nothing to do, stops when the consumers abort or when no
 // ring advanced for the wait limit, and before leaving waits for its copies
 // in flight, so that none lands after the CTA has gone.
-template <int HD, int WT>
+template <int HD, int WT, bool RAG>
 __device__ __noinline__ void producer(const Params& P, uint8_t* smem, Misc& M) {
   const int lane = threadIdx.x & 31;
   const uint64_t policy = policy_evict_first();
@@ -2232,8 +2234,8 @@ __device__ __noinline__ void producer(const Params& P, uint8_t* smem, Misc& M) {
   bool have = false;
   if (lane < NW) {
     c.s = P.stage_begin;
-    cursor_enter<WT>(P, c, lane);
-    have = cursor_next<WT>(P, c, lane, d);
+    cursor_enter<WT, RAG>(P, c, lane);
+    have = cursor_next<WT, RAG>(P, c, lane, d);
   }
   uint32_t n = 0;  // slots issued
   uint64_t t0 = 0;
@@ -2244,7 +2246,7 @@ __device__ __noinline__ void producer(const Params& P, uint8_t* smem, Misc& M) {
     if (have && (n < DEPTH || mbar_test_wait(ebar0 + (n % DEPTH) * 8, ((n / DEPTH) + 1) & 1))) {
       issue_slot<HD, WT>(c, d, slot0 + (n % DEPTH) * SLOT_BYTES, fbar0 + (n % DEPTH) * 8, policy);
       ++n;
-      have = cursor_next<WT>(P, c, lane, d);
+      have = cursor_next<WT, RAG>(P, c, lane, d);
       moved = true;
     }
     if (__any_sync(FULL, moved)) {
@@ -2274,7 +2276,7 @@ __device__ __noinline__ void producer(const Params& P, uint8_t* smem, Misc& M) {
 }
 
 // ------------------------------------------------------------------ the kernel
-template <int HD, int WT, bool WIDE>
+template <int HD, int WT, bool WIDE, bool RAG>
 __global__ void __launch_bounds__(NTHREADS_ALL, 1) decode_kernel(const __grid_constant__ Params P) {
   uint8_t* smem = g_smem;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -2319,7 +2321,7 @@ __global__ void __launch_bounds__(NTHREADS_ALL, 1) decode_kernel(const __grid_co
     regs_dec<PRODUCER_REGS>();
     if (warp == NW) {
       asm volatile("bar.sync 2, %0;" ::"n"(NTHREADS + 32) : "memory");
-      producer<HD, WT>(P, smem, M);
+      producer<HD, WT, RAG>(P, smem, M);
     }
     return;
   }
@@ -2353,7 +2355,7 @@ __global__ void __launch_bounds__(NTHREADS_ALL, 1) decode_kernel(const __grid_co
       if (threadIdx.x == 0) trace_stamp(P, s, 0);
       if (st == ST_ATT) {
         if (threadIdx.x == 0) trace_stamp(P, s, 1);
-        ok = stage_att<HD, WT>(P, layer, R, smem, M);
+        ok = stage_att<HD, WT, RAG>(P, layer, R, smem, M);
       } else {
         stage_gemv_wide<HD, WT>(P, layer, st, R, smem, M);
       }
@@ -2394,13 +2396,15 @@ static int prepare_kernel() {
   cudaGetDevice(&dev);
   if (done[dev]) return DDL_OK;
   if constexpr (WT == DDL_W_INT4) {  // the wide-batch variant
-    cudaError_t e = cudaFuncSetAttribute(decode_kernel<HD, WT, true>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, SM_TOTAL);
+    for (const void* f : {(const void*)decode_kernel<HD, WT, true, false>, (const void*)decode_kernel<HD, WT, true, true>}) {
+      cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, SM_TOTAL);
+      if (e != cudaSuccess) return cuda_status(e);
+    }
+  }
+  for (const void* f : {(const void*)decode_kernel<HD, WT, false, false>, (const void*)decode_kernel<HD, WT, false, true>}) {
+    cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, SM_TOTAL);
     if (e != cudaSuccess) return cuda_status(e);
   }
-  cudaError_t e = cudaFuncSetAttribute(decode_kernel<HD, WT, false>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, SM_TOTAL);
-  if (e != cudaSuccess) return cuda_status(e);
   done[dev] = true;
   return DDL_OK;
 }
@@ -2643,14 +2647,21 @@ static int decode(const ddl_shape* s, ddl_wtype wtype, const ddl_layer_w* layers
     return cuda_status(e);
   const bool coop = di.coop && g_launch_mode == 0 && !use_tc;
   const bool wide = B > NARROW_B;  // INT4, or only the attention stage (tensor-core path)
-  void* fn = HD == 128 ? (wtype == DDL_W_INT4 ? (wide ? (void*)decode_kernel<128, DDL_W_INT4, true>
-                                                      : (void*)decode_kernel<128, DDL_W_INT4, false>)
-                                              : (wide ? (void*)decode_kernel<128, DDL_W_INT4, true>
-                                                      : (void*)decode_kernel<128, DDL_W_BF16, false>))
-                       : (wtype == DDL_W_INT4 ? (wide ? (void*)decode_kernel<64, DDL_W_INT4, true>
-                                                      : (void*)decode_kernel<64, DDL_W_INT4, false>)
-                                              : (wide ? (void*)decode_kernel<64, DDL_W_INT4, true>
-                                                      : (void*)decode_kernel<64, DDL_W_BF16, false>));
+  // (bf16 weights past NARROW_B run only the attention stage, on the INT4 wide instance)
+  const int wsel = (wide || wtype == DDL_W_INT4) ? DDL_W_INT4 : DDL_W_BF16;
+  void* fn = nullptr;
+#define DDL_PICK(HDV, WTV, WIDEV)                                                                           \
+  fn = posv ? (void*)decode_kernel<HDV, WTV, WIDEV, true> : (void*)decode_kernel<HDV, WTV, WIDEV, false>
+  if (HD == 128) {
+    if (wide) DDL_PICK(128, DDL_W_INT4, true);
+    else if (wsel == DDL_W_INT4) DDL_PICK(128, DDL_W_INT4, false);
+    else DDL_PICK(128, DDL_W_BF16, false);
+  } else {
+    if (wide) DDL_PICK(64, DDL_W_INT4, true);
+    else if (wsel == DDL_W_INT4) DDL_PICK(64, DDL_W_INT4, false);
+    else DDL_PICK(64, DDL_W_BF16, false);
+  }
+#undef DDL_PICK
   for (int l0 = 0; l0 < L; l0 += MAX_LAYERS) {
     const int nL = L - l0 < MAX_LAYERS ? L - l0 : MAX_LAYERS;
     P.L = nL;
