@@ -218,8 +218,9 @@ int ddl_stack_decode_noalloc(const ddl_shape* shape, ddl_wtype wtype, const ddl_
 
 /* ------------------------------------------------------------ token step
  * The steps on either side of the layer stack in the primer's §1.2
- * decode_step: `embed(last_token_id)` before it and `sample(x @ W_emb.T)`
- * after it, for a vocabulary of V entries (Unsloth/Qwen-27B article §三:
+ * decode step: the last token's embedding row before it, and after it a token
+ * drawn from the logits of the last hidden state against the embedding table,
+ * for a vocabulary of V entries (Unsloth/Qwen-27B article §三:
  * about 152 thousand, reduced chunk by chunk without forming the
  * distribution over the whole vocabulary). */
 

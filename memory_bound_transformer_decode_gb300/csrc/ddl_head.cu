@@ -1,6 +1,7 @@
 // ddl_head.cu -- the token step around the layer stack ("把基础打牢" primer,
-// §1.2 decode_step: `embed(last_token_id)` before the layers and
-// `sample(x @ W_emb.T)` after them; Unsloth/Qwen-27B article §三: a vocabulary
+// §1.2 decode step: the last token's embedding row before the layers, and
+// after them a token drawn from the logits of the last hidden state against
+// the embedding table; Unsloth/Qwen-27B article §三: a vocabulary
 // of about 152 thousand entries whose logits are produced chunk by chunk).
 //
 //  - embed_kernel: the rows of the bf16 embedding table for B token ids.

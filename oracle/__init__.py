@@ -277,8 +277,9 @@ def layer_decode(shape, layer: dict, kc, vc, pos: int, x, stages: bool = False):
 
 # ---------------------------------------------------------------- token step
 # The steps on either side of the layer stack in the primer's §1.2
-# decode_step: `embed(last_token_id)` before it and `sample(x @ W_emb.T)`
-# after it, with the Unsloth/Qwen-27B article's §三 vocabulary of about
+# decode step: the last token's embedding row before the layers, and after
+# them a token drawn from the logits of the last hidden state against the
+# embedding table, with the Unsloth/Qwen-27B article's §三 vocabulary of about
 # 152 thousand entries.  Readings where the pages are silent: the output
 # matrix is the (tied) embedding table, in the same weight format as the
 # layers (INT4 quantized from the bf16 table, or the bf16 table itself); an
@@ -305,7 +306,7 @@ def embed(table_bf16, tokens) -> np.ndarray:
 
 def lm_head_logits(x, head: OracleMat, norm_w=None, eps: float = 0.0) -> np.ndarray:
     """Logits over the vocabulary of B hidden states (primer §1.2
-    `x[:, -1] @ W_emb.T`): l = W h with h = rmsnorm(x, norm_w) when a final
+    decode step: the last hidden state times the transposed embedding table): l = W h with h = rmsnorm(x, norm_w) when a final
     norm weight is given, else h = x.
 
     x: fp64 [B, D].  head: OracleMat [V, D], INT4 (q, s) or bf16 (w).
