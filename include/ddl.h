@@ -190,6 +190,21 @@ int ddl_stack_decode_ragged(const ddl_shape* shape, ddl_wtype wtype, const ddl_l
                             const float* resid_in, const uint16_t* x_bf16, float* resid_out,
                             uint16_t* out_bf16, void* workspace, size_t ws_bytes, void* stream);
 
+/* Prefill of S <= DDL_MAX_BATCH prompt tokens of one sequence (primer §1.2:
+ * the prompt goes through the layers and its K/V are kept in the cache) as
+ * one batched step: row i is the token at position p0 + i; it writes slot
+ * p0 + i of the sequence's cache and attends over slots 0..p0 + i, the
+ * history and the prompt's rows before it (causal).  kv: the sequence's own
+ * caches, each [1][H_kv][s_max][head_dim]; p0 + S <= s_max (DDL_ERR_POS).
+ * x_bf16 / resid_in: [S][D] (row i the token at p0 + i); outputs [S][D].  A
+ * longer prompt goes in chunks, p0 advancing by S each call.  The workspace
+ * is sized by ddl_workspace_bytes(shape, S, s_max).  Other arguments as
+ * ddl_stack_decode. */
+int ddl_stack_prefill(const ddl_shape* shape, ddl_wtype wtype, const ddl_layer_w* layers,
+                      const ddl_kv* kv, int32_t L, int32_t S, int64_t p0, const float* resid_in,
+                      const uint16_t* x_bf16, float* resid_out, uint16_t* out_bf16, void* workspace,
+                      size_t ws_bytes, void* stream);
+
 /* Size of the library's own static scratch array (32 MiB), used only by
  * ddl_stack_decode_noalloc. */
 #define DDL_NOALLOC_SCRATCH_BYTES (32u << 20)

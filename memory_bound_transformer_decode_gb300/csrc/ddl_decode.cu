@@ -85,6 +85,11 @@ __device__ __forceinline__ int64_t seq_pos(const Params& P, int b) { return P.ra
 __device__ __forceinline__ int att_tiles(const Params& P, int64_t seq) {
   return P.ragged ? (int)(P.posb[seq / P.Hkv] / 16) + 1 : P.nt_att;
 }
+// First cache-view row of attention sequence seq = (b, kv head) (per-sequence
+// positions and prefill, whose rows may share one cache).
+__device__ __forceinline__ int64_t att_row0(const Params& P, int64_t seq) {
+  return (seq / P.Hkv) * P.kv_bstride + (seq % P.Hkv) * P.s_max;
+}
 __device__ __forceinline__ float2 rope_cs(const Params& P, int b, int i) {
   if (P.ragged) return *reinterpret_cast<const float2*>(P.rope_b + ((int64_t)b * 64 + i) * 2);
   return make_float2(sp().rope[i][0], sp().rope[i][1]);
@@ -303,14 +308,14 @@ __device__ __forceinline__ void cursor_enter(const Params& P, Cursor& c, int w) 
   if (st == ST_ATT) {
     c.aseq = (int)(e.lo / (uint32_t)P.nt_att);
     c.ai = (int)(e.lo - (uint32_t)c.aseq * (uint32_t)P.nt_att);
-    c.a = (uint32_t)((int64_t)c.aseq * P.s_max + 16 * c.ai);
+    c.a = (uint32_t)((RAG ? att_row0(P, c.aseq) : (int64_t)c.aseq * P.s_max) + 16 * c.ai);
     c.pos *= 2;
     c.end *= 2;
     if (RAG && c.ai >= att_tiles(P, c.aseq)) {  // the range starts past a sequence's new token
       c.pos += 2u * (uint32_t)(P.nt_att - c.ai);
       c.ai = 0;
       ++c.aseq;
-      c.a = (uint32_t)((int64_t)c.aseq * P.s_max);
+      c.a = (uint32_t)att_row0(P, c.aseq);
     }
     c.kmap = &P.kmap[c.s / NSTAGE];
     c.vmap = &P.vmap[c.s / NSTAGE];
@@ -347,7 +352,7 @@ __device__ __forceinline__ bool cursor_next(const Params& P, Cursor& c, int w, S
         c.pos += 2u * (uint32_t)(P.nt_att - c.ai);
         c.ai = 0;
         ++c.aseq;
-        c.a = (uint32_t)((int64_t)c.aseq * P.s_max);
+        c.a = (uint32_t)(RAG ? att_row0(P, c.aseq) : (int64_t)c.aseq * P.s_max);
       } else {
         c.a += 16;
       }
@@ -791,7 +796,7 @@ __device__ __noinline__ void gemv_epilogue(const Params& P, const GemvCtx& E, in
     } else {
       const bool is_k = head < P.Hq + P.Hkv;
       const int kvh = is_k ? head - P.Hq : head - P.Hq - P.Hkv;
-      uint16_t* row = (is_k ? E.kc : E.vc) + (((int64_t)t * P.Hkv + kvh) * P.s_max + seq_pos(P, t)) * HD;
+      uint16_t* row = (is_k ? E.kc : E.vc) + ((int64_t)t * P.kv_bstride + (int64_t)kvh * P.s_max + seq_pos(P, t)) * HD;
       row[i] = f32_to_bf16_bits(v0);
       row[i + HD / 2] = f32_to_bf16_bits(v1);
     }
@@ -2044,19 +2049,42 @@ __device__ __forceinline__ bool stage_att_body(const Params& P, int layer, Ring&
     if (P.trace) nslots += 2;
     const bool newtok = i == ntq - 1;  // the tile holding the new token
     const int rnew = (int)(pq - 16 * (int64_t)i);
-    const int64_t ro = ((seq * P.s_max) + pq) * HD;  // its row in the cache ([seq][s_max][hd])
-    // the new token's row from the cache (written by the QKV stage after the
-    // copy may have been made) and zero rows after it; these generic writes
-    // come before the slot's next bulk (async-proxy) fill
+    // Rows of the tile written by this step's QKV stage, possibly after the
+    // producer's copy: the new token's, and in a prefill every prompt row from
+    // p0 on (the rows share one cache).  They are reloaded from the cache, and
+    // the rows after the new token zeroed; these generic writes come before
+    // the slot's next bulk (async-proxy) fill.
+    int r_lo = rnew, r_hi = rnew;
+    int64_t ro = ((seq * P.s_max) + pq) * HD;  // the new token's row in the cache ([seq][s_max][hd])
+    bool fix = newtok;
+    if constexpr (RAG) {
+      ro = (att_row0(P, seq) + 16 * (int64_t)i) * HD;  // the tile's first row
+      r_hi = newtok ? rnew : 15;
+      if (P.p0 >= 0) {
+        const int64_t lo = P.p0 - 16 * (int64_t)i;
+        r_lo = lo > 0 ? (int)lo : 0;
+        fix = 16 * (int64_t)i + 15 >= P.p0;
+      }
+    }
     auto patch = [&](uint32_t sl, const uint16_t* cache) {
-      if (lane < HD / 8) sts128(kv_addr(sl, rnew, lane), ldcg_u128(cache + ro + lane * 8));
-      const int nz = (15 - rnew) * (HD / 8);
-      for (int z = lane; z < nz; z += 32)
-        sts128(kv_addr(sl, rnew + 1 + z / (HD / 8), z % (HD / 8)), make_uint4(0u, 0u, 0u, 0u));
+      if constexpr (RAG) {
+        const int n = (r_hi - r_lo + 1) * (HD / 8);
+        for (int z = lane; z < n; z += 32) {
+          const int r = r_lo + z / (HD / 8), ch = z % (HD / 8);
+          sts128(kv_addr(sl, r, ch), ldcg_u128(cache + ro + (int64_t)r * HD + ch * 8));
+        }
+      } else {
+        if (lane < HD / 8) sts128(kv_addr(sl, rnew, lane), ldcg_u128(cache + ro + lane * 8));
+      }
+      if (newtok) {
+        const int nz = (15 - rnew) * (HD / 8);
+        for (int z = lane; z < nz; z += 32)
+          sts128(kv_addr(sl, rnew + 1 + z / (HD / 8), z % (HD / 8)), make_uint4(0u, 0u, 0u, 0u));
+      }
       fence_proxy_async_smem();
       __syncwarp();
     };
-    if (newtok) patch(ks, Ld.kc);
+    if (fix) patch(ks, Ld.kc);
     // scores: rows g = high-part dot products, rows g+8 = low-part ones
     float s[2][4];
 #pragma unroll
@@ -2082,7 +2110,7 @@ __device__ __forceinline__ bool stage_att_body(const Params& P, int layer, Ring&
       }
       if (P.trace) wcyc += clock64() - tw;
     }
-    if (newtok) patch(vs, Ld.vc);
+    if (fix) patch(vs, Ld.vc);
     // online softmax over this tile (score of key 8n + 2t + e = s[n][e] + s[n][e+2])
     float sv[2][2];
     float mt = -INFINITY;
@@ -2546,7 +2574,7 @@ __global__ void rope_fill_kernel(const __grid_constant__ RopeFill R) {
 static int decode(const ddl_shape* s, ddl_wtype wtype, const ddl_layer_w* layers, const ddl_kv* kv,
                   int32_t L, int32_t B, int64_t pos, const float* resid_in, const uint16_t* x_bf16,
                   float* resid_out, uint16_t* out_bf16, void* workspace, size_t ws_bytes,
-                  void* stream, const int64_t* posv = nullptr) {
+                  void* stream, const int64_t* posv = nullptr, bool shared = false) {
   int st = check_shape(s);
   if (st) return st;
   if (!layers || !kv || L <= 0 || !workspace) return !workspace ? DDL_ERR_WORKSPACE : DDL_ERR_ARG;
@@ -2559,6 +2587,7 @@ static int decode(const ddl_shape* s, ddl_wtype wtype, const ddl_layer_w* layers
   if (!resid_in && !x_bf16) return DDL_ERR_ARG;
   const int64_t s_max = kv[0].s_max;
   if ((int64_t)B * s->H_kv * s_max >= (1ll << 31)) return DDL_ERR_UNSUPPORTED;  // K/V tensor-map rows
+  const int64_t kv_rows = (shared ? 1 : (int64_t)B) * s->H_kv * s_max;  // rows of a layer's cache view
   if (posv) {  // the largest position sets the attention's tile count
     pos = 0;
     for (int b = 0; b < B; ++b) {
@@ -2596,6 +2625,8 @@ static int decode(const ddl_shape* s, ddl_wtype wtype, const ddl_layer_w* layers
   P.D = s->D; P.Hq = s->H_q; P.Hkv = s->H_kv; P.hd = HD; P.dff = s->d_ff; P.B = B;
   P.GH = s->H_q / s->H_kv; P.eps = s->eps; P.wtype = wtype; P.rope_base = s->rope_base;
   P.pos = pos; P.s_max = s_max;
+  P.kv_bstride = shared ? 0 : (int64_t)s->H_kv * s_max;
+  P.p0 = -1;
   P.wait_ns = g_wait_ns;
   P.hold_stage = g_hold_stage;
   P.nt_att = (int32_t)((pos + 1 + 15) / 16);
@@ -2639,6 +2670,7 @@ static int decode(const ddl_shape* s, ddl_wtype wtype, const ddl_layer_w* layers
     if ((e = cudaGetLastError()) != cudaSuccess) return cuda_status(e);
     P.ragged = 1;
     for (int b = 0; b < B; ++b) P.posb[b] = (int32_t)posv[b];
+    P.p0 = shared ? (int32_t)posv[0] : -1;
     P.rope_b = rf.table;
   }
   // empty partial slots (each reader empties the slots it consumed, so they
@@ -2673,9 +2705,8 @@ static int decode(const ddl_shape* s, ddl_wtype wtype, const ddl_layer_w* layers
       P.layers[l].norm2 = layers[l0 + l].norm2;
       P.layers[l].kc = kv[l0 + l].k;
       P.layers[l].vc = kv[l0 + l].v;
-      const int64_t rows = (int64_t)B * s->H_kv * s_max;
-      if ((st = encode_kv_map(&P.kmap[l], kv[l0 + l].k, rows, HD)) != DDL_OK ||
-          (st = encode_kv_map(&P.vmap[l], kv[l0 + l].v, rows, HD)) != DDL_OK)
+      if ((st = encode_kv_map(&P.kmap[l], kv[l0 + l].k, kv_rows, HD)) != DDL_OK ||
+          (st = encode_kv_map(&P.vmap[l], kv[l0 + l].v, kv_rows, HD)) != DDL_OK)
         return st;
     }
     const size_t need_trace = (size_t)nL * NSTAGE * C * TRACE_WORDS * 8;
@@ -2694,6 +2725,7 @@ static int decode(const ddl_shape* s, ddl_wtype wtype, const ddl_layer_w* layers
       R.wtype = wtype; R.C = C; R.eps = P.eps; R.pos = pos; R.s_max = s_max;
       memcpy(R.rope, P.rope, sizeof R.rope);
       R.posb = posv ? (const int32_t*)(ws + w.rope + (int64_t)B * 64 * 2 * 4) : nullptr;
+      R.kv_bstride = P.kv_bstride;
       R.rope_b = posv ? (const float*)(ws + w.rope) : nullptr;
       make_geoms(*s, wtype, R.mg);
       R.layers = tl; R.L = nL; R.l0 = l0; R.final_last = P.final_last;
@@ -2796,6 +2828,18 @@ extern "C" int ddl_stack_decode_ragged(const ddl_shape* shape, ddl_wtype wtype, 
   if (B < 1 || B > TC_MAX_B) return DDL_ERR_UNSUPPORTED;
   return decode(shape, wtype, layers, kv, L, B, 0, resid_in, x_bf16, resid_out, out_bf16, workspace, ws_bytes,
                 stream, pos);
+}
+
+extern "C" int ddl_stack_prefill(const ddl_shape* shape, ddl_wtype wtype, const ddl_layer_w* layers,
+                                 const ddl_kv* kv, int32_t L, int32_t S, int64_t p0, const float* resid_in,
+                                 const uint16_t* x_bf16, float* resid_out, uint16_t* out_bf16, void* workspace,
+                                 size_t ws_bytes, void* stream) {
+  if (S < 1 || S > TC_MAX_B) return DDL_ERR_UNSUPPORTED;
+  if (p0 < 0) return DDL_ERR_POS;
+  int64_t pos[TC_MAX_B];
+  for (int i = 0; i < S; ++i) pos[i] = p0 + i;  // (the last must stay below s_max: checked with the others)
+  return decode(shape, wtype, layers, kv, L, S, 0, resid_in, x_bf16, resid_out, out_bf16, workspace, ws_bytes,
+                stream, pos, true);
 }
 
 extern "C" int ddl_set_launch_mode(int32_t mode) {

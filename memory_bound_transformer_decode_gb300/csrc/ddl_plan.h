@@ -237,6 +237,8 @@ struct Params {
   int32_t ragged;       // sequences at their own positions: posb, rope_b (else every sequence at pos, rope)
   int32_t posb[64];     // position of sequence b (ragged)
   const float* rope_b;  // [B][64][2] cos, sin of posb[b] * base^(-2i/hd) (ragged)
+  int64_t kv_bstride;   // cache rows from sequence b to b + 1: H_kv * s_max, or 0 when the rows share one cache (prefill)
+  int32_t p0;           // prefill: the first prompt position (rows p0 .. are written in this step), else -1
   uint64_t* trace;      // optional: per stage, CTA: start, prologue end, NW warp ends, end, 4 prologue steps (ns)
   LayerDev layers[MAX_LAYERS];
   // 2-D views [B * H_kv * s_max rows][hd] of each layer's K and V caches for

@@ -362,6 +362,7 @@ struct TcEpi {
   uint16_t* out_bf16;
   float rope[64][2];
   const int32_t* posb;       // ragged positions: posb[b] (device copy in the run's parameters) or NULL
+  int64_t kv_bstride;        // cache rows from sequence b to b + 1 (0: the rows share one cache)
   const float* rope_b;       // [B][64][2] with posb
 };
 
@@ -426,7 +427,7 @@ __global__ void __launch_bounds__(256) tc_epi_kernel(const __grid_constant__ TcE
             const bool is_k = head < E.Hq + E.Hkv;
             const int kvh = is_k ? head - E.Hq : head - E.Hq - E.Hkv;
             const int64_t pb = E.posb ? (int64_t)E.posb[b] : E.pos;
-            uint16_t* row = (is_k ? E.kc : E.vc) + (((int64_t)b * E.Hkv + kvh) * E.s_max + pb) * E.hd;
+            uint16_t* row = (is_k ? E.kc : E.vc) + ((int64_t)b * E.kv_bstride + (int64_t)kvh * E.s_max + pb) * E.hd;
             row[ii] = f32_to_bf16_bits(v0);
             row[ii + E.hd / 2] = f32_to_bf16_bits(v1);
           }
@@ -548,6 +549,7 @@ TcEpi epi_base(const TcRun& R) {
   E.ss_K = R.D;
   memcpy(E.rope, R.rope, sizeof E.rope);
   E.posb = R.posb;
+  E.kv_bstride = R.kv_bstride;
   E.rope_b = R.rope_b;
   return E;
 }

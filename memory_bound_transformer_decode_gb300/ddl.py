@@ -25,7 +25,8 @@ EXPORTED = ("ddl_quantize_int4", "ddl_packed_layer_bytes", "ddl_pack_layer", "dd
             "ddl_stack_decode_noalloc", "ddl_set_launch_mode", "ddl_set_wait_limit_ns",
             "ddl_test_hold_barrier", "ddl_set_trace", "ddl_read_device_status", "ddl_status_string",
             "ddl_last_cuda_error", "ddl_embed", "ddl_packed_head_bytes", "ddl_pack_head",
-            "ddl_head_workspace_bytes", "ddl_lm_head", "ddl_stack_decode_ragged")
+            "ddl_head_workspace_bytes", "ddl_lm_head", "ddl_stack_decode_ragged",
+            "ddl_stack_prefill")
 
 
 class DDLError(RuntimeError):
@@ -102,6 +103,8 @@ def load(build_if_missing: bool = False):
                                          vp, vp, vp, vp, vp, sz, vp]
         lib.ddl_stack_decode_ragged.argtypes = [P(Shape), ctypes.c_int, P(LayerW), P(KV), i32, i32, P(i64),
                                                 vp, vp, vp, vp, vp, sz, vp]
+        lib.ddl_stack_prefill.argtypes = [P(Shape), ctypes.c_int, P(LayerW), P(KV), i32, i32, i64, vp, vp, vp, vp,
+                                          vp, sz, vp]
         lib.ddl_stack_decode_noalloc.argtypes = [P(Shape), ctypes.c_int, P(LayerW), P(KV), i32, i32,
                                                  i64, vp, vp, vp, vp, vp]
         lib.ddl_set_launch_mode.argtypes = [i32]
@@ -266,6 +269,21 @@ def ddl_stack_decode_ragged(shape: Shape, wtype: int, layers: list, kvs: list, p
                                      _ptr(workspace), workspace.numel() * workspace.element_size(),
                                      _stream(stream))
     _check("ddl_stack_decode_ragged", st)
+
+
+def ddl_stack_prefill(shape: Shape, wtype: int, layers: list, kvs: list, p0: int, *,
+                      x_bf16: torch.Tensor | None = None, resid_in: torch.Tensor | None = None,
+                      resid_out: torch.Tensor | None = None, out_bf16: torch.Tensor | None = None,
+                      workspace: torch.Tensor, stream=None):
+    """S prompt tokens (rows of x) of one sequence at positions p0 .. p0 + S - 1;
+    kvs: that sequence's (K, V) caches [1, H_kv, s_max, hd]."""
+    lib = load()
+    S = (x_bf16 if x_bf16 is not None else resid_in).shape[0]
+    lw, kv = _layers_and_kv(layers, kvs)
+    st = lib.ddl_stack_prefill(ctypes.byref(shape), wtype, lw, kv, len(layers), S, int(p0), _ptr(resid_in),
+                               _ptr(x_bf16), _ptr(resid_out), _ptr(out_bf16), _ptr(workspace),
+                               workspace.numel() * workspace.element_size(), _stream(stream))
+    _check("ddl_stack_prefill", st)
 
 
 def ddl_stack_decode_noalloc(shape: Shape, wtype: int, layers: list, kvs: list, pos: int, *,

@@ -391,3 +391,27 @@ def layer_decode_ragged(shape, layer: dict, kc, vc, pos, x, stages: bool = False
     if not stages:
         return z
     return z, {k: np.concatenate([s[k] for s in sts]) for k in sts[0]}
+
+
+def layer_prefill(shape, layer: dict, kc, vc, p0: int, x, stages: bool = False):
+    """S prompt tokens of one sequence through one layer (the primer's §1.2
+    prefill, its K/V kept in the cache): row i is the token at position
+    p0 + i and sees the history and the rows before it.  Causality makes it
+    the plain decode step row after row on the one cache: row i appends slot
+    p0 + i before row i + 1 attends.
+
+    kc, vc: uint16 [1, H_kv, s_max, hd], slots p0 .. p0 + S - 1 written in
+    place.  x: fp64 [S, D].  Returns z [S, D] (and the rows' stages)."""
+    x = np.atleast_2d(np.asarray(x, np.float64))
+    zs, sts = [], []
+    for i in range(x.shape[0]):
+        r = layer_decode(shape, layer, kc, vc, int(p0) + i, x[i:i + 1], stages=stages)
+        if stages:
+            zs.append(r[0])
+            sts.append(r[1])
+        else:
+            zs.append(r)
+    z = np.concatenate(zs)
+    if not stages:
+        return z
+    return z, {k: np.concatenate([s[k] for s in sts]) for k in sts[0]}

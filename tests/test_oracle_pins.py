@@ -522,3 +522,65 @@ def test_ragged_sequences_are_independent_and_ignore_slots_past_their_position()
     z2 = oracle.layer_decode_ragged(cfg, lw, kc.copy(), vc.copy(), [0, 30, 40], x)
     np.testing.assert_array_equal(z[[0, 2]], z2[[0, 2]])
     assert not np.array_equal(z[1], z2[1])
+
+
+# ------------------------------------------------------------------ prefill
+
+
+def _torch_prefill(cfg, w, kc_bits, vc_bits, p0, x):
+    """A prefill layer from PyTorch routines in fp64: all rows at once, RoPE at
+    positions p0 + i, the new K/V rows rounded to bf16, one attention call
+    with a causal mask over the history and the prompt."""
+    def dq(m):
+        codes = torch.from_numpy(_numpy_codes(m.q).astype(np.float64))
+        sc = torch.from_numpy(np.repeat(oracle.bf16_to_f64(m.s), 64, axis=1))
+        return codes * sc
+
+    S, hd = x.shape[0], cfg.head_dim
+    posn = torch.arange(p0, p0 + S, dtype=torch.float64)
+
+    def rope(t):  # t [S, H, hd]
+        theta = torch.pow(torch.tensor(cfg.rope_base, dtype=torch.float64),
+                          -torch.arange(0, hd, 2, dtype=torch.float64) / hd)
+        ang = posn[:, None, None] * theta[None, None, :]
+        z = torch.complex(t[..., : hd // 2], t[..., hd // 2:]) * torch.polar(torch.ones_like(ang), ang)
+        return torch.cat([z.real, z.imag], dim=-1)
+
+    xt = torch.from_numpy(x)
+    h = F.rms_norm(xt, (cfg.D,), weight=torch.from_numpy(oracle.bf16_to_f64(w["norm1"])), eps=cfg.eps)
+    q = rope((h @ dq(w["wq"]).T).view(S, cfg.H_q, hd))
+    k = rope((h @ dq(w["wk"]).T).view(S, cfg.H_kv, hd))
+    v = (h @ dq(w["wv"]).T).view(S, cfg.H_kv, hd)
+    kb = torch.from_numpy(oracle.bf16_to_f64(kc_bits))[0, :, :p0].clone()  # [H_kv, p0, hd]
+    vb = torch.from_numpy(oracle.bf16_to_f64(vc_bits))[0, :, :p0].clone()
+    kk = torch.cat([kb, k.to(torch.bfloat16).to(torch.float64).transpose(0, 1)], dim=1)
+    vv = torch.cat([vb, v.to(torch.bfloat16).to(torch.float64).transpose(0, 1)], dim=1)
+    mask = torch.arange(p0 + S)[None, :] <= (p0 + torch.arange(S))[:, None]  # row i sees keys <= p0 + i
+    att = F.scaled_dot_product_attention(q.transpose(0, 1)[None], kk[None], vv[None], attn_mask=mask,
+                                         enable_gqa=True)
+    att = att[0].transpose(0, 1).reshape(S, -1)
+    y = xt + att @ dq(w["wo"]).T
+    h2 = F.rms_norm(y, (cfg.D,), weight=torch.from_numpy(oracle.bf16_to_f64(w["norm2"])), eps=cfg.eps)
+    a = F.silu(h2 @ dq(w["wg"]).T) * (h2 @ dq(w["wu"]).T)
+    return (y + a @ dq(w["wd"]).T).numpy()
+
+
+@pytest.mark.parametrize("p0,S", [(0, 5), (37, 9)])
+def test_prefill_vs_causal_torch_composition(p0, S):
+    cfg = configs.SMALL_LAYER.with_(kv_len=p0)
+    wb = {k: synth.bits(v) for k, v in synth.layer_weights(cfg, 0).items()}
+    lw = oracle.quantized_layer(wb)
+    kc, vc = (synth.bits(t).copy() for t in synth.kv_cache(cfg, 0, p0 + S + 3, batch=1))
+    x = oracle.bf16_to_f64(synth.bits(synth.normal_bf16((S, cfg.D), seed=99)))
+    want = _torch_prefill(cfg, lw, kc, vc, p0, x)
+    k2, v2 = kc.copy(), vc.copy()
+    z = oracle.layer_prefill(cfg, lw, k2, v2, p0, x)
+    np.testing.assert_allclose(z, want, rtol=1e-10, atol=1e-10)
+    # slots p0 .. p0 + S - 1 written, nothing else
+    changed = set(np.argwhere(k2 != kc)[:, 2]) | set(np.argwhere(v2 != vc)[:, 2])
+    assert changed <= set(range(p0, p0 + S))
+    # causal: a later row's input changes nothing before it
+    x2 = x.copy()
+    x2[-1] += 1.0
+    z2 = oracle.layer_prefill(cfg, lw, kc.copy(), vc.copy(), p0, x2)
+    np.testing.assert_array_equal(z2[:-1], z[:-1])
