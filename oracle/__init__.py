@@ -393,6 +393,50 @@ def layer_decode_ragged(shape, layer: dict, kc, vc, pos, x, stages: bool = False
     return z, {k: np.concatenate([s[k] for s in sts]) for k in sts[0]}
 
 
+def paged_gather(pool, table, page_size: int, b: int, n: int):
+    """The first n logical slots of sequence b from a paged cache: slot t sits
+    in physical page table[b][t // page_size] at row t % page_size.
+    pool: [pages, H_kv, page_size, hd]; returns [1, H_kv, n, hd] (a copy)."""
+    H, hd = pool.shape[1], pool.shape[3]
+    out = np.empty((1, H, n, hd), pool.dtype)
+    for t in range(n):
+        out[0, :, t] = pool[int(table[b][t // page_size]), :, t % page_size]
+    return out
+
+
+def layer_decode_paged(shape, layer: dict, kpool, vpool, table, page_size: int, pos, x, stages: bool = False):
+    """One decode step of one layer for B sequences at their own positions
+    whose caches are paged (the primer's §1.3 continuous batching with the
+    cache kept in fixed-size pages): sequence b's logical slots 0 .. pos[b]
+    are gathered through its page-table row, the plain step runs on them,
+    and its new K/V row goes back to logical slot pos[b], i.e. physical page
+    table[b][pos[b] // page_size], row pos[b] % page_size.
+
+    kpool, vpool: uint16 [pages, H_kv, page_size, hd], written in place at
+    the new slots only.  table: [B][>= pos[b] // page_size + 1] page ids.
+    x: fp64 [B, D].  Returns z [B, D] (and the stacked stages)."""
+    x = np.atleast_2d(np.asarray(x, np.float64))
+    pos = [int(p) for p in pos]
+    zs, sts = [], []
+    for b in range(x.shape[0]):
+        n = pos[b] + 1
+        kb = paged_gather(kpool, table, page_size, b, n)
+        vb = paged_gather(vpool, table, page_size, b, n)
+        r = layer_decode(shape, layer, kb, vb, pos[b], x[b:b + 1], stages=stages)
+        pg, row = int(table[b][pos[b] // page_size]), pos[b] % page_size
+        kpool[pg, :, row] = kb[0, :, pos[b]]
+        vpool[pg, :, row] = vb[0, :, pos[b]]
+        if stages:
+            zs.append(r[0])
+            sts.append(r[1])
+        else:
+            zs.append(r)
+    z = np.concatenate(zs)
+    if not stages:
+        return z
+    return z, {k: np.concatenate([s[k] for s in sts]) for k in sts[0]}
+
+
 def layer_prefill(shape, layer: dict, kc, vc, p0: int, x, stages: bool = False):
     """S prompt tokens of one sequence through one layer (the primer's §1.2
     prefill, its K/V kept in the cache): row i is the token at position

@@ -524,6 +524,85 @@ def test_ragged_sequences_are_independent_and_ignore_slots_past_their_position()
     assert not np.array_equal(z[1], z2[1])
 
 
+# ------------------------------------------------------------------ paged KV cache
+
+
+def _pages_of(cache, ps):
+    """A contiguous cache [B, H, s_max, hd] as pages [B * s_max / ps, H, ps, hd],
+    sequence b's logical page j at physical page b * (s_max / ps) + j (a
+    reshape and a transpose, no loop)."""
+    B, H, S, hd = cache.shape
+    return np.ascontiguousarray(cache.reshape(B, H, S // ps, ps, hd).transpose(0, 2, 1, 3, 4)).reshape(-1, H, ps, hd)
+
+
+def _paged_case(B=3, s_max=64):
+    cfg = configs.SMALL_LAYER.with_(kv_len=s_max - 1)
+    w = {k: synth.bits(v) for k, v in synth.layer_weights(cfg, 0).items()}
+    lw = oracle.quantized_layer(w)
+    kc, vc = (synth.bits(t).copy() for t in synth.kv_cache(cfg, 0, s_max, batch=B))
+    x = oracle.bf16_to_f64(synth.bits(synth.input_x(cfg, batch=B)))
+    return cfg, lw, kc, vc, x
+
+
+@pytest.mark.parametrize("ps", [16, 32])
+def test_paged_identity_layout_is_the_ragged_step(ps):
+    cfg, lw, kc, vc, x = _paged_case()
+    pos = [0, 33, 63]
+    npg = kc.shape[2] // ps
+    table = np.arange(3 * npg).reshape(3, npg)
+    kp, vp = _pages_of(kc, ps), _pages_of(vc, ps)
+    z, st = oracle.layer_decode_paged(cfg, lw, kp, vp, table, ps, pos, x, stages=True)
+    z2, st2 = oracle.layer_decode_ragged(cfg, lw, kc, vc, pos, x, stages=True)
+    np.testing.assert_array_equal(z, z2)
+    for k in st:
+        np.testing.assert_array_equal(st[k], st2[k])
+    # the new rows landed where the contiguous step put them, nothing else moved
+    np.testing.assert_array_equal(kp, _pages_of(kc, ps))
+    np.testing.assert_array_equal(vp, _pages_of(vc, ps))
+
+
+def test_paged_permuted_pages_with_junk_pages():
+    cfg, lw, kc, vc, x = _paged_case()
+    ps, pos = 16, [5, 47, 16]
+    npg = kc.shape[2] // ps
+    kp0, vp0 = _pages_of(kc, ps), _pages_of(vc, ps)
+    rng = np.random.default_rng(5)
+    n_phys = 3 * npg + 7  # 7 pages nobody owns, full of junk
+    perm = rng.permutation(n_phys)[: 3 * npg]  # logical page (b, j) -> physical page
+    kp = np.full((n_phys,) + kp0.shape[1:], 0x7F7F, np.uint16)
+    vp = np.full((n_phys,) + vp0.shape[1:], 0xFF7F, np.uint16)
+    kp[perm], vp[perm] = kp0, vp0
+    table = perm.reshape(3, npg)
+    kpb, vpb = kp.copy(), vp.copy()
+    z = oracle.layer_decode_paged(cfg, lw, kp, vp, table, ps, pos, x)
+    z2 = oracle.layer_decode_ragged(cfg, lw, kc, vc, pos, x)
+    np.testing.assert_array_equal(z, z2)
+    np.testing.assert_array_equal(kp[perm], _pages_of(kc, ps))
+    np.testing.assert_array_equal(vp[perm], _pages_of(vc, ps))
+    junk = np.setdiff1d(np.arange(n_phys), perm)
+    np.testing.assert_array_equal(kp[junk], kpb[junk])
+    np.testing.assert_array_equal(vp[junk], vpb[junk])
+    # exactly one row of one page per sequence changed
+    diff = np.argwhere((kp != kpb).any(axis=(1, 3)))
+    assert sorted(map(tuple, diff)) == sorted((int(table[b][p // ps]), p % ps) for b, p in enumerate(pos))
+
+
+def test_paged_shared_prefix_pages():
+    """Two sequences whose first two pages are one physical copy read the same
+    history as two sequences holding it twice."""
+    cfg, lw, kc, vc, x = _paged_case(B=2)
+    ps, pos = 16, [40, 50]
+    kc[1, :, : 2 * ps] = kc[0, :, : 2 * ps]  # the contiguous reference: prefix duplicated
+    vc[1, :, : 2 * ps] = vc[0, :, : 2 * ps]
+    kp0, vp0 = _pages_of(kc, ps), _pages_of(vc, ps)  # 4 pages per sequence
+    keep = [0, 1, 2, 3, 6, 7]  # sequence 1's first two pages dropped: it reads sequence 0's
+    kp, vp = kp0[keep].copy(), vp0[keep].copy()
+    table = np.array([[0, 1, 2, 3], [0, 1, 4, 5]])
+    z = oracle.layer_decode_paged(cfg, lw, kp, vp, table, ps, pos, x)
+    z2 = oracle.layer_decode_ragged(cfg, lw, kc, vc, pos, x)
+    np.testing.assert_array_equal(z, z2)
+
+
 # ------------------------------------------------------------------ prefill
 
 
