@@ -102,6 +102,15 @@ typedef struct {
     int64_t s_max;
 } ddl_kv;
 
+/* One layer's paged KV cache: k and v each [pages][H_kv][page_size][head_dim]
+ * bf16, device.  A sequence's slots live in pages named by its row of a page
+ * table (ddl_stack_decode_paged); every layer uses the same page table. */
+typedef struct {
+    uint16_t* k;
+    uint16_t* v;
+    int64_t pages;
+} ddl_kv_pages;
+
 /* ------------------------------------------------------------ weights */
 
 /* Symmetric INT4 quantization with group 64 along K and a bf16 scale per
@@ -204,6 +213,43 @@ int ddl_stack_prefill(const ddl_shape* shape, ddl_wtype wtype, const ddl_layer_w
                       const ddl_kv* kv, int32_t L, int32_t S, int64_t p0, const float* resid_in,
                       const uint16_t* x_bf16, float* resid_out, uint16_t* out_bf16, void* workspace,
                       size_t ws_bytes, void* stream);
+
+/* ddl_stack_decode_ragged on a paged KV cache (continuous batching, the
+ * primer's §1.3, with each sequence's history in fixed-size pages, so that
+ * sequences of any length share one pool without a contiguous region each):
+ * slot t of sequence b lives in page page_table[b * pages_per_seq +
+ * t / page_size] of every layer's pool, at row t % page_size.
+ *  - kv: L pools, each [pages][H_kv][page_size][head_dim] bf16 (device), all
+ *    with the same page count.
+ *  - page_table: host int32 [B][pages_per_seq], copied to the workspace
+ *    during the call (the caller may reuse it once the call returns).  Only
+ *    the live entries (pages of slots 0..pos[b]) are read; each must lie in
+ *    [0, pages), and the page that receives sequence b's new row must occur
+ *    once among all live entries of the batch (no sequence reads a page
+ *    being written, as with shared prefix pages) -- DDL_ERR_ARG otherwise.
+ *  - page_size: a power of two in [16, 2^20] (DDL_ERR_ARG); pos[b] <
+ *    pages_per_seq * page_size (DDL_ERR_POS); pages * H_kv * page_size <
+ *    2^31 (DDL_ERR_UNSUPPORTED).
+ *  - The workspace is sized by ddl_workspace_bytes(shape, B,
+ *    pages_per_seq * page_size).  Other arguments as ddl_stack_decode_ragged. */
+int ddl_stack_decode_paged(const ddl_shape* shape, ddl_wtype wtype, const ddl_layer_w* layers,
+                           const ddl_kv_pages* kv, int32_t L, int32_t B, const int64_t* pos,
+                           const int32_t* page_table, int32_t pages_per_seq, int32_t page_size,
+                           const float* resid_in, const uint16_t* x_bf16, float* resid_out,
+                           uint16_t* out_bf16, void* workspace, size_t ws_bytes, void* stream);
+
+/* ddl_stack_prefill into a paged KV cache: the S prompt rows of one sequence
+ * at positions p0..p0 + S - 1 write their K/V through the one page-table row
+ * page_table[0 .. pages_per_seq) and attend causally over the slots before
+ * them.  The pages receiving rows must each occur once among the live
+ * entries (pages of slots 0..p0 + S - 1).  Other rules as
+ * ddl_stack_decode_paged with B = 1; the workspace is sized by
+ * ddl_workspace_bytes(shape, S, pages_per_seq * page_size). */
+int ddl_stack_prefill_paged(const ddl_shape* shape, ddl_wtype wtype, const ddl_layer_w* layers,
+                            const ddl_kv_pages* kv, int32_t L, int32_t S, int64_t p0,
+                            const int32_t* page_table, int32_t pages_per_seq, int32_t page_size,
+                            const float* resid_in, const uint16_t* x_bf16, float* resid_out,
+                            uint16_t* out_bf16, void* workspace, size_t ws_bytes, void* stream);
 
 /* Size of the library's own static scratch array (32 MiB), used only by
  * ddl_stack_decode_noalloc. */

@@ -31,6 +31,9 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <unordered_map>
+#include <vector>
+
 #include <cudaTypedefs.h>
 
 #include "ddl_device.cuh"
@@ -89,6 +92,17 @@ __device__ __forceinline__ int att_tiles(const Params& P, int64_t seq) {
 // positions and prefill, whose rows may share one cache).
 __device__ __forceinline__ int64_t att_row0(const Params& P, int64_t seq) {
   return (seq / P.Hkv) * P.kv_bstride + (seq % P.Hkv) * P.s_max;
+}
+// Cache-view row of slot t of attention sequence seq = (b, kv head): in a
+// paged cache the row inside the page that holds slot t (the page table is
+// read-only for the whole call).
+__device__ __forceinline__ int64_t att_row(const Params& P, int64_t seq, int64_t t) {
+  if (P.pshift) {
+    const int64_t b = seq / P.Hkv, kvh = seq % P.Hkv;
+    const int64_t pg = __ldg(P.ptab + b * P.pstride + (t >> P.pshift));
+    return ((pg * P.Hkv + kvh) << P.pshift) + (t & ((1ll << P.pshift) - 1));
+  }
+  return att_row0(P, seq) + t;
 }
 __device__ __forceinline__ float2 rope_cs(const Params& P, int b, int i) {
   if (P.ragged) return *reinterpret_cast<const float2*>(P.rope_b + ((int64_t)b * 64 + i) * 2);
@@ -308,15 +322,17 @@ __device__ __forceinline__ void cursor_enter(const Params& P, Cursor& c, int w) 
   if (st == ST_ATT) {
     c.aseq = (int)(e.lo / (uint32_t)P.nt_att);
     c.ai = (int)(e.lo - (uint32_t)c.aseq * (uint32_t)P.nt_att);
-    c.a = (uint32_t)((RAG ? att_row0(P, c.aseq) : (int64_t)c.aseq * P.s_max) + 16 * c.ai);
     c.pos *= 2;
     c.end *= 2;
     if (RAG && c.ai >= att_tiles(P, c.aseq)) {  // the range starts past a sequence's new token
       c.pos += 2u * (uint32_t)(P.nt_att - c.ai);
       c.ai = 0;
       ++c.aseq;
-      c.a = (uint32_t)att_row0(P, c.aseq);
     }
+    // (a range that ends with the sequence it skipped to holds no tile of it:
+    // its row is never used, and the page table is not read for it)
+    c.a = RAG ? (c.pos < c.end ? (uint32_t)att_row(P, c.aseq, 16 * (int64_t)c.ai) : 0u)
+              : (uint32_t)((int64_t)c.aseq * P.s_max + 16 * c.ai);
     c.kmap = &P.kmap[c.s / NSTAGE];
     c.vmap = &P.vmap[c.s / NSTAGE];
   } else {
@@ -352,7 +368,9 @@ __device__ __forceinline__ bool cursor_next(const Params& P, Cursor& c, int w, S
         c.pos += 2u * (uint32_t)(P.nt_att - c.ai);
         c.ai = 0;
         ++c.aseq;
-        c.a = (uint32_t)(RAG ? att_row0(P, c.aseq) : (int64_t)c.aseq * P.s_max);
+        c.a = RAG ? (c.pos + 1 < c.end ? (uint32_t)att_row(P, c.aseq, 0) : 0u) : (uint32_t)((int64_t)c.aseq * P.s_max);
+      } else if (RAG && P.pshift && ((16 * c.ai) & ((1 << P.pshift) - 1)) == 0) {
+        c.a = (uint32_t)att_row(P, c.aseq, 16 * (int64_t)c.ai);  // the next page
       } else {
         c.a += 16;
       }
@@ -796,7 +814,7 @@ __device__ __noinline__ void gemv_epilogue(const Params& P, const GemvCtx& E, in
     } else {
       const bool is_k = head < P.Hq + P.Hkv;
       const int kvh = is_k ? head - P.Hq : head - P.Hq - P.Hkv;
-      uint16_t* row = (is_k ? E.kc : E.vc) + ((int64_t)t * P.kv_bstride + (int64_t)kvh * P.s_max + seq_pos(P, t)) * HD;
+      uint16_t* row = (is_k ? E.kc : E.vc) + att_row(P, (int64_t)t * P.Hkv + kvh, seq_pos(P, t)) * HD;
       row[i] = f32_to_bf16_bits(v0);
       row[i + HD / 2] = f32_to_bf16_bits(v1);
     }
@@ -2058,7 +2076,7 @@ __device__ __forceinline__ bool stage_att_body(const Params& P, int layer, Ring&
     int64_t ro = ((seq * P.s_max) + pq) * HD;  // the new token's row in the cache ([seq][s_max][hd])
     bool fix = newtok;
     if constexpr (RAG) {
-      ro = (att_row0(P, seq) + 16 * (int64_t)i) * HD;  // the tile's first row
+      ro = att_row(P, seq, 16 * (int64_t)i) * HD;  // the tile's first row
       r_hi = newtok ? rnew : 15;
       if (P.p0 >= 0) {
         const int64_t lo = P.p0 - 16 * (int64_t)i;
@@ -2458,7 +2476,7 @@ static int device_info(DevInfo& out) {
 }
 
 struct WsLayout {
-  int64_t ctrl, cnt, seqcnt, xmax, gpart, apart, Z, q, attn, y, a, rope, ximg, ximg_bytes, tc, total;
+  int64_t ctrl, cnt, seqcnt, xmax, gpart, apart, Z, q, attn, y, a, rope, ptab, ximg, ximg_bytes, tc, total;
 };
 
 static int64_t att_J(int64_t seqs, int64_t nt, int64_t C) {
@@ -2497,6 +2515,7 @@ static void ws_layout(const ddl_shape& s, int B, int64_t s_max, int C, const Mat
   w.y = off;     off = align256(off + (int64_t)B * s.D * 4);
   w.a = off;     off = align256(off + (int64_t)B * s.d_ff * 4);
   w.rope = off;  off = align256(off + (int64_t)B * (64 * 2 * 4 + 4));  // ragged positions: RoPE table, positions
+  w.ptab = off;  off = align256(off + (int64_t)B * ((s_max + 15) / 16) * 4);  // page table (pages >= 16 slots)
   // fragment images of a weight stage's input (fp16 high part and remainder
   // per element), two by stage parity; batches up to NARROW_B
   int64_t kmax = s.D > s.d_ff ? s.D : s.d_ff;
@@ -2570,11 +2589,44 @@ __global__ void rope_fill_kernel(const __grid_constant__ RopeFill R) {
   if (i == 0) R.pos[b] = R.posb[b];
 }
 
+// A paged cache: host page table [rows][per_seq], the page size (a power of
+// two >= 16) and the pool's page count.
+struct Paged {
+  const int32_t* table;
+  int32_t per_seq, page_size;
+  int64_t pages;
+};
+
+// Page-table checks: every live entry (the pages of slots 0 .. pos of each
+// table row in use) names a page of the pool, and every page that receives a
+// new row occurs once among them: no other sequence reads it and its own
+// sequence does not map it twice.  Prefill (shared) uses row 0 for all rows.
+static int check_pages(const Paged& pg, int32_t B, const int64_t* posv, bool shared) {
+  const int rows = shared ? 1 : B;
+  std::unordered_map<int32_t, int> seen;
+  for (int r = 0; r < rows; ++r) {
+    const int64_t last = shared ? posv[B - 1] : posv[r];
+    for (int64_t j = 0; j <= last / pg.page_size; ++j) {
+      const int32_t id = pg.table[(int64_t)r * pg.per_seq + j];
+      if (id < 0 || id >= pg.pages) return DDL_ERR_ARG;
+      ++seen[id];
+    }
+  }
+  for (int r = 0; r < rows; ++r) {
+    const int64_t first = shared ? posv[0] : posv[r], last = shared ? posv[B - 1] : posv[r];
+    for (int64_t j = first / pg.page_size; j <= last / pg.page_size; ++j)
+      if (seen[pg.table[(int64_t)r * pg.per_seq + j]] != 1) return DDL_ERR_ARG;
+  }
+  return DDL_OK;
+}
+
 // posv: NULL (every sequence at pos) or a host array of B positions (pos unused).
+// shared: the B rows are one sequence's consecutive tokens on one cache (prefill).
+// pg: paged caches (with posv), else NULL.
 static int decode(const ddl_shape* s, ddl_wtype wtype, const ddl_layer_w* layers, const ddl_kv* kv,
                   int32_t L, int32_t B, int64_t pos, const float* resid_in, const uint16_t* x_bf16,
                   float* resid_out, uint16_t* out_bf16, void* workspace, size_t ws_bytes,
-                  void* stream, const int64_t* posv = nullptr, bool shared = false) {
+                  void* stream, const int64_t* posv = nullptr, bool shared = false, const Paged* pg = nullptr) {
   int st = check_shape(s);
   if (st) return st;
   if (!layers || !kv || L <= 0 || !workspace) return !workspace ? DDL_ERR_WORKSPACE : DDL_ERR_ARG;
@@ -2586,8 +2638,9 @@ static int decode(const ddl_shape* s, ddl_wtype wtype, const ddl_layer_w* layers
   const bool use_tc = (wtype == DDL_W_INT4 && B >= TC_MIN_B) || (wtype == DDL_W_BF16 && B > NARROW_B);
   if (!resid_in && !x_bf16) return DDL_ERR_ARG;
   const int64_t s_max = kv[0].s_max;
-  if ((int64_t)B * s->H_kv * s_max >= (1ll << 31)) return DDL_ERR_UNSUPPORTED;  // K/V tensor-map rows
-  const int64_t kv_rows = (shared ? 1 : (int64_t)B) * s->H_kv * s_max;  // rows of a layer's cache view
+  // rows of a layer's cache view (the TMA tensor map's outer dimension, 32-bit in the kernel)
+  const int64_t kv_rows = pg ? pg->pages * s->H_kv * pg->page_size : (shared ? 1 : (int64_t)B) * s->H_kv * s_max;
+  if (kv_rows >= (1ll << 31) || (int64_t)B * s->H_kv * s_max >= (1ll << 31)) return DDL_ERR_UNSUPPORTED;
   if (posv) {  // the largest position sets the attention's tile count
     pos = 0;
     for (int b = 0; b < B; ++b) {
@@ -2596,6 +2649,7 @@ static int decode(const ddl_shape* s, ddl_wtype wtype, const ddl_layer_w* layers
     }
   }
   if (pos < 0 || pos >= s_max) return DDL_ERR_POS;
+  if (pg && (!posv || (st = check_pages(*pg, B, posv, shared)))) return posv ? st : DDL_ERR_ARG;
   for (int l = 0; l < L; ++l) {
     if (!layers[l].packed || !layers[l].norm1 || !layers[l].norm2 || !kv[l].k || !kv[l].v)
       return DDL_ERR_ARG;
@@ -2673,6 +2727,15 @@ static int decode(const ddl_shape* s, ddl_wtype wtype, const ddl_layer_w* layers
     P.p0 = shared ? (int32_t)posv[0] : -1;
     P.rope_b = rf.table;
   }
+  if (pg) {  // the page table rows in use, to the workspace (the host copy may go once this returns)
+    const size_t n = (size_t)(shared ? 1 : B) * pg->per_seq * 4;
+    if ((e = cudaMemcpyAsync(ws + w.ptab, pg->table, n, cudaMemcpyHostToDevice, cs)) != cudaSuccess)
+      return cuda_status(e);
+    P.ptab = (const int32_t*)(ws + w.ptab);
+    P.pshift = 0;
+    while ((1 << P.pshift) < pg->page_size) ++P.pshift;
+    P.pstride = shared ? 0 : pg->per_seq;
+  }
   // empty partial slots (each reader empties the slots it consumed, so they
   // stay empty from stage to stage within a launch)
   if ((e = cudaMemsetAsync(ws + w.gpart, 0xFF, (size_t)(w.apart - w.gpart), cs)) != cudaSuccess)
@@ -2727,6 +2790,9 @@ static int decode(const ddl_shape* s, ddl_wtype wtype, const ddl_layer_w* layers
       R.posb = posv ? (const int32_t*)(ws + w.rope + (int64_t)B * 64 * 2 * 4) : nullptr;
       R.kv_bstride = P.kv_bstride;
       R.rope_b = posv ? (const float*)(ws + w.rope) : nullptr;
+      R.ptab = P.ptab;
+      R.pshift = P.pshift;
+      R.pstride = P.pstride;
       make_geoms(*s, wtype, R.mg);
       R.layers = tl; R.L = nL; R.l0 = l0; R.final_last = P.final_last;
       R.resid_in = resid_in; R.x_bf16 = x_bf16; R.resid_out = resid_out; R.out_bf16 = out_bf16;
@@ -2840,6 +2906,56 @@ extern "C" int ddl_stack_prefill(const ddl_shape* shape, ddl_wtype wtype, const 
   for (int i = 0; i < S; ++i) pos[i] = p0 + i;  // (the last must stay below s_max: checked with the others)
   return decode(shape, wtype, layers, kv, L, S, 0, resid_in, x_bf16, resid_out, out_bf16, workspace, ws_bytes,
                 stream, pos, true);
+}
+
+// The paged pools as the contiguous-cache descriptors decode() checks (the
+// pointers and one logical s_max = pages_per_seq * page_size), and the page
+// table's description; DDL_ERR_ARG when an argument is out of range.
+static int paged_views(const ddl_kv_pages* kv, int32_t L, int32_t per_seq, int32_t page_size,
+                       std::vector<ddl_kv>& out, Paged& pg, const int32_t* table) {
+  if (!kv || !table || L <= 0 || per_seq < 1) return DDL_ERR_ARG;
+  if (page_size < 16 || page_size > (1 << 20) || (page_size & (page_size - 1))) return DDL_ERR_ARG;
+  const int64_t pages = kv[0].pages;
+  if (pages < 1) return DDL_ERR_ARG;
+  out.resize(L);
+  for (int l = 0; l < L; ++l) {
+    if (kv[l].pages != pages) return DDL_ERR_ARG;
+    out[l] = ddl_kv{kv[l].k, kv[l].v, (int64_t)per_seq * page_size};
+  }
+  pg = Paged{table, per_seq, page_size, pages};
+  return DDL_OK;
+}
+
+extern "C" int ddl_stack_decode_paged(const ddl_shape* shape, ddl_wtype wtype, const ddl_layer_w* layers,
+                                      const ddl_kv_pages* kv, int32_t L, int32_t B, const int64_t* pos,
+                                      const int32_t* page_table, int32_t pages_per_seq, int32_t page_size,
+                                      const float* resid_in, const uint16_t* x_bf16, float* resid_out,
+                                      uint16_t* out_bf16, void* workspace, size_t ws_bytes, void* stream) {
+  if (!pos) return DDL_ERR_ARG;
+  if (B < 1 || B > TC_MAX_B) return DDL_ERR_UNSUPPORTED;
+  std::vector<ddl_kv> views;
+  Paged pg;
+  int st = paged_views(kv, L, pages_per_seq, page_size, views, pg, page_table);
+  if (st) return st;
+  return decode(shape, wtype, layers, views.data(), L, B, 0, resid_in, x_bf16, resid_out, out_bf16, workspace,
+                ws_bytes, stream, pos, false, &pg);
+}
+
+extern "C" int ddl_stack_prefill_paged(const ddl_shape* shape, ddl_wtype wtype, const ddl_layer_w* layers,
+                                       const ddl_kv_pages* kv, int32_t L, int32_t S, int64_t p0,
+                                       const int32_t* page_table, int32_t pages_per_seq, int32_t page_size,
+                                       const float* resid_in, const uint16_t* x_bf16, float* resid_out,
+                                       uint16_t* out_bf16, void* workspace, size_t ws_bytes, void* stream) {
+  if (S < 1 || S > TC_MAX_B) return DDL_ERR_UNSUPPORTED;
+  if (p0 < 0) return DDL_ERR_POS;
+  std::vector<ddl_kv> views;
+  Paged pg;
+  int st = paged_views(kv, L, pages_per_seq, page_size, views, pg, page_table);
+  if (st) return st;
+  int64_t pos[TC_MAX_B];
+  for (int i = 0; i < S; ++i) pos[i] = p0 + i;
+  return decode(shape, wtype, layers, views.data(), L, S, 0, resid_in, x_bf16, resid_out, out_bf16, workspace,
+                ws_bytes, stream, pos, true, &pg);
 }
 
 extern "C" int ddl_set_launch_mode(int32_t mode) {

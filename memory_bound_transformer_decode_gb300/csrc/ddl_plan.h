@@ -239,6 +239,11 @@ struct Params {
   const float* rope_b;  // [B][64][2] cos, sin of posb[b] * base^(-2i/hd) (ragged)
   int64_t kv_bstride;   // cache rows from sequence b to b + 1: H_kv * s_max, or 0 when the rows share one cache (prefill)
   int32_t p0;           // prefill: the first prompt position (rows p0 .. are written in this step), else -1
+  // paged caches (pshift > 0): slot t of sequence b sits in page ptab[b * pstride + (t >> pshift)],
+  // row t & (2^pshift - 1); the K/V views are then [pages * H_kv * 2^pshift rows][hd]
+  const int32_t* ptab;  // device copy of the page table (workspace)
+  int32_t pshift;       // log2 of the page size (0: contiguous caches)
+  int32_t pstride;      // page-table entries per sequence (0: every row reads row 0, prefill)
   uint64_t* trace;      // optional: per stage, CTA: start, prologue end, NW warp ends, end, 4 prologue steps (ns)
   LayerDev layers[MAX_LAYERS];
   // 2-D views [B * H_kv * s_max rows][hd] of each layer's K and V caches for

@@ -364,6 +364,8 @@ struct TcEpi {
   const int32_t* posb;       // ragged positions: posb[b] (device copy in the run's parameters) or NULL
   int64_t kv_bstride;        // cache rows from sequence b to b + 1 (0: the rows share one cache)
   const float* rope_b;       // [B][64][2] with posb
+  const int32_t* ptab;       // paged caches: slot t of sequence b in page ptab[b * pstride + (t >> pshift)]
+  int32_t pshift, pstride;
 };
 
 // Position of element k, limb column c of a group's B-operand image.  Inside
@@ -427,7 +429,12 @@ __global__ void __launch_bounds__(256) tc_epi_kernel(const __grid_constant__ TcE
             const bool is_k = head < E.Hq + E.Hkv;
             const int kvh = is_k ? head - E.Hq : head - E.Hq - E.Hkv;
             const int64_t pb = E.posb ? (int64_t)E.posb[b] : E.pos;
-            uint16_t* row = (is_k ? E.kc : E.vc) + ((int64_t)b * E.kv_bstride + (int64_t)kvh * E.s_max + pb) * E.hd;
+            int64_t r = (int64_t)b * E.kv_bstride + (int64_t)kvh * E.s_max + pb;
+            if (E.pshift) {  // the row inside the page that holds slot pb
+              const int64_t pg = E.ptab[(int64_t)b * E.pstride + (pb >> E.pshift)];
+              r = ((pg * E.Hkv + kvh) << E.pshift) + (pb & ((1ll << E.pshift) - 1));
+            }
+            uint16_t* row = (is_k ? E.kc : E.vc) + r * E.hd;
             row[ii] = f32_to_bf16_bits(v0);
             row[ii + E.hd / 2] = f32_to_bf16_bits(v1);
           }
@@ -551,6 +558,9 @@ TcEpi epi_base(const TcRun& R) {
   E.posb = R.posb;
   E.kv_bstride = R.kv_bstride;
   E.rope_b = R.rope_b;
+  E.ptab = R.ptab;
+  E.pshift = R.pshift;
+  E.pstride = R.pstride;
   return E;
 }
 

@@ -51,6 +51,8 @@ struct TcRun {
   const int32_t* posb;           // ragged positions (device, [B]) or NULL: every sequence at pos
   const float* rope_b;           // [B][64][2] RoPE table of posb (device)
   int64_t kv_bstride;            // cache rows from sequence b to b + 1 (0: one shared cache)
+  const int32_t* ptab;           // paged caches: page table (device), else NULL
+  int32_t pshift, pstride;       // log2 page size, page-table entries per sequence (0: row 0 for all)
   MatGeom mg[4];                 // stream geometry (offsets into a packed layer)
   const TcLayer* layers;         // host array of this launch's layers
   int32_t L;                     // layers of this launch

@@ -12,6 +12,7 @@ import ctypes
 import os
 import threading
 
+import numpy as np
 import torch
 
 from . import build as _build
@@ -26,7 +27,7 @@ EXPORTED = ("ddl_quantize_int4", "ddl_packed_layer_bytes", "ddl_pack_layer", "dd
             "ddl_test_hold_barrier", "ddl_set_trace", "ddl_read_device_status", "ddl_status_string",
             "ddl_last_cuda_error", "ddl_embed", "ddl_packed_head_bytes", "ddl_pack_head",
             "ddl_head_workspace_bytes", "ddl_lm_head", "ddl_stack_decode_ragged",
-            "ddl_stack_prefill")
+            "ddl_stack_prefill", "ddl_stack_decode_paged", "ddl_stack_prefill_paged")
 
 
 class DDLError(RuntimeError):
@@ -60,6 +61,10 @@ class LayerW(ctypes.Structure):
 
 class KV(ctypes.Structure):
     _fields_ = [("k", ctypes.c_void_p), ("v", ctypes.c_void_p), ("s_max", ctypes.c_int64)]
+
+
+class KVPages(ctypes.Structure):
+    _fields_ = [("k", ctypes.c_void_p), ("v", ctypes.c_void_p), ("pages", ctypes.c_int64)]
 
 
 class WsView(ctypes.Structure):
@@ -105,6 +110,10 @@ def load(build_if_missing: bool = False):
                                                 vp, vp, vp, vp, vp, sz, vp]
         lib.ddl_stack_prefill.argtypes = [P(Shape), ctypes.c_int, P(LayerW), P(KV), i32, i32, i64, vp, vp, vp, vp,
                                           vp, sz, vp]
+        lib.ddl_stack_decode_paged.argtypes = [P(Shape), ctypes.c_int, P(LayerW), P(KVPages), i32, i32, P(i64),
+                                               P(i32), i32, i32, vp, vp, vp, vp, vp, sz, vp]
+        lib.ddl_stack_prefill_paged.argtypes = [P(Shape), ctypes.c_int, P(LayerW), P(KVPages), i32, i32, i64,
+                                                P(i32), i32, i32, vp, vp, vp, vp, vp, sz, vp]
         lib.ddl_stack_decode_noalloc.argtypes = [P(Shape), ctypes.c_int, P(LayerW), P(KV), i32, i32,
                                                  i64, vp, vp, vp, vp, vp]
         lib.ddl_set_launch_mode.argtypes = [i32]
@@ -269,6 +278,59 @@ def ddl_stack_decode_ragged(shape: Shape, wtype: int, layers: list, kvs: list, p
                                      _ptr(workspace), workspace.numel() * workspace.element_size(),
                                      _stream(stream))
     _check("ddl_stack_decode_ragged", st)
+
+
+def _layers_and_pages(layers, pools):
+    L = len(layers)
+    lw = (LayerW * L)()
+    kv = (KVPages * L)()
+    for i, (layer, (kp, vp_)) in enumerate(zip(layers, pools)):
+        lw[i] = LayerW(layer["packed"].data_ptr(), layer["norm1"].data_ptr(),
+                       layer["norm2"].data_ptr())
+        kv[i] = KVPages(kp.data_ptr(), vp_.data_ptr(), kp.shape[0])
+    return lw, kv
+
+
+def _page_table(table):
+    """(ctypes int32 array, rows, entries per row) of a 2-D page table."""
+    t = np.ascontiguousarray(np.asarray(table, dtype=np.int32))
+    if t.ndim != 2:
+        raise ValueError("page table: [rows][pages_per_seq]")
+    return (ctypes.c_int32 * t.size)(*t.ravel().tolist()), t.shape[0], t.shape[1]
+
+
+def ddl_stack_decode_paged(shape: Shape, wtype: int, layers: list, pools: list, pos, page_table, page_size: int,
+                           *, x_bf16: torch.Tensor | None = None, resid_in: torch.Tensor | None = None,
+                           resid_out: torch.Tensor | None = None, out_bf16: torch.Tensor | None = None,
+                           workspace: torch.Tensor, stream=None):
+    """ddl_stack_decode_ragged on paged caches.  pools: (K, V) per layer, each
+    [pages, H_kv, page_size, hd]; page_table: [B][pages_per_seq] page ids."""
+    lib = load()
+    B = (x_bf16 if x_bf16 is not None else resid_in).shape[0]
+    lw, kv = _layers_and_pages(layers, pools)
+    pv = (ctypes.c_int64 * B)(*[int(p) for p in pos])
+    pt, _, per = _page_table(page_table)
+    st = lib.ddl_stack_decode_paged(ctypes.byref(shape), wtype, lw, kv, len(layers), B, pv, pt, per,
+                                    int(page_size), _ptr(resid_in), _ptr(x_bf16), _ptr(resid_out),
+                                    _ptr(out_bf16), _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                    _stream(stream))
+    _check("ddl_stack_decode_paged", st)
+
+
+def ddl_stack_prefill_paged(shape: Shape, wtype: int, layers: list, pools: list, p0: int, page_row, page_size: int,
+                            *, x_bf16: torch.Tensor | None = None, resid_in: torch.Tensor | None = None,
+                            resid_out: torch.Tensor | None = None, out_bf16: torch.Tensor | None = None,
+                            workspace: torch.Tensor, stream=None):
+    """ddl_stack_prefill into paged caches through one page-table row."""
+    lib = load()
+    S = (x_bf16 if x_bf16 is not None else resid_in).shape[0]
+    lw, kv = _layers_and_pages(layers, pools)
+    pt, _, per = _page_table(np.asarray(page_row).reshape(1, -1))
+    st = lib.ddl_stack_prefill_paged(ctypes.byref(shape), wtype, lw, kv, len(layers), S, int(p0), pt, per,
+                                     int(page_size), _ptr(resid_in), _ptr(x_bf16), _ptr(resid_out),
+                                     _ptr(out_bf16), _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                     _stream(stream))
+    _check("ddl_stack_prefill_paged", st)
 
 
 def ddl_stack_prefill(shape: Shape, wtype: int, layers: list, kvs: list, p0: int, *,
