@@ -2517,11 +2517,11 @@ static void ws_layout(const ddl_shape& s, int B, int64_t s_max, int C, const Mat
   w.rope = off;  off = align256(off + (int64_t)B * (64 * 2 * 4 + 4));  // ragged positions: RoPE table, positions
   w.ptab = off;  off = align256(off + (int64_t)B * ((s_max + 15) / 16) * 4);  // page table (pages >= 16 slots)
   // fragment images of a weight stage's input (fp16 high part and remainder
-  // per element), two by stage parity; batches up to NARROW_B
+  // per element), two by stage parity; batches up to IMG_MAX_B
   int64_t kmax = s.D > s.d_ff ? s.D : s.d_ff;
   if (Nq > kmax) kmax = Nq;
   w.ximg = off;
-  w.ximg_bytes = B <= NARROW_B ? align256(kmax * 4 * B) + align256(2 * (kmax / 8) * B * 4) : 0;
+  w.ximg_bytes = B <= IMG_MAX_B ? align256(kmax * 4 * B) + align256(2 * (kmax / 8) * B * 4) : 0;
   off += 2 * w.ximg_bytes;
   w.tc = off;  // the tensor-core path's partials, operand images and sums (batches past NARROW_B)
   if (B > NARROW_B) off = align256(off + tc_workspace_bytes(s, B, DDL_W_INT4));

@@ -63,6 +63,12 @@ constexpr int GC = 32;                // groups per k-chunk
 constexpr int MAX_LAYERS = 96;        // layers per launch (longer stacks use several launches)
 constexpr int MAX_B = 16;             // sequences of a batch
 constexpr int NARROW_B = 4;           // up to this batch x is carried as fp16 hi/lo columns
+// Up to this batch (INT4) a weight stage's producer writes the next stage's
+// input as a fragment image that the next prologue bulk-copies into place; at
+// 3 and 4 sequences the image's bytes (4 per element per sequence) cost more
+// than the in-place conversion they replace (measured on one GB300: batch 2
+// 286 vs 263 tokens/s with and without, batch 4 336 vs 347).
+constexpr int IMG_MAX_B = 2;
 constexpr int MAX_GH = 8;             // query heads per KV head
 constexpr int NSTAGE = 5;
 constexpr int MAXP = 16;              // k-chunk panels per matrix
