@@ -127,6 +127,8 @@ def test_paged_decode_host_checks(lib):
     """The page-table rules are checked on the host before any device work: a
     call that passes them goes on to the device query (no GPU here: a CUDA
     error), one that breaks them returns DDL_ERR_ARG / DDL_ERR_POS."""
+    if torch.cuda.is_available():  # fake device pointers must never reach a GPU
+        pytest.skip("host checks with fake pointers run without a GPU; tests/test_gpu_paged.py has real buffers")
     s = ddl.Shape(512, 8, 2, 64, 1408, 1e-6, 1e4)
     p = ctypes.c_void_p(256)
     lw = (ddl.LayerW * 2)(ddl.LayerW(256, 256, 256), ddl.LayerW(256, 256, 256))
@@ -140,20 +142,15 @@ def test_paged_decode_host_checks(lib):
         return lib.ddl_stack_decode_paged(ctypes.byref(s), ddl.INT4, lw, kv, 2, len(pos), pv, pt, per, ps, None,
                                           p, None, None, p, 1 << 30, None)
 
-    # calls that pass the host checks go on to the device: only without one
-    # (the fake pointers must never reach a launch)
-    nodev = not torch.cuda.is_available()
     good = [[0, 1, 2], [3, 4, 9]]
-    if nodev:
-        assert call(good, [40, 33]) == 6
+    assert call(good, [40, 33]) == 6                  # past the host checks: no device here
     assert call(good, [40, 33], ps=24) == 8           # page size not a power of two
     assert call(good, [40, 33], ps=8) == 8            # below one 16-key tile
     assert call(good, [40, 48]) == 2                  # slot 48 past 3 pages of 16
     assert call([[0, 1, 2], [3, 4, 10]], [40, 33]) == 8   # page 10 of a 10-page pool
     assert call([[0, 1, -1], [3, 4, 9]], [40, 33]) == 8   # negative page id
-    if nodev:
-        assert call([[0, 1, 2], [3, 4, 77]], [40, 15]) == 6  # dead entries are not read
-        assert call([[0, 1, 2], [0, 1, 9]], [40, 33]) == 6   # a shared read-only prefix
+    assert call([[0, 1, 2], [3, 4, 77]], [40, 15]) == 6   # dead entries are not read
+    assert call([[0, 1, 2], [0, 1, 9]], [40, 33]) == 6    # a shared read-only prefix
     assert call([[0, 1, 2], [0, 2, 9]], [40, 33]) == 8    # page 2 receives a row that another sequence reads
     assert call([[0, 1, 1], [3, 4, 9]], [40, 33]) == 8    # a sequence mapping its written page twice
     assert call(good, [40, 33], pages=(10, 11)) == 8      # pools of different sizes
@@ -165,7 +162,6 @@ def test_paged_decode_host_checks(lib):
         return lib.ddl_stack_prefill_paged(ctypes.byref(s), ddl.INT4, lw, kv, 2, S, p0, pt, len(row), 16, None, p,
                                            None, None, p, 1 << 30, None)
 
-    if nodev:
-        assert pre([5, 6, 7], 10, 20) == 6
+    assert pre([5, 6, 7], 10, 20) == 6
     assert pre([5, 6, 6], 10, 30) == 8                # page 6 mapped twice and written
     assert pre([5, 6, 7], 40, 9) == 2                 # past 48 slots
