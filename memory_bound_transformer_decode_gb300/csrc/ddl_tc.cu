@@ -45,7 +45,8 @@ constexpr int A_COLS = 32;       // one group of A: four 16-wide slices of 8 col
 constexpr int LBO = 128, SBO = 1024;  // B-operand image: k-cores of 8 x 16 B, 8 k-cores per column group of 8
 
 struct TcGemm {
-  int32_t N, NT, G, Sk, Gc, glast, S, NR, units, NP, B;
+  int32_t N, NT, G, Sk, Gc, glast, NR, NP, B;
+  uint32_t W, parts;             // (128-row tile, group) items NR * G, CTAs sharing them (the grid)
   uint32_t wbytes, stage_bytes;  // bytes of a stage's weights area (aligned), of a whole stage
   int32_t stages;                // shared-memory ring depth
   int32_t gs;                    // groups per ring stage (at most)
@@ -98,6 +99,30 @@ __device__ __forceinline__ int stage_groups(const TcGemm& P, int g, int g1) {
   return e - g;
 }
 
+// A CTA's work: items [w, w1) of the (128-row tile, 64-wide group) order,
+// tile-major, an equal share of all items; cut at tile edges into segments,
+// each one accumulator's run and one split-K partial of its tile (slot: the
+// CTA's index minus that of the first CTA holding part of the tile).
+struct Seg {
+  uint32_t w, w1;
+  int r, g0, g1;
+  __device__ __forceinline__ bool next(uint32_t G) {
+    if (w >= w1) return false;
+    r = (int)(w / G);
+    g0 = (int)(w - (uint32_t)r * G);
+    const uint32_t e = w1 < (uint32_t)(r + 1) * G ? w1 : (uint32_t)(r + 1) * G;
+    g1 = g0 + (int)(e - w);
+    w = e;
+    return true;
+  }
+};
+__device__ __forceinline__ Seg cta_work(const TcGemm& P) {
+  Seg s;
+  s.w = (uint32_t)range_lo(P.W, P.parts, blockIdx.x);
+  s.w1 = (uint32_t)range_lo(P.W, P.parts, blockIdx.x + 1);
+  return s;
+}
+
 template <int WT>
 __global__ void __launch_bounds__(GT, 1) tc_gemm_kernel(const __grid_constant__ TcGemm P) {
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -140,20 +165,14 @@ __global__ void __launch_bounds__(GT, 1) tc_gemm_kernel(const __grid_constant__ 
     if ((threadIdx.x & 31) == 0) atomicExch(P.status, STATUS_TIMEOUT);
     *abort_flag = 1;
   };
-  auto unit_groups = [&](int u, int& g0, int& g1) {
-    const int s = u / P.NR;
-    g0 = (int)((int64_t)P.G * s / P.S);
-    g1 = (int)((int64_t)P.G * (s + 1) / P.S);
-  };
 
   if (warp == 0) {  // ------------------------------------------------ copies
     const uint64_t policy = policy_evict_first();
     uint32_t sc = 0;  // stages issued
     bool ok = true;
-    for (int u = blockIdx.x; u < P.units && ok; u += gridDim.x) {
-      const int T0 = (u % P.NR) * 8, nt = P.NT - T0 < 8 ? P.NT - T0 : 8;
-      int g0, g1;
-      unit_groups(u, g0, g1);
+    for (Seg sg = cta_work(P); ok && sg.next((uint32_t)P.G);) {
+      const int T0 = sg.r * 8, nt = P.NT - T0 < 8 ? P.NT - T0 : 8;
+      const int g0 = sg.g0, g1 = sg.g1;
       for (int g = g0; g < g1; ++sc) {
         const int ng = stage_groups(P, g, g1);
         const uint32_t st = sc % NS, k = sc / NS;
@@ -185,9 +204,8 @@ __global__ void __launch_bounds__(GT, 1) tc_gemm_kernel(const __grid_constant__ 
     const uint32_t gstep = (uint32_t)P.NP * 128u >> 4, sstep = P.stage_bytes >> 4;  // descriptor address units
     uint32_t sc = 0, it = 0, ui = 0;
     bool ok = true;
-    for (int u = blockIdx.x; u < P.units && ok; u += gridDim.x, ++ui) {
-      int g0, g1;
-      unit_groups(u, g0, g1);
+    for (Seg sg = cta_work(P); ok && sg.next((uint32_t)P.G); ++ui) {
+      const int g0 = sg.g0, g1 = sg.g1;
       const uint32_t db = ui % ND, dk = ui / ND, dcol = tm + D_COL0 + db * P.dstride;
       if (dk > 0 && !mbar_wait_warp(dfree0 + db * 8, (dk - 1) & 1, P.status, P.wait_ns)) {
         fail();
@@ -241,10 +259,9 @@ __global__ void __launch_bounds__(GT, 1) tc_gemm_kernel(const __grid_constant__ 
     const int d = (warp - 4) >> 2, q = warp & 3, g = lane >> 2;
     uint32_t sc = 0, it = 0;
     bool ok = true;
-    for (int u = blockIdx.x; u < P.units && ok; u += gridDim.x) {
-      const int T0 = (u % P.NR) * 8, nt = P.NT - T0 < 8 ? P.NT - T0 : 8;
-      int g0, g1;
-      unit_groups(u, g0, g1);
+    for (Seg sg = cta_work(P); ok && sg.next((uint32_t)P.G);) {
+      const int T0 = sg.r * 8, nt = P.NT - T0 < 8 ? P.NT - T0 : 8;
+      const int g0 = sg.g0, g1 = sg.g1;
       for (int gs = g0; gs < g1 && ok; ++sc) {
         const int ng = stage_groups(P, gs, g1);
         const uint32_t st = sc % NS, k = sc / NS;
@@ -304,8 +321,9 @@ __global__ void __launch_bounds__(GT, 1) tc_gemm_kernel(const __grid_constant__ 
     // the accumulator of each unit: row 32 q + lane, limb columns l * B + b (l = 0, 1)
     const int q = warp & 3;
     uint32_t ui = 0;
-    for (int u = blockIdx.x; u < P.units; u += gridDim.x, ++ui) {
-      const int rt = u % P.NR, s = u / P.NR;
+    for (Seg sg = cta_work(P); sg.next((uint32_t)P.G); ++ui) {
+      const int rt = sg.r;
+      const int s = (int)blockIdx.x - (int)owner32(P.W, P.parts, (uint32_t)rt * (uint32_t)P.G);
       const uint32_t db = ui % ND, dk = ui / ND;
       if (!mbar_wait_warp_nap(dready0 + db * 8, dk & 1, P.status, P.wait_ns, 500)) {  // a unit takes many us
         fail();
@@ -343,7 +361,8 @@ __global__ void __launch_bounds__(GT, 1) tc_gemm_kernel(const __grid_constant__ 
 enum EpiKind { EK_QKV = 0, EK_WO = 2, EK_GU = 3, EK_DOWN = 4, EK_PREP_X = 5, EK_PREP_ATT = 6 };
 
 struct TcEpi {
-  int32_t kind, N, S, B, D, Hq, Hkv, hd, dff, NP;
+  int32_t kind, N, B, D, Hq, Hkv, hd, dff, NP;
+  uint32_t W, parts, G;      // the GEMM's items, CTAs and groups per 128-row tile: which partials a row has
   float eps;
   int64_t pos, s_max;
   const float* part;
@@ -401,9 +420,11 @@ __global__ void __launch_bounds__(256) tc_epi_kernel(const __grid_constant__ TcE
   const int64_t items = (E.kind == EK_QKV || E.kind == EK_GU) ? (int64_t)(E.N / 16) * 8 : E.N;
   const int64_t i0 = items * blockIdx.x / gridDim.x, i1 = items * (blockIdx.x + 1) / gridDim.x;
   float ss = 0.f;
-  auto psum = [&](int row) {  // split-K partials of packed row `row`, sequence b, in split order
+  auto psum = [&](int row) {  // split-K partials of packed row `row`, sequence b, in CTA order
+    const uint32_t r = (uint32_t)row >> 7;
+    const int ns = (int)(owner32(E.W, E.parts, (r + 1) * E.G - 1) - owner32(E.W, E.parts, r * E.G)) + 1;
     float v = 0.f;
-    for (int s = 0; s < E.S; ++s) v += __ldcg(E.part + ((int64_t)s * E.N + row) * B + b);
+    for (int s = 0; s < ns; ++s) v += __ldcg(E.part + ((int64_t)s * E.N + row) * B + b);
     return v;
   };
   if (act)
@@ -512,13 +533,19 @@ int prepare(int wtype) {
 int64_t al256(int64_t x) { return (x + 255) & ~int64_t(255); }
 uint32_t al1024(uint32_t x) { return (x + 1023u) & ~1023u; }
 
-int split_of(const MatGeom& m, int C) {
-  const int NR = (m.NT + 7) / 8;
-  int S = (C + NR / 2) / NR;
-  if (S < 1) S = 1;
-  if (S > TC_MAX_SPLIT) S = TC_MAX_SPLIT;
-  if (S > m.G) S = m.G;
-  return S;
+// The GEMM's CTAs for matrix m on C SMs (each holds an equal share of the
+// NR * G items; every CTA at least one) and the most partials a tile gets.
+void split_of(const MatGeom& m, int C, uint32_t& parts, int& slots) {
+  const uint32_t NR = (uint32_t)(m.NT + 7) / 8, W = NR * (uint32_t)m.G;
+  parts = W < (uint32_t)C ? W : (uint32_t)C;
+  for (;; --parts) {  // a tile's partials within TC_MAX_SPLIT (a no-op at the model shapes)
+    slots = 0;
+    for (uint32_t r = 0; r < NR; ++r) {
+      const int n = (int)(owner32(W, parts, (r + 1) * m.G - 1) - owner32(W, parts, r * m.G)) + 1;
+      if (n > slots) slots = n;
+    }
+    if (slots <= TC_MAX_SPLIT || parts == 1) return;
+  }
 }
 
 void tc_sizes(const ddl_shape& s, int B, int C, int64_t& part_floats, int64_t& xl_bytes) {
@@ -527,7 +554,10 @@ void tc_sizes(const ddl_shape& s, int B, int C, int64_t& part_floats, int64_t& x
   part_floats = 0;
   xl_bytes = 0;
   for (int k = 0; k < 4; ++k) {
-    const int64_t p = (int64_t)split_of(mg[k], C) * mg[k].N * B;
+    uint32_t parts;
+    int slots;
+    split_of(mg[k], C, parts, slots);
+    const int64_t p = (int64_t)slots * mg[k].N * B;
     if (p > part_floats) part_floats = p;
     const int64_t x = (int64_t)mg[k].G * tc_ncols(B) * 128;
     if (x > xl_bytes) xl_bytes = x;
@@ -633,9 +663,11 @@ int tc_stage(const TcRun& R, int layer, int st, void* stream) {
   G.Sk = m.Sk;
   G.Gc = m.Gc;
   G.glast = m.G - (m.Sk - 1) * m.Gc;
-  G.S = split_of(m, R.C);
   G.NR = (m.NT + 7) / 8;
-  G.units = G.NR * G.S;
+  if ((uint64_t)G.NR * (uint64_t)m.G * (uint64_t)R.C >= (1ull << 32)) return DDL_ERR_UNSUPPORTED;  // owner32
+  int slots;
+  split_of(m, R.C, G.parts, slots);
+  G.W = (uint32_t)G.NR * (uint32_t)m.G;
   G.NP = NP;
   G.B = B;
   const uint32_t BB = R.wtype == DDL_W_INT4 ? QBLK_BYTES : BF16_BLK_BYTES;
@@ -666,14 +698,16 @@ int tc_stage(const TcRun& R, int layer, int st, void* stream) {
   if (smem > 227 * 1024) return DDL_ERR_UNSUPPORTED;
   {
     void* args[] = {&G};
-    const int grid = G.units < R.C ? G.units : R.C;
+    const int grid = (int)G.parts;
     const void* fn = R.wtype == DDL_W_INT4 ? (const void*)tc_gemm_kernel<DDL_W_INT4> : (const void*)tc_gemm_kernel<DDL_W_BF16>;
     if ((rc = cuda_status(cudaLaunchKernel(fn, dim3(grid), dim3(GT), args, smem, cs)))) return rc;
   }
   TcEpi E = epi_base(R);
   E.kind = st;
   E.N = m.N;
-  E.S = G.S;
+  E.W = G.W;
+  E.parts = G.parts;
+  E.G = (uint32_t)m.G;
   switch (st) {
     case ST_QKV:
       E.out = R.q;
