@@ -240,10 +240,16 @@ __device__ __noinline__ uint32_t owned_slots(const MatGeom& m, int T) {  // bit 
   }
   return mask;
 }
-// Compute this warp's entry for every stage kind (once per launch).
+// Compute this warp's entry for every stage kind the launch runs (once per
+// launch; a launch of the attention stage alone, as the tensor-core path
+// makes one per layer, skips the weight stages' entries, which cost up to
+// tens of microseconds on some CTAs).
 __device__ __noinline__ void compute_entries(const Params& P) {
   const int warp = threadIdx.x >> 5;
+  uint32_t kinds = 0;
+  for (int s = P.stage_begin; s < P.stage_end && kinds != (1u << NSTAGE) - 1; ++s) kinds |= 1u << (s % NSTAGE);
   for (int st = 0; st < NSTAGE; ++st) {
+    if (!(kinds & (1u << st))) continue;
     Entry e;
     if (st == ST_ATT) {
       int64_t lo, hi;
@@ -2374,6 +2380,7 @@ __global__ void __launch_bounds__(NTHREADS_ALL, 1) decode_kernel(const __grid_co
   regs_inc<CONSUMER_REGS>();
   compute_entries(P);
   asm volatile("bar.arrive 2, %0;" ::"n"(NTHREADS + 32) : "memory");
+  csync();  // every warp's entries written before any warp reads another's (the stage context reads warp 0's)
   Ring& R = ctx().ring[warp];
   bool ok = true;
   for (int s = P.stage_begin; s < P.stage_end && ok; ++s) {
