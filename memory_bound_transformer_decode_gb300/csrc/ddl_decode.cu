@@ -2332,6 +2332,7 @@ template <int HD, int WT, bool WIDE, bool RAG>
 __global__ void __launch_bounds__(NTHREADS_ALL, 1) decode_kernel(const __grid_constant__ Params P) {
   uint8_t* smem = g_smem;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  pdl_trigger();
   {  // indexed parameters to shared memory (read after the barrier below)
     SParams& S = *reinterpret_cast<SParams*>(smem + SM_SPAR);
     const uint32_t* src = reinterpret_cast<const uint32_t*>(P.mg);
@@ -2381,6 +2382,11 @@ __global__ void __launch_bounds__(NTHREADS_ALL, 1) decode_kernel(const __grid_co
   compute_entries(P);
   asm volatile("bar.arrive 2, %0;" ::"n"(NTHREADS + 32) : "memory");
   csync();  // every warp's entries written before any warp reads another's (the stage context reads warp 0's)
+  // A launch that overlaps the previous kernel (the tensor-core path's
+  // attention stage) waits for it here; the producer does not: it reads only
+  // weights and K/V history, and the consumers reload the rows this step
+  // appends.
+  pdl_wait();
   Ring& R = ctx().ring[warp];
   bool ok = true;
   for (int s = P.stage_begin; s < P.stage_end && ok; ++s) {
@@ -2814,7 +2820,7 @@ static int decode(const ddl_shape* s, ddl_wtype wtype, const ddl_layer_w* layers
         P.stage_begin = l * NSTAGE + ST_ATT;
         P.stage_end = P.stage_begin + 1;
         void* args[] = {&P};
-        if ((e = cudaLaunchKernel(fn, dim3(C), dim3(NTHREADS_ALL), args, SM_TOTAL, cs)) != cudaSuccess)
+        if ((e = launch_pdl(fn, dim3(C), dim3(NTHREADS_ALL), args, SM_TOTAL, cs)) != cudaSuccess)
           return cuda_status(e);
         for (int stg : {ST_WO, ST_GU, ST_DOWN})
           if ((st = tc_stage(R, l, stg, stream))) return st;

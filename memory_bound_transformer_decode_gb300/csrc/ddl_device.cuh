@@ -101,6 +101,12 @@ __device__ __forceinline__ bool mbar_wait_warp_nap(uint32_t bar, uint32_t parity
 // Block barrier of the consumer warps only (barrier 1, 256 threads); the
 // producer warp never takes part.
 __device__ __forceinline__ void csync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+// Programmatic dependent launch: let the next kernel of the stream be
+// scheduled (its blocks start as this grid's leave), and wait until the
+// previous kernel has completed with its writes visible (a no-op when the
+// launch has no programmatic dependency).
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 // Per-warpgroup register budgets (all four warps of a warpgroup execute it).
 template <int N>
 __device__ __forceinline__ void regs_dec() { asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N)); }

@@ -106,4 +106,22 @@ inline bool make_panels(MatGeom& m, int B, int C) {
   return true;
 }
 
+// A kernel launch that may overlap the previous kernel of the stream
+// (programmatic dependent launch): its blocks may start while that kernel
+// finishes, so the kernel waits (griddepcontrol.wait) before it reads what
+// that kernel writes or writes what it reads.
+inline cudaError_t launch_pdl(const void* fn, dim3 grid, dim3 block, void** args, size_t smem, cudaStream_t s) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelExC(&cfg, fn, args);
+}
+
 }  // namespace ddl

@@ -161,6 +161,7 @@ __global__ void __launch_bounds__(GT, 1) tc_gemm_kernel(const __grid_constant__ 
   tc_fence_after();
   const uint32_t tm = *tslot;
   const uint32_t sbase = smem_addr(smem);
+  pdl_wait();  // the previous kernel's operand images, and its reads of the partials this kernel writes
   auto fail = [&]() {
     if ((threadIdx.x & 31) == 0) atomicExch(P.status, STATUS_TIMEOUT);
     *abort_flag = 1;
@@ -351,6 +352,10 @@ __global__ void __launch_bounds__(GT, 1) tc_gemm_kernel(const __grid_constant__ 
   }
   tc_fence_before();
   __syncthreads();
+  // the epilogue may be scheduled now: released at the end, not the start, so
+  // its blocks land on SMs this grid is leaving (an early release measured
+  // slower at 64 sequences with bf16 weights)
+  pdl_trigger();
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tm, TMEM_COLS);
@@ -409,6 +414,8 @@ __global__ void __launch_bounds__(256) tc_epi_kernel(const __grid_constant__ TcE
   __shared__ float rfac[TC_MAX_B];
   const int tid = threadIdx.x, B = E.B, RR = 256 / B, rr = tid / B, b = tid - rr * B;
   const bool act = rr < RR;
+  pdl_trigger();
+  pdl_wait();  // the previous kernel's outputs (partials, sums of squares, vectors)
   // RMSNorm factor of the stage's input, per sequence, from the sums of squares
   // of the CTAs that wrote it (in CTA order)
   if (E.ss_in && tid < B) {
@@ -566,7 +573,7 @@ void tc_sizes(const ddl_shape& s, int B, int C, int64_t& part_floats, int64_t& x
 
 int launch_epi(const TcEpi& E, cudaStream_t cs) {
   void* args[] = {const_cast<TcEpi*>(&E)};
-  return cuda_status(cudaLaunchKernel((const void*)tc_epi_kernel, dim3(TC_EPI_CTAS), dim3(256), args, 0, cs));
+  return cuda_status(launch_pdl((const void*)tc_epi_kernel, dim3(TC_EPI_CTAS), dim3(256), args, 0, cs));
 }
 
 TcEpi epi_base(const TcRun& R) {
@@ -700,7 +707,7 @@ int tc_stage(const TcRun& R, int layer, int st, void* stream) {
     void* args[] = {&G};
     const int grid = (int)G.parts;
     const void* fn = R.wtype == DDL_W_INT4 ? (const void*)tc_gemm_kernel<DDL_W_INT4> : (const void*)tc_gemm_kernel<DDL_W_BF16>;
-    if ((rc = cuda_status(cudaLaunchKernel(fn, dim3(grid), dim3(GT), args, smem, cs)))) return rc;
+    if ((rc = cuda_status(launch_pdl(fn, dim3(grid), dim3(GT), args, smem, cs)))) return rc;
   }
   TcEpi E = epi_base(R);
   E.kind = st;
