@@ -54,7 +54,7 @@ struct TcGemm {
   int32_t dstride;               // columns of an accumulator: NP + 16 (the read-out takes 16 at a time)
   const uint8_t* w;              // the matrix's block stream
   const uint8_t* xl;             // B-operand images, NP * 128 bytes per group
-  float* part;                   // [S][N][B] partial sums, rows in the packed (tile) order
+  float* part;                   // [S][B][N] partial sums, rows in the packed (tile) order
   uint32_t* status;
   uint64_t wait_ns;
 };
@@ -339,10 +339,10 @@ __global__ void __launch_bounds__(GT, 1) tc_gemm_kernel(const __grid_constant__ 
         tmem_ld_32x32b_x16(tr + P.B + b0, v1);
         tmem_ld_wait();
         if (n < P.N) {
-          float* dst = P.part + ((int64_t)s * P.N + n) * P.B;
+          float* dst = P.part + (int64_t)s * P.B * P.N + n;  // [S][B][N]: the lanes' rows are consecutive
 #pragma unroll
           for (int j = 0; j < 16; ++j)
-            if (b0 + j < P.B) dst[b0 + j] = 256.f * (__uint_as_float(v0[j]) + __uint_as_float(v1[j]));
+            if (b0 + j < P.B) dst[(int64_t)(b0 + j) * P.N] = 256.f * (__uint_as_float(v0[j]) + __uint_as_float(v1[j]));
         }
       }
       tc_fence_before();
@@ -412,36 +412,57 @@ __device__ __forceinline__ void put_limbs(uint8_t* xl, int NP, int B, int k, int
 __global__ void __launch_bounds__(256) tc_epi_kernel(const __grid_constant__ TcEpi E) {
   __shared__ float red[256];
   __shared__ float rfac[TC_MAX_B];
-  const int tid = threadIdx.x, B = E.B, RR = 256 / B, rr = tid / B, b = tid - rr * B;
-  const bool act = rr < RR;
+  const int tid = threadIdx.x, B = E.B, lane = tid & 31, warp = tid >> 5;
   pdl_trigger();
   pdl_wait();  // the previous kernel's outputs (partials, sums of squares, vectors)
   // RMSNorm factor of the stage's input, per sequence, from the sums of squares
-  // of the CTAs that wrote it (in CTA order)
-  if (E.ss_in && tid < B) {
+  // of the CTAs that wrote it: thread (rr, b) sums CTAs rr, rr + RR, ... in
+  // that order, eight loads in flight at a time, then thread b sums the RR
+  // partials in rr order (a fixed order)
+  if (E.ss_in) {
+    const int RR = 256 / B, rr = tid / B, b = tid - rr * B;
     float ss = 0.f;
-    for (int c = 0; c < TC_EPI_CTAS; ++c) ss += E.ss_in[c * B + tid];
-    rfac[tid] = 1.0f / sqrtf(ss / (float)E.ss_K + E.eps);
+    if (rr < RR) {
+      int c = rr;
+      for (; c + 7 * RR < TC_EPI_CTAS; c += 8 * RR) {
+        float v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) v[u] = __ldcg(E.ss_in + (c + u * RR) * B + b);
+#pragma unroll
+        for (int u = 0; u < 8; ++u) ss += v[u];
+      }
+      for (; c < TC_EPI_CTAS; c += RR) ss += __ldcg(E.ss_in + c * B + b);
+    }
+    red[tid] = ss;
+    __syncthreads();
+    if (tid < B) {
+      float t = 0.f;
+      for (int k = 0; k < RR; ++k) t += red[k * B + tid];
+      rfac[tid] = 1.0f / sqrtf(t / (float)E.ss_K + E.eps);
+    }
   }
   __syncthreads();
   const int64_t items = (E.kind == EK_QKV || E.kind == EK_GU) ? (int64_t)(E.N / 16) * 8 : E.N;
   const int64_t i0 = items * blockIdx.x / gridDim.x, i1 = items * (blockIdx.x + 1) / gridDim.x;
-  float ss = 0.f;
-  auto psum = [&](int row) {  // split-K partials of packed row `row`, sequence b, in CTA order
+  auto psum = [&](int row, int b) {  // split-K partials of packed row `row`, sequence b, in CTA order
     const uint32_t r = (uint32_t)row >> 7;
     const int ns = (int)(owner32(E.W, E.parts, (r + 1) * E.G - 1) - owner32(E.W, E.parts, r * E.G)) + 1;
     float v = 0.f;
-    for (int s = 0; s < ns; ++s) v += __ldcg(E.part + ((int64_t)s * E.N + row) * B + b);
+    for (int s = 0; s < ns; ++s) v += __ldcg(E.part + ((int64_t)s * B + b) * E.N + row);
     return v;
   };
-  if (act)
-    for (int64_t it = i0 + rr; it < i1; it += RR) {
+  // Warp w takes sequences w, w + 8, ...; its lanes take the CTA's items, so
+  // that the partials, the [B][N] vectors and the limb images are read and
+  // written along rows (coalesced).
+  for (int b = warp; b < B; b += 8) {
+    float ss = 0.f;
+    for (int64_t it = i0 + lane; it < i1; it += 32) {
       const int i = (int)it;
       switch (E.kind) {
         case EK_QKV: {
           const int T = i >> 3, gg = i & 7, tph = E.hd / 16, head = T / tph, ii = 8 * (T % tph) + gg;
           const float r = rfac[b];
-          float v0 = psum(16 * T + gg) * r, v1 = psum(16 * T + gg + 8) * r;
+          float v0 = psum(16 * T + gg, b) * r, v1 = psum(16 * T + gg + 8, b) * r;
           if (head < E.Hq + E.Hkv) {  // RoPE on q and k: pair (ii, ii + hd/2)
             const float c = E.rope_b ? E.rope_b[((int64_t)b * 64 + ii) * 2] : E.rope[ii][0];
             const float sn = E.rope_b ? E.rope_b[((int64_t)b * 64 + ii) * 2 + 1] : E.rope[ii][1];
@@ -470,7 +491,7 @@ __global__ void __launch_bounds__(256) tc_epi_kernel(const __grid_constant__ TcE
         }
         case EK_GU: {
           const int T = i >> 3, gg = i & 7, j = 8 * T + gg;
-          const float r = rfac[b], gt = psum(16 * T + gg) * r, up = psum(16 * T + gg + 8) * r;
+          const float r = rfac[b], gt = psum(16 * T + gg, b) * r, up = psum(16 * T + gg + 8, b) * r;
           const float av = gt / (1.0f + expf(-gt)) * up;
           E.out[(int64_t)b * E.dff + j] = av;
           if (E.xl) put_limbs(E.xl, E.NP, B, j, b, av);
@@ -479,7 +500,7 @@ __global__ void __launch_bounds__(256) tc_epi_kernel(const __grid_constant__ TcE
         case EK_WO: {
           const int64_t o = (int64_t)b * E.D + i;
           const float x = E.xin32 ? __ldcg(E.xin32 + o) : bf16_bits_to_f32(E.xin16[o]);
-          const float y = x + psum(i);
+          const float y = x + psum(i, b);
           E.out[o] = y;
           ss = fmaf(y, y, ss);
           if (E.xl) put_limbs(E.xl, E.NP, B, i, b, y * bf16_bits_to_f32(E.nw[i]));
@@ -487,7 +508,7 @@ __global__ void __launch_bounds__(256) tc_epi_kernel(const __grid_constant__ TcE
         }
         case EK_DOWN: {
           const int64_t o = (int64_t)b * E.D + i;
-          const float z = __ldcg(E.vec + o) + psum(i);
+          const float z = __ldcg(E.vec + o) + psum(i, b);
           E.out[o] = z;
           ss = fmaf(z, z, ss);
           if (E.xl) put_limbs(E.xl, E.NP, B, i, b, z * bf16_bits_to_f32(E.nw[i]));
@@ -508,13 +529,10 @@ __global__ void __launch_bounds__(256) tc_epi_kernel(const __grid_constant__ TcE
         }
       }
     }
-  if (E.ss_out) {  // this CTA's sums of squares per sequence, reduced in a fixed order
-    red[tid] = act ? ss : 0.f;
-    __syncthreads();
-    if (tid < B) {
-      float t = 0.f;
-      for (int k = 0; k < RR; ++k) t += red[k * B + tid];
-      E.ss_out[blockIdx.x * B + tid] = t;
+    if (E.ss_out) {  // this CTA's sum of squares of sequence b: the lanes' sums in a fixed tree
+#pragma unroll
+      for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+      if (lane == 0) E.ss_out[blockIdx.x * B + b] = ss;
     }
   }
 }
