@@ -55,6 +55,10 @@ struct TcGemm {
   const uint8_t* w;              // the matrix's block stream
   const uint8_t* xl;             // B-operand images, NP * 128 bytes per group
   float* part;                   // [S][B][N] partial sums, rows in the packed (tile) order
+  const float* ss_in;            // QKV, gate/up: the epilogue CTAs' sums of squares of the stage input ...
+  float* rfac;                   // ... reduced here to the RMSNorm factor per sequence (else NULL)
+  int32_t ss_K;                  // the input's length
+  float eps;
   uint32_t* status;
   uint64_t wait_ns;
 };
@@ -254,6 +258,18 @@ __global__ void __launch_bounds__(GT, 1) tc_gemm_kernel(const __grid_constant__ 
     if (elect_one()) umma_commit(fin);
     __syncwarp();
     mbar_wait_warp(fin, 0, P.status, P.wait_ns);
+  } else if (warp == 3) {  // ----------------------------- RMSNorm factors
+    // for the stage's epilogue, once per sequence instead of in each of its
+    // CTAs: lane l sums CTAs l, l + 32, ... in that order, then a fixed tree
+    if (P.rfac)
+      for (int b = blockIdx.x; b < P.B; b += gridDim.x) {
+        float ss = 0.f;
+#pragma unroll
+        for (int c = lane; c < TC_EPI_CTAS; c += 32) ss += __ldcg(P.ss_in + c * P.B + b);
+#pragma unroll
+        for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+        if (lane == 0) P.rfac[b] = 1.0f / sqrtf(ss / (float)P.ss_K + P.eps);
+      }
   } else if (warp >= 4 && warp < 4 + 4 * NDW) {  // ------------------ A operand
     // expansion warpgroup d takes the CTA's groups it, it + NDW, ...; warp q
     // of it writes tensor-memory lanes 32 q .. 32 q + 31 (tiles 2q, 2q+1)
@@ -379,9 +395,8 @@ struct TcEpi {
   uint16_t* vc;
   const uint16_t* nw;        // RMSNorm weight the limbs are multiplied by (WO: norm2, DOWN: next norm1, PREP_X: norm1)
   uint8_t* xl;               // limb images written (NULL: none)
-  const float* ss_in;        // QKV, GU: sums of squares of the stage's input, per epilogue CTA
+  const float* rfac_in;      // QKV, GU: RMSNorm factor of the stage's input per sequence (from its GEMM)
   float* ss_out;             // WO, DOWN, PREP_X: of the vector written
-  int32_t ss_K;              // length of the vector of ss_in
   float* resid_out;          // DOWN of the stack's last layer
   uint16_t* out_bf16;
   float rope[64][2];
@@ -415,32 +430,7 @@ __global__ void __launch_bounds__(256) tc_epi_kernel(const __grid_constant__ TcE
   const int tid = threadIdx.x, B = E.B, lane = tid & 31, warp = tid >> 5;
   pdl_trigger();
   pdl_wait();  // the previous kernel's outputs (partials, sums of squares, vectors)
-  // RMSNorm factor of the stage's input, per sequence, from the sums of squares
-  // of the CTAs that wrote it: thread (rr, b) sums CTAs rr, rr + RR, ... in
-  // that order, eight loads in flight at a time, then thread b sums the RR
-  // partials in rr order (a fixed order)
-  if (E.ss_in) {
-    const int RR = 256 / B, rr = tid / B, b = tid - rr * B;
-    float ss = 0.f;
-    if (rr < RR) {
-      int c = rr;
-      for (; c + 7 * RR < TC_EPI_CTAS; c += 8 * RR) {
-        float v[8];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) v[u] = __ldcg(E.ss_in + (c + u * RR) * B + b);
-#pragma unroll
-        for (int u = 0; u < 8; ++u) ss += v[u];
-      }
-      for (; c < TC_EPI_CTAS; c += RR) ss += __ldcg(E.ss_in + c * B + b);
-    }
-    red[tid] = ss;
-    __syncthreads();
-    if (tid < B) {
-      float t = 0.f;
-      for (int k = 0; k < RR; ++k) t += red[k * B + tid];
-      rfac[tid] = 1.0f / sqrtf(t / (float)E.ss_K + E.eps);
-    }
-  }
+  if (E.rfac_in && tid < B) rfac[tid] = __ldcg(E.rfac_in + tid);  // RMSNorm factor of the stage input
   __syncthreads();
   const int64_t items = (E.kind == EK_QKV || E.kind == EK_GU) ? (int64_t)(E.N / 16) * 8 : E.N;
   const int64_t i0 = items * blockIdx.x / gridDim.x, i1 = items * (blockIdx.x + 1) / gridDim.x;
@@ -608,7 +598,6 @@ TcEpi epi_base(const TcRun& R) {
   E.pos = R.pos;
   E.s_max = R.s_max;
   E.part = R.part;
-  E.ss_K = R.D;
   memcpy(E.rope, R.rope, sizeof E.rope);
   E.posb = R.posb;
   E.kv_bstride = R.kv_bstride;
@@ -628,7 +617,7 @@ int64_t tc_workspace_bytes(const ddl_shape& s, int B, int wtype) {
     return -1;
   int64_t pf, xb;
   tc_sizes(s, B, C, pf, xb);
-  return al256(pf * 4) + al256(xb) + al256((int64_t)2 * TC_EPI_CTAS * B * 4);
+  return al256(pf * 4) + al256(xb) + al256((int64_t)2 * TC_EPI_CTAS * B * 4) + al256((int64_t)2 * B * 4);
 }
 
 void tc_workspace_carve(const ddl_shape& s, int B, int wtype, uint8_t* base, TcRun& R) {
@@ -638,6 +627,7 @@ void tc_workspace_carve(const ddl_shape& s, int B, int wtype, uint8_t* base, TcR
   R.part = reinterpret_cast<float*>(base);
   R.xl = base + al256(pf * 4);
   R.ss = reinterpret_cast<float*>(R.xl + al256(xb));
+  R.rfac = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(R.ss) + al256((int64_t)2 * TC_EPI_CTAS * B * 4));
 }
 
 int tc_begin(const TcRun& R, void* stream) {
@@ -710,6 +700,12 @@ int tc_stage(const TcRun& R, int layer, int st, void* stream) {
   G.w = Ly.packed + m.woff;
   G.xl = R.xl;
   G.part = R.part;
+  if (st == ST_QKV || st == ST_GU) {  // this GEMM also reduces its epilogue's RMSNorm factors
+    G.ss_in = R.ss + (st == ST_GU ? TC_EPI_CTAS * B : 0);
+    G.rfac = R.rfac + (st == ST_GU ? B : 0);
+    G.ss_K = R.D;
+    G.eps = R.eps;
+  }
   G.status = R.status;
   G.wait_ns = R.wait_ns;
   // as many ring stages as fit (at most MAX_STAGES); at least half of an SM's
@@ -738,7 +734,7 @@ int tc_stage(const TcRun& R, int layer, int st, void* stream) {
       E.out = R.q;
       E.kc = Ly.kc;
       E.vc = Ly.vc;
-      E.ss_in = R.ss;
+      E.rfac_in = R.rfac;
       break;
     case ST_WO:
       if (gl == 0) {
@@ -755,7 +751,7 @@ int tc_stage(const TcRun& R, int layer, int st, void* stream) {
     case ST_GU:
       E.out = R.a;
       E.xl = R.xl;
-      E.ss_in = R.ss + TC_EPI_CTAS * B;
+      E.rfac_in = R.rfac + B;
       break;
     default: {  // ST_DOWN
       E.vec = R.y;

@@ -68,6 +68,7 @@ struct TcRun {
   float* part;                   // split-K partials
   uint8_t* xl;                   // B-operand limb images of the next GEMM's input
   float* ss;                     // [2][TC_EPI_CTAS][B] partial sums of squares (QKV input, gate/up input)
+  float* rfac;                   // [2][B] RMSNorm factors of those inputs (from ss, by the stage's GEMM)
 };
 
 // Workspace bytes of the path (beyond the decode kernel's own layout).
