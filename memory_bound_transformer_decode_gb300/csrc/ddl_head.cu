@@ -172,6 +172,7 @@ __global__ void __launch_bounds__(PREP_THREADS) head_prep_kernel(const float* __
                                                                  float* __restrict__ osc) {
   __shared__ float red[2][PREP_THREADS / 32];
   const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  pdl_trigger();  // the logits kernel may be scheduled (it waits for this one before reading x's fragments)
   const float* xb = x + (int64_t)b * D;
   float ss = 0.f, mx = 0.f;
   for (int k = tid; k < D; k += PREP_THREADS) {
@@ -280,6 +281,8 @@ __device__ __forceinline__ void lse_merge(float& m, int& id, float& s, float m2,
 template <int WT, int NTN, int PER>
 __global__ void __launch_bounds__(HEAD_THREADS, NTN <= 4 ? HEAD_CTAS_PER_SM : 1)
     head_gemv_kernel(const HeadArgs A) {
+  pdl_trigger();
+  pdl_wait();  // the activation fragments from the preparation kernel
   constexpr int BLK = WT == DDL_W_INT4 ? QBLK_BYTES : BF16_BLK_BYTES;
   const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
   const int gw = blockIdx.x * (HEAD_THREADS / 32) + (threadIdx.x >> 5);
@@ -468,6 +471,7 @@ __global__ void __launch_bounds__(SEL_THREADS) head_select_kernel(const SelArgs 
   __shared__ uint32_t wsum[SEL_THREADS / 32];
   __shared__ unsigned long long cand[DDL_MAX_TOP_K];
   __shared__ float cw[DDL_MAX_TOP_K];
+  pdl_wait();  // the logits kernel's records and logits
   __shared__ uint32_t sh_digit, sh_krem;
   const int b = blockIdx.x, tid = threadIdx.x;
   // 1. the warps' records, merged in a fixed order: strided runs, then a tree
@@ -644,19 +648,20 @@ extern "C" size_t ddl_head_workspace_bytes(int32_t D, int64_t V, int32_t B) {
 }
 
 template <int WT, int NTN, int PER>
-static void launch_gemv(const HeadLayout& h, const HeadArgs& a, cudaStream_t s) {
-  head_gemv_kernel<WT, NTN, PER><<<h.ctas, HEAD_THREADS, 0, s>>>(a);
+static cudaError_t launch_gemv(const HeadLayout& h, const HeadArgs& a, cudaStream_t s) {
+  void* args[] = {const_cast<HeadArgs*>(&a)};
+  return launch_pdl((const void*)head_gemv_kernel<WT, NTN, PER>, dim3(h.ctas), dim3(HEAD_THREADS), args, 0, s);
 }
 
 template <int WT>
-static void launch_gemv_ntn(int ntn, const HeadLayout& h, const HeadArgs& a, cudaStream_t s) {
+static cudaError_t launch_gemv_ntn(int ntn, const HeadLayout& h, const HeadArgs& a, cudaStream_t s) {
   constexpr int P1 = WT == DDL_W_INT4 ? 8 : 2;
   switch (ntn) {
-    case 1: launch_gemv<WT, 1, P1>(h, a, s); break;
-    case 2: launch_gemv<WT, 2, P1 / 2>(h, a, s); break;
-    case 4: launch_gemv<WT, 4, (P1 / 4 > 0 ? P1 / 4 : 1)>(h, a, s); break;
-    case 8: launch_gemv<WT, 8, 1>(h, a, s); break;
-    default: launch_gemv<WT, 16, 1>(h, a, s); break;
+    case 1: return launch_gemv<WT, 1, P1>(h, a, s);
+    case 2: return launch_gemv<WT, 2, P1 / 2>(h, a, s);
+    case 4: return launch_gemv<WT, 4, (P1 / 4 > 0 ? P1 / 4 : 1)>(h, a, s);
+    case 8: return launch_gemv<WT, 8, 1>(h, a, s);
+    default: return launch_gemv<WT, 16, 1>(h, a, s);
   }
 }
 
@@ -699,9 +704,9 @@ extern "C" int ddl_lm_head(int32_t D, int64_t V, ddl_wtype wtype, const void* he
   a.NTt = (int32_t)((V + 15) / 16);
   a.B = B;
   a.nwarps = h.nwarps;
-  if (wtype == DDL_W_INT4) launch_gemv_ntn<DDL_W_INT4>(ntn, h, a, s);
-  else launch_gemv_ntn<DDL_W_BF16>(ntn, h, a, s);
-  if ((st = cuda_status(cudaGetLastError()))) return st;
+  const cudaError_t e = wtype == DDL_W_INT4 ? launch_gemv_ntn<DDL_W_INT4>(ntn, h, a, s)
+                                            : launch_gemv_ntn<DDL_W_BF16>(ntn, h, a, s);
+  if ((st = cuda_status(e))) return st;
   SelArgs sa;
   sa.rec = a.rec;
   sa.logits = logits;
@@ -712,6 +717,6 @@ extern "C" int ddl_lm_head(int32_t D, int64_t V, ddl_wtype wtype, const void* he
   sa.nwarps = h.nwarps;
   sa.top_k = top_k;
   sa.temperature = temperature;
-  head_select_kernel<<<B, SEL_THREADS, 0, s>>>(sa);
-  return cuda_status(cudaGetLastError());
+  void* sargs[] = {&sa};
+  return cuda_status(launch_pdl((const void*)head_select_kernel, dim3(B), dim3(SEL_THREADS), sargs, 0, s));
 }
