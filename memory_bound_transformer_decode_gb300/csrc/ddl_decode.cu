@@ -1934,13 +1934,6 @@ __device__ __noinline__ void merge_sequence(const Params& P, int layer, int64_t 
     }
     float* dst = P.attn + b * P.Hq * HD + (kvh * GH + h) * HD;
     reinterpret_cast<float4*>(dst)[dq] = acc;
-    if (P.att_xl) {  // the tensor-core path's Wo operands
-      const int k = (int)(kvh * GH + h) * HD + 4 * dq;
-      put_limbs(P.att_xl, P.att_np, P.B, k, (int)b, acc.x);
-      put_limbs(P.att_xl, P.att_np, P.B, k + 1, (int)b, acc.y);
-      put_limbs(P.att_xl, P.att_np, P.B, k + 2, (int)b, acc.z);
-      put_limbs(P.att_xl, P.att_np, P.B, k + 3, (int)b, acc.w);
-    }
     if (P.ximg[0]) {  // the Wo stage's fragments of the attention output
       uint8_t* img = img_out(P, layer, ST_ATT);
       const int64_t k = (kvh * GH + h) * HD + 4 * dq;
@@ -2822,8 +2815,6 @@ static int decode(const ddl_shape* s, ddl_wtype wtype, const ddl_layer_w* layers
       if ((st = tc_begin(R, stream))) return st;
       P.cooperative = 0;
       P.trace = nullptr;
-      P.att_xl = R.xl;
-      P.att_np = tc_ncols(B);
       for (int l = 0; l < nL; ++l) {
         if ((st = tc_stage(R, l, ST_QKV, stream))) return st;
         P.stage_begin = l * NSTAGE + ST_ATT;

@@ -250,8 +250,6 @@ struct Params {
   const int32_t* ptab;  // device copy of the page table (workspace)
   int32_t pshift;       // log2 of the page size (0: contiguous caches)
   int32_t pstride;      // page-table entries per sequence (0: every row reads row 0, prefill)
-  uint8_t* att_xl;      // tensor-core path: the Wo GEMM's operand image, written by the sequence merge (else NULL)
-  int32_t att_np;       // its columns (two limbs per sequence, padded to 16)
   uint64_t* trace;      // optional: per stage, CTA: start, prologue end, NW warp ends, end, 4 prologue steps (ns)
   LayerDev layers[MAX_LAYERS];
   // 2-D views [B * H_kv * s_max rows][hd] of each layer's K and V caches for

@@ -42,7 +42,7 @@ constexpr int MAX_STAGES = 8;
 constexpr int MAX_NA = 12;       // A buffers in tensor memory (barrier slots)
 constexpr int TMEM_COLS = 512;
 constexpr int A_COLS = 32;       // one group of A: four 16-wide slices of 8 columns
-constexpr int LBO = TC_LBO, SBO = TC_SBO;  // B-operand image: k-cores of 8 x 16 B, 8 k-cores per column group of 8
+constexpr int LBO = 128, SBO = 1024;  // B-operand image: k-cores of 8 x 16 B, 8 k-cores per column group of 8
 
 struct TcGemm {
   int32_t N, NT, G, Sk, Gc, glast, NR, NP, B;
@@ -379,7 +379,7 @@ __global__ void __launch_bounds__(GT, 1) tc_gemm_kernel(const __grid_constant__ 
 }
 
 // ------------------------------------------------------------------ epilogues
-enum EpiKind { EK_QKV = 0, EK_WO = 2, EK_GU = 3, EK_DOWN = 4, EK_PREP_X = 5 };
+enum EpiKind { EK_QKV = 0, EK_WO = 2, EK_GU = 3, EK_DOWN = 4, EK_PREP_X = 5, EK_PREP_ATT = 6 };
 
 struct TcEpi {
   int32_t kind, N, B, D, Hq, Hkv, hd, dff, NP;
@@ -389,7 +389,7 @@ struct TcEpi {
   const float* part;
   const float* xin32;        // WO: the layer's input residual (fp32) ...
   const uint16_t* xin16;     // ... or bf16; PREP_X: the vector
-  const float* vec;          // DOWN: y
+  const float* vec;          // DOWN: y; PREP_ATT: the attention output
   float* out;                // QKV: q; WO: y; GU: a; DOWN: z
   uint16_t* kc;
   uint16_t* vc;
@@ -407,6 +407,22 @@ struct TcEpi {
   int32_t pshift, pstride;
 };
 
+// Position of element k, limb column c of a group's B-operand image.  Inside
+// each 16-wide slice the order of k follows the A operand's tensor-memory
+// columns: (0,1) (8,9) (2,3) (10,11) (4,5) (12,13) (6,7) (14,15).
+__device__ __forceinline__ int64_t limb_offset(int NP, int k, int c) {
+  const int kk = k & 63, j = kk >> 4, k16 = kk & 15;
+  const int kap = (k16 < 8 ? 4 * (k16 >> 1) + (k16 & 1) : 4 * ((k16 - 8) >> 1) + 2 + (k16 & 1)) + 16 * j;
+  return (int64_t)(k >> 6) * NP * 128 + (c >> 3) * SBO + (kap >> 3) * LBO + (c & 7) * 16 + (kap & 7) * 2;
+}
+// v * 2^-8 as an fp16 high part (column b) and remainder (column B + b).
+__device__ __forceinline__ void put_limbs(uint8_t* xl, int NP, int B, int k, int b, float v) {
+  const float sv = v * (1.0f / 256.f);
+  const __half h0 = __float2half_rn(sv);
+  const __half h1 = __float2half_rn(sv - __half2float(h0));
+  *reinterpret_cast<__half*>(xl + limb_offset(NP, k, b)) = h0;
+  *reinterpret_cast<__half*>(xl + limb_offset(NP, k, B + b)) = h1;
+}
 
 __global__ void __launch_bounds__(256) tc_epi_kernel(const __grid_constant__ TcEpi E) {
   __shared__ float red[256];
@@ -495,6 +511,10 @@ __global__ void __launch_bounds__(256) tc_epi_kernel(const __grid_constant__ TcE
           const float x = E.xin32 ? __ldcg(E.xin32 + o) : bf16_bits_to_f32(E.xin16[o]);
           ss = fmaf(x, x, ss);
           put_limbs(E.xl, E.NP, B, i, b, x * bf16_bits_to_f32(E.nw[i]));
+          break;
+        }
+        default: {  // EK_PREP_ATT: the attention output, no norm
+          put_limbs(E.xl, E.NP, B, i, b, __ldcg(E.vec + (int64_t)b * E.N + i));
           break;
         }
       }
@@ -641,6 +661,14 @@ int tc_stage(const TcRun& R, int layer, int st, void* stream) {
   const int gl = R.l0 + layer, B = R.B, NP = tc_ncols(B);
   const TcLayer& Ly = R.layers[layer];
   int rc;
+  if (st == ST_WO) {  // the attention output becomes the Wo operands
+    TcEpi E = epi_base(R);
+    E.kind = EK_PREP_ATT;
+    E.N = R.Hq * R.hd;
+    E.vec = R.attn;
+    E.xl = R.xl;
+    if ((rc = launch_epi(E, cs))) return rc;
+  }
   const MatGeom& m = R.mg[stage_mat(st)];
   TcGemm G;
   memset(&G, 0, sizeof G);

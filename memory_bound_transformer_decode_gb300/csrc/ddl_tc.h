@@ -21,8 +21,6 @@
 #pragma once
 #include <stdint.h>
 
-#include <cuda_fp16.h>
-
 #include "../../include/ddl.h"
 #include "ddl_plan.h"
 
@@ -73,29 +71,6 @@ struct TcRun {
   float* rfac;                   // [2][B] RMSNorm factors of those inputs (from ss, by the stage's GEMM)
 };
 
-// The B-operand image of a GEMM input (the activations as two fp16 limbs per
-// sequence, in the no-swizzle K-major layout the tensor core reads): k-cores
-// of 8 x 16 bytes, LBO bytes apart along k, 8 column groups SBO bytes apart.
-constexpr int TC_LBO = 128, TC_SBO = 1024;
-#ifdef __CUDACC__
-// Position of element k, limb column c of a group's B-operand image.  Inside
-// each 16-wide slice the order of k follows the A operand's tensor-memory
-// columns: (0,1) (8,9) (2,3) (10,11) (4,5) (12,13) (6,7) (14,15).
-__device__ __forceinline__ int64_t limb_offset(int NP, int k, int c) {
-  const int kk = k & 63, j = kk >> 4, k16 = kk & 15;
-  const int kap = (k16 < 8 ? 4 * (k16 >> 1) + (k16 & 1) : 4 * ((k16 - 8) >> 1) + 2 + (k16 & 1)) + 16 * j;
-  return (int64_t)(k >> 6) * NP * 128 + (c >> 3) * TC_SBO + (kap >> 3) * TC_LBO + (c & 7) * 16 + (kap & 7) * 2;
-}
-// v * 2^-8 as an fp16 high part (column b) and remainder (column B + b).
-__device__ __forceinline__ void put_limbs(uint8_t* xl, int NP, int B, int k, int b, float v) {
-  const float sv = v * (1.0f / 256.f);
-  const __half h0 = __float2half_rn(sv);
-  const __half h1 = __float2half_rn(sv - __half2float(h0));
-  *reinterpret_cast<__half*>(xl + limb_offset(NP, k, b)) = h0;
-  *reinterpret_cast<__half*>(xl + limb_offset(NP, k, B + b)) = h1;
-}
-#endif
-
 // Workspace bytes of the path (beyond the decode kernel's own layout).
 int64_t tc_workspace_bytes(const ddl_shape& s, int B, int wtype);
 void tc_workspace_carve(const ddl_shape& s, int B, int wtype, uint8_t* base, TcRun& R);
@@ -104,8 +79,8 @@ void tc_workspace_carve(const ddl_shape& s, int B, int wtype, uint8_t* base, TcR
 // and, for the stack's first layer, turn its input into the QKV operands.
 int tc_begin(const TcRun& R, void* stream);
 // One weight stage (QKV, WO, GU or DOWN) of launch-local layer `layer`:
-// operands -> GEMM -> epilogue.  The Wo operands (the attention output as
-// limbs) are written by the attention stage's sequence merge.
+// operands -> GEMM -> epilogue.  For WO the attention output is converted
+// first.
 int tc_stage(const TcRun& R, int layer, int st, void* stream);
 
 }  // namespace ddl
