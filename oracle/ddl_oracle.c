@@ -18,7 +18,7 @@
  *    one K/V head; §二.3 4-bit weights expanded with their scale on arrival.
  *  - roofline reply (zhichai.net), §五: RoPE rotates q and k by dimension pairs.
  *
- * Readings where the pages are silent (each also listed in the design doc):
+ * Readings where the pages are silent (the plainest reading the rest supports):
  *  - RMSNorm: x * w / sqrt(mean(x^2) + eps), eps inside the root.
  *  - RoPE: half-split pairs (i, i + hd/2), theta_i = base^(-2i/hd), angle
  *    pos * theta_i, applied to q and k after the projection.
