@@ -1980,8 +1980,20 @@ __device__ __forceinline__ void att_flush(const Params& P, float* rec, const flo
 
 template <int HD, int WT, bool RAG>
 __device__ __forceinline__ bool stage_att_body(const Params& P, int layer, Ring& R, uint8_t* smem, Misc& M);
+// The stage waits for its grid barrier itself (wait) or for the CTA's other
+// warps, so that its own code is being fetched while the barrier completes.
 template <int HD, int WT, bool RAG>
-__device__ __noinline__ bool stage_att(const Params& P, int layer, Ring& Rm, uint8_t* smem, Misc& M) {
+__device__ __noinline__ bool stage_att(const Params& P, int layer, Ring& Rm, uint8_t* smem, Misc& M, bool wait,
+                                       uint32_t target) {
+  if (wait) {
+    if (!grid_wait(P, target, M)) return false;
+  } else {
+    csync();  // the stage context
+  }
+  if (threadIdx.x == 0) {
+    trace_stamp(P, layer * NSTAGE + ST_ATT, 0);
+    trace_stamp(P, layer * NSTAGE + ST_ATT, 1);
+  }
   __syncwarp();
   Ring R = Rm;
   const bool ok = stage_att_body<HD, WT, RAG>(P, layer, R, smem, M);
@@ -2402,6 +2414,9 @@ __global__ void __launch_bounds__(NTHREADS_ALL, 1) decode_kernel(const __grid_co
         ok = false;
         break;
       }
+    } else if (st == ST_ATT) {
+      ok = stage_att<HD, WT, RAG>(P, layer, R, smem, M, wait, target);
+      if (!ok) break;
     } else {
       if (wait) {
         if (!grid_wait(P, target, M)) {
@@ -2412,12 +2427,7 @@ __global__ void __launch_bounds__(NTHREADS_ALL, 1) decode_kernel(const __grid_co
         csync();  // the stage context
       }
       if (threadIdx.x == 0) trace_stamp(P, s, 0);
-      if (st == ST_ATT) {
-        if (threadIdx.x == 0) trace_stamp(P, s, 1);
-        ok = stage_att<HD, WT, RAG>(P, layer, R, smem, M);
-      } else {
-        stage_gemv_wide<HD, WT>(P, layer, st, R, smem, M);
-      }
+      stage_gemv_wide<HD, WT>(P, layer, st, R, smem, M);
     }
     csync();
     if (threadIdx.x == 0) trace_stamp(P, s, NW + 2);
