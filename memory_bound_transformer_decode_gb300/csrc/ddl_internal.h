@@ -53,6 +53,10 @@ inline int64_t make_geoms(const ddl_shape& s, int wtype, MatGeom mg[4]) {
     m.woff = off;  // INT4: one stream of blocks, each its codes then its scales (one copy per slot)
     off = align256(off + m.T * (wtype == DDL_W_INT4 ? QBLK_BYTES : BF16_BLK_BYTES));
     m.soff = wtype == DDL_W_INT4 ? m.woff + BLK_BYTES : off;
+    // the INT4 slot loop is bound by instruction issue, which the producer
+    // warp shares with consumer warps 0 and 4; bf16 weights' streams wait on
+    // memory, so their warps take equal shares
+    m.even = wtype == DDL_W_BF16;
   }
   return off;
 }

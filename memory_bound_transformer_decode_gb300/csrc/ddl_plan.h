@@ -93,6 +93,7 @@ struct MatGeom {
   int32_t J;          // partial slots per (tile, panel)
   int32_t NP;         // panels: k-chunks pk[p]..pk[p+1]-1, worked by CTAs pc[p]..pc[p+1]-1
   int32_t own_ok;     // split tiles may be finished by their owners: no warp owns more than two
+  int32_t even;       // equal warp shares (bf16 weights: data-bound streams), else 15 : 16 for warps 0 and 4
   int64_t T;          // blocks
   int64_t woff, soff; // packed layer: INT4 block b's codes at woff + b * QBLK_BYTES, its scales at
                       // soff + b * QBLK_BYTES (soff = woff + BLK_BYTES); bf16 block b at woff + b * 2048
@@ -156,23 +157,23 @@ DDL_HD uint32_t panel_blocks(const MatGeom& m, int p) { return (uint32_t)m.NT * 
 // proportion 15 : 16 for the two warps that share their scheduler with the
 // producer warp (warps 0 and 4) and the others: that scheduler issues the
 // producer's instructions too, and its consumer warps measured ~6 % slower.
-DDL_HD uint32_t warp_lo(uint32_t R, int nw, int w) {
-  if (nw != 8) return lo32(R, (uint32_t)nw, (uint32_t)w);
+DDL_HD uint32_t warp_lo(uint32_t R, int nw, int w, bool even = false) {
+  if (nw != 8 || even) return lo32(R, (uint32_t)nw, (uint32_t)w);
   const uint32_t cum = 16u * (uint32_t)w - (uint32_t)((w + 3) / 4);  // sum of the shares of warps < w
   return (uint32_t)((uint64_t)R * cum / 126u);
 }
 DDL_HD void warp_work(const MatGeom& m, int p, int cl, int w, int nw, uint32_t& lo, uint32_t& hi) {
   const uint32_t Tp = panel_blocks(m, p), Cp = (uint32_t)(m.pc[p + 1] - m.pc[p]);
   const uint32_t clo = lo32(Tp, Cp, cl), R = lo32(Tp, Cp, cl + 1) - clo;
-  lo = clo + warp_lo(R, nw, w);
-  hi = clo + warp_lo(R, nw, w + 1);
+  lo = clo + warp_lo(R, nw, w, m.even);
+  hi = clo + warp_lo(R, nw, w + 1, m.even);
 }
 // Panel-local warp index (cl * nw + w) owning panel work index i.
 DDL_HD uint32_t work_owner(const MatGeom& m, int p, uint32_t i, int nw) {
   const uint32_t Tp = panel_blocks(m, p), Cp = (uint32_t)(m.pc[p + 1] - m.pc[p]);
   const uint32_t cl = owner32(Tp, Cp, i), clo = lo32(Tp, Cp, cl), R = lo32(Tp, Cp, cl + 1) - clo;
   uint32_t w = 0;
-  while ((int)w + 1 < nw && warp_lo(R, nw, (int)w + 1) <= i - clo) ++w;
+  while ((int)w + 1 < nw && warp_lo(R, nw, (int)w + 1, m.even) <= i - clo) ++w;
   return cl * nw + w;
 }
 DDL_HD bool warp_empty(const MatGeom& m, int p, uint32_t v, int nw) {
