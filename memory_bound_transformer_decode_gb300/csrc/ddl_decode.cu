@@ -547,18 +547,28 @@ constexpr float X_SCALE = 256.f;  // x is carried as x * 2^-8
 constexpr int NW_HS_OFF = 24576;
 static_assert(NW_HS_OFF + XF_CHUNKS * GC * 8 * 4 <= SM_NW_BYTES, "half-slice sums");
 
-// fp16 high part and remainder of v * 2^-8 at element k of sequence b of a
-// fragment image (the layout above, B sequences, slice-major).
+// High part and remainder of v * 2^-8 at element k of sequence b of a
+// fragment image (the layout above, B sequences, slice-major): fp16 for INT4
+// weights, bf16 for bf16 weights (the type of that stage's MMAs).
 // Returns high part + remainder (what the MMAs multiply), for the sums below.
+template <int WT>
 __device__ __forceinline__ float img_put(uint8_t* img, int B, int64_t k, int b, float v) {
   const int p = (int)(k & 15), tq = (p & 7) >> 1;
   const float sv = v * (1.0f / X_SCALE);
-  const __half hi = __float2half_rn(sv);
-  const __half lo = __float2half_rn(sv - __half2float(hi));
   uint8_t* base = img + (k >> 4) * 64 * B + (p >> 3) * 4 + (p & 1) * 2 + tq * 8;
-  *reinterpret_cast<__half*>(base + 2 * b * 32) = hi;
-  *reinterpret_cast<__half*>(base + (2 * b + 1) * 32) = lo;
-  return __half2float(hi) + __half2float(lo);
+  if constexpr (WT == DDL_W_BF16) {
+    const __nv_bfloat16 hi = __float2bfloat16_rn(sv);
+    const __nv_bfloat16 lo = __float2bfloat16_rn(sv - __bfloat162float(hi));
+    *reinterpret_cast<__nv_bfloat16*>(base + 2 * b * 32) = hi;
+    *reinterpret_cast<__nv_bfloat16*>(base + (2 * b + 1) * 32) = lo;
+    return __bfloat162float(hi) + __bfloat162float(lo);
+  } else {
+    const __half hi = __float2half_rn(sv);
+    const __half lo = __float2half_rn(sv - __half2float(hi));
+    *reinterpret_cast<__half*>(base + 2 * b * 32) = hi;
+    *reinterpret_cast<__half*>(base + (2 * b + 1) * 32) = lo;
+    return __half2float(hi) + __half2float(lo);
+  }
 }
 // Beside an image of K elements: per 8-element half slice and sequence, the
 // sum of the fragments (high part + remainder) and the sum of squares of the
@@ -581,7 +591,7 @@ __device__ __forceinline__ uint8_t* img_out(const Params& P, int layer, int st) 
   return P.ximg[(layer * NSTAGE + st) & 1];
 }
 __device__ __forceinline__ bool img_in(const Params& P, int layer, int st) {
-  return P.ximg[0] != nullptr && P.wtype == DDL_W_INT4 && layer * NSTAGE + st > 0;
+  return P.ximg[0] != nullptr && layer * NSTAGE + st > 0;
 }
 
 template <int HD, int WT>
@@ -604,7 +614,7 @@ __device__ __forceinline__ void gemv_prologue(const Params& P, const GemvCtx& E,
   const int ngv = (nkc - 1) * GC + chunk_groups(m, kc_lo + nkc - 1);  // group slots holding data
   const int n_units = ngv * B * 4;
   const int kbase = kc_lo * GC * DDL_GROUP;
-  const bool from_img = WT == DDL_W_INT4 && img_in(P, E.layer, E.st);
+  const bool from_img = img_in(P, E.layer, E.st);
   const uint32_t invB = (65536u + B - 1) / B;  // g / B == (g * invB) >> 16 for g < 2^15
   const uint32_t raw = smem_addr(smem + SM_SCR);
   const uint32_t nws = smem_addr(smem + SM_NW);
@@ -797,7 +807,7 @@ __device__ __forceinline__ float epi_norm(const Params& P, const uint16_t* w, in
 }
 
 // Rows g and g+8 of tile T for sequence t (narrow batches: t = lane % 4).
-template <int HD>
+template <int HD, int WT>
 __device__ __noinline__ void gemv_epilogue(const Params& P, const GemvCtx& E, int T, int t, float v0,
                                            float v1, Misc& M, bool have_res = false, float res0 = 0.f,
                                            float res1 = 0.f) {
@@ -836,8 +846,8 @@ __device__ __noinline__ void gemv_epilogue(const Params& P, const GemvCtx& E, in
     const float yw0 = y0 * epi_norm(P, w2, r0), yw1 = y1 * epi_norm(P, w2, r1);
     if (P.ximg[0]) {  // the gate/up stage's fragments of y * norm2, their sums, sums of y^2
       uint8_t* img = img_out(P, E.layer, E.st);
-      const float f0 = tile_half_sum(img_put(img, P.B, r0, t, yw0), P.B);
-      const float f1 = tile_half_sum(img_put(img, P.B, r1, t, yw1), P.B);
+      const float f0 = tile_half_sum(img_put<WT>(img, P.B, r0, t, yw0), P.B);
+      const float f1 = tile_half_sum(img_put<WT>(img, P.B, r1, t, yw1), P.B);
       const float q0 = tile_half_sum(y0 * y0, P.B), q1 = tile_half_sum(y1 * y1, P.B);
       if (g == 0) {
         float* hs = img_hsum(img, P.B, P.D);
@@ -856,7 +866,7 @@ __device__ __noinline__ void gemv_epilogue(const Params& P, const GemvCtx& E, in
     P.a[(int64_t)t * P.dff + 8 * T + g] = av;
     if (P.ximg[0]) {  // the down stage's fragments of a and their sums (half slice T)
       uint8_t* img = img_out(P, E.layer, E.st);
-      const float f = tile_half_sum(img_put(img, P.B, 8 * T + g, t, av), P.B);
+      const float f = tile_half_sum(img_put<WT>(img, P.B, 8 * T + g, t, av), P.B);
       if (g == 0) img_hsum(img, P.B, P.dff)[T * P.B + t] = f;
     } else if (P.B > NARROW_B) {
       atomicMax(&M.cmax[t], __float_as_uint(fabsf(av)));
@@ -872,8 +882,8 @@ __device__ __noinline__ void gemv_epilogue(const Params& P, const GemvCtx& E, in
       const float zw0 = z0 * epi_norm(P, w1, r0), zw1 = z1 * epi_norm(P, w1, r1);
       if (P.ximg[0]) {
         uint8_t* img = img_out(P, E.layer, E.st);
-        const float f0 = tile_half_sum(img_put(img, P.B, r0, t, zw0), P.B);
-        const float f1 = tile_half_sum(img_put(img, P.B, r1, t, zw1), P.B);
+        const float f0 = tile_half_sum(img_put<WT>(img, P.B, r0, t, zw0), P.B);
+        const float f1 = tile_half_sum(img_put<WT>(img, P.B, r1, t, zw1), P.B);
         const float q0 = tile_half_sum(z0 * z0, P.B), q1 = tile_half_sum(z1 * z1, P.B);
         if (g == 0) {
           float* hs = img_hsum(img, P.B, P.D);
@@ -902,7 +912,7 @@ __device__ __noinline__ void gemv_epilogue(const Params& P, const GemvCtx& E, in
 
 // Sum the partials of tile T in slot order (panel, then warp; 8 loads in
 // flight) and run its epilogue.
-template <int HD>
+template <int HD, int WT>
 __device__ __noinline__ void gemv_fixup(const Params& P, const GemvCtx& E, int T, Misc& M) {
   const MatGeom& m = E.m;
   const int lane = threadIdx.x & 31;
@@ -922,14 +932,14 @@ __device__ __noinline__ void gemv_fixup(const Params& P, const GemvCtx& E, int T
       *reinterpret_cast<uint64_t*>(const_cast<float2*>(pp + (int64_t)(v - v0) * 32)) = PART_EMPTY;
     }
   }
-  if ((threadIdx.x & 3) < P.B) gemv_epilogue<HD>(P, E, T, threadIdx.x & 3, s0, s1, M);
+  if ((threadIdx.x & 3) < P.B) gemv_epilogue<HD, WT>(P, E, T, threadIdx.x & 3, s0, s1, M);
   if (lane == 0) P.cnt[T] = 0;
 }
 
 // Publish the partials this warp wrote: one fence, then per queued tile (on
 // its own lane) add the warp's block count to the tile's counter; the warp
 // that brings a counter to G finishes that tile.
-template <int HD>
+template <int HD, int WT>
 __device__ __noinline__ void gemv_publish(const Params& P, const GemvCtx& E, const uint32_t* pend,
                                           int npend, Misc& M) {
   const int lane = threadIdx.x & 31;
@@ -945,7 +955,7 @@ __device__ __noinline__ void gemv_publish(const Params& P, const GemvCtx& E, con
   while (mask) {
     const int l = __ffs(mask) - 1;
     mask &= mask - 1;
-    gemv_fixup<HD>(P, E, (int)(pend[l] & 0xFFFFFu), M);
+    gemv_fixup<HD, WT>(P, E, (int)(pend[l] & 0xFFFFFu), M);
   }
 }
 
@@ -958,7 +968,7 @@ __device__ __noinline__ void gemv_publish(const Params& P, const GemvCtx& E, con
 // order with the owner's own in its slot's place (deterministic), empties the
 // slots for the next stage and runs the epilogues, whose residual inputs were
 // loaded before the wait.
-template <int HD>
+template <int HD, int WT>
 __device__ __noinline__ void owner_fixup(const Params& P, const GemvCtx& E, int n, int T0, uint32_t mk0,
                                          float a0, float b0, int T1, uint32_t mk1, float a1, float b1,
                                          Misc& M) {
@@ -1031,8 +1041,8 @@ __device__ __noinline__ void owner_fixup(const Params& P, const GemvCtx& E, int 
   }
   __syncwarp();
   if (t < P.B) {
-    gemv_epilogue<HD>(P, E, T0, t, s0, s1, M, res, r00, r01);
-    if (n > 1) gemv_epilogue<HD>(P, E, T1, t, u0, u1, M, res, r10, r11);
+    gemv_epilogue<HD, WT>(P, E, T0, t, s0, s1, M, res, r00, r01);
+    if (n > 1) gemv_epilogue<HD, WT>(P, E, T1, t, u0, u1, M, res, r10, r11);
   }
 }
 
@@ -1040,7 +1050,7 @@ __device__ __noinline__ void owner_fixup(const Params& P, const GemvCtx& E, int 
 // scale): a warp that covered the whole tile runs the epilogue directly;
 // otherwise the partial goes to slot (T, panel, warp - first warp of the tile
 // in the panel) and the tile is queued for publication.
-template <int HD>
+template <int HD, int WT>
 __device__ __forceinline__ void tile_finish(const Params& P, const GemvCtx& E, const Entry& en, Misc& M, int T,
                                             uint32_t nblk, float v0, float v1, uint32_t* pend,
                                             int& npend, int& nown, int& oT0, float& oa0, float& ob0,
@@ -1048,7 +1058,7 @@ __device__ __forceinline__ void tile_finish(const Params& P, const GemvCtx& E, c
   const MatGeom& m = E.m;
   const int lane = threadIdx.x & 31;
   if (nblk == (uint32_t)m.G) {
-    if ((threadIdx.x & 3) < P.B) gemv_epilogue<HD>(P, E, T, threadIdx.x & 3, v0, v1, M);
+    if ((threadIdx.x & 3) < P.B) gemv_epilogue<HD, WT>(P, E, T, threadIdx.x & 3, v0, v1, M);
     return;
   }
   const uint32_t me = (uint32_t)E.cl * NW + (threadIdx.x >> 5);
@@ -1059,7 +1069,7 @@ __device__ __forceinline__ void tile_finish(const Params& P, const GemvCtx& E, c
     } else if (nown == 1) {
       oT1 = T; oa1 = v0; ob1 = v1;
     } else {  // more than two (not planned for the owner path): finish this one now
-      owner_fixup<HD>(P, E, 1, T, owned_slots(m, T), v0, v1, 0, 0u, 0.f, 0.f, M);
+      owner_fixup<HD, WT>(P, E, 1, T, owned_slots(m, T), v0, v1, 0, 0u, 0.f, 0.f, M);
       return;
     }
     ++nown;
@@ -1074,7 +1084,7 @@ __device__ __forceinline__ void tile_finish(const Params& P, const GemvCtx& E, c
   reinterpret_cast<float2*>(P.gpart)[slot * 32 + lane] = make_float2(v0, v1);
   if (lane == 0) pend[npend] = (uint32_t)T | (nblk << 20);
   if (++npend == 32) {
-    gemv_publish<HD>(P, E, pend, npend, M);
+    gemv_publish<HD, WT>(P, E, pend, npend, M);
     npend = 0;
   }
 }
@@ -1339,7 +1349,7 @@ __device__ __forceinline__ bool stage_gemv_body(const Params& P, int layer, int 
       acc0 = acc1 = 0.f;
       gi = 0;
       if (++kc == pk1) {  // end of the tile in this panel
-        tile_finish<HD>(P, E, en, M, T, nblk, tac0, tac1, pend, npend, nown, oT0, oa0, ob0, oT1, oa1, ob1);
+        tile_finish<HD, WT>(P, E, en, M, T, nblk, tac0, tac1, pend, npend, nown, oT0, oa0, ob0, oT1, oa1, ob1);
         tac0 = tac1 = 0.f;
         nblk = 0;
         kc = pk0;
@@ -1349,10 +1359,10 @@ __device__ __forceinline__ bool stage_gemv_body(const Params& P, int layer, int 
     }
   }
   if (nblk != 0)
-    tile_finish<HD>(P, E, en, M, T, nblk, fmaf(acc0, esc, tac0), fmaf(acc1, esc, tac1), pend, npend, nown, oT0,
+    tile_finish<HD, WT>(P, E, en, M, T, nblk, fmaf(acc0, esc, tac0), fmaf(acc1, esc, tac1), pend, npend, nown, oT0,
                     oa0, ob0, oT1, oa1, ob1);
-  if (npend) gemv_publish<HD>(P, E, pend, npend, M);
-  if (nown > 0) owner_fixup<HD>(P, E, nown, oT0, en.omask[0], oa0, ob0, oT1, en.omask[1], oa1, ob1, M);
+  if (npend) gemv_publish<HD, WT>(P, E, pend, npend, M);
+  if (nown > 0) owner_fixup<HD, WT>(P, E, nown, oT0, en.omask[0], oa0, ob0, oT1, en.omask[1], oa1, ob1, M);
   if (lane == 0) trace_stamp(P, layer * NSTAGE + st, 2 + warp);
   trace_ring(P, layer * NSTAGE + st, wcyc, nslots);
   return true;
@@ -1525,7 +1535,7 @@ __device__ __forceinline__ void wide_epilogues(const Params& P, const GemvCtx& E
 #pragma unroll
     for (int s = 0; s < 2; ++s) {
       const int b = nt * 8 + 2 * t + s;
-      if (b < P.B) gemv_epilogue<HD>(P, E, T, b, v[nt * 4 + s], v[nt * 4 + 2 + s], M);
+      if (b < P.B) gemv_epilogue<HD, DDL_W_INT4>(P, E, T, b, v[nt * 4 + s], v[nt * 4 + 2 + s], M);  // (INT4 only)
     }
 }
 template <int HD>
@@ -1855,7 +1865,7 @@ __device__ __forceinline__ void merge_head(const float* recs, int REC, int first
 // records).  Phase 2: the thread sums factor * o over the records (any past
 // 2 NW from global memory in rounds of 8).  A record whose factor is 0 (a
 // CTA without tiles holds none) is skipped, whatever its memory holds.
-template <int HD>
+template <int HD, int WT>
 __device__ __noinline__ void merge_sequence(const Params& P, int layer, int64_t seq, int64_t Ta, int64_t C,
                                             int64_t cf, int n, float* stage, float* fac, Misc& M) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -1937,10 +1947,10 @@ __device__ __noinline__ void merge_sequence(const Params& P, int layer, int64_t 
     if (P.ximg[0]) {  // the Wo stage's fragments of the attention output
       uint8_t* img = img_out(P, layer, ST_ATT);
       const int64_t k = (kvh * GH + h) * HD + 4 * dq;
-      float f = img_put(img, P.B, k, (int)b, acc.x);
-      f += img_put(img, P.B, k + 1, (int)b, acc.y);
-      f += img_put(img, P.B, k + 2, (int)b, acc.z);
-      f += img_put(img, P.B, k + 3, (int)b, acc.w);
+      float f = img_put<WT>(img, P.B, k, (int)b, acc.x);
+      f += img_put<WT>(img, P.B, k + 1, (int)b, acc.y);
+      f += img_put<WT>(img, P.B, k + 2, (int)b, acc.z);
+      f += img_put<WT>(img, P.B, k + 3, (int)b, acc.w);
       fsum = f;
     } else if (P.B > NARROW_B) {  // the Wo stage scales its staged x by this
       const float m = fmaxf(fmaxf(fabsf(acc.x), fabsf(acc.y)), fmaxf(fabsf(acc.z), fabsf(acc.w)));
@@ -2263,7 +2273,7 @@ __device__ __forceinline__ bool stage_att_body(const Params& P, int layer, Ring&
     float* fac = recs + NW * 2 * REC;  // per (head, record) factors of the merge
     for (int64_t sq = s0; sq <= s1; ++sq)
       if (M.mseq[(int)(sq - s0)] == sq)
-        merge_sequence<HD>(P, layer, sq, Ta, C, A.cf[sq - s0], A.span[sq - s0], recs, fac, M);
+        merge_sequence<HD, WT>(P, layer, sq, Ta, C, A.cf[sq - s0], A.span[sq - s0], recs, fac, M);
   }
   return true;
 }
@@ -2727,7 +2737,7 @@ static int decode(const ddl_shape* s, ddl_wtype wtype, const ddl_layer_w* layers
   P.q = (float*)(ws + w.q); P.attn = (float*)(ws + w.attn); P.y = (float*)(ws + w.y);
   P.a = (float*)(ws + w.a);
   P.ximg[0] = P.ximg[1] = nullptr;
-  if (wtype == DDL_W_INT4 && w.ximg_bytes > 0 && (int64_t)s->D / 8 * B * 4 <= NW_HS_OFF) {
+  if (w.ximg_bytes > 0 && (int64_t)s->D / 8 * B * 4 <= NW_HS_OFF) {  // (batches up to IMG_MAX_B)
     P.ximg[0] = ws + w.ximg;
     P.ximg[1] = ws + w.ximg + w.ximg_bytes;
   }
