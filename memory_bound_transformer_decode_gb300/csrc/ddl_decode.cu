@@ -633,10 +633,12 @@ __device__ __forceinline__ void gemv_prologue(const Params& P, const GemvCtx& E,
     fence_proxy_async_smem();    // the previous stage's generic accesses to this area come first
     if (from_img) {  // the panel's fragments, its half-slice sums and (norm stages) the sums of squares
       uint8_t* src = P.ximg[(E.layer * NSTAGE + E.st - 1) & 1];
-      const uint32_t ib = (uint32_t)n_units * 64, hb = (uint32_t)ngv * 8 * B * 4, qb = nw ? (uint32_t)(K / 8) * B * 4 : 0u;
+      // (bf16 weights need no sums of x: no offset to remove)
+      const uint32_t ib = (uint32_t)n_units * 64, hb = WT == DDL_W_INT4 ? (uint32_t)ngv * 8 * B * 4 : 0u;
+      const uint32_t qb = nw ? (uint32_t)(K / 8) * B * 4 : 0u;
       mbar_arrive_expect_tx(xbar, ib + hb + qb);
       bulk_g2s(raw, src + (int64_t)(kbase / 16) * 64 * B, ib, xbar);
-      bulk_g2s(nws + NW_HS_OFF, img_hsum(src, B, K) + (int64_t)(kbase / 8) * B, hb, xbar);
+      if (hb) bulk_g2s(nws + NW_HS_OFF, img_hsum(src, B, K) + (int64_t)(kbase / 8) * B, hb, xbar);
       if (qb) bulk_g2s(nws, img_hsq(src, B, K), qb, xbar);
     } else {
       mbar_arrive_expect_tx(xbar, (uint32_t)n_units * 64);
@@ -678,7 +680,7 @@ __device__ __forceinline__ void gemv_prologue(const Params& P, const GemvCtx& E,
   if (from_img) {  // per (group slot, sequence) the sum of its eight half slices, in order; the sum of squares
     const float* hs = reinterpret_cast<const float*>(smem + SM_NW + NW_HS_OFF);
 #pragma unroll 1
-    for (int i = tid; i < ngv * B; i += NTHREADS) {
+    for (int i = tid; i < (WT == DDL_W_INT4 ? ngv * B : 0); i += NTHREADS) {
       const int gs = (int)(((uint32_t)i * invB) >> 16), b = i - gs * B;
       float sum = 0.f;
 #pragma unroll
@@ -756,7 +758,7 @@ __device__ __forceinline__ void gemv_prologue(const Params& P, const GemvCtx& E,
   //    remainder, one unit per thread, the four units of a group in adjacent
   //    lanes
 #pragma unroll 1
-  for (int u0 = 0; u0 < (from_img ? 0 : n_units); u0 += NTHREADS) {
+  for (int u0 = 0; u0 < (from_img || WT != DDL_W_INT4 ? 0 : n_units); u0 += NTHREADS) {
     const int u = u0 + tid;
     float sum = 0.f;
     if (u < n_units) {
@@ -846,14 +848,18 @@ __device__ __noinline__ void gemv_epilogue(const Params& P, const GemvCtx& E, in
     const float yw0 = y0 * epi_norm(P, w2, r0), yw1 = y1 * epi_norm(P, w2, r1);
     if (P.ximg[0]) {  // the gate/up stage's fragments of y * norm2, their sums, sums of y^2
       uint8_t* img = img_out(P, E.layer, E.st);
-      const float f0 = tile_half_sum(img_put<WT>(img, P.B, r0, t, yw0), P.B);
-      const float f1 = tile_half_sum(img_put<WT>(img, P.B, r1, t, yw1), P.B);
+      const float p0 = img_put<WT>(img, P.B, r0, t, yw0), p1 = img_put<WT>(img, P.B, r1, t, yw1);
       const float q0 = tile_half_sum(y0 * y0, P.B), q1 = tile_half_sum(y1 * y1, P.B);
+      if constexpr (WT == DDL_W_INT4) {  // the sums of x remove the INT4 code offset
+        const float f0 = tile_half_sum(p0, P.B), f1 = tile_half_sum(p1, P.B);
+        if (g == 0) {
+          float* hs = img_hsum(img, P.B, P.D);
+          hs[(2 * T) * P.B + t] = f0;
+          hs[(2 * T + 1) * P.B + t] = f1;
+        }
+      }
       if (g == 0) {
-        float* hs = img_hsum(img, P.B, P.D);
         float* hq = img_hsq(img, P.B, P.D);
-        hs[(2 * T) * P.B + t] = f0;
-        hs[(2 * T + 1) * P.B + t] = f1;
         hq[(2 * T) * P.B + t] = q0;
         hq[(2 * T + 1) * P.B + t] = q1;
       }
@@ -866,8 +872,11 @@ __device__ __noinline__ void gemv_epilogue(const Params& P, const GemvCtx& E, in
     P.a[(int64_t)t * P.dff + 8 * T + g] = av;
     if (P.ximg[0]) {  // the down stage's fragments of a and their sums (half slice T)
       uint8_t* img = img_out(P, E.layer, E.st);
-      const float f = tile_half_sum(img_put<WT>(img, P.B, 8 * T + g, t, av), P.B);
-      if (g == 0) img_hsum(img, P.B, P.dff)[T * P.B + t] = f;
+      const float p = img_put<WT>(img, P.B, 8 * T + g, t, av);
+      if constexpr (WT == DDL_W_INT4) {
+        const float f = tile_half_sum(p, P.B);
+        if (g == 0) img_hsum(img, P.B, P.dff)[T * P.B + t] = f;
+      }
     } else if (P.B > NARROW_B) {
       atomicMax(&M.cmax[t], __float_as_uint(fabsf(av)));
     }
@@ -882,14 +891,18 @@ __device__ __noinline__ void gemv_epilogue(const Params& P, const GemvCtx& E, in
       const float zw0 = z0 * epi_norm(P, w1, r0), zw1 = z1 * epi_norm(P, w1, r1);
       if (P.ximg[0]) {
         uint8_t* img = img_out(P, E.layer, E.st);
-        const float f0 = tile_half_sum(img_put<WT>(img, P.B, r0, t, zw0), P.B);
-        const float f1 = tile_half_sum(img_put<WT>(img, P.B, r1, t, zw1), P.B);
+        const float p0 = img_put<WT>(img, P.B, r0, t, zw0), p1 = img_put<WT>(img, P.B, r1, t, zw1);
         const float q0 = tile_half_sum(z0 * z0, P.B), q1 = tile_half_sum(z1 * z1, P.B);
+        if constexpr (WT == DDL_W_INT4) {
+          const float f0 = tile_half_sum(p0, P.B), f1 = tile_half_sum(p1, P.B);
+          if (g == 0) {
+            float* hs = img_hsum(img, P.B, P.D);
+            hs[(2 * T) * P.B + t] = f0;
+            hs[(2 * T + 1) * P.B + t] = f1;
+          }
+        }
         if (g == 0) {
-          float* hs = img_hsum(img, P.B, P.D);
           float* hq = img_hsq(img, P.B, P.D);
-          hs[(2 * T) * P.B + t] = f0;
-          hs[(2 * T + 1) * P.B + t] = f1;
           hq[(2 * T) * P.B + t] = q0;
           hq[(2 * T + 1) * P.B + t] = q1;
         }
@@ -1957,11 +1970,14 @@ __device__ __noinline__ void merge_sequence(const Params& P, int layer, int64_t 
       if (b < MAX_B) atomicMax(&M.cmax[b], __float_as_uint(m));
     }
   }
-  // the half slice's other four elements are thread dq ^ 1's (the next lane)
-  fsum += __shfl_xor_sync(FULL, fsum, 1);
-  if (P.ximg[0] && act && (dq & 1) == 0) {
-    const int64_t k = (kvh * GH + h) * HD + 4 * dq;
-    img_hsum(img_out(P, layer, ST_ATT), P.B, P.Hq * HD)[(k >> 3) * P.B + b] = fsum;
+  // the half slice's other four elements are thread dq ^ 1's (the next lane);
+  // (bf16 weights need no sums of x)
+  if constexpr (WT == DDL_W_INT4) {
+    fsum += __shfl_xor_sync(FULL, fsum, 1);
+    if (P.ximg[0] && act && (dq & 1) == 0) {
+      const int64_t k = (kvh * GH + h) * HD + 4 * dq;
+      img_hsum(img_out(P, layer, ST_ATT), P.B, P.Hq * HD)[(k >> 3) * P.B + b] = fsum;
+    }
   }
   csync();
 }
