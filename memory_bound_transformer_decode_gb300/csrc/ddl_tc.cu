@@ -8,14 +8,19 @@
 // groups of the input dimension.  Warp 0 copies each group's eight packed
 // blocks and the group's B-operand image (the activations as two fp16 limbs, laid
 // out as the tensor core reads them) into a ring of shared-memory stages with
-// TMA bulk copies; warps 4-7 expand the 4-bit codes in registers to fp16
-// code * scale and store them into tensor memory as the A operand (one 32-lane
-// quarter each; the tcgen05.st 16x256b shape takes the tensor-core fragment
-// registers as they are); one thread of warp 1 issues the tcgen05.mma of the
-// group's four 16-wide slices into an fp32 accumulator in tensor memory and
-// commits them to mbarriers that hand the stage and the A buffer back.  At a
-// unit's end warps 4-7 read the accumulator (tcgen05.ld), combine the two
-// limb columns of each sequence and store the unit's partial sums.
+// TMA bulk copies; three warpgroups take the groups in turn, expand the 4-bit
+// codes (or bf16 weights) in registers to fp16 and store them into tensor
+// memory as the A operand (one 32-lane quarter per warp; the tcgen05.st
+// 16x256b shape takes the tensor-core fragment registers as they are); one
+// thread of warp 1 issues the tcgen05.mma of the group's four 16-wide slices
+// into an fp32 accumulator in tensor memory and commits them to mbarriers
+// that hand the A buffer back.  A stage goes back to the copy warp once its
+// MMAs have completed and every expansion warp has released it: each of them
+// waits for every stage in turn, also those without a group of its own, so
+// that no stage's barrier runs a phase ahead of a reader (a parity wait on a
+// barrier two phases behind would return at once).  At a unit's end the last
+// warpgroup reads the accumulator (tcgen05.ld), combines the two limb columns
+// of each sequence and stores the unit's partial sums.
 //
 // Epilogue kernel (one launch per stage): sums a stage's split-K partials in a
 // fixed order and applies what the layer does to that stage's output (RMSNorm
@@ -144,7 +149,7 @@ __global__ void __launch_bounds__(GT, 1) tc_gemm_kernel(const __grid_constant__ 
   if (threadIdx.x == 0) {
     for (int i = 0; i < NS; ++i) {
       mbar_init(full0 + i * 8, 1);
-      mbar_init(empty0 + i * 8, 1);
+      mbar_init(empty0 + i * 8, 1 + 4 * NDW);  // the MMA commit and each expansion warp
     }
     for (int i = 0; i < NA; ++i) {
       mbar_init(aready0 + i * 8, 4);
@@ -283,17 +288,21 @@ __global__ void __launch_bounds__(GT, 1) tc_gemm_kernel(const __grid_constant__ 
         const int ng = stage_groups(P, gs, g1);
         const uint32_t st = sc % NS, k = sc / NS;
         const uint32_t slot = sbase + st * P.stage_bytes;
-        bool waited = false;
+        // every stage, in order: the stage cannot be refilled before this
+        // warp has released it, so this phase is the barrier's next one
+        if (!mbar_wait_warp(full0 + st * 8, k & 1, P.status, P.wait_ns)) {
+          fail();
+          ok = false;
+          break;
+        }
         for (int gi = 0; gi < ng; ++gi, ++it) {
           if ((int)(it % NDW) != d) continue;
           const uint32_t ab = it % NA, ka = it / NA;
-          if ((!waited && !mbar_wait_warp(full0 + st * 8, k & 1, P.status, P.wait_ns)) ||
-              (ka > 0 && !mbar_wait_warp(afree0 + ab * 8, (ka - 1) & 1, P.status, P.wait_ns))) {
+          if (ka > 0 && !mbar_wait_warp(afree0 + ab * 8, (ka - 1) & 1, P.status, P.wait_ns)) {
             fail();
             ok = false;
             break;
           }
-          waited = true;
           tc_fence_after();
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
@@ -330,6 +339,11 @@ __global__ void __launch_bounds__(GT, 1) tc_gemm_kernel(const __grid_constant__ 
           __syncwarp();
           if (lane == 0) mbar_arrive_local(aready0 + ab * 8);
         }
+        if (!ok) break;
+        // this warp's reads of the stage's weights are done (their values
+        // went into tensor memory above): the stage may be refilled
+        __syncwarp();
+        if (lane == 0) mbar_arrive_local(empty0 + st * 8);
         gs += ng;
       }
       if (*abort_flag) ok = false;
