@@ -121,4 +121,3 @@ def test_layer_decode_with_residual_input():
                             resid.cpu().numpy().astype(np.float64))
     assert rel_l2(oracle.bf16_to_f64(synth.bits(out)), z) <= REL_L2
     assert float(np.max(np.abs(res.cpu().numpy().astype(np.float64) - z))) <= MAX_ABS
-
