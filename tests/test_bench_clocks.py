@@ -1,5 +1,5 @@
 """bench.py's clock sampler keeps the samples taken during the timed region
-(host logic; a fake nvidia-smi stands in for the driver tool)."""
+(host logic; a fake nvidia-smi stands in for the real one)."""
 import importlib.util
 import os
 import stat
