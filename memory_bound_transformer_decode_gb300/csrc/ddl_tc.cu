@@ -438,105 +438,157 @@ __device__ __forceinline__ void put_limbs(uint8_t* xl, int NP, int B, int k, int
   *reinterpret_cast<__half*>(xl + limb_offset(NP, k, B + b)) = h1;
 }
 
-__global__ void __launch_bounds__(256) tc_epi_kernel(const __grid_constant__ TcEpi E) {
-  __shared__ float red[256];
+__global__ void __launch_bounds__(256, 2) tc_epi_kernel(const __grid_constant__ TcEpi E) {
+  constexpr int U = TC_MAX_B / 16;  // sequences a warp takes in one pass: w + 8 u, then w + 8 (u + U)
   __shared__ float rfac[TC_MAX_B];
   const int tid = threadIdx.x, B = E.B, lane = tid & 31, warp = tid >> 5;
   pdl_trigger();
   pdl_wait();  // the previous kernel's outputs (partials, sums of squares, vectors)
   if (E.rfac_in && tid < B) rfac[tid] = __ldcg(E.rfac_in + tid);  // RMSNorm factor of the stage input
   __syncthreads();
-  const int64_t items = (E.kind == EK_QKV || E.kind == EK_GU) ? (int64_t)(E.N / 16) * 8 : E.N;
+  const bool two = E.kind == EK_QKV || E.kind == EK_GU;  // an item is two packed rows, 16T + gg and + 8
+  const int64_t items = two ? (int64_t)(E.N / 16) * 8 : E.N;
   const int64_t i0 = items * blockIdx.x / gridDim.x, i1 = items * (blockIdx.x + 1) / gridDim.x;
-  auto psum = [&](int row, int b) {  // split-K partials of packed row `row`, sequence b, in CTA order
-    const uint32_t r = (uint32_t)row >> 7;
-    const int ns = (int)(owner32(E.W, E.parts, (r + 1) * E.G - 1) - owner32(E.W, E.parts, r * E.G)) + 1;
-    float v = 0.f;
-    for (int s = 0; s < ns; ++s) v += __ldcg(E.part + ((int64_t)s * B + b) * E.N + row);
-    return v;
-  };
   // Warp w takes sequences w, w + 8, ...; its lanes take the CTA's items, so
   // that the partials, the [B][N] vectors and the limb images are read and
-  // written along rows (coalesced).
-  for (int b = warp; b < B; b += 8) {
-    float ss = 0.f;
+  // written along rows (coalesced).  For an item a lane first loads what all
+  // its sequences need (the split-K partials slot by slot, each sum in CTA
+  // order, then the vectors), so that those loads are in flight together,
+  // and then computes and stores sequence by sequence.
+#pragma unroll 1
+  for (int bh = warp; bh < B; bh += 8 * U) {  // (one pass when B <= 8 U)
+    float ss[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) ss[u] = 0.f;
     for (int64_t it = i0 + lane; it < i1; it += 32) {
       const int i = (int)it;
-      switch (E.kind) {
-        case EK_QKV: {
-          const int T = i >> 3, gg = i & 7, tph = E.hd / 16, head = T / tph, ii = 8 * (T % tph) + gg;
-          const float r = rfac[b];
-          float v0 = psum(16 * T + gg, b) * r, v1 = psum(16 * T + gg + 8, b) * r;
-          if (head < E.Hq + E.Hkv) {  // RoPE on q and k: pair (ii, ii + hd/2)
-            const float c = E.rope_b ? E.rope_b[((int64_t)b * 64 + ii) * 2] : E.rope[ii][0];
-            const float sn = E.rope_b ? E.rope_b[((int64_t)b * 64 + ii) * 2 + 1] : E.rope[ii][1];
-            const float x0 = v0, x1 = v1;
-            v0 = x0 * c - x1 * sn;
-            v1 = x0 * sn + x1 * c;
-          }
-          if (head < E.Hq) {
-            float* qp = E.out + (int64_t)b * E.Hq * E.hd + (int64_t)head * E.hd;
-            qp[ii] = v0;
-            qp[ii + E.hd / 2] = v1;
-          } else {
-            const bool is_k = head < E.Hq + E.Hkv;
-            const int kvh = is_k ? head - E.Hq : head - E.Hq - E.Hkv;
-            const int64_t pb = E.posb ? (int64_t)E.posb[b] : E.pos;
-            int64_t r = (int64_t)b * E.kv_bstride + (int64_t)kvh * E.s_max + pb;
-            if (E.pshift) {  // the row inside the page that holds slot pb
-              const int64_t pg = E.ptab[(int64_t)b * E.pstride + (pb >> E.pshift)];
-              r = ((pg * E.Hkv + kvh) << E.pshift) + (pb & ((1ll << E.pshift) - 1));
+      const int row0 = two ? 16 * (i >> 3) + (i & 7) : i;  // (row0 + 8 lies in the same 128-row tile)
+      float p0[U], p1[U], xv[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) p0[u] = p1[u] = xv[u] = 0.f;
+      if (E.kind != EK_PREP_X && E.kind != EK_PREP_ATT) {
+        const uint32_t r = (uint32_t)row0 >> 7;
+        const int ns = (int)(owner32(E.W, E.parts, (r + 1) * E.G - 1) - owner32(E.W, E.parts, r * E.G)) + 1;
+        // four slots at a time: their loads are issued together, then added
+        // in slot order
+        for (int s0 = 0; s0 < ns; s0 += 4) {
+          float l0[4][U], l1[4][U];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const float* ps = E.part + (int64_t)(s0 + j) * B * E.N + row0;
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+              const int b = bh + 8 * u;
+              const bool ok = s0 + j < ns && b < B;
+              l0[j][u] = ok ? __ldcg(ps + (int64_t)b * E.N) : 0.f;
+              l1[j][u] = ok && two ? __ldcg(ps + (int64_t)b * E.N + 8) : 0.f;
             }
-            uint16_t* row = (is_k ? E.kc : E.vc) + r * E.hd;
-            row[ii] = f32_to_bf16_bits(v0);
-            row[ii + E.hd / 2] = f32_to_bf16_bits(v1);
           }
-          break;
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+#pragma unroll
+            for (int u = 0; u < U; ++u)
+              if (s0 + j < ns) {
+                p0[u] += l0[j][u];
+                p1[u] += l1[j][u];
+              }
         }
-        case EK_GU: {
-          const int T = i >> 3, gg = i & 7, j = 8 * T + gg;
-          const float r = rfac[b], gt = psum(16 * T + gg, b) * r, up = psum(16 * T + gg + 8, b) * r;
-          const float av = gt / (1.0f + expf(-gt)) * up;
-          E.out[(int64_t)b * E.dff + j] = av;
-          if (E.xl) put_limbs(E.xl, E.NP, B, j, b, av);
-          break;
-        }
-        case EK_WO: {
-          const int64_t o = (int64_t)b * E.D + i;
-          const float x = E.xin32 ? __ldcg(E.xin32 + o) : bf16_bits_to_f32(E.xin16[o]);
-          const float y = x + psum(i, b);
-          E.out[o] = y;
-          ss = fmaf(y, y, ss);
-          if (E.xl) put_limbs(E.xl, E.NP, B, i, b, y * bf16_bits_to_f32(E.nw[i]));
-          break;
-        }
-        case EK_DOWN: {
-          const int64_t o = (int64_t)b * E.D + i;
-          const float z = __ldcg(E.vec + o) + psum(i, b);
-          E.out[o] = z;
-          ss = fmaf(z, z, ss);
-          if (E.xl) put_limbs(E.xl, E.NP, B, i, b, z * bf16_bits_to_f32(E.nw[i]));
-          if (E.resid_out) E.resid_out[o] = z;
-          if (E.out_bf16) E.out_bf16[o] = f32_to_bf16_bits(z);
-          break;
-        }
-        case EK_PREP_X: {
-          const int64_t o = (int64_t)b * E.D + i;
-          const float x = E.xin32 ? __ldcg(E.xin32 + o) : bf16_bits_to_f32(E.xin16[o]);
-          ss = fmaf(x, x, ss);
-          put_limbs(E.xl, E.NP, B, i, b, x * bf16_bits_to_f32(E.nw[i]));
-          break;
-        }
-        default: {  // EK_PREP_ATT: the attention output, no norm
-          put_limbs(E.xl, E.NP, B, i, b, __ldcg(E.vec + (int64_t)b * E.N + i));
-          break;
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {  // the vector the stage adds to (WO, DOWN) or converts (PREP)
+        const int b = bh + 8 * u;
+        if (b >= B) continue;
+        const int64_t o = (int64_t)b * E.D + i;
+        if (E.kind == EK_WO || E.kind == EK_PREP_X)
+          xv[u] = E.xin32 ? __ldcg(E.xin32 + o) : bf16_bits_to_f32(E.xin16[o]);
+        else if (E.kind == EK_DOWN)
+          xv[u] = __ldcg(E.vec + o);
+        else if (E.kind == EK_PREP_ATT)
+          xv[u] = __ldcg(E.vec + (int64_t)b * E.N + i);
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int b = bh + 8 * u;
+        if (b >= B) continue;
+        switch (E.kind) {
+          case EK_QKV: {
+            const int T = i >> 3, gg = i & 7, tph = E.hd / 16, head = T / tph, ii = 8 * (T % tph) + gg;
+            const float r = rfac[b];
+            float v0 = p0[u] * r, v1 = p1[u] * r;
+            if (head < E.Hq + E.Hkv) {  // RoPE on q and k: pair (ii, ii + hd/2)
+              const float c = E.rope_b ? E.rope_b[((int64_t)b * 64 + ii) * 2] : E.rope[ii][0];
+              const float sn = E.rope_b ? E.rope_b[((int64_t)b * 64 + ii) * 2 + 1] : E.rope[ii][1];
+              const float x0 = v0, x1 = v1;
+              v0 = x0 * c - x1 * sn;
+              v1 = x0 * sn + x1 * c;
+            }
+            if (head < E.Hq) {
+              float* qp = E.out + (int64_t)b * E.Hq * E.hd + (int64_t)head * E.hd;
+              qp[ii] = v0;
+              qp[ii + E.hd / 2] = v1;
+            } else {
+              const bool is_k = head < E.Hq + E.Hkv;
+              const int kvh = is_k ? head - E.Hq : head - E.Hq - E.Hkv;
+              const int64_t pb = E.posb ? (int64_t)E.posb[b] : E.pos;
+              int64_t rr = (int64_t)b * E.kv_bstride + (int64_t)kvh * E.s_max + pb;
+              if (E.pshift) {  // the row inside the page that holds slot pb
+                const int64_t pg = E.ptab[(int64_t)b * E.pstride + (pb >> E.pshift)];
+                rr = ((pg * E.Hkv + kvh) << E.pshift) + (pb & ((1ll << E.pshift) - 1));
+              }
+              uint16_t* row = (is_k ? E.kc : E.vc) + rr * E.hd;
+              row[ii] = f32_to_bf16_bits(v0);
+              row[ii + E.hd / 2] = f32_to_bf16_bits(v1);
+            }
+            break;
+          }
+          case EK_GU: {
+            const int j = 8 * (i >> 3) + (i & 7);
+            const float r = rfac[b], gt = p0[u] * r, up = p1[u] * r;
+            const float av = gt / (1.0f + expf(-gt)) * up;
+            E.out[(int64_t)b * E.dff + j] = av;
+            if (E.xl) put_limbs(E.xl, E.NP, B, j, b, av);
+            break;
+          }
+          case EK_WO: {
+            const int64_t o = (int64_t)b * E.D + i;
+            const float y = xv[u] + p0[u];
+            E.out[o] = y;
+            ss[u] = fmaf(y, y, ss[u]);
+            if (E.xl) put_limbs(E.xl, E.NP, B, i, b, y * bf16_bits_to_f32(E.nw[i]));
+            break;
+          }
+          case EK_DOWN: {
+            const int64_t o = (int64_t)b * E.D + i;
+            const float z = xv[u] + p0[u];
+            E.out[o] = z;
+            ss[u] = fmaf(z, z, ss[u]);
+            if (E.xl) put_limbs(E.xl, E.NP, B, i, b, z * bf16_bits_to_f32(E.nw[i]));
+            if (E.resid_out) E.resid_out[o] = z;
+            if (E.out_bf16) E.out_bf16[o] = f32_to_bf16_bits(z);
+            break;
+          }
+          case EK_PREP_X: {
+            const float x = xv[u];
+            ss[u] = fmaf(x, x, ss[u]);
+            put_limbs(E.xl, E.NP, B, i, b, x * bf16_bits_to_f32(E.nw[i]));
+            break;
+          }
+          default:  // EK_PREP_ATT: the attention output, no norm
+            put_limbs(E.xl, E.NP, B, i, b, xv[u]);
+            break;
         }
       }
     }
-    if (E.ss_out) {  // this CTA's sum of squares of sequence b: the lanes' sums in a fixed tree
+    if (E.ss_out) {  // this CTA's sum of squares of each sequence: the lanes' sums in a fixed tree
 #pragma unroll
-      for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-      if (lane == 0) E.ss_out[blockIdx.x * B + b] = ss;
+      for (int u = 0; u < U; ++u) {
+        const int b = bh + 8 * u;
+        if (b >= B) continue;
+        float v = ss[u];
+#pragma unroll
+        for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+        if (lane == 0) E.ss_out[blockIdx.x * B + b] = v;
+      }
     }
   }
 }
